@@ -1,0 +1,138 @@
+"""KDA oracle: plain fp64 CPU implementation of the KDA recurrence.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+package.  The CUDA product path never imports it, and the two share no code.
+
+``kda_oracle.c`` holds the token-by-token recurrence (update and read-out of
+the "Kimi K3" study notes, section 3-2 "2) Kimi Delta Attention"); ``affine.py``
+holds an independent brute-force form built from explicit transition matrices
+(the affine-pair view of "Kimi K3: 架构、训练与系统全景解析" section 7.1, KCP).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libkda_oracle.so")
+# Same flags on x86_64 and aarch64: no FMA contraction, IEEE fp64 throughout.
+CFLAGS = ["-O2", "-fPIC", "-shared", "-pthread", "-ffp-contract=off", "-fno-fast-math"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+def compile_source(src: str, out_path: str) -> str:
+    """Compile a C oracle source file into a shared library (used for mutants too)."""
+    os.makedirs(os.path.dirname(out_path), exist_ok=True)
+    cmd = ["gcc", *CFLAGS, src, "-o", out_path, "-lm"]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    return out_path
+
+
+def build(force: bool = False) -> str:
+    """Compile ``kda_oracle.c`` into ``oracle/_build/libkda_oracle.so``."""
+    with _lock:
+        stale = (not os.path.exists(_LIB_PATH)) or (
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+        if force or stale:
+            compile_source(_SRC, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    dp = ctypes.POINTER(ctypes.c_double)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    lib.kda_oracle_chunk_fwd.restype = ctypes.c_int
+    lib.kda_oracle_chunk_fwd.argtypes = [dp, dp, dp, dp, dp, dp, i64p,
+                                         ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                         ctypes.c_int64, dp, dp, ctypes.c_int]
+    lib.kda_oracle_decode_step.restype = ctypes.c_int
+    lib.kda_oracle_decode_step.argtypes = [dp, dp, dp, dp, dp, dp,
+                                           ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                           ctypes.c_int64, dp]
+    return lib
+
+
+def load_library(path: str) -> ctypes.CDLL:
+    return _bind(ctypes.CDLL(path))
+
+
+def _default_lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        _lib = load_library(build())
+    return _lib
+
+
+def _f64(x) -> np.ndarray:
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor -> exact fp64 copy on the host
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a, ctype=ctypes.c_double):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def chunk_fwd(q, k, v, log_alpha, beta, init_state=None, cu_seqlens=None,
+              n_threads: int | None = None, lib: ctypes.CDLL | None = None):
+    """Run the recurrence over packed varlen sequences.
+
+    Shapes: q, k, log_alpha ``[N, H, dk]``; v ``[N, H, dv]``; beta ``[N, H]``;
+    init_state ``[n_seqs, H, dk, dv]`` or None; cu_seqlens ``[n_seqs + 1]`` or
+    None (one sequence of length N).  Returns ``(out [N, H, dv], final_state
+    [n_seqs, H, dk, dv])`` as fp64 numpy arrays.
+    """
+    lib = lib or _default_lib()
+    q, k, v, la, b = (_f64(t) for t in (q, k, v, log_alpha, beta))
+    s0 = _f64(init_state)
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    if cu_seqlens is None:
+        cu = np.array([0, N], dtype=np.int64)
+    else:
+        if hasattr(cu_seqlens, "detach"):
+            cu_seqlens = cu_seqlens.detach().to("cpu").numpy()
+        cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
+    n_seqs = cu.shape[0] - 1
+    out = np.zeros((N, H, dv), dtype=np.float64)
+    fin = np.zeros((n_seqs, H, dk, dv), dtype=np.float64)
+    rc = lib.kda_oracle_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(b), _ptr(s0),
+                                  _ptr(cu, ctypes.c_int64), n_seqs, H, dk, dv,
+                                  _ptr(out), _ptr(fin), int(n_threads or default_threads()))
+    if rc != 0:
+        raise RuntimeError(f"kda_oracle_chunk_fwd failed with code {rc}")
+    return out, fin
+
+
+def decode_step(state, q, k, v, log_alpha, beta, lib: ctypes.CDLL | None = None):
+    """One in-place decode step.  ``state`` must be a C-contiguous fp64 numpy
+    array ``[B, H, dk, dv]``; it is updated in place.  Returns out ``[B, H, dv]``."""
+    lib = lib or _default_lib()
+    if not (isinstance(state, np.ndarray) and state.dtype == np.float64
+            and state.flags["C_CONTIGUOUS"]):
+        raise TypeError("state must be a C-contiguous float64 numpy array")
+    q, k, v, la, b = (_f64(t) for t in (q, k, v, log_alpha, beta))
+    B, H, dk, dv = state.shape
+    out = np.zeros((B, H, dv), dtype=np.float64)
+    rc = lib.kda_oracle_decode_step(_ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(b),
+                                    B, H, dk, dv, _ptr(out))
+    if rc != 0:
+        raise RuntimeError(f"kda_oracle_decode_step failed with code {rc}")
+    return out
