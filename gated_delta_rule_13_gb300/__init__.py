@@ -1,0 +1,10 @@
+"""GB300-native (sm_103a) KDA recurrence: chunked prefill and in-place decode.
+
+The compute lives in ``libkda.so`` (hand-written CUDA kernels behind a C ABI,
+``include/kda.h``); ``kda`` is its thin Python binding.
+"""
+from .kda import (KDAError, kda_chunk_fwd, kda_chunk_fwd_workspace_size, kda_decode_step,
+                  kda_read_device_status, kda_version, library, library_path)
+
+__all__ = ["KDAError", "kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_decode_step",
+           "kda_read_device_status", "kda_version", "library", "library_path"]

@@ -1,0 +1,183 @@
+// C ABI of libkda: argument validation (the error boundary), workspace layout,
+// and dispatch to the kernels.  See include/kda.h for the contract.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <vector>
+
+#include "../../include/kda.h"
+#include "kda_internal.h"
+
+namespace {
+
+using kda::kHeadDim;
+using kda::kStatusBytes;
+
+constexpr int kVersion = 1 * 10000 + 0 * 100 + 0;
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool aligned16(const void *p) { return aligned(p, 16); }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+int check_dims(int32_t dk, int32_t dv, int dtype) {
+  if (dk <= 0 || dv <= 0) return KDA_ERR_INVALID_ARG;
+  if (dk != kHeadDim || dv != kHeadDim) return KDA_ERR_UNSUPPORTED;
+  if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+  return KDA_OK;
+}
+
+size_t workspace_bytes_for(int32_t n_seqs) {
+  return kStatusBytes + round_up(sizeof(int32_t) * ((size_t)n_seqs + 1), 256);
+}
+
+// True when `p` is memory the device can read directly as a device array.
+bool is_device_pointer(const void *p, bool *ok) {
+  cudaPointerAttributes attr;
+  memset(&attr, 0, sizeof(attr));
+  const cudaError_t e = cudaPointerGetAttributes(&attr, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    *ok = false;
+    return false;
+  }
+  *ok = true;
+  return attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kda_status_string(int status) {
+  switch (status) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid argument";
+    case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: unsupported head size or dtype";
+    case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace missing or too small";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA runtime or launch failure";
+    case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded in-kernel wait gave up";
+    default: return "KDA: unknown status";
+  }
+}
+
+int kda_version(void) { return kVersion; }
+
+int kda_chunk_fwd_workspace_size(int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk,
+                                 int32_t dv, int dtype, size_t *bytes) {
+  if (!bytes || n_seqs < 0 || n_tokens < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+  const int d = check_dims(dk, dv, dtype);
+  if (d != KDA_OK) return d;
+  *bytes = workspace_bytes_for(n_seqs);
+  return KDA_OK;
+}
+
+int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                  const float *beta, const float *init_state, const int32_t *cu_seqlens,
+                  int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk, int32_t dv,
+                  int dtype, void *out, float *final_state, void *workspace,
+                  size_t workspace_bytes, void *stream) {
+  // ---- host-side validation: nothing is launched unless all of it passes
+  if (n_seqs < 0 || n_tokens < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+  const int d = check_dims(dk, dv, dtype);
+  if (d != KDA_OK) return d;
+  if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
+  if (n_tokens > 0 && (!q || !k || !v || !log_alpha || !beta || !out)) return KDA_ERR_INVALID_ARG;
+  if ((int64_t)n_seqs * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+  // TMA-read tensors and states: 16 bytes; beta is read element-wise.
+  const void *tensors[] = {q, k, v, log_alpha, init_state, out, final_state};
+  for (const void *p : tensors)
+    if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  if (beta && !aligned(beta, 4)) return KDA_ERR_INVALID_ARG;
+  const size_t state_bytes = (size_t)n_seqs * H * dk * dv * sizeof(float);
+  if (init_state && final_state && state_bytes > 0 &&
+      ranges_overlap(init_state, state_bytes, final_state, state_bytes))
+    return KDA_ERR_INVALID_ARG;
+  const size_t need = workspace_bytes_for(n_seqs);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return KDA_ERR_WORKSPACE;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  bool attr_ok = false;
+  const bool cu_on_device = is_device_pointer(cu_seqlens, &attr_ok);
+  if (!attr_ok) return KDA_ERR_CUDA;
+  const int32_t *cu_dev = cu_seqlens;
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  if (!cu_on_device) {
+    // Host array: validate it here, then stage a device copy in the workspace.
+    if (cu_seqlens[0] != 0 || cu_seqlens[n_seqs] != n_tokens) return KDA_ERR_INVALID_ARG;
+    for (int32_t s = 0; s < n_seqs; ++s)
+      if (cu_seqlens[s + 1] < cu_seqlens[s]) return KDA_ERR_INVALID_ARG;
+    int32_t *dst = reinterpret_cast<int32_t *>(ws + kStatusBytes);
+    if (cudaMemcpyAsync(dst, cu_seqlens, sizeof(int32_t) * ((size_t)n_seqs + 1),
+                        cudaMemcpyHostToDevice, st) != cudaSuccess) {
+      cudaGetLastError();
+      return KDA_ERR_CUDA;
+    }
+    cu_dev = dst;
+  }
+  kda::DeviceStatus *status = reinterpret_cast<kda::DeviceStatus *>(ws);
+  if (cudaMemsetAsync(status, 0, sizeof(kda::DeviceStatus), st) != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_CUDA;
+  }
+  if (n_seqs == 0) return KDA_OK;
+
+  kda::ChunkArgs a;
+  a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta;
+  a.init_state = init_state; a.cu_seqlens = cu_dev; a.n_seqs = n_seqs; a.n_tokens = n_tokens;
+  a.H = H; a.out = out; a.final_state = final_state; a.status = status;
+  const cudaError_t e = dtype == KDA_BF16 ? kda::launch_chunk_fwd_bf16_tc(a, st)
+                                          : kda::launch_chunk_fwd_f32(a, st);
+  if (e == cudaErrorNotSupported) return KDA_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_read_device_status(void *workspace, void *stream, int clear, int32_t *device_status) {
+  if (!workspace || !device_status) return KDA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  kda::DeviceStatus host;
+  if (cudaStreamSynchronize(st) != cudaSuccess ||
+      cudaMemcpy(&host, workspace, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_CUDA;
+  }
+  if (clear && cudaMemset(workspace, 0, sizeof(host)) != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_CUDA;
+  }
+  *device_status = host.code;
+  return KDA_OK;
+}
+
+int kda_decode_step(float *state, const void *q, const void *k, const void *v,
+                    const float *log_alpha, const float *beta, int32_t B, int32_t H,
+                    int32_t dk, int32_t dv, int dtype, void *out, void *stream) {
+  if (B < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+  const int d = check_dims(dk, dv, dtype);
+  if (d != KDA_OK) return d;
+  if (!state || !q || !k || !v || !log_alpha || !beta || !out) return KDA_ERR_INVALID_ARG;
+  const size_t units = (size_t)B * H;
+  const size_t esz = dtype == KDA_BF16 ? 2 : 4;
+  // state: float4 accesses; v and out: 4-element vectors; the rest element-wise.
+  if (!aligned16(state) || !aligned(v, 4 * esz) || !aligned(out, 4 * esz) || !aligned(q, esz) ||
+      !aligned(k, esz) || !aligned(log_alpha, 4) || !aligned(beta, 4))
+    return KDA_ERR_INVALID_ARG;
+  if (units > 0 && ranges_overlap(state, units * dk * dv * sizeof(float), out, units * dv * esz))
+    return KDA_ERR_INVALID_ARG;
+  const cudaError_t e = kda::launch_decode_step(state, q, k, v, log_alpha, beta, B, H,
+                                                dtype == KDA_BF16, out,
+                                                static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_CUDA;
+  }
+  return KDA_OK;
+}
+
+}  // extern "C"

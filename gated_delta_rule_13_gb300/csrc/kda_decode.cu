@@ -1,0 +1,160 @@
+// KDA recurrent decode step: one token per (sequence, head), state in place.
+//
+// Per unit (b, h) with state S in R^{128 x 128} (dk rows, dv contiguous):
+//   X   = Diag(alpha) S                       (alpha = exp(log_alpha), per key row)
+//   u   = beta (v - X^T k)                    (delta-rule correction)
+//   S'  = X + k u^T                           (= (I - beta k k^T) X + beta k v^T)
+//   o   = S'^T q = X^T q + (k . q) u
+// ("Kimi K3" study notes, section 3-2 "2) Kimi Delta Attention": update and
+// read-out equations; the decode state advances in place: "Kimi K3: 架构、训练
+// 与系统全景解析", section 4.2.7).
+//
+// HBM-bound: a unit reads and writes its 64 KiB state exactly once.  One CTA
+// of 8 warps per unit; warp w owns value columns [16w, 16w+16) for all 128 key
+// rows, lane l owns 4 consecutive columns (one float4) of rows l/4 + 8j,
+// j = 0..15.  Both column reductions over the key dimension (X^T k, X^T q)
+// then stay inside a warp (three xor-shuffles), so the only block-wide barrier
+// is the one that publishes alpha, k and q.  The 16 float4 state loads are
+// issued before that barrier so their HBM latency overlaps it.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int D = kHeadDim;
+constexpr int kThreads = 256;
+
+template <bool BF16>
+__device__ __forceinline__ float load_elem(const void *p, int64_t i) {
+  if constexpr (BF16) {
+    return __bfloat162float(static_cast<const __nv_bfloat16 *>(p)[i]);
+  } else {
+    return static_cast<const float *>(p)[i];
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ float4 load4(const void *p, int64_t i) {
+  if constexpr (BF16) {
+    const uint2 raw = *reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(p) + i);
+    const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
+    const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
+    const float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
+    return make_float4(a.x, a.y, b.x, b.y);
+  } else {
+    return *reinterpret_cast<const float4 *>(static_cast<const float *>(p) + i);
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void store4(void *p, int64_t i, float4 x) {
+  if constexpr (BF16) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
+    uint2 raw;
+    raw.x = *reinterpret_cast<uint32_t *>(&lo);
+    raw.y = *reinterpret_cast<uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p) + i) = raw;
+  } else {
+    *reinterpret_cast<float4 *>(static_cast<float *>(p) + i) = x;
+  }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads, 2)
+kda_decode_step_kernel(float *__restrict__ state, const void *__restrict__ q,
+                       const void *__restrict__ k, const void *__restrict__ v,
+                       const float *__restrict__ log_alpha, const float *__restrict__ beta,
+                       void *__restrict__ out) {
+  __shared__ float s_alpha[D], s_k[D], s_q[D];
+  const int64_t unit = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int col = 16 * warp + 4 * (lane & 3);
+  const int row0 = lane >> 2;
+  float *S = state + unit * (int64_t)(D * D);
+
+  float4 s[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    s[j] = __ldcs(reinterpret_cast<const float4 *>(S + (row0 + 8 * j) * D + col));
+
+  if (tid < D) {
+    s_alpha[tid] = expf(log_alpha[unit * D + tid]);
+    s_k[tid] = load_elem<BF16>(k, unit * D + tid);
+    s_q[tid] = load_elem<BF16>(q, unit * D + tid);
+  }
+  const float4 vv = load4<BF16>(v, unit * D + col);
+  const float b = beta[unit];
+  __syncthreads();
+
+  // X = Diag(alpha) S; partial sums of X^T k and X^T q over this lane's rows.
+  float pk0 = 0.f, pk1 = 0.f, pk2 = 0.f, pk3 = 0.f;
+  float pq0 = 0.f, pq1 = 0.f, pq2 = 0.f, pq3 = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int r = row0 + 8 * j;
+    const float a = s_alpha[r], kr = s_k[r], qr = s_q[r];
+    s[j].x *= a; s[j].y *= a; s[j].z *= a; s[j].w *= a;
+    pk0 = fmaf(kr, s[j].x, pk0); pk1 = fmaf(kr, s[j].y, pk1);
+    pk2 = fmaf(kr, s[j].z, pk2); pk3 = fmaf(kr, s[j].w, pk3);
+    pq0 = fmaf(qr, s[j].x, pq0); pq1 = fmaf(qr, s[j].y, pq1);
+    pq2 = fmaf(qr, s[j].z, pq2); pq3 = fmaf(qr, s[j].w, pq3);
+  }
+  // Lanes with equal (lane & 3) hold the same columns: reduce over lane bits 2..4.
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    pk0 += __shfl_xor_sync(0xffffffffu, pk0, off);
+    pk1 += __shfl_xor_sync(0xffffffffu, pk1, off);
+    pk2 += __shfl_xor_sync(0xffffffffu, pk2, off);
+    pk3 += __shfl_xor_sync(0xffffffffu, pk3, off);
+    pq0 += __shfl_xor_sync(0xffffffffu, pq0, off);
+    pq1 += __shfl_xor_sync(0xffffffffu, pq1, off);
+    pq2 += __shfl_xor_sync(0xffffffffu, pq2, off);
+    pq3 += __shfl_xor_sync(0xffffffffu, pq3, off);
+  }
+  // k . q over the 128 key channels (every warp computes it).
+  float kq = 0.f;
+#pragma unroll
+  for (int j = 0; j < D / 32; ++j) kq = fmaf(s_k[lane + 32 * j], s_q[lane + 32 * j], kq);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+
+  const float u0 = b * (vv.x - pk0), u1 = b * (vv.y - pk1);
+  const float u2 = b * (vv.z - pk2), u3 = b * (vv.w - pk3);
+  if (row0 == 0) {
+    store4<BF16>(out, unit * D + col,
+                 make_float4(fmaf(kq, u0, pq0), fmaf(kq, u1, pq1), fmaf(kq, u2, pq2),
+                             fmaf(kq, u3, pq3)));
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float kr = s_k[row0 + 8 * j];
+    float4 x = s[j];
+    x.x = fmaf(kr, u0, x.x); x.y = fmaf(kr, u1, x.y);
+    x.z = fmaf(kr, u2, x.z); x.w = fmaf(kr, u3, x.w);
+    __stcs(reinterpret_cast<float4 *>(S + (row0 + 8 * j) * D + col), x);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_step(float *state, const void *q, const void *k, const void *v,
+                               const float *log_alpha, const float *beta, int32_t B, int32_t H,
+                               bool bf16, void *out, cudaStream_t stream) {
+  const int64_t units = (int64_t)B * H;
+  if (units == 0) return cudaSuccess;
+  if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)units), block(kThreads);
+  if (bf16) {
+    kda_decode_step_kernel<true><<<grid, block, 0, stream>>>(state, q, k, v, log_alpha, beta, out);
+  } else {
+    kda_decode_step_kernel<false><<<grid, block, 0, stream>>>(state, q, k, v, log_alpha, beta, out);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace kda

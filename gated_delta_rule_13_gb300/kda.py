@@ -1,0 +1,200 @@
+"""Thin Python binding of libkda (argument marshalling only).
+
+Every function here has the name of the C entry point it wraps (include/kda.h)
+and does nothing but check tensor shapes, dtypes and devices, allocate outputs
+when the caller did not pass them, and forward raw device pointers plus the
+current CUDA stream.  All arithmetic runs in the CUDA kernels of libkda.so.
+There is no fallback: if the library is missing or a call fails, an exception
+is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = 1
+KDA_ERR_UNSUPPORTED = 2
+KDA_ERR_WORKSPACE = 3
+KDA_ERR_CUDA = 4
+KDA_ERR_TIMEOUT = 5
+KDA_F32 = 0
+KDA_BF16 = 1
+HEAD_DIM = 128
+
+# Symbols declared in include/kda.h.
+EXPORTED = ("kda_status_string", "kda_version", "kda_chunk_fwd_workspace_size",
+            "kda_chunk_fwd", "kda_read_device_status", "kda_decode_step")
+
+_lib = None
+
+
+class KDAError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} (code {code})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def library() -> ctypes.CDLL:
+    """Load libkda.so (built by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise ImportError(f"libkda.so is not built ({path}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_status_string.argtypes = [ctypes.c_int]
+        lib.kda_version.restype = ctypes.c_int
+        lib.kda_version.argtypes = []
+        lib.kda_chunk_fwd_workspace_size.restype = ctypes.c_int
+        lib.kda_chunk_fwd_workspace_size.argtypes = [i32, i64, i32, i32, i32, ctypes.c_int,
+                                                     ctypes.POINTER(sz)]
+        lib.kda_chunk_fwd.restype = ctypes.c_int
+        lib.kda_chunk_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32,
+                                      ctypes.c_int, vp, vp, vp, sz, vp]
+        lib.kda_read_device_status.restype = ctypes.c_int
+        lib.kda_read_device_status.argtypes = [vp, vp, ctypes.c_int, ctypes.POINTER(i32)]
+        lib.kda_decode_step.restype = ctypes.c_int
+        lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                        ctypes.c_int, vp, vp]
+        _lib = lib
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return library().kda_status_string(int(code)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != KDA_OK:
+        raise KDAError(rc, what)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_F32
+    raise TypeError(f"q/k/v must be bfloat16 or float32, got {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need_cuda(name, t, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def kda_version() -> int:
+    return library().kda_version()
+
+
+def kda_chunk_fwd_workspace_size(n_seqs: int, n_tokens: int, H: int, dk: int = HEAD_DIM,
+                                 dv: int = HEAD_DIM, dtype: int = KDA_BF16) -> int:
+    out = ctypes.c_size_t(0)
+    _check(library().kda_chunk_fwd_workspace_size(n_seqs, n_tokens, H, dk, dv, dtype,
+                                                  ctypes.byref(out)),
+           "kda_chunk_fwd_workspace_size")
+    return out.value
+
+
+def kda_chunk_fwd(q, k, v, log_alpha, beta, init_state=None, cu_seqlens=None, *, out=None,
+                  final_state=None, workspace=None, output_final_state=True, stream=None):
+    """Chunked KDA prefill.  q, k ``[N, H, 128]`` and v ``[N, H, 128]`` (bf16 or
+    fp32, same dtype); log_alpha ``[N, H, 128]`` fp32; beta ``[N, H]`` fp32;
+    init_state ``[n_seqs, H, 128, 128]`` fp32 or None; cu_seqlens int32
+    ``[n_seqs + 1]`` (CUDA or CPU tensor) or None for one sequence.
+    Returns ``(out, final_state)`` (final_state None if not requested)."""
+    _need_cuda("q", q)
+    N, H, dk = q.shape
+    dt = q.dtype
+    _need_cuda("k", k, dt, (N, H, dk))
+    _need_cuda("v", v, dt)
+    if v.shape[:2] != (N, H):
+        raise ValueError("v must be [N, H, dv]")
+    dv = v.shape[2]
+    _need_cuda("log_alpha", log_alpha, torch.float32, (N, H, dk))
+    _need_cuda("beta", beta, torch.float32, (N, H))
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, N], dtype=torch.int32, device=q.device)
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_contiguous():
+        raise TypeError("cu_seqlens must be a contiguous 1-D int32 tensor")
+    n_seqs = cu_seqlens.shape[0] - 1
+    if init_state is not None:
+        _need_cuda("init_state", init_state, torch.float32, (n_seqs, H, dk, dv))
+    if out is None:
+        out = torch.empty(N, H, dv, dtype=dt, device=q.device)
+    _need_cuda("out", out, dt, (N, H, dv))
+    if final_state is None and output_final_state:
+        final_state = torch.empty(n_seqs, H, dk, dv, dtype=torch.float32, device=q.device)
+    if final_state is not None:
+        _need_cuda("final_state", final_state, torch.float32, (n_seqs, H, dk, dv))
+    code = _dtype_code(q)
+    ws_bytes = kda_chunk_fwd_workspace_size(n_seqs, N, H, dk, dv, code)
+    if workspace is None:
+        workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=q.device)
+    _need_cuda("workspace", workspace)
+    rc = library().kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                 _ptr(init_state), _ptr(cu_seqlens), n_seqs, N, H, dk, dv,
+                                 code, _ptr(out), _ptr(final_state), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(),
+                                 _stream_handle(stream))
+    _check(rc, "kda_chunk_fwd")
+    return out, final_state
+
+
+def kda_read_device_status(workspace, stream=None, clear: bool = True) -> int:
+    """Synchronise the stream and return the device status a kda_chunk_fwd
+    workspace recorded (KDA_OK or a kda_status code)."""
+    _need_cuda("workspace", workspace)
+    st = ctypes.c_int32(0)
+    _check(library().kda_read_device_status(_ptr(workspace), _stream_handle(stream),
+                                            1 if clear else 0, ctypes.byref(st)),
+           "kda_read_device_status")
+    return st.value
+
+
+def kda_decode_step(state, q, k, v, log_alpha, beta, *, out=None, stream=None):
+    """One in-place decode step.  state ``[B, H, 128, 128]`` fp32 (updated in
+    place); q, k ``[B, H, 128]``, v ``[B, H, 128]`` (bf16 or fp32); log_alpha
+    ``[B, H, 128]`` fp32; beta ``[B, H]`` fp32.  Returns out ``[B, H, 128]``."""
+    _need_cuda("state", state, torch.float32)
+    B, H, dk, dv = state.shape
+    _need_cuda("q", q, None, (B, H, dk))
+    dt = q.dtype
+    _need_cuda("k", k, dt, (B, H, dk))
+    _need_cuda("v", v, dt, (B, H, dv))
+    _need_cuda("log_alpha", log_alpha, torch.float32, (B, H, dk))
+    _need_cuda("beta", beta, torch.float32, (B, H))
+    if out is None:
+        out = torch.empty(B, H, dv, dtype=dt, device=q.device)
+    _need_cuda("out", out, dt, (B, H, dv))
+    rc = library().kda_decode_step(_ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                                   _ptr(beta), B, H, dk, dv, _dtype_code(q), _ptr(out),
+                                   _stream_handle(stream))
+    _check(rc, "kda_decode_step")
+    return out

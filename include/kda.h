@@ -1,0 +1,162 @@
+/*
+ * kda.h: C ABI of the GB300 (sm_103a) KDA recurrence library (libkda.so).
+ *
+ * The operation.  Per (sequence, head), with key dimension dk and value
+ * dimension dv (both 128 here), a matrix state S in R^{dk x dv} evolves token
+ * by token as
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = S_t^T q_t
+ *
+ * ("Kimi K3" study notes, dimensionstp, section 3-2 "2) Kimi Delta Attention":
+ * state-update and read-out equations).  alpha_t = exp(log_alpha_t) is a decay
+ * per key channel ("Kimi K3: 架构、训练与系统全景解析", section 4.2.2, first of
+ * the three parts of the update), beta_t is the scalar write strength, and the
+ * read-out uses the post-update state with no scale factor (same section, last
+ * paragraph).  K3 bounds the log-decay below by -5 (same page, sections 2.1 and
+ * 4.2.5), so over any 16-token tile the cumulative log-decay lies in [-80, 0]
+ * and its inverse exponential stays within the bf16/fp32 range.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are caller-owned DEVICE memory unless stated
+ *     otherwise and C-contiguous.  Alignment: see each entry point (beta is
+ *     always only element-aligned).  The library never allocates or frees
+ *     device memory and keeps no global state.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = legacy default stream).  Inputs must stay alive and unmodified
+ *     until the stream has passed the call.
+ *   - Every function returns a kda_status code; nothing is launched when the
+ *     return value is not KDA_OK.  No exceptions cross the ABI.
+ *   - Preconditions that are NOT checked (accuracy is only guaranteed inside
+ *     them): log_alpha in [-5, 0], beta in [0, 1], q and k finite with
+ *     ||k||_2 <= 1 (the KDA layer L2-normalises q and k).
+ *   - Only dk = dv = 128 is supported (KDA head dimension of K3); any other
+ *     positive value returns KDA_ERR_UNSUPPORTED.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+enum kda_status_code {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1, /* null / misaligned / overlapping / inconsistent args */
+  KDA_ERR_UNSUPPORTED = 2, /* dk, dv or dtype outside what the kernels implement  */
+  KDA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required          */
+  KDA_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed         */
+  KDA_ERR_TIMEOUT = 5      /* a bounded in-kernel wait gave up (device status)     */
+};
+
+/* Element type of q, k, v and out.  log_alpha, beta and states are always fp32. */
+enum kda_dtype_code {
+  KDA_F32 = 0,
+  KDA_BF16 = 1
+};
+
+/* Static description of a status code.  Never returns NULL. */
+const char *kda_status_string(int status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int kda_version(void);
+
+/*
+ * Bytes of device workspace kda_chunk_fwd needs for this problem size, written
+ * to *bytes.  The workspace holds the device status word (bounded waits that
+ * give up record KDA_ERR_TIMEOUT there; a device-resident cu_seqlens that is
+ * not a valid prefix sum records KDA_ERR_INVALID_ARG) and, when cu_seqlens is
+ * a host pointer, a device copy of it.
+ * Errors: KDA_ERR_INVALID_ARG for a NULL `bytes` or negative sizes,
+ * KDA_ERR_UNSUPPORTED for dk/dv/dtype outside the supported set.
+ */
+int kda_chunk_fwd_workspace_size(int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk,
+                                 int32_t dv, int dtype, size_t *bytes);
+
+/*
+ * Chunkwise-parallel prefill over packed variable-length sequences.
+ *
+ * The sequences are cut into chunks of 64 tokens (never straddling a sequence
+ * boundary; the last chunk of a sequence may be partial).  Inside a chunk the
+ * causal token-token interactions are dense lower-triangular matrix products;
+ * across chunks the fp32 state is carried serially ("Kimi K3: 架构、训练与系统
+ * 全景解析", section 4.2.4: state passed between chunks, lower-triangular
+ * matrix work within a chunk, output = a term reading the pre-chunk state plus
+ * an intra-chunk causal term; the UT-transform form of the intra-chunk solve).
+ * The result equals the token-by-token recurrence above up to rounding.
+ *
+ * Arguments (N = n_tokens, S = n_seqs):
+ *   q, k       [N, H, dk]  dtype       queries / keys
+ *   v          [N, H, dv]  dtype       values
+ *   log_alpha  [N, H, dk]  fp32        per-channel log-decay (<= 0, >= -5)
+ *   beta       [N, H]      fp32        write strength
+ *   init_state [S, H, dk, dv] fp32 or NULL (zero state).  READ ONLY: a cached
+ *              state snapshot is never modified (prefix-cache snapshots are
+ *              copied, not advanced in place: same page, section 7.4).
+ *   cu_seqlens [S + 1] int32, cu_seqlens[0] = 0, non-decreasing,
+ *              cu_seqlens[S] = N.  May be host or device memory: a host array
+ *              is validated here (KDA_ERR_INVALID_ARG on failure) and copied
+ *              into the workspace; a device array is validated by the kernel,
+ *              which then writes nothing and records KDA_ERR_INVALID_ARG in
+ *              the device status.
+ *   dtype      KDA_F32 (fp32 CUDA-core path) or KDA_BF16 (tcgen05 tensor-core
+ *              path; fp32 state and accumulation).
+ *   out        [N, H, dv]  dtype       o_t for every token
+ *   final_state [S, H, dk, dv] fp32 or NULL.  Must not overlap init_state.
+ *   workspace  device memory of at least kda_chunk_fwd_workspace_size() bytes,
+ *              16-byte aligned; its device status word is cleared at the start
+ *              of every call (stream-ordered).
+ * Alignment: q, k, v, log_alpha, out, init_state, final_state 16 bytes (tiles
+ * are fetched by TMA); beta 4 bytes.
+ * A zero-length sequence writes final_state = init_state (or zeros).
+ * Errors (returned before any launch): KDA_ERR_INVALID_ARG (NULL required
+ * pointer, H <= 0, negative sizes, misalignment, init/final overlap, bad host
+ * cu_seqlens), KDA_ERR_UNSUPPORTED (dk or dv != 128, unknown dtype),
+ * KDA_ERR_WORKSPACE (NULL or too small), KDA_ERR_CUDA (launch failure).
+ */
+int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                  const float *beta, const float *init_state, const int32_t *cu_seqlens,
+                  int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk, int32_t dv,
+                  int dtype, void *out, float *final_state, void *workspace,
+                  size_t workspace_bytes, void *stream);
+
+/*
+ * Reads (and, if `clear` is non-zero, resets) the device status word of a
+ * kda_chunk_fwd workspace.  Synchronises `stream` first, so it reports the
+ * status of every call issued on that stream before it.  *device_status gets
+ * KDA_OK or the kda_status code a kernel recorded.
+ * Errors: KDA_ERR_INVALID_ARG (NULL workspace or device_status), KDA_ERR_CUDA.
+ */
+int kda_read_device_status(void *workspace, void *stream, int clear, int32_t *device_status);
+
+/*
+ * One recurrent decode step for B sequences x H heads, one new token each,
+ * state advanced IN PLACE (the decode state is advanced in place:
+ * "Kimi K3: 架构、训练与系统全景解析", section 4.2.7).
+ *
+ *   state      [B, H, dk, dv] fp32   read, then overwritten with S_t
+ *   q, k       [B, H, dk]  dtype
+ *   v          [B, H, dv]  dtype
+ *   log_alpha  [B, H, dk]  fp32
+ *   beta       [B, H]      fp32
+ *   out        [B, H, dv]  dtype     o_t = S_t^T q_t
+ * One HBM pass: each state is read once and written once.
+ * Alignment: state 16 bytes; v and out 4 elements; q, k 1 element;
+ * log_alpha and beta 4 bytes.
+ * Errors (before any launch): KDA_ERR_INVALID_ARG (NULL pointer, B < 0,
+ * H <= 0, misalignment, `out` overlapping `state`), KDA_ERR_UNSUPPORTED
+ * (dk or dv != 128, unknown dtype), KDA_ERR_CUDA (launch failure).
+ */
+int kda_decode_step(float *state, const void *q, const void *k, const void *v,
+                    const float *log_alpha, const float *beta, int32_t B, int32_t H,
+                    int32_t dk, int32_t dv, int dtype, void *out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,135 @@
+"""Host-only checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments before touching the GPU.
+
+Nothing here launches a kernel or needs a GPU: every call below fails host-side
+validation, which runs before any CUDA call.  Pointers are fake, 16-byte
+aligned addresses that are never dereferenced.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_delta_rule_13_gb300 import _build, kda
+    _build.build_library()
+    return kda.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_functions()
+    for n in ("kda_chunk_fwd", "kda_decode_step", "kda_chunk_fwd_workspace_size",
+              "kda_status_string", "kda_read_device_status", "kda_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libkda.so does not export {name}"
+    from gated_delta_rule_13_gb300 import kda
+    assert set(kda.EXPORTED) == set(declared_functions())
+
+
+def test_status_strings(lib):
+    from gated_delta_rule_13_gb300 import kda
+    for code in range(6):
+        s = kda.status_string(code)
+        assert s.startswith("KDA_")
+    assert "unknown" in kda.status_string(99)
+    assert kda.kda_version() >= 10000
+
+
+A = 0x10000  # fake aligned addresses, never dereferenced
+
+
+def _fwd(lib, **over):
+    args = dict(q=A, k=A + 0x1000, v=A + 0x2000, la=A + 0x3000, beta=A + 0x4000, s0=None,
+                cu=A + 0x5000, n_seqs=2, n_tokens=100, H=4, dk=128, dv=128, dtype=1,
+                out=A + 0x6000, fin=None, ws=A + 0x7000, ws_bytes=1 << 20, stream=None)
+    args.update(over)
+    vp = ctypes.c_void_p
+    return lib.kda_chunk_fwd(vp(args["q"]), vp(args["k"]), vp(args["v"]), vp(args["la"]),
+                             vp(args["beta"]), vp(args["s0"]), vp(args["cu"]), args["n_seqs"],
+                             args["n_tokens"], args["H"], args["dk"], args["dv"], args["dtype"],
+                             vp(args["out"]), vp(args["fin"]), vp(args["ws"]), args["ws_bytes"],
+                             vp(args["stream"]))
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(la=None), 1),
+    (dict(beta=None), 1), (dict(out=None), 1), (dict(cu=None), 1),
+    (dict(H=0), 1), (dict(H=-3), 1), (dict(n_seqs=-1), 1), (dict(n_tokens=-5), 1),
+    (dict(dk=0), 1), (dict(dk=64), 2), (dict(dv=256), 2), (dict(dtype=7), 2),
+    (dict(q=A + 8), 1), (dict(out=A + 0x6004), 1), (dict(la=A + 0x3002), 1),
+    (dict(s0=A + 0x100000, fin=A + 0x100000 + 4096), 1),   # init/final overlap
+    (dict(ws=None), 3), (dict(ws_bytes=16), 3), (dict(ws=A + 0x7008), 3),
+])
+def test_chunk_fwd_rejects_before_launch(lib, over, code):
+    assert _fwd(lib, **over) == code
+
+
+def test_workspace_size(lib):
+    from gated_delta_rule_13_gb300 import kda
+    a = kda.kda_chunk_fwd_workspace_size(1, 512, 1)
+    b = kda.kda_chunk_fwd_workspace_size(1000, 512, 1)
+    assert a >= 256 + 8 and b >= 256 + 4 * 1001 and a % 256 == 0 and b % 256 == 0
+    with pytest.raises(kda.KDAError) as e:
+        kda.kda_chunk_fwd_workspace_size(1, 512, 1, dk=64)
+    assert e.value.code == kda.KDA_ERR_UNSUPPORTED
+    with pytest.raises(kda.KDAError) as e:
+        kda.kda_chunk_fwd_workspace_size(-1, 512, 1)
+    assert e.value.code == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_chunk_fwd_workspace_size(1, 1, 1, 128, 128, 1, None) == 1
+
+
+def _dec(lib, **over):
+    args = dict(state=A, q=A + 0x1000, k=A + 0x2000, v=A + 0x3000, la=A + 0x4000,
+                beta=A + 0x5000, B=4, H=2, dk=128, dv=128, dtype=1, out=A + 0x40000000,
+                stream=None)
+    args.update(over)
+    vp = ctypes.c_void_p
+    return lib.kda_decode_step(vp(args["state"]), vp(args["q"]), vp(args["k"]), vp(args["v"]),
+                               vp(args["la"]), vp(args["beta"]), args["B"], args["H"],
+                               args["dk"], args["dv"], args["dtype"], vp(args["out"]),
+                               vp(args["stream"]))
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(state=None), 1), (dict(q=None), 1), (dict(out=None), 1), (dict(beta=None), 1),
+    (dict(B=-1), 1), (dict(H=0), 1), (dict(dk=32), 2), (dict(dv=64), 2), (dict(dtype=3), 2),
+    (dict(k=A + 0x2001), 1), (dict(v=A + 0x3004), 1), (dict(beta=A + 0x5002), 1),
+    (dict(out=A + 0x800), 1),                               # out inside the state
+])
+def test_decode_rejects_before_launch(lib, over, code):
+    assert _dec(lib, **over) == code
+
+
+def test_read_device_status_null(lib):
+    st = ctypes.c_int32(0)
+    assert lib.kda_read_device_status(None, None, 0, ctypes.byref(st)) == 1
+    assert lib.kda_read_device_status(ctypes.c_void_p(A), None, 0, None) == 1
+
+
+def test_product_path_does_not_import_oracle():
+    """The CUDA path never reaches the oracle (it is test infrastructure)."""
+    pkg = os.path.join(ROOT, "gated_delta_rule_13_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".c")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "kda_oracle" not in text, f

@@ -1,0 +1,162 @@
+"""GPU parity of kda_chunk_fwd against the fp64 oracle, plus properties and
+device-side error reporting.  fp32 inputs take the CUDA-core path (1e-4), bf16
+inputs the tcgen05 tensor-core path (2e-2)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from gated_delta_rule_13_gb300 import inputs, kda
+from parity_util import TOL, oracle_prefill, rel_l2
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+DTYPES = ["f32", "bf16"]
+
+
+def run(x, **kw):
+    out, fin = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
+                                 x["init_state"], x["cu_seqlens"], **kw)
+    torch.cuda.synchronize()
+    return out, fin
+
+
+def check(x, dtype, heads=None, seqs=None):
+    out, fin = run(x)
+    o_ref, s_ref, idx = oracle_prefill(x, heads=heads, seqs=seqs)
+    H = x["q"].shape[1]
+    hsel = torch.as_tensor(heads if heads is not None else list(range(H)), device=DEV)
+    got_o = out.index_select(0, torch.as_tensor(idx, device=DEV)).index_select(1, hsel)
+    n_seqs = x["cu_seqlens"].shape[0] - 1
+    ssel = torch.as_tensor(seqs if seqs is not None else list(range(n_seqs)), device=DEV)
+    got_s = fin.index_select(0, ssel).index_select(1, hsel)
+    eo, es = rel_l2(got_o, o_ref), rel_l2(got_s, s_ref)
+    assert eo <= TOL[dtype], f"out rel L2 {eo:.3e}"
+    assert es <= TOL[dtype], f"final state rel L2 {es:.3e}"
+    return eo, es
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_tiny_workload(dtype):
+    """B=1, H=1, T=512 (fp32 is the tiny workload itself)."""
+    x = inputs.prefill_inputs([512], H=1, dtype=dtype, device=DEV)
+    check(x, dtype)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("with_init", [False, True])
+def test_ragged_lengths(dtype, with_init):
+    lengths = [0, 1, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 200]
+    x = inputs.prefill_inputs(lengths, H=3, dtype=dtype, init_state=with_init, device=DEV, seed=1)
+    check(x, dtype)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("case", ["la0", "la_floor", "beta0", "beta1"])
+def test_edge_values(dtype, case):
+    x = inputs.prefill_inputs([300, 77], H=2, dtype=dtype, init_state=True, device=DEV, seed=2)
+    if case == "la0":
+        x["log_alpha"].zero_()
+    elif case == "la_floor":
+        x["log_alpha"].fill_(-5.0)          # worst case for the e^80 tile factors
+    elif case == "beta0":
+        # No writes: the state only decays.  Mild decay keeps the exact final
+        # state (fp64) inside fp32 range, where a relative error means something.
+        x["beta"].zero_()
+        x["log_alpha"].mul_(0.01)
+    else:
+        x["beta"].fill_(1.0)
+    check(x, dtype)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_init_state_is_read_only_and_zero_length(dtype):
+    x = inputs.prefill_inputs([0, 70, 0], H=2, dtype=dtype, init_state=True, device=DEV, seed=3)
+    s0 = x["init_state"].clone()
+    out, fin = run(x)
+    assert torch.equal(x["init_state"], s0)
+    assert torch.equal(fin[0], s0[0]) and torch.equal(fin[2], s0[2])
+    x["init_state"] = None
+    _, fin0 = run(x)
+    assert bool((fin0[0] == 0).all()) and bool((fin0[2] == 0).all())
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_deterministic(dtype):
+    x = inputs.prefill_inputs([257, 64], H=2, dtype=dtype, init_state=True, device=DEV, seed=4)
+    o1, s1 = run(x)
+    o1, s1 = o1.clone(), s1.clone()
+    o2, s2 = run(x)
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_split_with_state_handoff(dtype):
+    """One call over T tokens equals two calls with the state handed over at a
+    chunk-aligned cut (a prefix-cache resume) and at a ragged cut."""
+    T = 1024
+    x = inputs.prefill_inputs([T], H=2, dtype=dtype, init_state=True, device=DEV, seed=5)
+    out, fin = run(x)
+    for cut in (512, 389):
+        a = {k: (v[:cut] if k in ("q", "k", "v", "log_alpha", "beta") else v)
+             for k, v in x.items()}
+        a["cu_seqlens"] = torch.tensor([0, cut], dtype=torch.int32, device=DEV)
+        o1, s1 = run(a)
+        b = {k: (v[cut:] if k in ("q", "k", "v", "log_alpha", "beta") else v)
+             for k, v in x.items()}
+        b["cu_seqlens"] = torch.tensor([0, T - cut], dtype=torch.int32, device=DEV)
+        b["init_state"] = s1
+        o2, s2 = run(b)
+        tol = TOL[dtype]
+        assert rel_l2(torch.cat([o1, o2]), out) <= tol
+        assert rel_l2(s2, fin) <= tol
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_decode_steps_equal_prefill(dtype):
+    T = 40
+    x = inputs.prefill_inputs([T], H=2, dtype=dtype, init_state=True, device=DEV, seed=6)
+    out, fin = run(x)
+    state = x["init_state"].clone()
+    outs = []
+    for t in range(T):
+        outs.append(kda.kda_decode_step(state, x["q"][t:t + 1], x["k"][t:t + 1],
+                                        x["v"][t:t + 1], x["log_alpha"][t:t + 1],
+                                        x["beta"][t:t + 1]))
+    torch.cuda.synchronize()
+    tol = TOL[dtype]
+    assert rel_l2(torch.cat(outs), out) <= tol
+    assert rel_l2(state, fin) <= tol
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_host_cu_seqlens(dtype):
+    x = inputs.prefill_inputs([100, 50], H=2, dtype=dtype, init_state=True, device=DEV, seed=7)
+    o_dev, s_dev = run(x)
+    o_dev, s_dev = o_dev.clone(), s_dev.clone()
+    x["cu_seqlens"] = x["cu_seqlens"].cpu()
+    o_host, s_host = run(x)
+    assert torch.equal(o_dev, o_host) and torch.equal(s_dev, s_host)
+    bad = dict(x)
+    bad["cu_seqlens"] = torch.tensor([0, 120, 110], dtype=torch.int32)
+    with pytest.raises(kda.KDAError) as e:
+        run(bad)
+    assert e.value.code == kda.KDA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_invalid_device_cu_seqlens_reports_status(dtype):
+    x = inputs.prefill_inputs([100, 50], H=2, dtype=dtype, device=DEV, seed=8)
+    x["cu_seqlens"] = torch.tensor([0, 120, 110], dtype=torch.int32, device=DEV)
+    ws = torch.zeros(kda.kda_chunk_fwd_workspace_size(2, 150, 2, dtype=
+                                                      kda.KDA_BF16 if dtype == "bf16" else
+                                                      kda.KDA_F32),
+                     dtype=torch.uint8, device=DEV)
+    run(x, workspace=ws)
+    assert kda.kda_read_device_status(ws) == kda.KDA_ERR_INVALID_ARG
+    assert kda.kda_read_device_status(ws) == kda.KDA_OK  # cleared by the read
+    # a valid call afterwards on the same workspace reports OK
+    x["cu_seqlens"] = torch.tensor([0, 100, 150], dtype=torch.int32, device=DEV)
+    run(x, workspace=ws)
+    assert kda.kda_read_device_status(ws) == kda.KDA_OK
