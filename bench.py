@@ -1,0 +1,373 @@
+"""Benchmark of the KDA recurrence hot path on GB300.
+
+One step = one chunked prefill (kda_chunk_fwd) over the K3 head layout
+(B=1, H=96, T=32768, d=128, bf16 q/k/v, fp32 log_alpha/beta, fp32 final state)
+plus one in-place decode step (kda_decode_step) over 512 sequences x 96 heads.
+``value`` is prefill tokens/s (the prefill kernel's CUDA-event time over the
+timed steps); the decode step is reported beside it in GB/s against the HBM
+peak.  Inputs are synthetic (seeded, ``gated_delta_rule_13_gb300.inputs``) and
+larger than L2, so no flush is needed between iterations.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
+
+With N > 1 (launched by torch.distributed.run) every rank runs an independent
+replica on its own GPU (the path has no exchange step): value = all ranks'
+tokens / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s (H=96,d=128, % tensor roofline); decode GB/s vs HBM peak"
+PREFILL_FLOP_PER_TOKEN_HEAD = 139264      # 5*C*d + 6*d^2 at C = 64, d = 128
+PREFILL_BYTES_PER_TOKEN_HEAD = 1540       # bf16 q,k,v,out + fp32 log_alpha + fp32 beta
+STATE_BYTES = 128 * 128 * 4
+DECODE_BYTES_PER_UNIT = 2 * STATE_BYTES + 3 * 256 + 512 + 4 + 256
+L2_BYTES = 129 * 1024 * 1024
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- oracle (CPU)
+def oracle_rate(workload, n_heads_sample: int, n_tokens_sample: int, seed=0):
+    """Times the fp64 oracle on `n_heads_sample` heads x the first
+    `n_tokens_sample` tokens of the workload; returns (token-heads/s, threads, desc)."""
+    import numpy as np
+    import oracle
+    from gated_delta_rule_13_gb300 import inputs
+    w = inputs.WORKLOADS[workload]
+    x = inputs.prefill_inputs([n_tokens_sample], H=n_heads_sample, dtype=w.dtype,
+                              init_state=w.init_state, device="cpu", seed=seed)
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["init_state"],
+                     np.array([0, n_tokens_sample]), n_threads=threads)
+    dt = time.perf_counter() - t0
+    th = n_heads_sample * n_tokens_sample
+    desc = (f"oracle on {n_heads_sample} heads x {n_tokens_sample} tokens of {workload} "
+            f"(same value distributions), {threads} threads, {dt:.2f} s")
+    return th / dt, threads, desc, dt
+
+
+def calibrated_sample(workload, target_s: float):
+    """Chooses (heads, tokens) of the workload so that one multi-threaded oracle
+    run takes about `target_s` seconds: first one head per host thread, growing
+    the token count up to the sequence length, then more heads."""
+    import oracle
+    from gated_delta_rule_13_gb300 import inputs
+    w = inputs.WORKLOADS[workload]
+    threads = oracle.default_threads()
+    rate1, _, _, _ = oracle_rate(workload, 1, 256)        # single chain = single thread
+    heads = min(w.H, threads)
+    T = int(max(256, min(w.seq_lengths[0], target_s * rate1)))
+    if T >= w.seq_lengths[0]:
+        rounds = max(1, int(target_s * rate1 / T))
+        heads = min(w.H, threads * rounds)
+    return heads, T
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from gated_delta_rule_13_gb300 import inputs
+    w = inputs.WORKLOADS[args.workload]
+    budget = args.ref_step_s if args.ref_step_s > 0 else max(0.5, 150.0 / (args.steps + args.warmup))
+    heads, T = calibrated_sample(args.workload, budget)
+    rates = []
+    desc = ""
+    threads = 1
+    for s in range(args.warmup + args.steps):
+        rate, threads, desc, dt = oracle_rate(args.workload, heads, T, seed=s)
+        if s >= args.warmup:
+            rates.append(rate)
+    th_rate = statistics.median(rates)
+    value = th_rate / w.H                      # tokens/s of the H-head workload
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * heads * T / th_rate, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": args.workload, "note": w.note},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def prefill_bytes(x, H):
+    n_tok = int(x["q"].shape[0])
+    n_seqs = int(x["cu_seqlens"].shape[0] - 1)
+    states = n_seqs * H * (2 if x["init_state"] is not None else 1)
+    return n_tok * H * PREFILL_BYTES_PER_TOKEN_HEAD + states * STATE_BYTES
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    from gated_delta_rule_13_gb300 import inputs, kda
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (use --impl reference for the CPU oracle)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+    w = inputs.WORKLOADS[args.workload]
+    H = w.H
+
+    # ---- inputs resident in HBM
+    x = inputs.workload_inputs(args.workload, device=dev, seed=rank)
+    n_tok = int(x["q"].shape[0])
+    out = torch.empty(n_tok, H, 128, dtype=torch.bfloat16, device=dev)
+    fin = torch.empty(len(x["lengths"]), H, 128, 128, dtype=torch.float32, device=dev)
+    ws = torch.zeros(kda.kda_chunk_fwd_workspace_size(len(x["lengths"]), n_tok, H),
+                     dtype=torch.uint8, device=dev)
+    dw = inputs.WORKLOADS["decode_b512_h96"]
+    n_dec_steps = 4
+    d = inputs.decode_inputs(B=dw.B, H=dw.H, steps=n_dec_steps, dtype=dw.dtype, device=dev,
+                             seed=rank)
+    state = d["state"]
+    dout = torch.empty(dw.B, dw.H, 128, dtype=torch.bfloat16, device=dev)
+
+    def prefill():
+        kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["init_state"],
+                          x["cu_seqlens"], out=out, final_state=fin, workspace=ws)
+
+    def decode(s):
+        i = s % n_dec_steps
+        kda.kda_decode_step(state, d["q"][i], d["k"][i], d["v"][i], d["log_alpha"][i],
+                            d["beta"][i], out=dout)
+
+    for s in range(args.warmup):
+        prefill()
+        decode(s)
+    torch.cuda.synchronize()
+    if kda.kda_read_device_status(ws) != kda.KDA_OK:
+        raise RuntimeError("prefill kernel reported a device error during warm-up")
+
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_wall = time.perf_counter()
+        for s in range(args.steps):
+            e0, e1, e2 = ev[s]
+            e0.record(stream)
+            prefill()
+            e1.record(stream)
+            decode(args.warmup + s)
+            e2.record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    pre_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    dec_ms = [b.elapsed_time(c) for _, b, c in ev]
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    tot_ms = sum(step_ms)
+    pre_avg = sum(pre_ms) / len(pre_ms)
+    dec_avg = sum(dec_ms) / len(dec_ms)
+    if world > 1:
+        t = torch.tensor([tot_ms, pre_avg, dec_avg], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_ms, pre_avg, dec_avg = (float(v) for v in t.tolist())
+    status_ok = kda.kda_read_device_status(ws) == kda.KDA_OK
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {k: x[k].cpu().pin_memory() for k in ("q", "k", "v", "log_alpha", "beta")}
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h_fin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+        dev_bufs = {k: torch.empty_like(x[k]) for k in host}
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = h_out.numel() * h_out.element_size() + h_fin.numel() * h_fin.element_size()
+
+        def e2e_step():
+            for k2 in host:
+                dev_bufs[k2].copy_(host[k2], non_blocking=True)
+            kda.kda_chunk_fwd(dev_bufs["q"], dev_bufs["k"], dev_bufs["v"], dev_bufs["log_alpha"],
+                              dev_bufs["beta"], x["init_state"], x["cu_seqlens"], out=out,
+                              final_state=fin, workspace=ws)
+            h_out.copy_(out, non_blocking=True)
+            h_fin.copy_(fin, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(1, min(args.steps, 5))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / n_e2e
+        e2e = {"value": world * n_tok / (e2e_ms / 1000.0), "unit": "tokens/s",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        del host, dev_bufs
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        heads, T = calibrated_sample(args.workload, args.cpu_seconds)
+        rate, threads, desc, _ = oracle_rate(args.workload, heads, T)
+        cpu = {"value": rate / H, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": desc}
+
+    if rank != 0:
+        return 0
+    pbytes = prefill_bytes(x, H)
+    pflop = n_tok * H * PREFILL_FLOP_PER_TOKEN_HEAD
+    achieved_gbs = pbytes / (pre_avg / 1000.0) / 1e9
+    dbytes = dw.B * dw.H * DECODE_BYTES_PER_UNIT
+    dec_gbs = dbytes / (dec_avg / 1000.0) / 1e9
+    tokens_per_s = world * n_tok / (pre_avg / 1000.0)
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "note": w.note, "tokens": n_tok, "heads": H,
+                   "decode_workload": "decode_b512_h96: 512 sequences x 96 heads, fp32 state",
+                   "l2": f"inputs {pbytes / 1e9:.1f} GB and decode state "
+                         f"{dbytes / 1e9:.1f} GB exceed the {L2_BYTES >> 20} MiB L2; no flush",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "kda_chunk_fwd_tc_kernel",
+                     "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": peaks["source"], "bytes_per_launch": pbytes,
+                     "ms_per_launch": pre_avg,
+                     "tensor_tflops": pflop / (pre_avg / 1000.0) / 1e12,
+                     "tensor_frac": pflop / (pre_avg / 1000.0) / 1e12 / peaks["bf16_tflops"]},
+        "decode": {"value": dec_gbs, "unit": "GB/s", "ms_per_step": dec_avg,
+                   "tokens_per_s": dw.B / (dec_avg / 1000.0),
+                   "roofline": {"bound": "hbm", "kernel": "kda_decode_step_kernel",
+                                "achieved": dec_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                "frac": dec_gbs / peaks["hbm_gbs"], "traffic": None,
+                                "bytes_per_launch": dbytes}},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(),
+        "device_status_ok": status_ok,
+        "wall_s_timed": t_wall,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default="k3_h96_t32768",
+                    choices=["k3_h96_t32768", "b4_h16_t4096", "varlen_h96_1m"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target duration of the CPU oracle baseline sample")
+    ap.add_argument("--ref-step-s", type=float, default=0.0,
+                    help="target duration of one reference-arm step (default: about 150 s "
+                         "spread over all steps)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
