@@ -65,27 +65,32 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Shared memory map (byte offsets from a 1024-byte aligned base).  Operand
 // tiles use 128-byte rows with the 128-byte swizzle; a "K-major tile of R rows"
 // stores columns 0-63 as R rows of 128 B, then columns 64-127 likewise.
-constexpr uint32_t SM_Q = 0;                  // q chunk (TMA), 64 rows
-constexpr uint32_t SM_K = SM_Q + 16384;       // k chunk (TMA), 64 rows
-constexpr uint32_t SM_V = SM_K + 16384;       // v chunk (TMA), 64 rows
-constexpr uint32_t SM_LA = SM_V + 16384;      // log_alpha fp32 [64][128]; then [Kt; Qt], 128 rows
-constexpr uint32_t SM_VX = SM_LA + 32768;     // factor version buffer X, 128 rows; then fp32 A
-constexpr uint32_t SM_VY = SM_VX + 32768;     // factor version buffer Y, 128 rows; then fp32 T
-constexpr uint32_t SM_KHAT = SM_VY + 32768;   // K o e^{ref_b - g}, 64 rows
-constexpr uint32_t SM_KDEC = SM_KHAT + 16384; // K o e^{g_C - g}, 64 rows
-constexpr uint32_t SM_TMAT = SM_KDEC + 16384; // T' = T Diag(beta), [64 r][64 i]
-constexpr uint32_t SM_PMAT = SM_TMAT + 8192;  // P, [64 r][64 i]
-constexpr uint32_t SM_WMAT = SM_PMAT + 8192;  // -W, stored [128 c][64 r]
-constexpr uint32_t SM_MISC = SM_WMAT + 16384;
+constexpr uint32_t SM_Q = 0;                    // q chunk (TMA), 64 rows
+constexpr uint32_t SM_K = SM_Q + 16384;         // k chunk (TMA), 64 rows
+constexpr uint32_t SM_V = SM_K + 16384;         // v chunk (TMA), 64 rows
+constexpr uint32_t SM_LA = SM_V + 16384;        // log_alpha fp32 [64][128] -> tile prefixes L
+constexpr uint32_t SM_VX = SM_LA + 32768;       // factor versions 0, 2; then A^T fp32; then out staging
+constexpr uint32_t SM_VY = SM_VX + 32768;       // factor versions 1, 3; then T fp32
+constexpr uint32_t SM_STACK = SM_VY + 32768;    // [Kt; Qt] = [K; Q] o e^{g}, 128 rows
+constexpr uint32_t SM_KHAT = SM_STACK + 32768;  // K o e^{ref_b - g}; then T'; then -W
+constexpr uint32_t SM_KDEC = SM_KHAT + 16384;   // K o e^{g_C - g}, 64 rows
+constexpr uint32_t SM_PMAT = SM_KDEC + 16384;   // P, [64 r][64 i]
+constexpr uint32_t SM_MISC = SM_PMAT + 8192;
 
-constexpr int AP = 68;  // pitch (floats) of the fp32 64 x 64 matrices in SM_VX / SM_VY
+constexpr int FP = 72;  // pitch (floats) of the fp32 64 x 64 matrices of the solve
+constexpr int XP = 24;  // pitch (floats) of the 16 x 16 intermediate blocks
+
+// Per-channel factor table rows (fp32, 128 channels each).
+//   0..9 : F[a][b] = 2^{st_a - ref_b} at index a(a+1)/2 + b   (tile starts/ends in log2 units)
+//   10   : 2^{ref_0}      11 : 2^{tot_3}      12 : Gamma_C = 2^{g_C}
+constexpr int TAB_R0 = 10, TAB_T3 = 11, TAB_GAMMA = 12, TAB_ROWS = 13;
 
 struct Misc {
   float beta[C];
-  float gammaC[D];
-  float tot[4][D];
-  uint64_t bar_qk, bar_la, bar_v;                        // TMA arrivals
-  uint64_t bar_vx, bar_vy, bar_gp, bar_wu, bar_m1, bar_m2, bar_fin;  // MMA completions
+  float tot[4][D];            // per-tile total log2-decay
+  float tab[TAB_ROWS][D];
+  uint64_t bar_qk, bar_la, bar_v;                            // TMA arrivals
+  uint64_t bar_v01, bar_gp, bar_wu, bar_m1, bar_m2, bar_fin; // MMA completions
   uint32_t tmem_base;
   int abort;
   uint32_t tma_issued[3], tma_waited[3];  // per TMA barrier: phases issued / consumed
@@ -93,7 +98,8 @@ struct Misc {
 
 constexpr uint32_t SMEM_BYTES = SM_MISC + sizeof(Misc) + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(64 * AP * 4 + 3 * 256 * 4 <= 32768, "fp32 matrices fit a version buffer");
+static_assert(64 * FP * 4 <= 32768, "A^T fits SM_VX");
+static_assert(64 * FP * 4 + 3 * 16 * XP * 4 <= 32768, "T and X blocks fit SM_VY");
 
 // TMEM columns (fp32 cells).
 constexpr uint32_t TM_S = 0;     // S^T, 128 columns
@@ -113,6 +119,19 @@ constexpr uint32_t ID_KM128 = idesc_bf16(128, 128, false, true);
 
 enum { TMA_QK = 0, TMA_LA = 1, TMA_V = 2 };
 
+// Optional per-phase cycle stamps of chain 0 (profiling builds only).
+#ifdef KDA_PHASE_PROFILE
+__device__ long long g_phase_clock[4096 * 16];
+#define PHASE_MARK(i)                                                                    \
+  do {                                                                                   \
+    if (tid == 0 && chain == 0 && ci < 4096) g_phase_clock[ci * 16 + (i)] = clock64();  \
+  } while (0)
+#else
+#define PHASE_MARK(i) \
+  do {                \
+  } while (0)
+#endif
+
 __device__ __forceinline__ void cta_sync() {
   tc_fence_before();
   __syncthreads();
@@ -125,21 +144,6 @@ __device__ void record_status(DeviceStatus *st, int code, int detail, int chain,
     st->chain = chain;
     st->chunk = chunk;
   }
-}
-
-// Byte offset of the bf16 pair (row, c..c+1), c even, in a K-major tile whose
-// 64-column halves hold `rows` rows each.
-__device__ __forceinline__ uint32_t kmaj_off(uint32_t rows, int row, int c) {
-  return (uint32_t)(c >> 6) * rows * 128u + sw128_offset(row, (uint32_t)(c & 63) * 2u);
-}
-
-__device__ __forceinline__ float2 ld_pair(const uint8_t *tile, uint32_t rows, int row, int c) {
-  return unpack_bf16x2(*reinterpret_cast<const uint32_t *>(tile + kmaj_off(rows, row, c)));
-}
-
-__device__ __forceinline__ void st_pair(uint8_t *tile, uint32_t rows, int row, int c, float x,
-                                        float y) {
-  *reinterpret_cast<uint32_t *>(tile + kmaj_off(rows, row, c)) = pack_bf16x2(x, y);
 }
 
 struct Ctx {
@@ -167,6 +171,28 @@ __device__ __forceinline__ uint64_t mndesc(const uint8_t *tile_base, uint32_t by
   return sdesc_sw128(smem_u32(tile_base) + byte_off, lbo, 1024);
 }
 
+// 8 consecutive fp32 from shared memory (16-byte aligned).
+__device__ __forceinline__ void ld8(float (&v)[8], const float *p) {
+  const float4 a = *reinterpret_cast<const float4 *>(p);
+  const float4 b = *reinterpret_cast<const float4 *>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+__device__ __forceinline__ void unpack8(float (&v)[8], uint4 u) {
+  const float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y);
+  const float2 c = unpack_bf16x2(u.z), d = unpack_bf16x2(u.w);
+  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+  v[4] = c.x; v[5] = c.y; v[6] = d.x; v[7] = d.y;
+}
+
+// Stores x[i] * f[i] (i < 8) as 8 bf16 at a shared address.
+__device__ __forceinline__ void st8_scaled(uint32_t saddr, const float (&x)[8],
+                                           const float (&f)[8]) {
+  st_shared_v4(saddr, pack_bf16x2(x[0] * f[0], x[1] * f[1]), pack_bf16x2(x[2] * f[2], x[3] * f[3]),
+               pack_bf16x2(x[4] * f[4], x[5] * f[5]), pack_bf16x2(x[6] * f[6], x[7] * f[7]));
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -184,6 +210,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int chain = blockIdx.x;
   const int seq = chain / H, h = chain % H;
   const Ctx cx{smem, &m, status, chain};
+  const uint32_t sbase_u32 = smem_u32(smem);
 
   const int64_t t0 = cu_seqlens[seq], t1 = cu_seqlens[seq + 1];
   if (t0 < 0 || t1 < t0 || t1 > n_tokens ||
@@ -196,9 +223,8 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   if (tid == 0) {
     mbar_init(&m.bar_qk, 1); mbar_init(&m.bar_la, 1); mbar_init(&m.bar_v, 1);
-    mbar_init(&m.bar_vx, 1); mbar_init(&m.bar_vy, 1); mbar_init(&m.bar_gp, 1);
-    mbar_init(&m.bar_wu, 1); mbar_init(&m.bar_m1, 1); mbar_init(&m.bar_m2, 1);
-    mbar_init(&m.bar_fin, 1);
+    mbar_init(&m.bar_v01, 1); mbar_init(&m.bar_gp, 1); mbar_init(&m.bar_wu, 1);
+    mbar_init(&m.bar_m1, 1); mbar_init(&m.bar_m2, 1); mbar_init(&m.bar_fin, 1);
     fence_mbarrier_init();
     m.abort = 0;
     for (int i = 0; i < 3; ++i) m.tma_issued[i] = m.tma_waited[i] = 0;
@@ -209,10 +235,10 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   }
   cta_sync();
   const uint32_t tm = m.tmem_base;
-  const int q4 = warp & 3, hf = warp >> 2;     // TMEM lane quadrant, column half
+  const int q4 = warp & 3, hf = warp >> 2;  // TMEM lane quadrant, column half
   const uint32_t lane_base = 32u * q4;
 
-  // Issues the TMA loads of chunk `ci` (thread 0 only).
+  // TMA loads of chunk `ci` (thread 0 only).
   auto issue_qk = [&](int ci) {
     const int32_t tb = (int32_t)(t0 + (int64_t)C * ci);
     mbar_arrive_expect_tx(&m.bar_qk, 2 * 16384);
@@ -259,33 +285,37 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   }
   cta_sync();
 
+  // Build-task coordinates: 8-channel group gg of one row per tile.
+  const int gg = tid & 15, rsub = tid >> 4;
+  const int ghalf = gg >> 3, gchunk = gg & 7, gc0 = 8 * gg;
+
   bool failed = false;
   for (int ci = 0; ci < n_chunks && !failed; ++ci) {
     const uint32_t par = (uint32_t)(ci & 1);
     const int64_t tb = t0 + (int64_t)C * ci;
     const int nv = (int)((len - (int64_t)C * ci) < C ? (len - (int64_t)C * ci) : C);
     const bool has_next = ci + 1 < n_chunks;
+    PHASE_MARK(0);
 
-    // ================= phase 1: decay factors and operand tiles (all threads)
+    // ================= phase 1a: per-tile prefix of the log2-decay, in place
     const bool ok_qk = wait_bar(cx, &m.bar_qk, par, 10, ci);
     const bool ok_la = wait_bar(cx, &m.bar_la, par, 11, ci);
-    const int a = tid >> 6, cp = tid & 63, c = 2 * cp;
-    float L0[16], L1[16];
-    if (ok_qk && ok_la) {
-      const float *la = reinterpret_cast<const float *>(smem + SM_LA);
-      float s0 = 0.f, s1 = 0.f;
+    {
+      float *la = reinterpret_cast<float *>(smem + SM_LA);
+      const int c = tid & 127, hh = tid >> 7;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int row = 16 * a + j;
-        float2 x = *reinterpret_cast<const float2 *>(la + row * D + c);
-        if (row >= nv) x = make_float2(0.f, 0.f);
-        s0 = fmaf(x.x, kLog2e, s0);
-        s1 = fmaf(x.y, kLog2e, s1);
-        L0[j] = s0;
-        L1[j] = s1;
+      for (int t2 = 0; t2 < 2; ++t2) {
+        const int a = 2 * hh + t2;
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int r = 16 * a + j;
+          const float x = r < nv ? la[r * D + c] : 0.f;
+          acc = fmaf(x, kLog2e, acc);
+          la[r * D + c] = acc;
+        }
+        m.tot[a][c] = acc;
       }
-      m.tot[a][c] = s0;
-      m.tot[a][c + 1] = s1;
     }
     if (tid < C) m.beta[tid] = tid < nv ? beta[(tb + tid) * H + h] : 0.f;
     if (tid == 0) {
@@ -293,99 +323,158 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (ok_la) m.tma_waited[TMA_LA]++;
     }
     cta_sync();
+    PHASE_MARK(1);
     if (m.abort) { failed = true; break; }
 
-    // Tile starts st[b] and ends rf[b] of the cumulative log2-decay, channels c, c+1.
-    float st0[4], st1[4], rf0[4], rf1[4];
-    {
-      float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        st0[b] = acc0; st1[b] = acc1;
-        acc0 += m.tot[b][c]; acc1 += m.tot[b][c + 1];
-        rf0[b] = acc0; rf1[b] = acc1;
-      }
+    // ================= phase 1b: per-channel factor table
+    if (tid < D) {
+      const int c = tid;
+      const float x0 = m.tot[0][c], x1 = m.tot[1][c], x2 = m.tot[2][c], x3 = m.tot[3][c];
+      const float st1 = x0, st2 = x0 + x1, st3 = x0 + x1 + x2;  // tile starts (st0 = 0)
+      const float rf0 = x0, rf1 = st2, rf2 = st3, rf3 = st3 + x3;  // tile ends
+      m.tab[0][c] = ex2(-rf0);
+      m.tab[1][c] = ex2(st1 - rf0);
+      m.tab[2][c] = ex2(st1 - rf1);
+      m.tab[3][c] = ex2(st2 - rf0);
+      m.tab[4][c] = ex2(st2 - rf1);
+      m.tab[5][c] = ex2(st2 - rf2);
+      m.tab[6][c] = ex2(st3 - rf0);
+      m.tab[7][c] = ex2(st3 - rf1);
+      m.tab[8][c] = ex2(st3 - rf2);
+      m.tab[9][c] = ex2(st3 - rf3);
+      m.tab[TAB_R0][c] = ex2(rf0);
+      m.tab[TAB_T3][c] = ex2(x3);
+      m.tab[TAB_GAMMA][c] = ex2(rf3);
     }
-    const float sa0 = a == 0 ? st0[0] : a == 1 ? st0[1] : a == 2 ? st0[2] : st0[3];
-    const float sa1 = a == 0 ? st1[0] : a == 1 ? st1[1] : a == 2 ? st1[2] : st1[3];
-    const float ra0 = a == 0 ? rf0[0] : a == 1 ? rf0[1] : a == 2 ? rf0[2] : rf0[3];
-    const float ra1 = a == 0 ? rf1[0] : a == 1 ? rf1[1] : a == 2 ? rf1[2] : rf1[3];
-    const float gC0 = rf0[3], gC1 = rf1[3];
-    const float tot0 = ra0 - sa0, tot1 = ra1 - sa1;
+    __syncthreads();
 
-    // E_r = 2^{L_r} (row side, relative to the tile start); Ec_r = 2^{tot - L_r}.
-    float E0[16], E1[16];
+    // ================= phase 1c: operand tiles, versions 0 and 1
+    // Task: row r = 16a + rsub, channels gc0..gc0+7.  E = 2^{L} (row factor from
+    // the tile start), Ec = 2^{tot_a - L} (column factor to the tile end).
     {
-      uint8_t *khat = smem + SM_KHAT, *kdec = smem + SM_KDEC, *stack = smem + SM_LA;
-      const float fd0 = ex2(gC0 - ra0), fd1 = ex2(gC1 - ra1);   // e^{g_C - ref_a}
-      const float fs0 = ex2(sa0), fs1 = ex2(sa1);               // e^{start_a}
+      const float *L = reinterpret_cast<const float *>(smem + SM_LA);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int row = 16 * a + j;
-        E0[j] = ex2(L0[j]);
-        E1[j] = ex2(L1[j]);
-        const float ec0 = ex2(tot0 - L0[j]), ec1 = ex2(tot1 - L1[j]);
-        const float2 kk = ld_pair(smem + SM_K, 64, row, c);
-        const float2 qq = ld_pair(smem + SM_Q, 64, row, c);
-        st_pair(khat, 64, row, c, kk.x * ec0, kk.y * ec1);
-        st_pair(kdec, 64, row, c, kk.x * (ec0 * fd0), kk.y * (ec1 * fd1));
-        const float e0 = E0[j] * fs0, e1 = E1[j] * fs1;          // e^{g_r}
-        st_pair(stack, 128, row, c, kk.x * e0, kk.y * e1);
-        st_pair(stack, 128, 64 + row, c, qq.x * e0, qq.y * e1);
+      for (int a = 0; a < 4; ++a) {
+        const int r = 16 * a + rsub;
+        const uint32_t swz = (uint32_t)((gchunk ^ (r & 7)) << 4);
+        const uint32_t o64 = ghalf * 8192u + r * 128u + swz;           // 64-row tiles
+        const uint32_t o128 = ghalf * 16384u + r * 128u + swz;         // 128-row tiles, row r
+        const uint32_t o128q = o128 + 64u * 128u;                       // row 64 + r
+        float Lv[8], tv[8], kf[8], qf[8];
+        ld8(Lv, L + r * D + gc0);
+        ld8(tv, &m.tot[a][gc0]);
+        unpack8(kf, ld_shared_v4(sbase_u32 + SM_K + o64));
+        unpack8(qf, ld_shared_v4(sbase_u32 + SM_Q + o64));
+        float E[8], Ec[8], ke[8], qe[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          E[i] = ex2(Lv[i]);
+          Ec[i] = ex2(tv[i] - Lv[i]);
+          ke[i] = kf[i] * E[i];
+          qe[i] = qf[i] * E[i];
+        }
+        st8_scaled(sbase_u32 + SM_KHAT + o64, kf, Ec);
+        {
+          float f[8];   // e^{g_C - ref_a} Ec
+          if (a == 3) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[i] = Ec[i];
+          } else {
+            float t3[8], fa[8];
+            ld8(t3, &m.tab[TAB_T3][gc0]);
+            ld8(fa, &m.tab[6 + a][gc0]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[i] = Ec[i] * (t3[i] * fa[i]);
+          }
+          st8_scaled(sbase_u32 + SM_KDEC + o64, kf, f);
+        }
+        {
+          float f0[8], r0[8], fs[8];   // version-0 factor and e^{st_a} = F[a][0] 2^{ref_0}
+          ld8(f0, &m.tab[a * (a + 1) / 2][gc0]);
+          ld8(r0, &m.tab[TAB_R0][gc0]);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) fs[i] = f0[i] * r0[i];
+          st8_scaled(sbase_u32 + SM_STACK + o128, ke, fs);
+          st8_scaled(sbase_u32 + SM_STACK + o128q, qe, fs);
+          st8_scaled(sbase_u32 + SM_VX + o128, ke, f0);
+          st8_scaled(sbase_u32 + SM_VX + o128q, qe, f0);
+        }
+        if (a >= 1) {
+          float f1[8];
+          ld8(f1, &m.tab[a * (a + 1) / 2 + 1][gc0]);
+          st8_scaled(sbase_u32 + SM_VY + o128, ke, f1);
+          st8_scaled(sbase_u32 + SM_VY + o128q, qe, f1);
+        }
       }
-      if (a == 0) { m.gammaC[c] = ex2(gC0); m.gammaC[c + 1] = ex2(gC1); }
     }
-    // Factor version b: rows of tiles a >= b scaled by e^{g_r - ref_b}.
-    auto build_version = [&](uint8_t *buf, int b) {
-      const float rb0 = b == 0 ? rf0[0] : b == 1 ? rf0[1] : b == 2 ? rf0[2] : rf0[3];
-      const float rb1 = b == 0 ? rf1[0] : b == 1 ? rf1[1] : b == 2 ? rf1[2] : rf1[3];
-      const float f0 = ex2(sa0 - rb0), f1 = ex2(sa1 - rb1);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int row = 16 * a + j;
-        const float2 kk = ld_pair(smem + SM_K, 64, row, c);
-        const float2 qq = ld_pair(smem + SM_Q, 64, row, c);
-        const float e0 = E0[j] * f0, e1 = E1[j] * f1;
-        st_pair(buf, 128, row, c, kk.x * e0, kk.y * e1);
-        st_pair(buf, 128, 64 + row, c, qq.x * e0, qq.y * e1);
-      }
-    };
-    auto issue_gp = [&](const uint8_t *buf, int b) {
+    fence_proxy_async_smem();
+    cta_sync();
+    PHASE_MARK(2);
+
+    auto issue_gp = [&](uint32_t buf, int b) {
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        const uint64_t ad = kdesc(buf, (ks >> 2) * 16384u + (ks & 3) * 32u);
+        const uint64_t ad = kdesc(smem + buf, (ks >> 2) * 16384u + (ks & 3) * 32u);
         const uint64_t bd = kdesc(smem + SM_KHAT, (ks >> 2) * 8192u + 2048u * b + (ks & 3) * 32u);
         umma_ss(tm + TM_GP + 16 * b, ad, bd, ID_GP, ks > 0 ? 1u : 0u);
       }
     };
-    build_version(smem + SM_VX, 0);
-    fence_proxy_async_smem();
-    cta_sync();
-    if (tid == 0) { issue_gp(smem + SM_VX, 0); umma_commit(&m.bar_vx); }
-    if (a >= 1) build_version(smem + SM_VY, 1);
-    fence_proxy_async_smem();
-    cta_sync();
-    if (tid == 0) { issue_gp(smem + SM_VY, 1); umma_commit(&m.bar_vy); }
-    wait_bar(cx, &m.bar_vx, par, 20, ci);
-    if (a >= 2) build_version(smem + SM_VX, 2);
-    fence_proxy_async_smem();
-    cta_sync();
-    if (m.abort) { failed = true; break; }
-    if (tid == 0) issue_gp(smem + SM_VX, 2);
-    wait_bar(cx, &m.bar_vy, par, 21, ci);
-    if (a >= 3) build_version(smem + SM_VY, 3);
-    fence_proxy_async_smem();
-    cta_sync();
-    if (m.abort) { failed = true; break; }
     if (tid == 0) {
-      issue_gp(smem + SM_VY, 3);
-      umma_commit(&m.bar_gp);
-      if (has_next) issue_qk(ci + 1);   // q, k tiles are no longer read
+      issue_gp(SM_VX, 0);
+      issue_gp(SM_VY, 1);
+      umma_commit(&m.bar_v01);
     }
 
-    // ================= phase 2: A (fp32, for the solve) and P (bf16 operand)
+    // ================= phase 1d: versions 2 and 3 (rows of tiles 2, 3)
+    wait_bar(cx, &m.bar_v01, par, 20, ci);
+    {
+      const float *L = reinterpret_cast<const float *>(smem + SM_LA);
+#pragma unroll
+      for (int t2 = 0; t2 < 2; ++t2) {
+        const int a = 2 + t2;
+        const int r = 16 * a + rsub;
+        const uint32_t swz = (uint32_t)((gchunk ^ (r & 7)) << 4);
+        const uint32_t o64 = ghalf * 8192u + r * 128u + swz;
+        const uint32_t o128 = ghalf * 16384u + r * 128u + swz;
+        const uint32_t o128q = o128 + 64u * 128u;
+        float Lv[8], kf[8], qf[8];
+        ld8(Lv, L + r * D + gc0);
+        unpack8(kf, ld_shared_v4(sbase_u32 + SM_K + o64));
+        unpack8(qf, ld_shared_v4(sbase_u32 + SM_Q + o64));
+        float ke[8], qe[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float e = ex2(Lv[i]);
+          ke[i] = kf[i] * e;
+          qe[i] = qf[i] * e;
+        }
+        float f2[8];
+        ld8(f2, &m.tab[a * (a + 1) / 2 + 2][gc0]);
+        st8_scaled(sbase_u32 + SM_VX + o128, ke, f2);
+        st8_scaled(sbase_u32 + SM_VX + o128q, qe, f2);
+        if (a == 3) {
+          float f3[8];
+          ld8(f3, &m.tab[9][gc0]);
+          st8_scaled(sbase_u32 + SM_VY + o128, ke, f3);
+          st8_scaled(sbase_u32 + SM_VY + o128q, qe, f3);
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    cta_sync();
+    PHASE_MARK(3);
+    if (m.abort) { failed = true; break; }
+    if (tid == 0) {
+      issue_gp(SM_VX, 2);
+      issue_gp(SM_VY, 3);
+      umma_commit(&m.bar_gp);
+      if (has_next) { issue_qk(ci + 1); issue_la(ci + 1); }  // q, k, L no longer read
+    }
+
+    // ================= phase 2: A^T (fp32, for the solve) and P (bf16 operand)
     wait_bar(cx, &m.bar_gp, par, 22, ci);
     tc_fence_after();
+    PHASE_MARK(4);
     {
       uint32_t r[32];
       tmem_ld32(tmem_addr(tm, lane_base, TM_GP + 32 * hf), r);
@@ -393,11 +482,11 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (q4 < 2) {
         const int row = 32 * q4 + lane;
         const float br = m.beta[row];
-        float *amat = reinterpret_cast<float *>(smem + SM_VX);
+        float *amatT = reinterpret_cast<float *>(smem + SM_VX);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int i = 32 * hf + j;
-          amat[row * AP + i] = i < row ? br * __uint_as_float(r[j]) : 0.f;
+          amatT[i * FP + row] = i < row ? br * __uint_as_float(r[j]) : 0.f;
         }
       } else {
         const int row = 32 * (q4 - 2) + lane;
@@ -411,76 +500,110 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             const float hi = i + 1 <= row ? __uint_as_float(r[j + 1]) : 0.f;
             w[t] = pack_bf16x2(lo, hi);
           }
-          st_shared_v4(smem_u32(smem + SM_PMAT) + sw128_offset(row, (32 * hf + 8 * g) * 2),
-                       w[0], w[1], w[2], w[3]);
+          st_shared_v4(sbase_u32 + SM_PMAT + sw128_offset(row, (32 * hf + 8 * g) * 2), w[0],
+                       w[1], w[2], w[3]);
         }
       }
     }
     cta_sync();
+    PHASE_MARK(5);
     if (m.abort) { failed = true; break; }
 
     // ================= phase 3: T = (I + A)^{-1}, blocked by 16 x 16 tiles
     {
-      const float *amat = reinterpret_cast<const float *>(smem + SM_VX);
-      float *tinv = reinterpret_cast<float *>(smem + SM_VY);
-      float *xb = tinv + 64 * AP;
-      if (warp < 4 && lane < 16) {  // diagonal blocks by forward substitution
-        const int a0 = 16 * warp, j = lane;
-        float tcol[16];
+      const float *amatT = reinterpret_cast<const float *>(smem + SM_VX);  // A^T, [i][r]
+      float *tinv = reinterpret_cast<float *>(smem + SM_VY);               // T, [r][i]
+      float *xbuf = tinv + 64 * FP;
+      if (warp < 2) {
+        // Diagonal blocks by column-oriented forward substitution: lane owns
+        // column j of block a; after step m, t[m] is final and is eliminated
+        // from every later row.
+        const int a = 2 * warp + (lane >> 4), j = lane & 15, b0 = 16 * a;
+        float t[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          float acc = 0.f;
+        for (int r = 0; r < 16; ++r) t[r] = (r == j) ? 1.f : 0.f;
 #pragma unroll
-          for (int mm = 0; mm < r; ++mm) acc = fmaf(amat[(a0 + r) * AP + a0 + mm], tcol[mm], acc);
-          tcol[r] = (j == r) ? 1.f : ((j < r) ? -acc : 0.f);
+        for (int mc = 0; mc < 15; ++mc) {
+          float col[16];
+          ld8(*reinterpret_cast<float(*)[8]>(col), amatT + (b0 + mc) * FP + b0);
+          ld8(*reinterpret_cast<float(*)[8]>(col + 8), amatT + (b0 + mc) * FP + b0 + 8);
+          const float tm = t[mc];
+#pragma unroll
+          for (int r = mc + 1; r < 16; ++r) t[r] = fmaf(-col[r], tm, t[r]);
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) tinv[(a0 + r) * AP + a0 + j] = tcol[r];
+        for (int r = 0; r < 16; ++r) tinv[(b0 + r) * FP + b0 + j] = t[r];
       }
       __syncthreads();
-      // Off-diagonal blocks by distance d = a - b:
-      //   T_ab = -T_aa * sum_{m=b}^{a-1} A_am T_mb
+      PHASE_MARK(6);
+      // Off-diagonal blocks by distance d = a - b, one warp per block, TF32 MMA:
+      //   X = sum_{m=b}^{a-1} A_am T_mb,  T_ab = -T_aa X
+      const int g = lane >> 2, t4 = lane & 3;
 #pragma unroll 1
       for (int d = 1; d < 4; ++d) {
-        const int nblk = 4 - d;
-        for (int e = tid; e < nblk * 256; e += kThreads) {
-          const int blk = e >> 8, r = (e >> 4) & 15, jj = e & 15;
-          const int ab = d + blk, bb = blk;
-          float acc = 0.f;
-          for (int mm = bb; mm < ab; ++mm)
+        if (warp < 4 - d) {
+          const int bb = warp, ab = warp + d;
+          float x0[4] = {0.f, 0.f, 0.f, 0.f}, x1[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int mm = bb; mm < ab; ++mm) {
 #pragma unroll
-            for (int l = 0; l < 16; ++l)
-              acc = fmaf(amat[(16 * ab + r) * AP + 16 * mm + l],
-                         tinv[(16 * mm + l) * AP + 16 * bb + jj], acc);
-          xb[blk * 256 + r * 16 + jj] = acc;
-        }
-        __syncthreads();
-        for (int e = tid; e < nblk * 256; e += kThreads) {
-          const int blk = e >> 8, r = (e >> 4) & 15, jj = e & 15;
-          const int ab = d + blk, bb = blk;
-          float acc = 0.f;
+            for (int kk = 0; kk < 2; ++kk) {
+              const int kc = 16 * mm + 8 * kk;   // k index base
+              const uint32_t a0 = to_tf32(amatT[(kc + t4) * FP + 16 * ab + g]);
+              const uint32_t a1 = to_tf32(amatT[(kc + t4) * FP + 16 * ab + g + 8]);
+              const uint32_t a2 = to_tf32(amatT[(kc + t4 + 4) * FP + 16 * ab + g]);
+              const uint32_t a3 = to_tf32(amatT[(kc + t4 + 4) * FP + 16 * ab + g + 8]);
+              const float *tb0 = tinv + (kc + t4) * FP + 16 * bb + g;
+              const float *tb1 = tinv + (kc + t4 + 4) * FP + 16 * bb + g;
+              mma_tf32_16x8x8(x0, a0, a1, a2, a3, to_tf32(tb0[0]), to_tf32(tb1[0]));
+              mma_tf32_16x8x8(x1, a0, a1, a2, a3, to_tf32(tb0[8]), to_tf32(tb1[8]));
+            }
+          }
+          float *xb = xbuf + warp * 16 * XP;
+          xb[g * XP + 2 * t4] = x0[0];       xb[g * XP + 2 * t4 + 1] = x0[1];
+          xb[(g + 8) * XP + 2 * t4] = x0[2]; xb[(g + 8) * XP + 2 * t4 + 1] = x0[3];
+          xb[g * XP + 8 + 2 * t4] = x1[0];       xb[g * XP + 8 + 2 * t4 + 1] = x1[1];
+          xb[(g + 8) * XP + 8 + 2 * t4] = x1[2]; xb[(g + 8) * XP + 8 + 2 * t4 + 1] = x1[3];
+          __syncwarp();
+          float o0[4] = {0.f, 0.f, 0.f, 0.f}, o1[4] = {0.f, 0.f, 0.f, 0.f};
+          const float *taa = tinv + (16 * ab) * FP + 16 * ab;
 #pragma unroll
-          for (int l = 0; l < 16; ++l)
-            acc = fmaf(tinv[(16 * ab + r) * AP + 16 * ab + l], xb[blk * 256 + l * 16 + jj], acc);
-          tinv[(16 * ab + r) * AP + 16 * bb + jj] = -acc;
+          for (int kk = 0; kk < 2; ++kk) {
+            const uint32_t a0 = to_tf32(taa[g * FP + 8 * kk + t4]);
+            const uint32_t a1 = to_tf32(taa[(g + 8) * FP + 8 * kk + t4]);
+            const uint32_t a2 = to_tf32(taa[g * FP + 8 * kk + t4 + 4]);
+            const uint32_t a3 = to_tf32(taa[(g + 8) * FP + 8 * kk + t4 + 4]);
+            const float *xr0 = xb + (8 * kk + t4) * XP + g;
+            const float *xr1 = xb + (8 * kk + t4 + 4) * XP + g;
+            mma_tf32_16x8x8(o0, a0, a1, a2, a3, to_tf32(xr0[0]), to_tf32(xr1[0]));
+            mma_tf32_16x8x8(o1, a0, a1, a2, a3, to_tf32(xr0[8]), to_tf32(xr1[8]));
+          }
+          float *tab_ = tinv + (16 * ab) * FP + 16 * bb;
+          tab_[g * FP + 2 * t4] = -o0[0];       tab_[g * FP + 2 * t4 + 1] = -o0[1];
+          tab_[(g + 8) * FP + 2 * t4] = -o0[2]; tab_[(g + 8) * FP + 2 * t4 + 1] = -o0[3];
+          tab_[g * FP + 8 + 2 * t4] = -o1[0];       tab_[g * FP + 8 + 2 * t4 + 1] = -o1[1];
+          tab_[(g + 8) * FP + 8 + 2 * t4] = -o1[2]; tab_[(g + 8) * FP + 8 + 2 * t4 + 1] = -o1[3];
         }
         __syncthreads();
       }
-      // T' = T Diag(beta) -> bf16, K-major [r][i]; upper triangle zero.
+      PHASE_MARK(7);
+      // T' = T Diag(beta) -> bf16, K-major [r][i] (in the KHAT region); upper triangle zero.
       {
         const int row = tid >> 2, qd = tid & 3;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int hh = 0; hh < 2; ++hh) {
+          const int i0 = 16 * qd + 8 * hh;
+          float tv[8], bv[8];
+          ld8(tv, tinv + row * FP + i0);
+          ld8(bv, &m.beta[i0]);
           uint32_t w[4];
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
-            const int i0 = 16 * qd + 8 * half + 2 * t;
-            const float lo = i0 <= row ? tinv[row * AP + i0] * m.beta[i0] : 0.f;
-            const float hi = i0 + 1 <= row ? tinv[row * AP + i0 + 1] * m.beta[i0 + 1] : 0.f;
+            const int i = i0 + 2 * t;
+            const float lo = i <= row ? tv[2 * t] * bv[2 * t] : 0.f;
+            const float hi = i + 1 <= row ? tv[2 * t + 1] * bv[2 * t + 1] : 0.f;
             w[t] = pack_bf16x2(lo, hi);
           }
-          st_shared_v4(smem_u32(smem + SM_TMAT) + sw128_offset(row, (16 * qd + 8 * half) * 2),
-                       w[0], w[1], w[2], w[3]);
+          st_shared_v4(sbase_u32 + SM_KHAT + sw128_offset(row, i0 * 2), w[0], w[1], w[2], w[3]);
         }
       }
       fence_proxy_async_smem();
@@ -496,11 +619,17 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         tmem_ld_wait(s);
         uint32_t ab[16];
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          const float f0 = __uint_as_float(s[2 * jj]), f1 = __uint_as_float(s[2 * jj + 1]);
-          ab[jj] = pack_bf16x2(f0, f1);
-          s[2 * jj] = __float_as_uint(f0 * m.gammaC[c0 + 2 * jj]);
-          s[2 * jj + 1] = __float_as_uint(f1 * m.gammaC[c0 + 2 * jj + 1]);
+        for (int q8 = 0; q8 < 4; ++q8) {
+          float gv[8];
+          ld8(gv, &m.tab[TAB_GAMMA][c0 + 8 * q8]);
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int j = 8 * q8 + 2 * jj;
+            const float f0 = __uint_as_float(s[j]), f1 = __uint_as_float(s[j + 1]);
+            ab[4 * q8 + jj] = pack_bf16x2(f0, f1);
+            s[j] = __float_as_uint(f0 * gv[2 * jj]);
+            s[j + 1] = __float_as_uint(f1 * gv[2 * jj + 1]);
+          }
         }
         tmem_st32(tmem_addr(tm, lane_base, TM_S + c0), s);
         tmem_st16(tmem_addr(tm, lane_base, TM_AS + c0 / 2), ab);
@@ -508,29 +637,32 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       tmem_st_wait();
     }
     cta_sync();
+    PHASE_MARK(8);
     if (tid == 0) {
       if (wait_bar(cx, &m.bar_v, par, 12, ci)) {
         m.tma_waited[TMA_V]++;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {   // U^T = V^T T'^T ; W^T = Kt^T T'^T
-          const uint64_t bd = kdesc(smem + SM_TMAT, ks * 32u);
+          const uint64_t bd = kdesc(smem + SM_KHAT, ks * 32u);
           umma_ss(tm + TM_U, mndesc(smem + SM_V, ks * 2048u, 8192), bd, ID_UW, ks > 0);
-          umma_ss(tm + TM_W, mndesc(smem + SM_LA, ks * 2048u, 16384), bd, ID_UW, ks > 0);
+          umma_ss(tm + TM_W, mndesc(smem + SM_STACK, ks * 2048u, 16384), bd, ID_UW, ks > 0);
         }
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {   // O^T = S^T Qt^T
-          const uint64_t bd = kdesc(smem + SM_LA, 64u * 128u + (ks >> 2) * 16384u + (ks & 3) * 32u);
+          const uint64_t bd =
+              kdesc(smem + SM_STACK, 64u * 128u + (ks >> 2) * 16384u + (ks & 3) * 32u);
           umma_ts(tm + TM_O, tm + TM_AS + 8 * ks, bd, ID_KK64, ks > 0);
         }
         umma_commit(&m.bar_wu);
       }
     }
 
-    // ================= phase 5: -W -> smem; Delta^T = U^T - S^T W^T
+    // ================= phase 5: -W -> smem (KHAT region); Delta^T = U^T - S^T W^T
     wait_bar(cx, &m.bar_wu, par, 23, ci);
     tc_fence_after();
-    if (tid == 0 && has_next) { issue_v(ci + 1); issue_la(ci + 1); }
+    PHASE_MARK(9);
+    if (tid == 0 && has_next) issue_v(ci + 1);
     {
       uint32_t r[32];
       tmem_ld32(tmem_addr(tm, lane_base, TM_W + 32 * hf), r);
@@ -541,24 +673,28 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         uint32_t w[4];
 #pragma unroll
         for (int t = 0; t < 4; ++t)
-          w[t] = pack_bf16x2(-__uint_as_float(r[8 * g + 2 * t]), -__uint_as_float(r[8 * g + 2 * t + 1]));
-        st_shared_v4(smem_u32(smem + SM_WMAT) + sw128_offset(crow, (32 * hf + 8 * g) * 2), w[0],
-                     w[1], w[2], w[3]);
+          w[t] = pack_bf16x2(-__uint_as_float(r[8 * g + 2 * t]),
+                             -__uint_as_float(r[8 * g + 2 * t + 1]));
+        st_shared_v4(sbase_u32 + SM_KHAT + sw128_offset(crow, (32 * hf + 8 * g) * 2), w[0], w[1],
+                     w[2], w[3]);
       }
       fence_proxy_async_smem();
     }
     cta_sync();
+    PHASE_MARK(10);
     if (m.abort) { failed = true; break; }
     if (tid == 0) {
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        umma_ts(tm + TM_U, tm + TM_AS + 8 * ks, mndesc(smem + SM_WMAT, ks * 2048u, 8192), ID_KM64, 1u);
+        umma_ts(tm + TM_U, tm + TM_AS + 8 * ks, mndesc(smem + SM_KHAT, ks * 2048u, 8192),
+                ID_KM64, 1u);
       umma_commit(&m.bar_m1);
     }
 
     // ================= phase 6: bf16 Delta^T; O^T += Delta^T P^T; S^T += Delta^T Kdec
     wait_bar(cx, &m.bar_m1, par, 24, ci);
     tc_fence_after();
+    PHASE_MARK(11);
     {
       uint32_t r[32];
       tmem_ld32(tmem_addr(tm, lane_base, TM_U + 32 * hf), r);
@@ -571,6 +707,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       tmem_st_wait();
     }
     cta_sync();
+    PHASE_MARK(12);
     if (m.abort) { failed = true; break; }
     if (tid == 0) {
 #pragma unroll
@@ -582,20 +719,35 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       umma_commit(&m.bar_m2);
     }
 
-    // ================= phase 7: output rows of this chunk
+    // ================= phase 7: output rows of this chunk, staged through SM_VX
     wait_bar(cx, &m.bar_m2, par, 25, ci);
     tc_fence_after();
+    PHASE_MARK(13);
     {
       uint32_t r[32];
       tmem_ld32(tmem_addr(tm, lane_base, TM_O + 32 * hf), r);
       tmem_ld_wait(r);
+      __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(smem + SM_VX);
       const int n = lane_base + lane;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int rr = 32 * hf + j;
-        if (rr < nv) out[((tb + rr) * H + h) * D + n] = __float2bfloat16_rn(__uint_as_float(r[j]));
+      for (int j = 0; j < 32; ++j)
+        stg[(32 * hf + j) * D + n] = __float2bfloat16_rn(__uint_as_float(r[j]));
+    }
+    __syncthreads();
+    {
+      const uint4 *stg = reinterpret_cast<const uint4 *>(smem + SM_VX);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int e = tid + kThreads * j;   // 16-byte chunk: row e / 16, column chunk e % 16
+        const int rr = e >> 4;
+        if (rr < nv) {
+          uint4 *dst = reinterpret_cast<uint4 *>(out + ((tb + rr) * H + h) * D) + (e & 15);
+          *dst = stg[e];
+        }
       }
     }
+    PHASE_MARK(14);
+    __syncthreads();
   }
 
   cta_sync();
@@ -609,7 +761,8 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         tmem_ld32(tmem_addr(tm, lane_base, TM_S + c0), r);
         tmem_ld_wait(r);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) final_state[sbase + (int64_t)(c0 + j) * D + n] = __uint_as_float(r[j]);
+        for (int j = 0; j < 32; ++j)
+          final_state[sbase + (int64_t)(c0 + j) * D + n] = __uint_as_float(r[j]);
       }
     }
   } else if (tid == 0) {
@@ -654,6 +807,12 @@ bool make_map(CUtensorMap *map, const void *base, CUtensorMapDataType dt, uint32
 }
 
 }  // namespace
+
+#ifdef KDA_PHASE_PROFILE
+extern "C" int kda_debug_phase_clock(long long *host, int n) {
+  return cudaMemcpyFromSymbol(host, g_phase_clock, sizeof(long long) * n) == cudaSuccess ? 0 : 4;
+}
+#endif
 
 cudaError_t launch_chunk_fwd_bf16_tc(const ChunkArgs &a, cudaStream_t stream) {
   const int64_t chains = (int64_t)a.n_seqs * a.H;
