@@ -15,35 +15,35 @@
 //   Delta = U - W S,  O = (Q o e^{g}) S + P Delta,  P = lower_incl([q_r . k_i e^{g_r - g_i}])
 //   S <- Diag(e^{g_C}) S + (K o e^{g_C - g})^T Delta
 //
-// Decay factorisation on tensor cores.  The ratio e^{g_r - g_i} is split as
-// e^{g_r - R} e^{R - g_i} with one reference R per 16-token column tile b: R =
-// ref_b = cumulative log-decay at the end of tile b.  Because log_alpha >= -5,
-// a 16-token tile spans at most 80 in log-decay, so for i in tile b
-// e^{ref_b - g_i} is in [e^-80, 1] and for rows r of tile b e^{g_r - ref_b} is
-// in [1, e^80]; rows of later tiles give factors <= 1 ("Kimi K3: 架构、训练与系统
-// 全景解析", section 4.2.5: a 16-token tile's cumulative log-decay lies in
-// (-80, 0), its reciprocal within e^80, so diagonal and off-diagonal tiles both
-// run as dense tensor-core matmuls).  Every factor is representable in bf16 and
-// fp32, and a factor only underflows where the exact product is below e^-87.
-// Row factors are built from E_r = e^{g_r - start(tile(r))} (in [e^-80, 1]) times
-// one per-(tile, channel) constant, so each element costs two exponentials.
+// Decay factorisation on tensor cores.  With 16-token tiles a, b and per-channel
+// tile starts st_a / ends ref_b of the cumulative log-decay,
+//   e^{g_r - g_i} = e^{g_r - st_a} * e^{st_a - ref_b} * e^{ref_b - g_i}
+// for row r in tile a >= b and column i in tile b.  Because log_alpha >= -5 a
+// tile spans at most 80 in log-decay ("Kimi K3: 架构、训练与系统全景解析",
+// section 4.2.5: the cumulative log-decay of a 16-token tile lies in (-80, 0)
+// and its reciprocal within e^80, so diagonal and off-diagonal tiles both run
+// as dense tensor-core matmuls): the row factor is in [e^-80, 1], the column
+// factor e^{st_a - g_i} = e^{st_a - ref_b} e^{ref_b - g_i} is at most e^80 (a = b)
+// or 1 (a > b), and a factor underflows only where the exact product is below
+// e^-87.  So one row operand [K o E; Q o E] (E_r = e^{g_r - st_a}) serves every
+// block, and the column operand holds one 16-row block per tile pair (a, b),
+// a >= b: the Gram and P matrices of a chunk are 8 MMAs of M = 128 (64 key
+// rows, 64 query rows), N = 160 (10 blocks), K = 16 each.
 //
 // TMEM orientation: the state is held transposed (S^T: lane = value index n,
-// column = key index c), so every state-side product is an M = 128 MMA with
-// the bf16 copy of S^T (or Delta^T) as a TMEM A operand:
-//   U^T  = V^T T'^T           (A = V, smem MN-major;  B = T', K-major)
-//   W^T  = Kt^T T'^T          (A = Kt, smem MN-major)
-//   O^T  = S^T Qt^T           (A = bf16 S^T in TMEM;  B = Qt, K-major)
-//   D^T  = U^T - S^T W^T      (accumulate, B = -W, MN-major)
-//   O^T += Delta^T P^T        (A = bf16 Delta^T in TMEM; B = P, K-major)
-//   S^T += Delta^T Kdec       (B = Kdec, MN-major), after S^T <- S^T Diag(e^{g_C})
-// The Gram and P matrices are 4 MMAs of M = 128 (rows: 64 key rows then 64
-// query rows of one factor version), N = 16 (one column tile), K = 128.
+// column = key index c), so every state-side product is an M = 128 MMA:
+//   U^T  = V^T T'^T                 (A = V, smem MN-major;  B = T', K-major)
+//   W^T  = Kt^T T'^T                (A = Kt, smem MN-major)
+//   [O^T | D^T] = S^T [Qt; -W]^T    (A = bf16 S^T in TMEM; D^T accumulates onto U^T)
+//   [S^T | O^T] += Delta^T [Kdec | P_mn]   (A = bf16 Delta^T in TMEM; B MN-major),
+//                                    after S^T <- S^T Diag(e^{g_C})
+// where D = Delta = U - W S.  28 tcgen05.mma instructions per chunk.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include <mutex>
 
@@ -69,28 +69,31 @@ constexpr uint32_t SM_Q = 0;                    // q chunk (TMA), 64 rows
 constexpr uint32_t SM_K = SM_Q + 16384;         // k chunk (TMA), 64 rows
 constexpr uint32_t SM_V = SM_K + 16384;         // v chunk (TMA), 64 rows
 constexpr uint32_t SM_LA = SM_V + 16384;        // log_alpha fp32 [64][128] -> tile prefixes L
-constexpr uint32_t SM_VX = SM_LA + 32768;       // factor versions 0, 2; then A^T fp32; then out staging
-constexpr uint32_t SM_VY = SM_VX + 32768;       // factor versions 1, 3; then T fp32
-constexpr uint32_t SM_STACK = SM_VY + 32768;    // [Kt; Qt] = [K; Q] o e^{g}, 128 rows
-constexpr uint32_t SM_KHAT = SM_STACK + 32768;  // K o e^{ref_b - g}; then T'; then -W
-constexpr uint32_t SM_KDEC = SM_KHAT + 16384;   // K o e^{g_C - g}, 64 rows
-constexpr uint32_t SM_PMAT = SM_KDEC + 16384;   // P, [64 r][64 i]
-constexpr uint32_t SM_MISC = SM_PMAT + 8192;
+constexpr uint32_t SM_GA = SM_LA + 32768;       // Gram rows [K o E; Q o E], 128 rows; then A^T fp32
+constexpr uint32_t SM_GB = SM_GA + 32768;       // Gram columns, 160 rows; then T fp32, X, T'
+constexpr uint32_t SM_STACK = SM_GB + 40960;    // [Qt; Kt -> -W], 128 rows; output staging
+constexpr uint32_t SM_KDEC = SM_STACK + 32768;  // K o e^{g_C - g}, 64 rows (MN-major operand)
+constexpr uint32_t SM_PMN = SM_KDEC + 16384;    // P stored [i][r] (MN-major), right after Kdec
+constexpr uint32_t SM_MISC = SM_PMN + 8192;
 
+constexpr uint32_t GB_ROWS = 160;
+constexpr uint32_t OFF_TINV = 0;               // inside SM_GB, after the Gram MMAs
+constexpr uint32_t OFF_XBUF = 64 * 72 * 4;
+constexpr uint32_t OFF_TPRIME = 24576;
 constexpr int FP = 72;  // pitch (floats) of the fp32 64 x 64 matrices of the solve
 constexpr int XP = 24;  // pitch (floats) of the 16 x 16 intermediate blocks
 
 // Per-channel factor table rows (fp32, 128 channels each).
-//   0..9 : F[a][b] = 2^{st_a - ref_b} at index a(a+1)/2 + b   (tile starts/ends in log2 units)
+//   0..9 : F[a][b] = 2^{st_a - ref_b} at index a(a+1)/2 + b   (log2 units)
 //   10   : 2^{ref_0}      11 : 2^{tot_3}      12 : Gamma_C = 2^{g_C}
 constexpr int TAB_R0 = 10, TAB_T3 = 11, TAB_GAMMA = 12, TAB_ROWS = 13;
 
 struct Misc {
-  float beta[C];
+  float beta[2][C];           // beta of the current chunk and the prefetched next one
   float tot[4][D];            // per-tile total log2-decay
   float tab[TAB_ROWS][D];
-  uint64_t bar_qk, bar_la, bar_v;                            // TMA arrivals
-  uint64_t bar_v01, bar_gp, bar_wu, bar_m1, bar_m2, bar_fin; // MMA completions
+  uint64_t bar_qk, bar_la, bar_v;               // TMA arrivals
+  uint64_t bar_gp, bar_wu, bar_m1, bar_m2, bar_fin;  // MMA completions
   uint32_t tmem_base;
   int abort;
   uint32_t tma_issued[3], tma_waited[3];  // per TMA barrier: phases issued / consumed
@@ -98,24 +101,24 @@ struct Misc {
 
 constexpr uint32_t SMEM_BYTES = SM_MISC + sizeof(Misc) + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(64 * FP * 4 <= 32768, "A^T fits SM_VX");
-static_assert(64 * FP * 4 + 3 * 16 * XP * 4 <= 32768, "T and X blocks fit SM_VY");
+static_assert(64 * FP * 4 <= 32768, "A^T fits SM_GA");
+static_assert(OFF_XBUF + 3 * 16 * XP * 4 <= OFF_TPRIME && OFF_TPRIME + 8192 <= 40960,
+              "T, X blocks and T' fit SM_GB");
 
 // TMEM columns (fp32 cells).
-constexpr uint32_t TM_S = 0;     // S^T, 128 columns
-constexpr uint32_t TM_AS = 128;  // bf16 S^T (A operand), 64 columns
+constexpr uint32_t TM_S = 0;     // S^T, 128 columns      } M2 writes [S^T | O^T]
+constexpr uint32_t TM_O = 128;   // O^T, 64 columns       } O+M1 writes [O^T | U^T]
 constexpr uint32_t TM_U = 192;   // U^T, then Delta^T (fp32), 64 columns
-constexpr uint32_t TM_O = 256;   // O^T, 64 columns
-constexpr uint32_t TM_GP = 320;  // [Gram; P] rows x 64 column-tile columns
-constexpr uint32_t TM_W = 384;   // W^T, 64 columns
-constexpr uint32_t TM_AD = 448;  // bf16 Delta^T (A operand), 32 columns
+constexpr uint32_t TM_AS = 256;  // bf16 S^T (A operand), 64 columns
+constexpr uint32_t TM_AD = 320;  // bf16 Delta^T (A operand), 32 columns
+constexpr uint32_t TM_GP = 352;  // [Gram; P] rows x 160 block columns
+constexpr uint32_t TM_W = 352;   // W^T, 64 columns (after the Gram/P epilogue)
 constexpr uint32_t TM_COLS = 512;
 
-constexpr uint32_t ID_GP = idesc_bf16(128, 16, false, false);
+constexpr uint32_t ID_GP = idesc_bf16(128, GB_ROWS, false, false);
 constexpr uint32_t ID_UW = idesc_bf16(128, 64, true, false);
-constexpr uint32_t ID_KK64 = idesc_bf16(128, 64, false, false);
-constexpr uint32_t ID_KM64 = idesc_bf16(128, 64, false, true);
-constexpr uint32_t ID_KM128 = idesc_bf16(128, 128, false, true);
+constexpr uint32_t ID_OM1 = idesc_bf16(128, 128, false, false);
+constexpr uint32_t ID_M2 = idesc_bf16(128, 192, false, true);
 
 enum { TMA_QK = 0, TMA_LA = 1, TMA_V = 2 };
 
@@ -193,6 +196,9 @@ __device__ __forceinline__ void st8_scaled(uint32_t saddr, const float (&x)[8],
                pack_bf16x2(x[4] * f[4], x[5] * f[5]), pack_bf16x2(x[6] * f[6], x[7] * f[7]));
 }
 
+// Block column index of tile pair (a, b), a >= b, in the Gram column operand.
+__host__ __device__ constexpr int blk(int a, int b) { return a * (a + 1) / 2 + b; }
+
 __global__ void __launch_bounds__(kThreads, 1)
 kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -210,7 +216,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int chain = blockIdx.x;
   const int seq = chain / H, h = chain % H;
   const Ctx cx{smem, &m, status, chain};
-  const uint32_t sbase_u32 = smem_u32(smem);
+  const uint32_t sb = smem_u32(smem);
 
   const int64_t t0 = cu_seqlens[seq], t1 = cu_seqlens[seq + 1];
   if (t0 < 0 || t1 < t0 || t1 > n_tokens ||
@@ -223,8 +229,8 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   if (tid == 0) {
     mbar_init(&m.bar_qk, 1); mbar_init(&m.bar_la, 1); mbar_init(&m.bar_v, 1);
-    mbar_init(&m.bar_v01, 1); mbar_init(&m.bar_gp, 1); mbar_init(&m.bar_wu, 1);
-    mbar_init(&m.bar_m1, 1); mbar_init(&m.bar_m2, 1); mbar_init(&m.bar_fin, 1);
+    mbar_init(&m.bar_gp, 1); mbar_init(&m.bar_wu, 1); mbar_init(&m.bar_m1, 1);
+    mbar_init(&m.bar_m2, 1); mbar_init(&m.bar_fin, 1);
     fence_mbarrier_init();
     m.abort = 0;
     for (int i = 0; i < 3; ++i) m.tma_issued[i] = m.tma_waited[i] = 0;
@@ -233,6 +239,9 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     tmem_alloc(&m.tmem_base, TM_COLS);
     tmem_relinquish();
   }
+  // P blocks above the diagonal are never written: zero the tile once.
+  for (int e = tid; e < 8192 / 16; e += kThreads) st_shared_v4(sb + SM_PMN + 16 * e, 0, 0, 0, 0);
+  if (tid < C) m.beta[0][tid] = (n_chunks > 0 && tid < len) ? beta[(t0 + tid) * H + h] : 0.f;
   cta_sync();
   const uint32_t tm = m.tmem_base;
   const int q4 = warp & 3, hf = warp >> 2;  // TMEM lane quadrant, column half
@@ -268,7 +277,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     issue_qk(0); issue_la(0); issue_v(0);
   }
 
-  // ---- initial state -> S^T in TMEM (thread: lane n, 64 key columns of its half)
+  // ---- initial state -> S^T in TMEM (thread: lane n, 64 key columns of its half); O^T = 0
   const int64_t sbase = ((int64_t)seq * H + h) * D * D;
   {
     const int n = lane_base + lane;
@@ -281,25 +290,68 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         r[j] = __float_as_uint(init_state ? init_state[sbase + (int64_t)(c0 + j) * D + n] : 0.f);
       tmem_st32(tmem_addr(tm, lane_base, TM_S + c0), r);
     }
+    uint32_t z[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) z[j] = 0u;
+    tmem_st32(tmem_addr(tm, lane_base, TM_O + 32 * hf), z);
     tmem_st_wait();
   }
   cta_sync();
+
+  // Writes the output rows of a finished chunk: O^T (TMEM) -> bf16 staging in
+  // SM_STACK -> coalesced 16-byte stores; clears O^T for the next chunk.
+  auto flush_output = [&](int64_t otb, int onv) {
+    {
+      uint32_t r[32];
+      tmem_ld32(tmem_addr(tm, lane_base, TM_O + 32 * hf), r);
+      tmem_ld_wait(r);
+      __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(smem + SM_STACK);
+      const int n = lane_base + lane;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        stg[(32 * hf + j) * D + n] = __float2bfloat16_rn(__uint_as_float(r[j]));
+      uint32_t z[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) z[j] = 0u;
+      tmem_st32(tmem_addr(tm, lane_base, TM_O + 32 * hf), z);
+      tmem_st_wait();
+    }
+    __syncthreads();
+    const uint4 *stg = reinterpret_cast<const uint4 *>(smem + SM_STACK);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = tid + kThreads * j;  // 16-byte chunk: row e / 16, column chunk e % 16
+      const int rr = e >> 4;
+      if (rr < onv) {
+        uint4 *dst = reinterpret_cast<uint4 *>(out + ((otb + rr) * H + h) * D) + (e & 15);
+        *dst = stg[e];
+      }
+    }
+  };
 
   // Build-task coordinates: 8-channel group gg of one row per tile.
   const int gg = tid & 15, rsub = tid >> 4;
   const int ghalf = gg >> 3, gchunk = gg & 7, gc0 = 8 * gg;
 
   bool failed = false;
+  int64_t prev_tb = 0;
+  int prev_nv = 0;
+  float beta_next = 0.f;
   for (int ci = 0; ci < n_chunks && !failed; ++ci) {
     const uint32_t par = (uint32_t)(ci & 1);
     const int64_t tb = t0 + (int64_t)C * ci;
     const int nv = (int)((len - (int64_t)C * ci) < C ? (len - (int64_t)C * ci) : C);
     const bool has_next = ci + 1 < n_chunks;
+    const float *bcur = m.beta[ci & 1];
     PHASE_MARK(0);
 
-    // ================= phase 1a: per-tile prefix of the log2-decay, in place
+    // ================= phase 1: per-tile prefix of the log2-decay, in place
     const bool ok_qk = wait_bar(cx, &m.bar_qk, par, 10, ci);
     const bool ok_la = wait_bar(cx, &m.bar_la, par, 11, ci);
+    if (has_next && tid < C) {   // prefetch next chunk's beta into a register
+      const int64_t len_next = len - (int64_t)C * (ci + 1);
+      beta_next = tid < len_next ? beta[(tb + C + tid) * H + h] : 0.f;
+    }
     {
       float *la = reinterpret_cast<float *>(smem + SM_LA);
       const int c = tid & 127, hh = tid >> 7;
@@ -317,7 +369,6 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         m.tot[a][c] = acc;
       }
     }
-    if (tid < C) m.beta[tid] = tid < nv ? beta[(tb + tid) * H + h] : 0.f;
     if (tid == 0) {
       if (ok_qk) m.tma_waited[TMA_QK]++;
       if (ok_la) m.tma_waited[TMA_LA]++;
@@ -326,11 +377,11 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     PHASE_MARK(1);
     if (m.abort) { failed = true; break; }
 
-    // ================= phase 1b: per-channel factor table
+    // ================= phase 2: per-channel factor table
     if (tid < D) {
       const int c = tid;
       const float x0 = m.tot[0][c], x1 = m.tot[1][c], x2 = m.tot[2][c], x3 = m.tot[3][c];
-      const float st1 = x0, st2 = x0 + x1, st3 = x0 + x1 + x2;  // tile starts (st0 = 0)
+      const float st1 = x0, st2 = x0 + x1, st3 = x0 + x1 + x2;     // tile starts (st0 = 0)
       const float rf0 = x0, rf1 = st2, rf2 = st3, rf3 = st3 + x3;  // tile ends
       m.tab[0][c] = ex2(-rf0);
       m.tab[1][c] = ex2(st1 - rf0);
@@ -348,172 +399,181 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     __syncthreads();
 
-    // ================= phase 1c: operand tiles, versions 0 and 1
-    // Task: row r = 16a + rsub, channels gc0..gc0+7.  E = 2^{L} (row factor from
-    // the tile start), Ec = 2^{tot_a - L} (column factor to the tile end).
+    // ================= phase 3: Gram operands.  Task: row r = 16a + rsub, channels
+    // gc0..gc0+7; E = 2^{L} (to the tile start), Ec = 2^{tot_a - L} (to the tile end).
     {
       const float *L = reinterpret_cast<const float *>(smem + SM_LA);
 #pragma unroll
       for (int a = 0; a < 4; ++a) {
         const int r = 16 * a + rsub;
         const uint32_t swz = (uint32_t)((gchunk ^ (r & 7)) << 4);
-        const uint32_t o64 = ghalf * 8192u + r * 128u + swz;           // 64-row tiles
-        const uint32_t o128 = ghalf * 16384u + r * 128u + swz;         // 128-row tiles, row r
-        const uint32_t o128q = o128 + 64u * 128u;                       // row 64 + r
-        float Lv[8], tv[8], kf[8], qf[8];
+        const uint32_t o64 = ghalf * 8192u + r * 128u + swz;
+        float Lv[8], tv[8], kf[8], qf[8], E[8], Ec[8];
         ld8(Lv, L + r * D + gc0);
         ld8(tv, &m.tot[a][gc0]);
-        unpack8(kf, ld_shared_v4(sbase_u32 + SM_K + o64));
-        unpack8(qf, ld_shared_v4(sbase_u32 + SM_Q + o64));
-        float E[8], Ec[8], ke[8], qe[8];
+        unpack8(kf, ld_shared_v4(sb + SM_K + o64));
+        unpack8(qf, ld_shared_v4(sb + SM_Q + o64));
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           E[i] = ex2(Lv[i]);
           Ec[i] = ex2(tv[i] - Lv[i]);
-          ke[i] = kf[i] * E[i];
-          qe[i] = qf[i] * E[i];
         }
-        st8_scaled(sbase_u32 + SM_KHAT + o64, kf, Ec);
-        {
-          float f[8];   // e^{g_C - ref_a} Ec
-          if (a == 3) {
+        // rows r and 64 + r of [K o E; Q o E]
+        const uint32_t oa = ghalf * 16384u + r * 128u + swz;
+        st8_scaled(sb + SM_GA + oa, kf, E);
+        st8_scaled(sb + SM_GA + oa + 64u * 128u, qf, E);
+        // column blocks (a2, a) for a2 >= a: k_i Ec_i F[a2][a]
 #pragma unroll
-            for (int i = 0; i < 8; ++i) f[i] = Ec[i];
-          } else {
-            float t3[8], fa[8];
-            ld8(t3, &m.tab[TAB_T3][gc0]);
-            ld8(fa, &m.tab[6 + a][gc0]);
+        for (int a2 = a; a2 < 4; ++a2) {
+          float f[8], kc[8];
+          ld8(f, &m.tab[blk(a2, a)][gc0]);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) f[i] = Ec[i] * (t3[i] * fa[i]);
-          }
-          st8_scaled(sbase_u32 + SM_KDEC + o64, kf, f);
-        }
-        {
-          float f0[8], r0[8], fs[8];   // version-0 factor and e^{st_a} = F[a][0] 2^{ref_0}
-          ld8(f0, &m.tab[a * (a + 1) / 2][gc0]);
-          ld8(r0, &m.tab[TAB_R0][gc0]);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) fs[i] = f0[i] * r0[i];
-          st8_scaled(sbase_u32 + SM_STACK + o128, ke, fs);
-          st8_scaled(sbase_u32 + SM_STACK + o128q, qe, fs);
-          st8_scaled(sbase_u32 + SM_VX + o128, ke, f0);
-          st8_scaled(sbase_u32 + SM_VX + o128q, qe, f0);
-        }
-        if (a >= 1) {
-          float f1[8];
-          ld8(f1, &m.tab[a * (a + 1) / 2 + 1][gc0]);
-          st8_scaled(sbase_u32 + SM_VY + o128, ke, f1);
-          st8_scaled(sbase_u32 + SM_VY + o128q, qe, f1);
+          for (int i = 0; i < 8; ++i) kc[i] = kf[i] * Ec[i];
+          const int brow = 16 * blk(a2, a) + rsub;
+          st8_scaled(sb + SM_GB + ghalf * (GB_ROWS * 128u) + brow * 128u +
+                         (uint32_t)((gchunk ^ (brow & 7)) << 4),
+                     kc, f);
         }
       }
     }
     fence_proxy_async_smem();
     cta_sync();
     PHASE_MARK(2);
-
-    auto issue_gp = [&](uint32_t buf, int b) {
+    if (tid == 0) {
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        const uint64_t ad = kdesc(smem + buf, (ks >> 2) * 16384u + (ks & 3) * 32u);
-        const uint64_t bd = kdesc(smem + SM_KHAT, (ks >> 2) * 8192u + 2048u * b + (ks & 3) * 32u);
-        umma_ss(tm + TM_GP + 16 * b, ad, bd, ID_GP, ks > 0 ? 1u : 0u);
+        const uint64_t ad = kdesc(smem + SM_GA, (ks >> 2) * 16384u + (ks & 3) * 32u);
+        const uint64_t bd = kdesc(smem + SM_GB, (ks >> 2) * (GB_ROWS * 128u) + (ks & 3) * 32u);
+        umma_ss(tm + TM_GP, ad, bd, ID_GP, ks > 0 ? 1u : 0u);
       }
-    };
-    if (tid == 0) {
-      issue_gp(SM_VX, 0);
-      issue_gp(SM_VY, 1);
-      umma_commit(&m.bar_v01);
+      umma_commit(&m.bar_gp);
     }
 
-    // ================= phase 1d: versions 2 and 3 (rows of tiles 2, 3)
-    wait_bar(cx, &m.bar_v01, par, 20, ci);
+    // ================= phase 4 (while the Gram MMAs run): S pass, previous output
+    if (ci > 0) {
+      wait_bar(cx, &m.bar_m2, par ^ 1u, 25, ci - 1);
+      tc_fence_after();
+    }
+    {
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        const int c0 = 64 * hf + 32 * part;
+        uint32_t s[32];
+        tmem_ld32(tmem_addr(tm, lane_base, TM_S + c0), s);
+        tmem_ld_wait(s);
+        uint32_t ab[16];
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          float gv[8];
+          ld8(gv, &m.tab[TAB_GAMMA][c0 + 8 * q8]);
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int j = 8 * q8 + 2 * jj;
+            const float f0 = __uint_as_float(s[j]), f1 = __uint_as_float(s[j + 1]);
+            ab[4 * q8 + jj] = pack_bf16x2(f0, f1);
+            s[j] = __float_as_uint(f0 * gv[2 * jj]);
+            s[j + 1] = __float_as_uint(f1 * gv[2 * jj + 1]);
+          }
+        }
+        tmem_st32(tmem_addr(tm, lane_base, TM_S + c0), s);
+        tmem_st16(tmem_addr(tm, lane_base, TM_AS + c0 / 2), ab);
+      }
+      tmem_st_wait();
+    }
+    if (ci > 0) flush_output(prev_tb, prev_nv);
+    __syncthreads();   // staging reads done before the stack is rebuilt
+    PHASE_MARK(3);
+
+    // ================= phase 5: [Qt; Kt] (chunk-start reference) and Kdec
     {
       const float *L = reinterpret_cast<const float *>(smem + SM_LA);
 #pragma unroll
-      for (int t2 = 0; t2 < 2; ++t2) {
-        const int a = 2 + t2;
+      for (int a = 0; a < 4; ++a) {
         const int r = 16 * a + rsub;
         const uint32_t swz = (uint32_t)((gchunk ^ (r & 7)) << 4);
         const uint32_t o64 = ghalf * 8192u + r * 128u + swz;
         const uint32_t o128 = ghalf * 16384u + r * 128u + swz;
-        const uint32_t o128q = o128 + 64u * 128u;
-        float Lv[8], kf[8], qf[8];
+        float Lv[8], tv[8], kf[8], qf[8], f0[8], r0[8];
         ld8(Lv, L + r * D + gc0);
-        unpack8(kf, ld_shared_v4(sbase_u32 + SM_K + o64));
-        unpack8(qf, ld_shared_v4(sbase_u32 + SM_Q + o64));
-        float ke[8], qe[8];
+        ld8(tv, &m.tot[a][gc0]);
+        unpack8(kf, ld_shared_v4(sb + SM_K + o64));
+        unpack8(qf, ld_shared_v4(sb + SM_Q + o64));
+        ld8(f0, &m.tab[blk(a, 0)][gc0]);
+        ld8(r0, &m.tab[TAB_R0][gc0]);
+        float e[8], ed[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float e = ex2(Lv[i]);
-          ke[i] = kf[i] * e;
-          qe[i] = qf[i] * e;
-        }
-        float f2[8];
-        ld8(f2, &m.tab[a * (a + 1) / 2 + 2][gc0]);
-        st8_scaled(sbase_u32 + SM_VX + o128, ke, f2);
-        st8_scaled(sbase_u32 + SM_VX + o128q, qe, f2);
+        for (int i = 0; i < 8; ++i) e[i] = ex2(Lv[i]) * (f0[i] * r0[i]);   // e^{g_r}
         if (a == 3) {
-          float f3[8];
-          ld8(f3, &m.tab[9][gc0]);
-          st8_scaled(sbase_u32 + SM_VY + o128, ke, f3);
-          st8_scaled(sbase_u32 + SM_VY + o128q, qe, f3);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) ed[i] = ex2(tv[i] - Lv[i]);          // e^{g_C - g_i}
+        } else {
+          float t3[8], fa[8];
+          ld8(t3, &m.tab[TAB_T3][gc0]);
+          ld8(fa, &m.tab[blk(3, a)][gc0]);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) ed[i] = ex2(tv[i] - Lv[i]) * (t3[i] * fa[i]);
+        }
+        st8_scaled(sb + SM_STACK + o128, qf, e);
+        st8_scaled(sb + SM_STACK + o128 + 64u * 128u, kf, e);
+        st8_scaled(sb + SM_KDEC + o64, kf, ed);
+      }
+    }
+    fence_proxy_async_smem();
+    if (tid < C && has_next) m.beta[(ci + 1) & 1][tid] = beta_next;
+    cta_sync();
+    PHASE_MARK(4);
+    if (m.abort) { failed = true; break; }
+    if (tid == 0 && has_next) { issue_qk(ci + 1); issue_la(ci + 1); }   // q, k, L consumed
+
+    // ================= phase 6: A^T (fp32, for the solve) and P (bf16, stored [i][r])
+    wait_bar(cx, &m.bar_gp, par, 22, ci);
+    tc_fence_after();
+    PHASE_MARK(5);
+    {
+      // Quadrant rows: 32 (q4 & 1) + lane; block columns of tiles {0,1} are [0, 48),
+      // of tiles {2,3} are [48, 160); the two warps of a quadrant split them.
+      const int row = 32 * (q4 & 1) + lane;
+      const int ta = row >> 4;
+      const bool gram = q4 < 2;
+      const float br = bcur[row];
+      float *amatT = reinterpret_cast<float *>(smem + SM_GA);
+      __nv_bfloat16 *pmn = reinterpret_cast<__nv_bfloat16 *>(smem + SM_PMN);
+      const int nld = (q4 & 1) ? 2 : 1;
+      const int col_first = (q4 & 1) ? 32 + 64 * hf : 32 * hf;
+      for (int li = 0; li < nld; ++li) {
+        const int col0 = col_first + 32 * li;
+        uint32_t v[32];
+        tmem_ld32(tmem_addr(tm, lane_base, TM_GP + col0), v);
+        tmem_ld_wait(v);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int bk = (col0 >> 4) + half;    // block index of these 16 columns
+          const int ba = bk >= 6 ? 3 : bk >= 3 ? 2 : bk >= 1 ? 1 : 0;
+          const int bb = bk - ba * (ba + 1) / 2;
+          if (ba != ta) continue;
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int i = 16 * bb + jj;
+            const float x = __uint_as_float(v[16 * half + jj]);
+            if (gram) {
+              amatT[i * FP + row] = i < row ? br * x : 0.f;
+            } else {
+              pmn[(sw128_offset(i, row * 2)) >> 1] = __float2bfloat16_rn(i <= row ? x : 0.f);
+            }
+          }
         }
       }
     }
     fence_proxy_async_smem();
     cta_sync();
-    PHASE_MARK(3);
-    if (m.abort) { failed = true; break; }
-    if (tid == 0) {
-      issue_gp(SM_VX, 2);
-      issue_gp(SM_VY, 3);
-      umma_commit(&m.bar_gp);
-      if (has_next) { issue_qk(ci + 1); issue_la(ci + 1); }  // q, k, L no longer read
-    }
-
-    // ================= phase 2: A^T (fp32, for the solve) and P (bf16 operand)
-    wait_bar(cx, &m.bar_gp, par, 22, ci);
-    tc_fence_after();
-    PHASE_MARK(4);
-    {
-      uint32_t r[32];
-      tmem_ld32(tmem_addr(tm, lane_base, TM_GP + 32 * hf), r);
-      tmem_ld_wait(r);
-      if (q4 < 2) {
-        const int row = 32 * q4 + lane;
-        const float br = m.beta[row];
-        float *amatT = reinterpret_cast<float *>(smem + SM_VX);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int i = 32 * hf + j;
-          amatT[i * FP + row] = i < row ? br * __uint_as_float(r[j]) : 0.f;
-        }
-      } else {
-        const int row = 32 * (q4 - 2) + lane;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          uint32_t w[4];
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int j = 8 * g + 2 * t, i = 32 * hf + j;
-            const float lo = i <= row ? __uint_as_float(r[j]) : 0.f;
-            const float hi = i + 1 <= row ? __uint_as_float(r[j + 1]) : 0.f;
-            w[t] = pack_bf16x2(lo, hi);
-          }
-          st_shared_v4(sbase_u32 + SM_PMAT + sw128_offset(row, (32 * hf + 8 * g) * 2), w[0],
-                       w[1], w[2], w[3]);
-        }
-      }
-    }
-    cta_sync();
-    PHASE_MARK(5);
+    PHASE_MARK(6);
     if (m.abort) { failed = true; break; }
 
-    // ================= phase 3: T = (I + A)^{-1}, blocked by 16 x 16 tiles
+    // ================= phase 7: T = (I + A)^{-1}, blocked by 16 x 16 tiles
     {
-      const float *amatT = reinterpret_cast<const float *>(smem + SM_VX);  // A^T, [i][r]
-      float *tinv = reinterpret_cast<float *>(smem + SM_VY);               // T, [r][i]
-      float *xbuf = tinv + 64 * FP;
+      const float *amatT = reinterpret_cast<const float *>(smem + SM_GA);        // A^T, [i][r]
+      float *tinv = reinterpret_cast<float *>(smem + SM_GB + OFF_TINV);          // T, [r][i]
+      float *xbuf = reinterpret_cast<float *>(smem + SM_GB + OFF_XBUF);
       if (warp < 2) {
         // Diagonal blocks by column-oriented forward substitution: lane owns
         // column j of block a; after step m, t[m] is final and is eliminated
@@ -527,15 +587,14 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           float col[16];
           ld8(*reinterpret_cast<float(*)[8]>(col), amatT + (b0 + mc) * FP + b0);
           ld8(*reinterpret_cast<float(*)[8]>(col + 8), amatT + (b0 + mc) * FP + b0 + 8);
-          const float tm = t[mc];
+          const float tmv = t[mc];
 #pragma unroll
-          for (int r = mc + 1; r < 16; ++r) t[r] = fmaf(-col[r], tm, t[r]);
+          for (int r = mc + 1; r < 16; ++r) t[r] = fmaf(-col[r], tmv, t[r]);
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) tinv[(b0 + r) * FP + b0 + j] = t[r];
       }
       __syncthreads();
-      PHASE_MARK(6);
       // Off-diagonal blocks by distance d = a - b, one warp per block, TF32 MMA:
       //   X = sum_{m=b}^{a-1} A_am T_mb,  T_ab = -T_aa X
       const int g = lane >> 2, t4 = lane & 3;
@@ -547,7 +606,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           for (int mm = bb; mm < ab; ++mm) {
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
-              const int kc = 16 * mm + 8 * kk;   // k index base
+              const int kc = 16 * mm + 8 * kk;
               const uint32_t a0 = to_tf32(amatT[(kc + t4) * FP + 16 * ab + g]);
               const uint32_t a1 = to_tf32(amatT[(kc + t4) * FP + 16 * ab + g + 8]);
               const uint32_t a2 = to_tf32(amatT[(kc + t4 + 4) * FP + 16 * ab + g]);
@@ -586,7 +645,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         __syncthreads();
       }
       PHASE_MARK(7);
-      // T' = T Diag(beta) -> bf16, K-major [r][i] (in the KHAT region); upper triangle zero.
+      // T' = T Diag(beta) -> bf16, K-major [r][i]; upper triangle zero.
       {
         const int row = tid >> 2, qd = tid & 3;
 #pragma unroll
@@ -594,7 +653,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           const int i0 = 16 * qd + 8 * hh;
           float tv[8], bv[8];
           ld8(tv, tinv + row * FP + i0);
-          ld8(bv, &m.beta[i0]);
+          ld8(bv, &bcur[i0]);
           uint32_t w[4];
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
@@ -603,38 +662,11 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             const float hi = i + 1 <= row ? tv[2 * t + 1] * bv[2 * t + 1] : 0.f;
             w[t] = pack_bf16x2(lo, hi);
           }
-          st_shared_v4(sbase_u32 + SM_KHAT + sw128_offset(row, i0 * 2), w[0], w[1], w[2], w[3]);
+          st_shared_v4(sb + SM_GB + OFF_TPRIME + sw128_offset(row, i0 * 2), w[0], w[1], w[2],
+                       w[3]);
         }
       }
       fence_proxy_async_smem();
-    }
-
-    // ================= phase 4: S pass (scale by e^{g_C}, bf16 copy as A operand)
-    {
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        const int c0 = 64 * hf + 32 * part;
-        uint32_t s[32];
-        tmem_ld32(tmem_addr(tm, lane_base, TM_S + c0), s);
-        tmem_ld_wait(s);
-        uint32_t ab[16];
-#pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {
-          float gv[8];
-          ld8(gv, &m.tab[TAB_GAMMA][c0 + 8 * q8]);
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const int j = 8 * q8 + 2 * jj;
-            const float f0 = __uint_as_float(s[j]), f1 = __uint_as_float(s[j + 1]);
-            ab[4 * q8 + jj] = pack_bf16x2(f0, f1);
-            s[j] = __float_as_uint(f0 * gv[2 * jj]);
-            s[j + 1] = __float_as_uint(f1 * gv[2 * jj + 1]);
-          }
-        }
-        tmem_st32(tmem_addr(tm, lane_base, TM_S + c0), s);
-        tmem_st16(tmem_addr(tm, lane_base, TM_AS + c0 / 2), ab);
-      }
-      tmem_st_wait();
     }
     cta_sync();
     PHASE_MARK(8);
@@ -643,22 +675,17 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         m.tma_waited[TMA_V]++;
         tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {   // U^T = V^T T'^T ; W^T = Kt^T T'^T
-          const uint64_t bd = kdesc(smem + SM_KHAT, ks * 32u);
+        for (int ks = 0; ks < 4; ++ks) {   // U^T = V^T T'^T ; W^T = Kt^T T'^T, interleaved
+          const uint64_t bd = kdesc(smem + SM_GB, OFF_TPRIME + ks * 32u);
           umma_ss(tm + TM_U, mndesc(smem + SM_V, ks * 2048u, 8192), bd, ID_UW, ks > 0);
-          umma_ss(tm + TM_W, mndesc(smem + SM_STACK, ks * 2048u, 16384), bd, ID_UW, ks > 0);
-        }
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {   // O^T = S^T Qt^T
-          const uint64_t bd =
-              kdesc(smem + SM_STACK, 64u * 128u + (ks >> 2) * 16384u + (ks & 3) * 32u);
-          umma_ts(tm + TM_O, tm + TM_AS + 8 * ks, bd, ID_KK64, ks > 0);
+          umma_ss(tm + TM_W, mndesc(smem + SM_STACK, 64u * 128u + ks * 2048u, 16384), bd, ID_UW,
+                  ks > 0);
         }
         umma_commit(&m.bar_wu);
       }
     }
 
-    // ================= phase 5: -W -> smem (KHAT region); Delta^T = U^T - S^T W^T
+    // ================= phase 8: -W -> stack rows 64.. (K-major); [O^T | D^T] = S^T [Qt; -W]^T
     wait_bar(cx, &m.bar_wu, par, 23, ci);
     tc_fence_after();
     PHASE_MARK(9);
@@ -667,16 +694,13 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       uint32_t r[32];
       tmem_ld32(tmem_addr(tm, lane_base, TM_W + 32 * hf), r);
       tmem_ld_wait(r);
-      const int crow = lane_base + lane;
+      const int c = lane_base + lane;   // key channel of this lane; W^T columns are rows r
+      __nv_bfloat16 *stk = reinterpret_cast<__nv_bfloat16 *>(smem + SM_STACK);
+      const uint32_t cbyte = (uint32_t)(c & 63) * 2u, chalf = (uint32_t)(c >> 6) * 16384u;
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        uint32_t w[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-          w[t] = pack_bf16x2(-__uint_as_float(r[8 * g + 2 * t]),
-                             -__uint_as_float(r[8 * g + 2 * t + 1]));
-        st_shared_v4(sbase_u32 + SM_KHAT + sw128_offset(crow, (32 * hf + 8 * g) * 2), w[0], w[1],
-                     w[2], w[3]);
+      for (int j = 0; j < 32; ++j) {
+        const int row = 64 + 32 * hf + j;
+        stk[(chalf + sw128_offset(row, cbyte)) >> 1] = __float2bfloat16_rn(-__uint_as_float(r[j]));
       }
       fence_proxy_async_smem();
     }
@@ -686,12 +710,12 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (tid == 0) {
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        umma_ts(tm + TM_U, tm + TM_AS + 8 * ks, mndesc(smem + SM_KHAT, ks * 2048u, 8192),
-                ID_KM64, 1u);
+        umma_ts(tm + TM_O, tm + TM_AS + 8 * ks,
+                kdesc(smem + SM_STACK, (ks >> 2) * 16384u + (ks & 3) * 32u), ID_OM1, 1u);
       umma_commit(&m.bar_m1);
     }
 
-    // ================= phase 6: bf16 Delta^T; O^T += Delta^T P^T; S^T += Delta^T Kdec
+    // ================= phase 9: bf16 Delta^T; [S^T | O^T] += Delta^T [Kdec | P]
     wait_bar(cx, &m.bar_m1, par, 24, ci);
     tc_fence_after();
     PHASE_MARK(11);
@@ -711,45 +735,21 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (m.abort) { failed = true; break; }
     if (tid == 0) {
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        umma_ts(tm + TM_O, tm + TM_AD + 8 * ks, kdesc(smem + SM_PMAT, ks * 32u), ID_KK64, 1u);
-        umma_ts(tm + TM_S, tm + TM_AD + 8 * ks, mndesc(smem + SM_KDEC, ks * 2048u, 8192),
-                ID_KM128, 1u);
-      }
+      for (int ks = 0; ks < 4; ++ks)
+        umma_ts(tm + TM_S, tm + TM_AD + 8 * ks, mndesc(smem + SM_KDEC, ks * 2048u, 8192), ID_M2,
+                1u);
       umma_commit(&m.bar_m2);
     }
-
-    // ================= phase 7: output rows of this chunk, staged through SM_VX
-    wait_bar(cx, &m.bar_m2, par, 25, ci);
-    tc_fence_after();
-    PHASE_MARK(13);
-    {
-      uint32_t r[32];
-      tmem_ld32(tmem_addr(tm, lane_base, TM_O + 32 * hf), r);
-      tmem_ld_wait(r);
-      __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(smem + SM_VX);
-      const int n = lane_base + lane;
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        stg[(32 * hf + j) * D + n] = __float2bfloat16_rn(__uint_as_float(r[j]));
-    }
-    __syncthreads();
-    {
-      const uint4 *stg = reinterpret_cast<const uint4 *>(smem + SM_VX);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int e = tid + kThreads * j;   // 16-byte chunk: row e / 16, column chunk e % 16
-        const int rr = e >> 4;
-        if (rr < nv) {
-          uint4 *dst = reinterpret_cast<uint4 *>(out + ((tb + rr) * H + h) * D) + (e & 15);
-          *dst = stg[e];
-        }
-      }
-    }
-    PHASE_MARK(14);
-    __syncthreads();
+    prev_tb = tb;
+    prev_nv = nv;
   }
 
+  // ---- the last chunk's output and the final state
+  if (!failed && n_chunks > 0) {
+    wait_bar(cx, &m.bar_m2, (uint32_t)((n_chunks - 1) & 1), 26, n_chunks - 1);
+    tc_fence_after();
+    flush_output(prev_tb, prev_nv);
+  }
   cta_sync();
   if (!failed && !m.abort) {
     if (final_state) {
