@@ -68,10 +68,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t SM_Q = 0;                    // q chunk (TMA), 64 rows
 constexpr uint32_t SM_K = SM_Q + 16384;         // k chunk (TMA), 64 rows
 constexpr uint32_t SM_V = SM_K + 16384;         // v chunk (TMA), 64 rows
-constexpr uint32_t SM_LA = SM_V + 16384;        // log_alpha fp32 [64][128] -> tile prefixes L
+constexpr uint32_t SM_LA = SM_V + 16384;        // log_alpha fp32 [64][128]; then output staging
 constexpr uint32_t SM_GA = SM_LA + 32768;       // Gram rows [K o E; Q o E], 128 rows; then A^T fp32
 constexpr uint32_t SM_GB = SM_GA + 32768;       // Gram columns, 160 rows; then T fp32, X, T'
-constexpr uint32_t SM_STACK = SM_GB + 40960;    // [Qt; Kt -> -W], 128 rows; output staging
+constexpr uint32_t SM_STACK = SM_GB + 40960;    // [Qt; Kt -> -W], 128 rows
 constexpr uint32_t SM_KDEC = SM_STACK + 32768;  // K o e^{g_C - g}, 64 rows (MN-major operand)
 constexpr uint32_t SM_PMN = SM_KDEC + 16384;    // P stored [i][r] (MN-major), right after Kdec
 constexpr uint32_t SM_MISC = SM_PMN + 8192;
@@ -83,15 +83,11 @@ constexpr uint32_t OFF_TPRIME = 24576;
 constexpr int FP = 72;  // pitch (floats) of the fp32 64 x 64 matrices of the solve
 constexpr int XP = 24;  // pitch (floats) of the 16 x 16 intermediate blocks
 
-// Per-channel factor table rows (fp32, 128 channels each).
-//   0..9 : F[a][b] = 2^{st_a - ref_b} at index a(a+1)/2 + b   (log2 units)
-//   10   : 2^{ref_0}      11 : 2^{tot_3}      12 : Gamma_C = 2^{g_C}
-constexpr int TAB_R0 = 10, TAB_T3 = 11, TAB_GAMMA = 12, TAB_ROWS = 13;
 
 struct Misc {
   float beta[2][C];           // beta of the current chunk and the prefetched next one
   float tot[4][D];            // per-tile total log2-decay
-  float tab[TAB_ROWS][D];
+  float gamma[D];             // Gamma_C = e^{g_C} per key channel
   uint64_t bar_qk, bar_la, bar_v;               // TMA arrivals
   uint64_t bar_gp, bar_wu, bar_m1, bar_m2, bar_fin;  // MMA completions
   uint32_t tmem_base;
@@ -99,7 +95,7 @@ struct Misc {
   uint32_t tma_issued[3], tma_waited[3];  // per TMA barrier: phases issued / consumed
 };
 
-constexpr uint32_t SMEM_BYTES = SM_MISC + sizeof(Misc) + 1024;
+constexpr uint32_t SMEM_BYTES = SM_MISC + sizeof(Misc);
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(64 * FP * 4 <= 32768, "A^T fits SM_GA");
 static_assert(OFF_XBUF + 3 * 16 * XP * 4 <= OFF_TPRIME && OFF_TPRIME + 8192 <= 40960,
@@ -196,6 +192,19 @@ __device__ __forceinline__ void st8_scaled(uint32_t saddr, const float (&x)[8],
                pack_bf16x2(x[4] * f[4], x[5] * f[5]), pack_bf16x2(x[6] * f[6], x[7] * f[7]));
 }
 
+// Byte offset of the bf16 pair (row, c..c+1), c even, in a K-major tile whose
+// 64-column halves hold `rows` rows each.
+__device__ __forceinline__ uint32_t kmaj_off(uint32_t rows, int row, int c) {
+  return (uint32_t)(c >> 6) * rows * 128u + sw128_offset(row, (uint32_t)(c & 63) * 2u);
+}
+__device__ __forceinline__ float2 ld_pair(const uint8_t *tile, uint32_t rows, int row, int c) {
+  return unpack_bf16x2(*reinterpret_cast<const uint32_t *>(tile + kmaj_off(rows, row, c)));
+}
+__device__ __forceinline__ void st_pair(uint8_t *tile, uint32_t rows, int row, int c, float x,
+                                        float y) {
+  *reinterpret_cast<uint32_t *>(tile + kmaj_off(rows, row, c)) = pack_bf16x2(x, y);
+}
+
 // Block column index of tile pair (a, b), a >= b, in the Gram column operand.
 __host__ __device__ constexpr int blk(int a, int b) { return a * (a + 1) / 2 + b; }
 
@@ -208,15 +217,20 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const int32_t *__restrict__ cu_seqlens, int32_t n_seqs, int64_t n_tokens,
                         int32_t H, __nv_bfloat16 *__restrict__ out,
                         float *__restrict__ final_state, DeviceStatus *status) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // Indexing the __shared__ array directly (no integer round trip) keeps every
+  // access a shared-memory instruction.  The 128-byte swizzle atoms need a
+  // 1024-byte aligned base, checked below.
+  extern __shared__ __align__(1024) uint8_t smem[];
   Misc &m = *reinterpret_cast<Misc *>(smem + SM_MISC);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int chain = blockIdx.x;
   const int seq = chain / H, h = chain % H;
   const Ctx cx{smem, &m, status, chain};
   const uint32_t sb = smem_u32(smem);
+  if (sb & 1023u) {
+    if (tid == 0) record_status(status, KDA_ERR_UNSUPPORTED, 2, chain, -1);
+    return;
+  }
 
   const int64_t t0 = cu_seqlens[seq], t1 = cu_seqlens[seq + 1];
   if (t0 < 0 || t1 < t0 || t1 > n_tokens ||
@@ -299,13 +313,14 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   cta_sync();
 
   // Writes the output rows of a finished chunk: O^T (TMEM) -> bf16 staging in
-  // SM_STACK -> coalesced 16-byte stores; clears O^T for the next chunk.
+  // the log_alpha tile (free once the scan has read it) -> coalesced 16-byte
+  // stores; clears O^T for the next chunk.
   auto flush_output = [&](int64_t otb, int onv) {
     {
       uint32_t r[32];
       tmem_ld32(tmem_addr(tm, lane_base, TM_O + 32 * hf), r);
       tmem_ld_wait(r);
-      __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(smem + SM_STACK);
+      __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(smem + SM_LA);
       const int n = lane_base + lane;
 #pragma unroll
       for (int j = 0; j < 32; ++j)
@@ -317,7 +332,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       tmem_st_wait();
     }
     __syncthreads();
-    const uint4 *stg = reinterpret_cast<const uint4 *>(smem + SM_STACK);
+    const uint4 *stg = reinterpret_cast<const uint4 *>(smem + SM_LA);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int e = tid + kThreads * j;  // 16-byte chunk: row e / 16, column chunk e % 16
@@ -329,9 +344,6 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
   };
 
-  // Build-task coordinates: 8-channel group gg of one row per tile.
-  const int gg = tid & 15, rsub = tid >> 4;
-  const int ghalf = gg >> 3, gchunk = gg & 7, gc0 = 8 * gg;
 
   bool failed = false;
   int64_t prev_tb = 0;
@@ -345,100 +357,101 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     const float *bcur = m.beta[ci & 1];
     PHASE_MARK(0);
 
-    // ================= phase 1: per-tile prefix of the log2-decay, in place
+    // ================= phase 1: tile-local prefix of the log2-decay (registers)
+    // Thread (tile a, channel pair cp) owns rows 16a..16a+15 of channels c, c+1.
     const bool ok_qk = wait_bar(cx, &m.bar_qk, par, 10, ci);
     const bool ok_la = wait_bar(cx, &m.bar_la, par, 11, ci);
     if (has_next && tid < C) {   // prefetch next chunk's beta into a register
       const int64_t len_next = len - (int64_t)C * (ci + 1);
       beta_next = tid < len_next ? beta[(tb + C + tid) * H + h] : 0.f;
     }
+    const int ta = tid >> 6, cp = tid & 63, cc = 2 * cp;
+    float L0[16], L1[16];
     {
-      float *la = reinterpret_cast<float *>(smem + SM_LA);
-      const int c = tid & 127, hh = tid >> 7;
+      const float2 *la = reinterpret_cast<const float2 *>(smem + SM_LA);
+      float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-      for (int t2 = 0; t2 < 2; ++t2) {
-        const int a = 2 * hh + t2;
-        float acc = 0.f;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int r = 16 * a + j;
-          const float x = r < nv ? la[r * D + c] : 0.f;
-          acc = fmaf(x, kLog2e, acc);
-          la[r * D + c] = acc;
-        }
-        m.tot[a][c] = acc;
+      for (int j = 0; j < 16; ++j) {
+        const int row = 16 * ta + j;
+        float2 x = la[row * (D / 2) + cp];
+        if (row >= nv) x = make_float2(0.f, 0.f);
+        s0 = fmaf(x.x, kLog2e, s0);
+        s1 = fmaf(x.y, kLog2e, s1);
+        L0[j] = s0;
+        L1[j] = s1;
       }
+      *reinterpret_cast<float2 *>(&m.tot[ta][cc]) = make_float2(s0, s1);
     }
     if (tid == 0) {
       if (ok_qk) m.tma_waited[TMA_QK]++;
       if (ok_la) m.tma_waited[TMA_LA]++;
     }
+    if (ci > 0) {   // Kdec / P of the previous chunk consumed, its state final
+      wait_bar(cx, &m.bar_m2, par ^ 1u, 25, ci - 1);
+      tc_fence_after();
+    }
     cta_sync();
     PHASE_MARK(1);
     if (m.abort) { failed = true; break; }
 
-    // ================= phase 2: per-channel factor table
-    if (tid < D) {
-      const int c = tid;
-      const float x0 = m.tot[0][c], x1 = m.tot[1][c], x2 = m.tot[2][c], x3 = m.tot[3][c];
-      const float st1 = x0, st2 = x0 + x1, st3 = x0 + x1 + x2;     // tile starts (st0 = 0)
-      const float rf0 = x0, rf1 = st2, rf2 = st3, rf3 = st3 + x3;  // tile ends
-      m.tab[0][c] = ex2(-rf0);
-      m.tab[1][c] = ex2(st1 - rf0);
-      m.tab[2][c] = ex2(st1 - rf1);
-      m.tab[3][c] = ex2(st2 - rf0);
-      m.tab[4][c] = ex2(st2 - rf1);
-      m.tab[5][c] = ex2(st2 - rf2);
-      m.tab[6][c] = ex2(st3 - rf0);
-      m.tab[7][c] = ex2(st3 - rf1);
-      m.tab[8][c] = ex2(st3 - rf2);
-      m.tab[9][c] = ex2(st3 - rf3);
-      m.tab[TAB_R0][c] = ex2(rf0);
-      m.tab[TAB_T3][c] = ex2(x3);
-      m.tab[TAB_GAMMA][c] = ex2(rf3);
-    }
-    __syncthreads();
-
-    // ================= phase 3: Gram operands.  Task: row r = 16a + rsub, channels
-    // gc0..gc0+7; E = 2^{L} (to the tile start), Ec = 2^{tot_a - L} (to the tile end).
+    // ================= phase 2: every operand tile of the chunk in one pass
     {
-      const float *L = reinterpret_cast<const float *>(smem + SM_LA);
+      float st0[4], st1[4], rf0[4], rf1[4];   // tile starts / ends, channels c, c+1
+      {
+        float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        const int r = 16 * a + rsub;
-        const uint32_t swz = (uint32_t)((gchunk ^ (r & 7)) << 4);
-        const uint32_t o64 = ghalf * 8192u + r * 128u + swz;
-        float Lv[8], tv[8], kf[8], qf[8], E[8], Ec[8];
-        ld8(Lv, L + r * D + gc0);
-        ld8(tv, &m.tot[a][gc0]);
-        unpack8(kf, ld_shared_v4(sb + SM_K + o64));
-        unpack8(qf, ld_shared_v4(sb + SM_Q + o64));
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          E[i] = ex2(Lv[i]);
-          Ec[i] = ex2(tv[i] - Lv[i]);
+        for (int b = 0; b < 4; ++b) {
+          const float2 t = *reinterpret_cast<const float2 *>(&m.tot[b][cc]);
+          st0[b] = acc0; st1[b] = acc1;
+          acc0 += t.x; acc1 += t.y;
+          rf0[b] = acc0; rf1[b] = acc1;
         }
-        // rows r and 64 + r of [K o E; Q o E]
-        const uint32_t oa = ghalf * 16384u + r * 128u + swz;
-        st8_scaled(sb + SM_GA + oa, kf, E);
-        st8_scaled(sb + SM_GA + oa + 64u * 128u, qf, E);
-        // column blocks (a2, a) for a2 >= a: k_i Ec_i F[a2][a]
+      }
+      const float sa0 = ta == 0 ? st0[0] : ta == 1 ? st0[1] : ta == 2 ? st0[2] : st0[3];
+      const float sa1 = ta == 0 ? st1[0] : ta == 1 ? st1[1] : ta == 2 ? st1[2] : st1[3];
+      const float ra0 = ta == 0 ? rf0[0] : ta == 1 ? rf0[1] : ta == 2 ? rf0[2] : rf0[3];
+      const float ra1 = ta == 0 ? rf1[0] : ta == 1 ? rf1[1] : ta == 2 ? rf1[2] : rf1[3];
+      const float tot0 = ra0 - sa0, tot1 = ra1 - sa1;
+      // column-block factors F[a2][ta] = 2^{st_a2 - ref_ta}, a2 = ta..3
+      float fb0[4], fb1[4];
 #pragma unroll
-        for (int a2 = a; a2 < 4; ++a2) {
-          float f[8], kc[8];
-          ld8(f, &m.tab[blk(a2, a)][gc0]);
+      for (int a2 = 0; a2 < 4; ++a2) {
+        fb0[a2] = ex2(st0[a2] - ra0);
+        fb1[a2] = ex2(st1[a2] - ra1);
+      }
+      const float fs0 = ex2(sa0), fs1 = ex2(sa1);                 // e^{st_a}
+      const float fd0 = ex2(rf0[3] - ra0), fd1 = ex2(rf1[3] - ra1);  // e^{g_C - ref_a}
+      if (ta == 0) {
+        m.gamma[cc] = ex2(rf0[3]);
+        m.gamma[cc + 1] = ex2(rf1[3]);
+      }
 #pragma unroll
-          for (int i = 0; i < 8; ++i) kc[i] = kf[i] * Ec[i];
-          const int brow = 16 * blk(a2, a) + rsub;
-          st8_scaled(sb + SM_GB + ghalf * (GB_ROWS * 128u) + brow * 128u +
-                         (uint32_t)((gchunk ^ (brow & 7)) << 4),
-                     kc, f);
+      for (int j = 0; j < 16; ++j) {
+        const int row = 16 * ta + j;
+        const float2 kk = ld_pair(smem + SM_K, 64, row, cc);
+        const float2 qq = ld_pair(smem + SM_Q, 64, row, cc);
+        const float e0 = ex2(L0[j]), e1 = ex2(L1[j]);                    // e^{g_r - st_a}
+        const float ec0 = ex2(tot0 - L0[j]), ec1 = ex2(tot1 - L1[j]);    // e^{ref_a - g_r}
+        st_pair(smem + SM_GA, 128, row, cc, kk.x * e0, kk.y * e1);
+        st_pair(smem + SM_GA, 128, 64 + row, cc, qq.x * e0, qq.y * e1);
+        const float kc0 = kk.x * ec0, kc1 = kk.y * ec1;
+#pragma unroll
+        for (int a2 = 0; a2 < 4; ++a2) {
+          if (a2 < ta) continue;
+          const int brow = 16 * blk(a2, 0) + 16 * ta + j;   // block (a2, ta), row j
+          st_pair(smem + SM_GB, GB_ROWS, brow, cc, kc0 * fb0[a2], kc1 * fb1[a2]);
         }
+        const float g0 = e0 * fs0, g1 = e1 * fs1;                        // e^{g_r}
+        st_pair(smem + SM_STACK, 128, row, cc, qq.x * g0, qq.y * g1);
+        st_pair(smem + SM_STACK, 128, 64 + row, cc, kk.x * g0, kk.y * g1);
+        st_pair(smem + SM_KDEC, 64, row, cc, kc0 * fd0, kc1 * fd1);
       }
     }
     fence_proxy_async_smem();
+    if (tid < C && has_next) m.beta[(ci + 1) & 1][tid] = beta_next;
     cta_sync();
     PHASE_MARK(2);
+    if (m.abort) { failed = true; break; }
     if (tid == 0) {
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
@@ -447,13 +460,10 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         umma_ss(tm + TM_GP, ad, bd, ID_GP, ks > 0 ? 1u : 0u);
       }
       umma_commit(&m.bar_gp);
+      if (has_next) issue_qk(ci + 1);   // q, k consumed
     }
 
-    // ================= phase 4 (while the Gram MMAs run): S pass, previous output
-    if (ci > 0) {
-      wait_bar(cx, &m.bar_m2, par ^ 1u, 25, ci - 1);
-      tc_fence_after();
-    }
+    // ================= phase 3 (while the Gram MMAs run): S pass, previous output
     {
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
@@ -465,7 +475,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
         for (int q8 = 0; q8 < 4; ++q8) {
           float gv[8];
-          ld8(gv, &m.tab[TAB_GAMMA][c0 + 8 * q8]);
+          ld8(gv, &m.gamma[c0 + 8 * q8]);
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
             const int j = 8 * q8 + 2 * jj;
@@ -481,49 +491,10 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       tmem_st_wait();
     }
     if (ci > 0) flush_output(prev_tb, prev_nv);
-    __syncthreads();   // staging reads done before the stack is rebuilt
+    __syncthreads();   // staging (log_alpha tile) read before the next load lands there
     PHASE_MARK(3);
-
-    // ================= phase 5: [Qt; Kt] (chunk-start reference) and Kdec
-    {
-      const float *L = reinterpret_cast<const float *>(smem + SM_LA);
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        const int r = 16 * a + rsub;
-        const uint32_t swz = (uint32_t)((gchunk ^ (r & 7)) << 4);
-        const uint32_t o64 = ghalf * 8192u + r * 128u + swz;
-        const uint32_t o128 = ghalf * 16384u + r * 128u + swz;
-        float Lv[8], tv[8], kf[8], qf[8], f0[8], r0[8];
-        ld8(Lv, L + r * D + gc0);
-        ld8(tv, &m.tot[a][gc0]);
-        unpack8(kf, ld_shared_v4(sb + SM_K + o64));
-        unpack8(qf, ld_shared_v4(sb + SM_Q + o64));
-        ld8(f0, &m.tab[blk(a, 0)][gc0]);
-        ld8(r0, &m.tab[TAB_R0][gc0]);
-        float e[8], ed[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) e[i] = ex2(Lv[i]) * (f0[i] * r0[i]);   // e^{g_r}
-        if (a == 3) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) ed[i] = ex2(tv[i] - Lv[i]);          // e^{g_C - g_i}
-        } else {
-          float t3[8], fa[8];
-          ld8(t3, &m.tab[TAB_T3][gc0]);
-          ld8(fa, &m.tab[blk(3, a)][gc0]);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) ed[i] = ex2(tv[i] - Lv[i]) * (t3[i] * fa[i]);
-        }
-        st8_scaled(sb + SM_STACK + o128, qf, e);
-        st8_scaled(sb + SM_STACK + o128 + 64u * 128u, kf, e);
-        st8_scaled(sb + SM_KDEC + o64, kf, ed);
-      }
-    }
-    fence_proxy_async_smem();
-    if (tid < C && has_next) m.beta[(ci + 1) & 1][tid] = beta_next;
-    cta_sync();
+    if (tid == 0 && has_next) issue_la(ci + 1);
     PHASE_MARK(4);
-    if (m.abort) { failed = true; break; }
-    if (tid == 0 && has_next) { issue_qk(ci + 1); issue_la(ci + 1); }   // q, k, L consumed
 
     // ================= phase 6: A^T (fp32, for the solve) and P (bf16, stored [i][r])
     wait_bar(cx, &m.bar_gp, par, 22, ci);
@@ -533,7 +504,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       // Quadrant rows: 32 (q4 & 1) + lane; block columns of tiles {0,1} are [0, 48),
       // of tiles {2,3} are [48, 160); the two warps of a quadrant split them.
       const int row = 32 * (q4 & 1) + lane;
-      const int ta = row >> 4;
+      const int rta = row >> 4;
       const bool gram = q4 < 2;
       const float br = bcur[row];
       float *amatT = reinterpret_cast<float *>(smem + SM_GA);
@@ -550,7 +521,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           const int bk = (col0 >> 4) + half;    // block index of these 16 columns
           const int ba = bk >= 6 ? 3 : bk >= 3 ? 2 : bk >= 1 ? 1 : 0;
           const int bb = bk - ba * (ba + 1) / 2;
-          if (ba != ta) continue;
+          if (ba != rta) continue;
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             const int i = 16 * bb + jj;
