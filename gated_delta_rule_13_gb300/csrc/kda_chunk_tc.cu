@@ -35,9 +35,11 @@
 //   U^T  = V^T T'^T                 (A = V, smem MN-major;  B = T', K-major)
 //   W^T  = Kt^T T'^T                (A = Kt, smem MN-major)
 //   [O^T | D^T] = S^T [Qt; -W]^T    (A = bf16 S^T in TMEM; D^T accumulates onto U^T)
-//   [S^T | O^T] += Delta^T [Kdec | P_mn]   (A = bf16 Delta^T in TMEM; B MN-major),
+//   S^T += Delta^T Kdec, O^T += Delta^T P^T   (A = bf16 Delta^T in TMEM),
 //                                    after S^T <- S^T Diag(e^{g_C})
-// where D = Delta = U - W S.  28 tcgen05.mma instructions per chunk.
+// where D = Delta = U - W S.  32 tcgen05.mma instructions per chunk.  The
+// triangular solve (warps 0-3) overlaps the previous chunk's output stores
+// (warps 4-7), and the next chunk's decay prefix overlaps the state MMAs.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -73,12 +75,12 @@ constexpr uint32_t SM_GA = SM_LA + 32768;       // Gram rows [K o E; Q o E], 128
 constexpr uint32_t SM_GB = SM_GA + 32768;       // Gram columns, 160 rows; then T fp32, X, T'
 constexpr uint32_t SM_STACK = SM_GB + 40960;    // [Qt; Kt -> -W], 128 rows
 constexpr uint32_t SM_KDEC = SM_STACK + 32768;  // K o e^{g_C - g}, 64 rows (MN-major operand)
-constexpr uint32_t SM_PMN = SM_KDEC + 16384;    // P stored [i][r] (MN-major), right after Kdec
-constexpr uint32_t SM_MISC = SM_PMN + 8192;
+constexpr uint32_t SM_PMAT = SM_KDEC + 16384;   // P, K-major [64 r][64 i]
+constexpr uint32_t SM_MISC = SM_PMAT + 8192;
 
 constexpr uint32_t GB_ROWS = 160;
 constexpr uint32_t OFF_TINV = 0;               // inside SM_GB, after the Gram MMAs
-constexpr uint32_t OFF_XBUF = 64 * 72 * 4;
+constexpr uint32_t OFF_XBUF = 64 * 72 * 4;   // 4 blocks of 16 x XP fp32
 constexpr uint32_t OFF_TPRIME = 24576;
 constexpr int FP = 72;  // pitch (floats) of the fp32 64 x 64 matrices of the solve
 constexpr int XP = 24;  // pitch (floats) of the 16 x 16 intermediate blocks
@@ -98,11 +100,11 @@ struct Misc {
 constexpr uint32_t SMEM_BYTES = SM_MISC + sizeof(Misc);
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(64 * FP * 4 <= 32768, "A^T fits SM_GA");
-static_assert(OFF_XBUF + 3 * 16 * XP * 4 <= OFF_TPRIME && OFF_TPRIME + 8192 <= 40960,
+static_assert(OFF_XBUF + 4 * 16 * XP * 4 <= OFF_TPRIME && OFF_TPRIME + 8192 <= 40960,
               "T, X blocks and T' fit SM_GB");
 
 // TMEM columns (fp32 cells).
-constexpr uint32_t TM_S = 0;     // S^T, 128 columns      } M2 writes [S^T | O^T]
+constexpr uint32_t TM_S = 0;     // S^T, 128 columns
 constexpr uint32_t TM_O = 128;   // O^T, 64 columns       } O+M1 writes [O^T | U^T]
 constexpr uint32_t TM_U = 192;   // U^T, then Delta^T (fp32), 64 columns
 constexpr uint32_t TM_AS = 256;  // bf16 S^T (A operand), 64 columns
@@ -114,7 +116,8 @@ constexpr uint32_t TM_COLS = 512;
 constexpr uint32_t ID_GP = idesc_bf16(128, GB_ROWS, false, false);
 constexpr uint32_t ID_UW = idesc_bf16(128, 64, true, false);
 constexpr uint32_t ID_OM1 = idesc_bf16(128, 128, false, false);
-constexpr uint32_t ID_M2 = idesc_bf16(128, 192, false, true);
+constexpr uint32_t ID_KM128 = idesc_bf16(128, 128, false, true);
+constexpr uint32_t ID_KK64 = idesc_bf16(128, 64, false, false);
 
 enum { TMA_QK = 0, TMA_LA = 1, TMA_V = 2 };
 
@@ -254,7 +257,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     tmem_relinquish();
   }
   // P blocks above the diagonal are never written: zero the tile once.
-  for (int e = tid; e < 8192 / 16; e += kThreads) st_shared_v4(sb + SM_PMN + 16 * e, 0, 0, 0, 0);
+  for (int e = tid; e < 8192 / 16; e += kThreads) st_shared_v4(sb + SM_PMAT + 16 * e, 0, 0, 0, 0);
   if (tid < C) m.beta[0][tid] = (n_chunks > 0 && tid < len) ? beta[(t0 + tid) * H + h] : 0.f;
   cta_sync();
   const uint32_t tm = m.tmem_base;
@@ -312,43 +315,79 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   }
   cta_sync();
 
-  // Writes the output rows of a finished chunk: O^T (TMEM) -> bf16 staging in
-  // the log_alpha tile (free once the scan has read it) -> coalesced 16-byte
-  // stores; clears O^T for the next chunk.
+  // Writes the output rows of a finished chunk (warps 4-7 only): O^T (TMEM) ->
+  // bf16 staging in the log_alpha tile (free between the scan and the next
+  // log_alpha load) -> coalesced 16-byte stores; clears O^T for the next chunk.
   auto flush_output = [&](int64_t otb, int onv) {
-    {
+    __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(smem + SM_LA);
+    const int n = lane_base + lane;
+    uint32_t z[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) z[j] = 0u;
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
       uint32_t r[32];
-      tmem_ld32(tmem_addr(tm, lane_base, TM_O + 32 * hf), r);
+      tmem_ld32(tmem_addr(tm, lane_base, TM_O + 32 * part), r);
       tmem_ld_wait(r);
-      __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(smem + SM_LA);
-      const int n = lane_base + lane;
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        stg[(32 * hf + j) * D + n] = __float2bfloat16_rn(__uint_as_float(r[j]));
-      uint32_t z[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) z[j] = 0u;
-      tmem_st32(tmem_addr(tm, lane_base, TM_O + 32 * hf), z);
-      tmem_st_wait();
+        stg[(32 * part + j) * D + n] = __float2bfloat16_rn(__uint_as_float(r[j]));
+      tmem_st32(tmem_addr(tm, lane_base, TM_O + 32 * part), z);
     }
-    __syncthreads();
-    const uint4 *stg = reinterpret_cast<const uint4 *>(smem + SM_LA);
+    tmem_st_wait();
+    named_sync(2, 128);
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(smem + SM_LA);
+    const int t = tid - 128;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = tid + kThreads * j;  // 16-byte chunk: row e / 16, column chunk e % 16
+    for (int j = 0; j < 8; ++j) {
+      const int e = t + 128 * j;  // 16-byte chunk: row e / 16, column chunk e % 16
       const int rr = e >> 4;
       if (rr < onv) {
         uint4 *dst = reinterpret_cast<uint4 *>(out + ((otb + rr) * H + h) * D) + (e & 15);
-        *dst = stg[e];
+        *dst = s4[e];
       }
     }
   };
 
+  // Tile-local prefix of the log2-decay of chunk `ci` into registers; thread
+  // (tile ta, channel pair cp) owns rows 16 ta .. 16 ta + 15 of channels cc, cc+1.
+  const int ta = tid >> 6, cp = tid & 63, cc = 2 * cp;
+  float L0[16], L1[16];
+  float beta_next = 0.f;
+  auto scan = [&](int ci) -> bool {
+    const uint32_t par = (uint32_t)(ci & 1);
+    const int64_t tb = t0 + (int64_t)C * ci;
+    const int nv = (int)((len - (int64_t)C * ci) < C ? (len - (int64_t)C * ci) : C);
+    const bool ok_qk = wait_bar(cx, &m.bar_qk, par, 10, ci);
+    const bool ok_la = wait_bar(cx, &m.bar_la, par, 11, ci);
+    if (ci + 1 < n_chunks && tid < C) {   // prefetch the following chunk's beta
+      const int64_t len_next = len - (int64_t)C * (ci + 1);
+      beta_next = tid < len_next ? beta[(tb + C + tid) * H + h] : 0.f;
+    }
+    const float2 *la = reinterpret_cast<const float2 *>(smem + SM_LA);
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int row = 16 * ta + j;
+      float2 x = la[row * (D / 2) + cp];
+      if (row >= nv) x = make_float2(0.f, 0.f);
+      s0 = fmaf(x.x, kLog2e, s0);
+      s1 = fmaf(x.y, kLog2e, s1);
+      L0[j] = s0;
+      L1[j] = s1;
+    }
+    *reinterpret_cast<float2 *>(&m.tot[ta][cc]) = make_float2(s0, s1);
+    if (tid == 0) {
+      if (ok_qk) m.tma_waited[TMA_QK]++;
+      if (ok_la) m.tma_waited[TMA_LA]++;
+    }
+    return ok_qk && ok_la;
+  };
 
   bool failed = false;
   int64_t prev_tb = 0;
   int prev_nv = 0;
-  float beta_next = 0.f;
+  if (n_chunks > 0) scan(0);
   for (int ci = 0; ci < n_chunks && !failed; ++ci) {
     const uint32_t par = (uint32_t)(ci & 1);
     const int64_t tb = t0 + (int64_t)C * ci;
@@ -356,41 +395,11 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     const bool has_next = ci + 1 < n_chunks;
     const float *bcur = m.beta[ci & 1];
     PHASE_MARK(0);
-
-    // ================= phase 1: tile-local prefix of the log2-decay (registers)
-    // Thread (tile a, channel pair cp) owns rows 16a..16a+15 of channels c, c+1.
-    const bool ok_qk = wait_bar(cx, &m.bar_qk, par, 10, ci);
-    const bool ok_la = wait_bar(cx, &m.bar_la, par, 11, ci);
-    if (has_next && tid < C) {   // prefetch next chunk's beta into a register
-      const int64_t len_next = len - (int64_t)C * (ci + 1);
-      beta_next = tid < len_next ? beta[(tb + C + tid) * H + h] : 0.f;
-    }
-    const int ta = tid >> 6, cp = tid & 63, cc = 2 * cp;
-    float L0[16], L1[16];
-    {
-      const float2 *la = reinterpret_cast<const float2 *>(smem + SM_LA);
-      float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int row = 16 * ta + j;
-        float2 x = la[row * (D / 2) + cp];
-        if (row >= nv) x = make_float2(0.f, 0.f);
-        s0 = fmaf(x.x, kLog2e, s0);
-        s1 = fmaf(x.y, kLog2e, s1);
-        L0[j] = s0;
-        L1[j] = s1;
-      }
-      *reinterpret_cast<float2 *>(&m.tot[ta][cc]) = make_float2(s0, s1);
-    }
-    if (tid == 0) {
-      if (ok_qk) m.tma_waited[TMA_QK]++;
-      if (ok_la) m.tma_waited[TMA_LA]++;
-    }
     if (ci > 0) {   // Kdec / P of the previous chunk consumed, its state final
       wait_bar(cx, &m.bar_m2, par ^ 1u, 25, ci - 1);
       tc_fence_after();
     }
-    cta_sync();
+    cta_sync();     // tile totals of this chunk visible
     PHASE_MARK(1);
     if (m.abort) { failed = true; break; }
 
@@ -490,16 +499,10 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
       tmem_st_wait();
     }
-    if (ci > 0) flush_output(prev_tb, prev_nv);
-    __syncthreads();   // staging (log_alpha tile) read before the next load lands there
-    PHASE_MARK(3);
-    if (tid == 0 && has_next) issue_la(ci + 1);
-    PHASE_MARK(4);
-
-    // ================= phase 6: A^T (fp32, for the solve) and P (bf16, stored [i][r])
+    // ================= phase 4: A^T (fp32, for the solve) and P (bf16, K-major [r][i])
     wait_bar(cx, &m.bar_gp, par, 22, ci);
     tc_fence_after();
-    PHASE_MARK(5);
+    PHASE_MARK(3);
     {
       // Quadrant rows: 32 (q4 & 1) + lane; block columns of tiles {0,1} are [0, 48),
       // of tiles {2,3} are [48, 160); the two warps of a quadrant split them.
@@ -508,7 +511,6 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       const bool gram = q4 < 2;
       const float br = bcur[row];
       float *amatT = reinterpret_cast<float *>(smem + SM_GA);
-      __nv_bfloat16 *pmn = reinterpret_cast<__nv_bfloat16 *>(smem + SM_PMN);
       const int nld = (q4 & 1) ? 2 : 1;
       const int col_first = (q4 & 1) ? 32 + 64 * hf : 32 * hf;
       for (int li = 0; li < nld; ++li) {
@@ -522,14 +524,25 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           const int ba = bk >= 6 ? 3 : bk >= 3 ? 2 : bk >= 1 ? 1 : 0;
           const int bb = bk - ba * (ba + 1) / 2;
           if (ba != rta) continue;
+          if (gram) {
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int i = 16 * bb + jj;
-            const float x = __uint_as_float(v[16 * half + jj]);
-            if (gram) {
-              amatT[i * FP + row] = i < row ? br * x : 0.f;
-            } else {
-              pmn[(sw128_offset(i, row * 2)) >> 1] = __float2bfloat16_rn(i <= row ? x : 0.f);
+            for (int jj = 0; jj < 16; ++jj) {
+              const int i = 16 * bb + jj;
+              amatT[i * FP + row] = i < row ? br * __uint_as_float(v[16 * half + jj]) : 0.f;
+            }
+          } else {
+#pragma unroll
+            for (int g8 = 0; g8 < 2; ++g8) {
+              uint32_t w[4];
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const int j = 8 * g8 + 2 * t, i = 16 * bb + j;
+                const float lo = i <= row ? __uint_as_float(v[16 * half + j]) : 0.f;
+                const float hi = i + 1 <= row ? __uint_as_float(v[16 * half + j + 1]) : 0.f;
+                w[t] = pack_bf16x2(lo, hi);
+              }
+              st_shared_v4(sb + SM_PMAT + sw128_offset(row, (16 * bb + 8 * g8) * 2), w[0], w[1],
+                           w[2], w[3]);
             }
           }
         }
@@ -537,13 +550,14 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     fence_proxy_async_smem();
     cta_sync();
-    PHASE_MARK(6);
+    PHASE_MARK(4);
     if (m.abort) { failed = true; break; }
 
-    // ================= phase 7: T = (I + A)^{-1}, blocked by 16 x 16 tiles
-    {
-      const float *amatT = reinterpret_cast<const float *>(smem + SM_GA);        // A^T, [i][r]
-      float *tinv = reinterpret_cast<float *>(smem + SM_GB + OFF_TINV);          // T, [r][i]
+    // ================= phase 5: T = (I + A)^{-1} (warps 0-3) while warps 4-7 write
+    // the previous chunk's output.
+    const float *amatT = reinterpret_cast<const float *>(smem + SM_GA);   // A^T, [i][r]
+    float *tinv = reinterpret_cast<float *>(smem + SM_GB + OFF_TINV);     // T, [r][i]
+    if (warp < 4) {
       float *xbuf = reinterpret_cast<float *>(smem + SM_GB + OFF_XBUF);
       if (warp < 2) {
         // Diagonal blocks by column-oriented forward substitution: lane owns
@@ -565,82 +579,104 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
         for (int r = 0; r < 16; ++r) tinv[(b0 + r) * FP + b0 + j] = t[r];
       }
-      __syncthreads();
-      // Off-diagonal blocks by distance d = a - b, one warp per block, TF32 MMA:
-      //   X = sum_{m=b}^{a-1} A_am T_mb,  T_ab = -T_aa X
+      named_sync(1, 128);
+      // Off-diagonal blocks, block-recursive: 16 -> 32 (blocks (1,0), (3,2)), then
+      // 32 -> 64 (blocks (2,0), (2,1), (3,0), (3,1)), TF32 warp MMAs.
       const int g = lane >> 2, t4 = lane & 3;
-#pragma unroll 1
-      for (int d = 1; d < 4; ++d) {
-        if (warp < 4 - d) {
-          const int bb = warp, ab = warp + d;
-          float x0[4] = {0.f, 0.f, 0.f, 0.f}, x1[4] = {0.f, 0.f, 0.f, 0.f};
-          for (int mm = bb; mm < ab; ++mm) {
+      // acc (+)= A_{ab} T_{mb} with A from A^T (column-major, pitch FP) ...
+      auto mul_AT = [&](float (&acc)[2][4], int ab, int mb, int tcol) {
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-              const int kc = 16 * mm + 8 * kk;
-              const uint32_t a0 = to_tf32(amatT[(kc + t4) * FP + 16 * ab + g]);
-              const uint32_t a1 = to_tf32(amatT[(kc + t4) * FP + 16 * ab + g + 8]);
-              const uint32_t a2 = to_tf32(amatT[(kc + t4 + 4) * FP + 16 * ab + g]);
-              const uint32_t a3 = to_tf32(amatT[(kc + t4 + 4) * FP + 16 * ab + g + 8]);
-              const float *tb0 = tinv + (kc + t4) * FP + 16 * bb + g;
-              const float *tb1 = tinv + (kc + t4 + 4) * FP + 16 * bb + g;
-              mma_tf32_16x8x8(x0, a0, a1, a2, a3, to_tf32(tb0[0]), to_tf32(tb1[0]));
-              mma_tf32_16x8x8(x1, a0, a1, a2, a3, to_tf32(tb0[8]), to_tf32(tb1[8]));
-            }
-          }
-          float *xb = xbuf + warp * 16 * XP;
-          xb[g * XP + 2 * t4] = x0[0];       xb[g * XP + 2 * t4 + 1] = x0[1];
-          xb[(g + 8) * XP + 2 * t4] = x0[2]; xb[(g + 8) * XP + 2 * t4 + 1] = x0[3];
-          xb[g * XP + 8 + 2 * t4] = x1[0];       xb[g * XP + 8 + 2 * t4 + 1] = x1[1];
-          xb[(g + 8) * XP + 8 + 2 * t4] = x1[2]; xb[(g + 8) * XP + 8 + 2 * t4 + 1] = x1[3];
-          __syncwarp();
-          float o0[4] = {0.f, 0.f, 0.f, 0.f}, o1[4] = {0.f, 0.f, 0.f, 0.f};
-          const float *taa = tinv + (16 * ab) * FP + 16 * ab;
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            const uint32_t a0 = to_tf32(taa[g * FP + 8 * kk + t4]);
-            const uint32_t a1 = to_tf32(taa[(g + 8) * FP + 8 * kk + t4]);
-            const uint32_t a2 = to_tf32(taa[g * FP + 8 * kk + t4 + 4]);
-            const uint32_t a3 = to_tf32(taa[(g + 8) * FP + 8 * kk + t4 + 4]);
-            const float *xr0 = xb + (8 * kk + t4) * XP + g;
-            const float *xr1 = xb + (8 * kk + t4 + 4) * XP + g;
-            mma_tf32_16x8x8(o0, a0, a1, a2, a3, to_tf32(xr0[0]), to_tf32(xr1[0]));
-            mma_tf32_16x8x8(o1, a0, a1, a2, a3, to_tf32(xr0[8]), to_tf32(xr1[8]));
-          }
-          float *tab_ = tinv + (16 * ab) * FP + 16 * bb;
-          tab_[g * FP + 2 * t4] = -o0[0];       tab_[g * FP + 2 * t4 + 1] = -o0[1];
-          tab_[(g + 8) * FP + 2 * t4] = -o0[2]; tab_[(g + 8) * FP + 2 * t4 + 1] = -o0[3];
-          tab_[g * FP + 8 + 2 * t4] = -o1[0];       tab_[g * FP + 8 + 2 * t4 + 1] = -o1[1];
-          tab_[(g + 8) * FP + 8 + 2 * t4] = -o1[2]; tab_[(g + 8) * FP + 8 + 2 * t4 + 1] = -o1[3];
+        for (int kk = 0; kk < 2; ++kk) {
+          const int kc = 16 * mb + 8 * kk;
+          const uint32_t a0 = to_tf32(amatT[(kc + t4) * FP + 16 * ab + g]);
+          const uint32_t a1 = to_tf32(amatT[(kc + t4) * FP + 16 * ab + g + 8]);
+          const uint32_t a2 = to_tf32(amatT[(kc + t4 + 4) * FP + 16 * ab + g]);
+          const uint32_t a3 = to_tf32(amatT[(kc + t4 + 4) * FP + 16 * ab + g + 8]);
+          const float *b0p = tinv + (kc + t4) * FP + tcol + g;
+          const float *b1p = tinv + (kc + t4 + 4) * FP + tcol + g;
+          mma_tf32_16x8x8(acc[0], a0, a1, a2, a3, to_tf32(b0p[0]), to_tf32(b1p[0]));
+          mma_tf32_16x8x8(acc[1], a0, a1, a2, a3, to_tf32(b0p[8]), to_tf32(b1p[8]));
         }
-        __syncthreads();
-      }
-      PHASE_MARK(7);
-      // T' = T Diag(beta) -> bf16, K-major [r][i]; upper triangle zero.
-      {
-        const int row = tid >> 2, qd = tid & 3;
+      };
+      // ... and acc (+)= T_{ar} X with T row-major (pitch FP), X a 16 x 16 block (pitch XP).
+      auto mul_TX = [&](float (&acc)[2][4], int ar, int ac, const float *x) {
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int i0 = 16 * qd + 8 * hh;
-          float tv[8], bv[8];
-          ld8(tv, tinv + row * FP + i0);
-          ld8(bv, &bcur[i0]);
-          uint32_t w[4];
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int i = i0 + 2 * t;
-            const float lo = i <= row ? tv[2 * t] * bv[2 * t] : 0.f;
-            const float hi = i + 1 <= row ? tv[2 * t + 1] * bv[2 * t + 1] : 0.f;
-            w[t] = pack_bf16x2(lo, hi);
-          }
-          st_shared_v4(sb + SM_GB + OFF_TPRIME + sw128_offset(row, i0 * 2), w[0], w[1], w[2],
-                       w[3]);
+        for (int kk = 0; kk < 2; ++kk) {
+          const float *tp = tinv + (16 * ar) * FP + 16 * ac + 8 * kk;
+          const uint32_t a0 = to_tf32(tp[g * FP + t4]);
+          const uint32_t a1 = to_tf32(tp[(g + 8) * FP + t4]);
+          const uint32_t a2 = to_tf32(tp[g * FP + t4 + 4]);
+          const uint32_t a3 = to_tf32(tp[(g + 8) * FP + t4 + 4]);
+          const float *x0 = x + (8 * kk + t4) * XP + g;
+          const float *x1 = x + (8 * kk + t4 + 4) * XP + g;
+          mma_tf32_16x8x8(acc[0], a0, a1, a2, a3, to_tf32(x0[0]), to_tf32(x1[0]));
+          mma_tf32_16x8x8(acc[1], a0, a1, a2, a3, to_tf32(x0[8]), to_tf32(x1[8]));
         }
+      };
+      auto store_blk = [&](float *dst, int pitch, const float (&acc)[2][4], float sgn) {
+#pragma unroll
+        for (int nh = 0; nh < 2; ++nh) {
+          dst[g * pitch + 8 * nh + 2 * t4] = sgn * acc[nh][0];
+          dst[g * pitch + 8 * nh + 2 * t4 + 1] = sgn * acc[nh][1];
+          dst[(g + 8) * pitch + 8 * nh + 2 * t4] = sgn * acc[nh][2];
+          dst[(g + 8) * pitch + 8 * nh + 2 * t4 + 1] = sgn * acc[nh][3];
+        }
+      };
+      float *xw = xbuf + warp * 16 * XP;
+      if (warp < 2) {   // level 16 -> 32: block (1,0) on warp 0, (3,2) on warp 1
+        const int ab = 2 * warp + 1, bb = 2 * warp;
+        float acc[2][4] = {};
+        mul_AT(acc, ab, bb, 16 * bb);                 // X = A_ab T_bb
+        store_blk(xw, XP, acc, 1.f);
+        __syncwarp();
+        float o[2][4] = {};
+        mul_TX(o, ab, ab, xw);                        // T_ab = -T_aa X
+        store_blk(tinv + (16 * ab) * FP + 16 * bb, FP, o, -1.f);
       }
-      fence_proxy_async_smem();
+      named_sync(1, 128);
+      {                 // level 32 -> 64: warp w -> block (2 + w/2, w%2)
+        const int ab = 2 + (warp >> 1), bb = warp & 1;
+        float acc[2][4] = {};
+        // X_{ab} = A_{ab,0:2} T_{0:2, bb} = sum_{m=bb}^{1} A_{ab,m} T_{m,bb}
+        for (int mb = bb; mb < 2; ++mb) mul_AT(acc, ab, mb, 16 * bb);
+        store_blk(xw, XP, acc, 1.f);
+        named_sync(1, 128);
+        // T_{ab} = -sum_{k=2}^{ab} T_{ab,k} X_{k,bb}
+        float o[2][4] = {};
+        for (int k = 2; k <= ab; ++k) mul_TX(o, ab, k, xbuf + (2 * (k - 2) + bb) * 16 * XP);
+        store_blk(tinv + (16 * ab) * FP + 16 * bb, FP, o, -1.f);
+      }
+    } else {
+      if (ci > 0) flush_output(prev_tb, prev_nv);
     }
+    __syncthreads();
+    PHASE_MARK(5);
+    if (tid == 0 && has_next) issue_la(ci + 1);   // output staging read
+
+    // T' = T Diag(beta) -> bf16, K-major [r][i]; upper triangle zero.
+    {
+      const int row = tid >> 2, qd = tid & 3;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int i0 = 16 * qd + 8 * hh;
+        float tv[8], bv[8];
+        ld8(tv, tinv + row * FP + i0);
+        ld8(bv, &bcur[i0]);
+        uint32_t w[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int i = i0 + 2 * t;
+          const float lo = i <= row ? tv[2 * t] * bv[2 * t] : 0.f;
+          const float hi = i + 1 <= row ? tv[2 * t + 1] * bv[2 * t + 1] : 0.f;
+          w[t] = pack_bf16x2(lo, hi);
+        }
+        st_shared_v4(sb + SM_GB + OFF_TPRIME + sw128_offset(row, i0 * 2), w[0], w[1], w[2],
+                     w[3]);
+      }
+    }
+    fence_proxy_async_smem();
     cta_sync();
-    PHASE_MARK(8);
+    PHASE_MARK(6);
     if (tid == 0) {
       if (wait_bar(cx, &m.bar_v, par, 12, ci)) {
         m.tma_waited[TMA_V]++;
@@ -656,10 +692,10 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
     }
 
-    // ================= phase 8: -W -> stack rows 64.. (K-major); [O^T | D^T] = S^T [Qt; -W]^T
+    // ================= phase 6: -W -> stack rows 64.. (K-major); [O^T | D^T] = S^T [Qt; -W]^T
     wait_bar(cx, &m.bar_wu, par, 23, ci);
     tc_fence_after();
-    PHASE_MARK(9);
+    PHASE_MARK(7);
     if (tid == 0 && has_next) issue_v(ci + 1);
     {
       uint32_t r[32];
@@ -676,7 +712,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       fence_proxy_async_smem();
     }
     cta_sync();
-    PHASE_MARK(10);
+    PHASE_MARK(8);
     if (m.abort) { failed = true; break; }
     if (tid == 0) {
 #pragma unroll
@@ -685,11 +721,14 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 kdesc(smem + SM_STACK, (ks >> 2) * 16384u + (ks & 3) * 32u), ID_OM1, 1u);
       umma_commit(&m.bar_m1);
     }
+    // next chunk's decay prefix while the MMAs run
+    if (has_next) scan(ci + 1);
+    PHASE_MARK(9);
 
-    // ================= phase 9: bf16 Delta^T; [S^T | O^T] += Delta^T [Kdec | P]
+    // ================= phase 7: bf16 Delta^T; S^T += Delta^T Kdec; O^T += Delta^T P^T
     wait_bar(cx, &m.bar_m1, par, 24, ci);
     tc_fence_after();
-    PHASE_MARK(11);
+    PHASE_MARK(10);
     {
       uint32_t r[32];
       tmem_ld32(tmem_addr(tm, lane_base, TM_U + 32 * hf), r);
@@ -702,13 +741,15 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       tmem_st_wait();
     }
     cta_sync();
-    PHASE_MARK(12);
+    PHASE_MARK(11);
     if (m.abort) { failed = true; break; }
     if (tid == 0) {
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        umma_ts(tm + TM_S, tm + TM_AD + 8 * ks, mndesc(smem + SM_KDEC, ks * 2048u, 8192), ID_M2,
-                1u);
+      for (int ks = 0; ks < 4; ++ks) {
+        umma_ts(tm + TM_S, tm + TM_AD + 8 * ks, mndesc(smem + SM_KDEC, ks * 2048u, 8192),
+                ID_KM128, 1u);
+        umma_ts(tm + TM_O, tm + TM_AD + 8 * ks, kdesc(smem + SM_PMAT, ks * 32u), ID_KK64, 1u);
+      }
       umma_commit(&m.bar_m2);
     }
     prev_tb = tb;
@@ -719,7 +760,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   if (!failed && n_chunks > 0) {
     wait_bar(cx, &m.bar_m2, (uint32_t)((n_chunks - 1) & 1), 26, n_chunks - 1);
     tc_fence_after();
-    flush_output(prev_tb, prev_nv);
+    if (warp >= 4) flush_output(prev_tb, prev_nv);
   }
   cta_sync();
   if (!failed && !m.abort) {
