@@ -11,6 +11,7 @@ constexpr int kHeadDim = 128;    // dk = dv = 128 (KDA head dimension of K3)
 constexpr int kChunk = 64;       // tokens per chunk of the tensor-core prefill
 constexpr int kChunkF32 = 32;    // tokens per chunk of the fp32 CUDA-core prefill
 constexpr size_t kStatusBytes = 256;  // device status block at the start of the workspace
+constexpr int kNoAllocMaxSeqs = 4095;  // sequence limit of kda_chunk_fwd_noalloc
 
 // Device status block, first bytes of the kda_chunk_fwd workspace.
 struct DeviceStatus {

@@ -28,7 +28,8 @@ HEAD_DIM = 128
 
 # Symbols declared in include/kda.h.
 EXPORTED = ("kda_status_string", "kda_version", "kda_chunk_fwd_workspace_size",
-            "kda_chunk_fwd", "kda_read_device_status", "kda_decode_step")
+            "kda_chunk_fwd", "kda_read_device_status", "kda_decode_step",
+            "kda_chunk_fwd_noalloc")
 
 _lib = None
 
@@ -64,6 +65,9 @@ def library() -> ctypes.CDLL:
                                       ctypes.c_int, vp, vp, vp, sz, vp]
         lib.kda_read_device_status.restype = ctypes.c_int
         lib.kda_read_device_status.argtypes = [vp, vp, ctypes.c_int, ctypes.POINTER(i32)]
+        lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
+        lib.kda_chunk_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32,
+                                              ctypes.c_int, vp, vp, vp]
         lib.kda_decode_step.restype = ctypes.c_int
         lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                         ctypes.c_int, vp, vp]
@@ -164,6 +168,36 @@ def kda_chunk_fwd(q, k, v, log_alpha, beta, init_state=None, cu_seqlens=None, *,
                                  workspace.numel() * workspace.element_size(),
                                  _stream_handle(stream))
     _check(rc, "kda_chunk_fwd")
+    return out, final_state
+
+
+def kda_chunk_fwd_noalloc(q, k, v, log_alpha, beta, init_state=None, cu_seqlens=None, *,
+                          out=None, final_state=None, output_final_state=True, stream=None):
+    """kda_chunk_fwd without a workspace: the library's fixed device scratch is
+    used instead (at most 4095 sequences; concurrent calls on different streams
+    race on that scratch).  Same arguments and results as ``kda_chunk_fwd``."""
+    _need_cuda("q", q)
+    N, H, dk = q.shape
+    dt = q.dtype
+    _need_cuda("k", k, dt, (N, H, dk))
+    _need_cuda("v", v, dt)
+    dv = v.shape[2]
+    _need_cuda("log_alpha", log_alpha, torch.float32, (N, H, dk))
+    _need_cuda("beta", beta, torch.float32, (N, H))
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, N], dtype=torch.int32, device=q.device)
+    n_seqs = cu_seqlens.shape[0] - 1
+    if init_state is not None:
+        _need_cuda("init_state", init_state, torch.float32, (n_seqs, H, dk, dv))
+    if out is None:
+        out = torch.empty(N, H, dv, dtype=dt, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty(n_seqs, H, dk, dv, dtype=torch.float32, device=q.device)
+    rc = library().kda_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                         _ptr(init_state), _ptr(cu_seqlens), n_seqs, N, H, dk, dv,
+                                         _dtype_code(q), _ptr(out), _ptr(final_state),
+                                         _stream_handle(stream))
+    _check(rc, "kda_chunk_fwd_noalloc")
     return out, final_state
 
 

@@ -125,6 +125,35 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
                   size_t workspace_bytes, void *stream);
 
 /*
+ * kda_chunk_fwd without a workspace argument, for callers that cannot provide
+ * or allocate device memory for the library: for instance a serving engine
+ * whose framework allocator owns all device memory and forbids cudaMalloc or
+ * extra buffers outside its pool.  (Library-level entry point: the pages have
+ * no counterpart; it computes exactly what kda_chunk_fwd computes.)
+ *
+ * Arguments and errors are those of kda_chunk_fwd minus the workspace.  The
+ * scratch kda_chunk_fwd keeps in its workspace (device status block, device
+ * copy of a host cu_seqlens) lives instead in one fixed-size device array
+ * inside libkda, which every GPU that loads the library holds until process
+ * exit.  Nothing is allocated or freed by the call.
+ *   - At most 4095 sequences per call; more returns KDA_ERR_WORKSPACE and
+ *     launches nothing.
+ *   - The array is shared by every call on a device and keeps the last call's
+ *     contents (the status block is cleared, stream-ordered, by each call).
+ *     Calls that overlap on the GPU race on it: issue them on one stream or
+ *     serialise them.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, once per device); make that first call before
+ *     any stream capture begins.
+ *   - The device status recorded by the kernels stays in the library's array;
+ *     it is not readable through this entry point.
+ */
+int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *log_alpha,
+                          const float *beta, const float *init_state, const int32_t *cu_seqlens,
+                          int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk, int32_t dv,
+                          int dtype, void *out, float *final_state, void *stream);
+
+/*
  * Reads (and, if `clear` is non-zero, resets) the device status word of a
  * kda_chunk_fwd workspace.  Synchronises `stream` first, so it reports the
  * status of every call issued on that stream before it.  *device_status gets
