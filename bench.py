@@ -47,6 +47,22 @@ def load_peaks():
             "source": "fallback"}
 
 
+def recorded_traffic(kernel: str, source: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary (profiles/traffic.txt),
+    or None when the kernel source changed since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    src = os.path.join(ROOT, "gated_delta_rule_13_gb300", "csrc", source)
+    if not (os.path.exists(path) and os.path.exists(src)):
+        return None
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for line in open(path):
+        f = line.split()
+        if len(f) == 4 and not line.startswith("#") and f[0] == kernel and f[2] == workload:
+            return int(f[3]) if f[1] == digest else None
+    return None
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -326,7 +342,9 @@ def run_gpu(args):
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "kernel": "kda_chunk_fwd_tc_kernel",
                      "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": None,
+                     "frac": achieved_gbs / peaks["hbm_gbs"],
+                     "traffic": recorded_traffic("kda_chunk_fwd_tc_kernel", "kda_chunk_tc.cu",
+                                                 args.workload),
                      "peak_source": peaks["source"], "bytes_per_launch": pbytes,
                      "ms_per_launch": pre_avg,
                      "tensor_tflops": pflop / (pre_avg / 1000.0) / 1e12,
@@ -335,7 +353,9 @@ def run_gpu(args):
                    "tokens_per_s": dw.B / (dec_avg / 1000.0),
                    "roofline": {"bound": "hbm", "kernel": "kda_decode_step_kernel",
                                 "achieved": dec_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                "frac": dec_gbs / peaks["hbm_gbs"], "traffic": None,
+                                "frac": dec_gbs / peaks["hbm_gbs"],
+                                "traffic": recorded_traffic("kda_decode_step_kernel",
+                                                            "kda_decode.cu", "decode_b512_h96"),
                                 "bytes_per_launch": dbytes}},
         "cpu_baseline": cpu,
         "e2e": e2e,

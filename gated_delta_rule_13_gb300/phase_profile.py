@@ -1,0 +1,69 @@
+"""Per-phase cycle breakdown of the tensor-core prefill kernel.
+
+Builds a separate copy of libkda with ``-DKDA_PHASE_PROFILE`` (the kernel then
+stamps ``clock64()`` at its phase boundaries for chain 0) into
+``gated_delta_rule_13_gb300/_build/prof/``, runs one workload twice and prints
+the median cycles of every phase over the chunks of chain 0.  The normal library
+is not touched.
+
+    python -m gated_delta_rule_13_gb300.phase_profile [workload]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import sys
+
+from . import _build
+
+# Phase boundaries stamped by the kernel (PHASE_MARK indices 0..11).
+PHASES = ["wait m2(prev) + sync", "build all tiles", "S pass + wait gp", "A/P epilogue",
+          "inverse || flush(prev)", "T' + sync", "wait wu (U/W)", "W epilogue", "scan(next)",
+          "wait m1 (O+M1)", "Delta + sync", "M2 issue -> next chunk"]
+
+
+def build_profiling_library() -> str:
+    out = os.path.join(_build.OBJ_DIR, "prof")
+    os.makedirs(out, exist_ok=True)
+    objs = []
+    for src in _build.sources():
+        obj = os.path.join(out, os.path.basename(src)[:-3] + ".o")
+        subprocess.run([_build.nvcc(), *_build.ARCH, *_build.NVCC_FLAGS, "-DKDA_PHASE_PROFILE",
+                        "-c", src, "-o", obj], check=True)
+        objs.append(obj)
+    lib = os.path.join(out, "libkda_prof.so")
+    subprocess.run([_build.nvcc(), *_build.ARCH, "-shared", "-o", lib, *objs, "-cudart",
+                    "static"], check=True)
+    return lib
+
+
+def main(workload: str = "k3_h96_t32768") -> None:
+    import numpy as np
+    import torch
+
+    from . import inputs, kda
+
+    _build.LIB_PATH = build_profiling_library()
+    x = inputs.workload_inputs(workload, device="cuda")
+    for _ in range(2):
+        kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["init_state"],
+                          x["cu_seqlens"])
+    torch.cuda.synchronize()
+    n_chunks = min(4096, (int(x["lengths"][0]) + 63) // 64)
+    buf = (ctypes.c_longlong * (4096 * 16))()
+    kda.library().kda_debug_phase_clock(buf, 4096 * 16)
+    stamps = np.array(buf[:], dtype=np.int64).reshape(4096, 16)[:n_chunks, :len(PHASES)]
+    # interval k = stamp k+1 - stamp k; the last one runs to the next chunk's stamp 0
+    nxt = np.concatenate([stamps[1:, :1], stamps[-1:, :1]])
+    d = np.diff(np.concatenate([stamps, nxt], axis=1), axis=1)[1:-1]
+    med = np.median(d, axis=0)
+    total = med.sum()
+    print(f"{workload}: median cycles per chunk of chain 0 over {d.shape[0]} chunks")
+    for name, v in zip(PHASES, med):
+        print(f"  {name:28s} {v:8.0f}  {100 * v / total:5.1f}%")
+    print(f"  {'total per chunk':28s} {total:8.0f}")
+
+
+if __name__ == "__main__":
+    main(*sys.argv[1:2])
