@@ -67,21 +67,21 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Shared memory map (byte offsets from a 1024-byte aligned base).  Operand
 // tiles use 128-byte rows with the 128-byte swizzle; a "K-major tile of R rows"
 // stores columns 0-63 as R rows of 128 B, then columns 64-127 likewise.
-constexpr uint32_t SM_Q = 0;                    // q chunk (TMA), 64 rows
+constexpr uint32_t SM_Q = 0;                    // q chunk (TMA), 64 rows; then output staging
 constexpr uint32_t SM_K = SM_Q + 16384;         // k chunk (TMA), 64 rows
 constexpr uint32_t SM_V = SM_K + 16384;         // v chunk (TMA), 64 rows
-constexpr uint32_t SM_LA = SM_V + 16384;        // log_alpha fp32 [64][128]; then output staging
+constexpr uint32_t SM_LA = SM_V + 16384;        // log_alpha fp32 [64][128]
 constexpr uint32_t SM_GA = SM_LA + 32768;       // Gram rows [K o E; Q o E], 128 rows; then A^T fp32
 constexpr uint32_t SM_GB = SM_GA + 32768;       // Gram columns, 160 rows; then T fp32, X, T'
 constexpr uint32_t SM_STACK = SM_GB + 40960;    // [Qt; Kt -> -W], 128 rows
 constexpr uint32_t SM_KDEC = SM_STACK + 32768;  // K o e^{g_C - g}, 64 rows (MN-major operand)
 constexpr uint32_t SM_PMAT = SM_KDEC + 16384;   // P, K-major [64 r][64 i]
-constexpr uint32_t SM_MISC = SM_PMAT + 8192;
+constexpr uint32_t SM_TMAT = SM_PMAT + 8192;    // T' = T Diag(beta), K-major [64 r][64 i]
+constexpr uint32_t SM_MISC = SM_TMAT + 8192;
 
 constexpr uint32_t GB_ROWS = 160;
 constexpr uint32_t OFF_TINV = 0;               // inside SM_GB, after the Gram MMAs
 constexpr uint32_t OFF_XBUF = 64 * 72 * 4;   // 4 blocks of 16 x XP fp32
-constexpr uint32_t OFF_TPRIME = 24576;
 constexpr int FP = 72;  // pitch (floats) of the fp32 64 x 64 matrices of the solve
 constexpr int XP = 24;  // pitch (floats) of the 16 x 16 intermediate blocks
 
@@ -100,8 +100,7 @@ struct Misc {
 constexpr uint32_t SMEM_BYTES = SM_MISC + sizeof(Misc);
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(64 * FP * 4 <= 32768, "A^T fits SM_GA");
-static_assert(OFF_XBUF + 4 * 16 * XP * 4 <= OFF_TPRIME && OFF_TPRIME + 8192 <= 40960,
-              "T, X blocks and T' fit SM_GB");
+static_assert(OFF_XBUF + 4 * 16 * XP * 4 <= 40960, "T and X blocks fit SM_GB");
 
 // TMEM columns (fp32 cells).
 constexpr uint32_t TM_S = 0;     // S^T, 128 columns
@@ -256,8 +255,8 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     tmem_alloc(&m.tmem_base, TM_COLS);
     tmem_relinquish();
   }
-  // P blocks above the diagonal are never written: zero the tile once.
-  for (int e = tid; e < 8192 / 16; e += kThreads) st_shared_v4(sb + SM_PMAT + 16 * e, 0, 0, 0, 0);
+  // P and T' blocks above the diagonal are never written: zero both tiles once.
+  for (int e = tid; e < 2 * 8192 / 16; e += kThreads) st_shared_v4(sb + SM_PMAT + 16 * e, 0, 0, 0, 0);
   if (tid < C) m.beta[0][tid] = (n_chunks > 0 && tid < len) ? beta[(t0 + tid) * H + h] : 0.f;
   cta_sync();
   const uint32_t tm = m.tmem_base;
@@ -316,10 +315,10 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   cta_sync();
 
   // Writes the output rows of a finished chunk (warps 4-7 only): O^T (TMEM) ->
-  // bf16 staging in the log_alpha tile (free between the scan and the next
-  // log_alpha load) -> coalesced 16-byte stores; clears O^T for the next chunk.
+  // bf16 staging in the q tile (free between the operand build and the next q
+  // load) -> coalesced 16-byte stores; clears O^T for the next chunk.
   auto flush_output = [&](int64_t otb, int onv) {
-    __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(smem + SM_LA);
+    __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(smem + SM_Q);
     const int n = lane_base + lane;
     uint32_t z[32];
 #pragma unroll
@@ -336,7 +335,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     tmem_st_wait();
     named_sync(2, 128);
-    const uint4 *s4 = reinterpret_cast<const uint4 *>(smem + SM_LA);
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(smem + SM_Q);
     const int t = tid - 128;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -352,13 +351,16 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   // Tile-local prefix of the log2-decay of chunk `ci` into registers; thread
   // (tile ta, channel pair cp) owns rows 16 ta .. 16 ta + 15 of channels cc, cc+1.
   const int ta = tid >> 6, cp = tid & 63, cc = 2 * cp;
+  const uint32_t hsel = (uint32_t)(cc >> 6), cb = (uint32_t)(cc & 63) * 2u;
+  uint32_t swzk[8];   // swizzled byte offset of channel pair cc in a row with row % 8 == k
+#pragma unroll
+  for (int k = 0; k < 8; ++k) swzk[k] = ((((cb >> 4) ^ (uint32_t)k) << 4) | (cb & 15u));
   float L0[16], L1[16];
   float beta_next = 0.f;
   auto scan = [&](int ci) -> bool {
     const uint32_t par = (uint32_t)(ci & 1);
     const int64_t tb = t0 + (int64_t)C * ci;
     const int nv = (int)((len - (int64_t)C * ci) < C ? (len - (int64_t)C * ci) : C);
-    const bool ok_qk = wait_bar(cx, &m.bar_qk, par, 10, ci);
     const bool ok_la = wait_bar(cx, &m.bar_la, par, 11, ci);
     if (ci + 1 < n_chunks && tid < C) {   // prefetch the following chunk's beta
       const int64_t len_next = len - (int64_t)C * (ci + 1);
@@ -377,11 +379,8 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       L1[j] = s1;
     }
     *reinterpret_cast<float2 *>(&m.tot[ta][cc]) = make_float2(s0, s1);
-    if (tid == 0) {
-      if (ok_qk) m.tma_waited[TMA_QK]++;
-      if (ok_la) m.tma_waited[TMA_LA]++;
-    }
-    return ok_qk && ok_la;
+    if (tid == 0 && ok_la) m.tma_waited[TMA_LA]++;
+    return ok_la;
   };
 
   bool failed = false;
@@ -402,9 +401,12 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     cta_sync();     // tile totals of this chunk visible
     PHASE_MARK(1);
     if (m.abort) { failed = true; break; }
+    if (tid == 0 && ci == 0 && n_chunks > 1) issue_la(1);   // log_alpha tile scanned
 
     // ================= phase 2: every operand tile of the chunk in one pass
     {
+      const bool ok_qk = wait_bar(cx, &m.bar_qk, par, 10, ci);
+      if (tid == 0 && ok_qk) m.tma_waited[TMA_QK]++;
       float st0[4], st1[4], rf0[4], rf1[4];   // tile starts / ends, channels c, c+1
       {
         float acc0 = 0.f, acc1 = 0.f;
@@ -434,26 +436,39 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         m.gamma[cc] = ex2(rf0[3]);
         m.gamma[cc + 1] = ex2(rf1[3]);
       }
+      // Row-tile bases (column half of cc, first row of tile ta); element (row
+      // 16 ta + j) sits j * 128 + swzk[j & 7] bytes further (128-byte swizzle).
+      const uint32_t r0 = 16u * ta * 128u, h64 = hsel * 8192u, h128 = hsel * 16384u;
+      const uint32_t bK = sb + SM_K + h64 + r0, bQ = sb + SM_Q + h64 + r0;
+      const uint32_t bGA = sb + SM_GA + h128 + r0, bST = sb + SM_STACK + h128 + r0;
+      const uint32_t bKD = sb + SM_KDEC + h64 + r0;
+      const uint32_t bGB = sb + SM_GB + hsel * (GB_ROWS * 128u) + r0;
+      uint32_t kraw[16], qraw[16];   // all k, q pairs of this thread, loaded up front
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        const int row = 16 * ta + j;
-        const float2 kk = ld_pair(smem + SM_K, 64, row, cc);
-        const float2 qq = ld_pair(smem + SM_Q, 64, row, cc);
+        kraw[j] = ld_shared_b32(bK + (uint32_t)j * 128u + swzk[j & 7]);
+        qraw[j] = ld_shared_b32(bQ + (uint32_t)j * 128u + swzk[j & 7]);
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t o = (uint32_t)j * 128u + swzk[j & 7];
+        const float2 kk = unpack_bf16x2(kraw[j]);
+        const float2 qq = unpack_bf16x2(qraw[j]);
         const float e0 = ex2(L0[j]), e1 = ex2(L1[j]);                    // e^{g_r - st_a}
         const float ec0 = ex2(tot0 - L0[j]), ec1 = ex2(tot1 - L1[j]);    // e^{ref_a - g_r}
-        st_pair(smem + SM_GA, 128, row, cc, kk.x * e0, kk.y * e1);
-        st_pair(smem + SM_GA, 128, 64 + row, cc, qq.x * e0, qq.y * e1);
+        st_shared_b32(bGA + o, pack_bf16x2(kk.x * e0, kk.y * e1));
+        st_shared_b32(bGA + 8192u + o, pack_bf16x2(qq.x * e0, qq.y * e1));
         const float kc0 = kk.x * ec0, kc1 = kk.y * ec1;
 #pragma unroll
-        for (int a2 = 0; a2 < 4; ++a2) {
+        for (int a2 = 0; a2 < 4; ++a2) {   // block (a2, ta) of the column operand, row j
           if (a2 < ta) continue;
-          const int brow = 16 * blk(a2, 0) + 16 * ta + j;   // block (a2, ta), row j
-          st_pair(smem + SM_GB, GB_ROWS, brow, cc, kc0 * fb0[a2], kc1 * fb1[a2]);
+          st_shared_b32(bGB + 16u * blk(a2, 0) * 128u + o,
+                        pack_bf16x2(kc0 * fb0[a2], kc1 * fb1[a2]));
         }
         const float g0 = e0 * fs0, g1 = e1 * fs1;                        // e^{g_r}
-        st_pair(smem + SM_STACK, 128, row, cc, qq.x * g0, qq.y * g1);
-        st_pair(smem + SM_STACK, 128, 64 + row, cc, kk.x * g0, kk.y * g1);
-        st_pair(smem + SM_KDEC, 64, row, cc, kc0 * fd0, kc1 * fd1);
+        st_shared_b32(bST + o, pack_bf16x2(qq.x * g0, qq.y * g1));
+        st_shared_b32(bST + 8192u + o, pack_bf16x2(kk.x * g0, kk.y * g1));
+        st_shared_b32(bKD + o, pack_bf16x2(kc0 * fd0, kc1 * fd1));
       }
     }
     fence_proxy_async_smem();
@@ -469,7 +484,6 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         umma_ss(tm + TM_GP, ad, bd, ID_GP, ks > 0 ? 1u : 0u);
       }
       umma_commit(&m.bar_gp);
-      if (has_next) issue_qk(ci + 1);   // q, k consumed
     }
 
     // ================= phase 3 (while the Gram MMAs run): S pass, previous output
@@ -567,17 +581,30 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         float t[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) t[r] = (r == j) ? 1.f : 0.f;
+        float col[16], nxt[16];   // column mc of the block, and the next one in flight
+        ld8(*reinterpret_cast<float(*)[8]>(col), amatT + b0 * FP + b0);
+        ld8(*reinterpret_cast<float(*)[8]>(col + 8), amatT + b0 * FP + b0 + 8);
 #pragma unroll
         for (int mc = 0; mc < 15; ++mc) {
-          float col[16];
-          ld8(*reinterpret_cast<float(*)[8]>(col), amatT + (b0 + mc) * FP + b0);
-          ld8(*reinterpret_cast<float(*)[8]>(col + 8), amatT + (b0 + mc) * FP + b0 + 8);
+          if (mc + 1 < 15) {
+            ld8(*reinterpret_cast<float(*)[8]>(nxt), amatT + (b0 + mc + 1) * FP + b0);
+            ld8(*reinterpret_cast<float(*)[8]>(nxt + 8), amatT + (b0 + mc + 1) * FP + b0 + 8);
+          }
           const float tmv = t[mc];
 #pragma unroll
           for (int r = mc + 1; r < 16; ++r) t[r] = fmaf(-col[r], tmv, t[r]);
-        }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) tinv[(b0 + r) * FP + b0 + j] = t[r];
+          for (int r = 0; r < 16; ++r) col[r] = nxt[r];
+        }
+        // T (fp32, for the block recursion) and T' = T Diag(beta) (bf16 MMA operand;
+        // the block's upper triangle is zero because t[r] = 0 for r < j).
+        const float bj = bcur[b0 + j];
+        __nv_bfloat16 *tp = reinterpret_cast<__nv_bfloat16 *>(smem + SM_TMAT);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          tinv[(b0 + r) * FP + b0 + j] = t[r];
+          tp[sw128_offset(b0 + r, (b0 + j) * 2) >> 1] = __float2bfloat16_rn(t[r] * bj);
+        }
       }
       named_sync(1, 128);
       // Off-diagonal blocks, block-recursive: 16 -> 32 (blocks (1,0), (3,2)), then
@@ -622,6 +649,19 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           dst[(g + 8) * pitch + 8 * nh + 2 * t4 + 1] = sgn * acc[nh][3];
         }
       };
+      // Final block T_ab: fp32 into T, and T' = T Diag(beta) as bf16 pairs.
+      auto store_T = [&](int ab, int bb, const float (&acc)[2][4]) {
+        store_blk(tinv + (16 * ab) * FP + 16 * bb, FP, acc, -1.f);
+#pragma unroll
+        for (int nh = 0; nh < 2; ++nh) {
+          const int col = 16 * bb + 8 * nh + 2 * t4;
+          const float b0v = bcur[col], b1v = bcur[col + 1];
+          const uint32_t lo = pack_bf16x2(-acc[nh][0] * b0v, -acc[nh][1] * b1v);
+          const uint32_t hi = pack_bf16x2(-acc[nh][2] * b0v, -acc[nh][3] * b1v);
+          *reinterpret_cast<uint32_t *>(smem + SM_TMAT + sw128_offset(16 * ab + g, col * 2)) = lo;
+          *reinterpret_cast<uint32_t *>(smem + SM_TMAT + sw128_offset(16 * ab + g + 8, col * 2)) = hi;
+        }
+      };
       float *xw = xbuf + warp * 16 * XP;
       if (warp < 2) {   // level 16 -> 32: block (1,0) on warp 0, (3,2) on warp 1
         const int ab = 2 * warp + 1, bb = 2 * warp;
@@ -631,7 +671,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         __syncwarp();
         float o[2][4] = {};
         mul_TX(o, ab, ab, xw);                        // T_ab = -T_aa X
-        store_blk(tinv + (16 * ab) * FP + 16 * bb, FP, o, -1.f);
+        store_T(ab, bb, o);
       }
       named_sync(1, 128);
       {                 // level 32 -> 64: warp w -> block (2 + w/2, w%2)
@@ -644,36 +684,17 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         // T_{ab} = -sum_{k=2}^{ab} T_{ab,k} X_{k,bb}
         float o[2][4] = {};
         for (int k = 2; k <= ab; ++k) mul_TX(o, ab, k, xbuf + (2 * (k - 2) + bb) * 16 * XP);
-        store_blk(tinv + (16 * ab) * FP + 16 * bb, FP, o, -1.f);
+        store_T(ab, bb, o);
       }
+      fence_proxy_async_smem();   // T' is an MMA operand
     } else {
       if (ci > 0) flush_output(prev_tb, prev_nv);
+      named_sync(2, 128);   // output staging (q tile) read by warps 4-7
+      if (tid == 128 && has_next) issue_qk(ci + 1);
     }
     __syncthreads();
     PHASE_MARK(5);
-    if (tid == 0 && has_next) issue_la(ci + 1);   // output staging read
 
-    // T' = T Diag(beta) -> bf16, K-major [r][i]; upper triangle zero.
-    {
-      const int row = tid >> 2, qd = tid & 3;
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int i0 = 16 * qd + 8 * hh;
-        float tv[8], bv[8];
-        ld8(tv, tinv + row * FP + i0);
-        ld8(bv, &bcur[i0]);
-        uint32_t w[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const int i = i0 + 2 * t;
-          const float lo = i <= row ? tv[2 * t] * bv[2 * t] : 0.f;
-          const float hi = i + 1 <= row ? tv[2 * t + 1] * bv[2 * t + 1] : 0.f;
-          w[t] = pack_bf16x2(lo, hi);
-        }
-        st_shared_v4(sb + SM_GB + OFF_TPRIME + sw128_offset(row, i0 * 2), w[0], w[1], w[2],
-                     w[3]);
-      }
-    }
     fence_proxy_async_smem();
     cta_sync();
     PHASE_MARK(6);
@@ -683,7 +704,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {   // U^T = V^T T'^T ; W^T = Kt^T T'^T, interleaved
-          const uint64_t bd = kdesc(smem + SM_GB, OFF_TPRIME + ks * 32u);
+          const uint64_t bd = kdesc(smem + SM_TMAT, ks * 32u);
           umma_ss(tm + TM_U, mndesc(smem + SM_V, ks * 2048u, 8192), bd, ID_UW, ks > 0);
           umma_ss(tm + TM_W, mndesc(smem + SM_STACK, 64u * 128u + ks * 2048u, 16384), bd, ID_UW,
                   ks > 0);
@@ -696,18 +717,21 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     wait_bar(cx, &m.bar_wu, par, 23, ci);
     tc_fence_after();
     PHASE_MARK(7);
-    if (tid == 0 && has_next) issue_v(ci + 1);
+    if (tid == 128 && has_next) issue_v(ci + 1);
     {
       uint32_t r[32];
       tmem_ld32(tmem_addr(tm, lane_base, TM_W + 32 * hf), r);
       tmem_ld_wait(r);
       const int c = lane_base + lane;   // key channel of this lane; W^T columns are rows r
-      __nv_bfloat16 *stk = reinterpret_cast<__nv_bfloat16 *>(smem + SM_STACK);
-      const uint32_t cbyte = (uint32_t)(c & 63) * 2u, chalf = (uint32_t)(c >> 6) * 16384u;
+      const uint32_t cbyte = (uint32_t)(c & 63) * 2u;
+      const uint32_t base = sb + SM_STACK + (uint32_t)(c >> 6) * 16384u + (64u + 32u * hf) * 128u;
+      uint32_t sw[8];   // swizzled byte offset of channel c in a row with row % 8 == k
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sw[k] = ((((cbyte >> 4) ^ (uint32_t)k) << 4) | (cbyte & 15u));
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const int row = 64 + 32 * hf + j;
-        stk[(chalf + sw128_offset(row, cbyte)) >> 1] = __float2bfloat16_rn(-__uint_as_float(r[j]));
+        const __nv_bfloat16 w = __float2bfloat16_rn(-__uint_as_float(r[j]));
+        st_shared_b16(base + (uint32_t)j * 128u + sw[j & 7], *reinterpret_cast<const uint16_t *>(&w));
       }
       fence_proxy_async_smem();
     }
@@ -751,6 +775,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         umma_ts(tm + TM_O, tm + TM_AD + 8 * ks, kdesc(smem + SM_PMAT, ks * 32u), ID_KK64, 1u);
       }
       umma_commit(&m.bar_m2);
+      if (ci + 2 < n_chunks) issue_la(ci + 2);   // the next chunk's tile was scanned above
     }
     prev_tb = tb;
     prev_nv = nv;

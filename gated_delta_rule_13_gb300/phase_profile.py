@@ -19,7 +19,7 @@ from . import _build
 
 # Phase boundaries stamped by the kernel (PHASE_MARK indices 0..11).
 PHASES = ["wait m2(prev) + sync", "build all tiles", "S pass + wait gp", "A/P epilogue",
-          "inverse || flush(prev)", "T' + sync", "wait wu (U/W)", "W epilogue", "scan(next)",
+          "solve + T' || flush(prev)", "sync", "wait wu (U/W)", "W epilogue", "scan(next)",
           "wait m1 (O+M1)", "Delta + sync", "M2 issue -> next chunk"]
 
 
