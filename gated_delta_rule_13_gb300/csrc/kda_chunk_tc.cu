@@ -1,19 +1,21 @@
 // bf16 chunkwise KDA prefill on the 5th-generation tensor cores (tcgen05).
 //
-// One CTA (8 warps) carries one (sequence, head) chain through chunks of C = 64
-// tokens.  The fp32 state lives in tensor memory for the whole chain; every
-// dense contraction of a chunk is a tcgen05.mma (bf16 operands, fp32 TMEM
-// accumulators); q, k, v and log_alpha tiles arrive by TMA with a 128-byte
-// swizzle, prefetched one chunk ahead.
+// One CTA carries one (sequence, head) chain through chunks of C = 64 tokens.
+// Eight compute warps do the CUDA-core work; a ninth warp issues every TMA load
+// and every tcgen05.mma, so no compute warp ever blocks on an MMA issue.  The
+// fp32 state lives in tensor memory for the whole chain; every dense
+// contraction of a chunk is a tcgen05.mma (bf16 operands, fp32 accumulators).
 //
 // Chunk algebra ("Kimi K3: 架构、训练与系统全景解析", section 4.2.4: state passed
 // between chunks, lower-triangular matrix work inside, output = pre-chunk-state
 // term + intra-chunk causal term; UT-transform form of the solve), with g_r the
 // within-chunk cumulative log-decay per key channel and S the incoming state:
 //   A = strict_lower(Diag(beta) [k_r . k_i e^{g_r - g_i}]),  T = (I + A)^{-1}
-//   T' = T Diag(beta),  U = T' V,  W = T' (K o e^{g})
-//   Delta = U - W S,  O = (Q o e^{g}) S + P Delta,  P = lower_incl([q_r . k_i e^{g_r - g_i}])
+//   T' = T Diag(beta),  Kt = K o e^{g},  Qt = Q o e^{g},  Y = Kt S
+//   Delta = T' (V - Y),  O = Qt S + P Delta,  P = lower_incl([q_r . k_i e^{g_r - g_i}])
 //   S <- Diag(e^{g_C}) S + (K o e^{g_C - g})^T Delta
+// (Delta = T'V - T'Kt S is the usual U - W S with U = T'V and W = T'Kt, taken
+// in the other association so that W never has to be formed.)
 //
 // Decay factorisation on tensor cores.  With 16-token tiles a, b and per-channel
 // tile starts st_a / ends ref_b of the cumulative log-decay,
@@ -32,14 +34,17 @@
 //
 // TMEM orientation: the state is held transposed (S^T: lane = value index n,
 // column = key index c), so every state-side product is an M = 128 MMA:
-//   U^T  = V^T T'^T                 (A = V, smem MN-major;  B = T', K-major)
-//   W^T  = Kt^T T'^T                (A = Kt, smem MN-major)
-//   [O^T | D^T] = S^T [Qt; -W]^T    (A = bf16 S^T in TMEM; D^T accumulates onto U^T)
-//   S^T += Delta^T Kdec, O^T += Delta^T P^T   (A = bf16 Delta^T in TMEM),
+//   O^T = S^T Qt^T,  Y^T = S^T Kt^T      (A = bf16 S^T in TMEM)
+//   Delta^T = V^T T'^T + (-Y)^T T'^T      (A = V in smem, then bf16 -Y^T in TMEM)
+//   S^T += Delta^T Kdec,  O^T += Delta^T P^T   (A = bf16 Delta^T in TMEM),
 //                                    after S^T <- S^T Diag(e^{g_C})
-// where D = Delta = U - W S.  32 tcgen05.mma instructions per chunk.  The
-// triangular solve (warps 0-3) overlaps the previous chunk's output stores
-// (warps 4-7), and the next chunk's decay prefix overlaps the state MMAs.
+// The products with the lower-triangular T' and P skip the zero blocks: K step
+// s only touches output columns r >= 16 s.
+//
+// Pipeline.  O^T is double-buffered in TMEM and Kdec in shared memory, so the
+// next chunk's operand build overlaps this chunk's state MMAs, the triangular
+// solve (warps 0-3) overlaps the previous chunk's output stores and the -Y pass
+// (warps 4-7), and the Gram MMAs of chunk c+1 overlap the state pass of c+1.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -60,38 +65,45 @@ using namespace sm100;
 
 constexpr int D = kHeadDim;  // 128
 constexpr int C = kChunk;    // 64
-constexpr int kThreads = 256;
+constexpr int kComputeWarps = 8;                   // warpgroups 0 and 1
+constexpr int kMmaWarp = kComputeWarps;            // warp 8: TMA + MMA issue (warps 9-11 idle)
+constexpr int kThreads = 32 * (kComputeWarps + 4);  // 384: three whole warpgroups
+// Register split (setmaxnreg): the launch gives every thread 65536 / 384 = 168;
+// the issue warpgroup returns most of its share to the compute warpgroups.
+constexpr uint32_t kLaunchRegs = 168, kComputeRegs = 208, kIssueRegs = 88;
+static_assert(256 * kComputeRegs + 128 * kIssueRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr uint64_t kWaitNs = 2000000000ull;  // bound on any single wait: 2 s
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Shared memory map (byte offsets from a 1024-byte aligned base).  Operand
 // tiles use 128-byte rows with the 128-byte swizzle; a "K-major tile of R rows"
 // stores columns 0-63 as R rows of 128 B, then columns 64-127 likewise.
-constexpr uint32_t SM_Q = 0;                    // q chunk (TMA), 64 rows; then output staging
+constexpr uint32_t SM_Q = 0;                    // q chunk (TMA), 64 rows
 constexpr uint32_t SM_K = SM_Q + 16384;         // k chunk (TMA), 64 rows
 constexpr uint32_t SM_V = SM_K + 16384;         // v chunk (TMA), 64 rows
-constexpr uint32_t SM_LA = SM_V + 16384;        // log_alpha fp32 [64][128]
-constexpr uint32_t SM_GA = SM_LA + 32768;       // Gram rows [K o E; Q o E], 128 rows; then A^T fp32
-constexpr uint32_t SM_GB = SM_GA + 32768;       // Gram columns, 160 rows; then T fp32, X, T'
-constexpr uint32_t SM_STACK = SM_GB + 40960;    // [Qt; Kt -> -W], 128 rows
-constexpr uint32_t SM_KDEC = SM_STACK + 32768;  // K o e^{g_C - g}, 64 rows (MN-major operand)
-constexpr uint32_t SM_PMAT = SM_KDEC + 16384;   // P, K-major [64 r][64 i]
-constexpr uint32_t SM_TMAT = SM_PMAT + 8192;    // T' = T Diag(beta), K-major [64 r][64 i]
-constexpr uint32_t SM_MISC = SM_TMAT + 8192;
+constexpr uint32_t SM_LA = SM_V + 16384;        // log_alpha fp32 [64][128]; then tile totals
+constexpr uint32_t SM_GA = SM_LA + 32768;       // Gram rows, 128 rows; then A^T fp32
+constexpr uint32_t SM_GB = SM_GA + 32768;       // Gram columns, 160 rows; then T, X, T'
+constexpr uint32_t SM_STACK = SM_GB + 40960;    // [Qt; Kt], 128 rows
+constexpr uint32_t SM_KDEC = SM_STACK + 32768;  // 2 x (K o e^{g_C - g}), 64 rows (MN-major)
+constexpr uint32_t SM_PMAT = SM_KDEC + 32768;   // P, K-major [64 r][64 i]
+constexpr uint32_t SM_MISC = SM_PMAT + 8192;
 
 constexpr uint32_t GB_ROWS = 160;
-constexpr uint32_t OFF_TINV = 0;               // inside SM_GB, after the Gram MMAs
-constexpr uint32_t OFF_XBUF = 64 * 72 * 4;   // 4 blocks of 16 x XP fp32
 constexpr int FP = 72;  // pitch (floats) of the fp32 64 x 64 matrices of the solve
 constexpr int XP = 24;  // pitch (floats) of the 16 x 16 intermediate blocks
-
+constexpr uint32_t OFF_TINV = 0;                     // inside SM_GB, after the Gram MMAs
+constexpr uint32_t OFF_XBUF = 64 * FP * 4;           // 4 blocks of 16 x XP fp32
+constexpr uint32_t OFF_TMAT = OFF_XBUF + 4 * 16 * XP * 4;  // T' = T Diag(beta), K-major
+constexpr uint32_t SM_TMAT = SM_GB + OFF_TMAT;
 
 struct Misc {
-  float beta[2][C];           // beta of the current chunk and the prefetched next one
-  float tot[4][D];            // per-tile total log2-decay
-  float gamma[D];             // Gamma_C = e^{g_C} per key channel
-  uint64_t bar_qk, bar_la, bar_v;               // TMA arrivals
-  uint64_t bar_gp, bar_wu, bar_m1, bar_m2, bar_fin;  // MMA completions
+  float beta[2][C];  // beta of the chunk in flight and of the next one
+  float gamma[D];    // Gamma_C = e^{g_C} per key channel
+  uint64_t bar_qk, bar_la, bar_v;                     // TMA arrivals
+  uint64_t bar_gp, bar_m1, bar_u, bar_m2, bar_fin;    // MMA completions
+  uint64_t bar_build, bar_om, bar_t, bar_ny, bar_ad;  // operands ready (one arrival per warp)
   uint32_t tmem_base;
   int abort;
   uint32_t tma_issued[3], tma_waited[3];  // per TMA barrier: phases issued / consumed
@@ -100,43 +112,79 @@ struct Misc {
 constexpr uint32_t SMEM_BYTES = SM_MISC + sizeof(Misc);
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(64 * FP * 4 <= 32768, "A^T fits SM_GA");
-static_assert(OFF_XBUF + 4 * 16 * XP * 4 <= 40960, "T and X blocks fit SM_GB");
+static_assert(OFF_TMAT % 1024 == 0 && OFF_TMAT + 8192 <= 40960, "T, X and T' fit SM_GB");
 
 // TMEM columns (fp32 cells).
 constexpr uint32_t TM_S = 0;     // S^T, 128 columns
-constexpr uint32_t TM_O = 128;   // O^T, 64 columns       } O+M1 writes [O^T | U^T]
-constexpr uint32_t TM_U = 192;   // U^T, then Delta^T (fp32), 64 columns
-constexpr uint32_t TM_AS = 256;  // bf16 S^T (A operand), 64 columns
-constexpr uint32_t TM_AD = 320;  // bf16 Delta^T (A operand), 32 columns
-constexpr uint32_t TM_GP = 352;  // [Gram; P] rows x 160 block columns
-constexpr uint32_t TM_W = 352;   // W^T, 64 columns (after the Gram/P epilogue)
+constexpr uint32_t TM_AS = 128;  // bf16 S^T (A operand), 64 columns
+constexpr uint32_t TM_O = 192;   // O^T, 2 x 64 columns (chunk parity)
+constexpr uint32_t TM_GP = 320;  // [Gram; P] rows x 160 block columns, then:
+constexpr uint32_t TM_Y = TM_GP;        //   Y^T fp32, 64 columns
+constexpr uint32_t TM_NY = TM_GP + 64;  //   bf16 -Y^T (A operand), 32 columns
+constexpr uint32_t TM_AD = TM_GP + 64;  //   bf16 Delta^T (A operand), after -Y^T is consumed
+constexpr uint32_t TM_D = TM_GP + 96;   //   Delta^T fp32, 64 columns
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint32_t ID_GP = idesc_bf16(128, GB_ROWS, false, false);
-constexpr uint32_t ID_UW = idesc_bf16(128, 64, true, false);
-constexpr uint32_t ID_OM1 = idesc_bf16(128, 128, false, false);
+constexpr uint32_t ID_N64 = idesc_bf16(128, 64, false, false);
 constexpr uint32_t ID_KM128 = idesc_bf16(128, 128, false, true);
-constexpr uint32_t ID_KK64 = idesc_bf16(128, 64, false, false);
+// Triangle-trimmed products: K step s writes output columns 16 s .. 63.
+__host__ __device__ constexpr uint32_t id_tri(int s, bool a_mn) {
+  return idesc_bf16(128, 64 - 16 * s, a_mn, false);
+}
 
 enum { TMA_QK = 0, TMA_LA = 1, TMA_V = 2 };
 
-// Optional per-phase cycle stamps of chain 0 (profiling builds only).
+// Optional per-phase cycle stamps of chain 0 (profiling builds only): thread 0
+// uses slots 0-15, thread 128 slots 16-23, the MMA thread slots 24-31.
 #ifdef KDA_PHASE_PROFILE
-__device__ long long g_phase_clock[4096 * 16];
-#define PHASE_MARK(i)                                                                    \
+__device__ long long g_phase_clock[4096 * 32];
+#define PHASE_STAMP(t, i)                                                                \
   do {                                                                                   \
-    if (tid == 0 && chain == 0 && ci < 4096) g_phase_clock[ci * 16 + (i)] = clock64();  \
+    if (tid == (t) && chain == 0 && ci < 4096) g_phase_clock[ci * 32 + (i)] = clock64(); \
   } while (0)
 #else
-#define PHASE_MARK(i) \
-  do {                \
+#define PHASE_STAMP(t, i) \
+  do {                    \
   } while (0)
 #endif
+#define PHASE_MARK(i) PHASE_STAMP(0, i)
+#define PHASE_MARK_W4(i) PHASE_STAMP(128, 16 + (i))
+#define PHASE_MARK_MMA(i) PHASE_STAMP(32 * kMmaWarp, 24 + (i))
 
+// CTA-wide barrier of all 288 threads, ordered with the tcgen05 operations.
 __device__ __forceinline__ void cta_sync() {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+}
+
+// Compute-warp barrier that also decides, identically for all 256 threads,
+// whether the CTA is aborting: each thread contributes the flag as it read it
+// and every thread receives the OR.  (The issue thread may raise the flag at any
+// moment, so a plain read after the barrier could differ between threads.)
+__device__ __forceinline__ bool compute_sync_abort(const int *abort_flag) {
+  const uint32_t mine = *reinterpret_cast<const volatile int *>(abort_flag) != 0 ? 1u : 0u;
+  uint32_t any;
+  tc_fence_before();
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "barrier.cta.red.or.pred p, 1, %2, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(any)
+      : "r"(mine), "n"(32 * kComputeWarps)
+      : "memory");
+  tc_fence_after();
+  return any != 0;
+}
+
+// One arrival per warp on an "operands ready" barrier: every lane has already
+// fenced its own shared-memory / TMEM writes; the warp barrier orders them
+// before lane 0's release-arrive.
+__device__ __forceinline__ void warp_arrive(uint64_t *bar, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
 }
 
 __device__ void record_status(DeviceStatus *st, int code, int detail, int chain, int chunk) {
@@ -155,21 +203,14 @@ struct Ctx {
 };
 
 // Bounded mbarrier wait; on timeout records KDA_ERR_TIMEOUT and raises the abort
-// flag.  The flag is only tested right after a CTA-wide barrier, so every thread
-// leaves the chunk loop at the same point.
+// flag.  Compute warps test the flag only through compute_sync_abort, so they
+// all leave the chunk loop at the same point; the MMA thread leaves its loop at
+// the failed wait.
 __device__ bool wait_bar(const Ctx &x, uint64_t *bar, uint32_t parity, int where, int chunk) {
   if (mbar_wait(bar, parity, kWaitNs)) return true;
   record_status(x.status, KDA_ERR_TIMEOUT, where, x.chain, chunk);
   atomicExch(&x.m->abort, 1);
   return false;
-}
-
-__device__ __forceinline__ uint64_t kdesc(const uint8_t *tile_base, uint32_t byte_off) {
-  return sdesc_sw128(smem_u32(tile_base) + byte_off, 16, 1024);
-}
-__device__ __forceinline__ uint64_t mndesc(const uint8_t *tile_base, uint32_t byte_off,
-                                           uint32_t lbo) {
-  return sdesc_sw128(smem_u32(tile_base) + byte_off, lbo, 1024);
 }
 
 // 8 consecutive fp32 from shared memory (16-byte aligned).
@@ -178,33 +219,6 @@ __device__ __forceinline__ void ld8(float (&v)[8], const float *p) {
   const float4 b = *reinterpret_cast<const float4 *>(p + 4);
   v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-
-__device__ __forceinline__ void unpack8(float (&v)[8], uint4 u) {
-  const float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y);
-  const float2 c = unpack_bf16x2(u.z), d = unpack_bf16x2(u.w);
-  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
-  v[4] = c.x; v[5] = c.y; v[6] = d.x; v[7] = d.y;
-}
-
-// Stores x[i] * f[i] (i < 8) as 8 bf16 at a shared address.
-__device__ __forceinline__ void st8_scaled(uint32_t saddr, const float (&x)[8],
-                                           const float (&f)[8]) {
-  st_shared_v4(saddr, pack_bf16x2(x[0] * f[0], x[1] * f[1]), pack_bf16x2(x[2] * f[2], x[3] * f[3]),
-               pack_bf16x2(x[4] * f[4], x[5] * f[5]), pack_bf16x2(x[6] * f[6], x[7] * f[7]));
-}
-
-// Byte offset of the bf16 pair (row, c..c+1), c even, in a K-major tile whose
-// 64-column halves hold `rows` rows each.
-__device__ __forceinline__ uint32_t kmaj_off(uint32_t rows, int row, int c) {
-  return (uint32_t)(c >> 6) * rows * 128u + sw128_offset(row, (uint32_t)(c & 63) * 2u);
-}
-__device__ __forceinline__ float2 ld_pair(const uint8_t *tile, uint32_t rows, int row, int c) {
-  return unpack_bf16x2(*reinterpret_cast<const uint32_t *>(tile + kmaj_off(rows, row, c)));
-}
-__device__ __forceinline__ void st_pair(uint8_t *tile, uint32_t rows, int row, int c, float x,
-                                        float y) {
-  *reinterpret_cast<uint32_t *>(tile + kmaj_off(rows, row, c)) = pack_bf16x2(x, y);
 }
 
 // Block column index of tile pair (a, b), a >= b, in the Gram column operand.
@@ -245,8 +259,11 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   if (tid == 0) {
     mbar_init(&m.bar_qk, 1); mbar_init(&m.bar_la, 1); mbar_init(&m.bar_v, 1);
-    mbar_init(&m.bar_gp, 1); mbar_init(&m.bar_wu, 1); mbar_init(&m.bar_m1, 1);
+    mbar_init(&m.bar_gp, 1); mbar_init(&m.bar_m1, 1); mbar_init(&m.bar_u, 1);
     mbar_init(&m.bar_m2, 1); mbar_init(&m.bar_fin, 1);
+    mbar_init(&m.bar_build, kComputeWarps); mbar_init(&m.bar_om, kComputeWarps);
+    mbar_init(&m.bar_t, kComputeWarps / 2); mbar_init(&m.bar_ny, kComputeWarps / 2);
+    mbar_init(&m.bar_ad, kComputeWarps);
     fence_mbarrier_init();
     m.abort = 0;
     for (int i = 0; i < 3; ++i) m.tma_issued[i] = m.tma_waited[i] = 0;
@@ -255,164 +272,206 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     tmem_alloc(&m.tmem_base, TM_COLS);
     tmem_relinquish();
   }
-  // P and T' blocks above the diagonal are never written: zero both tiles once.
-  for (int e = tid; e < 2 * 8192 / 16; e += kThreads) st_shared_v4(sb + SM_PMAT + 16 * e, 0, 0, 0, 0);
-  if (tid < C) m.beta[0][tid] = (n_chunks > 0 && tid < len) ? beta[(t0 + tid) * H + h] : 0.f;
+  float beta_pref = 0.f;   // beta of the chunk after the one being built (threads < C)
+  if (tid < C) {
+    m.beta[0][tid] = (n_chunks > 0 && tid < len) ? beta[(t0 + tid) * H + h] : 0.f;
+    beta_pref = (n_chunks > 1 && tid < len - C) ? beta[(t0 + C + tid) * H + h] : 0.f;
+  }
   cta_sync();
   const uint32_t tm = m.tmem_base;
-  const int q4 = warp & 3, hf = warp >> 2;  // TMEM lane quadrant, column half
-  const uint32_t lane_base = 32u * q4;
 
-  // TMA loads of chunk `ci` (thread 0 only).
-  auto issue_qk = [&](int ci) {
-    const int32_t tb = (int32_t)(t0 + (int64_t)C * ci);
-    mbar_arrive_expect_tx(&m.bar_qk, 2 * 16384);
-    tma_load_3d(smem + SM_Q, &tm_q, &m.bar_qk, 0, h, tb);
-    tma_load_3d(smem + SM_Q + 8192, &tm_q, &m.bar_qk, 64, h, tb);
-    tma_load_3d(smem + SM_K, &tm_k, &m.bar_qk, 0, h, tb);
-    tma_load_3d(smem + SM_K + 8192, &tm_k, &m.bar_qk, 64, h, tb);
-    m.tma_issued[TMA_QK]++;
-  };
-  auto issue_la = [&](int ci) {
-    const int32_t tb = (int32_t)(t0 + (int64_t)C * ci);
-    mbar_arrive_expect_tx(&m.bar_la, 32768);
-    tma_load_3d(smem + SM_LA, &tm_la, &m.bar_la, 0, h, tb);
-    m.tma_issued[TMA_LA]++;
-  };
-  auto issue_v = [&](int ci) {
-    const int32_t tb = (int32_t)(t0 + (int64_t)C * ci);
-    mbar_arrive_expect_tx(&m.bar_v, 16384);
-    tma_load_3d(smem + SM_V, &tm_v, &m.bar_v, 0, h, tb);
-    tma_load_3d(smem + SM_V + 8192, &tm_v, &m.bar_v, 64, h, tb);
-    m.tma_issued[TMA_V]++;
-  };
-
-  if (tid == 0 && n_chunks > 0) {
-    prefetch_tensormap(&tm_q); prefetch_tensormap(&tm_k);
-    prefetch_tensormap(&tm_v); prefetch_tensormap(&tm_la);
-    issue_qk(0); issue_la(0); issue_v(0);
-  }
-
-  // ---- initial state -> S^T in TMEM (thread: lane n, 64 key columns of its half); O^T = 0
-  const int64_t sbase = ((int64_t)seq * H + h) * D * D;
-  {
-    const int n = lane_base + lane;
+  if (warp >= kComputeWarps) {
+    // ===================== TMA + MMA issue (one thread) =====================
+    setmaxnreg_dec<kIssueRegs>();
+    if (warp == kMmaWarp && lane == 0 && n_chunks > 0) {
+      auto issue_qk = [&](int ci) {
+        const int32_t tb = (int32_t)(t0 + (int64_t)C * ci);
+        mbar_arrive_expect_tx(&m.bar_qk, 2 * 16384);
+        tma_load_3d(smem + SM_Q, &tm_q, &m.bar_qk, 0, h, tb);
+        tma_load_3d(smem + SM_Q + 8192, &tm_q, &m.bar_qk, 64, h, tb);
+        tma_load_3d(smem + SM_K, &tm_k, &m.bar_qk, 0, h, tb);
+        tma_load_3d(smem + SM_K + 8192, &tm_k, &m.bar_qk, 64, h, tb);
+        m.tma_issued[TMA_QK]++;
+      };
+      auto issue_la = [&](int ci) {
+        const int32_t tb = (int32_t)(t0 + (int64_t)C * ci);
+        mbar_arrive_expect_tx(&m.bar_la, 32768);
+        tma_load_3d(smem + SM_LA, &tm_la, &m.bar_la, 0, h, tb);
+        m.tma_issued[TMA_LA]++;
+      };
+      auto issue_v = [&](int ci) {
+        const int32_t tb = (int32_t)(t0 + (int64_t)C * ci);
+        mbar_arrive_expect_tx(&m.bar_v, 16384);
+        tma_load_3d(smem + SM_V, &tm_v, &m.bar_v, 0, h, tb);
+        tma_load_3d(smem + SM_V + 8192, &tm_v, &m.bar_v, 64, h, tb);
+        m.tma_issued[TMA_V]++;
+      };
+      prefetch_tensormap(&tm_q); prefetch_tensormap(&tm_k);
+      prefetch_tensormap(&tm_v); prefetch_tensormap(&tm_la);
+      issue_la(0); issue_qk(0); issue_v(0);
+      for (int ci = 0; ci < n_chunks; ++ci) {
+        const uint32_t par = (uint32_t)(ci & 1);
+        const bool has_next = ci + 1 < n_chunks;
+        // Opaque per-iteration copies of the shared-memory and TMEM bases: the
+        // descriptors below are rebuilt at each use instead of being hoisted out
+        // of the loop into (many) registers.
+        uint32_t sa = sb, tmb = tm;
+        asm volatile("" : "+r"(sa), "+r"(tmb));
+        auto kd = [&](uint32_t off) { return sdesc_sw128(sa + off, 16, 1024); };
+        auto mnd = [&](uint32_t off, uint32_t lbo) { return sdesc_sw128(sa + off, lbo, 1024); };
+        const uint32_t to = tmb + TM_O + 64u * (uint32_t)(ci & 1);
+        // Gram / P of chunk ci.  Its accumulator columns also hold the previous
+        // chunk's bf16 Delta^T, so the previous M2 group must have finished.
+        if (!wait_bar(cx, &m.bar_build, par, 30, ci)) break;
+        PHASE_MARK_MMA(0);
+        if (ci > 0 && !wait_bar(cx, &m.bar_m2, par ^ 1u, 36, ci - 1)) break;
+        tc_fence_after();
 #pragma unroll
-    for (int part = 0; part < 2; ++part) {
-      const int c0 = 64 * hf + 32 * part;
-      uint32_t r[32];
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t ad = kd(SM_GA + (ks >> 2) * 16384u + (ks & 3) * 32u);
+          const uint64_t bd = kd(SM_GB + (ks >> 2) * (GB_ROWS * 128u) + (ks & 3) * 32u);
+          umma_ss(tmb + TM_GP, ad, bd, ID_GP, ks > 0 ? 1u : 0u);
+        }
+        umma_commit(&m.bar_gp);
+        if (has_next) { issue_la(ci + 1); issue_qk(ci + 1); }   // both tiles consumed
+        // [O^T | Y^T] = S^T [Qt; Kt]^T
+        if (!wait_bar(cx, &m.bar_om, par, 31, ci)) break;
+        PHASE_MARK_MMA(1);
+        tc_fence_after();
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        r[j] = __float_as_uint(init_state ? init_state[sbase + (int64_t)(c0 + j) * D + n] : 0.f);
-      tmem_st32(tmem_addr(tm, lane_base, TM_S + c0), r);
-    }
-    uint32_t z[32];
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t a = tmb + TM_AS + 8u * ks;
+          const uint32_t off = SM_STACK + (ks >> 2) * 16384u + (ks & 3) * 32u;
+          umma_ts(to, a, kd(off), ID_N64, ks > 0 ? 1u : 0u);
+          umma_ts(tmb + TM_Y, a, kd(off + 8192u), ID_N64, ks > 0 ? 1u : 0u);
+        }
+        umma_commit(&m.bar_m1);
+        // Delta^T = V^T T'^T (needs only T' and this chunk's v tile) ...
+        if (!wait_bar(cx, &m.bar_v, par, 12, ci)) break;
+        m.tma_waited[TMA_V]++;
+        if (!wait_bar(cx, &m.bar_t, par, 32, ci)) break;
+        PHASE_MARK_MMA(2);
+        tc_fence_after();
 #pragma unroll
-    for (int j = 0; j < 32; ++j) z[j] = 0u;
-    tmem_st32(tmem_addr(tm, lane_base, TM_O + 32 * hf), z);
-    tmem_st_wait();
-  }
-  cta_sync();
-
-  // Writes the output rows of a finished chunk (warps 4-7 only): O^T (TMEM) ->
-  // bf16 staging in the q tile (free between the operand build and the next q
-  // load) -> coalesced 16-byte stores; clears O^T for the next chunk.
-  auto flush_output = [&](int64_t otb, int onv) {
-    __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(smem + SM_Q);
-    const int n = lane_base + lane;
-    uint32_t z[32];
+        for (int ks = 0; ks < 4; ++ks)
+          umma_ss(tmb + TM_D + 16u * ks, mnd(SM_V + ks * 2048u, 8192),
+                  kd(SM_TMAT + ks * 2048u + ks * 32u), id_tri(ks, true), ks > 0 ? 1u : 0u);
+        // ... + (-Y)^T T'^T
+        if (!wait_bar(cx, &m.bar_ny, par, 33, ci)) break;
+        PHASE_MARK_MMA(3);
+        tc_fence_after();
 #pragma unroll
-    for (int j = 0; j < 32; ++j) z[j] = 0u;
+        for (int ks = 0; ks < 4; ++ks)
+          umma_ts(tmb + TM_D + 16u * ks, tmb + TM_NY + 8u * ks,
+                  kd(SM_TMAT + ks * 2048u + ks * 32u), id_tri(ks, false), 1u);
+        umma_commit(&m.bar_u);
+        if (has_next) {   // the v tile is free once the Delta MMAs have read it
+          if (!wait_bar(cx, &m.bar_u, par, 34, ci)) break;
+          issue_v(ci + 1);
+        }
+        // S^T += Delta^T Kdec ; O^T += Delta^T P^T
+        if (!wait_bar(cx, &m.bar_ad, par, 35, ci)) break;
+        PHASE_MARK_MMA(4);
+        tc_fence_after();
+        const uint32_t kdec = SM_KDEC + 16384u * (uint32_t)(ci & 1);
 #pragma unroll
-    for (int part = 0; part < 2; ++part) {
-      uint32_t r[32];
-      tmem_ld32(tmem_addr(tm, lane_base, TM_O + 32 * part), r);
-      tmem_ld_wait(r);
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        stg[(32 * part + j) * D + n] = __float2bfloat16_rn(__uint_as_float(r[j]));
-      tmem_st32(tmem_addr(tm, lane_base, TM_O + 32 * part), z);
-    }
-    tmem_st_wait();
-    named_sync(2, 128);
-    const uint4 *s4 = reinterpret_cast<const uint4 *>(smem + SM_Q);
-    const int t = tid - 128;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = t + 128 * j;  // 16-byte chunk: row e / 16, column chunk e % 16
-      const int rr = e >> 4;
-      if (rr < onv) {
-        uint4 *dst = reinterpret_cast<uint4 *>(out + ((otb + rr) * H + h) * D) + (e & 15);
-        *dst = s4[e];
+        for (int ks = 0; ks < 4; ++ks) {
+          umma_ts(tmb + TM_S, tmb + TM_AD + 8u * ks, mnd(kdec + ks * 2048u, 8192), ID_KM128, 1u);
+          umma_ts(to + 16u * ks, tmb + TM_AD + 8u * ks, kd(SM_PMAT + ks * 2048u + ks * 32u),
+                  id_tri(ks, false), 1u);
+        }
+        umma_commit(&m.bar_m2);
       }
     }
-  };
+    __syncwarp();
+  } else {
+    // ===================== compute warps 0-7 =====================
+    setmaxnreg_inc<kComputeRegs>();
+    const int q4 = warp & 3, hf = warp >> 2;  // TMEM lane quadrant, column half
+    const uint32_t lane_base = 32u * q4;
+    const int64_t sbase = ((int64_t)seq * H + h) * D * D;
 
-  // Tile-local prefix of the log2-decay of chunk `ci` into registers; thread
-  // (tile ta, channel pair cp) owns rows 16 ta .. 16 ta + 15 of channels cc, cc+1.
-  const int ta = tid >> 6, cp = tid & 63, cc = 2 * cp;
-  const uint32_t hsel = (uint32_t)(cc >> 6), cb = (uint32_t)(cc & 63) * 2u;
-  uint32_t swzk[8];   // swizzled byte offset of channel pair cc in a row with row % 8 == k
-#pragma unroll
-  for (int k = 0; k < 8; ++k) swzk[k] = ((((cb >> 4) ^ (uint32_t)k) << 4) | (cb & 15u));
-  float L0[16], L1[16];
-  float beta_next = 0.f;
-  auto scan = [&](int ci) -> bool {
-    const uint32_t par = (uint32_t)(ci & 1);
-    const int64_t tb = t0 + (int64_t)C * ci;
-    const int nv = (int)((len - (int64_t)C * ci) < C ? (len - (int64_t)C * ci) : C);
-    const bool ok_la = wait_bar(cx, &m.bar_la, par, 11, ci);
-    if (ci + 1 < n_chunks && tid < C) {   // prefetch the following chunk's beta
-      const int64_t len_next = len - (int64_t)C * (ci + 1);
-      beta_next = tid < len_next ? beta[(tb + C + tid) * H + h] : 0.f;
-    }
-    const float2 *la = reinterpret_cast<const float2 *>(smem + SM_LA);
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int row = 16 * ta + j;
-      float2 x = la[row * (D / 2) + cp];
-      if (row >= nv) x = make_float2(0.f, 0.f);
-      s0 = fmaf(x.x, kLog2e, s0);
-      s1 = fmaf(x.y, kLog2e, s1);
-      L0[j] = s0;
-      L1[j] = s1;
-    }
-    *reinterpret_cast<float2 *>(&m.tot[ta][cc]) = make_float2(s0, s1);
-    if (tid == 0 && ok_la) m.tma_waited[TMA_LA]++;
-    return ok_la;
-  };
-
-  bool failed = false;
-  int64_t prev_tb = 0;
-  int prev_nv = 0;
-  if (n_chunks > 0) scan(0);
-  for (int ci = 0; ci < n_chunks && !failed; ++ci) {
-    const uint32_t par = (uint32_t)(ci & 1);
-    const int64_t tb = t0 + (int64_t)C * ci;
-    const int nv = (int)((len - (int64_t)C * ci) < C ? (len - (int64_t)C * ci) : C);
-    const bool has_next = ci + 1 < n_chunks;
-    const float *bcur = m.beta[ci & 1];
-    PHASE_MARK(0);
-    if (ci > 0) {   // Kdec / P of the previous chunk consumed, its state final
-      wait_bar(cx, &m.bar_m2, par ^ 1u, 25, ci - 1);
-      tc_fence_after();
-    }
-    cta_sync();     // tile totals of this chunk visible
-    PHASE_MARK(1);
-    if (m.abort) { failed = true; break; }
-    if (tid == 0 && ci == 0 && n_chunks > 1) issue_la(1);   // log_alpha tile scanned
-
-    // ================= phase 2: every operand tile of the chunk in one pass
+    // ---- initial state -> S^T in TMEM (thread: lane n, 64 key columns of its half)
     {
+      const int n = lane_base + lane;
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        const int c0 = 64 * hf + 32 * part;
+        uint32_t r[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          r[j] = __float_as_uint(init_state ? init_state[sbase + (int64_t)(c0 + j) * D + n] : 0.f);
+        tmem_st32(tmem_addr(tm, lane_base, TM_S + c0), r);
+      }
+      tmem_st_wait();
+    }
+
+    // Writes the output rows of a finished chunk (warps 4-7): O^T (TMEM) -> bf16,
+    // one 64-byte row segment per warp store.
+    auto flush_output = [&](int64_t otb, int onv, uint32_t ocol) {
+      const int n = lane_base + lane;
+      __nv_bfloat16 *dst = out + (otb * H + h) * D + n;
+      const int64_t rs = (int64_t)H * D;  // elements between consecutive tokens
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        uint32_t r[32];
+        tmem_ld32(tmem_addr(tm, lane_base, ocol + 32u * part), r);
+        tmem_ld_wait(r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (32 * part + j < onv)
+            dst[(int64_t)(32 * part + j) * rs] = __float2bfloat16_rn(__uint_as_float(r[j]));
+      }
+    };
+
+    // Thread (tile ta, channel pair cp) owns rows 16 ta .. 16 ta + 15 of key
+    // channels cc, cc + 1 in the decay prefix and the operand build.
+    const int ta = tid >> 6, cp = tid & 63, cc = 2 * cp;
+    const uint32_t hsel = (uint32_t)(cc >> 6), cb = (uint32_t)(cc & 63) * 2u;
+    uint32_t swzk[8];  // swizzled byte offset of channel pair cc in a row with row % 8 == k
+#pragma unroll
+    for (int k = 0; k < 8; ++k) swzk[k] = ((((cb >> 4) ^ (uint32_t)k) << 4) | (cb & 15u));
+    float *laf = reinterpret_cast<float *>(smem + SM_LA);
+
+    // Decay prefix and every operand tile of chunk ci; false if the CTA aborts.
+    auto scan_build = [&](int ci) -> bool {
+      const uint32_t par = (uint32_t)(ci & 1);
+      const int64_t tb = t0 + (int64_t)C * ci;
+      const int nv = (int)((len - (int64_t)C * ci) < C ? (len - (int64_t)C * ci) : C);
+      if (tid < C && ci > 0) {   // beta of this chunk, prefetch of the next one
+        m.beta[ci & 1][tid] = beta_pref;
+        const int64_t rem = len - (int64_t)C * (ci + 1);
+        beta_pref = (ci + 1 < n_chunks && tid < rem) ? beta[(tb + C + tid) * H + h] : 0.f;
+      }
+      // tile-local prefix of the log2-decay
+      const bool ok_la = wait_bar(cx, &m.bar_la, par, 11, ci);
+      if (tid == 0 && ok_la) m.tma_waited[TMA_LA]++;
+      float L0[16], L1[16];
+      {
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int row = 16 * ta + j;
+          float2 x = *reinterpret_cast<const float2 *>(laf + row * D + cc);
+          if (row >= nv) x = make_float2(0.f, 0.f);
+          s0 = fmaf(x.x, kLog2e, s0);
+          s1 = fmaf(x.y, kLog2e, s1);
+          L0[j] = s0;
+          L1[j] = s1;
+        }
+        // tile totals, written over this thread's own (already read) first row
+        *reinterpret_cast<float2 *>(laf + (16 * ta) * D + cc) = make_float2(s0, s1);
+      }
+      if (compute_sync_abort(&m.abort)) return false;
+      PHASE_MARK(9);
       const bool ok_qk = wait_bar(cx, &m.bar_qk, par, 10, ci);
       if (tid == 0 && ok_qk) m.tma_waited[TMA_QK]++;
-      float st0[4], st1[4], rf0[4], rf1[4];   // tile starts / ends, channels c, c+1
+      float st0[4], st1[4], rf0[4], rf1[4];  // tile starts / ends, channels cc, cc + 1
       {
         float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-          const float2 t = *reinterpret_cast<const float2 *>(&m.tot[b][cc]);
+          const float2 t = *reinterpret_cast<const float2 *>(laf + (16 * b) * D + cc);
           st0[b] = acc0; st1[b] = acc1;
           acc0 += t.x; acc1 += t.y;
           rf0[b] = acc0; rf1[b] = acc1;
@@ -430,7 +489,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         fb0[a2] = ex2(st0[a2] - ra0);
         fb1[a2] = ex2(st1[a2] - ra1);
       }
-      const float fs0 = ex2(sa0), fs1 = ex2(sa1);                 // e^{st_a}
+      const float fs0 = ex2(sa0), fs1 = ex2(sa1);                    // e^{st_a}
       const float fd0 = ex2(rf0[3] - ra0), fd1 = ex2(rf1[3] - ra1);  // e^{g_C - ref_a}
       if (ta == 0) {
         m.gamma[cc] = ex2(rf0[3]);
@@ -438,12 +497,15 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
       // Row-tile bases (column half of cc, first row of tile ta); element (row
       // 16 ta + j) sits j * 128 + swzk[j & 7] bytes further (128-byte swizzle).
+      // The Gram row operand interleaves tiles: rows 32 a .. 32 a + 15 hold K o E
+      // of tile a and rows 32 a + 16 .. 32 a + 31 hold Q o E of tile a, so each
+      // TMEM lane quadrant of the Gram result belongs to one row tile.
       const uint32_t r0 = 16u * ta * 128u, h64 = hsel * 8192u, h128 = hsel * 16384u;
       const uint32_t bK = sb + SM_K + h64 + r0, bQ = sb + SM_Q + h64 + r0;
-      const uint32_t bGA = sb + SM_GA + h128 + r0, bST = sb + SM_STACK + h128 + r0;
-      const uint32_t bKD = sb + SM_KDEC + h64 + r0;
+      const uint32_t bGA = sb + SM_GA + h128 + 2u * r0, bST = sb + SM_STACK + h128 + r0;
+      const uint32_t bKD = sb + SM_KDEC + 16384u * (uint32_t)(ci & 1) + h64 + r0;
       const uint32_t bGB = sb + SM_GB + hsel * (GB_ROWS * 128u) + r0;
-      uint32_t kraw[16], qraw[16];   // all k, q pairs of this thread, loaded up front
+      uint32_t kraw[16], qraw[16];  // all k, q pairs of this thread, loaded up front
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         kraw[j] = ld_shared_b32(bK + (uint32_t)j * 128u + swzk[j & 7]);
@@ -454,95 +516,94 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         const uint32_t o = (uint32_t)j * 128u + swzk[j & 7];
         const float2 kk = unpack_bf16x2(kraw[j]);
         const float2 qq = unpack_bf16x2(qraw[j]);
-        const float e0 = ex2(L0[j]), e1 = ex2(L1[j]);                    // e^{g_r - st_a}
-        const float ec0 = ex2(tot0 - L0[j]), ec1 = ex2(tot1 - L1[j]);    // e^{ref_a - g_r}
+        const float e0 = ex2(L0[j]), e1 = ex2(L1[j]);                  // e^{g_r - st_a}
+        const float ec0 = ex2(tot0 - L0[j]), ec1 = ex2(tot1 - L1[j]);  // e^{ref_a - g_r}
         st_shared_b32(bGA + o, pack_bf16x2(kk.x * e0, kk.y * e1));
-        st_shared_b32(bGA + 8192u + o, pack_bf16x2(qq.x * e0, qq.y * e1));
+        st_shared_b32(bGA + 2048u + o, pack_bf16x2(qq.x * e0, qq.y * e1));
         const float kc0 = kk.x * ec0, kc1 = kk.y * ec1;
 #pragma unroll
-        for (int a2 = 0; a2 < 4; ++a2) {   // block (a2, ta) of the column operand, row j
+        for (int a2 = 0; a2 < 4; ++a2) {  // block (a2, ta) of the column operand, row j
           if (a2 < ta) continue;
           st_shared_b32(bGB + 16u * blk(a2, 0) * 128u + o,
                         pack_bf16x2(kc0 * fb0[a2], kc1 * fb1[a2]));
         }
-        const float g0 = e0 * fs0, g1 = e1 * fs1;                        // e^{g_r}
+        const float g0 = e0 * fs0, g1 = e1 * fs1;  // e^{g_r}
         st_shared_b32(bST + o, pack_bf16x2(qq.x * g0, qq.y * g1));
         st_shared_b32(bST + 8192u + o, pack_bf16x2(kk.x * g0, kk.y * g1));
         st_shared_b32(bKD + o, pack_bf16x2(kc0 * fd0, kc1 * fd1));
       }
-    }
-    fence_proxy_async_smem();
-    if (tid < C && has_next) m.beta[(ci + 1) & 1][tid] = beta_next;
-    cta_sync();
-    PHASE_MARK(2);
-    if (m.abort) { failed = true; break; }
-    if (tid == 0) {
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint64_t ad = kdesc(smem + SM_GA, (ks >> 2) * 16384u + (ks & 3) * 32u);
-        const uint64_t bd = kdesc(smem + SM_GB, (ks >> 2) * (GB_ROWS * 128u) + (ks & 3) * 32u);
-        umma_ss(tm + TM_GP, ad, bd, ID_GP, ks > 0 ? 1u : 0u);
-      }
-      umma_commit(&m.bar_gp);
-    }
+      fence_proxy_async_smem();
+      warp_arrive(&m.bar_build, lane);
+      return true;
+    };
 
-    // ================= phase 3 (while the Gram MMAs run): S pass, previous output
-    {
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        const int c0 = 64 * hf + 32 * part;
-        uint32_t s[32];
-        tmem_ld32(tmem_addr(tm, lane_base, TM_S + c0), s);
-        tmem_ld_wait(s);
-        uint32_t ab[16];
-#pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {
-          float gv[8];
-          ld8(gv, &m.gamma[c0 + 8 * q8]);
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const int j = 8 * q8 + 2 * jj;
-            const float f0 = __uint_as_float(s[j]), f1 = __uint_as_float(s[j + 1]);
-            ab[4 * q8 + jj] = pack_bf16x2(f0, f1);
-            s[j] = __float_as_uint(f0 * gv[2 * jj]);
-            s[j + 1] = __float_as_uint(f1 * gv[2 * jj + 1]);
-          }
-        }
-        tmem_st32(tmem_addr(tm, lane_base, TM_S + c0), s);
-        tmem_st16(tmem_addr(tm, lane_base, TM_AS + c0 / 2), ab);
+    bool failed = false;
+    int64_t prev_tb = 0;
+    int prev_nv = 0;
+    if (n_chunks > 0 && !scan_build(0)) failed = true;
+    for (int ci = 0; ci < n_chunks && !failed; ++ci) {
+      const uint32_t par = (uint32_t)(ci & 1);
+      const int64_t tb = t0 + (int64_t)C * ci;
+      const int nv = (int)((len - (int64_t)C * ci) < C ? (len - (int64_t)C * ci) : C);
+      const float *bcur = m.beta[ci & 1];
+      PHASE_MARK(0);
+      if (ci > 0) {  // the previous chunk's state update and output are final
+        wait_bar(cx, &m.bar_m2, par ^ 1u, 25, ci - 1);
+        tc_fence_after();
       }
-      tmem_st_wait();
-    }
-    // ================= phase 4: A^T (fp32, for the solve) and P (bf16, K-major [r][i])
-    wait_bar(cx, &m.bar_gp, par, 22, ci);
-    tc_fence_after();
-    PHASE_MARK(3);
-    {
-      // Quadrant rows: 32 (q4 & 1) + lane; block columns of tiles {0,1} are [0, 48),
-      // of tiles {2,3} are [48, 160); the two warps of a quadrant split them.
-      const int row = 32 * (q4 & 1) + lane;
-      const int rta = row >> 4;
-      const bool gram = q4 < 2;
-      const float br = bcur[row];
-      float *amatT = reinterpret_cast<float *>(smem + SM_GA);
-      const int nld = (q4 & 1) ? 2 : 1;
-      const int col_first = (q4 & 1) ? 32 + 64 * hf : 32 * hf;
-      for (int li = 0; li < nld; ++li) {
-        const int col0 = col_first + 32 * li;
-        uint32_t v[32];
-        tmem_ld32(tmem_addr(tm, lane_base, TM_GP + col0), v);
-        tmem_ld_wait(v);
+      // Gamma, beta and the operand tiles of this chunk visible
+      if (compute_sync_abort(&m.abort)) { failed = true; break; }
+      PHASE_MARK(1);
+
+      // ---- S^T <- S^T Diag(Gamma_C); bf16 pre-chunk S^T as the A operand
+      {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int bk = (col0 >> 4) + half;    // block index of these 16 columns
-          const int ba = bk >= 6 ? 3 : bk >= 3 ? 2 : bk >= 1 ? 1 : 0;
-          const int bb = bk - ba * (ba + 1) / 2;
-          if (ba != rta) continue;
-          if (gram) {
+        for (int part = 0; part < 2; ++part) {
+          const int c0 = 64 * hf + 32 * part;
+          uint32_t s[32];
+          tmem_ld32(tmem_addr(tm, lane_base, TM_S + c0), s);
+          tmem_ld_wait(s);
+          uint32_t ab[16];
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {
+            float gv[8];
+            ld8(gv, &m.gamma[c0 + 8 * q8]);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const int j = 8 * q8 + 2 * jj;
+              const float f0 = __uint_as_float(s[j]), f1 = __uint_as_float(s[j + 1]);
+              ab[4 * q8 + jj] = pack_bf16x2(f0, f1);
+              s[j] = __float_as_uint(f0 * gv[2 * jj]);
+              s[j + 1] = __float_as_uint(f1 * gv[2 * jj + 1]);
+            }
+          }
+          tmem_st32(tmem_addr(tm, lane_base, TM_S + c0), s);
+          tmem_st16(tmem_addr(tm, lane_base, TM_AS + c0 / 2), ab);
+        }
+        tmem_st_wait();
+      }
+      PHASE_MARK(2);
+
+      // ---- Gram / P -> A^T (fp32, for the solve) and P (bf16, K-major [r][i]).
+      // Quadrant q4 holds row tile a = q4: lanes 0-15 key rows, 16-31 query rows.
+      wait_bar(cx, &m.bar_gp, par, 22, ci);
+      tc_fence_after();
+      PHASE_MARK(3);
+      {
+        const int a = q4, j = lane & 15, r = 16 * a + j;
+        const bool isq = lane >= 16;
+        const float br = bcur[r];
+        float *amatT = reinterpret_cast<float *>(smem + SM_GA);
+        for (int b = hf; b <= a; b += 2) {
+          __syncwarp();  // key and query lanes diverged in the previous block
+          uint32_t v[16];
+          tmem_ld16(tmem_addr(tm, lane_base, TM_GP + 16u * blk(a, b)), v);
+          tmem_ld_wait(v);
+          if (!isq) {
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
-              const int i = 16 * bb + jj;
-              amatT[i * FP + row] = i < row ? br * __uint_as_float(v[16 * half + jj]) : 0.f;
+              const int i = 16 * b + jj;
+              amatT[i * FP + r] = i < r ? br * __uint_as_float(v[jj]) : 0.f;
             }
           } else {
 #pragma unroll
@@ -550,246 +611,203 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
               uint32_t w[4];
 #pragma unroll
               for (int t = 0; t < 4; ++t) {
-                const int j = 8 * g8 + 2 * t, i = 16 * bb + j;
-                const float lo = i <= row ? __uint_as_float(v[16 * half + j]) : 0.f;
-                const float hi = i + 1 <= row ? __uint_as_float(v[16 * half + j + 1]) : 0.f;
+                const int jj = 8 * g8 + 2 * t, i = 16 * b + jj;
+                const float lo = i <= r ? __uint_as_float(v[jj]) : 0.f;
+                const float hi = i + 1 <= r ? __uint_as_float(v[jj + 1]) : 0.f;
                 w[t] = pack_bf16x2(lo, hi);
               }
-              st_shared_v4(sb + SM_PMAT + sw128_offset(row, (16 * bb + 8 * g8) * 2), w[0], w[1],
+              st_shared_v4(sb + SM_PMAT + sw128_offset(r, (16 * b + 8 * g8) * 2), w[0], w[1],
                            w[2], w[3]);
             }
           }
         }
       }
-    }
-    fence_proxy_async_smem();
-    cta_sync();
-    PHASE_MARK(4);
-    if (m.abort) { failed = true; break; }
-
-    // ================= phase 5: T = (I + A)^{-1} (warps 0-3) while warps 4-7 write
-    // the previous chunk's output.
-    const float *amatT = reinterpret_cast<const float *>(smem + SM_GA);   // A^T, [i][r]
-    float *tinv = reinterpret_cast<float *>(smem + SM_GB + OFF_TINV);     // T, [r][i]
-    if (warp < 4) {
-      float *xbuf = reinterpret_cast<float *>(smem + SM_GB + OFF_XBUF);
-      if (warp < 2) {
-        // Diagonal blocks by column-oriented forward substitution: lane owns
-        // column j of block a; after step m, t[m] is final and is eliminated
-        // from every later row.
-        const int a = 2 * warp + (lane >> 4), j = lane & 15, b0 = 16 * a;
-        float t[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) t[r] = (r == j) ? 1.f : 0.f;
-        float col[16], nxt[16];   // column mc of the block, and the next one in flight
-        ld8(*reinterpret_cast<float(*)[8]>(col), amatT + b0 * FP + b0);
-        ld8(*reinterpret_cast<float(*)[8]>(col + 8), amatT + b0 * FP + b0 + 8);
-#pragma unroll
-        for (int mc = 0; mc < 15; ++mc) {
-          if (mc + 1 < 15) {
-            ld8(*reinterpret_cast<float(*)[8]>(nxt), amatT + (b0 + mc + 1) * FP + b0);
-            ld8(*reinterpret_cast<float(*)[8]>(nxt + 8), amatT + (b0 + mc + 1) * FP + b0 + 8);
-          }
-          const float tmv = t[mc];
-#pragma unroll
-          for (int r = mc + 1; r < 16; ++r) t[r] = fmaf(-col[r], tmv, t[r]);
-#pragma unroll
-          for (int r = 0; r < 16; ++r) col[r] = nxt[r];
-        }
-        // T (fp32, for the block recursion) and T' = T Diag(beta) (bf16 MMA operand;
-        // the block's upper triangle is zero because t[r] = 0 for r < j).
-        const float bj = bcur[b0 + j];
-        __nv_bfloat16 *tp = reinterpret_cast<__nv_bfloat16 *>(smem + SM_TMAT);
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          tinv[(b0 + r) * FP + b0 + j] = t[r];
-          tp[sw128_offset(b0 + r, (b0 + j) * 2) >> 1] = __float2bfloat16_rn(t[r] * bj);
-        }
-      }
-      named_sync(1, 128);
-      // Off-diagonal blocks, block-recursive: 16 -> 32 (blocks (1,0), (3,2)), then
-      // 32 -> 64 (blocks (2,0), (2,1), (3,0), (3,1)), TF32 warp MMAs.
-      const int g = lane >> 2, t4 = lane & 3;
-      // acc (+)= A_{ab} T_{mb} with A from A^T (column-major, pitch FP) ...
-      auto mul_AT = [&](float (&acc)[2][4], int ab, int mb, int tcol) {
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          const int kc = 16 * mb + 8 * kk;
-          const uint32_t a0 = to_tf32(amatT[(kc + t4) * FP + 16 * ab + g]);
-          const uint32_t a1 = to_tf32(amatT[(kc + t4) * FP + 16 * ab + g + 8]);
-          const uint32_t a2 = to_tf32(amatT[(kc + t4 + 4) * FP + 16 * ab + g]);
-          const uint32_t a3 = to_tf32(amatT[(kc + t4 + 4) * FP + 16 * ab + g + 8]);
-          const float *b0p = tinv + (kc + t4) * FP + tcol + g;
-          const float *b1p = tinv + (kc + t4 + 4) * FP + tcol + g;
-          mma_tf32_16x8x8(acc[0], a0, a1, a2, a3, to_tf32(b0p[0]), to_tf32(b1p[0]));
-          mma_tf32_16x8x8(acc[1], a0, a1, a2, a3, to_tf32(b0p[8]), to_tf32(b1p[8]));
-        }
-      };
-      // ... and acc (+)= T_{ar} X with T row-major (pitch FP), X a 16 x 16 block (pitch XP).
-      auto mul_TX = [&](float (&acc)[2][4], int ar, int ac, const float *x) {
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          const float *tp = tinv + (16 * ar) * FP + 16 * ac + 8 * kk;
-          const uint32_t a0 = to_tf32(tp[g * FP + t4]);
-          const uint32_t a1 = to_tf32(tp[(g + 8) * FP + t4]);
-          const uint32_t a2 = to_tf32(tp[g * FP + t4 + 4]);
-          const uint32_t a3 = to_tf32(tp[(g + 8) * FP + t4 + 4]);
-          const float *x0 = x + (8 * kk + t4) * XP + g;
-          const float *x1 = x + (8 * kk + t4 + 4) * XP + g;
-          mma_tf32_16x8x8(acc[0], a0, a1, a2, a3, to_tf32(x0[0]), to_tf32(x1[0]));
-          mma_tf32_16x8x8(acc[1], a0, a1, a2, a3, to_tf32(x0[8]), to_tf32(x1[8]));
-        }
-      };
-      auto store_blk = [&](float *dst, int pitch, const float (&acc)[2][4], float sgn) {
-#pragma unroll
-        for (int nh = 0; nh < 2; ++nh) {
-          dst[g * pitch + 8 * nh + 2 * t4] = sgn * acc[nh][0];
-          dst[g * pitch + 8 * nh + 2 * t4 + 1] = sgn * acc[nh][1];
-          dst[(g + 8) * pitch + 8 * nh + 2 * t4] = sgn * acc[nh][2];
-          dst[(g + 8) * pitch + 8 * nh + 2 * t4 + 1] = sgn * acc[nh][3];
-        }
-      };
-      // Final block T_ab: fp32 into T, and T' = T Diag(beta) as bf16 pairs.
-      auto store_T = [&](int ab, int bb, const float (&acc)[2][4]) {
-        store_blk(tinv + (16 * ab) * FP + 16 * bb, FP, acc, -1.f);
-#pragma unroll
-        for (int nh = 0; nh < 2; ++nh) {
-          const int col = 16 * bb + 8 * nh + 2 * t4;
-          const float b0v = bcur[col], b1v = bcur[col + 1];
-          const uint32_t lo = pack_bf16x2(-acc[nh][0] * b0v, -acc[nh][1] * b1v);
-          const uint32_t hi = pack_bf16x2(-acc[nh][2] * b0v, -acc[nh][3] * b1v);
-          *reinterpret_cast<uint32_t *>(smem + SM_TMAT + sw128_offset(16 * ab + g, col * 2)) = lo;
-          *reinterpret_cast<uint32_t *>(smem + SM_TMAT + sw128_offset(16 * ab + g + 8, col * 2)) = hi;
-        }
-      };
-      float *xw = xbuf + warp * 16 * XP;
-      if (warp < 2) {   // level 16 -> 32: block (1,0) on warp 0, (3,2) on warp 1
-        const int ab = 2 * warp + 1, bb = 2 * warp;
-        float acc[2][4] = {};
-        mul_AT(acc, ab, bb, 16 * bb);                 // X = A_ab T_bb
-        store_blk(xw, XP, acc, 1.f);
-        __syncwarp();
-        float o[2][4] = {};
-        mul_TX(o, ab, ab, xw);                        // T_ab = -T_aa X
-        store_T(ab, bb, o);
-      }
-      named_sync(1, 128);
-      {                 // level 32 -> 64: warp w -> block (2 + w/2, w%2)
-        const int ab = 2 + (warp >> 1), bb = warp & 1;
-        float acc[2][4] = {};
-        // X_{ab} = A_{ab,0:2} T_{0:2, bb} = sum_{m=bb}^{1} A_{ab,m} T_{m,bb}
-        for (int mb = bb; mb < 2; ++mb) mul_AT(acc, ab, mb, 16 * bb);
-        store_blk(xw, XP, acc, 1.f);
-        named_sync(1, 128);
-        // T_{ab} = -sum_{k=2}^{ab} T_{ab,k} X_{k,bb}
-        float o[2][4] = {};
-        for (int k = 2; k <= ab; ++k) mul_TX(o, ab, k, xbuf + (2 * (k - 2) + bb) * 16 * XP);
-        store_T(ab, bb, o);
-      }
-      fence_proxy_async_smem();   // T' is an MMA operand
-    } else {
-      if (ci > 0) flush_output(prev_tb, prev_nv);
-      named_sync(2, 128);   // output staging (q tile) read by warps 4-7
-      if (tid == 128 && has_next) issue_qk(ci + 1);
-    }
-    __syncthreads();
-    PHASE_MARK(5);
-
-    fence_proxy_async_smem();
-    cta_sync();
-    PHASE_MARK(6);
-    if (tid == 0) {
-      if (wait_bar(cx, &m.bar_v, par, 12, ci)) {
-        m.tma_waited[TMA_V]++;
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {   // U^T = V^T T'^T ; W^T = Kt^T T'^T, interleaved
-          const uint64_t bd = kdesc(smem + SM_TMAT, ks * 32u);
-          umma_ss(tm + TM_U, mndesc(smem + SM_V, ks * 2048u, 8192), bd, ID_UW, ks > 0);
-          umma_ss(tm + TM_W, mndesc(smem + SM_STACK, 64u * 128u + ks * 2048u, 16384), bd, ID_UW,
-                  ks > 0);
-        }
-        umma_commit(&m.bar_wu);
-      }
-    }
-
-    // ================= phase 6: -W -> stack rows 64.. (K-major); [O^T | D^T] = S^T [Qt; -W]^T
-    wait_bar(cx, &m.bar_wu, par, 23, ci);
-    tc_fence_after();
-    PHASE_MARK(7);
-    if (tid == 128 && has_next) issue_v(ci + 1);
-    {
-      uint32_t r[32];
-      tmem_ld32(tmem_addr(tm, lane_base, TM_W + 32 * hf), r);
-      tmem_ld_wait(r);
-      const int c = lane_base + lane;   // key channel of this lane; W^T columns are rows r
-      const uint32_t cbyte = (uint32_t)(c & 63) * 2u;
-      const uint32_t base = sb + SM_STACK + (uint32_t)(c >> 6) * 16384u + (64u + 32u * hf) * 128u;
-      uint32_t sw[8];   // swizzled byte offset of channel c in a row with row % 8 == k
-#pragma unroll
-      for (int k = 0; k < 8; ++k) sw[k] = ((((cbyte >> 4) ^ (uint32_t)k) << 4) | (cbyte & 15u));
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const __nv_bfloat16 w = __float2bfloat16_rn(-__uint_as_float(r[j]));
-        st_shared_b16(base + (uint32_t)j * 128u + sw[j & 7], *reinterpret_cast<const uint16_t *>(&w));
-      }
       fence_proxy_async_smem();
-    }
-    cta_sync();
-    PHASE_MARK(8);
-    if (m.abort) { failed = true; break; }
-    if (tid == 0) {
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-        umma_ts(tm + TM_O, tm + TM_AS + 8 * ks,
-                kdesc(smem + SM_STACK, (ks >> 2) * 16384u + (ks & 3) * 32u), ID_OM1, 1u);
-      umma_commit(&m.bar_m1);
-    }
-    // next chunk's decay prefix while the MMAs run
-    if (has_next) scan(ci + 1);
-    PHASE_MARK(9);
+      tc_fence_before();
+      warp_arrive(&m.bar_om, lane);  // S^T operand ready, Gram columns free: O+M1 may start
+      // A^T visible to the solve warps
+      if (compute_sync_abort(&m.abort)) { failed = true; break; }
+      PHASE_MARK(4);
 
-    // ================= phase 7: bf16 Delta^T; S^T += Delta^T Kdec; O^T += Delta^T P^T
-    wait_bar(cx, &m.bar_m1, par, 24, ci);
-    tc_fence_after();
-    PHASE_MARK(10);
-    {
-      uint32_t r[32];
-      tmem_ld32(tmem_addr(tm, lane_base, TM_U + 32 * hf), r);
-      tmem_ld_wait(r);
-      uint32_t ab[16];
+      if (warp < 4) {
+        // ---- T = (I + A)^{-1} and T' = T Diag(beta) (warps 0-3)
+        const float *amatT = reinterpret_cast<const float *>(smem + SM_GA);  // A^T, [i][r]
+        float *tinv = reinterpret_cast<float *>(smem + SM_GB + OFF_TINV);    // T, [r][i]
+        float *xbuf = reinterpret_cast<float *>(smem + SM_GB + OFF_XBUF);
+        if (warp < 2) {
+          // Diagonal blocks by column-oriented forward substitution: lane owns
+          // column j of block a; after step m, t[m] is final and is eliminated
+          // from every later row.
+          const int a = 2 * warp + (lane >> 4), j = lane & 15, b0 = 16 * a;
+          float t[16];
 #pragma unroll
-      for (int jj = 0; jj < 16; ++jj)
-        ab[jj] = pack_bf16x2(__uint_as_float(r[2 * jj]), __uint_as_float(r[2 * jj + 1]));
-      tmem_st16(tmem_addr(tm, lane_base, TM_AD + 16 * hf), ab);
-      tmem_st_wait();
-    }
-    cta_sync();
-    PHASE_MARK(11);
-    if (m.abort) { failed = true; break; }
-    if (tid == 0) {
+          for (int r = 0; r < 16; ++r) t[r] = (r == j) ? 1.f : 0.f;
+          float col[16], nxt[16];  // column mc of the block, and the next one in flight
+          ld8(*reinterpret_cast<float(*)[8]>(col), amatT + b0 * FP + b0);
+          ld8(*reinterpret_cast<float(*)[8]>(col + 8), amatT + b0 * FP + b0 + 8);
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        umma_ts(tm + TM_S, tm + TM_AD + 8 * ks, mndesc(smem + SM_KDEC, ks * 2048u, 8192),
-                ID_KM128, 1u);
-        umma_ts(tm + TM_O, tm + TM_AD + 8 * ks, kdesc(smem + SM_PMAT, ks * 32u), ID_KK64, 1u);
+          for (int mc = 0; mc < 15; ++mc) {
+            if (mc + 1 < 15) {
+              ld8(*reinterpret_cast<float(*)[8]>(nxt), amatT + (b0 + mc + 1) * FP + b0);
+              ld8(*reinterpret_cast<float(*)[8]>(nxt + 8), amatT + (b0 + mc + 1) * FP + b0 + 8);
+            }
+            const float tmv = t[mc];
+#pragma unroll
+            for (int r = mc + 1; r < 16; ++r) t[r] = fmaf(-col[r], tmv, t[r]);
+#pragma unroll
+            for (int r = 0; r < 16; ++r) col[r] = nxt[r];
+          }
+          // T (fp32, for the block recursion) and T' = T Diag(beta) (bf16 MMA operand;
+          // the block's upper triangle is zero because t[r] = 0 for r < j).
+          const float bj = bcur[b0 + j];
+          __nv_bfloat16 *tp = reinterpret_cast<__nv_bfloat16 *>(smem + SM_TMAT);
+#pragma unroll
+          for (int r = 0; r < 16; ++r) {
+            tinv[(b0 + r) * FP + b0 + j] = t[r];
+            tp[sw128_offset(b0 + r, (b0 + j) * 2) >> 1] = __float2bfloat16_rn(t[r] * bj);
+          }
+        }
+        named_sync(2, 128);
+        // Off-diagonal blocks, block-recursive: 16 -> 32 (blocks (1,0), (3,2)), then
+        // 32 -> 64 (blocks (2,0), (2,1), (3,0), (3,1)), TF32 warp MMAs.
+        const int g = lane >> 2, t4 = lane & 3;
+        // acc (+)= A_{ab} T_{mb} with A from A^T (column-major, pitch FP) ...
+        auto mul_AT = [&](float (&acc)[2][4], int ab, int mb, int tcol) {
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const int kc = 16 * mb + 8 * kk;
+            const uint32_t a0 = to_tf32(amatT[(kc + t4) * FP + 16 * ab + g]);
+            const uint32_t a1 = to_tf32(amatT[(kc + t4) * FP + 16 * ab + g + 8]);
+            const uint32_t a2 = to_tf32(amatT[(kc + t4 + 4) * FP + 16 * ab + g]);
+            const uint32_t a3 = to_tf32(amatT[(kc + t4 + 4) * FP + 16 * ab + g + 8]);
+            const float *b0p = tinv + (kc + t4) * FP + tcol + g;
+            const float *b1p = tinv + (kc + t4 + 4) * FP + tcol + g;
+            mma_tf32_16x8x8(acc[0], a0, a1, a2, a3, to_tf32(b0p[0]), to_tf32(b1p[0]));
+            mma_tf32_16x8x8(acc[1], a0, a1, a2, a3, to_tf32(b0p[8]), to_tf32(b1p[8]));
+          }
+        };
+        // ... and acc (+)= T_{ar} X with T row-major (pitch FP), X a 16 x 16 block (pitch XP).
+        auto mul_TX = [&](float (&acc)[2][4], int ar, int ac, const float *x) {
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const float *tq = tinv + (16 * ar) * FP + 16 * ac + 8 * kk;
+            const uint32_t a0 = to_tf32(tq[g * FP + t4]);
+            const uint32_t a1 = to_tf32(tq[(g + 8) * FP + t4]);
+            const uint32_t a2 = to_tf32(tq[g * FP + t4 + 4]);
+            const uint32_t a3 = to_tf32(tq[(g + 8) * FP + t4 + 4]);
+            const float *x0 = x + (8 * kk + t4) * XP + g;
+            const float *x1 = x + (8 * kk + t4 + 4) * XP + g;
+            mma_tf32_16x8x8(acc[0], a0, a1, a2, a3, to_tf32(x0[0]), to_tf32(x1[0]));
+            mma_tf32_16x8x8(acc[1], a0, a1, a2, a3, to_tf32(x0[8]), to_tf32(x1[8]));
+          }
+        };
+        auto store_blk = [&](float *dst, int pitch, const float (&acc)[2][4], float sgn) {
+#pragma unroll
+          for (int nh = 0; nh < 2; ++nh) {
+            dst[g * pitch + 8 * nh + 2 * t4] = sgn * acc[nh][0];
+            dst[g * pitch + 8 * nh + 2 * t4 + 1] = sgn * acc[nh][1];
+            dst[(g + 8) * pitch + 8 * nh + 2 * t4] = sgn * acc[nh][2];
+            dst[(g + 8) * pitch + 8 * nh + 2 * t4 + 1] = sgn * acc[nh][3];
+          }
+        };
+        // Final block T_ab: fp32 into T, and T' = T Diag(beta) as bf16 pairs.
+        auto store_T = [&](int ab, int bb, const float (&acc)[2][4]) {
+          store_blk(tinv + (16 * ab) * FP + 16 * bb, FP, acc, -1.f);
+#pragma unroll
+          for (int nh = 0; nh < 2; ++nh) {
+            const int col = 16 * bb + 8 * nh + 2 * t4;
+            const float b0v = bcur[col], b1v = bcur[col + 1];
+            const uint32_t lo = pack_bf16x2(-acc[nh][0] * b0v, -acc[nh][1] * b1v);
+            const uint32_t hi = pack_bf16x2(-acc[nh][2] * b0v, -acc[nh][3] * b1v);
+            st_shared_b32(sb + SM_TMAT + sw128_offset(16 * ab + g, col * 2), lo);
+            st_shared_b32(sb + SM_TMAT + sw128_offset(16 * ab + g + 8, col * 2), hi);
+          }
+        };
+        float *xw = xbuf + warp * 16 * XP;
+        if (warp < 2) {  // level 16 -> 32: block (1,0) on warp 0, (3,2) on warp 1
+          const int ab = 2 * warp + 1, bb = 2 * warp;
+          float acc[2][4] = {};
+          mul_AT(acc, ab, bb, 16 * bb);  // X = A_ab T_bb
+          store_blk(xw, XP, acc, 1.f);
+          __syncwarp();
+          float o[2][4] = {};
+          mul_TX(o, ab, ab, xw);  // T_ab = -T_aa X
+          store_T(ab, bb, o);
+        }
+        named_sync(2, 128);
+        {  // level 32 -> 64: warp w -> block (2 + w/2, w%2)
+          const int ab = 2 + (warp >> 1), bb = warp & 1;
+          float acc[2][4] = {};
+          // X_{ab} = A_{ab,0:2} T_{0:2, bb} = sum_{m=bb}^{1} A_{ab,m} T_{m,bb}
+          for (int mb = bb; mb < 2; ++mb) mul_AT(acc, ab, mb, 16 * bb);
+          store_blk(xw, XP, acc, 1.f);
+          named_sync(2, 128);
+          // T_{ab} = -sum_{k=2}^{ab} T_{ab,k} X_{k,bb}
+          float o[2][4] = {};
+          for (int k = 2; k <= ab; ++k) mul_TX(o, ab, k, xbuf + (2 * (k - 2) + bb) * 16 * XP);
+          store_T(ab, bb, o);
+        }
+        fence_proxy_async_smem();  // T' is an MMA operand
+        warp_arrive(&m.bar_t, lane);
+        PHASE_MARK(5);
+      } else {
+        // ---- previous chunk's output rows, then -Y^T as a bf16 A operand (warps 4-7)
+        PHASE_MARK_W4(0);
+        if (ci > 0) flush_output(prev_tb, prev_nv, TM_O + 64u * (par ^ 1u));
+        PHASE_MARK_W4(1);
+        wait_bar(cx, &m.bar_m1, par, 24, ci);
+        tc_fence_after();
+        PHASE_MARK_W4(2);
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          uint32_t y[32];
+          tmem_ld32(tmem_addr(tm, lane_base, TM_Y + 32u * part), y);
+          tmem_ld_wait(y);
+          uint32_t p[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj)
+            p[jj] = pack_bf16x2(-__uint_as_float(y[2 * jj]), -__uint_as_float(y[2 * jj + 1]));
+          tmem_st16(tmem_addr(tm, lane_base, TM_NY + 16u * part), p);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        warp_arrive(&m.bar_ny, lane);
+        PHASE_MARK_W4(3);
       }
-      umma_commit(&m.bar_m2);
-      if (ci + 2 < n_chunks) issue_la(ci + 2);   // the next chunk's tile was scanned above
-    }
-    prev_tb = tb;
-    prev_nv = nv;
-  }
 
-  // ---- the last chunk's output and the final state
-  if (!failed && n_chunks > 0) {
-    wait_bar(cx, &m.bar_m2, (uint32_t)((n_chunks - 1) & 1), 26, n_chunks - 1);
-    tc_fence_after();
-    if (warp >= 4) flush_output(prev_tb, prev_nv);
-  }
-  cta_sync();
-  if (!failed && !m.abort) {
-    if (final_state) {
+      // ---- bf16 Delta^T, the A operand of the state and output updates
+      wait_bar(cx, &m.bar_u, par, 23, ci);
+      tc_fence_after();
+      PHASE_MARK(6);
+      {
+        uint32_t r[32];
+        tmem_ld32(tmem_addr(tm, lane_base, TM_D + 32u * hf), r);
+        tmem_ld_wait(r);
+        uint32_t ab[16];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj)
+          ab[jj] = pack_bf16x2(__uint_as_float(r[2 * jj]), __uint_as_float(r[2 * jj + 1]));
+        tmem_st16(tmem_addr(tm, lane_base, TM_AD + 16u * hf), ab);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      warp_arrive(&m.bar_ad, lane);
+      PHASE_MARK(7);
+      prev_tb = tb;
+      prev_nv = nv;
+      // ---- the next chunk's operand tiles, while the state MMAs run
+      if (ci + 1 < n_chunks && !scan_build(ci + 1)) { failed = true; break; }
+      PHASE_MARK(8);
+    }
+
+    // ---- the last chunk's output and the final state
+    if (!failed && n_chunks > 0) {
+      wait_bar(cx, &m.bar_m2, (uint32_t)((n_chunks - 1) & 1), 26, n_chunks - 1);
+      tc_fence_after();
+      if (warp >= 4) flush_output(prev_tb, prev_nv, TM_O + 64u * (uint32_t)((n_chunks - 1) & 1));
+    }
+    const bool aborted = compute_sync_abort(&m.abort);
+    if (!failed && !aborted && final_state) {
       const int n = lane_base + lane;
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
@@ -802,7 +820,11 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           final_state[sbase + (int64_t)(c0 + j) * D + n] = __uint_as_float(r[j]);
       }
     }
-  } else if (tid == 0) {
+  }
+
+  // ---- teardown (all warps)
+  cta_sync();
+  if (warp == kMmaWarp && lane == 0 && m.abort && n_chunks > 0) {
     // Drain what is still in flight (bounded), so no copy or MMA outlives the CTA.
     umma_commit(&m.bar_fin);
     mbar_wait(&m.bar_fin, 0, kWaitNs);
@@ -871,6 +893,12 @@ cudaError_t launch_chunk_fwd_bf16_tc(const ChunkArgs &a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kda_chunk_fwd_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  // The setmaxnreg split assumes the launch allocation it was sized for; with a
+  // smaller one the compute warpgroups' .inc could never be satisfied.
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kda_chunk_fwd_tc_kernel);
+  if (e != cudaSuccess) return e;
+  if ((uint32_t)fa.numRegs < kLaunchRegs) return cudaErrorNotSupported;
   kda_chunk_fwd_tc_kernel<<<(unsigned)chains, kThreads, SMEM_BYTES, stream>>>(
       mq, mk, mv, mla, a.beta, a.init_state, a.cu_seqlens, a.n_seqs, a.n_tokens, a.H,
       static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.status);

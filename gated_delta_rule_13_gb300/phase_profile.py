@@ -17,10 +17,18 @@ import sys
 
 from . import _build
 
-# Phase boundaries stamped by the kernel (PHASE_MARK indices 0..11).
-PHASES = ["wait m2(prev) + sync", "build all tiles", "S pass + wait gp", "A/P epilogue",
-          "solve + T' || flush(prev)", "sync", "wait wu (U/W)", "W epilogue", "scan(next)",
-          "wait m1 (O+M1)", "Delta + sync", "M2 issue -> next chunk"]
+# Phase boundaries stamped by thread 0 (PHASE_MARK indices 0..8); the last
+# interval runs to the next chunk's first stamp.
+PHASES = ["wait m2(prev) + sync", "S pass", "wait Gram MMAs", "A/P epilogue + sync",
+          "solve (warps 0-3)", "wait Delta MMAs", "Delta pass", "scan + build (next)",
+          "loop"]
+# Extra stamps, printed as offsets from the chunk's first stamp: thread 0 slot 9
+# (this chunk's build started, stamped during the previous iteration), thread 128
+# (warp 4) slots 16-19, the MMA thread slots 24-28.
+EXTRA = {9: "t0: build of this chunk started (prev. iteration)", 16: "w4: flush start",
+         17: "w4: flush done", 18: "w4: O+Y MMAs done", 19: "w4: -Y pass done",
+         24: "mma: operands built, Gram issue", 25: "mma: O+Y issue", 26: "mma: T' ready",
+         27: "mma: -Y ready", 28: "mma: Delta ready, M2 issue"}
 
 
 def build_profiling_library() -> str:
@@ -51,9 +59,10 @@ def main(workload: str = "k3_h96_t32768") -> None:
                           x["cu_seqlens"])
     torch.cuda.synchronize()
     n_chunks = min(4096, (int(x["lengths"][0]) + 63) // 64)
-    buf = (ctypes.c_longlong * (4096 * 16))()
-    kda.library().kda_debug_phase_clock(buf, 4096 * 16)
-    stamps = np.array(buf[:], dtype=np.int64).reshape(4096, 16)[:n_chunks, :len(PHASES)]
+    buf = (ctypes.c_longlong * (4096 * 32))()
+    kda.library().kda_debug_phase_clock(buf, 4096 * 32)
+    raw = np.array(buf[:], dtype=np.int64).reshape(4096, 32)[:n_chunks]
+    stamps = raw[:, :len(PHASES)]
     # interval k = stamp k+1 - stamp k; the last one runs to the next chunk's stamp 0
     nxt = np.concatenate([stamps[1:, :1], stamps[-1:, :1]])
     d = np.diff(np.concatenate([stamps, nxt], axis=1), axis=1)[1:-1]
@@ -63,7 +72,13 @@ def main(workload: str = "k3_h96_t32768") -> None:
     for name, v in zip(PHASES, med):
         print(f"  {name:28s} {v:8.0f}  {100 * v / total:5.1f}%")
     print(f"  {'total per chunk':28s} {total:8.0f}")
-
+    print("stamps as offsets from the chunk's first stamp (median):")
+    marks = sorted([(np.median(raw[1:-1, i] - raw[1:-1, 0]), EXTRA[i]) for i in EXTRA
+                    if raw[1:-1, i].any()] +
+                   [(np.median(raw[1:-1, i] - raw[1:-1, 0]), "t0: end of " + PHASES[i - 1])
+                    for i in range(1, len(PHASES))])
+    for off, name in marks:
+        print(f"  {off:8.0f}  {name}")
 
 if __name__ == "__main__":
     main(*sys.argv[1:2])
