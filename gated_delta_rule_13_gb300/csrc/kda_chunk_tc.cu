@@ -35,7 +35,7 @@
 // TMEM orientation: the state is held transposed (S^T: lane = value index n,
 // column = key index c), so every state-side product is an M = 128 MMA:
 //   O^T = S^T Qt^T,  Y^T = S^T Kt^T      (A = bf16 S^T in TMEM)
-//   Delta^T = V^T T'^T + (-Y)^T T'^T      (A = V in smem, then bf16 -Y^T in TMEM)
+//   Delta^T = (V - Y)^T T'^T              (A = bf16 (V - Y)^T in TMEM)
 //   S^T += Delta^T Kdec,  O^T += Delta^T P^T   (A = bf16 Delta^T in TMEM),
 //                                    after S^T <- S^T Diag(e^{g_C})
 // The products with the lower-triangular T' and P skip the zero blocks: K step
@@ -43,8 +43,8 @@
 //
 // Pipeline.  O^T is double-buffered in TMEM and Kdec in shared memory, so the
 // next chunk's operand build overlaps this chunk's state MMAs, the triangular
-// solve (warps 0-3) overlaps the previous chunk's output stores and the -Y pass
-// (warps 4-7), and the Gram MMAs of chunk c+1 overlap the state pass of c+1.
+// solve (warps 0-3) overlaps the (V - Y) pass and the previous chunk's output
+// stores (warps 4-7), and the Gram MMAs of chunk c+1 overlap the state pass of c+1.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -81,7 +81,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // stores columns 0-63 as R rows of 128 B, then columns 64-127 likewise.
 constexpr uint32_t SM_Q = 0;                    // q chunk (TMA), 64 rows
 constexpr uint32_t SM_K = SM_Q + 16384;         // k chunk (TMA), 64 rows
-constexpr uint32_t SM_V = SM_K + 16384;         // v chunk (TMA), 64 rows
+constexpr uint32_t SM_V = SM_K + 16384;         // v chunk (TMA), [64 r][128 n] bf16, unswizzled
 constexpr uint32_t SM_LA = SM_V + 16384;        // log_alpha fp32 [64][128]; then tile totals
 constexpr uint32_t SM_GA = SM_LA + 32768;       // Gram rows, 128 rows; then A^T fp32
 constexpr uint32_t SM_GB = SM_GA + 32768;       // Gram columns, 160 rows; then T, X, T'
@@ -110,6 +110,8 @@ struct Misc {
 };
 
 constexpr uint32_t SMEM_BYTES = SM_MISC + sizeof(Misc);
+constexpr uint32_t SM_BETA = SM_MISC + offsetof(Misc, beta);
+constexpr uint32_t SM_GAMMA = SM_MISC + offsetof(Misc, gamma);
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(64 * FP * 4 <= 32768, "A^T fits SM_GA");
 static_assert(OFF_TMAT % 1024 == 0 && OFF_TMAT + 8192 <= 40960, "T, X and T' fit SM_GB");
@@ -120,8 +122,8 @@ constexpr uint32_t TM_AS = 128;  // bf16 S^T (A operand), 64 columns
 constexpr uint32_t TM_O = 192;   // O^T, 2 x 64 columns (chunk parity)
 constexpr uint32_t TM_GP = 320;  // [Gram; P] rows x 160 block columns, then:
 constexpr uint32_t TM_Y = TM_GP;        //   Y^T fp32, 64 columns
-constexpr uint32_t TM_NY = TM_GP + 64;  //   bf16 -Y^T (A operand), 32 columns
-constexpr uint32_t TM_AD = TM_GP + 64;  //   bf16 Delta^T (A operand), after -Y^T is consumed
+constexpr uint32_t TM_NY = TM_GP + 64;  //   bf16 (V - Y)^T (A operand), 32 columns
+constexpr uint32_t TM_AD = TM_GP + 64;  //   bf16 Delta^T (A operand), after (V - Y)^T is consumed
 constexpr uint32_t TM_D = TM_GP + 96;   //   Delta^T fp32, 64 columns
 constexpr uint32_t TM_COLS = 512;
 
@@ -135,13 +137,14 @@ __host__ __device__ constexpr uint32_t id_tri(int s, bool a_mn) {
 
 enum { TMA_QK = 0, TMA_LA = 1, TMA_V = 2 };
 
-// Optional per-phase cycle stamps of chain 0 (profiling builds only): thread 0
-// uses slots 0-15, thread 128 slots 16-23, the MMA thread slots 24-31.
+// Optional per-phase cycle stamps of chain 0 (profiling builds only), 64 slots
+// per chunk: thread 0 uses slots 0-15, thread 128 slots 16-23, the MMA thread
+// slots 24-31, thread 96 (warp 3) slots 32-39, thread 224 (warp 7) slots 40-47.
 #ifdef KDA_PHASE_PROFILE
-__device__ long long g_phase_clock[4096 * 32];
+__device__ long long g_phase_clock[4096 * 64];
 #define PHASE_STAMP(t, i)                                                                \
   do {                                                                                   \
-    if (tid == (t) && chain == 0 && ci < 4096) g_phase_clock[ci * 32 + (i)] = clock64(); \
+    if (tid == (t) && chain == 0 && ci < 4096) g_phase_clock[ci * 64 + (i)] = clock64(); \
   } while (0)
 #else
 #define PHASE_STAMP(t, i) \
@@ -151,6 +154,8 @@ __device__ long long g_phase_clock[4096 * 32];
 #define PHASE_MARK(i) PHASE_STAMP(0, i)
 #define PHASE_MARK_W4(i) PHASE_STAMP(128, 16 + (i))
 #define PHASE_MARK_MMA(i) PHASE_STAMP(32 * kMmaWarp, 24 + (i))
+#define PHASE_MARK_W3(i) PHASE_STAMP(96, 32 + (i))
+#define PHASE_MARK_W7(i) PHASE_STAMP(224, 40 + (i))
 
 // CTA-wide barrier of all 288 threads, ordered with the tcgen05 operations.
 __device__ __forceinline__ void cta_sync() {
@@ -213,10 +218,10 @@ __device__ bool wait_bar(const Ctx &x, uint64_t *bar, uint32_t parity, int where
   return false;
 }
 
-// 8 consecutive fp32 from shared memory (16-byte aligned).
-__device__ __forceinline__ void ld8(float (&v)[8], const float *p) {
-  const float4 a = *reinterpret_cast<const float4 *>(p);
-  const float4 b = *reinterpret_cast<const float4 *>(p + 4);
+// 8 consecutive fp32 from a 16-byte aligned shared address.
+__device__ __forceinline__ void lds8(float (&v)[8], uint32_t saddr) {
+  const float4 a = ld_shared_f32x4(saddr);
+  const float4 b = ld_shared_f32x4(saddr + 16u);
   v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
@@ -228,7 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
-                        const __grid_constant__ CUtensorMap tm_la, const float *__restrict__ beta,
+                        const __grid_constant__ CUtensorMap tm_la,
+                        const __grid_constant__ CUtensorMap tm_o, const float *__restrict__ beta,
                         const float *__restrict__ init_state,
                         const int32_t *__restrict__ cu_seqlens, int32_t n_seqs, int64_t n_tokens,
                         int32_t H, __nv_bfloat16 *__restrict__ out,
@@ -274,7 +280,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   }
   float beta_pref = 0.f;   // beta of the chunk after the one being built (threads < C)
   if (tid < C) {
-    m.beta[0][tid] = (n_chunks > 0 && tid < len) ? beta[(t0 + tid) * H + h] : 0.f;
+    st_shared_f32(sb + SM_BETA + 4u * tid, (n_chunks > 0 && tid < len) ? beta[(t0 + tid) * H + h] : 0.f);
     beta_pref = (n_chunks > 1 && tid < len - C) ? beta[(t0 + C + tid) * H + h] : 0.f;
   }
   cta_sync();
@@ -303,11 +309,10 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         const int32_t tb = (int32_t)(t0 + (int64_t)C * ci);
         mbar_arrive_expect_tx(&m.bar_v, 16384);
         tma_load_3d(smem + SM_V, &tm_v, &m.bar_v, 0, h, tb);
-        tma_load_3d(smem + SM_V + 8192, &tm_v, &m.bar_v, 64, h, tb);
         m.tma_issued[TMA_V]++;
       };
       prefetch_tensormap(&tm_q); prefetch_tensormap(&tm_k);
-      prefetch_tensormap(&tm_v); prefetch_tensormap(&tm_la);
+      prefetch_tensormap(&tm_v); prefetch_tensormap(&tm_la); prefetch_tensormap(&tm_o);
       issue_la(0); issue_qk(0); issue_v(0);
       for (int ci = 0; ci < n_chunks; ++ci) {
         const uint32_t par = (uint32_t)(ci & 1);
@@ -333,6 +338,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           umma_ss(tmb + TM_GP, ad, bd, ID_GP, ks > 0 ? 1u : 0u);
         }
         umma_commit(&m.bar_gp);
+        PHASE_MARK_MMA(5);
         if (has_next) { issue_la(ci + 1); issue_qk(ci + 1); }   // both tiles consumed
         // [O^T | Y^T] = S^T [Qt; Kt]^T
         if (!wait_bar(cx, &m.bar_om, par, 31, ci)) break;
@@ -346,29 +352,19 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           umma_ts(tmb + TM_Y, a, kd(off + 8192u), ID_N64, ks > 0 ? 1u : 0u);
         }
         umma_commit(&m.bar_m1);
-        // Delta^T = V^T T'^T (needs only T' and this chunk's v tile) ...
-        if (!wait_bar(cx, &m.bar_v, par, 12, ci)) break;
-        m.tma_waited[TMA_V]++;
+        PHASE_MARK_MMA(6);
+        // Delta^T = (V - Y)^T T'^T
+        if (!wait_bar(cx, &m.bar_ny, par, 33, ci)) break;
+        PHASE_MARK_MMA(3);
+        if (has_next) issue_v(ci + 1);   // the (V - Y) pass has read this chunk's v tile
         if (!wait_bar(cx, &m.bar_t, par, 32, ci)) break;
         PHASE_MARK_MMA(2);
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          umma_ss(tmb + TM_D + 16u * ks, mnd(SM_V + ks * 2048u, 8192),
-                  kd(SM_TMAT + ks * 2048u + ks * 32u), id_tri(ks, true), ks > 0 ? 1u : 0u);
-        // ... + (-Y)^T T'^T
-        if (!wait_bar(cx, &m.bar_ny, par, 33, ci)) break;
-        PHASE_MARK_MMA(3);
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
           umma_ts(tmb + TM_D + 16u * ks, tmb + TM_NY + 8u * ks,
-                  kd(SM_TMAT + ks * 2048u + ks * 32u), id_tri(ks, false), 1u);
+                  kd(SM_TMAT + ks * 2048u + ks * 32u), id_tri(ks, false), ks > 0 ? 1u : 0u);
         umma_commit(&m.bar_u);
-        if (has_next) {   // the v tile is free once the Delta MMAs have read it
-          if (!wait_bar(cx, &m.bar_u, par, 34, ci)) break;
-          issue_v(ci + 1);
-        }
         // S^T += Delta^T Kdec ; O^T += Delta^T P^T
         if (!wait_bar(cx, &m.bar_ad, par, 35, ci)) break;
         PHASE_MARK_MMA(4);
@@ -381,6 +377,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                   id_tri(ks, false), 1u);
         }
         umma_commit(&m.bar_m2);
+        PHASE_MARK_MMA(7);
       }
     }
     __syncwarp();
@@ -406,21 +403,38 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       tmem_st_wait();
     }
 
-    // Writes the output rows of a finished chunk (warps 4-7): O^T (TMEM) -> bf16,
-    // one 64-byte row segment per warp store.
-    auto flush_output = [&](int64_t otb, int onv, uint32_t ocol) {
+    // Writes the output rows of a finished chunk (warps 4-7): O^T (TMEM) -> bf16
+    // rows [r][n] staged in an idle Kdec buffer -> one TMA store of the whole
+    // 64 x 128 tile (issued by thread 128, which later waits for its read), or,
+    // for a sequence's ragged last chunk, 16-byte stores of the valid rows.
+    auto flush_output = [&](int64_t otb, int onv, uint32_t ocol, uint32_t stg_off) {
       const int n = lane_base + lane;
-      __nv_bfloat16 *dst = out + (otb * H + h) * D + n;
-      const int64_t rs = (int64_t)H * D;  // elements between consecutive tokens
+      const uint32_t stg = sb + stg_off;
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         uint32_t r[32];
         tmem_ld32(tmem_addr(tm, lane_base, ocol + 32u * part), r);
         tmem_ld_wait(r);
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (32 * part + j < onv)
-            dst[(int64_t)(32 * part + j) * rs] = __float2bfloat16_rn(__uint_as_float(r[j]));
+        for (int j = 0; j < 32; ++j) {
+          const __nv_bfloat16 o = __float2bfloat16_rn(__uint_as_float(r[j]));
+          st_shared_b16(stg + (uint32_t)(32 * part + j) * 256u + 2u * n,
+                        *reinterpret_cast<const uint16_t *>(&o));
+        }
+      }
+      fence_proxy_async_smem();
+      named_sync(3, 128);
+      if (onv == C) {
+        if (tid == 128) {
+          tma_store_3d(&tm_o, smem + stg_off, 0, h, (int32_t)otb);
+          bulk_commit();
+        }
+      } else {
+        for (int e = tid - 128; e < onv * 16; e += 128) {   // row e / 16, 16-byte chunk e % 16
+          const int row = e >> 4, ch = e & 15;
+          *reinterpret_cast<uint4 *>(out + ((otb + row) * H + h) * D + 8 * ch) =
+              ld_shared_v4(stg + (uint32_t)row * 256u + 16u * ch);
+        }
       }
     };
 
@@ -431,7 +445,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     uint32_t swzk[8];  // swizzled byte offset of channel pair cc in a row with row % 8 == k
 #pragma unroll
     for (int k = 0; k < 8; ++k) swzk[k] = ((((cb >> 4) ^ (uint32_t)k) << 4) | (cb & 15u));
-    float *laf = reinterpret_cast<float *>(smem + SM_LA);
+    const uint32_t sla = sb + SM_LA;  // log_alpha tile [64][128] fp32, then the tile totals
 
     // Decay prefix and every operand tile of chunk ci; false if the CTA aborts.
     auto scan_build = [&](int ci) -> bool {
@@ -439,7 +453,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       const int64_t tb = t0 + (int64_t)C * ci;
       const int nv = (int)((len - (int64_t)C * ci) < C ? (len - (int64_t)C * ci) : C);
       if (tid < C && ci > 0) {   // beta of this chunk, prefetch of the next one
-        m.beta[ci & 1][tid] = beta_pref;
+        st_shared_f32(sb + SM_BETA + 4u * ((ci & 1) * C + tid), beta_pref);
         const int64_t rem = len - (int64_t)C * (ci + 1);
         beta_pref = (ci + 1 < n_chunks && tid < rem) ? beta[(tb + C + tid) * H + h] : 0.f;
       }
@@ -452,7 +466,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int row = 16 * ta + j;
-          float2 x = *reinterpret_cast<const float2 *>(laf + row * D + cc);
+          float2 x = ld_shared_f32x2(sla + 4u * (row * D + cc));
           if (row >= nv) x = make_float2(0.f, 0.f);
           s0 = fmaf(x.x, kLog2e, s0);
           s1 = fmaf(x.y, kLog2e, s1);
@@ -460,18 +474,19 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           L1[j] = s1;
         }
         // tile totals, written over this thread's own (already read) first row
-        *reinterpret_cast<float2 *>(laf + (16 * ta) * D + cc) = make_float2(s0, s1);
+        st_shared_f32x2(sla + 4u * ((16 * ta) * D + cc), s0, s1);
       }
       if (compute_sync_abort(&m.abort)) return false;
       PHASE_MARK(9);
       const bool ok_qk = wait_bar(cx, &m.bar_qk, par, 10, ci);
       if (tid == 0 && ok_qk) m.tma_waited[TMA_QK]++;
+      PHASE_MARK(14);
       float st0[4], st1[4], rf0[4], rf1[4];  // tile starts / ends, channels cc, cc + 1
       {
         float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-          const float2 t = *reinterpret_cast<const float2 *>(laf + (16 * b) * D + cc);
+          const float2 t = ld_shared_f32x2(sla + 4u * ((16 * b) * D + cc));
           st0[b] = acc0; st1[b] = acc1;
           acc0 += t.x; acc1 += t.y;
           rf0[b] = acc0; rf1[b] = acc1;
@@ -482,30 +497,20 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       const float ra0 = ta == 0 ? rf0[0] : ta == 1 ? rf0[1] : ta == 2 ? rf0[2] : rf0[3];
       const float ra1 = ta == 0 ? rf1[0] : ta == 1 ? rf1[1] : ta == 2 ? rf1[2] : rf1[3];
       const float tot0 = ra0 - sa0, tot1 = ra1 - sa1;
-      // column-block factors F[a2][ta] = 2^{st_a2 - ref_ta}, a2 = ta..3
-      float fb0[4], fb1[4];
+      uint32_t fb2[4];
 #pragma unroll
-      for (int a2 = 0; a2 < 4; ++a2) {
-        fb0[a2] = ex2(st0[a2] - ra0);
-        fb1[a2] = ex2(st1[a2] - ra1);
-      }
-      const float fs0 = ex2(sa0), fs1 = ex2(sa1);                    // e^{st_a}
-      const float fd0 = ex2(rf0[3] - ra0), fd1 = ex2(rf1[3] - ra1);  // e^{g_C - ref_a}
+      for (int a2 = 0; a2 < 4; ++a2) fb2[a2] = pack_bf16x2(ex2(st0[a2] - ra0), ex2(st1[a2] - ra1));
+      const float fs0 = ex2(sa0), fs1 = ex2(sa1);
+      const uint32_t fd2 = pack_bf16x2(ex2(rf0[3] - ra0), ex2(rf1[3] - ra1));
       if (ta == 0) {
-        m.gamma[cc] = ex2(rf0[3]);
-        m.gamma[cc + 1] = ex2(rf1[3]);
+        st_shared_f32x2(sb + SM_GAMMA + 4u * cc, ex2(rf0[3]), ex2(rf1[3]));
       }
-      // Row-tile bases (column half of cc, first row of tile ta); element (row
-      // 16 ta + j) sits j * 128 + swzk[j & 7] bytes further (128-byte swizzle).
-      // The Gram row operand interleaves tiles: rows 32 a .. 32 a + 15 hold K o E
-      // of tile a and rows 32 a + 16 .. 32 a + 31 hold Q o E of tile a, so each
-      // TMEM lane quadrant of the Gram result belongs to one row tile.
       const uint32_t r0 = 16u * ta * 128u, h64 = hsel * 8192u, h128 = hsel * 16384u;
       const uint32_t bK = sb + SM_K + h64 + r0, bQ = sb + SM_Q + h64 + r0;
       const uint32_t bGA = sb + SM_GA + h128 + 2u * r0, bST = sb + SM_STACK + h128 + r0;
       const uint32_t bKD = sb + SM_KDEC + 16384u * (uint32_t)(ci & 1) + h64 + r0;
       const uint32_t bGB = sb + SM_GB + hsel * (GB_ROWS * 128u) + r0;
-      uint32_t kraw[16], qraw[16];  // all k, q pairs of this thread, loaded up front
+      uint32_t kraw[16], qraw[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         kraw[j] = ld_shared_b32(bK + (uint32_t)j * 128u + swzk[j & 7]);
@@ -514,24 +519,25 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const uint32_t o = (uint32_t)j * 128u + swzk[j & 7];
-        const float2 kk = unpack_bf16x2(kraw[j]);
-        const float2 qq = unpack_bf16x2(qraw[j]);
-        const float e0 = ex2(L0[j]), e1 = ex2(L1[j]);                  // e^{g_r - st_a}
-        const float ec0 = ex2(tot0 - L0[j]), ec1 = ex2(tot1 - L1[j]);  // e^{ref_a - g_r}
-        st_shared_b32(bGA + o, pack_bf16x2(kk.x * e0, kk.y * e1));
-        st_shared_b32(bGA + 2048u + o, pack_bf16x2(qq.x * e0, qq.y * e1));
-        const float kc0 = kk.x * ec0, kc1 = kk.y * ec1;
+        const uint32_t k2 = kraw[j], q2 = qraw[j];
+        const float e0 = ex2(L0[j]), e1 = ex2(L1[j]);
+        const uint32_t e2 = pack_bf16x2(e0, e1);
+        const uint32_t ec2 = pack_bf16x2(ex2(tot0 - L0[j]), ex2(tot1 - L1[j]));
+        st_shared_b32(bGA + o, hmul2_bf16(k2, e2));
+        st_shared_b32(bGA + 2048u + o, hmul2_bf16(q2, e2));
+        const uint32_t kc2 = hmul2_bf16(k2, ec2);
 #pragma unroll
-        for (int a2 = 0; a2 < 4; ++a2) {  // block (a2, ta) of the column operand, row j
+        for (int a2 = 0; a2 < 4; ++a2) {
           if (a2 < ta) continue;
-          st_shared_b32(bGB + 16u * blk(a2, 0) * 128u + o,
-                        pack_bf16x2(kc0 * fb0[a2], kc1 * fb1[a2]));
+          st_shared_b32(bGB + 16u * blk(a2, 0) * 128u + o, hmul2_bf16(kc2, fb2[a2]));
         }
-        const float g0 = e0 * fs0, g1 = e1 * fs1;  // e^{g_r}
-        st_shared_b32(bST + o, pack_bf16x2(qq.x * g0, qq.y * g1));
-        st_shared_b32(bST + 8192u + o, pack_bf16x2(kk.x * g0, kk.y * g1));
-        st_shared_b32(bKD + o, pack_bf16x2(kc0 * fd0, kc1 * fd1));
+        const uint32_t g2 = pack_bf16x2(e0 * fs0, e1 * fs1);
+        st_shared_b32(bST + o, hmul2_bf16(q2, g2));
+        st_shared_b32(bST + 8192u + o, hmul2_bf16(k2, g2));
+        st_shared_b32(bKD + o, hmul2_bf16(kc2, fd2));
       }
+      PHASE_MARK(15);
+      PHASE_MARK_W7(2);
       fence_proxy_async_smem();
       warp_arrive(&m.bar_build, lane);
       return true;
@@ -545,7 +551,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       const uint32_t par = (uint32_t)(ci & 1);
       const int64_t tb = t0 + (int64_t)C * ci;
       const int nv = (int)((len - (int64_t)C * ci) < C ? (len - (int64_t)C * ci) : C);
-      const float *bcur = m.beta[ci & 1];
+      const uint32_t sbeta = sb + SM_BETA + 4u * C * (uint32_t)(ci & 1);  // this chunk's beta
       PHASE_MARK(0);
       if (ci > 0) {  // the previous chunk's state update and output are final
         wait_bar(cx, &m.bar_m2, par ^ 1u, 25, ci - 1);
@@ -563,11 +569,12 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           uint32_t s[32];
           tmem_ld32(tmem_addr(tm, lane_base, TM_S + c0), s);
           tmem_ld_wait(s);
+          if (part == 0) PHASE_MARK_W3(5);
           uint32_t ab[16];
 #pragma unroll
           for (int q8 = 0; q8 < 4; ++q8) {
             float gv[8];
-            ld8(gv, &m.gamma[c0 + 8 * q8]);
+            lds8(gv, sb + SM_GAMMA + 4u * (c0 + 8 * q8));
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
               const int j = 8 * q8 + 2 * jj;
@@ -589,22 +596,21 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       wait_bar(cx, &m.bar_gp, par, 22, ci);
       tc_fence_after();
       PHASE_MARK(3);
+      PHASE_MARK_W3(0);
       {
+        // Warps 0-3 take blocks b = 0, 1 of their row tile, warps 4-7 blocks 2, 3
+        // (b <= a): adjacent block columns, so one TMEM load per warp.
         const int a = q4, j = lane & 15, r = 16 * a + j;
         const bool isq = lane >= 16;
-        const float br = bcur[r];
-        float *amatT = reinterpret_cast<float *>(smem + SM_GA);
-        for (int b = hf; b <= a; b += 2) {
-          __syncwarp();  // key and query lanes diverged in the previous block
-          uint32_t v[16];
-          tmem_ld16(tmem_addr(tm, lane_base, TM_GP + 16u * blk(a, b)), v);
-          tmem_ld_wait(v);
-          if (!isq) {
+        const float br = ld_shared_f32(sbeta + 4u * r);
+        const uint32_t sat = sb + SM_GA;  // A^T, fp32 [i][r], pitch FP
+        const int b0 = 2 * hf, nb = a + 1 - b0 < 2 ? a + 1 - b0 : 2;  // warp-uniform
+        uint32_t v[32];
+        auto block = [&](int b, int off) {
+          if (!isq) {   // entries i >= r of A are never read by the solve
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              const int i = 16 * b + jj;
-              amatT[i * FP + r] = i < r ? br * __uint_as_float(v[jj]) : 0.f;
-            }
+            for (int jj = 0; jj < 16; ++jj)
+              st_shared_f32(sat + 4u * ((16 * b + jj) * FP + r), br * __uint_as_float(v[off + jj]));
           } else {
 #pragma unroll
             for (int g8 = 0; g8 < 2; ++g8) {
@@ -612,16 +618,35 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
               for (int t = 0; t < 4; ++t) {
                 const int jj = 8 * g8 + 2 * t, i = 16 * b + jj;
-                const float lo = i <= r ? __uint_as_float(v[jj]) : 0.f;
-                const float hi = i + 1 <= r ? __uint_as_float(v[jj + 1]) : 0.f;
+                const float lo = i <= r ? __uint_as_float(v[off + jj]) : 0.f;
+                const float hi = i + 1 <= r ? __uint_as_float(v[off + jj + 1]) : 0.f;
                 w[t] = pack_bf16x2(lo, hi);
               }
               st_shared_v4(sb + SM_PMAT + sw128_offset(r, (16 * b + 8 * g8) * 2), w[0], w[1],
                            w[2], w[3]);
             }
           }
+        };
+        const uint32_t src = tmem_addr(tm, lane_base, TM_GP + 16u * blk(a, b0));
+        if (nb == 2) {
+          tmem_ld32(src, v);
+          tmem_ld_wait(v);
+          PHASE_MARK_W3(3);
+          block(b0, 0);
+          PHASE_MARK_W3(4);
+          block(b0 + 1, 16);
+        } else if (nb == 1) {
+          uint32_t w[16];
+          tmem_ld16(src, w);
+          tmem_ld_wait(w);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = w[i];
+          block(b0, 0);
         }
       }
+      PHASE_MARK(10);
+      PHASE_MARK_W3(1);
+      PHASE_MARK_W7(0);
       fence_proxy_async_smem();
       tc_fence_before();
       warp_arrive(&m.bar_om, lane);  // S^T operand ready, Gram columns free: O+M1 may start
@@ -631,42 +656,47 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 
       if (warp < 4) {
         // ---- T = (I + A)^{-1} and T' = T Diag(beta) (warps 0-3)
-        const float *amatT = reinterpret_cast<const float *>(smem + SM_GA);  // A^T, [i][r]
-        float *tinv = reinterpret_cast<float *>(smem + SM_GB + OFF_TINV);    // T, [r][i]
-        float *xbuf = reinterpret_cast<float *>(smem + SM_GB + OFF_XBUF);
+        const uint32_t sat = sb + SM_GA;                // A^T, fp32 [i][r], pitch FP
+        const uint32_t stv = sb + SM_GB + OFF_TINV;     // T, fp32 [r][i], pitch FP
+        const uint32_t sxb = sb + SM_GB + OFF_XBUF;     // 4 blocks of 16 x XP fp32
         if (warp < 2) {
-          // Diagonal blocks by column-oriented forward substitution: lane owns
-          // column j of block a; after step m, t[m] is final and is eliminated
-          // from every later row.
+          // Diagonal 16 x 16 blocks by column-oriented forward substitution: lane
+          // owns column j of block a; after step m, t[m] is final and is eliminated
+          // from every later row.  Columns stream through a ring, three steps ahead.
           const int a = 2 * warp + (lane >> 4), j = lane & 15, b0 = 16 * a;
           float t[16];
 #pragma unroll
           for (int r = 0; r < 16; ++r) t[r] = (r == j) ? 1.f : 0.f;
-          float col[16], nxt[16];  // column mc of the block, and the next one in flight
-          ld8(*reinterpret_cast<float(*)[8]>(col), amatT + b0 * FP + b0);
-          ld8(*reinterpret_cast<float(*)[8]>(col + 8), amatT + b0 * FP + b0 + 8);
+          float cbuf[4][16];
+#pragma unroll
+          for (int p = 0; p < 3; ++p) {
+            lds8(*reinterpret_cast<float(*)[8]>(cbuf[p]), sat + 4u * ((b0 + p) * FP + b0));
+            lds8(*reinterpret_cast<float(*)[8]>(cbuf[p] + 8), sat + 4u * ((b0 + p) * FP + b0 + 8));
+          }
 #pragma unroll
           for (int mc = 0; mc < 15; ++mc) {
-            if (mc + 1 < 15) {
-              ld8(*reinterpret_cast<float(*)[8]>(nxt), amatT + (b0 + mc + 1) * FP + b0);
-              ld8(*reinterpret_cast<float(*)[8]>(nxt + 8), amatT + (b0 + mc + 1) * FP + b0 + 8);
+            if (mc + 3 < 15) {
+              float *nb = cbuf[(mc + 3) & 3];
+              lds8(*reinterpret_cast<float(*)[8]>(nb), sat + 4u * ((b0 + mc + 3) * FP + b0));
+              lds8(*reinterpret_cast<float(*)[8]>(nb + 8), sat + 4u * ((b0 + mc + 3) * FP + b0 + 8));
             }
             const float tmv = t[mc];
+            const float *col = cbuf[mc & 3];
 #pragma unroll
             for (int r = mc + 1; r < 16; ++r) t[r] = fmaf(-col[r], tmv, t[r]);
-#pragma unroll
-            for (int r = 0; r < 16; ++r) col[r] = nxt[r];
           }
           // T (fp32, for the block recursion) and T' = T Diag(beta) (bf16 MMA operand;
           // the block's upper triangle is zero because t[r] = 0 for r < j).
-          const float bj = bcur[b0 + j];
-          __nv_bfloat16 *tp = reinterpret_cast<__nv_bfloat16 *>(smem + SM_TMAT);
+          const float bj = ld_shared_f32(sbeta + 4u * (b0 + j));
 #pragma unroll
           for (int r = 0; r < 16; ++r) {
-            tinv[(b0 + r) * FP + b0 + j] = t[r];
-            tp[sw128_offset(b0 + r, (b0 + j) * 2) >> 1] = __float2bfloat16_rn(t[r] * bj);
+            st_shared_f32(stv + 4u * ((b0 + r) * FP + b0 + j), t[r]);
+            const __nv_bfloat16 tb16 = __float2bfloat16_rn(t[r] * bj);
+            st_shared_b16(sb + SM_TMAT + sw128_offset(b0 + r, (b0 + j) * 2),
+                          *reinterpret_cast<const uint16_t *>(&tb16));
           }
         }
+        PHASE_MARK(11);
         named_sync(2, 128);
         // Off-diagonal blocks, block-recursive: 16 -> 32 (blocks (1,0), (3,2)), then
         // 32 -> 64 (blocks (2,0), (2,1), (3,0), (3,1)), TF32 warp MMAs.
@@ -676,54 +706,59 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk) {
             const int kc = 16 * mb + 8 * kk;
-            const uint32_t a0 = to_tf32(amatT[(kc + t4) * FP + 16 * ab + g]);
-            const uint32_t a1 = to_tf32(amatT[(kc + t4) * FP + 16 * ab + g + 8]);
-            const uint32_t a2 = to_tf32(amatT[(kc + t4 + 4) * FP + 16 * ab + g]);
-            const uint32_t a3 = to_tf32(amatT[(kc + t4 + 4) * FP + 16 * ab + g + 8]);
-            const float *b0p = tinv + (kc + t4) * FP + tcol + g;
-            const float *b1p = tinv + (kc + t4 + 4) * FP + tcol + g;
-            mma_tf32_16x8x8(acc[0], a0, a1, a2, a3, to_tf32(b0p[0]), to_tf32(b1p[0]));
-            mma_tf32_16x8x8(acc[1], a0, a1, a2, a3, to_tf32(b0p[8]), to_tf32(b1p[8]));
+            const uint32_t a0 = to_tf32(ld_shared_f32(sat + 4u * ((kc + t4) * FP + 16 * ab + g)));
+            const uint32_t a1 = to_tf32(ld_shared_f32(sat + 4u * ((kc + t4) * FP + 16 * ab + g + 8)));
+            const uint32_t a2 = to_tf32(ld_shared_f32(sat + 4u * ((kc + t4 + 4) * FP + 16 * ab + g)));
+            const uint32_t a3 = to_tf32(ld_shared_f32(sat + 4u * ((kc + t4 + 4) * FP + 16 * ab + g + 8)));
+            const uint32_t b0p = stv + 4u * ((kc + t4) * FP + tcol + g);
+            const uint32_t b1p = stv + 4u * ((kc + t4 + 4) * FP + tcol + g);
+            mma_tf32_16x8x8(acc[0], a0, a1, a2, a3, to_tf32(ld_shared_f32(b0p)),
+                            to_tf32(ld_shared_f32(b1p)));
+            mma_tf32_16x8x8(acc[1], a0, a1, a2, a3, to_tf32(ld_shared_f32(b0p + 32u)),
+                            to_tf32(ld_shared_f32(b1p + 32u)));
           }
         };
         // ... and acc (+)= T_{ar} X with T row-major (pitch FP), X a 16 x 16 block (pitch XP).
-        auto mul_TX = [&](float (&acc)[2][4], int ar, int ac, const float *x) {
+        auto mul_TX = [&](float (&acc)[2][4], int ar, int ac, uint32_t x) {
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk) {
-            const float *tq = tinv + (16 * ar) * FP + 16 * ac + 8 * kk;
-            const uint32_t a0 = to_tf32(tq[g * FP + t4]);
-            const uint32_t a1 = to_tf32(tq[(g + 8) * FP + t4]);
-            const uint32_t a2 = to_tf32(tq[g * FP + t4 + 4]);
-            const uint32_t a3 = to_tf32(tq[(g + 8) * FP + t4 + 4]);
-            const float *x0 = x + (8 * kk + t4) * XP + g;
-            const float *x1 = x + (8 * kk + t4 + 4) * XP + g;
-            mma_tf32_16x8x8(acc[0], a0, a1, a2, a3, to_tf32(x0[0]), to_tf32(x1[0]));
-            mma_tf32_16x8x8(acc[1], a0, a1, a2, a3, to_tf32(x0[8]), to_tf32(x1[8]));
+            const uint32_t tq = stv + 4u * ((16 * ar) * FP + 16 * ac + 8 * kk);
+            const uint32_t a0 = to_tf32(ld_shared_f32(tq + 4u * (g * FP + t4)));
+            const uint32_t a1 = to_tf32(ld_shared_f32(tq + 4u * ((g + 8) * FP + t4)));
+            const uint32_t a2 = to_tf32(ld_shared_f32(tq + 4u * (g * FP + t4 + 4)));
+            const uint32_t a3 = to_tf32(ld_shared_f32(tq + 4u * ((g + 8) * FP + t4 + 4)));
+            const uint32_t x0 = x + 4u * ((8 * kk + t4) * XP + g);
+            const uint32_t x1 = x + 4u * ((8 * kk + t4 + 4) * XP + g);
+            mma_tf32_16x8x8(acc[0], a0, a1, a2, a3, to_tf32(ld_shared_f32(x0)),
+                            to_tf32(ld_shared_f32(x1)));
+            mma_tf32_16x8x8(acc[1], a0, a1, a2, a3, to_tf32(ld_shared_f32(x0 + 32u)),
+                            to_tf32(ld_shared_f32(x1 + 32u)));
           }
         };
-        auto store_blk = [&](float *dst, int pitch, const float (&acc)[2][4], float sgn) {
+        auto store_blk = [&](uint32_t dst, int pitch, const float (&acc)[2][4], float sgn) {
 #pragma unroll
           for (int nh = 0; nh < 2; ++nh) {
-            dst[g * pitch + 8 * nh + 2 * t4] = sgn * acc[nh][0];
-            dst[g * pitch + 8 * nh + 2 * t4 + 1] = sgn * acc[nh][1];
-            dst[(g + 8) * pitch + 8 * nh + 2 * t4] = sgn * acc[nh][2];
-            dst[(g + 8) * pitch + 8 * nh + 2 * t4 + 1] = sgn * acc[nh][3];
+            st_shared_f32x2(dst + 4u * (g * pitch + 8 * nh + 2 * t4), sgn * acc[nh][0],
+                            sgn * acc[nh][1]);
+            st_shared_f32x2(dst + 4u * ((g + 8) * pitch + 8 * nh + 2 * t4), sgn * acc[nh][2],
+                            sgn * acc[nh][3]);
           }
         };
         // Final block T_ab: fp32 into T, and T' = T Diag(beta) as bf16 pairs.
         auto store_T = [&](int ab, int bb, const float (&acc)[2][4]) {
-          store_blk(tinv + (16 * ab) * FP + 16 * bb, FP, acc, -1.f);
+          store_blk(stv + 4u * ((16 * ab) * FP + 16 * bb), FP, acc, -1.f);
 #pragma unroll
           for (int nh = 0; nh < 2; ++nh) {
             const int col = 16 * bb + 8 * nh + 2 * t4;
-            const float b0v = bcur[col], b1v = bcur[col + 1];
+            const float2 bv = ld_shared_f32x2(sbeta + 4u * col);
+            const float b0v = bv.x, b1v = bv.y;
             const uint32_t lo = pack_bf16x2(-acc[nh][0] * b0v, -acc[nh][1] * b1v);
             const uint32_t hi = pack_bf16x2(-acc[nh][2] * b0v, -acc[nh][3] * b1v);
             st_shared_b32(sb + SM_TMAT + sw128_offset(16 * ab + g, col * 2), lo);
             st_shared_b32(sb + SM_TMAT + sw128_offset(16 * ab + g + 8, col * 2), hi);
           }
         };
-        float *xw = xbuf + warp * 16 * XP;
+        const uint32_t xw = sxb + 4u * (warp * 16 * XP);
         if (warp < 2) {  // level 16 -> 32: block (1,0) on warp 0, (3,2) on warp 1
           const int ab = 2 * warp + 1, bb = 2 * warp;
           float acc[2][4] = {};
@@ -734,6 +769,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           mul_TX(o, ab, ab, xw);  // T_ab = -T_aa X
           store_T(ab, bb, o);
         }
+        PHASE_MARK(12);
         named_sync(2, 128);
         {  // level 32 -> 64: warp w -> block (2 + w/2, w%2)
           const int ab = 2 + (warp >> 1), bb = warp & 1;
@@ -741,38 +777,53 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           // X_{ab} = A_{ab,0:2} T_{0:2, bb} = sum_{m=bb}^{1} A_{ab,m} T_{m,bb}
           for (int mb = bb; mb < 2; ++mb) mul_AT(acc, ab, mb, 16 * bb);
           store_blk(xw, XP, acc, 1.f);
+          PHASE_MARK(13);
           named_sync(2, 128);
           // T_{ab} = -sum_{k=2}^{ab} T_{ab,k} X_{k,bb}
           float o[2][4] = {};
-          for (int k = 2; k <= ab; ++k) mul_TX(o, ab, k, xbuf + (2 * (k - 2) + bb) * 16 * XP);
+          for (int k = 2; k <= ab; ++k) mul_TX(o, ab, k, sxb + 4u * ((2 * (k - 2) + bb) * 16 * XP));
           store_T(ab, bb, o);
         }
+        PHASE_MARK_W3(2);
         fence_proxy_async_smem();  // T' is an MMA operand
         warp_arrive(&m.bar_t, lane);
         PHASE_MARK(5);
       } else {
-        // ---- previous chunk's output rows, then -Y^T as a bf16 A operand (warps 4-7)
-        PHASE_MARK_W4(0);
-        if (ci > 0) flush_output(prev_tb, prev_nv, TM_O + 64u * (par ^ 1u));
-        PHASE_MARK_W4(1);
+        // ---- (V - Y)^T as a bf16 A operand, then the previous chunk's output rows
+        // (warps 4-7; lane n of quadrant q4 is value channel n)
         wait_bar(cx, &m.bar_m1, par, 24, ci);
         tc_fence_after();
+        const bool ok_v = wait_bar(cx, &m.bar_v, par, 12, ci);
+        if (tid == 128 && ok_v) m.tma_waited[TMA_V]++;
         PHASE_MARK_W4(2);
+        {
+          const uint32_t vb = sb + SM_V + 2u * (lane_base + lane);
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-          uint32_t y[32];
-          tmem_ld32(tmem_addr(tm, lane_base, TM_Y + 32u * part), y);
-          tmem_ld_wait(y);
-          uint32_t p[16];
+          for (int part = 0; part < 2; ++part) {
+            uint32_t y[32];
+            tmem_ld32(tmem_addr(tm, lane_base, TM_Y + 32u * part), y);
+            tmem_ld_wait(y);
+            uint32_t p[16];
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj)
-            p[jj] = pack_bf16x2(-__uint_as_float(y[2 * jj]), -__uint_as_float(y[2 * jj + 1]));
-          tmem_st16(tmem_addr(tm, lane_base, TM_NY + 16u * part), p);
+            for (int jj = 0; jj < 16; ++jj) {
+              const uint32_t row = 32u * part + 2u * jj;
+              const float v0 = __uint_as_float(ld_shared_u16(vb + row * 256u) << 16);
+              const float v1 = __uint_as_float(ld_shared_u16(vb + (row + 1u) * 256u) << 16);
+              p[jj] = pack_bf16x2(v0 - __uint_as_float(y[2 * jj]), v1 - __uint_as_float(y[2 * jj + 1]));
+            }
+            tmem_st16(tmem_addr(tm, lane_base, TM_NY + 16u * part), p);
+          }
+          tmem_st_wait();
         }
-        tmem_st_wait();
         tc_fence_before();
         warp_arrive(&m.bar_ny, lane);
         PHASE_MARK_W4(3);
+        PHASE_MARK_W7(1);
+        PHASE_MARK_W4(0);
+        // staging: the Kdec buffer of chunks ci - 1 and ci + 1, idle until the next build
+        if (ci > 0) flush_output(prev_tb, prev_nv, TM_O + 64u * (par ^ 1u), SM_KDEC + 16384u * (par ^ 1u));
+        if (tid == 128) bulk_wait_read_all();   // staging free before the next build
+        PHASE_MARK_W4(1);
       }
 
       // ---- bf16 Delta^T, the A operand of the state and output updates
@@ -804,7 +855,10 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (!failed && n_chunks > 0) {
       wait_bar(cx, &m.bar_m2, (uint32_t)((n_chunks - 1) & 1), 26, n_chunks - 1);
       tc_fence_after();
-      if (warp >= 4) flush_output(prev_tb, prev_nv, TM_O + 64u * (uint32_t)((n_chunks - 1) & 1));
+      if (warp >= 4) {
+        flush_output(prev_tb, prev_nv, TM_O + 64u * (uint32_t)((n_chunks - 1) & 1), SM_KDEC);
+        if (tid == 128) bulk_wait_all();
+      }
     }
     const bool aborted = compute_sync_abort(&m.abort);
     if (!failed && !aborted && final_state) {
@@ -820,6 +874,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           final_state[sbase + (int64_t)(c0 + j) * D + n] = __uint_as_float(r[j]);
       }
     }
+    if (tid == 128) bulk_wait_all();  // no output store outlives the CTA, on any path
   }
 
   // ---- teardown (all warps)
@@ -878,16 +933,17 @@ cudaError_t launch_chunk_fwd_bf16_tc(const ChunkArgs &a, cudaStream_t stream) {
   if (chains == 0) return cudaSuccess;
   if (chains > 0x7fffffffLL || a.n_tokens > 0x7fffffffLL - C) return cudaErrorInvalidValue;
   if (!encode_fn()) return cudaErrorNotSupported;
-  CUtensorMap mq, mk, mv, mla;
+  CUtensorMap mq, mk, mv, mla, mo;
   memset(&mq, 0, sizeof(mq)); memset(&mk, 0, sizeof(mk));
-  memset(&mv, 0, sizeof(mv)); memset(&mla, 0, sizeof(mla));
+  memset(&mv, 0, sizeof(mv)); memset(&mla, 0, sizeof(mla)); memset(&mo, 0, sizeof(mo));
   if (a.n_tokens > 0) {
     const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     if (!make_map(&mq, a.q, bf, 2, a.n_tokens, a.H, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&mk, a.k, bf, 2, a.n_tokens, a.H, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mv, a.v, bf, 2, a.n_tokens, a.H, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mv, a.v, bf, 2, a.n_tokens, a.H, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map(&mla, a.log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.n_tokens, a.H, 128,
-                  CU_TENSOR_MAP_SWIZZLE_NONE))
+                  CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&mo, a.out, bf, 2, a.n_tokens, a.H, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   }
   cudaError_t e = cudaFuncSetAttribute(kda_chunk_fwd_tc_kernel,
@@ -900,7 +956,7 @@ cudaError_t launch_chunk_fwd_bf16_tc(const ChunkArgs &a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if ((uint32_t)fa.numRegs < kLaunchRegs) return cudaErrorNotSupported;
   kda_chunk_fwd_tc_kernel<<<(unsigned)chains, kThreads, SMEM_BYTES, stream>>>(
-      mq, mk, mv, mla, a.beta, a.init_state, a.cu_seqlens, a.n_seqs, a.n_tokens, a.H,
+      mq, mk, mv, mla, mo, a.beta, a.init_state, a.cu_seqlens, a.n_seqs, a.n_tokens, a.H,
       static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.status);
   return cudaGetLastError();
 }

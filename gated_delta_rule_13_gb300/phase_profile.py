@@ -22,13 +22,21 @@ from . import _build
 PHASES = ["wait m2(prev) + sync", "S pass", "wait Gram MMAs", "A/P epilogue + sync",
           "solve (warps 0-3)", "wait Delta MMAs", "Delta pass", "scan + build (next)",
           "loop"]
-# Extra stamps, printed as offsets from the chunk's first stamp: thread 0 slot 9
-# (this chunk's build started, stamped during the previous iteration), thread 128
-# (warp 4) slots 16-19, the MMA thread slots 24-28.
-EXTRA = {9: "t0: build of this chunk started (prev. iteration)", 16: "w4: flush start",
-         17: "w4: flush done", 18: "w4: O+Y MMAs done", 19: "w4: -Y pass done",
-         24: "mma: operands built, Gram issue", 25: "mma: O+Y issue", 26: "mma: T' ready",
-         27: "mma: -Y ready", 28: "mma: Delta ready, M2 issue"}
+# Extra stamps, printed as offsets from the chunk's first stamp.  Slots 9, 14
+# and 15 belong to the build of this chunk, which runs in the previous iteration.
+EXTRA = {9: "t0: build of this chunk: decay prefix done", 14: "t0: build: q/k tile arrived",
+         15: "t0: build done (before arrive)", 10: "t0: A/P done (before sync)",
+         11: "t0: diagonal blocks done", 12: "t0: level 16->32 done", 13: "t0: level 32->64 X stored",
+         16: "w4: flush start", 17: "w4: flush done", 18: "w4: O+Y MMAs done",
+         19: "w4: -Y pass done", 24: "mma: operands built, Gram issue",
+         25: "mma: O+Y issue", 26: "mma: T' ready", 27: "mma: -Y ready",
+         28: "mma: Delta ready, M2 issue", 29: "mma: Gram committed", 30: "mma: O+Y committed",
+         31: "mma: M2 committed", 32: "w3: Gram waited", 33: "w3: A/P done (before sync)",
+         34: "w3: solve done", 35: "w3: A/P TMEM load returned", 36: "w3: A/P first block done",
+         37: "w3: S pass first TMEM load returned", 48: "w12: flush start",
+         49: "w12: flush done", 40: "w7: A/P done (before sync)", 41: "w7: -Y pass done",
+         42: "w7: build done (before arrive)"}
+SLOTS = 64
 
 
 def build_profiling_library() -> str:
@@ -59,9 +67,9 @@ def main(workload: str = "k3_h96_t32768") -> None:
                           x["cu_seqlens"])
     torch.cuda.synchronize()
     n_chunks = min(4096, (int(x["lengths"][0]) + 63) // 64)
-    buf = (ctypes.c_longlong * (4096 * 32))()
-    kda.library().kda_debug_phase_clock(buf, 4096 * 32)
-    raw = np.array(buf[:], dtype=np.int64).reshape(4096, 32)[:n_chunks]
+    buf = (ctypes.c_longlong * (4096 * SLOTS))()
+    kda.library().kda_debug_phase_clock(buf, 4096 * SLOTS)
+    raw = np.array(buf[:], dtype=np.int64).reshape(4096, SLOTS)[:n_chunks]
     stamps = raw[:, :len(PHASES)]
     # interval k = stamp k+1 - stamp k; the last one runs to the next chunk's stamp 0
     nxt = np.concatenate([stamps[1:, :1], stamps[-1:, :1]])
