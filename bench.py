@@ -63,6 +63,20 @@ def recorded_traffic(kernel: str, source: str, workload: str):
     return None
 
 
+def max_over_ranks(values, world: int, device="cpu"):
+    """Element-wise maximum of this rank's floats over all ranks (one all_reduce
+    MAX; the identity for a single process).  Used for every time the JSON line
+    reports, so that N replicas are timed by their slowest rank."""
+    values = [float(v) for v in values]
+    if world == 1:
+        return values
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -276,10 +290,7 @@ def run_gpu(args):
     tot_ms = sum(step_ms)
     pre_avg = sum(pre_ms) / len(pre_ms)
     dec_avg = sum(dec_ms) / len(dec_ms)
-    if world > 1:
-        t = torch.tensor([tot_ms, pre_avg, dec_avg], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms, pre_avg, dec_avg = (float(v) for v in t.tolist())
+    tot_ms, pre_avg, dec_avg = max_over_ranks([tot_ms, pre_avg, dec_avg], world, dev)
     status_ok = kda.kda_read_device_status(ws) == kda.KDA_OK
 
     # ---- end to end through the public API with host buffers
@@ -310,7 +321,7 @@ def run_gpu(args):
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = a.elapsed_time(b) / n_e2e
+        e2e_ms, = max_over_ranks([a.elapsed_time(b) / n_e2e], world, dev)
         e2e = {"value": world * n_tok / (e2e_ms / 1000.0), "unit": "tokens/s",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
         del host, dev_bufs
