@@ -43,8 +43,8 @@
 //
 // Pipeline.  O^T is double-buffered in TMEM and Kdec in shared memory, so the
 // next chunk's operand build overlaps this chunk's state MMAs, the triangular
-// solve (warps 0-3) overlaps the (V - Y) pass and the previous chunk's output
-// stores (warps 4-7), and the Gram MMAs of chunk c+1 overlap the state pass of c+1.
+// solve (warps 0-3) overlaps the previous chunk's output stores and the (V - Y)
+// pass (warps 4-7), and the Gram MMAs of chunk c+1 overlap the state pass of c+1.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -103,7 +103,7 @@ struct Misc {
   float gamma[D];    // Gamma_C = e^{g_C} per key channel
   uint64_t bar_qk, bar_la, bar_v;                     // TMA arrivals
   uint64_t bar_gp, bar_m1, bar_u, bar_m2, bar_fin;    // MMA completions
-  uint64_t bar_build, bar_om, bar_t, bar_ny, bar_ad;  // operands ready (one arrival per warp)
+  uint64_t bar_build, bar_om, bar_t1, bar_t, bar_ny, bar_ad;  // operands ready (one arrival per warp)
   uint32_t tmem_base;
   int abort;
   uint32_t tma_issued[3], tma_waited[3];  // per TMA barrier: phases issued / consumed
@@ -130,6 +130,8 @@ constexpr uint32_t TM_COLS = 512;
 constexpr uint32_t ID_GP = idesc_bf16(128, GB_ROWS, false, false);
 constexpr uint32_t ID_N64 = idesc_bf16(128, 64, false, false);
 constexpr uint32_t ID_KM128 = idesc_bf16(128, 128, false, true);
+constexpr uint32_t ID_N32 = idesc_bf16(128, 32, false, false);
+constexpr uint32_t ID_N16 = idesc_bf16(128, 16, false, false);
 // Triangle-trimmed products: K step s writes output columns 16 s .. 63.
 __host__ __device__ constexpr uint32_t id_tri(int s, bool a_mn) {
   return idesc_bf16(128, 64 - 16 * s, a_mn, false);
@@ -268,7 +270,8 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     mbar_init(&m.bar_gp, 1); mbar_init(&m.bar_m1, 1); mbar_init(&m.bar_u, 1);
     mbar_init(&m.bar_m2, 1); mbar_init(&m.bar_fin, 1);
     mbar_init(&m.bar_build, kComputeWarps); mbar_init(&m.bar_om, kComputeWarps);
-    mbar_init(&m.bar_t, kComputeWarps / 2); mbar_init(&m.bar_ny, kComputeWarps / 2);
+    mbar_init(&m.bar_t1, kComputeWarps / 2); mbar_init(&m.bar_t, kComputeWarps / 2);
+    mbar_init(&m.bar_ny, kComputeWarps / 2);
     mbar_init(&m.bar_ad, kComputeWarps);
     fence_mbarrier_init();
     m.abort = 0;
@@ -353,17 +356,29 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         umma_commit(&m.bar_m1);
         PHASE_MARK_MMA(6);
-        // Delta^T = (V - Y)^T T'^T
+        // Delta^T = (V - Y)^T T'^T, K step s covering tokens 16 s .. 16 s + 15 and
+        // writing only output columns r >= 16 s (T' is lower triangular).  Output
+        // columns 0-31 and K steps 2, 3 need only the diagonal and 16 -> 32 blocks
+        // of T' and are issued as soon as those exist; the two remaining products
+        // wait for the 32 -> 64 blocks.
         if (!wait_bar(cx, &m.bar_ny, par, 33, ci)) break;
         PHASE_MARK_MMA(3);
         if (has_next) issue_v(ci + 1);   // the (V - Y) pass has read this chunk's v tile
+        if (!wait_bar(cx, &m.bar_t1, par, 37, ci)) break;
+        tc_fence_after();
+        umma_ts(tmb + TM_D, tmb + TM_NY, kd(SM_TMAT), ID_N32, 0u);                       // r 0-31, s 0
+        umma_ts(tmb + TM_D + 16u, tmb + TM_NY + 8u, kd(SM_TMAT + 16u * 128u + 32u), ID_N16,
+                1u);                                                                   // r 16-31, s 1
+        umma_ts(tmb + TM_D + 32u, tmb + TM_NY + 16u, kd(SM_TMAT + 32u * 128u + 64u), ID_N32,
+                0u);                                                                   // r 32-63, s 2
+        umma_ts(tmb + TM_D + 48u, tmb + TM_NY + 24u, kd(SM_TMAT + 48u * 128u + 96u), ID_N16,
+                1u);                                                                   // r 48-63, s 3
         if (!wait_bar(cx, &m.bar_t, par, 32, ci)) break;
         PHASE_MARK_MMA(2);
         tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          umma_ts(tmb + TM_D + 16u * ks, tmb + TM_NY + 8u * ks,
-                  kd(SM_TMAT + ks * 2048u + ks * 32u), id_tri(ks, false), ks > 0 ? 1u : 0u);
+        umma_ts(tmb + TM_D + 32u, tmb + TM_NY, kd(SM_TMAT + 32u * 128u), ID_N32, 1u);        // r 32-63, s 0
+        umma_ts(tmb + TM_D + 32u, tmb + TM_NY + 8u, kd(SM_TMAT + 32u * 128u + 32u), ID_N32,
+                1u);                                                                   // r 32-63, s 1
         umma_commit(&m.bar_u);
         // S^T += Delta^T Kdec ; O^T += Delta^T P^T
         if (!wait_bar(cx, &m.bar_ad, par, 35, ci)) break;
@@ -697,7 +712,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           }
         }
         PHASE_MARK(11);
-        named_sync(2, 128);
+        __syncwarp();   // the 16 -> 32 level of a warp reads only that warp's diagonal blocks
         // Off-diagonal blocks, block-recursive: 16 -> 32 (blocks (1,0), (3,2)), then
         // 32 -> 64 (blocks (2,0), (2,1), (3,0), (3,1)), TF32 warp MMAs.
         const int g = lane >> 2, t4 = lane & 3;
@@ -771,6 +786,8 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         PHASE_MARK(12);
         named_sync(2, 128);
+        fence_proxy_async_smem();   // diagonal and 16 -> 32 blocks of T' are MMA operands
+        warp_arrive(&m.bar_t1, lane);
         {  // level 32 -> 64: warp w -> block (2 + w/2, w%2)
           const int ab = 2 + (warp >> 1), bb = warp & 1;
           float acc[2][4] = {};
@@ -789,8 +806,13 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         warp_arrive(&m.bar_t, lane);
         PHASE_MARK(5);
       } else {
-        // ---- (V - Y)^T as a bf16 A operand, then the previous chunk's output rows
-        // (warps 4-7; lane n of quadrant q4 is value channel n)
+        // ---- the previous chunk's output rows (while the O+Y MMAs run), then
+        // (V - Y)^T as a bf16 A operand (warps 4-7; lane n of quadrant q4 is value
+        // channel n).  Staging: the Kdec buffer of chunks ci - 1 and ci + 1, idle
+        // until the next build.
+        PHASE_MARK_W4(0);
+        if (ci > 0) flush_output(prev_tb, prev_nv, TM_O + 64u * (par ^ 1u), SM_KDEC + 16384u * (par ^ 1u));
+        PHASE_MARK_W4(1);
         wait_bar(cx, &m.bar_m1, par, 24, ci);
         tc_fence_after();
         const bool ok_v = wait_bar(cx, &m.bar_v, par, 12, ci);
@@ -817,13 +839,9 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         tc_fence_before();
         warp_arrive(&m.bar_ny, lane);
+        if (tid == 128) bulk_wait_read_all();   // staging free before the next build
         PHASE_MARK_W4(3);
         PHASE_MARK_W7(1);
-        PHASE_MARK_W4(0);
-        // staging: the Kdec buffer of chunks ci - 1 and ci + 1, idle until the next build
-        if (ci > 0) flush_output(prev_tb, prev_nv, TM_O + 64u * (par ^ 1u), SM_KDEC + 16384u * (par ^ 1u));
-        if (tid == 128) bulk_wait_read_all();   // staging free before the next build
-        PHASE_MARK_W4(1);
       }
 
       // ---- bf16 Delta^T, the A operand of the state and output updates
