@@ -211,6 +211,52 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------------------- GPU arm
+def replay_bench(dev, peaks, steps: int = 20, warmup: int = 3, T: int = 4):
+    """kda_decode_replay on 512 sequences x 96 heads x T cached draft tokens with
+    seeded accepted counts in [0, T] (the step after a speculative verification).
+    Algorithmic bytes: one state read and write per unit with an accepted token,
+    plus the accepted tokens' inputs and outputs."""
+    import torch
+    from gated_delta_rule_13_gb300 import inputs, kda
+    B, H = 512, 96
+    d = inputs.decode_inputs(B=B, H=H, steps=T, dtype="bf16", device=dev, seed=17)
+    r = {x: d[x].transpose(0, 1).contiguous() for x in ("q", "k", "v", "log_alpha", "beta")}
+    state = d["state"]
+    g = torch.Generator(device="cpu").manual_seed(17)
+    n = torch.randint(0, T + 1, (B,), generator=g, dtype=torch.int32)
+    n_dev = n.to(dev)
+    out = torch.empty(B, T, H, 128, dtype=torch.bfloat16, device=dev)
+
+    def run():
+        kda.kda_decode_replay(state, r["q"], r["k"], r["v"], r["log_alpha"], r["beta"], n_dev,
+                              out=out)
+
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        run()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    accepted = int(n.sum())
+    active = int((n > 0).sum())
+    nbytes = H * (active * 2 * STATE_BYTES + accepted * (DECODE_BYTES_PER_UNIT - 2 * STATE_BYTES))
+    gbs = nbytes / (ms / 1000.0) / 1e9
+    del d, r, state, out
+    return {"value": gbs, "unit": "GB/s", "ms_per_launch": ms,
+            "workload": f"512 sequences x 96 heads, {T} cached draft tokens, accepted counts "
+                        f"seeded uniform in [0, {T}] (mean {accepted / B:.2f})",
+            "accepted_tokens_per_s": accepted / (ms / 1000.0),
+            "roofline": {"bound": "hbm", "kernel": "kda_decode_replay_kernel", "achieved": gbs,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                         "bytes_per_launch": nbytes}}
+
+
 def prefill_bytes(x, H):
     n_tok = int(x["q"].shape[0])
     n_seqs = int(x["cu_seqlens"].shape[0] - 1)
@@ -326,6 +372,10 @@ def run_gpu(args):
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
         del host, dev_bufs
 
+    replay = replay_bench(dev, peaks)
+    if world > 1:
+        replay["ms_per_launch"], = max_over_ranks([replay["ms_per_launch"]], world, dev)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         heads, T = calibrated_sample(args.workload, args.cpu_seconds)
@@ -368,6 +418,7 @@ def run_gpu(args):
                                 "traffic": recorded_traffic("kda_decode_step_kernel",
                                                             "kda_decode.cu", "decode_b512_h96"),
                                 "bytes_per_launch": dbytes}},
+        "replay": replay,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": 2 * args.steps,

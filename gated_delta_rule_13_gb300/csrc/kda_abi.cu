@@ -180,4 +180,31 @@ int kda_decode_step(float *state, const void *q, const void *k, const void *v,
   return KDA_OK;
 }
 
+int kda_decode_replay(float *state, const void *q, const void *k, const void *v,
+                      const float *log_alpha, const float *beta, const int32_t *n_accept,
+                      int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, int dtype,
+                      void *out, void *stream) {
+  if (B < 0 || T <= 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+  const int d = check_dims(dk, dv, dtype);
+  if (d != KDA_OK) return d;
+  if (!state || !q || !k || !v || !log_alpha || !beta || !n_accept) return KDA_ERR_INVALID_ARG;
+  const size_t esz = dtype == KDA_BF16 ? 2 : 4;
+  if (!aligned16(state) || !aligned(v, 4 * esz) || (out && !aligned(out, 4 * esz)) ||
+      !aligned(q, esz) || !aligned(k, esz) || !aligned(log_alpha, 4) || !aligned(beta, 4) ||
+      !aligned(n_accept, 4))
+    return KDA_ERR_INVALID_ARG;
+  const size_t units = (size_t)B * H;
+  if (out && units > 0 &&
+      ranges_overlap(state, units * dk * dv * sizeof(float), out, units * (size_t)T * dv * esz))
+    return KDA_ERR_INVALID_ARG;
+  const cudaError_t e = kda::launch_decode_replay(state, q, k, v, log_alpha, beta, n_accept, B, T,
+                                                  H, dtype == KDA_BF16, out,
+                                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_CUDA;
+  }
+  return KDA_OK;
+}
+
 }  // extern "C"

@@ -38,6 +38,11 @@ cudaError_t launch_decode_step(float *state, const void *q, const void *k, const
                                const float *log_alpha, const float *beta, int32_t B, int32_t H,
                                bool bf16, void *out, cudaStream_t stream);
 
+cudaError_t launch_decode_replay(float *state, const void *q, const void *k, const void *v,
+                                 const float *log_alpha, const float *beta,
+                                 const int32_t *n_accept, int32_t B, int32_t T, int32_t H,
+                                 bool bf16, void *out, cudaStream_t stream);
+
 cudaError_t launch_chunk_fwd_f32(const ChunkArgs &a, cudaStream_t stream);
 
 // Returns cudaErrorNotSupported if the tensor-map entry point is unavailable.

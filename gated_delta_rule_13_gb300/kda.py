@@ -29,7 +29,7 @@ HEAD_DIM = 128
 # Symbols declared in include/kda.h.
 EXPORTED = ("kda_status_string", "kda_version", "kda_chunk_fwd_workspace_size",
             "kda_chunk_fwd", "kda_read_device_status", "kda_decode_step",
-            "kda_chunk_fwd_noalloc")
+            "kda_chunk_fwd_noalloc", "kda_decode_replay")
 
 _lib = None
 
@@ -68,6 +68,9 @@ def library() -> ctypes.CDLL:
         lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
         lib.kda_chunk_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32,
                                               ctypes.c_int, vp, vp, vp]
+        lib.kda_decode_replay.restype = ctypes.c_int
+        lib.kda_decode_replay.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                          ctypes.c_int, vp, vp]
         lib.kda_decode_step.restype = ctypes.c_int
         lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                         ctypes.c_int, vp, vp]
@@ -231,4 +234,35 @@ def kda_decode_step(state, q, k, v, log_alpha, beta, *, out=None, stream=None):
                                    _ptr(beta), B, H, dk, dv, _dtype_code(q), _ptr(out),
                                    _stream_handle(stream))
     _check(rc, "kda_decode_step")
+    return out
+
+
+def kda_decode_replay(state, q, k, v, log_alpha, beta, n_accept, *, out=None,
+                      output=True, stream=None):
+    """Replays the accepted draft tokens of a speculative decode step in place.
+    state ``[B, H, 128, 128]`` fp32 (updated in place); q, k, v ``[B, T, H, 128]``
+    (bf16 or fp32); log_alpha ``[B, T, H, 128]`` fp32; beta ``[B, T, H]`` fp32;
+    n_accept int32 CUDA tensor ``[B]`` (clamped to [0, T] on the device).
+    Returns out ``[B, T, H, 128]`` (rows t >= n_accept[b] untouched) or None
+    when ``output`` is false."""
+    _need_cuda("state", state, torch.float32)
+    B, H, dk, dv = state.shape
+    _need_cuda("q", q)
+    if q.dim() != 4 or q.shape[0] != B or q.shape[2] != H or q.shape[3] != dk:
+        raise ValueError("q must be [B, T, H, dk]")
+    T = q.shape[1]
+    dt = q.dtype
+    _need_cuda("k", k, dt, (B, T, H, dk))
+    _need_cuda("v", v, dt, (B, T, H, dv))
+    _need_cuda("log_alpha", log_alpha, torch.float32, (B, T, H, dk))
+    _need_cuda("beta", beta, torch.float32, (B, T, H))
+    _need_cuda("n_accept", n_accept, torch.int32, (B,))
+    if out is None and output:
+        out = torch.empty(B, T, H, dv, dtype=dt, device=q.device)
+    if out is not None:
+        _need_cuda("out", out, dt, (B, T, H, dv))
+    rc = library().kda_decode_replay(_ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                                     _ptr(beta), _ptr(n_accept), B, T, H, dk, dv,
+                                     _dtype_code(q), _ptr(out), _stream_handle(stream))
+    _check(rc, "kda_decode_replay")
     return out

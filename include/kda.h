@@ -184,6 +184,38 @@ int kda_decode_step(float *state, const void *q, const void *k, const void *v,
                     const float *log_alpha, const float *beta, int32_t B, int32_t H,
                     int32_t dk, int32_t dv, int dtype, void *out, void *stream);
 
+/*
+ * Replay of accepted draft tokens after speculative-decode verification ("Kimi
+ * K3: 架构、训练与系统全景解析", KDA state replay under speculative decoding: the
+ * per-token projected inputs of the draft tokens are cached instead of a state
+ * per draft position; after verification only the accepted prefix is replayed
+ * in an on-chip recurrence and only the final state is written back).
+ *
+ * For every sequence b and head h, applies the decode step of kda_decode_step
+ * to tokens t = 0 .. n_b - 1 in order, n_b = n_accept[b] clamped to [0, T]:
+ *
+ *   state      [B, H, dk, dv] fp32   read once, overwritten once with the state
+ *                                    after token n_b - 1 (untouched if n_b = 0)
+ *   q, k       [B, T, H, dk]  dtype  cached inputs of the T draft positions
+ *   v          [B, T, H, dv]  dtype
+ *   log_alpha  [B, T, H, dk]  fp32
+ *   beta       [B, T, H]      fp32
+ *   n_accept   [B]            int32, DEVICE memory: accepted tokens per sequence
+ *   out        [B, T, H, dv]  dtype  o_t of every replayed token, or NULL; rows
+ *                                    t >= n_b are not written
+ * Alignment: state 16 bytes; v and out 4 elements; q, k 1 element;
+ * log_alpha, beta and n_accept 4 bytes.
+ * Errors (before any launch): KDA_ERR_INVALID_ARG (NULL pointer other than
+ * out, B < 0, T <= 0, H <= 0, misalignment, `out` overlapping `state`),
+ * KDA_ERR_UNSUPPORTED (dk or dv != 128, unknown dtype), KDA_ERR_CUDA.
+ * No counterpart on the pages' interface (they give none); the layout is this
+ * library's.
+ */
+int kda_decode_replay(float *state, const void *q, const void *k, const void *v,
+                      const float *log_alpha, const float *beta, const int32_t *n_accept,
+                      int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, int dtype,
+                      void *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

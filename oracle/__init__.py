@@ -136,3 +136,28 @@ def decode_step(state, q, k, v, log_alpha, beta, lib: ctypes.CDLL | None = None)
     if rc != 0:
         raise RuntimeError(f"kda_oracle_decode_step failed with code {rc}")
     return out
+
+
+def decode_replay(state, q, k, v, log_alpha, beta, n_accept, lib: ctypes.CDLL | None = None):
+    """Replay of accepted draft tokens after speculative-decode verification
+    ("Kimi K3: 架构、训练与系统全景解析", KDA state replay under speculative
+    decoding: only the accepted prefix of the cached per-token inputs is replayed
+    and only the final state is kept).  For every sequence b, the decode step is
+    applied to tokens t = 0 .. n_b - 1 in order, n_b = n_accept[b] clamped to
+    [0, T].  ``state`` (C-contiguous fp64 ``[B, H, dk, dv]``) is updated in place;
+    q, k ``[B, T, H, dk]``, v ``[B, T, H, dv]``, log_alpha ``[B, T, H, dk]``,
+    beta ``[B, T, H]``.  Returns out ``[B, T, H, dv]``, zero where t >= n_b."""
+    q, k, v, la, b = (_f64(t) for t in (q, k, v, log_alpha, beta))
+    B, T, H, _ = q.shape
+    dv = v.shape[3]
+    n = np.clip(np.asarray(n_accept, dtype=np.int64).reshape(B), 0, T)
+    out = np.zeros((B, T, H, dv), dtype=np.float64)
+    for t in range(T):
+        sel = np.nonzero(n > t)[0]
+        if sel.size == 0:
+            break
+        sub = np.ascontiguousarray(state[sel])
+        out[sel, t] = decode_step(sub, q[sel, t], k[sel, t], v[sel, t], la[sel, t], b[sel, t],
+                                  lib=lib)
+        state[sel] = sub
+    return out

@@ -32,7 +32,7 @@ def declared_functions():
 
 def test_header_declares_expected_entry_points():
     names = declared_functions()
-    for n in ("kda_chunk_fwd", "kda_decode_step", "kda_chunk_fwd_workspace_size",
+    for n in ("kda_chunk_fwd", "kda_decode_step", "kda_decode_replay", "kda_chunk_fwd_workspace_size",
               "kda_status_string", "kda_read_device_status", "kda_version"):
         assert n in names
 
@@ -116,6 +116,32 @@ def _dec(lib, **over):
 ])
 def test_decode_rejects_before_launch(lib, over, code):
     assert _dec(lib, **over) == code
+
+
+def _replay(lib, **over):
+    args = dict(state=A, q=A + 0x1000, k=A + 0x2000, v=A + 0x3000, la=A + 0x4000,
+                beta=A + 0x5000, n=A + 0x6000, B=4, T=3, H=2, dk=128, dv=128, dtype=1,
+                out=A + 0x40000000, stream=None)
+    args.update(over)
+    vp = ctypes.c_void_p
+    return lib.kda_decode_replay(vp(args["state"]), vp(args["q"]), vp(args["k"]), vp(args["v"]),
+                                 vp(args["la"]), vp(args["beta"]), vp(args["n"]), args["B"],
+                                 args["T"], args["H"], args["dk"], args["dv"], args["dtype"],
+                                 vp(args["out"]), vp(args["stream"]))
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(state=None), 1), (dict(q=None), 1), (dict(n=None), 1), (dict(beta=None), 1),
+    (dict(B=-1), 1), (dict(T=0), 1), (dict(H=0), 1), (dict(dk=32), 2), (dict(dtype=3), 2),
+    (dict(k=A + 0x2001), 1), (dict(v=A + 0x3004), 1), (dict(n=A + 0x6002), 1),
+    (dict(out=A + 0x800), 1),                               # out inside the state
+])
+def test_replay_rejects_before_launch(lib, over, code):
+    assert _replay(lib, **over) == code
+
+
+def test_replay_empty_batch_launches_nothing(lib):
+    assert _replay(lib, B=0) == 0
 
 
 def test_read_device_status_null(lib):

@@ -1,0 +1,105 @@
+"""GPU parity of kda_decode_replay (replay of the accepted draft tokens of a
+speculative decode step) against the fp64 oracle."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_delta_rule_13_gb300 import inputs, kda
+from parity_util import TOL, rel_l2
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def replay_inputs(B, T, H, dtype, seed=0):
+    """Cached draft inputs [B, T, H, ...] (the decode generator's T steps)."""
+    d = inputs.decode_inputs(B=B, H=H, steps=T, dtype=dtype, device=DEV, seed=seed)
+    r = {name: d[name].transpose(0, 1).contiguous()
+         for name in ("q", "k", "v", "log_alpha", "beta")}
+    r["state"] = d["state"]
+    return r
+
+
+def _oracle(r, n):
+    state = r["state"].double().cpu().numpy().copy()
+    out = oracle.decode_replay(state, *(r[x].double().cpu().numpy()
+                                        for x in ("q", "k", "v", "log_alpha", "beta")), n)
+    return out, state
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_replay_matches_oracle(dtype):
+    B, T, H = 5, 4, 3
+    r = replay_inputs(B, T, H, dtype, seed=3)
+    n = np.array([0, 1, 4, 2, 9], dtype=np.int32)          # 9 > T is clamped to T
+    state = r["state"].clone()
+    out = torch.full((B, T, H, 128), float("nan"), dtype=r["q"].dtype, device=DEV)
+    kda.kda_decode_replay(state, r["q"], r["k"], r["v"], r["log_alpha"], r["beta"],
+                          torch.as_tensor(n, device=DEV), out=out)
+    torch.cuda.synchronize()
+    ref_out, ref_state = _oracle(r, n)
+    for b in range(B):
+        nb = min(int(n[b]), T)
+        if nb == 0:
+            assert torch.equal(state[b], r["state"][b])     # nothing accepted: untouched
+        else:
+            assert rel_l2(state[b], ref_state[b]) <= TOL[dtype]
+            assert rel_l2(out[b, :nb], ref_out[b, :nb]) <= TOL[dtype]
+        assert torch.isnan(out[b, nb:]).all()               # rejected rows never written
+
+
+def test_replay_equals_consecutive_decode_steps():
+    """Replaying every draft token equals that many kda_decode_step calls."""
+    B, T, H = 3, 5, 4
+    r = replay_inputs(B, T, H, "bf16", seed=5)
+    s1 = r["state"].clone()
+    out = kda.kda_decode_replay(s1, r["q"], r["k"], r["v"], r["log_alpha"], r["beta"],
+                                torch.full((B,), T, dtype=torch.int32, device=DEV))
+    s2 = r["state"].clone()
+    outs = [kda.kda_decode_step(s2, *(r[x][:, t].contiguous()
+                                      for x in ("q", "k", "v", "log_alpha", "beta")))
+            for t in range(T)]
+    torch.cuda.synchronize()
+    assert rel_l2(s1, s2) <= 1e-6
+    assert rel_l2(out, torch.stack(outs, dim=1)) <= 1e-6
+
+
+def test_replay_without_output_updates_state():
+    B, T, H = 2, 3, 2
+    r = replay_inputs(B, T, H, "f32", seed=7)
+    n = np.array([3, 1], dtype=np.int32)
+    state = r["state"].clone()
+    assert kda.kda_decode_replay(state, r["q"], r["k"], r["v"], r["log_alpha"], r["beta"],
+                                 torch.as_tensor(n, device=DEV), output=False) is None
+    torch.cuda.synchronize()
+    _, ref_state = _oracle(r, n)
+    assert rel_l2(state, ref_state) <= TOL["f32"]
+
+
+def test_replay_full_size_sampled_units():
+    """512 sequences x 96 heads x 4 draft tokens (the benchmark's launch
+    configuration) with mixed accepted counts; 48 sampled units against the
+    oracle one by one."""
+    B, T, H = 512, 4, 96
+    r = replay_inputs(B, T, H, "bf16", seed=11)
+    g = np.random.default_rng(11)
+    n = g.integers(0, T + 1, size=B).astype(np.int32)
+    state = r["state"].clone()
+    out = kda.kda_decode_replay(state, r["q"], r["k"], r["v"], r["log_alpha"], r["beta"],
+                                torch.as_tensor(n, device=DEV))
+    torch.cuda.synchronize()
+    units = np.sort(g.choice(B * H, size=48, replace=False))
+    for u in units:
+        b, h = divmod(int(u), H)
+        nb = int(n[b])
+        sub = {x: r[x][b:b + 1, :, h:h + 1] for x in ("q", "k", "v", "log_alpha", "beta")}
+        st = r["state"][b:b + 1, h:h + 1].double().cpu().numpy().copy()
+        ref_out = oracle.decode_replay(st, *(sub[x].double().cpu().numpy()
+                                             for x in ("q", "k", "v", "log_alpha", "beta")),
+                                       np.array([nb]))
+        assert rel_l2(state[b, h], st[0, 0]) <= TOL["bf16"]
+        if nb:
+            assert rel_l2(out[b, :nb, h], ref_out[0, :nb, 0]) <= TOL["bf16"]

@@ -241,10 +241,40 @@ def pin_segment_combine(lib):
         np.testing.assert_allclose(s_in, f_cut[0, h], rtol=1e-12, atol=1e-13)
 
 
+def pin_decode_replay(lib):
+    """Replay of accepted draft tokens ("Kimi K3: 架构、训练与系统全景解析", KDA state
+    replay under speculative decoding): per sequence, the accepted prefix replayed
+    from the cached inputs gives the brute-force transition-matrix outputs and
+    final state (oracle.affine); nothing accepted leaves the state untouched; an
+    accepted count above T is clamped; rows of rejected tokens stay zero."""
+    r = _rng(31)
+    B, T, H, dk, dv = 4, 5, 2, 5, 3
+    q = _unit(r.standard_normal((B, T, H, dk)))
+    k = _unit(r.standard_normal((B, T, H, dk)))
+    v = r.standard_normal((B, T, H, dv))
+    la = -5.0 / (1.0 + np.exp(-r.standard_normal((B, T, H, dk))))
+    b = 1.0 / (1.0 + np.exp(-r.standard_normal((B, T, H))))
+    s0 = 0.3 * r.standard_normal((B, H, dk, dv))
+    n = np.array([0, 2, 5, 7])
+    state = s0.copy()
+    out = oracle.decode_replay(state, q, k, v, la, b, n, lib=lib)
+    for bi in range(B):
+        nb = min(int(n[bi]), T)
+        assert np.all(out[bi, nb:] == 0.0)
+        for h in range(H):
+            if nb == 0:
+                assert np.array_equal(state[bi, h], s0[bi, h])
+                continue
+            o_ref, s_ref = affine.chain(q[bi, :nb, h], k[bi, :nb, h], v[bi, :nb, h],
+                                        la[bi, :nb, h], b[bi, :nb, h], s0[bi, h])
+            np.testing.assert_allclose(out[bi, :nb, h], o_ref, rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(state[bi, h], s_ref, rtol=1e-12, atol=1e-12)
+
+
 PINS = [pin_delta_rule_1d, pin_orthogonal_write_query, pin_orthogonal_write_query_d128,
         pin_beta_zero_closed_form, pin_alpha_one_orthonormal_linear_attention,
         pin_bruteforce_affine, pin_split_invariance, pin_varlen_equals_separate,
-        pin_contraction_bound, pin_decode_step, pin_segment_combine]
+        pin_contraction_bound, pin_decode_step, pin_segment_combine, pin_decode_replay]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
