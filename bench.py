@@ -257,6 +257,52 @@ def replay_bench(dev, peaks, steps: int = 20, warmup: int = 3, T: int = 4):
                          "bytes_per_launch": nbytes}}
 
 
+def layer_ops_bench(dev, peaks, steps: int = 20, warmup: int = 3):
+    """kda_prep_fwd and kda_post_fwd on the K3 layout (one sequence of 32768
+    tokens, 96 heads, bf16).  Algorithmic bytes per token-head: prep reads
+    q, k, v (bf16) and both gate logits and writes q, k, v, log_alpha and beta
+    (2568 B); post reads o and the gate logits and writes the output (768 B)."""
+    import torch
+    from gated_delta_rule_13_gb300 import inputs, kda
+    T, H = 32768, 96
+    x = inputs.layer_inputs([T], H=H, dtype="bf16", device=dev, seed=29)
+    o = x["v_raw"]
+
+    def prep():
+        return kda.kda_prep_fwd(x["q_raw"], x["k_raw"], x["v_raw"], x["conv_w"], x["a_logit"],
+                                x["b_logit"], x["cu_seqlens"])
+
+    y = torch.empty_like(o)
+
+    def post():
+        kda.kda_post_fwd(o, x["g"], x["gamma"], out=y)
+
+    res = {}
+    stream = torch.cuda.current_stream()
+    for name, fn, per_th in (("prep", prep, 2568), ("post", post, 768)):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / steps
+        nbytes = T * H * per_th
+        gbs = nbytes / (ms / 1000.0) / 1e9
+        res[name] = {"value": gbs, "unit": "GB/s", "ms_per_launch": ms,
+                     "tokens_per_s": T / (ms / 1000.0),
+                     "roofline": {"bound": "hbm", "kernel": f"kda_{name}_kernel", "achieved": gbs,
+                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                                  "bytes_per_launch": nbytes}}
+    del x, o, y
+    res["workload"] = "one sequence of 32768 tokens x 96 heads, bf16"
+    return res
+
+
 def prefill_bytes(x, H):
     n_tok = int(x["q"].shape[0])
     n_seqs = int(x["cu_seqlens"].shape[0] - 1)
@@ -373,6 +419,7 @@ def run_gpu(args):
         del host, dev_bufs
 
     replay = replay_bench(dev, peaks)
+    layer_ops = layer_ops_bench(dev, peaks)
     if world > 1:
         replay["ms_per_launch"], = max_over_ranks([replay["ms_per_launch"]], world, dev)
 
@@ -419,6 +466,7 @@ def run_gpu(args):
                                                             "kda_decode.cu", "decode_b512_h96"),
                                 "bytes_per_launch": dbytes}},
         "replay": replay,
+        "layer_ops": layer_ops,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": 2 * args.steps,

@@ -5,8 +5,8 @@ The compute lives in ``libkda.so`` (hand-written CUDA kernels behind a C ABI,
 ``include/kda.h``); ``kda`` is its thin Python binding.
 """
 from .kda import (KDAError, kda_chunk_fwd, kda_chunk_fwd_noalloc, kda_chunk_fwd_workspace_size,
-                  kda_decode_replay, kda_decode_step,
+                  kda_decode_replay, kda_decode_step, kda_post_fwd, kda_prep_fwd,
                   kda_read_device_status, kda_version, library, library_path)
 
-__all__ = ["KDAError", "kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_chunk_fwd_workspace_size", "kda_decode_replay", "kda_decode_step",
+__all__ = ["KDAError", "kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_chunk_fwd_workspace_size", "kda_decode_replay", "kda_decode_step", "kda_post_fwd", "kda_prep_fwd",
            "kda_read_device_status", "kda_version", "library", "library_path"]

@@ -207,4 +207,59 @@ int kda_decode_replay(float *state, const void *q, const void *k, const void *v,
   return KDA_OK;
 }
 
+int kda_prep_fwd(const void *q_raw, const void *k_raw, const void *v_raw, const float *conv_w,
+                 const float *a_logit, const float *b_logit, const int32_t *cu_seqlens,
+                 int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk, int32_t dv, int dtype,
+                 void *q, void *k, void *v, float *log_alpha, float *beta, void *stream) {
+  if (n_seqs < 1 || n_tokens < 0 || n_tokens > 0x7fffffffLL || H <= 0) return KDA_ERR_INVALID_ARG;
+  const int d = check_dims(dk, dv, dtype);
+  if (d != KDA_OK) return d;
+  if (!q_raw || !k_raw || !v_raw || !conv_w || !a_logit || !b_logit || !cu_seqlens || !q || !k ||
+      !v || !log_alpha || !beta)
+    return KDA_ERR_INVALID_ARG;
+  const size_t esz = dtype == KDA_BF16 ? 2 : 4;
+  const void *vec[] = {q_raw, k_raw, v_raw, q, k, v};
+  for (const void *p : vec)
+    if (!aligned(p, 4 * esz)) return KDA_ERR_INVALID_ARG;
+  if (!aligned16(conv_w) || !aligned16(a_logit) || !aligned16(log_alpha) || !aligned(b_logit, 4) ||
+      !aligned(beta, 4) || !aligned(cu_seqlens, 4))
+    return KDA_ERR_INVALID_ARG;
+  // The convolution reads neighbouring tokens: no output may overlap an input.
+  const size_t n = (size_t)n_tokens * H * dk;
+  const void *outs[] = {q, k, v};
+  const void *ins[] = {q_raw, k_raw, v_raw};
+  for (const void *o : outs)
+    for (const void *i : ins)
+      if (n > 0 && ranges_overlap(o, n * esz, i, n * esz)) return KDA_ERR_INVALID_ARG;
+  if (n > 0 && (ranges_overlap(log_alpha, n * 4, a_logit, n * 4) ||
+                ranges_overlap(beta, (size_t)n_tokens * H * 4, b_logit, (size_t)n_tokens * H * 4)))
+    return KDA_ERR_INVALID_ARG;
+  const cudaError_t e = kda::launch_prep(q_raw, k_raw, v_raw, conv_w, a_logit, b_logit,
+                                         cu_seqlens, n_seqs, n_tokens, H, dtype == KDA_BF16, q, k,
+                                         v, log_alpha, beta, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_CUDA;
+  }
+  return KDA_OK;
+}
+
+int kda_post_fwd(const void *o, const void *g, const float *gamma, int64_t n_tokens, int32_t H,
+                 int32_t dv, int dtype, void *out, void *stream) {
+  if (n_tokens < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+  const int d = check_dims(dv, dv, dtype);
+  if (d != KDA_OK) return d;
+  if (!o || !g || !gamma || !out) return KDA_ERR_INVALID_ARG;
+  const size_t esz = dtype == KDA_BF16 ? 2 : 4;
+  if (!aligned(o, 4 * esz) || !aligned(g, 4 * esz) || !aligned(out, 4 * esz) || !aligned16(gamma))
+    return KDA_ERR_INVALID_ARG;
+  const cudaError_t e = kda::launch_post(o, g, gamma, n_tokens, H, dtype == KDA_BF16, out,
+                                         static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_CUDA;
+  }
+  return KDA_OK;
+}
+
 }  // extern "C"

@@ -43,6 +43,15 @@ cudaError_t launch_decode_replay(float *state, const void *q, const void *k, con
                                  const int32_t *n_accept, int32_t B, int32_t T, int32_t H,
                                  bool bf16, void *out, cudaStream_t stream);
 
+cudaError_t launch_prep(const void *q_raw, const void *k_raw, const void *v_raw,
+                        const float *conv_w, const float *a_logit, const float *b_logit,
+                        const int32_t *cu_seqlens, int32_t n_seqs, int64_t n_tokens, int32_t H,
+                        bool bf16, void *q, void *k, void *v, float *log_alpha, float *beta,
+                        cudaStream_t stream);
+
+cudaError_t launch_post(const void *o, const void *g, const float *gamma, int64_t n_tokens,
+                        int32_t H, bool bf16, void *out, cudaStream_t stream);
+
 cudaError_t launch_chunk_fwd_f32(const ChunkArgs &a, cudaStream_t stream);
 
 // Returns cudaErrorNotSupported if the tensor-map entry point is unavailable.

@@ -1,0 +1,316 @@
+// The per-token operations either side of the KDA recurrence, each one HBM pass.
+//
+// Before the recurrence ("Kimi K3: 架构、训练与系统全景解析", section 4.2.3; "Kimi K3"
+// study notes, section 3-2 "2) Kimi Delta Attention"): a short causal
+// convolution (kernel size 4) of q, k and v within each sequence, Swish, and an
+// L2 normalisation of q and k; beta = sigmoid(b) and the lower-bounded decay
+// log_alpha = -5 sigmoid(a) (全景解析 sections 2.1 and 4.2.5).  After it
+// (全景解析 section 4.2.6): head-wise RMSNorm of the recurrent output times a
+// sigmoid output gate whose logits come from the full-rank projection.
+//   conv:    y[t] = sum_j w[j] x[t - 3 + j], zero before the sequence start
+//   swish:   x sigmoid(x)
+//   l2norm:  x / sqrt(sum_c x^2 + 1e-6)
+//   rmsnorm: o / sqrt(mean_c o^2 + 1e-5) * gamma[c]
+//
+// Lane l of a warp owns channels 4l .. 4l + 3 of one (token, head) row, so both
+// per-token reductions over the 128 channels are warp shuffles.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <type_traits>
+
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int D = kHeadDim;
+constexpr int kWarps = 8;
+constexpr int kTokensPerCta = 64;
+constexpr int kConv = 4;
+constexpr float kL2Eps = 1e-6f;
+constexpr float kRmsEps = 1e-5f;
+constexpr float kDecayBound = -5.0f;
+
+template <bool BF16>
+__device__ __forceinline__ float4 ld4(const void *p, int64_t i) {
+  if constexpr (BF16) {
+    const uint2 raw = *reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(p) + i);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  } else {
+    return *reinterpret_cast<const float4 *>(static_cast<const float *>(p) + i);
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void st4(void *p, int64_t i, float4 x) {
+  if constexpr (BF16) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
+    uint2 raw;
+    raw.x = *reinterpret_cast<const uint32_t *>(&lo);
+    raw.y = *reinterpret_cast<const uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p) + i) = raw;
+  } else {
+    *reinterpret_cast<float4 *>(static_cast<float *>(p) + i) = x;
+  }
+}
+
+// sigmoid through the fast exponential and the approximate divide (relative
+// error ~1e-6, far below the bf16 rounding of q, k, v and within the fp32 gate
+// tolerance); 1 + e^-x = inf for very negative x gives exactly 0.
+__device__ __forceinline__ float sigmoidf(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
+// The taps of channels c0 .. c0 + 3 of head h from one [H, d, 4] weight tensor.
+__device__ __forceinline__ void load_taps(float4 (&w)[4], const float *wt, int h, int c0) {
+  const float4 *wv = reinterpret_cast<const float4 *>(wt + ((int64_t)h * D + c0) * kConv);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) w[i] = wv[i];
+}
+
+__device__ __forceinline__ float4 scale4(float4 x, float s) {
+  return make_float4(x.x * s, x.y * s, x.z * s, x.w * s);
+}
+
+// Four channels of one row as loaded: packed bf16 pairs or fp32.
+template <bool BF16> struct Raw4;
+template <> struct Raw4<true> { using type = uint2; };
+template <> struct Raw4<false> { using type = float4; };
+template <bool BF16> using raw4_t = typename Raw4<BF16>::type;
+
+template <bool BF16>
+__device__ __forceinline__ raw4_t<BF16> ld_raw(const void *p, int64_t i) {
+  if constexpr (BF16)
+    return *reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(p) + i);
+  else
+    return *reinterpret_cast<const float4 *>(static_cast<const float *>(p) + i);
+}
+
+template <bool BF16> __device__ __forceinline__ raw4_t<BF16> raw_zero() {
+  if constexpr (BF16) return make_uint2(0u, 0u);
+  else return make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+template <bool BF16> __device__ __forceinline__ float4 to_f4(raw4_t<BF16> r) {
+  if constexpr (BF16) {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  } else {
+    return r;
+  }
+}
+
+// Index of the sequence holding token t: the last s < n_seqs with cu[s] <= t.
+__device__ __forceinline__ int sequence_of(const int32_t *cu, int32_t n_seqs, int64_t t) {
+  int lo = 0, hi = n_seqs;  // invariant: answer in [lo, hi)
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if ((int64_t)cu[mid] <= t) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Convolution of rows x0 .. x3 (tokens t-3 .. t) with taps w (w[i]: the four
+// taps of channel c0 + i, oldest first), then Swish.
+__device__ __forceinline__ float4 conv_swish(float4 x0, float4 x1, float4 x2, float4 x3,
+                                             const float4 (&w)[4]) {
+  float4 y;
+  y.x = w[0].x * x0.x + w[0].y * x1.x + w[0].z * x2.x + w[0].w * x3.x;
+  y.y = w[1].x * x0.y + w[1].y * x1.y + w[1].z * x2.y + w[1].w * x3.y;
+  y.z = w[2].x * x0.z + w[2].y * x1.z + w[2].z * x2.z + w[2].w * x3.z;
+  y.w = w[3].x * x0.w + w[3].y * x1.w + w[3].z * x2.w + w[3].w * x3.w;
+  y.x *= sigmoidf(y.x);
+  y.y *= sigmoidf(y.y);
+  y.z *= sigmoidf(y.z);
+  y.w *= sigmoidf(y.w);
+  return y;
+}
+
+// Work split: blockIdx.z picks the output (0 q, 1 k, 2 v, 3 the gates), the
+// CTA's kWarps warps take kWarps consecutive heads (one 2 KB bf16 span per
+// token), and each warp walks kRunTokens consecutive tokens.  For q, k, v the
+// warp slides a window of the three previous raw rows through registers and
+// loads the next kGroup rows while it works on the current ones, so each input
+// row is read once, plus a three-row halo per run.
+constexpr int kRunTokens = 32;
+
+template <bool BF16>
+__global__ void __launch_bounds__(32 * kWarps, 4)
+kda_prep_kernel(const void *__restrict__ q_raw, const void *__restrict__ k_raw,
+                const void *__restrict__ v_raw, const float *__restrict__ conv_w,
+                const float *__restrict__ a_logit, const float *__restrict__ b_logit,
+                const int32_t *__restrict__ cu_seqlens, int32_t n_seqs, int64_t n_tokens,
+                int32_t H, void *__restrict__ q, void *__restrict__ k, void *__restrict__ v,
+                float *__restrict__ log_alpha, float *__restrict__ beta) {
+  constexpr int kGroup = BF16 ? 4 : 2;  // rows in flight per warp
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * kWarps + warp;
+  if (h >= H) return;
+  const int c0 = 4 * lane;
+  const int64_t t0 = (int64_t)blockIdx.x * kRunTokens;
+  const int64_t t_end = t0 + kRunTokens < n_tokens ? t0 + kRunTokens : n_tokens;
+  auto row_of = [&](int64_t t) { return (t * H + h) * D + c0; };
+
+  if (blockIdx.z == 3) {  // gates: log_alpha = -5 sigmoid(a), beta = sigmoid(b)
+    const int64_t tb = t0 + lane;
+    if (tb < t_end) beta[tb * H + h] = sigmoidf(b_logit[tb * H + h]);
+    const int64_t rs = (int64_t)H * D;
+    const float *ain = a_logit + row_of(t0);
+    float *aout = log_alpha + row_of(t0);
+    const int n_run = (int)(t_end - t0);
+    for (int ig = 0; ig < n_run; ig += 4) {
+      float4 g[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (ig + i < n_run) g[i] = *reinterpret_cast<const float4 *>(ain + i * rs);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (ig + i < n_run)
+          *reinterpret_cast<float4 *>(aout + i * rs) =
+              make_float4(kDecayBound * sigmoidf(g[i].x), kDecayBound * sigmoidf(g[i].y),
+                          kDecayBound * sigmoidf(g[i].z), kDecayBound * sigmoidf(g[i].w));
+      ain += 4 * rs;
+      aout += 4 * rs;
+    }
+    return;
+  }
+
+  const int z = blockIdx.z;
+  const void *x = z == 0 ? q_raw : (z == 1 ? k_raw : v_raw);
+  void *y = z == 0 ? q : (z == 1 ? k : v);
+  const bool normalise = z < 2;
+  float4 w[4];
+  load_taps(w, conv_w + (int64_t)z * H * D * kConv, h, c0);
+
+  // sequence bookkeeping (token indices fit int32, like cu_seqlens): ts = first
+  // token of the current sequence, nxt = the start of the next one
+  int s = sequence_of(cu_seqlens, n_seqs, t0);
+  int32_t ts = cu_seqlens[s];
+  int32_t nxt = s + 1 < n_seqs ? cu_seqlens[s + 1] : INT32_MAX;
+
+  // element pointers to this lane's channels of token t0, advanced token by token
+  using elem_t = typename std::conditional<BF16, __nv_bfloat16, float>::type;
+  const int64_t rs = (int64_t)H * D;  // elements between consecutive tokens
+  const elem_t *xin = static_cast<const elem_t *>(x) + row_of(t0);
+  elem_t *yout = static_cast<elem_t *>(y) + row_of(t0);
+  raw4_t<BF16> w0, w1, w2;  // raw rows t-3, t-2, t-1 (zero before token 0)
+  w0 = t0 >= 3 ? ld_raw<BF16>(xin - 3 * rs, 0) : raw_zero<BF16>();
+  w1 = t0 >= 2 ? ld_raw<BF16>(xin - 2 * rs, 0) : raw_zero<BF16>();
+  w2 = t0 >= 1 ? ld_raw<BF16>(xin - rs, 0) : raw_zero<BF16>();
+  raw4_t<BF16> cur[kGroup], ahead[kGroup];
+  const int n_run = (int)(t_end - t0);
+#pragma unroll
+  for (int i = 0; i < kGroup; ++i) {
+    cur[i] = i < n_run ? ld_raw<BF16>(xin, 0) : raw_zero<BF16>();
+    xin += rs;
+  }
+  for (int ig = 0; ig < n_run; ig += kGroup) {
+#pragma unroll
+    for (int i = 0; i < kGroup; ++i) {  // xin points at token t0 + ig + kGroup + i
+      ahead[i] = ig + kGroup + i < n_run ? ld_raw<BF16>(xin, 0) : raw_zero<BF16>();
+      xin += rs;
+    }
+#pragma unroll
+    for (int i = 0; i < kGroup; ++i) {
+      if (ig + i >= n_run) break;
+      const int32_t t = (int32_t)t0 + ig + i;
+      while (t >= nxt) {  // crossed into a later sequence (warp-uniform)
+        ++s;
+        ts = nxt;
+        nxt = s + 1 < n_seqs ? cu_seqlens[s + 1] : INT32_MAX;
+      }
+      const int32_t start = ts < t ? ts : t;
+      const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 x0 = t - 3 >= start ? to_f4<BF16>(w0) : zero;
+      const float4 x1 = t - 2 >= start ? to_f4<BF16>(w1) : zero;
+      const float4 x2 = t - 1 >= start ? to_f4<BF16>(w2) : zero;
+      float4 o = conv_swish(x0, x1, x2, to_f4<BF16>(cur[i]), w);
+      if (normalise)
+        o = scale4(o, rsqrtf(warp_sum(o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w) + kL2Eps));
+      st4<BF16>(yout, 0, o);
+      yout += rs;
+      w0 = w1;
+      w1 = w2;
+      w2 = cur[i];
+    }
+#pragma unroll
+    for (int i = 0; i < kGroup; ++i) cur[i] = ahead[i];
+  }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(32 * kWarps)
+kda_post_kernel(const void *__restrict__ o, const void *__restrict__ g,
+                const float *__restrict__ gamma, int64_t n_tokens, int32_t H,
+                void *__restrict__ out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y, c0 = 4 * lane;
+  const float4 gm = *reinterpret_cast<const float4 *>(gamma + c0);
+  // two tokens per step, so each warp has four rows in flight
+  for (int i = warp; i < kTokensPerCta; i += 2 * kWarps) {
+    const int64_t ta = (int64_t)blockIdx.x * kTokensPerCta + i, tb = ta + kWarps;
+    if (ta >= n_tokens) break;
+    const bool has_b = tb < n_tokens;
+    const int64_t ra = (ta * H + h) * D + c0, rb = (tb * H + h) * D + c0;
+    const float4 oa = ld4<BF16>(o, ra), ga = ld4<BF16>(g, ra);
+    float4 ob = oa, gb = ga;
+    if (has_b) { ob = ld4<BF16>(o, rb); gb = ld4<BF16>(g, rb); }
+    const float sa = warp_sum(oa.x * oa.x + oa.y * oa.y + oa.z * oa.z + oa.w * oa.w);
+    const float sb = warp_sum(ob.x * ob.x + ob.y * ob.y + ob.z * ob.z + ob.w * ob.w);
+    const float na = rsqrtf(sa * (1.0f / D) + kRmsEps), nb = rsqrtf(sb * (1.0f / D) + kRmsEps);
+    st4<BF16>(out, ra,
+              make_float4(oa.x * na * gm.x * sigmoidf(ga.x), oa.y * na * gm.y * sigmoidf(ga.y),
+                          oa.z * na * gm.z * sigmoidf(ga.z), oa.w * na * gm.w * sigmoidf(ga.w)));
+    if (has_b)
+      st4<BF16>(out, rb,
+                make_float4(ob.x * nb * gm.x * sigmoidf(gb.x), ob.y * nb * gm.y * sigmoidf(gb.y),
+                            ob.z * nb * gm.z * sigmoidf(gb.z), ob.w * nb * gm.w * sigmoidf(gb.w)));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const void *q_raw, const void *k_raw, const void *v_raw,
+                        const float *conv_w, const float *a_logit, const float *b_logit,
+                        const int32_t *cu_seqlens, int32_t n_seqs, int64_t n_tokens, int32_t H,
+                        bool bf16, void *q, void *k, void *v, float *log_alpha, float *beta,
+                        cudaStream_t stream) {
+  if (n_tokens == 0 || H == 0) return cudaSuccess;
+  const int64_t blocks = (n_tokens + kRunTokens - 1) / kRunTokens;
+  if (blocks > 0x7fffffffLL || H > 65535) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)blocks, (unsigned)((H + kWarps - 1) / kWarps), 4), block(32 * kWarps);
+  if (bf16)
+    kda_prep_kernel<true><<<grid, block, 0, stream>>>(q_raw, k_raw, v_raw, conv_w, a_logit,
+                                                      b_logit, cu_seqlens, n_seqs, n_tokens, H,
+                                                      q, k, v, log_alpha, beta);
+  else
+    kda_prep_kernel<false><<<grid, block, 0, stream>>>(q_raw, k_raw, v_raw, conv_w, a_logit,
+                                                       b_logit, cu_seqlens, n_seqs, n_tokens, H,
+                                                       q, k, v, log_alpha, beta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_post(const void *o, const void *g, const float *gamma, int64_t n_tokens,
+                        int32_t H, bool bf16, void *out, cudaStream_t stream) {
+  if (n_tokens == 0 || H == 0) return cudaSuccess;
+  const int64_t blocks = (n_tokens + kTokensPerCta - 1) / kTokensPerCta;
+  if (blocks > 0x7fffffffLL || H > 65535) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)blocks, (unsigned)H), block(32 * kWarps);
+  if (bf16)
+    kda_post_kernel<true><<<grid, block, 0, stream>>>(o, g, gamma, n_tokens, H, out);
+  else
+    kda_post_kernel<false><<<grid, block, 0, stream>>>(o, g, gamma, n_tokens, H, out);
+  return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -21,6 +21,8 @@ million-token workload and keeps small and large cases on the same recipe.
 """
 from __future__ import annotations
 
+import itertools
+
 from dataclasses import dataclass, field
 
 import torch
@@ -145,3 +147,25 @@ def decode_inputs(B: int, H: int, steps: int, dtype: str = "bf16", device="cpu",
     state = STATE_STD * torch.randn(B, H, dk, dv, generator=gen, device=device)
     return dict(state=state, q=torch.stack(qs), k=torch.stack(ks), v=torch.stack(vs),
                 log_alpha=torch.stack(las), beta=torch.stack(bts))
+
+
+def layer_inputs(lengths, H: int, dtype: str = "bf16", device="cpu", seed: int = 0,
+                 d: int = DK) -> dict:
+    """Inputs of the per-token steps around the recurrence for packed sequences of
+    the given lengths: projected q, k, v ``[N, H, d]`` ~ N(0, 1) in ``dtype``,
+    depthwise convolution weights ``[3, H, d, 4]`` ~ N(0, 0.5^2), decay and beta
+    logits ~ N(0, 1), output-gate logits ``[N, H, d]`` ~ N(0, 1) in ``dtype`` and
+    an RMSNorm weight ``[d]`` ~ 1 + N(0, 0.1^2)."""
+    gen = torch.Generator(device=device).manual_seed(seed)
+    dt = torch_dtype(dtype)
+    N = int(sum(lengths))
+
+    def randn(*shape, std=1.0):
+        return std * torch.randn(*shape, generator=gen, device=device)
+
+    cu = torch.tensor([0] + list(itertools.accumulate(lengths)), dtype=torch.int32,
+                      device=device)
+    return dict(q_raw=randn(N, H, d).to(dt), k_raw=randn(N, H, d).to(dt),
+                v_raw=randn(N, H, d).to(dt), conv_w=randn(3, H, d, 4, std=0.5),
+                a_logit=randn(N, H, d), b_logit=randn(N, H), g=randn(N, H, d).to(dt),
+                gamma=1.0 + randn(d, std=0.1), cu_seqlens=cu, lengths=list(lengths))

@@ -29,7 +29,7 @@ HEAD_DIM = 128
 # Symbols declared in include/kda.h.
 EXPORTED = ("kda_status_string", "kda_version", "kda_chunk_fwd_workspace_size",
             "kda_chunk_fwd", "kda_read_device_status", "kda_decode_step",
-            "kda_chunk_fwd_noalloc", "kda_decode_replay")
+            "kda_chunk_fwd_noalloc", "kda_decode_replay", "kda_prep_fwd", "kda_post_fwd")
 
 _lib = None
 
@@ -71,6 +71,11 @@ def library() -> ctypes.CDLL:
         lib.kda_decode_replay.restype = ctypes.c_int
         lib.kda_decode_replay.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                           ctypes.c_int, vp, vp]
+        lib.kda_prep_fwd.restype = ctypes.c_int
+        lib.kda_prep_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32,
+                                     ctypes.c_int, vp, vp, vp, vp, vp, vp]
+        lib.kda_post_fwd.restype = ctypes.c_int
+        lib.kda_post_fwd.argtypes = [vp, vp, vp, i64, i32, i32, ctypes.c_int, vp, vp]
         lib.kda_decode_step.restype = ctypes.c_int
         lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                         ctypes.c_int, vp, vp]
@@ -265,4 +270,47 @@ def kda_decode_replay(state, q, k, v, log_alpha, beta, n_accept, *, out=None,
                                      _ptr(beta), _ptr(n_accept), B, T, H, dk, dv,
                                      _dtype_code(q), _ptr(out), _stream_handle(stream))
     _check(rc, "kda_decode_replay")
+    return out
+
+
+def kda_prep_fwd(q_raw, k_raw, v_raw, conv_w, a_logit, b_logit, cu_seqlens, *, stream=None):
+    """Short convolution + Swish (+ L2Norm for q, k) and the beta / decay gates
+    before the recurrence.  q_raw, k_raw, v_raw ``[N, H, 128]`` (bf16 or fp32);
+    conv_w ``[3, H, 128, 4]`` fp32; a_logit ``[N, H, 128]`` and b_logit ``[N, H]``
+    fp32; cu_seqlens int32 CUDA tensor ``[n_seqs + 1]``.
+    Returns ``(q, k, v, log_alpha, beta)`` ready for ``kda_chunk_fwd``."""
+    _need_cuda("q_raw", q_raw)
+    N, H, dk = q_raw.shape
+    dt = q_raw.dtype
+    _need_cuda("k_raw", k_raw, dt, (N, H, dk))
+    _need_cuda("v_raw", v_raw, dt, (N, H, dk))
+    _need_cuda("conv_w", conv_w, torch.float32, (3, H, dk, 4))
+    _need_cuda("a_logit", a_logit, torch.float32, (N, H, dk))
+    _need_cuda("b_logit", b_logit, torch.float32, (N, H))
+    _need_cuda("cu_seqlens", cu_seqlens, torch.int32)
+    n_seqs = cu_seqlens.shape[0] - 1
+    q, k, v = (torch.empty_like(q_raw) for _ in range(3))
+    log_alpha = torch.empty_like(a_logit)
+    beta = torch.empty_like(b_logit)
+    rc = library().kda_prep_fwd(_ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(conv_w),
+                                _ptr(a_logit), _ptr(b_logit), _ptr(cu_seqlens), n_seqs, N, H,
+                                dk, dk, _dtype_code(q_raw), _ptr(q), _ptr(k), _ptr(v),
+                                _ptr(log_alpha), _ptr(beta), _stream_handle(stream))
+    _check(rc, "kda_prep_fwd")
+    return q, k, v, log_alpha, beta
+
+
+def kda_post_fwd(o, g, gamma, *, out=None, stream=None):
+    """Head-wise RMSNorm of the recurrent output times the sigmoid output gate.
+    o, g ``[N, H, 128]`` (same dtype); gamma ``[128]`` fp32.  Returns out (may be o)."""
+    _need_cuda("o", o)
+    N, H, dv = o.shape
+    _need_cuda("g", g, o.dtype, (N, H, dv))
+    _need_cuda("gamma", gamma, torch.float32, (dv,))
+    if out is None:
+        out = torch.empty_like(o)
+    _need_cuda("out", out, o.dtype, (N, H, dv))
+    rc = library().kda_post_fwd(_ptr(o), _ptr(g), _ptr(gamma), N, H, dv, _dtype_code(o), _ptr(out),
+                                _stream_handle(stream))
+    _check(rc, "kda_post_fwd")
     return out

@@ -216,6 +216,51 @@ int kda_decode_replay(float *state, const void *q, const void *k, const void *v,
                       int32_t B, int32_t T, int32_t H, int32_t dk, int32_t dv, int dtype,
                       void *out, void *stream);
 
+/*
+ * The per-token steps before the recurrence, in one pass ("Kimi K3: 架构、训练与
+ * 系统全景解析", section 4.2.3: short convolution of kernel size 4, Swish,
+ * L2Norm(q, k), the write strength beta and the decay alpha; sections 2.1 and
+ * 4.2.5: the decay is a lower-bounded scaled sigmoid with bound -5).  The pages
+ * print no formulas for these steps; this library computes, per packed
+ * sequence, token t, head h and channel c:
+ *   conv(x)[t]  = sum_{j<4} conv_w[., h, c, j] x[t - 3 + j]   (0 before the
+ *                 sequence start; no state carried across calls)
+ *   q = l2norm(swish(conv(q_raw))),  k = l2norm(swish(conv(k_raw))),
+ *   v = swish(conv(v_raw)),  swish(x) = x sigmoid(x),
+ *   l2norm(x) = x / sqrt(sum_c x^2 + 1e-6)  (over the 128 channels of a head),
+ *   log_alpha = -5 sigmoid(a_logit),  beta = sigmoid(b_logit).
+ *
+ *   q_raw, k_raw, v_raw, q, k, v  [N, H, 128] dtype
+ *   conv_w      [3, H, 128, 4] fp32   (q, k, v weights; taps oldest first)
+ *   a_logit, log_alpha            [N, H, 128] fp32
+ *   b_logit, beta                 [N, H] fp32
+ *   cu_seqlens  [n_seqs + 1] int32, DEVICE memory, prefix sums from 0 to N
+ * Alignment: the dtype tensors 4 elements; conv_w, a_logit, log_alpha 16
+ * bytes; b_logit, beta, cu_seqlens 4 bytes.  No output may overlap an input.
+ * Errors: KDA_ERR_INVALID_ARG (NULL pointer, n_seqs < 1, n_tokens < 0 or above
+ * INT32_MAX (cu_seqlens is int32), H <= 0, misalignment, overlap),
+ * KDA_ERR_UNSUPPORTED (dk or dv != 128, unknown dtype), KDA_ERR_CUDA.  A
+ * malformed device cu_seqlens gives wrong values, never an out-of-range access.
+ */
+int kda_prep_fwd(const void *q_raw, const void *k_raw, const void *v_raw, const float *conv_w,
+                 const float *a_logit, const float *b_logit, const int32_t *cu_seqlens,
+                 int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk, int32_t dv, int dtype,
+                 void *q, void *k, void *v, float *log_alpha, float *beta, void *stream);
+
+/*
+ * The step after the recurrence ("Kimi K3: 架构、训练与系统全景解析", section
+ * 4.2.6): head-wise RMSNorm of the recurrent output, then the sigmoid output
+ * gate whose logits g come from the input-dependent full-rank projection
+ * (computed outside this library):
+ *   out = o / sqrt(mean_c o^2 + 1e-5) * gamma[c] * sigmoid(g)
+ *   o, g, out  [N, H, 128] dtype;  gamma [128] fp32 (shared by all heads)
+ * out may alias o (in place).  Alignment: o, g, out 4 elements; gamma 16 bytes.
+ * Errors: KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED (dv != 128, unknown dtype),
+ * KDA_ERR_CUDA.
+ */
+int kda_post_fwd(const void *o, const void *g, const float *gamma, int64_t n_tokens, int32_t H,
+                 int32_t dv, int dtype, void *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -32,7 +32,8 @@ def declared_functions():
 
 def test_header_declares_expected_entry_points():
     names = declared_functions()
-    for n in ("kda_chunk_fwd", "kda_decode_step", "kda_decode_replay", "kda_chunk_fwd_workspace_size",
+    for n in ("kda_chunk_fwd", "kda_decode_step", "kda_decode_replay", "kda_prep_fwd",
+              "kda_post_fwd", "kda_chunk_fwd_workspace_size",
               "kda_status_string", "kda_read_device_status", "kda_version"):
         assert n in names
 
@@ -142,6 +143,51 @@ def test_replay_rejects_before_launch(lib, over, code):
 
 def test_replay_empty_batch_launches_nothing(lib):
     assert _replay(lib, B=0) == 0
+
+
+def _prep(lib, **over):
+    n = 0x100000
+    args = dict(qr=A, kr=A + n, vr=A + 2 * n, w=A + 3 * n, a=A + 4 * n, b=A + 5 * n,
+                cu=A + 6 * n, n_seqs=1, N=64, H=2, dk=128, dv=128, dtype=1, q=A + 7 * n,
+                k=A + 8 * n, v=A + 9 * n, la=A + 10 * n, beta=A + 11 * n, stream=None)
+    args.update(over)
+    vp = ctypes.c_void_p
+    return lib.kda_prep_fwd(*(vp(args[x]) for x in ("qr", "kr", "vr", "w", "a", "b", "cu")),
+                            args["n_seqs"], args["N"], args["H"], args["dk"], args["dv"],
+                            args["dtype"],
+                            *(vp(args[x]) for x in ("q", "k", "v", "la", "beta", "stream")))
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(qr=None), 1), (dict(cu=None), 1), (dict(beta=None), 1), (dict(n_seqs=0), 1),
+    (dict(N=-1), 1), (dict(H=0), 1), (dict(dk=64), 2), (dict(dtype=3), 2),
+    (dict(qr=A + 4), 1), (dict(w=A + 0x300008), 1), (dict(b=A + 0x500002), 1),
+    (dict(q=A + 0x40), 1),                                 # q overlaps q_raw
+])
+def test_prep_rejects_before_launch(lib, over, code):
+    assert _prep(lib, **over) == code
+
+
+def _post(lib, **over):
+    args = dict(o=A, g=A + 0x100000, gamma=A + 0x200000, N=64, H=2, dv=128, dtype=1,
+                out=A + 0x300000, stream=None)
+    args.update(over)
+    vp = ctypes.c_void_p
+    return lib.kda_post_fwd(vp(args["o"]), vp(args["g"]), vp(args["gamma"]), args["N"],
+                            args["H"], args["dv"], args["dtype"], vp(args["out"]),
+                            vp(args["stream"]))
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(o=None), 1), (dict(gamma=None), 1), (dict(N=-1), 1), (dict(H=0), 1),
+    (dict(dv=64), 2), (dict(dtype=7), 2), (dict(gamma=A + 0x200004), 1), (dict(g=A + 2), 1),
+])
+def test_post_rejects_before_launch(lib, over, code):
+    assert _post(lib, **over) == code
+
+
+def test_empty_layer_ops_launch_nothing(lib):
+    assert _prep(lib, N=0) == 0 and _post(lib, N=0) == 0
 
 
 def test_read_device_status_null(lib):
