@@ -253,18 +253,20 @@ def replay_bench(dev, peaks, steps: int = 20, warmup: int = 3, T: int = 4):
             "accepted_tokens_per_s": accepted / (ms / 1000.0),
             "roofline": {"bound": "hbm", "kernel": "kda_decode_replay_kernel", "achieved": gbs,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                         "frac": gbs / peaks["hbm_gbs"],
+                         "traffic": recorded_traffic("kda_decode_replay_kernel", "kda_decode.cu",
+                                                     f"replay_b{B}_h{H}_t{T}"),
                          "bytes_per_launch": nbytes}}
 
 
-def layer_ops_bench(dev, peaks, steps: int = 20, warmup: int = 3):
-    """kda_prep_fwd and kda_post_fwd on the K3 layout (one sequence of 32768
+def layer_ops_bench(dev, peaks, steps: int = 20, warmup: int = 3, T: int = 32768):
+    """kda_prep_fwd and kda_post_fwd on the K3 layout (one sequence of T = 32768
     tokens, 96 heads, bf16).  Algorithmic bytes per token-head: prep reads
     q, k, v (bf16) and both gate logits and writes q, k, v, log_alpha and beta
     (2568 B); post reads o and the gate logits and writes the output (768 B)."""
     import torch
     from gated_delta_rule_13_gb300 import inputs, kda
-    T, H = 32768, 96
+    H = 96
     x = inputs.layer_inputs([T], H=H, dtype="bf16", device=dev, seed=29)
     o = x["v_raw"]
 
@@ -296,10 +298,12 @@ def layer_ops_bench(dev, peaks, steps: int = 20, warmup: int = 3):
                      "tokens_per_s": T / (ms / 1000.0),
                      "roofline": {"bound": "hbm", "kernel": f"kda_{name}_kernel", "achieved": gbs,
                                   "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                  "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                                  "frac": gbs / peaks["hbm_gbs"],
+                                  "traffic": recorded_traffic(f"kda_{name}_kernel",
+                                                              "kda_layer_ops.cu", f"t{T}_h{H}"),
                                   "bytes_per_launch": nbytes}}
     del x, o, y
-    res["workload"] = "one sequence of 32768 tokens x 96 heads, bf16"
+    res["workload"] = f"one sequence of {T} tokens x 96 heads, bf16"
     return res
 
 
@@ -418,8 +422,8 @@ def run_gpu(args):
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
         del host, dev_bufs
 
-    replay = replay_bench(dev, peaks)
-    layer_ops = layer_ops_bench(dev, peaks)
+    replay = replay_bench(dev, peaks, steps=args.sub_steps)
+    layer_ops = layer_ops_bench(dev, peaks, steps=args.sub_steps, T=args.layer_tokens)
     if world > 1:
         replay["ms_per_launch"], = max_over_ranks([replay["ms_per_launch"]], world, dev)
 
@@ -493,6 +497,10 @@ def main():
                          "spread over all steps)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sub-steps", type=int, default=20,
+                    help="timed launches of the replay and per-token-step sub-benchmarks")
+    ap.add_argument("--layer-tokens", type=int, default=32768,
+                    help="tokens of the per-token-step sub-benchmark (96 heads)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
