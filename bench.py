@@ -307,6 +307,57 @@ def layer_ops_bench(dev, peaks, steps: int = 20, warmup: int = 3, T: int = 32768
     return res
 
 
+def few_chains_bench(dev, peaks, steps: int = 20, warmup: int = 3, T: int = 65536, H: int = 8):
+    """Prefill of one long sequence over few heads (8 of K3's 96: the share of a
+    GPU under head-sharded tensor parallelism), with the helper CTAs that then
+    fill the idle SMs, and without them (KDA_CHUNK_HELPERS=0)."""
+    import torch
+    from gated_delta_rule_13_gb300 import inputs, kda
+    x = inputs.prefill_inputs([T], H=H, dtype="bf16", device=dev, seed=35)
+    out = torch.empty_like(x["v"])
+    fin = torch.empty(1, H, 128, 128, device=dev)
+    res = {"workload": f"one sequence of {T} tokens x {H} heads, bf16"}
+    stream = torch.cuda.current_stream()
+    old = os.environ.get("KDA_CHUNK_HELPERS")
+    try:
+        for name, env in (("without_helpers", "0"), ("with_helpers", None)):
+            if env is None:
+                os.environ.pop("KDA_CHUNK_HELPERS", None)
+            else:
+                os.environ["KDA_CHUNK_HELPERS"] = env
+            ws = torch.empty(kda.kda_chunk_fwd_workspace_size(1, T, H, dtype=kda.KDA_BF16),
+                             dtype=torch.uint8, device=dev)
+
+            def run():
+                kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], None,
+                                  x["cu_seqlens"], out=out, final_state=fin, workspace=ws)
+
+            for _ in range(warmup):
+                run()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(steps):
+                run()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b) / steps
+            pub, used = kda.kda_read_chunk_stats(ws)
+            gbs = prefill_bytes(x, H) / (ms / 1000.0) / 1e9
+            res[name] = {"tokens_per_s": T / (ms / 1000.0), "ms_per_launch": ms,
+                         "hbm_frac": gbs / peaks["hbm_gbs"],
+                         "chunks_from_helpers": used, "chunks": H * ((T + 63) // 64),
+                         "packages_published": pub}
+    finally:
+        if old is None:
+            os.environ.pop("KDA_CHUNK_HELPERS", None)
+        else:
+            os.environ["KDA_CHUNK_HELPERS"] = old
+    res["speedup"] = res["without_helpers"]["ms_per_launch"] / res["with_helpers"]["ms_per_launch"]
+    del x, out, fin
+    return res
+
+
 def prefill_bytes(x, H):
     n_tok = int(x["q"].shape[0])
     n_seqs = int(x["cu_seqlens"].shape[0] - 1)
@@ -423,6 +474,7 @@ def run_gpu(args):
         del host, dev_bufs
 
     replay = replay_bench(dev, peaks, steps=args.sub_steps)
+    few_chains = few_chains_bench(dev, peaks, steps=args.sub_steps)
     layer_ops = layer_ops_bench(dev, peaks, steps=args.sub_steps, T=args.layer_tokens)
     if world > 1:
         replay["ms_per_launch"], = max_over_ranks([replay["ms_per_launch"]], world, dev)
@@ -470,6 +522,7 @@ def run_gpu(args):
                                                             "kda_decode.cu", "decode_b512_h96"),
                                 "bytes_per_launch": dbytes}},
         "replay": replay,
+        "prefill_few_chains": few_chains,
         "layer_ops": layer_ops,
         "cpu_baseline": cpu,
         "e2e": e2e,

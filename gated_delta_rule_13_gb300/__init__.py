@@ -6,7 +6,9 @@ The compute lives in ``libkda.so`` (hand-written CUDA kernels behind a C ABI,
 """
 from .kda import (KDAError, kda_chunk_fwd, kda_chunk_fwd_noalloc, kda_chunk_fwd_workspace_size,
                   kda_decode_replay, kda_decode_step, kda_post_fwd, kda_prep_fwd,
-                  kda_read_device_status, kda_version, library, library_path)
+                  kda_read_device_status, kda_read_chunk_stats, kda_version, library,
+                  library_path)
 
 __all__ = ["KDAError", "kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_chunk_fwd_workspace_size", "kda_decode_replay", "kda_decode_step", "kda_post_fwd", "kda_prep_fwd",
-           "kda_read_device_status", "kda_version", "library", "library_path"]
+           "kda_read_device_status", "kda_read_chunk_stats", "kda_version", "library",
+           "library_path"]

@@ -98,17 +98,28 @@ constexpr uint32_t OFF_XBUF = 64 * FP * 4;           // 4 blocks of 16 x XP fp32
 constexpr uint32_t OFF_TMAT = OFF_XBUF + 4 * 16 * XP * 4;  // T' = T Diag(beta), K-major
 constexpr uint32_t SM_TMAT = SM_GB + OFF_TMAT;
 
+// A chunk a helper CTA has claimed (written by its issue thread).
+struct HelpClaim {
+  int32_t valid, chain, chunk, tb, nv, head;
+};
+
 struct Misc {
   float beta[2][C];  // beta of the chunk in flight and of the next one
   float gamma[D];    // Gamma_C = e^{g_C} per key channel
   uint64_t bar_qk, bar_la, bar_v;                     // TMA arrivals
   uint64_t bar_gp, bar_m1, bar_u, bar_m2, bar_fin;    // MMA completions
   uint64_t bar_build, bar_om, bar_t1, bar_t, bar_ny, bar_ad;  // operands ready (one arrival per warp)
+  uint64_t bar_plan;            // the issue thread has planned the next chunk
+  uint64_t bar_pka, bar_pkb;    // package copies: [Gamma, Qt; Kt, Kdec] and [T', P]
+  uint64_t bar_wb;              // helper: the package has been read out of shared memory
   uint32_t tmem_base;
   int abort;
-  uint32_t tma_issued[3], tma_waited[3];  // per TMA barrier: phases issued / consumed
+  int32_t plan[2];              // chain CTA: 1 if that chunk's package comes from a helper
+  HelpClaim claim[2];           // helper CTA: the chunk being built / the next one
+  // Per copy barrier (TMA_*): phase index + 1 of the last phase that carried a
+  // real copy (0: none), so an aborting CTA can wait for it before exiting.
+  uint32_t last_copy[5];
 };
-
 constexpr uint32_t SMEM_BYTES = SM_MISC + sizeof(Misc);
 constexpr uint32_t SM_BETA = SM_MISC + offsetof(Misc, beta);
 constexpr uint32_t SM_GAMMA = SM_MISC + offsetof(Misc, gamma);
@@ -137,7 +148,14 @@ __host__ __device__ constexpr uint32_t id_tri(int s, bool a_mn) {
   return idesc_bf16(128, 64 - 16 * s, a_mn, false);
 }
 
-enum { TMA_QK = 0, TMA_LA = 1, TMA_V = 2 };
+enum { TMA_QK = 0, TMA_LA = 1, TMA_V = 2, TMA_PKA = 3, TMA_PKB = 4 };
+
+// Package layout (byte offsets in a helper ring slot): shared-memory images.
+constexpr uint32_t PKG_STACK = 0, PKG_KDEC = 32768, PKG_TMAT = 49152, PKG_PMAT = 57344,
+                   PKG_GAMMA = 65536;
+static_assert(PKG_GAMMA + 512 == kHelpPackageBytes, "package layout");
+constexpr int kHelpMaxSeqs = 16384 / 8;  // sequence table of a helper (in its v buffer)
+constexpr uint64_t kHelpIdleNs = 200000000ull;  // a helper with nothing to claim for 0.2 s stops
 
 // Optional per-phase cycle stamps of chain 0 (profiling builds only), 64 slots
 // per chunk: thread 0 uses slots 0-15, thread 128 slots 16-23, the MMA thread
@@ -148,9 +166,17 @@ __device__ long long g_phase_clock[4096 * 64];
   do {                                                                                   \
     if (tid == (t) && chain == 0 && ci < 4096) g_phase_clock[ci * 64 + (i)] = clock64(); \
   } while (0)
+// Records a value (not a clock) in slot i of chain 0's chunk.
+#define PHASE_VALUE(t, i, v)                                                       \
+  do {                                                                             \
+    if (tid == (t) && chain == 0 && ci < 4096) g_phase_clock[ci * 64 + (i)] = (v); \
+  } while (0)
 #else
 #define PHASE_STAMP(t, i) \
   do {                    \
+  } while (0)
+#define PHASE_VALUE(t, i, v) \
+  do {                       \
   } while (0)
 #endif
 #define PHASE_MARK(i) PHASE_STAMP(0, i)
@@ -231,6 +257,11 @@ __device__ __forceinline__ void lds8(float (&v)[8], uint32_t saddr) {
 // Block column index of tile pair (a, b), a >= b, in the Gram column operand.
 __host__ __device__ constexpr int blk(int a, int b) { return a * (a + 1) / 2 + b; }
 
+// kHelp selects the instantiation with helper CTAs (and the chain CTAs' side of
+// their protocol); without it every helper branch compiles away, which keeps
+// the plain path as fast as it was before helpers existed (the runtime checks
+// alone cost about 10 % on a 96-chain prefill).
+template <bool kHelp>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -240,7 +271,8 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const float *__restrict__ init_state,
                         const int32_t *__restrict__ cu_seqlens, int32_t n_seqs, int64_t n_tokens,
                         int32_t H, __nv_bfloat16 *__restrict__ out,
-                        float *__restrict__ final_state, DeviceStatus *status) {
+                        float *__restrict__ final_state, DeviceStatus *status,
+                        const HelpRing help) {
   // Indexing the __shared__ array directly (no integer round trip) keeps every
   // access a shared-memory instruction.  The 128-byte swizzle atoms need a
   // 1024-byte aligned base, checked below.
@@ -248,21 +280,37 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   Misc &m = *reinterpret_cast<Misc *>(smem + SM_MISC);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int chain = blockIdx.x;
+  // Blocks past the chains are helpers (only when the call has a helper ring).
+  const bool helping = kHelp && help.ring != nullptr;
+  const bool helper = helping && chain >= help.n_chains;
   const int seq = chain / H, h = chain % H;
   const Ctx cx{smem, &m, status, chain};
   const uint32_t sb = smem_u32(smem);
+  // A chain CTA that stops early tells the helpers to leave its chunks alone.
+  auto chain_done = [&]() {
+    if (helping && !helper && tid == 0) {
+      st_relaxed_gpu(help.cons_pos + chain, 0x7fffffff);
+      atomicAdd(help.finished, 1);
+    }
+  };
   if (sb & 1023u) {
     if (tid == 0) record_status(status, KDA_ERR_UNSUPPORTED, 2, chain, -1);
+    chain_done();
     return;
   }
 
-  const int64_t t0 = cu_seqlens[seq], t1 = cu_seqlens[seq + 1];
-  if (t0 < 0 || t1 < t0 || t1 > n_tokens ||
-      (chain == 0 && (cu_seqlens[0] != 0 || cu_seqlens[n_seqs] != n_tokens))) {
-    if (tid == 0) record_status(status, KDA_ERR_INVALID_ARG, 1, chain, -1);
-    return;
+  int64_t t0 = 0, len = 0;
+  if (!helper) {
+    const int64_t a = cu_seqlens[seq], b = cu_seqlens[seq + 1];
+    if (a < 0 || b < a || b > n_tokens ||
+        (chain == 0 && (cu_seqlens[0] != 0 || cu_seqlens[n_seqs] != n_tokens))) {
+      if (tid == 0) record_status(status, KDA_ERR_INVALID_ARG, 1, chain, -1);
+      chain_done();
+      return;
+    }
+    t0 = a;
+    len = b - a;
   }
-  const int64_t len = t1 - t0;
   const int n_chunks = (int)((len + C - 1) / C);
 
   if (tid == 0) {
@@ -273,16 +321,18 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     mbar_init(&m.bar_t1, kComputeWarps / 2); mbar_init(&m.bar_t, kComputeWarps / 2);
     mbar_init(&m.bar_ny, kComputeWarps / 2);
     mbar_init(&m.bar_ad, kComputeWarps);
+    mbar_init(&m.bar_plan, 1); mbar_init(&m.bar_pka, 1); mbar_init(&m.bar_pkb, 1);
+    mbar_init(&m.bar_wb, 1);
     fence_mbarrier_init();
     m.abort = 0;
-    for (int i = 0; i < 3; ++i) m.tma_issued[i] = m.tma_waited[i] = 0;
+    for (int i = 0; i < 5; ++i) m.last_copy[i] = 0;
   }
   if (warp == 0) {
     tmem_alloc(&m.tmem_base, TM_COLS);
     tmem_relinquish();
   }
   float beta_pref = 0.f;   // beta of the chunk after the one being built (threads < C)
-  if (tid < C) {
+  if (tid < C && !helper) {
     st_shared_f32(sb + SM_BETA + 4u * tid, (n_chunks > 0 && tid < len) ? beta[(t0 + tid) * H + h] : 0.f);
     beta_pref = (n_chunks > 1 && tid < len - C) ? beta[(t0 + C + tid) * H + h] : 0.f;
   }
@@ -292,31 +342,175 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   if (warp >= kComputeWarps) {
     // ===================== TMA + MMA issue (one thread) =====================
     setmaxnreg_dec<kIssueRegs>();
-    if (warp == kMmaWarp && lane == 0 && n_chunks > 0) {
-      auto issue_qk = [&](int ci) {
-        const int32_t tb = (int32_t)(t0 + (int64_t)C * ci);
-        mbar_arrive_expect_tx(&m.bar_qk, 2 * 16384);
-        tma_load_3d(smem + SM_Q, &tm_q, &m.bar_qk, 0, h, tb);
-        tma_load_3d(smem + SM_Q + 8192, &tm_q, &m.bar_qk, 64, h, tb);
-        tma_load_3d(smem + SM_K, &tm_k, &m.bar_qk, 0, h, tb);
-        tma_load_3d(smem + SM_K + 8192, &tm_k, &m.bar_qk, 64, h, tb);
-        m.tma_issued[TMA_QK]++;
+    // Copies of a chunk's q, k, log_alpha and v tiles: `phase` is the chunk's
+    // index in this CTA's sequence of chunks, `hd` the head, `tb` the first token.
+    auto issue_qk = [&](int phase, int hd, int32_t tb) {
+      mbar_arrive_expect_tx(&m.bar_qk, 2 * 16384);
+      tma_load_3d(smem + SM_Q, &tm_q, &m.bar_qk, 0, hd, tb);
+      tma_load_3d(smem + SM_Q + 8192, &tm_q, &m.bar_qk, 64, hd, tb);
+      tma_load_3d(smem + SM_K, &tm_k, &m.bar_qk, 0, hd, tb);
+      tma_load_3d(smem + SM_K + 8192, &tm_k, &m.bar_qk, 64, hd, tb);
+      m.last_copy[TMA_QK] = (uint32_t)phase + 1u;
+    };
+    auto issue_la = [&](int phase, int hd, int32_t tb) {
+      mbar_arrive_expect_tx(&m.bar_la, 32768);
+      tma_load_3d(smem + SM_LA, &tm_la, &m.bar_la, 0, hd, tb);
+      m.last_copy[TMA_LA] = (uint32_t)phase + 1u;
+    };
+    auto issue_v = [&](int phase, int hd, int32_t tb) {
+      mbar_arrive_expect_tx(&m.bar_v, 16384);
+      tma_load_3d(smem + SM_V, &tm_v, &m.bar_v, 0, hd, tb);
+      m.last_copy[TMA_V] = (uint32_t)phase + 1u;
+    };
+    auto tok = [&](int ci) { return (int32_t)(t0 + (int64_t)C * ci); };
+    // The Gram / P MMAs of the chunk whose operands were just built.  Their
+    // accumulator columns also hold the previous chunk's bf16 Delta^T, so the
+    // caller has waited for the previous M2 group.
+    auto issue_gram = [&](uint32_t sa, uint32_t tmb) {
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint64_t ad = sdesc_sw128(sa + SM_GA + (ks >> 2) * 16384u + (ks & 3) * 32u, 16, 1024);
+        const uint64_t bd =
+            sdesc_sw128(sa + SM_GB + (ks >> 2) * (GB_ROWS * 128u) + (ks & 3) * 32u, 16, 1024);
+        umma_ss(tmb + TM_GP, ad, bd, ID_GP, ks > 0 ? 1u : 0u);
+      }
+      umma_commit(&m.bar_gp);
+    };
+    if (warp == kMmaWarp && lane == 0 && helper) {
+      // ---- helper: claim a chunk well ahead of its chain CTA, build it, publish it
+      const int hid = chain - help.n_chains, n_help = (int)gridDim.x - help.n_chains;
+      int rr = (int)((int64_t)hid * help.n_chains / n_help);  // spread the starting chains
+      // Claims the lowest chunk of some chain in [pos + kHelpLead, pos + kHelpSlots - 1]
+      // (pos: the chunk its chain CTA has started) into m.claim[slot], together with
+      // its ring slot: a slot is written by one helper at a time (busy word), so a
+      // late writer can never mix into a newer package.  Returns false when nothing
+      // is claimable: at once unless `wait`, else once every chain CTA has finished
+      // or nothing was claimable for kHelpIdleNs.
+      // Sequence table (start, length; length 0 for a malformed entry) in the v
+      // buffer, which a helper never uses: the claim scans read no global memory
+      // but the chain positions and claim counters.
+      int32_t *tab = reinterpret_cast<int32_t *>(smem + SM_V);
+      const int n_tab = help.n_chains / H;
+      for (int sq = 0; sq < n_tab; ++sq) {
+        const int64_t a = cu_seqlens[sq], b = cu_seqlens[sq + 1];
+        const bool ok = a >= 0 && b >= a && b <= n_tokens;
+        tab[2 * sq] = ok ? (int32_t)a : 0;
+        tab[2 * sq + 1] = ok ? (int32_t)(b - a) : 0;
+      }
+      auto claim = [&](int slot, bool wait) -> bool {
+        HelpClaim &cl = m.claim[slot];
+        cl.valid = 0;
+        const uint64_t idle0 = global_timer_ns();
+        for (;;) {
+          for (int k = 0; k < help.n_chains; ++k) {
+            const int hc = rr;
+            rr = rr + 1 == help.n_chains ? 0 : rr + 1;
+            const int sq = hc / H;
+            const int64_t a = tab[2 * sq], b = a + tab[2 * sq + 1];
+            const int64_t nch = (b - a + C - 1) / C;
+            if (nch <= 0) continue;
+            const int64_t pos = ld_relaxed_gpu(help.cons_pos + hc);
+            const int64_t lo = pos + kHelpLead;
+            const int64_t hi = pos + kHelpSlots - 1 < nch - 1 ? pos + kHelpSlots - 1 : nch - 1;
+            if (lo > hi) continue;
+            int o = ld_relaxed_gpu(help.next_claim + hc);
+            for (;;) {
+              const int64_t want = o > lo ? o : lo;
+              if (want > hi) break;
+              const int prev = atomicCAS(help.next_claim + hc, o, (int)want + 1);
+              if (prev == o) {
+                // The chunk is ours; so must its slot be (else its chain computes it).
+                int32_t *bz = help.busy + (size_t)hc * kHelpSlots + want % kHelpSlots;
+                if (atomicCAS(bz, 0, (int)want + 1) != 0) break;
+                __threadfence();  // the slot's last writer is done before we write
+                cl.chain = hc;
+                cl.chunk = (int)want;
+                cl.tb = (int32_t)(a + C * want);
+                cl.nv = (int)(b - (a + C * want) < C ? b - (a + C * want) : C);
+                cl.head = hc % H;
+                cl.valid = 1;
+                return true;
+              }
+              o = prev;
+            }
+          }
+          if (!wait || ld_relaxed_gpu(help.finished) >= help.n_chains) return false;
+          if (global_timer_ns() - idle0 > kHelpIdleNs) return false;
+          __nanosleep(1000);
+        }
       };
-      auto issue_la = [&](int ci) {
-        const int32_t tb = (int32_t)(t0 + (int64_t)C * ci);
-        mbar_arrive_expect_tx(&m.bar_la, 32768);
-        tma_load_3d(smem + SM_LA, &tm_la, &m.bar_la, 0, h, tb);
-        m.tma_issued[TMA_LA]++;
+      prefetch_tensormap(&tm_q); prefetch_tensormap(&tm_k); prefetch_tensormap(&tm_la);
+      auto load_claim = [&](int phase) {
+        const HelpClaim &c = m.claim[phase & 1];
+        issue_la(phase, c.head, c.tb);
+        issue_qk(phase, c.head, c.tb);
       };
-      auto issue_v = [&](int ci) {
-        const int32_t tb = (int32_t)(t0 + (int64_t)C * ci);
-        mbar_arrive_expect_tx(&m.bar_v, 16384);
-        tma_load_3d(smem + SM_V, &tm_v, &m.bar_v, 0, h, tb);
-        m.tma_issued[TMA_V]++;
-      };
+      int n_published = 0;
+      bool have = claim(0, true);
+      mbar_arrive(&m.bar_plan);
+      if (have) load_claim(0);
+      for (int j = 0; have; ++j) {
+        const uint32_t par = (uint32_t)(j & 1);
+        uint32_t sa = sb, tmb = tm;
+        asm volatile("" : "+r"(sa), "+r"(tmb));
+        if (!wait_bar(cx, &m.bar_build, par, 60, j)) break;
+        if (*reinterpret_cast<volatile int *>(&m.abort)) break;
+        tc_fence_after();
+        issue_gram(sa, tmb);
+        // One pass for the next claim now, so its tiles load during this chunk
+        // (the build has consumed q, k and log_alpha); if nothing is claimable
+        // yet, claim again, waiting, only after this chunk is published.
+        bool next = claim((j + 1) & 1, false);
+        if (next) {
+          mbar_arrive(&m.bar_plan);
+          load_claim(j + 1);
+        }
+        // The package: P after the A/P epilogue, T' after the solve.
+        if (!wait_bar(cx, &m.bar_om, par, 61, j)) break;
+        if (!wait_bar(cx, &m.bar_t, par, 62, j)) break;
+        const HelpClaim &cl = m.claim[par];
+        const size_t si = (size_t)cl.chain * kHelpSlots + cl.chunk % kHelpSlots;
+        // Written only while its chain CTA has not reached the chunk yet.
+        if (ld_relaxed_gpu(help.cons_pos + cl.chain) < cl.chunk - 1) {
+          unsigned char *slot = help.ring + si * kHelpSlotStride;
+          fence_proxy_async_global();  // after the slot claim, before the async writes
+          bulk_store(slot + PKG_STACK, sa + SM_STACK, 32768);
+          bulk_store(slot + PKG_KDEC, sa + SM_KDEC, 16384);
+          bulk_store(slot + PKG_TMAT, sa + SM_TMAT, 8192);
+          bulk_store(slot + PKG_PMAT, sa + SM_PMAT, 8192);
+          bulk_store(slot + PKG_GAMMA, sa + SM_GAMMA, 512);
+          bulk_commit();
+          bulk_wait_read_all();
+          mbar_arrive(&m.bar_wb);  // the compute warps may build the next chunk
+          bulk_wait_all();
+          fence_proxy_async_global();  // the package's writes before the flag that publishes it
+          st_release_gpu(help.flag + si, cl.chunk + 1);
+          ++n_published;
+        } else {
+          mbar_arrive(&m.bar_wb);
+        }
+        __threadfence();
+        st_release_gpu(help.busy + si, 0);  // the slot may take a later chunk
+        if (!next) {
+          next = claim((j + 1) & 1, true);
+          mbar_arrive(&m.bar_plan);
+          if (next) load_claim(j + 1);
+        }
+        have = next;
+      }
+      bulk_wait_all();
+      if (n_published) atomicAdd(&status->help_published, n_published);
+    } else if (warp == kMmaWarp && lane == 0 && n_chunks > 0) {
+      // A ready package of chunk ci sits in ring slot ci % kHelpSlots of this chain.
+      unsigned char *my_ring =
+          helping ? help.ring + (size_t)chain * kHelpSlots * kHelpSlotStride : nullptr;
+      const int32_t *my_flag = helping ? help.flag + (size_t)chain * kHelpSlots : nullptr;
+      auto slot_of = [&](int ci) { return my_ring + (size_t)(ci % kHelpSlots) * kHelpSlotStride; };
       prefetch_tensormap(&tm_q); prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v); prefetch_tensormap(&tm_la); prefetch_tensormap(&tm_o);
-      issue_la(0); issue_qk(0); issue_v(0);
+      issue_la(0, h, tok(0)); issue_qk(0, h, tok(0)); issue_v(0, h, tok(0));
+      bool helped_cur = false;  // chunk ci comes from a helper's package
+      int n_used = 0;           // packages used
       for (int ci = 0; ci < n_chunks; ++ci) {
         const uint32_t par = (uint32_t)(ci & 1);
         const bool has_next = ci + 1 < n_chunks;
@@ -328,24 +522,59 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         auto kd = [&](uint32_t off) { return sdesc_sw128(sa + off, 16, 1024); };
         auto mnd = [&](uint32_t off, uint32_t lbo) { return sdesc_sw128(sa + off, lbo, 1024); };
         const uint32_t to = tmb + TM_O + 64u * (uint32_t)(ci & 1);
-        // Gram / P of chunk ci.  Its accumulator columns also hold the previous
-        // chunk's bf16 Delta^T, so the previous M2 group must have finished.
         if (!wait_bar(cx, &m.bar_build, par, 30, ci)) break;
+        if (*reinterpret_cast<volatile int *>(&m.abort)) break;  // no new copies once aborting
         PHASE_MARK_MMA(0);
         if (ci > 0 && !wait_bar(cx, &m.bar_m2, par ^ 1u, 36, ci - 1)) break;
         tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t ad = kd(SM_GA + (ks >> 2) * 16384u + (ks & 3) * 32u);
-          const uint64_t bd = kd(SM_GB + (ks >> 2) * (GB_ROWS * 128u) + (ks & 3) * 32u);
-          umma_ss(tmb + TM_GP, ad, bd, ID_GP, ks > 0 ? 1u : 0u);
+        if (helped_cur) {
+          // T' and P of the package: the previous chunk's Delta and M2 MMAs have
+          // read theirs.  One phase of bar_gp per chunk either way.
+          mbar_arrive_expect_tx(&m.bar_pkb, 16384);
+          bulk_load(sa + SM_TMAT, slot_of(ci) + PKG_TMAT, 8192, &m.bar_pkb);
+          bulk_load(sa + SM_PMAT, slot_of(ci) + PKG_PMAT, 8192, &m.bar_pkb);
+          m.last_copy[TMA_PKB] = (uint32_t)ci + 1u;
+          mbar_arrive(&m.bar_gp);
+        } else {
+          issue_gram(sa, tmb);
+          mbar_arrive(&m.bar_pkb);
         }
-        umma_commit(&m.bar_gp);
         PHASE_MARK_MMA(5);
-        if (has_next) { issue_la(ci + 1); issue_qk(ci + 1); }   // both tiles consumed
+        // Plan the next chunk: a helper's package if one is ready (its q, k and
+        // log_alpha tiles are then never loaded), else its own tiles.
+        const bool helped_next = has_next && helping && ci + 1 >= kHelpLead &&
+                                 ld_acquire_gpu(my_flag + (ci + 1) % kHelpSlots) == ci + 2;
+        if (has_next) {
+          if (helped_next) {
+            fence_proxy_async_global();  // the package's writes before the copies that read it
+            mbar_arrive(&m.bar_la);
+            mbar_arrive(&m.bar_qk);
+            ++n_used;
+          } else {
+            issue_la(ci + 1, h, tok(ci + 1));
+            issue_qk(ci + 1, h, tok(ci + 1));
+          }
+          if (helping) {
+            m.plan[(ci + 1) & 1] = helped_next ? 1 : 0;
+            mbar_arrive(&m.bar_plan);
+          }
+          PHASE_STAMP(32 * kMmaWarp, 51);
+        }
         // [O^T | Y^T] = S^T [Qt; Kt]^T
         if (!wait_bar(cx, &m.bar_om, par, 31, ci)) break;
         PHASE_MARK_MMA(1);
+        if (helped_cur && !wait_bar(cx, &m.bar_pka, par ^ 1u, 38, ci)) break;
+        if (has_next) {
+          // Gamma of the next chunk (this chunk's state pass has read Gamma); the
+          // phase's byte count covers the two copies issued after the (V - Y) pass.
+          if (helped_next) {
+            mbar_arrive_expect_tx(&m.bar_pka, 512 + 32768 + 16384);
+            bulk_load(sa + SM_GAMMA, slot_of(ci + 1) + PKG_GAMMA, 512, &m.bar_pka);
+            m.last_copy[TMA_PKA] = (uint32_t)ci + 1u;
+          } else {
+            mbar_arrive(&m.bar_pka);
+          }
+        }
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
@@ -363,8 +592,16 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         // wait for the 32 -> 64 blocks.
         if (!wait_bar(cx, &m.bar_ny, par, 33, ci)) break;
         PHASE_MARK_MMA(3);
-        if (has_next) issue_v(ci + 1);   // the (V - Y) pass has read this chunk's v tile
+        if (has_next) issue_v(ci + 1, h, tok(ci + 1));   // the (V - Y) pass has read this chunk's v tile
+        if (helped_next) {
+          // [Qt; Kt] and Kdec of the next chunk: this chunk's O+Y MMAs have read
+          // the stack and the staged output stores have left the Kdec buffer.
+          bulk_load(sa + SM_STACK, slot_of(ci + 1) + PKG_STACK, 32768, &m.bar_pka);
+          bulk_load(sa + SM_KDEC + 16384u * (uint32_t)((ci + 1) & 1), slot_of(ci + 1) + PKG_KDEC,
+                    16384, &m.bar_pka);
+        }
         if (!wait_bar(cx, &m.bar_t1, par, 37, ci)) break;
+        if (helped_cur && !wait_bar(cx, &m.bar_pkb, par, 39, ci)) break;
         tc_fence_after();
         umma_ts(tmb + TM_D, tmb + TM_NY, kd(SM_TMAT), ID_N32, 0u);                       // r 0-31, s 0
         umma_ts(tmb + TM_D + 16u, tmb + TM_NY + 8u, kd(SM_TMAT + 16u * 128u + 32u), ID_N16,
@@ -393,7 +630,9 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         umma_commit(&m.bar_m2);
         PHASE_MARK_MMA(7);
+        helped_cur = helped_next;
       }
+      if (n_used) atomicAdd(&status->help_consumed, n_used);
     }
     __syncwarp();
   } else {
@@ -404,7 +643,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int64_t sbase = ((int64_t)seq * H + h) * D * D;
 
     // ---- initial state -> S^T in TMEM (thread: lane n, 64 key columns of its half)
-    {
+    if (!helper) {
       const int n = lane_base + lane;
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
@@ -462,19 +701,13 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     for (int k = 0; k < 8; ++k) swzk[k] = ((((cb >> 4) ^ (uint32_t)k) << 4) | (cb & 15u));
     const uint32_t sla = sb + SM_LA;  // log_alpha tile [64][128] fp32, then the tile totals
 
-    // Decay prefix and every operand tile of chunk ci; false if the CTA aborts.
-    auto scan_build = [&](int ci) -> bool {
-      const uint32_t par = (uint32_t)(ci & 1);
-      const int64_t tb = t0 + (int64_t)C * ci;
-      const int nv = (int)((len - (int64_t)C * ci) < C ? (len - (int64_t)C * ci) : C);
-      if (tid < C && ci > 0) {   // beta of this chunk, prefetch of the next one
-        st_shared_f32(sb + SM_BETA + 4u * ((ci & 1) * C + tid), beta_pref);
-        const int64_t rem = len - (int64_t)C * (ci + 1);
-        beta_pref = (ci + 1 < n_chunks && tid < rem) ? beta[(tb + C + tid) * H + h] : 0.f;
-      }
+    // Decay prefix and every operand tile of a chunk of nv valid rows, whose
+    // q, k and log_alpha tiles are phase `par` of their barriers (ci: the chunk's
+    // index in this CTA's sequence), with Kdec into the buffer at kdec_off;
+    // false if the CTA aborts.  The chunk's beta must already be in shared memory.
+    auto build_tiles = [&](int ci, uint32_t par, int nv, uint32_t kdec_off) -> bool {
       // tile-local prefix of the log2-decay
-      const bool ok_la = wait_bar(cx, &m.bar_la, par, 11, ci);
-      if (tid == 0 && ok_la) m.tma_waited[TMA_LA]++;
+      wait_bar(cx, &m.bar_la, par, 11, ci);
       float L0[16], L1[16];
       {
         float s0 = 0.f, s1 = 0.f;
@@ -493,8 +726,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
       if (compute_sync_abort(&m.abort)) return false;
       PHASE_MARK(9);
-      const bool ok_qk = wait_bar(cx, &m.bar_qk, par, 10, ci);
-      if (tid == 0 && ok_qk) m.tma_waited[TMA_QK]++;
+      wait_bar(cx, &m.bar_qk, par, 10, ci);
       PHASE_MARK(14);
       float st0[4], st1[4], rf0[4], rf1[4];  // tile starts / ends, channels cc, cc + 1
       {
@@ -523,7 +755,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       const uint32_t r0 = 16u * ta * 128u, h64 = hsel * 8192u, h128 = hsel * 16384u;
       const uint32_t bK = sb + SM_K + h64 + r0, bQ = sb + SM_Q + h64 + r0;
       const uint32_t bGA = sb + SM_GA + h128 + 2u * r0, bST = sb + SM_STACK + h128 + r0;
-      const uint32_t bKD = sb + SM_KDEC + 16384u * (uint32_t)(ci & 1) + h64 + r0;
+      const uint32_t bKD = sb + kdec_off + h64 + r0;
       const uint32_t bGB = sb + SM_GB + hsel * (GB_ROWS * 128u) + r0;
       uint32_t kraw[16], qraw[16];
 #pragma unroll
@@ -557,61 +789,27 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       warp_arrive(&m.bar_build, lane);
       return true;
     };
-
-    bool failed = false;
-    int64_t prev_tb = 0;
-    int prev_nv = 0;
-    if (n_chunks > 0 && !scan_build(0)) failed = true;
-    for (int ci = 0; ci < n_chunks && !failed; ++ci) {
-      const uint32_t par = (uint32_t)(ci & 1);
-      const int64_t tb = t0 + (int64_t)C * ci;
-      const int nv = (int)((len - (int64_t)C * ci) < C ? (len - (int64_t)C * ci) : C);
-      const uint32_t sbeta = sb + SM_BETA + 4u * C * (uint32_t)(ci & 1);  // this chunk's beta
-      PHASE_MARK(0);
-      if (ci > 0) {  // the previous chunk's state update and output are final
-        wait_bar(cx, &m.bar_m2, par ^ 1u, 25, ci - 1);
-        tc_fence_after();
+    // Chain CTA: beta of chunk ci into its buffer and the next chunk's prefetched.
+    auto chain_beta = [&](int ci) {
+      if (tid < C && ci > 0) {
+        const int64_t tb = t0 + (int64_t)C * ci;
+        st_shared_f32(sb + SM_BETA + 4u * ((ci & 1) * C + tid), beta_pref);
+        const int64_t rem = len - (int64_t)C * (ci + 1);
+        beta_pref = (ci + 1 < n_chunks && tid < rem) ? beta[(tb + C + tid) * H + h] : 0.f;
       }
-      // Gamma, beta and the operand tiles of this chunk visible
-      if (compute_sync_abort(&m.abort)) { failed = true; break; }
-      PHASE_MARK(1);
+    };
+    auto chunk_rows = [&](int ci) {
+      return (int)((len - (int64_t)C * ci) < C ? (len - (int64_t)C * ci) : C);
+    };
+    auto scan_build = [&](int ci) -> bool {
+      chain_beta(ci);
+      return build_tiles(ci, (uint32_t)(ci & 1), chunk_rows(ci), SM_KDEC + 16384u * (uint32_t)(ci & 1));
+    };
 
-      // ---- S^T <- S^T Diag(Gamma_C); bf16 pre-chunk S^T as the A operand
-      {
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-          const int c0 = 64 * hf + 32 * part;
-          uint32_t s[32];
-          tmem_ld32(tmem_addr(tm, lane_base, TM_S + c0), s);
-          tmem_ld_wait(s);
-          if (part == 0) PHASE_MARK_W3(5);
-          uint32_t ab[16];
-#pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            float gv[8];
-            lds8(gv, sb + SM_GAMMA + 4u * (c0 + 8 * q8));
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-              const int j = 8 * q8 + 2 * jj;
-              const float f0 = __uint_as_float(s[j]), f1 = __uint_as_float(s[j + 1]);
-              ab[4 * q8 + jj] = pack_bf16x2(f0, f1);
-              s[j] = __float_as_uint(f0 * gv[2 * jj]);
-              s[j + 1] = __float_as_uint(f1 * gv[2 * jj + 1]);
-            }
-          }
-          tmem_st32(tmem_addr(tm, lane_base, TM_S + c0), s);
-          tmem_st16(tmem_addr(tm, lane_base, TM_AS + c0 / 2), ab);
-        }
-        tmem_st_wait();
-      }
-      PHASE_MARK(2);
-
-      // ---- Gram / P -> A^T (fp32, for the solve) and P (bf16, K-major [r][i]).
-      // Quadrant q4 holds row tile a = q4: lanes 0-15 key rows, 16-31 query rows.
-      wait_bar(cx, &m.bar_gp, par, 22, ci);
-      tc_fence_after();
-      PHASE_MARK(3);
-      PHASE_MARK_W3(0);
+    // Gram / P accumulators -> A^T (fp32, for the solve) and P (bf16, K-major
+    // [r][i]), with the chunk's beta at sbeta.  Quadrant q4 holds row tile a = q4:
+    // lanes 0-15 key rows, 16-31 query rows.
+    auto ap_epilogue = [&](uint32_t sbeta, int ci) {
       {
         // Warps 0-3 take blocks b = 0, 1 of their row tile, warps 4-7 blocks 2, 3
         // (b <= a): adjacent block columns, so one TMEM load per warp.
@@ -659,10 +857,212 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           block(b0, 0);
         }
       }
+    };
+
+    // T = (I + A)^{-1} and T' = T Diag(beta) from A^T (warps 0-3), beta at sbeta;
+    // arrives on bar_t1 once the diagonal and 16 -> 32 blocks of T' exist and on
+    // bar_t when all of T' does.
+    auto solve_T = [&](uint32_t sbeta, int ci) {
+      // ---- T = (I + A)^{-1} and T' = T Diag(beta) (warps 0-3)
+      const uint32_t sat = sb + SM_GA;                // A^T, fp32 [i][r], pitch FP
+      const uint32_t stv = sb + SM_GB + OFF_TINV;     // T, fp32 [r][i], pitch FP
+      const uint32_t sxb = sb + SM_GB + OFF_XBUF;     // 4 blocks of 16 x XP fp32
+      if (warp < 2) {
+        // Diagonal 16 x 16 blocks by column-oriented forward substitution: lane
+        // owns column j of block a; after step m, t[m] is final and is eliminated
+        // from every later row.  Columns stream through a ring, three steps ahead.
+        const int a = 2 * warp + (lane >> 4), j = lane & 15, b0 = 16 * a;
+        float t[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) t[r] = (r == j) ? 1.f : 0.f;
+        float cbuf[4][16];
+#pragma unroll
+        for (int p = 0; p < 3; ++p) {
+          lds8(*reinterpret_cast<float(*)[8]>(cbuf[p]), sat + 4u * ((b0 + p) * FP + b0));
+          lds8(*reinterpret_cast<float(*)[8]>(cbuf[p] + 8), sat + 4u * ((b0 + p) * FP + b0 + 8));
+        }
+#pragma unroll
+        for (int mc = 0; mc < 15; ++mc) {
+          if (mc + 3 < 15) {
+            float *nb = cbuf[(mc + 3) & 3];
+            lds8(*reinterpret_cast<float(*)[8]>(nb), sat + 4u * ((b0 + mc + 3) * FP + b0));
+            lds8(*reinterpret_cast<float(*)[8]>(nb + 8), sat + 4u * ((b0 + mc + 3) * FP + b0 + 8));
+          }
+          const float tmv = t[mc];
+          const float *col = cbuf[mc & 3];
+#pragma unroll
+          for (int r = mc + 1; r < 16; ++r) t[r] = fmaf(-col[r], tmv, t[r]);
+        }
+        // T (fp32, for the block recursion) and T' = T Diag(beta) (bf16 MMA operand;
+        // the block's upper triangle is zero because t[r] = 0 for r < j).
+        const float bj = ld_shared_f32(sbeta + 4u * (b0 + j));
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          st_shared_f32(stv + 4u * ((b0 + r) * FP + b0 + j), t[r]);
+          const __nv_bfloat16 tb16 = __float2bfloat16_rn(t[r] * bj);
+          st_shared_b16(sb + SM_TMAT + sw128_offset(b0 + r, (b0 + j) * 2),
+                        *reinterpret_cast<const uint16_t *>(&tb16));
+        }
+      }
+      PHASE_MARK(11);
+      __syncwarp();   // the 16 -> 32 level of a warp reads only that warp's diagonal blocks
+      // Off-diagonal blocks, block-recursive: 16 -> 32 (blocks (1,0), (3,2)), then
+      // 32 -> 64 (blocks (2,0), (2,1), (3,0), (3,1)), TF32 warp MMAs.
+      const int g = lane >> 2, t4 = lane & 3;
+      // acc (+)= A_{ab} T_{mb} with A from A^T (column-major, pitch FP) ...
+      auto mul_AT = [&](float (&acc)[2][4], int ab, int mb, int tcol) {
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const int kc = 16 * mb + 8 * kk;
+          const uint32_t a0 = to_tf32(ld_shared_f32(sat + 4u * ((kc + t4) * FP + 16 * ab + g)));
+          const uint32_t a1 = to_tf32(ld_shared_f32(sat + 4u * ((kc + t4) * FP + 16 * ab + g + 8)));
+          const uint32_t a2 = to_tf32(ld_shared_f32(sat + 4u * ((kc + t4 + 4) * FP + 16 * ab + g)));
+          const uint32_t a3 = to_tf32(ld_shared_f32(sat + 4u * ((kc + t4 + 4) * FP + 16 * ab + g + 8)));
+          const uint32_t b0p = stv + 4u * ((kc + t4) * FP + tcol + g);
+          const uint32_t b1p = stv + 4u * ((kc + t4 + 4) * FP + tcol + g);
+          mma_tf32_16x8x8(acc[0], a0, a1, a2, a3, to_tf32(ld_shared_f32(b0p)),
+                          to_tf32(ld_shared_f32(b1p)));
+          mma_tf32_16x8x8(acc[1], a0, a1, a2, a3, to_tf32(ld_shared_f32(b0p + 32u)),
+                          to_tf32(ld_shared_f32(b1p + 32u)));
+        }
+      };
+      // ... and acc (+)= T_{ar} X with T row-major (pitch FP), X a 16 x 16 block (pitch XP).
+      auto mul_TX = [&](float (&acc)[2][4], int ar, int ac, uint32_t x) {
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const uint32_t tq = stv + 4u * ((16 * ar) * FP + 16 * ac + 8 * kk);
+          const uint32_t a0 = to_tf32(ld_shared_f32(tq + 4u * (g * FP + t4)));
+          const uint32_t a1 = to_tf32(ld_shared_f32(tq + 4u * ((g + 8) * FP + t4)));
+          const uint32_t a2 = to_tf32(ld_shared_f32(tq + 4u * (g * FP + t4 + 4)));
+          const uint32_t a3 = to_tf32(ld_shared_f32(tq + 4u * ((g + 8) * FP + t4 + 4)));
+          const uint32_t x0 = x + 4u * ((8 * kk + t4) * XP + g);
+          const uint32_t x1 = x + 4u * ((8 * kk + t4 + 4) * XP + g);
+          mma_tf32_16x8x8(acc[0], a0, a1, a2, a3, to_tf32(ld_shared_f32(x0)),
+                          to_tf32(ld_shared_f32(x1)));
+          mma_tf32_16x8x8(acc[1], a0, a1, a2, a3, to_tf32(ld_shared_f32(x0 + 32u)),
+                          to_tf32(ld_shared_f32(x1 + 32u)));
+        }
+      };
+      auto store_blk = [&](uint32_t dst, int pitch, const float (&acc)[2][4], float sgn) {
+#pragma unroll
+        for (int nh = 0; nh < 2; ++nh) {
+          st_shared_f32x2(dst + 4u * (g * pitch + 8 * nh + 2 * t4), sgn * acc[nh][0],
+                          sgn * acc[nh][1]);
+          st_shared_f32x2(dst + 4u * ((g + 8) * pitch + 8 * nh + 2 * t4), sgn * acc[nh][2],
+                          sgn * acc[nh][3]);
+        }
+      };
+      // Final block T_ab: fp32 into T, and T' = T Diag(beta) as bf16 pairs.
+      auto store_T = [&](int ab, int bb, const float (&acc)[2][4]) {
+        store_blk(stv + 4u * ((16 * ab) * FP + 16 * bb), FP, acc, -1.f);
+#pragma unroll
+        for (int nh = 0; nh < 2; ++nh) {
+          const int col = 16 * bb + 8 * nh + 2 * t4;
+          const float2 bv = ld_shared_f32x2(sbeta + 4u * col);
+          const float b0v = bv.x, b1v = bv.y;
+          const uint32_t lo = pack_bf16x2(-acc[nh][0] * b0v, -acc[nh][1] * b1v);
+          const uint32_t hi = pack_bf16x2(-acc[nh][2] * b0v, -acc[nh][3] * b1v);
+          st_shared_b32(sb + SM_TMAT + sw128_offset(16 * ab + g, col * 2), lo);
+          st_shared_b32(sb + SM_TMAT + sw128_offset(16 * ab + g + 8, col * 2), hi);
+        }
+      };
+      const uint32_t xw = sxb + 4u * (warp * 16 * XP);
+      if (warp < 2) {  // level 16 -> 32: block (1,0) on warp 0, (3,2) on warp 1
+        const int ab = 2 * warp + 1, bb = 2 * warp;
+        float acc[2][4] = {};
+        mul_AT(acc, ab, bb, 16 * bb);  // X = A_ab T_bb
+        store_blk(xw, XP, acc, 1.f);
+        __syncwarp();
+        float o[2][4] = {};
+        mul_TX(o, ab, ab, xw);  // T_ab = -T_aa X
+        store_T(ab, bb, o);
+      }
+      PHASE_MARK(12);
+      named_sync(2, 128);
+      fence_proxy_async_smem();   // diagonal and 16 -> 32 blocks of T' are MMA operands
+      warp_arrive(&m.bar_t1, lane);
+      {  // level 32 -> 64: warp w -> block (2 + w/2, w%2)
+        const int ab = 2 + (warp >> 1), bb = warp & 1;
+        float acc[2][4] = {};
+        // X_{ab} = A_{ab,0:2} T_{0:2, bb} = sum_{m=bb}^{1} A_{ab,m} T_{m,bb}
+        for (int mb = bb; mb < 2; ++mb) mul_AT(acc, ab, mb, 16 * bb);
+        store_blk(xw, XP, acc, 1.f);
+        PHASE_MARK(13);
+        named_sync(2, 128);
+        // T_{ab} = -sum_{k=2}^{ab} T_{ab,k} X_{k,bb}
+        float o[2][4] = {};
+        for (int k = 2; k <= ab; ++k) mul_TX(o, ab, k, sxb + 4u * ((2 * (k - 2) + bb) * 16 * XP));
+        store_T(ab, bb, o);
+      }
+      PHASE_MARK_W3(2);
+      fence_proxy_async_smem();  // T' is an MMA operand
+      warp_arrive(&m.bar_t, lane);
+      PHASE_MARK(5);
+    };
+
+    bool failed = false;
+    int64_t prev_tb = 0;
+    int prev_nv = 0;
+    bool helped = false;  // this chunk's package comes from a helper
+    if (!helper && n_chunks > 0 && !scan_build(0)) failed = true;
+    for (int ci = 0; ci < n_chunks && !failed; ++ci) {
+      const uint32_t par = (uint32_t)(ci & 1);
+      const int64_t tb = t0 + (int64_t)C * ci;
+      const int nv = (int)((len - (int64_t)C * ci) < C ? (len - (int64_t)C * ci) : C);
+      const uint32_t sbeta = sb + SM_BETA + 4u * C * (uint32_t)(ci & 1);  // this chunk's beta
+      if (helping && tid == 0) st_relaxed_gpu(help.cons_pos + chain, ci);
+      PHASE_MARK(0);
+      PHASE_VALUE(0, 50, helped ? 1 : 0);
+      if (ci > 0) {  // the previous chunk's state update and output are final
+        wait_bar(cx, &m.bar_m2, par ^ 1u, 25, ci - 1);
+        tc_fence_after();
+      }
+      // Gamma, beta and the operand tiles of this chunk visible
+      if (compute_sync_abort(&m.abort)) { failed = true; break; }
+      PHASE_MARK(1);
+      if (helped) wait_bar(cx, &m.bar_pka, par ^ 1u, 43, ci);  // Gamma, [Qt; Kt], Kdec of the package
+
+      // ---- S^T <- S^T Diag(Gamma_C); bf16 pre-chunk S^T as the A operand
+      {
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          const int c0 = 64 * hf + 32 * part;
+          uint32_t s[32];
+          tmem_ld32(tmem_addr(tm, lane_base, TM_S + c0), s);
+          tmem_ld_wait(s);
+          if (part == 0) PHASE_MARK_W3(5);
+          uint32_t ab[16];
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {
+            float gv[8];
+            lds8(gv, sb + SM_GAMMA + 4u * (c0 + 8 * q8));
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const int j = 8 * q8 + 2 * jj;
+              const float f0 = __uint_as_float(s[j]), f1 = __uint_as_float(s[j + 1]);
+              ab[4 * q8 + jj] = pack_bf16x2(f0, f1);
+              s[j] = __float_as_uint(f0 * gv[2 * jj]);
+              s[j + 1] = __float_as_uint(f1 * gv[2 * jj + 1]);
+            }
+          }
+          tmem_st32(tmem_addr(tm, lane_base, TM_S + c0), s);
+          tmem_st16(tmem_addr(tm, lane_base, TM_AS + c0 / 2), ab);
+        }
+        tmem_st_wait();
+      }
+      PHASE_MARK(2);
+
+      if (!helped) {
+        wait_bar(cx, &m.bar_gp, par, 22, ci);
+        tc_fence_after();
+        PHASE_MARK(3);
+        PHASE_MARK_W3(0);
+        ap_epilogue(sbeta, ci);
+      }
       PHASE_MARK(10);
       PHASE_MARK_W3(1);
       PHASE_MARK_W7(0);
-      fence_proxy_async_smem();
+      if (!helped) fence_proxy_async_smem();
       tc_fence_before();
       warp_arrive(&m.bar_om, lane);  // S^T operand ready, Gram columns free: O+M1 may start
       // A^T visible to the solve warps
@@ -670,141 +1070,13 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       PHASE_MARK(4);
 
       if (warp < 4) {
-        // ---- T = (I + A)^{-1} and T' = T Diag(beta) (warps 0-3)
-        const uint32_t sat = sb + SM_GA;                // A^T, fp32 [i][r], pitch FP
-        const uint32_t stv = sb + SM_GB + OFF_TINV;     // T, fp32 [r][i], pitch FP
-        const uint32_t sxb = sb + SM_GB + OFF_XBUF;     // 4 blocks of 16 x XP fp32
-        if (warp < 2) {
-          // Diagonal 16 x 16 blocks by column-oriented forward substitution: lane
-          // owns column j of block a; after step m, t[m] is final and is eliminated
-          // from every later row.  Columns stream through a ring, three steps ahead.
-          const int a = 2 * warp + (lane >> 4), j = lane & 15, b0 = 16 * a;
-          float t[16];
-#pragma unroll
-          for (int r = 0; r < 16; ++r) t[r] = (r == j) ? 1.f : 0.f;
-          float cbuf[4][16];
-#pragma unroll
-          for (int p = 0; p < 3; ++p) {
-            lds8(*reinterpret_cast<float(*)[8]>(cbuf[p]), sat + 4u * ((b0 + p) * FP + b0));
-            lds8(*reinterpret_cast<float(*)[8]>(cbuf[p] + 8), sat + 4u * ((b0 + p) * FP + b0 + 8));
-          }
-#pragma unroll
-          for (int mc = 0; mc < 15; ++mc) {
-            if (mc + 3 < 15) {
-              float *nb = cbuf[(mc + 3) & 3];
-              lds8(*reinterpret_cast<float(*)[8]>(nb), sat + 4u * ((b0 + mc + 3) * FP + b0));
-              lds8(*reinterpret_cast<float(*)[8]>(nb + 8), sat + 4u * ((b0 + mc + 3) * FP + b0 + 8));
-            }
-            const float tmv = t[mc];
-            const float *col = cbuf[mc & 3];
-#pragma unroll
-            for (int r = mc + 1; r < 16; ++r) t[r] = fmaf(-col[r], tmv, t[r]);
-          }
-          // T (fp32, for the block recursion) and T' = T Diag(beta) (bf16 MMA operand;
-          // the block's upper triangle is zero because t[r] = 0 for r < j).
-          const float bj = ld_shared_f32(sbeta + 4u * (b0 + j));
-#pragma unroll
-          for (int r = 0; r < 16; ++r) {
-            st_shared_f32(stv + 4u * ((b0 + r) * FP + b0 + j), t[r]);
-            const __nv_bfloat16 tb16 = __float2bfloat16_rn(t[r] * bj);
-            st_shared_b16(sb + SM_TMAT + sw128_offset(b0 + r, (b0 + j) * 2),
-                          *reinterpret_cast<const uint16_t *>(&tb16));
-          }
+        if (helped) {  // T' of the package
+          wait_bar(cx, &m.bar_pkb, par, 44, ci);
+          warp_arrive(&m.bar_t1, lane);
+          warp_arrive(&m.bar_t, lane);
+        } else {
+          solve_T(sbeta, ci);
         }
-        PHASE_MARK(11);
-        __syncwarp();   // the 16 -> 32 level of a warp reads only that warp's diagonal blocks
-        // Off-diagonal blocks, block-recursive: 16 -> 32 (blocks (1,0), (3,2)), then
-        // 32 -> 64 (blocks (2,0), (2,1), (3,0), (3,1)), TF32 warp MMAs.
-        const int g = lane >> 2, t4 = lane & 3;
-        // acc (+)= A_{ab} T_{mb} with A from A^T (column-major, pitch FP) ...
-        auto mul_AT = [&](float (&acc)[2][4], int ab, int mb, int tcol) {
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            const int kc = 16 * mb + 8 * kk;
-            const uint32_t a0 = to_tf32(ld_shared_f32(sat + 4u * ((kc + t4) * FP + 16 * ab + g)));
-            const uint32_t a1 = to_tf32(ld_shared_f32(sat + 4u * ((kc + t4) * FP + 16 * ab + g + 8)));
-            const uint32_t a2 = to_tf32(ld_shared_f32(sat + 4u * ((kc + t4 + 4) * FP + 16 * ab + g)));
-            const uint32_t a3 = to_tf32(ld_shared_f32(sat + 4u * ((kc + t4 + 4) * FP + 16 * ab + g + 8)));
-            const uint32_t b0p = stv + 4u * ((kc + t4) * FP + tcol + g);
-            const uint32_t b1p = stv + 4u * ((kc + t4 + 4) * FP + tcol + g);
-            mma_tf32_16x8x8(acc[0], a0, a1, a2, a3, to_tf32(ld_shared_f32(b0p)),
-                            to_tf32(ld_shared_f32(b1p)));
-            mma_tf32_16x8x8(acc[1], a0, a1, a2, a3, to_tf32(ld_shared_f32(b0p + 32u)),
-                            to_tf32(ld_shared_f32(b1p + 32u)));
-          }
-        };
-        // ... and acc (+)= T_{ar} X with T row-major (pitch FP), X a 16 x 16 block (pitch XP).
-        auto mul_TX = [&](float (&acc)[2][4], int ar, int ac, uint32_t x) {
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            const uint32_t tq = stv + 4u * ((16 * ar) * FP + 16 * ac + 8 * kk);
-            const uint32_t a0 = to_tf32(ld_shared_f32(tq + 4u * (g * FP + t4)));
-            const uint32_t a1 = to_tf32(ld_shared_f32(tq + 4u * ((g + 8) * FP + t4)));
-            const uint32_t a2 = to_tf32(ld_shared_f32(tq + 4u * (g * FP + t4 + 4)));
-            const uint32_t a3 = to_tf32(ld_shared_f32(tq + 4u * ((g + 8) * FP + t4 + 4)));
-            const uint32_t x0 = x + 4u * ((8 * kk + t4) * XP + g);
-            const uint32_t x1 = x + 4u * ((8 * kk + t4 + 4) * XP + g);
-            mma_tf32_16x8x8(acc[0], a0, a1, a2, a3, to_tf32(ld_shared_f32(x0)),
-                            to_tf32(ld_shared_f32(x1)));
-            mma_tf32_16x8x8(acc[1], a0, a1, a2, a3, to_tf32(ld_shared_f32(x0 + 32u)),
-                            to_tf32(ld_shared_f32(x1 + 32u)));
-          }
-        };
-        auto store_blk = [&](uint32_t dst, int pitch, const float (&acc)[2][4], float sgn) {
-#pragma unroll
-          for (int nh = 0; nh < 2; ++nh) {
-            st_shared_f32x2(dst + 4u * (g * pitch + 8 * nh + 2 * t4), sgn * acc[nh][0],
-                            sgn * acc[nh][1]);
-            st_shared_f32x2(dst + 4u * ((g + 8) * pitch + 8 * nh + 2 * t4), sgn * acc[nh][2],
-                            sgn * acc[nh][3]);
-          }
-        };
-        // Final block T_ab: fp32 into T, and T' = T Diag(beta) as bf16 pairs.
-        auto store_T = [&](int ab, int bb, const float (&acc)[2][4]) {
-          store_blk(stv + 4u * ((16 * ab) * FP + 16 * bb), FP, acc, -1.f);
-#pragma unroll
-          for (int nh = 0; nh < 2; ++nh) {
-            const int col = 16 * bb + 8 * nh + 2 * t4;
-            const float2 bv = ld_shared_f32x2(sbeta + 4u * col);
-            const float b0v = bv.x, b1v = bv.y;
-            const uint32_t lo = pack_bf16x2(-acc[nh][0] * b0v, -acc[nh][1] * b1v);
-            const uint32_t hi = pack_bf16x2(-acc[nh][2] * b0v, -acc[nh][3] * b1v);
-            st_shared_b32(sb + SM_TMAT + sw128_offset(16 * ab + g, col * 2), lo);
-            st_shared_b32(sb + SM_TMAT + sw128_offset(16 * ab + g + 8, col * 2), hi);
-          }
-        };
-        const uint32_t xw = sxb + 4u * (warp * 16 * XP);
-        if (warp < 2) {  // level 16 -> 32: block (1,0) on warp 0, (3,2) on warp 1
-          const int ab = 2 * warp + 1, bb = 2 * warp;
-          float acc[2][4] = {};
-          mul_AT(acc, ab, bb, 16 * bb);  // X = A_ab T_bb
-          store_blk(xw, XP, acc, 1.f);
-          __syncwarp();
-          float o[2][4] = {};
-          mul_TX(o, ab, ab, xw);  // T_ab = -T_aa X
-          store_T(ab, bb, o);
-        }
-        PHASE_MARK(12);
-        named_sync(2, 128);
-        fence_proxy_async_smem();   // diagonal and 16 -> 32 blocks of T' are MMA operands
-        warp_arrive(&m.bar_t1, lane);
-        {  // level 32 -> 64: warp w -> block (2 + w/2, w%2)
-          const int ab = 2 + (warp >> 1), bb = warp & 1;
-          float acc[2][4] = {};
-          // X_{ab} = A_{ab,0:2} T_{0:2, bb} = sum_{m=bb}^{1} A_{ab,m} T_{m,bb}
-          for (int mb = bb; mb < 2; ++mb) mul_AT(acc, ab, mb, 16 * bb);
-          store_blk(xw, XP, acc, 1.f);
-          PHASE_MARK(13);
-          named_sync(2, 128);
-          // T_{ab} = -sum_{k=2}^{ab} T_{ab,k} X_{k,bb}
-          float o[2][4] = {};
-          for (int k = 2; k <= ab; ++k) mul_TX(o, ab, k, sxb + 4u * ((2 * (k - 2) + bb) * 16 * XP));
-          store_T(ab, bb, o);
-        }
-        PHASE_MARK_W3(2);
-        fence_proxy_async_smem();  // T' is an MMA operand
-        warp_arrive(&m.bar_t, lane);
-        PHASE_MARK(5);
       } else {
         // ---- the previous chunk's output rows (while the O+Y MMAs run), then
         // (V - Y)^T as a bf16 A operand (warps 4-7; lane n of quadrant q4 is value
@@ -815,8 +1087,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         PHASE_MARK_W4(1);
         wait_bar(cx, &m.bar_m1, par, 24, ci);
         tc_fence_after();
-        const bool ok_v = wait_bar(cx, &m.bar_v, par, 12, ci);
-        if (tid == 128 && ok_v) m.tma_waited[TMA_V]++;
+        wait_bar(cx, &m.bar_v, par, 12, ci);
         PHASE_MARK_W4(2);
         {
           const uint32_t vb = sb + SM_V + 2u * (lane_base + lane);
@@ -838,8 +1109,11 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           tmem_st_wait();
         }
         tc_fence_before();
+        // The staged output stores must have read the Kdec buffer before anything
+        // reuses it: a package copy (issued once bar_ny completes) or the next build.
+        if (helping && tid == 128) bulk_wait_read_all();
         warp_arrive(&m.bar_ny, lane);
-        if (tid == 128) bulk_wait_read_all();   // staging free before the next build
+        if (!helping && tid == 128) bulk_wait_read_all();
         PHASE_MARK_W4(3);
         PHASE_MARK_W7(1);
       }
@@ -864,9 +1138,48 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       PHASE_MARK(7);
       prev_tb = tb;
       prev_nv = nv;
-      // ---- the next chunk's operand tiles, while the state MMAs run
-      if (ci + 1 < n_chunks && !scan_build(ci + 1)) { failed = true; break; }
+      // ---- the next chunk's operand tiles, while the state MMAs run, unless a
+      // helper's package of it is on its way
+      if (ci + 1 < n_chunks) {
+        if (helping) {
+          wait_bar(cx, &m.bar_plan, par, 45, ci);
+          PHASE_STAMP(0, 52);
+          if (compute_sync_abort(&m.abort)) { failed = true; break; }
+          helped = m.plan[(ci + 1) & 1] != 0;
+        }
+        if (helped) {
+          chain_beta(ci + 1);
+          warp_arrive(&m.bar_build, lane);
+        } else if (!scan_build(ci + 1)) {
+          failed = true;
+          break;
+        }
+      }
       PHASE_MARK(8);
+    }
+    chain_done();
+
+    // ---- helper CTA: operand build, Gram / P and solve of each claimed chunk
+    for (int j = 0; helper && !failed; ++j) {
+      const uint32_t par = (uint32_t)(j & 1);
+      wait_bar(cx, &m.bar_plan, par, 63, j);
+      if (compute_sync_abort(&m.abort)) break;
+      const HelpClaim cl = m.claim[par];
+      if (!cl.valid) break;
+      if (j > 0) wait_bar(cx, &m.bar_wb, par ^ 1u, 64, j);  // the last package is out of smem
+      const uint32_t sbeta = sb + SM_BETA + 4u * C * par;
+      if (tid < C)
+        st_shared_f32(sbeta + 4u * tid,
+                      tid < cl.nv ? beta[((int64_t)cl.tb + tid) * H + cl.head] : 0.f);
+      if (!build_tiles(j, par, cl.nv, SM_KDEC)) break;
+      wait_bar(cx, &m.bar_gp, par, 65, j);
+      tc_fence_after();
+      ap_epilogue(sbeta, j);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      warp_arrive(&m.bar_om, lane);
+      if (compute_sync_abort(&m.abort)) break;
+      if (warp < 4) solve_T(sbeta, j);
     }
 
     // ---- the last chunk's output and the final state
@@ -879,7 +1192,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
     }
     const bool aborted = compute_sync_abort(&m.abort);
-    if (!failed && !aborted && final_state) {
+    if (!helper && !failed && !aborted && final_state) {
       const int n = lane_base + lane;
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
@@ -897,13 +1210,16 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   // ---- teardown (all warps)
   cta_sync();
-  if (warp == kMmaWarp && lane == 0 && m.abort && n_chunks > 0) {
-    // Drain what is still in flight (bounded), so no copy or MMA outlives the CTA.
+  if (warp == kMmaWarp && lane == 0 && m.abort) {
+    // Drain what is still in flight (bounded), so no copy or MMA outlives the CTA:
+    // the MMAs, then the last phase that carried a copy on each copy barrier (a
+    // barrier's phases complete in order).
     umma_commit(&m.bar_fin);
     mbar_wait(&m.bar_fin, 0, kWaitNs);
-    uint64_t *bars[3] = {&m.bar_qk, &m.bar_la, &m.bar_v};
-    for (int i = 0; i < 3; ++i)
-      if (m.tma_issued[i] > m.tma_waited[i]) mbar_wait(bars[i], m.tma_waited[i] & 1u, kWaitNs);
+    uint64_t *bars[5] = {&m.bar_qk, &m.bar_la, &m.bar_v, &m.bar_pka, &m.bar_pkb};
+    for (int i = 0; i < 5; ++i)
+      if (m.last_copy[i]) mbar_wait(bars[i], (m.last_copy[i] - 1u) & 1u, kWaitNs);
+    bulk_wait_all();
   }
   cta_sync();
   if (warp == 0) tmem_dealloc(tm, TM_COLS);
@@ -964,18 +1280,33 @@ cudaError_t launch_chunk_fwd_bf16_tc(const ChunkArgs &a, cudaStream_t stream) {
         !make_map(&mo, a.out, bf, 2, a.n_tokens, a.H, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(kda_chunk_fwd_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  HelpRing help;
+  memset(&help, 0, sizeof(help));
+  int32_t n_help = 0;
+  if (a.help_ws && a.n_help > 0 && a.n_tokens > 0 && a.n_seqs <= kHelpMaxSeqs) {
+    int32_t *hdr = reinterpret_cast<int32_t *>(a.help_ws);
+    help.cons_pos = hdr;
+    help.next_claim = hdr + chains;
+    help.flag = hdr + 2 * chains;
+    help.busy = hdr + (2 + kHelpSlots) * chains;
+    help.finished = hdr + (2 + 2 * kHelpSlots) * chains;
+    help.ring = a.help_ws + help_header_bytes(chains);
+    help.n_chains = (int32_t)chains;
+    n_help = a.n_help;
+  }
+  auto kernel = n_help > 0 ? kda_chunk_fwd_tc_kernel<true> : kda_chunk_fwd_tc_kernel<false>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   // The setmaxnreg split assumes the launch allocation it was sized for; with a
   // smaller one the compute warpgroups' .inc could never be satisfied.
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, kda_chunk_fwd_tc_kernel);
+  e = cudaFuncGetAttributes(&fa, kernel);
   if (e != cudaSuccess) return e;
   if ((uint32_t)fa.numRegs < kLaunchRegs) return cudaErrorNotSupported;
-  kda_chunk_fwd_tc_kernel<<<(unsigned)chains, kThreads, SMEM_BYTES, stream>>>(
+  kernel<<<(unsigned)(chains + n_help), kThreads, SMEM_BYTES, stream>>>(
       mq, mk, mv, mla, mo, a.beta, a.init_state, a.cu_seqlens, a.n_seqs, a.n_tokens, a.H,
-      static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.status);
+      static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.status, help);
   return cudaGetLastError();
 }
 

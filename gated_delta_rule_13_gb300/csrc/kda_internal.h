@@ -19,7 +19,36 @@ struct DeviceStatus {
   int32_t detail;   // where it happened (kernel-specific tag)
   int32_t chain;    // chain (seq * H + head) that recorded it
   int32_t chunk;    // chunk index inside the chain
+  int32_t help_published;  // chunk packages the helper CTAs wrote (bf16 prefill)
+  int32_t help_consumed;   // of those, the ones a chain CTA used
 };
+
+// Helper CTAs of the tensor-core prefill.  When a call has fewer chains than the
+// GPU has SMs, the idle SMs run "helpers" that compute the state-independent
+// half of chunks ahead of the chain CTAs: the operand build, the Gram matrix,
+// P and the triangular solve.  Each result ("package": the shared-memory images
+// of [Qt; Kt], Kdec, T', P and Gamma) goes to a per-chain ring of slots in the
+// workspace.  A chain CTA that finds a chunk's package ready copies it in and
+// skips that work; otherwise it computes the chunk itself.  It never waits for a
+// helper.
+constexpr int kHelpLead = 4;    // helpers claim chunks >= (chain's current chunk) + kHelpLead
+constexpr int kHelpSlots = 7;   // ring slots per chain (> kHelpLead + 1)
+constexpr size_t kHelpPackageBytes = 66048;   // 32768 + 16384 + 8192 + 8192 + 512
+constexpr size_t kHelpSlotStride = 66560;     // 1024-byte aligned slots
+struct HelpRing {
+  int32_t *cons_pos;    // [chains] chunk each chain CTA has started (n_chunks when done)
+  int32_t *next_claim;  // [chains] lowest chunk no helper has claimed yet
+  int32_t *flag;        // [chains * kHelpSlots] chunk + 1 of the package a slot holds, 0: none
+  int32_t *busy;        // [chains * kHelpSlots] chunk + 1 of the helper writing a slot, 0: free
+  int32_t *finished;    // chain CTAs that have finished
+  unsigned char *ring;  // [chains * kHelpSlots] package slots
+  int32_t n_chains;     // chain CTAs; blocks beyond them are helpers
+};
+// Bytes of the helper header (cons_pos, next_claim, flag, busy, counter), 1024-aligned.
+inline size_t help_header_bytes(int64_t chains) {
+  const size_t words = (size_t)chains * (2 + 2 * kHelpSlots) + 1;
+  return (words * sizeof(int32_t) + 1023) / 1024 * 1024;
+}
 
 // Arguments common to the prefill launchers.
 struct ChunkArgs {
@@ -32,6 +61,10 @@ struct ChunkArgs {
   void *out;
   float *final_state;
   DeviceStatus *status;
+  // Helper workspace (header then ring) for the bf16 prefill, or nullptr; its
+  // header must be zeroed before each launch.
+  unsigned char *help_ws;
+  int32_t n_help;  // helper CTAs to launch beside the chains (0: none)
 };
 
 cudaError_t launch_decode_step(float *state, const void *q, const void *k, const void *v,

@@ -29,7 +29,8 @@ HEAD_DIM = 128
 # Symbols declared in include/kda.h.
 EXPORTED = ("kda_status_string", "kda_version", "kda_chunk_fwd_workspace_size",
             "kda_chunk_fwd", "kda_read_device_status", "kda_decode_step",
-            "kda_chunk_fwd_noalloc", "kda_decode_replay", "kda_prep_fwd", "kda_post_fwd")
+            "kda_chunk_fwd_noalloc", "kda_decode_replay", "kda_prep_fwd", "kda_post_fwd",
+            "kda_read_chunk_stats")
 
 _lib = None
 
@@ -65,6 +66,8 @@ def library() -> ctypes.CDLL:
                                       ctypes.c_int, vp, vp, vp, sz, vp]
         lib.kda_read_device_status.restype = ctypes.c_int
         lib.kda_read_device_status.argtypes = [vp, vp, ctypes.c_int, ctypes.POINTER(i32)]
+        lib.kda_read_chunk_stats.restype = ctypes.c_int
+        lib.kda_read_chunk_stats.argtypes = [vp, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]
         lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
         lib.kda_chunk_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32,
                                               ctypes.c_int, vp, vp, vp]
@@ -168,7 +171,8 @@ def kda_chunk_fwd(q, k, v, log_alpha, beta, init_state=None, cu_seqlens=None, *,
     code = _dtype_code(q)
     ws_bytes = kda_chunk_fwd_workspace_size(n_seqs, N, H, dk, dv, code)
     if workspace is None:
-        workspace = torch.zeros(ws_bytes, dtype=torch.uint8, device=q.device)
+        # the library clears what it reads (status block, helper header) itself
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     _need_cuda("workspace", workspace)
     rc = library().kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
                                  _ptr(init_state), _ptr(cu_seqlens), n_seqs, N, H, dk, dv,
@@ -207,6 +211,17 @@ def kda_chunk_fwd_noalloc(q, k, v, log_alpha, beta, init_state=None, cu_seqlens=
                                          _stream_handle(stream))
     _check(rc, "kda_chunk_fwd_noalloc")
     return out, final_state
+
+
+def kda_read_chunk_stats(workspace, stream=None):
+    """Synchronise the stream and return (packages published by helper CTAs,
+    packages chain CTAs used) of the last kda_chunk_fwd on this workspace."""
+    _need_cuda("workspace", workspace)
+    pub, con = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(library().kda_read_chunk_stats(_ptr(workspace), _stream_handle(stream),
+                                          ctypes.byref(pub), ctypes.byref(con)),
+           "kda_read_chunk_stats")
+    return pub.value, con.value
 
 
 def kda_read_device_status(workspace, stream=None, clear: bool = True) -> int:

@@ -35,7 +35,8 @@ EXTRA = {9: "t0: build of this chunk: decay prefix done", 14: "t0: build: q/k ti
          34: "w3: solve done", 35: "w3: A/P TMEM load returned", 36: "w3: A/P first block done",
          37: "w3: S pass first TMEM load returned", 48: "w12: flush start",
          49: "w12: flush done", 40: "w7: A/P done (before sync)", 41: "w7: -Y pass done",
-         42: "w7: build done (before arrive)"}
+         42: "w7: build done (before arrive)", 51: "mma: next chunk planned",
+         52: "t0: plan seen"}
 SLOTS = 64
 
 
@@ -80,6 +81,15 @@ def main(workload: str = "k3_h96_t32768") -> None:
     for name, v in zip(PHASES, med):
         print(f"  {name:28s} {v:8.0f}  {100 * v / total:5.1f}%")
     print(f"  {'total per chunk':28s} {total:8.0f}")
+    # chunks whose state-independent half came from a helper CTA (slot 50)
+    helped = raw[1:-1, 50] == 1
+    for label, sel in (("helped", helped), ("computed", ~helped)):
+        if sel.sum() == 0:
+            continue
+        m = np.median(d[sel], axis=0)
+        print(f"  {label} chunks ({int(sel.sum())}): " +
+              ", ".join(f"{n.split(' ')[0]} {v:.0f}" for n, v in zip(PHASES, m)) +
+              f"; total {m.sum():.0f}")
     print("stamps as offsets from the chunk's first stamp (median):")
     marks = sorted([(np.median(raw[1:-1, i] - raw[1:-1, 0]), EXTRA[i]) for i in EXTRA
                     if raw[1:-1, i].any()] +

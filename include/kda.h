@@ -66,11 +66,21 @@ const char *kda_status_string(int status);
 int kda_version(void);
 
 /*
- * Bytes of device workspace kda_chunk_fwd needs for this problem size, written
- * to *bytes.  The workspace holds the device status word (bounded waits that
- * give up record KDA_ERR_TIMEOUT there; a device-resident cu_seqlens that is
- * not a valid prefix sum records KDA_ERR_INVALID_ARG) and, when cu_seqlens is
- * a host pointer, a device copy of it.
+ * Bytes of device workspace kda_chunk_fwd needs for this problem size on the
+ * current device, written to *bytes.  The workspace holds:
+ *   - the device status word (bounded waits that give up record
+ *     KDA_ERR_TIMEOUT there; a device-resident cu_seqlens that is not a valid
+ *     prefix sum records KDA_ERR_INVALID_ARG);
+ *   - when cu_seqlens is a host pointer, a device copy of it;
+ *   - for a bf16 call whose (sequence, head) chains leave at least three times
+ *     as many of the device's SMs idle as there are chains, the ring of the
+ *     helper CTAs.
+ *     These run on the idle SMs and compute the state-independent half of
+ *     later chunks (operand build, Gram matrix, triangular solve); about
+ *     455 KiB per chain.
+ * kda_chunk_fwd runs without helpers, with identical results, when the
+ * workspace it gets is large enough for everything but the ring.
+ * The environment variable KDA_CHUNK_HELPERS caps the helper count (0: none).
  * Errors: KDA_ERR_INVALID_ARG for a NULL `bytes` or negative sizes,
  * KDA_ERR_UNSUPPORTED for dk/dv/dtype outside the supported set.
  */
@@ -161,6 +171,16 @@ int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const flo
  * Errors: KDA_ERR_INVALID_ARG (NULL workspace or device_status), KDA_ERR_CUDA.
  */
 int kda_read_device_status(void *workspace, void *stream, int clear, int32_t *device_status);
+
+/*
+ * Helper activity of the last kda_chunk_fwd call that used `workspace`:
+ * *help_published = chunk packages the helper CTAs wrote, *help_consumed = the
+ * ones a chain CTA used instead of computing the chunk itself (both 0 when no
+ * helpers ran).  Synchronises `stream` first.
+ * Errors: KDA_ERR_INVALID_ARG (NULL pointer), KDA_ERR_CUDA.
+ */
+int kda_read_chunk_stats(void *workspace, void *stream, int32_t *help_published,
+                         int32_t *help_consumed);
 
 /*
  * One recurrent decode step for B sequences x H heads, one new token each,

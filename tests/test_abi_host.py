@@ -34,7 +34,8 @@ def test_header_declares_expected_entry_points():
     names = declared_functions()
     for n in ("kda_chunk_fwd", "kda_decode_step", "kda_decode_replay", "kda_prep_fwd",
               "kda_post_fwd", "kda_chunk_fwd_workspace_size",
-              "kda_status_string", "kda_read_device_status", "kda_version"):
+              "kda_status_string", "kda_read_device_status", "kda_read_chunk_stats",
+              "kda_version"):
         assert n in names
 
 
@@ -194,6 +195,13 @@ def test_read_device_status_null(lib):
     st = ctypes.c_int32(0)
     assert lib.kda_read_device_status(None, None, 0, ctypes.byref(st)) == 1
     assert lib.kda_read_device_status(ctypes.c_void_p(A), None, 0, None) == 1
+
+
+def test_read_chunk_stats_null(lib):
+    a, b = ctypes.c_int32(0), ctypes.c_int32(0)
+    assert lib.kda_read_chunk_stats(None, None, ctypes.byref(a), ctypes.byref(b)) == 1
+    assert lib.kda_read_chunk_stats(ctypes.c_void_p(A), None, None, ctypes.byref(b)) == 1
+    assert lib.kda_read_chunk_stats(ctypes.c_void_p(A), None, ctypes.byref(a), None) == 1
 
 
 def test_product_path_does_not_import_oracle():
