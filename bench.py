@@ -309,8 +309,10 @@ def layer_ops_bench(dev, peaks, steps: int = 20, warmup: int = 3, T: int = 32768
 
 def few_chains_bench(dev, peaks, steps: int = 20, warmup: int = 3, T: int = 65536, H: int = 8):
     """Prefill of one long sequence over few heads (8 of K3's 96: the share of a
-    GPU under head-sharded tensor parallelism), with the helper CTAs that then
-    fill the idle SMs, and without them (KDA_CHUNK_HELPERS=0)."""
+    GPU under head-sharded tensor parallelism), three ways: each (sequence, head)
+    chain on one SM ("plain"), with helper CTAs on the idle SMs ("helpers"),
+    and with the in-device split of the sequence into segments ("split", what
+    kda_chunk_fwd picks for this shape)."""
     import torch
     from gated_delta_rule_13_gb300 import inputs, kda
     x = inputs.prefill_inputs([T], H=H, dtype="bf16", device=dev, seed=35)
@@ -318,13 +320,17 @@ def few_chains_bench(dev, peaks, steps: int = 20, warmup: int = 3, T: int = 6553
     fin = torch.empty(1, H, 128, 128, device=dev)
     res = {"workload": f"one sequence of {T} tokens x {H} heads, bf16"}
     stream = torch.cuda.current_stream()
-    old = os.environ.get("KDA_CHUNK_HELPERS")
+    saved = {k: os.environ.get(k) for k in ("KDA_CHUNK_SPLIT", "KDA_CHUNK_HELPERS")}
+    variants = (("plain", {"KDA_CHUNK_SPLIT": "0", "KDA_CHUNK_HELPERS": "0"}),
+                ("helpers", {"KDA_CHUNK_SPLIT": "0", "KDA_CHUNK_HELPERS": None}),
+                ("split", {"KDA_CHUNK_SPLIT": None, "KDA_CHUNK_HELPERS": None}))
     try:
-        for name, env in (("without_helpers", "0"), ("with_helpers", None)):
-            if env is None:
-                os.environ.pop("KDA_CHUNK_HELPERS", None)
-            else:
-                os.environ["KDA_CHUNK_HELPERS"] = env
+        for name, env in variants:
+            for k, v in env.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
             ws = torch.empty(kda.kda_chunk_fwd_workspace_size(1, T, H, dtype=kda.KDA_BF16),
                              dtype=torch.uint8, device=dev)
 
@@ -345,15 +351,18 @@ def few_chains_bench(dev, peaks, steps: int = 20, warmup: int = 3, T: int = 6553
             pub, used = kda.kda_read_chunk_stats(ws)
             gbs = prefill_bytes(x, H) / (ms / 1000.0) / 1e9
             res[name] = {"tokens_per_s": T / (ms / 1000.0), "ms_per_launch": ms,
-                         "hbm_frac": gbs / peaks["hbm_gbs"],
-                         "chunks_from_helpers": used, "chunks": H * ((T + 63) // 64),
-                         "packages_published": pub}
+                         "hbm_frac": gbs / peaks["hbm_gbs"]}
+            if name == "helpers":
+                res[name].update({"chunks_from_helpers": used, "packages_published": pub,
+                                  "chunks": H * ((T + 63) // 64)})
     finally:
-        if old is None:
-            os.environ.pop("KDA_CHUNK_HELPERS", None)
-        else:
-            os.environ["KDA_CHUNK_HELPERS"] = old
-    res["speedup"] = res["without_helpers"]["ms_per_launch"] / res["with_helpers"]["ms_per_launch"]
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    for name in ("helpers", "split"):
+        res[name]["speedup_vs_plain"] = res["plain"]["ms_per_launch"] / res[name]["ms_per_launch"]
     del x, out, fin
     return res
 

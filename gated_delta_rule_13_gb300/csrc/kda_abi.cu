@@ -61,15 +61,44 @@ int32_t help_ctas(int64_t chains, int dtype) {
   return n > 0 ? (int32_t)n : 0;
 }
 
+// Segments per sequence for the in-device split of a bf16 prefill (0: no
+// split).  Its first pass runs 2 K CTAs per chain and both passes take about
+// T / K chunk-steps, so it needs 2 K x chains <= SMs and pays off from K = 3
+// on; segments are kept at two chunks or more on average.  The environment
+// variable KDA_CHUNK_SPLIT caps K (0 turns the split off).
+int32_t split_factor(int32_t n_seqs, int64_t n_tokens, int32_t H, int dtype) {
+  const int64_t chains = (int64_t)n_seqs * H;
+  if (dtype != KDA_BF16 || chains <= 0 || n_tokens <= 0) return 0;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  int64_t k = sms / (2 * chains);
+  const int64_t by_length = n_tokens / ((int64_t)n_seqs * 2 * kda::kChunk);
+  if (by_length < k) k = by_length;
+  if (const char *env = getenv("KDA_CHUNK_SPLIT")) {
+    const long cap = strtol(env, nullptr, 10);
+    if (cap >= 0 && cap < k) k = cap;
+  }
+  return k >= 3 ? (int32_t)k : 0;
+}
+
 size_t help_workspace_bytes(int64_t chains) {
   return kda::help_header_bytes(chains) + (size_t)chains * kda::kHelpSlots * kda::kHelpSlotStride;
 }
 
-// Full workspace: the base part, then (when helpers would run) the helper header and ring.
-size_t workspace_bytes_for(int32_t n_seqs, int32_t H, int dtype) {
+// Full workspace: the base part, then the scratch of the in-device split, or
+// (when helpers would run instead) the helper header and ring.
+size_t workspace_bytes_for(int32_t n_seqs, int64_t n_tokens, int32_t H, int dtype) {
   const int64_t chains = (int64_t)n_seqs * H;
   size_t b = base_workspace_bytes(n_seqs);
-  if (help_ctas(chains, dtype) > 0) b += help_workspace_bytes(chains);
+  const int32_t n_split = split_factor(n_seqs, n_tokens, H, dtype);
+  if (n_split > 0)
+    b += kda::split_workspace_bytes(n_seqs, H, n_split);
+  else if (help_ctas(chains, dtype) > 0)
+    b += help_workspace_bytes(chains);
   return b;
 }
 
@@ -110,7 +139,7 @@ int kda_chunk_fwd_workspace_size(int32_t n_seqs, int64_t n_tokens, int32_t H, in
   if (!bytes || n_seqs < 0 || n_tokens < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
   const int d = check_dims(dk, dv, dtype);
   if (d != KDA_OK) return d;
-  *bytes = workspace_bytes_for(n_seqs, H, dtype);
+  *bytes = workspace_bytes_for(n_seqs, n_tokens, H, dtype);
   return KDA_OK;
 }
 
@@ -170,9 +199,16 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
   a.H = H; a.out = out; a.final_state = final_state; a.status = status;
   a.help_ws = nullptr;
   a.n_help = 0;
+  const int64_t chains = (int64_t)n_seqs * H;
+  // The in-device split, when it applies and the workspace has its scratch.
+  const int32_t n_split = split_factor(n_seqs, n_tokens, H, dtype);
+  if (n_split > 0 && workspace_bytes >= need + kda::split_workspace_bytes(n_seqs, H, n_split)) {
+    const cudaError_t e = kda::launch_chunk_fwd_split(a, n_split, ws + need, st);
+    if (e == cudaErrorNotSupported) return KDA_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+  }
   // Helpers run when the workspace has room for their ring (a workspace sized by
   // kda_chunk_fwd_workspace_size on this device does); their header starts zeroed.
-  const int64_t chains = (int64_t)n_seqs * H;
   const int32_t n_help = help_ctas(chains, dtype);
   if (n_help > 0 && n_tokens > 0 && workspace_bytes >= need + help_workspace_bytes(chains)) {
     a.help_ws = ws + need;

@@ -257,11 +257,16 @@ __device__ __forceinline__ void lds8(float (&v)[8], uint32_t saddr) {
 // Block column index of tile pair (a, b), a >= b, in the Gram column operand.
 __host__ __device__ constexpr int blk(int a, int b) { return a * (a + 1) / 2 + b; }
 
-// kHelp selects the instantiation with helper CTAs (and the chain CTAs' side of
-// their protocol); without it every helper branch compiles away, which keeps
-// the plain path as fast as it was before helpers existed (the runtime checks
-// alone cost about 10 % on a 96-chain prefill).
-template <bool kHelp>
+// Kernel variants.  kModeHelp adds helper CTAs (and the chain CTAs' side of
+// their protocol); kModeTransitions is the first pass of the in-device split of
+// long sequences: block b < gridDim.x / 2 runs chain b from a zero state (its
+// final state is the segment's B), block b + gridDim.x / 2 runs the same chain
+// as a transition (state I, v = 0: its final state is the segment's transition
+// matrix M), and neither writes outputs.  Each mode compiles its branches away
+// in the others, which keeps the plain path as fast as before (the runtime
+// checks alone cost about 10 % on a 96-chain prefill).
+constexpr int kModePlain = 0, kModeHelp = 1, kModeTransitions = 2;
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -272,16 +277,18 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const int32_t *__restrict__ cu_seqlens, int32_t n_seqs, int64_t n_tokens,
                         int32_t H, __nv_bfloat16 *__restrict__ out,
                         float *__restrict__ final_state, DeviceStatus *status,
-                        const HelpRing help) {
+                        const HelpRing help, float *__restrict__ final_state_m) {
   // Indexing the __shared__ array directly (no integer round trip) keeps every
   // access a shared-memory instruction.  The 128-byte swizzle atoms need a
   // 1024-byte aligned base, checked below.
   extern __shared__ __align__(1024) uint8_t smem[];
   Misc &m = *reinterpret_cast<Misc *>(smem + SM_MISC);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int chain = blockIdx.x;
+  // transition run of chain blockIdx.x - gridDim.x / 2 (first pass of a split)
+  const bool transition = kMode == kModeTransitions && blockIdx.x >= gridDim.x / 2;
+  const int chain = transition ? (int)(blockIdx.x - gridDim.x / 2) : (int)blockIdx.x;
   // Blocks past the chains are helpers (only when the call has a helper ring).
-  const bool helping = kHelp && help.ring != nullptr;
+  const bool helping = kMode == kModeHelp && help.ring != nullptr;
   const bool helper = helping && chain >= help.n_chains;
   const int seq = chain / H, h = chain % H;
   const Ctx cx{smem, &m, status, chain};
@@ -651,7 +658,9 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         uint32_t r[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          r[j] = __float_as_uint(init_state ? init_state[sbase + (int64_t)(c0 + j) * D + n] : 0.f);
+          r[j] = __float_as_uint(transition ? (c0 + j == n ? 1.f : 0.f)
+                                 : init_state ? init_state[sbase + (int64_t)(c0 + j) * D + n]
+                                              : 0.f);
         tmem_st32(tmem_addr(tm, lane_base, TM_S + c0), r);
       }
       tmem_st_wait();
@@ -1083,7 +1092,8 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         // channel n).  Staging: the Kdec buffer of chunks ci - 1 and ci + 1, idle
         // until the next build.
         PHASE_MARK_W4(0);
-        if (ci > 0) flush_output(prev_tb, prev_nv, TM_O + 64u * (par ^ 1u), SM_KDEC + 16384u * (par ^ 1u));
+        if (kMode != kModeTransitions && ci > 0)
+          flush_output(prev_tb, prev_nv, TM_O + 64u * (par ^ 1u), SM_KDEC + 16384u * (par ^ 1u));
         PHASE_MARK_W4(1);
         wait_bar(cx, &m.bar_m1, par, 24, ci);
         tc_fence_after();
@@ -1100,8 +1110,11 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
               const uint32_t row = 32u * part + 2u * jj;
-              const float v0 = __uint_as_float(ld_shared_u16(vb + row * 256u) << 16);
-              const float v1 = __uint_as_float(ld_shared_u16(vb + (row + 1u) * 256u) << 16);
+              // a transition run has v = 0
+              const float v0 =
+                  transition ? 0.f : __uint_as_float(ld_shared_u16(vb + row * 256u) << 16);
+              const float v1 =
+                  transition ? 0.f : __uint_as_float(ld_shared_u16(vb + (row + 1u) * 256u) << 16);
               p[jj] = pack_bf16x2(v0 - __uint_as_float(y[2 * jj]), v1 - __uint_as_float(y[2 * jj + 1]));
             }
             tmem_st16(tmem_addr(tm, lane_base, TM_NY + 16u * part), p);
@@ -1187,7 +1200,8 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       wait_bar(cx, &m.bar_m2, (uint32_t)((n_chunks - 1) & 1), 26, n_chunks - 1);
       tc_fence_after();
       if (warp >= 4) {
-        flush_output(prev_tb, prev_nv, TM_O + 64u * (uint32_t)((n_chunks - 1) & 1), SM_KDEC);
+        if (kMode != kModeTransitions)
+          flush_output(prev_tb, prev_nv, TM_O + 64u * (uint32_t)((n_chunks - 1) & 1), SM_KDEC);
         if (tid == 128) bulk_wait_all();
       }
     }
@@ -1202,7 +1216,8 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         tmem_ld_wait(r);
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          final_state[sbase + (int64_t)(c0 + j) * D + n] = __uint_as_float(r[j]);
+          (transition ? final_state_m : final_state)[sbase + (int64_t)(c0 + j) * D + n] =
+              __uint_as_float(r[j]);
       }
     }
     if (tid == 128) bulk_wait_all();  // no output store outlives the CTA, on any path
@@ -1283,7 +1298,7 @@ cudaError_t launch_chunk_fwd_bf16_tc(const ChunkArgs &a, cudaStream_t stream) {
   HelpRing help;
   memset(&help, 0, sizeof(help));
   int32_t n_help = 0;
-  if (a.help_ws && a.n_help > 0 && a.n_tokens > 0 && a.n_seqs <= kHelpMaxSeqs) {
+  if (a.mode == ChunkArgs::kPlain && a.help_ws && a.n_help > 0 && a.n_tokens > 0 && a.n_seqs <= kHelpMaxSeqs) {
     int32_t *hdr = reinterpret_cast<int32_t *>(a.help_ws);
     help.cons_pos = hdr;
     help.next_claim = hdr + chains;
@@ -1294,7 +1309,12 @@ cudaError_t launch_chunk_fwd_bf16_tc(const ChunkArgs &a, cudaStream_t stream) {
     help.n_chains = (int32_t)chains;
     n_help = a.n_help;
   }
-  auto kernel = n_help > 0 ? kda_chunk_fwd_tc_kernel<true> : kda_chunk_fwd_tc_kernel<false>;
+  const bool transitions = a.mode == ChunkArgs::kTransitions;
+  if (transitions) n_help = 0;
+  if (transitions && (!a.final_state || !a.final_state_m)) return cudaErrorInvalidValue;
+  auto kernel = transitions ? kda_chunk_fwd_tc_kernel<kModeTransitions>
+                : n_help > 0 ? kda_chunk_fwd_tc_kernel<kModeHelp>
+                             : kda_chunk_fwd_tc_kernel<kModePlain>;
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -1304,9 +1324,11 @@ cudaError_t launch_chunk_fwd_bf16_tc(const ChunkArgs &a, cudaStream_t stream) {
   e = cudaFuncGetAttributes(&fa, kernel);
   if (e != cudaSuccess) return e;
   if ((uint32_t)fa.numRegs < kLaunchRegs) return cudaErrorNotSupported;
-  kernel<<<(unsigned)(chains + n_help), kThreads, SMEM_BYTES, stream>>>(
+  const int64_t blocks = transitions ? 2 * chains : chains + n_help;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  kernel<<<(unsigned)blocks, kThreads, SMEM_BYTES, stream>>>(
       mq, mk, mv, mla, mo, a.beta, a.init_state, a.cu_seqlens, a.n_seqs, a.n_tokens, a.H,
-      static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.status, help);
+      static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.status, help, a.final_state_m);
   return cudaGetLastError();
 }
 

@@ -65,6 +65,13 @@ struct ChunkArgs {
   // header must be zeroed before each launch.
   unsigned char *help_ws;
   int32_t n_help;  // helper CTAs to launch beside the chains (0: none)
+  // kTransitions (bf16 only): first pass of an in-device split.  Every chain runs
+  // twice without writing outputs: from a zero state (final state -> final_state,
+  // the segment's B) and from the identity with v = 0 (final state ->
+  // final_state_m, the segment's transition M).  init_state is ignored.
+  enum Mode { kPlain = 0, kTransitions = 2 };
+  int32_t mode = kPlain;
+  float *final_state_m = nullptr;
 };
 
 cudaError_t launch_decode_step(float *state, const void *q, const void *k, const void *v,
@@ -89,5 +96,11 @@ cudaError_t launch_chunk_fwd_f32(const ChunkArgs &a, cudaStream_t stream);
 
 // Returns cudaErrorNotSupported if the tensor-map entry point is unavailable.
 cudaError_t launch_chunk_fwd_bf16_tc(const ChunkArgs &a, cudaStream_t stream);
+
+// In-device split of every sequence into K segments (K >= 2; bf16): scratch of
+// split_workspace_bytes() at `ws` (1024-byte aligned); a.help_ws is ignored.
+size_t split_workspace_bytes(int32_t n_seqs, int32_t H, int32_t K);
+cudaError_t launch_chunk_fwd_split(const ChunkArgs &a, int32_t K, unsigned char *ws,
+                                   cudaStream_t stream);
 
 }  // namespace kda

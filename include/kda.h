@@ -72,15 +72,23 @@ int kda_version(void);
  *     KDA_ERR_TIMEOUT there; a device-resident cu_seqlens that is not a valid
  *     prefix sum records KDA_ERR_INVALID_ARG);
  *   - when cu_seqlens is a host pointer, a device copy of it;
- *   - for a bf16 call whose (sequence, head) chains leave at least three times
- *     as many of the device's SMs idle as there are chains, the ring of the
+ *   - for a bf16 call with few enough (sequence, head) chains that each
+ *     sequence can be cut into K >= 3 segments with 2 K x chains <= SMs, the
+ *     scratch of the in-device split (segment bounds and three fp32 states per
+ *     segment and head): the segments run side by side and their states are
+ *     stitched together exactly ("Kimi K3: 架构、训练与系统全景解析", section
+ *     7.1: segments compose as affine maps of the state);
+ *   - otherwise, for a bf16 call whose chains leave at least three times as
+ *     many of the device's SMs idle as there are chains, the ring of the
  *     helper CTAs.
  *     These run on the idle SMs and compute the state-independent half of
  *     later chunks (operand build, Gram matrix, triangular solve); about
  *     455 KiB per chain.
- * kda_chunk_fwd runs without helpers, with identical results, when the
- * workspace it gets is large enough for everything but the ring.
- * The environment variable KDA_CHUNK_HELPERS caps the helper count (0: none).
+ * kda_chunk_fwd runs without the split or the helpers when the workspace it
+ * gets has room for neither.  Helpers leave the results bitwise unchanged; the
+ * split changes the rounding (its results meet the same tolerances).  The
+ * environment variables KDA_CHUNK_SPLIT and KDA_CHUNK_HELPERS cap the segment
+ * and helper counts (0 turns either off).
  * Errors: KDA_ERR_INVALID_ARG for a NULL `bytes` or negative sizes,
  * KDA_ERR_UNSUPPORTED for dk/dv/dtype outside the supported set.
  */

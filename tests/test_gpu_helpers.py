@@ -17,6 +17,19 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
+@pytest.fixture(autouse=True)
+def _no_split():
+    """These calls are small enough for the in-device split, which takes
+    precedence over helpers: turn it off here."""
+    old = os.environ.get("KDA_CHUNK_SPLIT")
+    os.environ["KDA_CHUNK_SPLIT"] = "0"
+    yield
+    if old is None:
+        os.environ.pop("KDA_CHUNK_SPLIT", None)
+    else:
+        os.environ["KDA_CHUNK_SPLIT"] = old
+
+
 def _run(x, helpers):
     """kda_chunk_fwd with helpers on (library default) or off; returns the
     outputs and the helper counters of the call."""
