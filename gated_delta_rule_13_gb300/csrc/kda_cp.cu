@@ -31,7 +31,7 @@ constexpr int C = kChunk;
 // pieces of equal whole-chunk length (the last one shorter, trailing ones
 // possibly empty); seg_cu[n_seqs K] = cu[n_seqs].  A malformed cu_seqlens gives
 // a malformed seg_cu, which the prefill kernel then reports.
-__global__ void segment_bounds_kernel(const int32_t *__restrict__ cu, int32_t n_seqs, int32_t K,
+__global__ void kda_split_bounds_kernel(const int32_t *__restrict__ cu, int32_t n_seqs, int32_t K,
                                       int32_t *__restrict__ seg_cu) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t n = (int64_t)n_seqs * K;
@@ -53,7 +53,7 @@ __global__ void segment_bounds_kernel(const int32_t *__restrict__ cu, int32_t n_
 // S evolve independently under S <- M S + B.  start[s K + j] receives S_j.
 constexpr int kCols = 32;
 __global__ void __launch_bounds__(256, 1)
-combine_kernel(const float *__restrict__ init, const float *__restrict__ B,
+kda_split_combine_kernel(const float *__restrict__ init, const float *__restrict__ B,
                const float *__restrict__ M, int32_t n_seqs, int32_t K, int32_t H,
                float *__restrict__ start) {
   __shared__ float4 sbuf[2][D][kCols / 4];
@@ -124,7 +124,7 @@ cudaError_t launch_chunk_fwd_split(const ChunkArgs &a, int32_t K, unsigned char 
   int32_t *seg_cu = reinterpret_cast<int32_t *>(ws);
   float *B = reinterpret_cast<float *>(ws + cu_bytes), *M = B + states, *S = M + states;
 
-  segment_bounds_kernel<<<(unsigned)((nseg + 1 + 255) / 256), 256, 0, stream>>>(
+  kda_split_bounds_kernel<<<(unsigned)((nseg + 1 + 255) / 256), 256, 0, stream>>>(
       a.cu_seqlens, a.n_seqs, K, seg_cu);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -141,7 +141,7 @@ cudaError_t launch_chunk_fwd_split(const ChunkArgs &a, int32_t K, unsigned char 
   e = launch_chunk_fwd_bf16_tc(p, stream);
   if (e != cudaSuccess) return e;
 
-  combine_kernel<<<dim3((unsigned)(a.n_seqs * a.H), D / kCols), 256, 0, stream>>>(
+  kda_split_combine_kernel<<<dim3((unsigned)(a.n_seqs * a.H), D / kCols), 256, 0, stream>>>(
       a.init_state, B, M, a.n_seqs, K, a.H, S);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
