@@ -241,6 +241,97 @@ int kda_read_device_status(void *workspace, void *stream, int clear, int32_t *de
   return KDA_OK;
 }
 
+int kda_chunk_fwd_transitions(const void *q, const void *k, const void *v,
+                              const float *log_alpha, const float *beta,
+                              const int32_t *cu_seqlens, int32_t n_seqs, int64_t n_tokens,
+                              int32_t H, int32_t dk, int32_t dv, int dtype, float *state_b,
+                              float *state_m, void *workspace, size_t workspace_bytes,
+                              void *stream) {
+  if (n_seqs < 0 || n_tokens < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+  const int d = check_dims(dk, dv, dtype);
+  if (d != KDA_OK) return d;
+  if (dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+  if (!cu_seqlens || !state_b || !state_m) return KDA_ERR_INVALID_ARG;
+  if (n_tokens > 0 && (!q || !k || !v || !log_alpha || !beta)) return KDA_ERR_INVALID_ARG;
+  if ((int64_t)n_seqs * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+  const void *tensors[] = {q, k, v, log_alpha, state_b, state_m};
+  for (const void *p : tensors)
+    if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  if (beta && !aligned(beta, 4)) return KDA_ERR_INVALID_ARG;
+  const size_t state_bytes = (size_t)n_seqs * H * dk * dv * sizeof(float);
+  if (state_bytes > 0 && ranges_overlap(state_b, state_bytes, state_m, state_bytes))
+    return KDA_ERR_INVALID_ARG;
+  const size_t need = base_workspace_bytes(n_seqs);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return KDA_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  bool attr_ok = false;
+  const bool cu_on_device = is_device_pointer(cu_seqlens, &attr_ok);
+  if (!attr_ok) return KDA_ERR_CUDA;
+  const int32_t *cu_dev = cu_seqlens;
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  if (!cu_on_device) {
+    if (cu_seqlens[0] != 0 || cu_seqlens[n_seqs] != n_tokens) return KDA_ERR_INVALID_ARG;
+    for (int32_t s = 0; s < n_seqs; ++s)
+      if (cu_seqlens[s + 1] < cu_seqlens[s]) return KDA_ERR_INVALID_ARG;
+    int32_t *dst = reinterpret_cast<int32_t *>(ws + kStatusBytes);
+    if (cudaMemcpyAsync(dst, cu_seqlens, sizeof(int32_t) * ((size_t)n_seqs + 1),
+                        cudaMemcpyHostToDevice, st) != cudaSuccess) {
+      cudaGetLastError();
+      return KDA_ERR_CUDA;
+    }
+    cu_dev = dst;
+  }
+  kda::DeviceStatus *status = reinterpret_cast<kda::DeviceStatus *>(ws);
+  if (cudaMemsetAsync(status, 0, sizeof(kda::DeviceStatus), st) != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_CUDA;
+  }
+  if (n_seqs == 0) return KDA_OK;
+  kda::ChunkArgs a;
+  a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta;
+  a.init_state = nullptr; a.cu_seqlens = cu_dev; a.n_seqs = n_seqs; a.n_tokens = n_tokens;
+  a.H = H;
+  a.out = const_cast<void *>(q);  // a valid tensor map base; this pass writes no outputs
+  a.final_state = state_b; a.status = status;
+  a.help_ws = nullptr; a.n_help = 0;
+  a.mode = kda::ChunkArgs::kTransitions;
+  a.final_state_m = state_m;
+  const cudaError_t e = kda::launch_chunk_fwd_bf16_tc(a, st);
+  if (e == cudaErrorNotSupported) return KDA_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_state_combine(const float *init_state, const float *state_b, const float *state_m,
+                      int32_t n_seqs, int32_t n_segments, int32_t H, int32_t dk, int32_t dv,
+                      float *start_states, float *end_state, void *stream) {
+  if (n_seqs < 0 || n_segments < 1 || H <= 0) return KDA_ERR_INVALID_ARG;
+  const int d = check_dims(dk, dv, KDA_F32);
+  if (d != KDA_OK) return d;
+  if (!state_b || !state_m) return KDA_ERR_INVALID_ARG;
+  if ((int64_t)n_seqs * n_segments * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+  const void *tensors[] = {init_state, state_b, state_m, start_states, end_state};
+  for (const void *p : tensors)
+    if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  const size_t one = (size_t)H * dk * dv * sizeof(float);
+  const size_t seg = one * n_seqs * n_segments, seqs = one * n_seqs;
+  // the outputs may not overlap any input, nor each other
+  const void *ins[] = {init_state, state_b, state_m};
+  const size_t in_bytes[] = {seqs, seg, seg};
+  for (int i = 0; i < 3; ++i) {
+    if (!ins[i] || seqs == 0) continue;
+    if (start_states && ranges_overlap(start_states, seg, ins[i], in_bytes[i]))
+      return KDA_ERR_INVALID_ARG;
+    if (end_state && ranges_overlap(end_state, seqs, ins[i], in_bytes[i]))
+      return KDA_ERR_INVALID_ARG;
+  }
+  if (start_states && end_state && seqs > 0 && ranges_overlap(start_states, seg, end_state, seqs))
+    return KDA_ERR_INVALID_ARG;
+  const cudaError_t e = kda::launch_state_combine(init_state, state_b, state_m, n_seqs,
+                                                  n_segments, H, start_states, end_state,
+                                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 int kda_read_chunk_stats(void *workspace, void *stream, int32_t *help_published,
                          int32_t *help_consumed) {
   if (!workspace || !help_published || !help_consumed) return KDA_ERR_INVALID_ARG;

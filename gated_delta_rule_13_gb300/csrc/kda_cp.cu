@@ -50,12 +50,13 @@ __global__ void kda_split_bounds_kernel(const int32_t *__restrict__ cu, int32_t 
 }
 
 // One CTA per (sequence, head, 32-column block of the state): the columns of
-// S evolve independently under S <- M S + B.  start[s K + j] receives S_j.
+// S evolve independently under S <- M S + B.  start[s K + j] receives S_j
+// (j < K) and end[s] the composed S_K, each when non-null.
 constexpr int kCols = 32;
 __global__ void __launch_bounds__(256, 1)
 kda_split_combine_kernel(const float *__restrict__ init, const float *__restrict__ B,
                const float *__restrict__ M, int32_t n_seqs, int32_t K, int32_t H,
-               float *__restrict__ start) {
+               float *__restrict__ start, float *__restrict__ end) {
   __shared__ float4 sbuf[2][D][kCols / 4];
   const int sh = blockIdx.x, s = sh / H, h = sh % H;
   const int col0 = kCols * blockIdx.y;
@@ -73,13 +74,16 @@ kda_split_combine_kernel(const float *__restrict__ init, const float *__restrict
     sbuf[0][r][c] = v;
   }
   __syncthreads();
-  for (int j = 0; j < K; ++j) {
+  for (int j = 0;; ++j) {
     const int64_t seg = (int64_t)s * K + j;
     const int cur = j & 1;
-    float4 *out = reinterpret_cast<float4 *>(start + blk(seg) + (int64_t)row * D + col0);
+    float *dst = j < K ? (start ? start + blk(seg) : nullptr) : (end ? end + blk(s) : nullptr);
+    if (dst) {
+      float4 *out = reinterpret_cast<float4 *>(dst + (int64_t)row * D + col0);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) out[c4 + q] = sbuf[cur][row][c4 + q];
-    if (j + 1 == K) break;
+      for (int q = 0; q < 4; ++q) out[c4 + q] = sbuf[cur][row][c4 + q];
+    }
+    if (j == K || (j + 1 == K && !end)) break;
     // S_{j+1}[row][cols] = B_j[row][cols] + sum_k M_j[row][k] S_j[k][cols]
     const float *m = M + blk(seg) + (int64_t)row * D;
     const float4 *b = reinterpret_cast<const float4 *>(B + blk(seg) + (int64_t)row * D + col0);
@@ -142,7 +146,7 @@ cudaError_t launch_chunk_fwd_split(const ChunkArgs &a, int32_t K, unsigned char 
   if (e != cudaSuccess) return e;
 
   kda_split_combine_kernel<<<dim3((unsigned)(a.n_seqs * a.H), D / kCols), 256, 0, stream>>>(
-      a.init_state, B, M, a.n_seqs, K, a.H, S);
+      a.init_state, B, M, a.n_seqs, K, a.H, S, nullptr);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -163,6 +167,16 @@ cudaError_t launch_chunk_fwd_split(const ChunkArgs &a, int32_t K, unsigned char 
     }
   }
   return cudaSuccess;
+}
+
+cudaError_t launch_state_combine(const float *init, const float *B, const float *M,
+                                 int32_t n_seqs, int32_t K, int32_t H, float *start, float *end,
+                                 cudaStream_t stream) {
+  if (n_seqs == 0 || H == 0) return cudaSuccess;
+  if ((int64_t)n_seqs * H > 0x7fffffffLL) return cudaErrorInvalidValue;
+  kda_split_combine_kernel<<<dim3((unsigned)(n_seqs * H), D / kCols), 256, 0, stream>>>(
+      init, B, M, n_seqs, K, H, start, end);
+  return cudaGetLastError();
 }
 
 }  // namespace kda

@@ -100,6 +100,12 @@ cudaError_t launch_chunk_fwd_bf16_tc(const ChunkArgs &a, cudaStream_t stream);
 // In-device split of every sequence into K segments (K >= 2; bf16): scratch of
 // split_workspace_bytes() at `ws` (1024-byte aligned); a.help_ws is ignored.
 size_t split_workspace_bytes(int32_t n_seqs, int32_t H, int32_t K);
+// Composition of affine state maps: for each (sequence s, head), S_0 = init
+// (zeros if NULL), S_{j+1} = M[s K + j] S_j + B[s K + j]; start[s K + j] = S_j
+// for j < K and end[s] = S_K, each when non-null.  States [., H, 128, 128] fp32.
+cudaError_t launch_state_combine(const float *init, const float *B, const float *M,
+                                 int32_t n_seqs, int32_t K, int32_t H, float *start, float *end,
+                                 cudaStream_t stream);
 cudaError_t launch_chunk_fwd_split(const ChunkArgs &a, int32_t K, unsigned char *ws,
                                    cudaStream_t stream);
 

@@ -30,7 +30,7 @@ HEAD_DIM = 128
 EXPORTED = ("kda_status_string", "kda_version", "kda_chunk_fwd_workspace_size",
             "kda_chunk_fwd", "kda_read_device_status", "kda_decode_step",
             "kda_chunk_fwd_noalloc", "kda_decode_replay", "kda_prep_fwd", "kda_post_fwd",
-            "kda_read_chunk_stats")
+            "kda_read_chunk_stats", "kda_chunk_fwd_transitions", "kda_state_combine")
 
 _lib = None
 
@@ -68,6 +68,11 @@ def library() -> ctypes.CDLL:
         lib.kda_read_device_status.argtypes = [vp, vp, ctypes.c_int, ctypes.POINTER(i32)]
         lib.kda_read_chunk_stats.restype = ctypes.c_int
         lib.kda_read_chunk_stats.argtypes = [vp, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+        lib.kda_chunk_fwd_transitions.restype = ctypes.c_int
+        lib.kda_chunk_fwd_transitions.argtypes = [vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32,
+                                                  ctypes.c_int, vp, vp, vp, sz, vp]
+        lib.kda_state_combine.restype = ctypes.c_int
+        lib.kda_state_combine.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
         lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
         lib.kda_chunk_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32,
                                               ctypes.c_int, vp, vp, vp]
@@ -181,6 +186,62 @@ def kda_chunk_fwd(q, k, v, log_alpha, beta, init_state=None, cu_seqlens=None, *,
                                  _stream_handle(stream))
     _check(rc, "kda_chunk_fwd")
     return out, final_state
+
+
+def kda_chunk_fwd_transitions(q, k, v, log_alpha, beta, cu_seqlens=None, *, workspace=None,
+                              stream=None):
+    """The affine state map of every packed sequence (bf16): returns
+    ``(state_b, state_m)``, each ``[n_seqs, H, 128, 128]`` fp32, with the
+    sequence mapping a start state S to ``state_m @ S + state_b``."""
+    _need_cuda("q", q)
+    N, H, dk = q.shape
+    dt = q.dtype
+    _need_cuda("k", k, dt, (N, H, dk))
+    _need_cuda("v", v, dt, (N, H, dk))
+    _need_cuda("log_alpha", log_alpha, torch.float32, (N, H, dk))
+    _need_cuda("beta", beta, torch.float32, (N, H))
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, N], dtype=torch.int32, device=q.device)
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_contiguous():
+        raise TypeError("cu_seqlens must be a contiguous 1-D int32 tensor")
+    n_seqs = cu_seqlens.shape[0] - 1
+    b = torch.empty(n_seqs, H, dk, dk, dtype=torch.float32, device=q.device)
+    m = torch.empty_like(b)
+    code = _dtype_code(q)
+    if workspace is None:
+        workspace = torch.empty(kda_chunk_fwd_workspace_size(n_seqs, N, H, dk, dk, code),
+                                dtype=torch.uint8, device=q.device)
+    _need_cuda("workspace", workspace)
+    rc = library().kda_chunk_fwd_transitions(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(cu_seqlens), n_seqs, N, H,
+        dk, dk, code, _ptr(b), _ptr(m), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(rc, "kda_chunk_fwd_transitions")
+    return b, m
+
+
+def kda_state_combine(state_b, state_m, n_segments: int, init_state=None, *, starts=True,
+                      end=True, stream=None):
+    """Composes per-segment affine state maps: ``state_b``, ``state_m`` are
+    ``[n_seqs * n_segments, H, 128, 128]`` (segment j of sequence s at index
+    ``s * n_segments + j``).  Returns ``(start_states, end_state)``: the state
+    each segment starts from, and each sequence's composed final state (either
+    None if not requested)."""
+    _need_cuda("state_b", state_b, torch.float32)
+    n_tot, H, dk, dv = state_b.shape
+    _need_cuda("state_m", state_m, torch.float32, (n_tot, H, dk, dv))
+    if n_segments < 1 or n_tot % n_segments:
+        raise ValueError("the number of pairs must be a multiple of n_segments")
+    n_seqs = n_tot // n_segments
+    if init_state is not None:
+        _need_cuda("init_state", init_state, torch.float32, (n_seqs, H, dk, dv))
+    st = torch.empty_like(state_b) if starts else None
+    en = torch.empty(n_seqs, H, dk, dv, dtype=torch.float32, device=state_b.device) if end else None
+    _check(library().kda_state_combine(_ptr(init_state), _ptr(state_b), _ptr(state_m), n_seqs,
+                                       n_segments, H, dk, dv, _ptr(st), _ptr(en),
+                                       _stream_handle(stream)),
+           "kda_state_combine")
+    return st, en
 
 
 def kda_chunk_fwd_noalloc(q, k, v, log_alpha, beta, init_state=None, cu_seqlens=None, *,

@@ -181,6 +181,45 @@ int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const flo
 int kda_read_device_status(void *workspace, void *stream, int clear, int32_t *device_status);
 
 /*
+ * The affine state map of every packed sequence, for context parallelism
+ * ("Kimi K3: 架构、训练与系统全景解析", section 7.1: a sequence segment maps the
+ * state it starts from to the one it ends with as S_end = M S_start + B, its
+ * "affine pair"; pairs of consecutive segments compose, so devices holding
+ * different segments of one sequence exchange their pairs once and each then
+ * runs its segment from its true start state).  For sequence s and head h:
+ *   state_b[s, h] = B = the final state of kda_chunk_fwd from a zero state,
+ *   state_m[s, h] = M = the product of the sequence's transitions
+ *                       (I - beta_t k_t k_t^T) Diag(alpha_t), latest on the left,
+ * computed in one launch (the chunk kernel run from 0, and from I with v = 0)
+ * that writes no outputs.
+ * Arguments as for kda_chunk_fwd; state_b, state_m [S, H, 128, 128] fp32,
+ * 16-byte aligned, not overlapping.
+ * Errors: as kda_chunk_fwd; KDA_ERR_UNSUPPORTED for fp32 inputs (bf16 only).
+ */
+int kda_chunk_fwd_transitions(const void *q, const void *k, const void *v,
+                              const float *log_alpha, const float *beta,
+                              const int32_t *cu_seqlens, int32_t n_seqs, int64_t n_tokens,
+                              int32_t H, int32_t dk, int32_t dv, int dtype, float *state_b,
+                              float *state_m, void *workspace, size_t workspace_bytes,
+                              void *stream);
+
+/*
+ * Composition of affine state maps (same section).  For every sequence s, head
+ * h, with the sequence's n_segments pairs (B_j, M_j) at index s * n_segments + j:
+ *   S_0 = init_state[s, h] (zeros if init_state is NULL),
+ *   S_{j+1} = M_j S_j + B_j          (fp32, DEVICE memory throughout)
+ *   start_states[s * n_segments + j, h] = S_j  (j < n_segments; if non-NULL)
+ *   end_state[s, h] = S_{n_segments}           (if non-NULL)
+ * State tensors are [., H, 128, 128] fp32, 16-byte aligned; outputs may not
+ * overlap inputs or each other.
+ * Errors: KDA_ERR_INVALID_ARG (NULL state_b/state_m, n_segments < 1, H <= 0,
+ * misalignment, overlap), KDA_ERR_UNSUPPORTED (dk or dv != 128), KDA_ERR_CUDA.
+ */
+int kda_state_combine(const float *init_state, const float *state_b, const float *state_m,
+                      int32_t n_seqs, int32_t n_segments, int32_t H, int32_t dk, int32_t dv,
+                      float *start_states, float *end_state, void *stream);
+
+/*
  * Helper activity of the last kda_chunk_fwd call that used `workspace`:
  * *help_published = chunk packages the helper CTAs wrote, *help_consumed = the
  * ones a chain CTA used instead of computing the chunk itself (both 0 when no

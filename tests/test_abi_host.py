@@ -35,7 +35,7 @@ def test_header_declares_expected_entry_points():
     for n in ("kda_chunk_fwd", "kda_decode_step", "kda_decode_replay", "kda_prep_fwd",
               "kda_post_fwd", "kda_chunk_fwd_workspace_size",
               "kda_status_string", "kda_read_device_status", "kda_read_chunk_stats",
-              "kda_version"):
+              "kda_chunk_fwd_transitions", "kda_state_combine", "kda_version"):
         assert n in names
 
 
@@ -195,6 +195,60 @@ def test_read_device_status_null(lib):
     st = ctypes.c_int32(0)
     assert lib.kda_read_device_status(None, None, 0, ctypes.byref(st)) == 1
     assert lib.kda_read_device_status(ctypes.c_void_p(A), None, 0, None) == 1
+
+
+def _transitions(lib, **over):
+    args = dict(q=A, k=A + 0x1000, v=A + 0x2000, la=A + 0x3000, beta=A + 0x4000, cu=A + 0x5000,
+                n_seqs=2, n_tokens=100, H=4, dk=128, dv=128, dtype=1, b=A + 0x100000,
+                m=A + 0x300000, ws=A + 0x7000, ws_bytes=1 << 20, stream=None)
+    args.update(over)
+    vp = ctypes.c_void_p
+    return lib.kda_chunk_fwd_transitions(
+        vp(args["q"]), vp(args["k"]), vp(args["v"]), vp(args["la"]), vp(args["beta"]),
+        vp(args["cu"]), args["n_seqs"], args["n_tokens"], args["H"], args["dk"], args["dv"],
+        args["dtype"], vp(args["b"]), vp(args["m"]), vp(args["ws"]), args["ws_bytes"],
+        vp(args["stream"]))
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(dtype=0), 2),              # fp32 inputs: bf16 only
+    (dict(dk=64), 2),
+    (dict(b=None), 1), (dict(m=None), 1), (dict(cu=None), 1),
+    (dict(H=0), 1), (dict(n_seqs=-1), 1),
+    (dict(b=A + 0x100008), 1),       # misaligned state
+    (dict(m=A + 0x100000), 1),       # B and M overlap
+    (dict(ws=None), 3), (dict(ws_bytes=16), 3),
+])
+def test_transitions_reject_before_launch(lib, over, code):
+    assert _transitions(lib, **over) == code
+
+
+def _combine(lib, **over):
+    one = 4 * 128 * 128 * 4  # H = 4 states of one sequence
+    args = dict(init=A, b=A + 0x1000000, m=A + 0x2000000, n_seqs=2, K=3, H=4, dk=128, dv=128,
+                starts=A + 0x3000000, end=A + 0x4000000, stream=None)
+    args.update(over)
+    vp = ctypes.c_void_p
+    return lib.kda_state_combine(vp(args["init"]), vp(args["b"]), vp(args["m"]), args["n_seqs"],
+                                 args["K"], args["H"], args["dk"], args["dv"],
+                                 vp(args["starts"]), vp(args["end"]), vp(args["stream"]))
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(K=0), 1), (dict(H=0), 1), (dict(n_seqs=-1), 1),
+    (dict(b=None), 1), (dict(m=None), 1), (dict(dk=64), 2),
+    (dict(end=A + 0x4000004), 1),               # misaligned
+    (dict(starts=A + 0x1000000), 1),            # starts overlap B
+    (dict(end=A + 0x2000000 + 65536), 1),       # end overlaps M
+    (dict(end=A + 0x3000000), 1),               # end overlaps starts
+    (dict(init=A + 0x4000000), 1),              # end overlaps init
+])
+def test_state_combine_rejects_before_launch(lib, over, code):
+    assert _combine(lib, **over) == code
+
+
+def test_empty_combine_launches_nothing(lib):
+    assert _combine(lib, n_seqs=0) == 0
 
 
 def test_read_chunk_stats_null(lib):
