@@ -244,6 +244,70 @@ def kda_state_combine(state_b, state_m, n_segments: int, init_state=None, *, sta
     return st, en
 
 
+def kda_chunk_fwd_host(q, k, v, log_alpha, beta, init_state=None, *, out=None,
+                       final_state=None, piece_tokens: int = 4096, device=None):
+    """Prefill of ONE sequence whose inputs are in host memory (pinned for the
+    copies to overlap): the tokens go through in pieces of ``piece_tokens`` (a
+    multiple of the 64-token chunk), each piece's host-to-device copy overlapping
+    the previous piece's prefill and the device-to-host copy of its outputs.
+    Piece i starts from piece i-1's final state (fp32, exact), so the results
+    are those of one kda_chunk_fwd call.  Returns host ``(out, final_state)``."""
+    if piece_tokens <= 0 or piece_tokens % 64:
+        raise ValueError("piece_tokens must be a positive multiple of 64")
+    device = torch.device(device or "cuda")
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    if out is None:
+        out = torch.empty(N, H, dv, dtype=q.dtype).pin_memory()
+    if final_state is None:
+        final_state = torch.empty(1, H, dk, dv, dtype=torch.float32).pin_memory()
+    if N == 0:
+        final_state.copy_(init_state if init_state is not None else torch.zeros_like(final_state))
+        return out, final_state
+    names = ("q", "k", "v", "log_alpha", "beta")
+    host = dict(zip(names, (q, k, v, log_alpha, beta)))
+    dev = {n: torch.empty(t.shape, dtype=t.dtype, device=device) for n, t in host.items()}
+    d_out = torch.empty(N, H, dv, dtype=q.dtype, device=device)
+    states = [torch.empty(1, H, dk, dv, dtype=torch.float32, device=device) for _ in range(2)]
+    s0 = init_state.to(device, non_blocking=True) if init_state is not None else None
+    compute = torch.cuda.current_stream(device)
+    copy_in, copy_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ws = torch.empty(kda_chunk_fwd_workspace_size(1, piece_tokens, H, dk, dv, _dtype_code(q)),
+                     dtype=torch.uint8, device=device)
+    cu = {}
+    bounds = list(range(0, N, piece_tokens)) + [N]
+    copied = []
+    copy_in.wait_stream(compute)  # the device buffers are free
+    for p0, p1 in zip(bounds[:-1], bounds[1:]):
+        with torch.cuda.stream(copy_in):
+            for n in names:
+                dev[n][p0:p1].copy_(host[n][p0:p1], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(copy_in)
+        copied.append(ev)
+    done = []
+    for i, (p0, p1) in enumerate(zip(bounds[:-1], bounds[1:])):
+        compute.wait_event(copied[i])
+        n_tok = p1 - p0
+        if n_tok not in cu:
+            cu[n_tok] = torch.tensor([0, n_tok], dtype=torch.int32, device=device)
+        last = p1 == N
+        kda_chunk_fwd(dev["q"][p0:p1], dev["k"][p0:p1], dev["v"][p0:p1],
+                      dev["log_alpha"][p0:p1], dev["beta"][p0:p1],
+                      s0 if i == 0 else states[(i - 1) & 1], cu[n_tok], out=d_out[p0:p1],
+                      final_state=states[i & 1], workspace=ws)
+        ev = torch.cuda.Event()
+        ev.record(compute)
+        done.append(ev)
+        with torch.cuda.stream(copy_out):
+            copy_out.wait_event(ev)
+            out[p0:p1].copy_(d_out[p0:p1], non_blocking=True)
+            if last:
+                final_state.copy_(states[i & 1], non_blocking=True)
+    compute.wait_stream(copy_out)
+    return out, final_state
+
+
 def kda_chunk_fwd_noalloc(q, k, v, log_alpha, beta, init_state=None, cu_seqlens=None, *,
                           out=None, final_state=None, output_final_state=True, stream=None):
     """kda_chunk_fwd without a workspace: the library's fixed device scratch is
