@@ -89,11 +89,16 @@ size_t help_workspace_bytes(int64_t chains) {
   return kda::help_header_bytes(chains) + (size_t)chains * kda::kHelpSlots * kda::kHelpSlotStride;
 }
 
-// Full workspace: the base part, then the scratch of the in-device split, or
-// (when helpers would run instead) the helper header and ring.
+// The sequence order of a bf16 prefill of several sequences (longest first).
+size_t order_bytes(int32_t n_seqs, int dtype) {
+  return (dtype == KDA_BF16 && n_seqs > 1) ? round_up(sizeof(int32_t) * (size_t)n_seqs, 1024) : 0;
+}
+
+// Full workspace: the base part, the sequence order, then the scratch of the
+// in-device split, or (when helpers would run instead) the helper header and ring.
 size_t workspace_bytes_for(int32_t n_seqs, int64_t n_tokens, int32_t H, int dtype) {
   const int64_t chains = (int64_t)n_seqs * H;
-  size_t b = base_workspace_bytes(n_seqs);
+  size_t b = base_workspace_bytes(n_seqs) + order_bytes(n_seqs, dtype);
   const int32_t n_split = split_factor(n_seqs, n_tokens, H, dtype);
   if (n_split > 0)
     b += kda::split_workspace_bytes(n_seqs, H, n_split);
@@ -164,7 +169,7 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
   if (init_state && final_state && state_bytes > 0 &&
       ranges_overlap(init_state, state_bytes, final_state, state_bytes))
     return KDA_ERR_INVALID_ARG;
-  const size_t need = base_workspace_bytes(n_seqs);
+  size_t need = base_workspace_bytes(n_seqs);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return KDA_ERR_WORKSPACE;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -200,6 +205,12 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
   a.help_ws = nullptr;
   a.n_help = 0;
   const int64_t chains = (int64_t)n_seqs * H;
+  // Longest sequences first, when the workspace has room for their order.
+  const size_t ob = order_bytes(n_seqs, dtype);
+  if (ob > 0 && workspace_bytes >= need + ob) {
+    a.seq_order = reinterpret_cast<int32_t *>(ws + need);
+    need += ob;
+  }
   // The in-device split, when it applies and the workspace has its scratch.
   const int32_t n_split = split_factor(n_seqs, n_tokens, H, dtype);
   if (n_split > 0 && workspace_bytes >= need + kda::split_workspace_bytes(n_seqs, H, n_split)) {

@@ -277,7 +277,8 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const int32_t *__restrict__ cu_seqlens, int32_t n_seqs, int64_t n_tokens,
                         int32_t H, __nv_bfloat16 *__restrict__ out,
                         float *__restrict__ final_state, DeviceStatus *status,
-                        const HelpRing help, float *__restrict__ final_state_m) {
+                        const HelpRing help, float *__restrict__ final_state_m,
+                        const int32_t *__restrict__ seq_order) {
   // Indexing the __shared__ array directly (no integer round trip) keeps every
   // access a shared-memory instruction.  The 128-byte swizzle atoms need a
   // 1024-byte aligned base, checked below.
@@ -286,11 +287,14 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // transition run of chain blockIdx.x - gridDim.x / 2 (first pass of a split)
   const bool transition = kMode == kModeTransitions && blockIdx.x >= gridDim.x / 2;
-  const int chain = transition ? (int)(blockIdx.x - gridDim.x / 2) : (int)blockIdx.x;
+  const int slot = transition ? (int)(blockIdx.x - gridDim.x / 2) : (int)blockIdx.x;
   // Blocks past the chains are helpers (only when the call has a helper ring).
   const bool helping = kMode == kModeHelp && help.ring != nullptr;
-  const bool helper = helping && chain >= help.n_chains;
-  const int seq = chain / H, h = chain % H;
+  const bool helper = helping && slot >= help.n_chains;
+  // With seq_order, block slots take the sequences longest first (every head of
+  // a sequence in turn), so the longest chains do not start last.
+  const int seq = (seq_order && !helper) ? seq_order[slot / H] : slot / H, h = slot % H;
+  const int chain = helper ? slot : seq * H + h;
   const Ctx cx{smem, &m, status, chain};
   const uint32_t sb = smem_u32(smem);
   // A chain CTA that stops early tells the helpers to leave its chunks alone.
@@ -1269,6 +1273,22 @@ bool make_map(CUtensorMap *map, const void *base, CUtensorMapDataType dt, uint32
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// order[r] = the sequence of rank r by length, longest first (ties by index).
+// Lengths come from a device cu_seqlens that may be malformed: the ranks are a
+// permutation of 0 .. n_seqs - 1 whatever the values.
+__global__ void kda_seq_order_kernel(const int32_t *__restrict__ cu, int32_t n_seqs,
+                                     int32_t *__restrict__ order) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= n_seqs) return;
+  const int64_t len = (int64_t)cu[s + 1] - cu[s];
+  int rank = 0;
+  for (int t = 0; t < n_seqs; ++t) {
+    const int64_t lt = (int64_t)cu[t + 1] - cu[t];
+    rank += (lt > len || (lt == len && t < s)) ? 1 : 0;
+  }
+  order[rank] = s;
+}
+
 }  // namespace
 
 #ifdef KDA_PHASE_PROFILE
@@ -1324,11 +1344,21 @@ cudaError_t launch_chunk_fwd_bf16_tc(const ChunkArgs &a, cudaStream_t stream) {
   e = cudaFuncGetAttributes(&fa, kernel);
   if (e != cudaSuccess) return e;
   if ((uint32_t)fa.numRegs < kLaunchRegs) return cudaErrorNotSupported;
+  // longest sequences first (plain launches of more than one sequence)
+  const int32_t *seq_order = nullptr;
+  if (a.seq_order && a.n_seqs > 1 && !transitions && n_help == 0) {
+    kda_seq_order_kernel<<<(a.n_seqs + 255) / 256, 256, 0, stream>>>(a.cu_seqlens, a.n_seqs,
+                                                                     a.seq_order);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    seq_order = a.seq_order;
+  }
   const int64_t blocks = transitions ? 2 * chains : chains + n_help;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   kernel<<<(unsigned)blocks, kThreads, SMEM_BYTES, stream>>>(
       mq, mk, mv, mla, mo, a.beta, a.init_state, a.cu_seqlens, a.n_seqs, a.n_tokens, a.H,
-      static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.status, help, a.final_state_m);
+      static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.status, help, a.final_state_m,
+      seq_order);
   return cudaGetLastError();
 }
 

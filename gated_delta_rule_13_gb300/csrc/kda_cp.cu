@@ -134,6 +134,7 @@ cudaError_t launch_chunk_fwd_split(const ChunkArgs &a, int32_t K, unsigned char 
   if (e != cudaSuccess) return e;
 
   ChunkArgs p = a;  // pass 1: every segment's B and M
+  p.seq_order = nullptr;  // sized for the sequences, not the segments
   p.cu_seqlens = seg_cu;
   p.n_seqs = (int32_t)nseg;
   p.init_state = nullptr;

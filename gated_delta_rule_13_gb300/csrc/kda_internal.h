@@ -72,6 +72,9 @@ struct ChunkArgs {
   enum Mode { kPlain = 0, kTransitions = 2 };
   int32_t mode = kPlain;
   float *final_state_m = nullptr;
+  // Scratch of n_seqs int32 (or nullptr): the bf16 prefill then runs the
+  // sequences longest first.
+  int32_t *seq_order = nullptr;
 };
 
 cudaError_t launch_decode_step(float *state, const void *q, const void *k, const void *v,
