@@ -101,7 +101,7 @@ size_t workspace_bytes_for(int32_t n_seqs, int64_t n_tokens, int32_t H, int dtyp
   size_t b = base_workspace_bytes(n_seqs) + order_bytes(n_seqs, dtype);
   const int32_t n_split = split_factor(n_seqs, n_tokens, H, dtype);
   if (n_split > 0)
-    b += kda::split_workspace_bytes(n_seqs, H, n_split);
+    b += kda::split_workspace_bytes(n_seqs, n_tokens, H, n_split);
   else if (help_ctas(chains, dtype) > 0)
     b += help_workspace_bytes(chains);
   return b;
@@ -213,7 +213,7 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
   }
   // The in-device split, when it applies and the workspace has its scratch.
   const int32_t n_split = split_factor(n_seqs, n_tokens, H, dtype);
-  if (n_split > 0 && workspace_bytes >= need + kda::split_workspace_bytes(n_seqs, H, n_split)) {
+  if (n_split > 0 && workspace_bytes >= need + kda::split_workspace_bytes(n_seqs, n_tokens, H, n_split)) {
     const cudaError_t e = kda::launch_chunk_fwd_split(a, n_split, ws + need, st);
     if (e == cudaErrorNotSupported) return KDA_ERR_UNSUPPORTED;
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
@@ -307,6 +307,7 @@ int kda_chunk_fwd_transitions(const void *q, const void *k, const void *v,
   a.help_ws = nullptr; a.n_help = 0;
   a.mode = kda::ChunkArgs::kTransitions;
   a.final_state_m = state_m;
+  a.write_out = false;
   const cudaError_t e = kda::launch_chunk_fwd_bf16_tc(a, st);
   if (e == cudaErrorNotSupported) return KDA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;

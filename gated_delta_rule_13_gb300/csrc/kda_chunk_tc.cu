@@ -278,7 +278,9 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         int32_t H, __nv_bfloat16 *__restrict__ out,
                         float *__restrict__ final_state, DeviceStatus *status,
                         const HelpRing help, float *__restrict__ final_state_m,
-                        const int32_t *__restrict__ seq_order) {
+                        const int32_t *__restrict__ seq_order,
+                        const __grid_constant__ CUtensorMap tm_om,
+                        __nv_bfloat16 *__restrict__ out_m, const int write_out) {
   // Indexing the __shared__ array directly (no integer round trip) keeps every
   // access a shared-memory instruction.  The 128-byte swizzle atoms need a
   // 1024-byte aligned base, checked below.
@@ -674,7 +676,11 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     // rows [r][n] staged in an idle Kdec buffer -> one TMA store of the whole
     // 64 x 128 tile (issued by thread 128, which later waits for its read), or,
     // for a sequence's ragged last chunk, 16-byte stores of the valid rows.
+    // (a transition run writes its outputs, M_t^T q_t, to out_m)
     auto flush_output = [&](int64_t otb, int onv, uint32_t ocol, uint32_t stg_off) {
+      if (kMode == kModeTransitions && !write_out) return;  // warp-uniform (warps 4-7)
+      const CUtensorMap *omap = transition ? &tm_om : &tm_o;
+      __nv_bfloat16 *optr = transition ? out_m : out;
       const int n = lane_base + lane;
       const uint32_t stg = sb + stg_off;
 #pragma unroll
@@ -693,13 +699,13 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       named_sync(3, 128);
       if (onv == C) {
         if (tid == 128) {
-          tma_store_3d(&tm_o, smem + stg_off, 0, h, (int32_t)otb);
+          tma_store_3d(omap, smem + stg_off, 0, h, (int32_t)otb);
           bulk_commit();
         }
       } else {
         for (int e = tid - 128; e < onv * 16; e += 128) {   // row e / 16, 16-byte chunk e % 16
           const int row = e >> 4, ch = e & 15;
-          *reinterpret_cast<uint4 *>(out + ((otb + row) * H + h) * D + 8 * ch) =
+          *reinterpret_cast<uint4 *>(optr + ((otb + row) * H + h) * D + 8 * ch) =
               ld_shared_v4(stg + (uint32_t)row * 256u + 16u * ch);
         }
       }
@@ -1096,7 +1102,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         // channel n).  Staging: the Kdec buffer of chunks ci - 1 and ci + 1, idle
         // until the next build.
         PHASE_MARK_W4(0);
-        if (kMode != kModeTransitions && ci > 0)
+        if (ci > 0)
           flush_output(prev_tb, prev_nv, TM_O + 64u * (par ^ 1u), SM_KDEC + 16384u * (par ^ 1u));
         PHASE_MARK_W4(1);
         wait_bar(cx, &m.bar_m1, par, 24, ci);
@@ -1204,7 +1210,6 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       wait_bar(cx, &m.bar_m2, (uint32_t)((n_chunks - 1) & 1), 26, n_chunks - 1);
       tc_fence_after();
       if (warp >= 4) {
-        if (kMode != kModeTransitions)
           flush_output(prev_tb, prev_nv, TM_O + 64u * (uint32_t)((n_chunks - 1) & 1), SM_KDEC);
         if (tid == 128) bulk_wait_all();
       }
@@ -1302,9 +1307,10 @@ cudaError_t launch_chunk_fwd_bf16_tc(const ChunkArgs &a, cudaStream_t stream) {
   if (chains == 0) return cudaSuccess;
   if (chains > 0x7fffffffLL || a.n_tokens > 0x7fffffffLL - C) return cudaErrorInvalidValue;
   if (!encode_fn()) return cudaErrorNotSupported;
-  CUtensorMap mq, mk, mv, mla, mo;
+  CUtensorMap mq, mk, mv, mla, mo, mom;
   memset(&mq, 0, sizeof(mq)); memset(&mk, 0, sizeof(mk));
   memset(&mv, 0, sizeof(mv)); memset(&mla, 0, sizeof(mla)); memset(&mo, 0, sizeof(mo));
+  memset(&mom, 0, sizeof(mom));
   if (a.n_tokens > 0) {
     const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     if (!make_map(&mq, a.q, bf, 2, a.n_tokens, a.H, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -1312,7 +1318,9 @@ cudaError_t launch_chunk_fwd_bf16_tc(const ChunkArgs &a, cudaStream_t stream) {
         !make_map(&mv, a.v, bf, 2, a.n_tokens, a.H, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map(&mla, a.log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.n_tokens, a.H, 128,
                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map(&mo, a.out, bf, 2, a.n_tokens, a.H, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+        !make_map(&mo, a.out, bf, 2, a.n_tokens, a.H, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        (a.out_m && !make_map(&mom, a.out_m, bf, 2, a.n_tokens, a.H, 128,
+                              CU_TENSOR_MAP_SWIZZLE_NONE)))
       return cudaErrorInvalidValue;
   }
   HelpRing help;
@@ -1358,7 +1366,9 @@ cudaError_t launch_chunk_fwd_bf16_tc(const ChunkArgs &a, cudaStream_t stream) {
   kernel<<<(unsigned)blocks, kThreads, SMEM_BYTES, stream>>>(
       mq, mk, mv, mla, mo, a.beta, a.init_state, a.cu_seqlens, a.n_seqs, a.n_tokens, a.H,
       static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.status, help, a.final_state_m,
-      seq_order);
+      seq_order, transitions && a.out_m ? mom : mo,
+      static_cast<__nv_bfloat16 *>(transitions && a.out_m ? a.out_m : a.out),
+      transitions ? (a.write_out ? 1 : 0) : 1);
   return cudaGetLastError();
 }
 

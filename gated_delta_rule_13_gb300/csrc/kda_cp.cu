@@ -6,24 +6,29 @@
 // S_end = M S_start + B, and such maps compose; the pages use this for context
 // parallelism across devices, and within one device to fill its SMs).
 //
-//   pass 1  one launch, 2 K chains per original chain, no outputs written:
-//           segment j from S = 0          -> B_j (final state)
+//   pass 1  one launch, 2 K chains per original chain:
+//           segment j from S = 0          -> B_j (final state), o0_t (outputs)
 //           segment j from S = I, v = 0   -> M_j (final state = the product of
-//                                            the segment's transitions)
-//   combine S_0 = init,  S_{j+1} = M_j S_j + B_j            (fp32, per head)
-//   pass 2  the plain kernel over all segments from S_j: outputs and final
-//           states; the last segment's final state is the sequence's.
+//                                            the segment's transitions) and
+//                                            q_eff_t = M_t^T q_t (outputs)
+//   combine S_0 = init,  S_{j+1} = M_j S_j + B_j            (fp32, per head);
+//           S_K is the sequence's final state
+//   correct o_t = o0_t + S_j^T q_eff_t   (S_t = M_t S_j + B_t, so
+//           o_t = S_t^T q_t = o0_t + S_j^T M_t^T q_t)
 //
-// Pass 1 runs 2 K x chains CTAs in one wave, pass 2 K x chains, so the wall
-// time is about 2 T / K chunk-steps instead of T.
+// Pass 1 runs 2 K x chains CTAs in one wave, so the wall time is about T / K
+// chunk-steps instead of T, plus the combine and the correction.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "kda_internal.h"
+#include "kda_sm100.cuh"
 
 namespace kda {
 namespace {
 
+using namespace sm100;
 constexpr int D = kHeadDim;
 constexpr int C = kChunk;
 
@@ -111,63 +116,144 @@ kda_split_combine_kernel(const float *__restrict__ init, const float *__restrict
   }
 }
 
+// out[t, h] += S_jᵀ q_eff[t, h] for the tokens t of segment j: the correction
+// that turns the zero-start outputs o⁰_t into the true ones,
+// o_t = o⁰_t + (M_t S_j)ᵀ q_t with q_eff = M_tᵀ q_t.  One CTA per (segment,
+// 64-token tile, head): block x = j * tiles + tile (tiles: a bound on any
+// segment's tile count; CTAs past their segment's end return).  Warp MMAs with
+// bf16 operands (S_j rounded like the state operands of the prefill), fp32
+// accumulation; `skip_first` leaves segment 0 of every sequence alone (its
+// start state is zero).
+constexpr int kCorrTile = 64;
+constexpr int kSbPitch = D + 8;   // u32 per row of the bf16 pairs of S_j: bank-conflict free
+constexpr int kQsPitch = D + 8;   // bf16 per row of the q_eff tile
+__global__ void __launch_bounds__(256, 2)
+kda_split_correct_kernel(__nv_bfloat16 *__restrict__ out, const __nv_bfloat16 *__restrict__ qe,
+                         const float *__restrict__ start, const int32_t *__restrict__ seg_cu,
+                         int64_t n_tokens, int32_t K, int32_t H, int32_t tiles,
+                         int skip_first) {
+  extern __shared__ __align__(16) uint32_t corr_smem[];
+  uint32_t *sb = corr_smem;                                              // [64 k-pairs][kSbPitch]
+  __nv_bfloat16 *qs = reinterpret_cast<__nv_bfloat16 *>(corr_smem + (D / 2) * kSbPitch);  // [64][kQsPitch]
+  const int seg = blockIdx.x / tiles, h = blockIdx.y;
+  if (skip_first && seg % K == 0) return;
+  const int64_t s0 = seg_cu[seg], s1 = seg_cu[seg + 1];
+  const int64_t tb = s0 + (int64_t)kCorrTile * (blockIdx.x % tiles);
+  if (s0 < 0 || s1 > n_tokens || tb >= s1) return;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  // S_j as bf16 pairs along k: sb[kp][n] = (S[2 kp][n], S[2 kp + 1][n])
+  const float *S = start + ((int64_t)seg * H + h) * D * D;
+  for (int i = tid; i < (D / 2) * D; i += 256) {
+    const int kp = i / D, n = i % D;
+    const __nv_bfloat162 v = __floats2bfloat162_rn(S[(2 * kp) * D + n], S[(2 * kp + 1) * D + n]);
+    sb[kp * kSbPitch + n] = *reinterpret_cast<const uint32_t *>(&v);
+  }
+  const int mt = warp & 3, nh = warp >> 2;  // 16 tokens x 64 columns per warp
+  {
+    const int rows = (int)(s1 - tb < kCorrTile ? s1 - tb : kCorrTile);
+    for (int i = tid; i < kCorrTile * (D / 8); i += 256) {
+      const int r = i / (D / 8), c8 = i % (D / 8);
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (r < rows) v = *reinterpret_cast<const uint4 *>(qe + ((tb + r) * H + h) * D + 8 * c8);
+      *reinterpret_cast<uint4 *>(qs + r * kQsPitch + 8 * c8) = v;
+    }
+    __syncthreads();
+    float acc[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
+#pragma unroll
+    for (int kt = 0; kt < D / 16; ++kt) {
+      const __nv_bfloat16 *qa = qs + (16 * mt + g) * kQsPitch + 16 * kt + 2 * t4;
+      const uint32_t a0 = *reinterpret_cast<const uint32_t *>(qa);
+      const uint32_t a1 = *reinterpret_cast<const uint32_t *>(qa + 8 * kQsPitch);
+      const uint32_t a2 = *reinterpret_cast<const uint32_t *>(qa + 8);
+      const uint32_t a3 = *reinterpret_cast<const uint32_t *>(qa + 8 * kQsPitch + 8);
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        const int n = 64 * nh + 8 * nt + g;
+        mma_bf16_16x8x16(acc[nt], a0, a1, a2, a3, sb[(8 * kt + t4) * kSbPitch + n],
+                         sb[(8 * kt + 4 + t4) * kSbPitch + n]);
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const int n = 64 * nh + 8 * nt + 2 * t4;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int r = 16 * mt + g + 8 * half;
+        if (r >= rows) continue;
+        __nv_bfloat162 *o = reinterpret_cast<__nv_bfloat162 *>(out + ((tb + r) * H + h) * D + n);
+        const float2 v = __bfloat1622float2(*o);
+        *o = __floats2bfloat162_rn(v.x + acc[nt][2 * half], v.y + acc[nt][2 * half + 1]);
+      }
+    }
+  }
+}
+constexpr size_t kCorrSmem = (size_t)(D / 2) * kSbPitch * 4 + (size_t)kCorrTile * kQsPitch * 2;
+
 }  // namespace
 
-size_t split_workspace_bytes(int32_t n_seqs, int32_t H, int32_t K) {
+size_t split_workspace_bytes(int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t K) {
   const size_t nseg = (size_t)n_seqs * K;
   const size_t cu_bytes = ((nseg + 1) * sizeof(int32_t) + 1023) / 1024 * 1024;
-  return cu_bytes + 3 * nseg * H * (size_t)D * D * sizeof(float);
+  return cu_bytes + 3 * nseg * H * (size_t)D * D * sizeof(float) +
+         (size_t)n_tokens * H * D * sizeof(__nv_bfloat16);
 }
 
 cudaError_t launch_chunk_fwd_split(const ChunkArgs &a, int32_t K, unsigned char *ws,
                                    cudaStream_t stream) {
   const int64_t nseg = (int64_t)a.n_seqs * K;
-  if (K < 2 || nseg > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (K < 2 || nseg > 0x7fffffffLL || nseg * a.H > 0x7fffffffLL) return cudaErrorInvalidValue;
   const size_t cu_bytes = ((size_t)(nseg + 1) * sizeof(int32_t) + 1023) / 1024 * 1024;
   const size_t states = (size_t)nseg * a.H * D * D;
   int32_t *seg_cu = reinterpret_cast<int32_t *>(ws);
   float *B = reinterpret_cast<float *>(ws + cu_bytes), *M = B + states, *S = M + states;
+  __nv_bfloat16 *qe = reinterpret_cast<__nv_bfloat16 *>(S + states);  // [N, H, 128]
 
   kda_split_bounds_kernel<<<(unsigned)((nseg + 1 + 255) / 256), 256, 0, stream>>>(
       a.cu_seqlens, a.n_seqs, K, seg_cu);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  ChunkArgs p = a;  // pass 1: every segment's B and M
-  p.seq_order = nullptr;  // sized for the sequences, not the segments
+  // pass 1: per segment, B and the outputs o0 from a zero state (into out), M and
+  // q_eff = M_t^T q_t from the identity with v = 0 (into qe)
+  ChunkArgs p = a;
   p.cu_seqlens = seg_cu;
   p.n_seqs = (int32_t)nseg;
   p.init_state = nullptr;
   p.final_state = B;
   p.final_state_m = M;
+  p.out_m = qe;
+  p.write_out = true;
   p.mode = ChunkArgs::kTransitions;
   p.help_ws = nullptr;
   p.n_help = 0;
+  p.seq_order = nullptr;  // sized for the sequences, not the segments
   e = launch_chunk_fwd_bf16_tc(p, stream);
   if (e != cudaSuccess) return e;
 
+  // the start state of every segment, and every sequence's final state
   kda_split_combine_kernel<<<dim3((unsigned)(a.n_seqs * a.H), D / kCols), 256, 0, stream>>>(
-      a.init_state, B, M, a.n_seqs, K, a.H, S, nullptr);
+      a.init_state, B, M, a.n_seqs, K, a.H, S, a.final_state);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  p.init_state = S;  // pass 2: the outputs, from each segment's true start state
-  p.final_state = B;
-  p.final_state_m = nullptr;
-  p.mode = ChunkArgs::kPlain;
-  e = launch_chunk_fwd_bf16_tc(p, stream);
+  // o_t = o0_t + S_j^T q_eff_t (segment 0 of a sequence without init state starts from 0)
+  e = cudaFuncSetAttribute(kda_split_correct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kCorrSmem);
   if (e != cudaSuccess) return e;
-
-  if (a.final_state) {  // the last segment's final state is the sequence's
-    const size_t bytes = (size_t)a.H * D * D * sizeof(float);
-    for (int32_t s = 0; s < a.n_seqs; ++s) {
-      e = cudaMemcpyAsync(a.final_state + (size_t)s * a.H * D * D,
-                          B + ((size_t)s * K + K - 1) * a.H * D * D, bytes,
-                          cudaMemcpyDeviceToDevice, stream);
-      if (e != cudaSuccess) return e;
-    }
-  }
-  return cudaSuccess;
+  // no segment is longer than ceil(ceil(N / 64) / K) chunks of 64 tokens
+  const int64_t tiles = ((a.n_tokens + kChunk - 1) / kChunk + K - 1) / K;
+  if (tiles == 0) return cudaSuccess;
+  if (nseg * tiles > 0x7fffffffLL || a.H > 65535) return cudaErrorInvalidValue;
+  kda_split_correct_kernel<<<dim3((unsigned)(nseg * tiles), (unsigned)a.H), 256, kCorrSmem,
+                             stream>>>(static_cast<__nv_bfloat16 *>(a.out), qe, S, seg_cu,
+                                       a.n_tokens, K, a.H, (int32_t)tiles,
+                                       a.init_state == nullptr ? 1 : 0);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_state_combine(const float *init, const float *B, const float *M,

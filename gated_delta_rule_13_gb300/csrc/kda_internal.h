@@ -75,6 +75,12 @@ struct ChunkArgs {
   // Scratch of n_seqs int32 (or nullptr): the bf16 prefill then runs the
   // sequences longest first.
   int32_t *seq_order = nullptr;
+  // kTransitions: the zero-start runs write their outputs to out and the
+  // transition runs theirs (M_t^T q_t) to out_m ([N, H, 128] bf16); with
+  // out_m NULL the transition runs write to out as well.  With write_out false
+  // no output is written at all (out is then only a valid tensor-map base).
+  void *out_m = nullptr;
+  bool write_out = true;
 };
 
 cudaError_t launch_decode_step(float *state, const void *q, const void *k, const void *v,
@@ -102,7 +108,7 @@ cudaError_t launch_chunk_fwd_bf16_tc(const ChunkArgs &a, cudaStream_t stream);
 
 // In-device split of every sequence into K segments (K >= 2; bf16): scratch of
 // split_workspace_bytes() at `ws` (1024-byte aligned); a.help_ws is ignored.
-size_t split_workspace_bytes(int32_t n_seqs, int32_t H, int32_t K);
+size_t split_workspace_bytes(int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t K);
 // Composition of affine state maps: for each (sequence s, head), S_0 = init
 // (zeros if NULL), S_{j+1} = M[s K + j] S_j + B[s K + j]; start[s K + j] = S_j
 // for j < K and end[s] = S_K, each when non-null.  States [., H, 128, 128] fp32.

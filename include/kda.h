@@ -74,10 +74,11 @@ int kda_version(void);
  *   - when cu_seqlens is a host pointer, a device copy of it;
  *   - for a bf16 call with few enough (sequence, head) chains that each
  *     sequence can be cut into K >= 3 segments with 2 K x chains <= SMs, the
- *     scratch of the in-device split (segment bounds and three fp32 states per
- *     segment and head): the segments run side by side and their states are
- *     stitched together exactly ("Kimi K3: 架构、训练与系统全景解析", section
- *     7.1: segments compose as affine maps of the state);
+ *     scratch of the in-device split (segment bounds, three fp32 states per
+ *     segment and head, and one bf16 value per token, head and channel): the
+ *     segments run side by side and their states are stitched together exactly
+ *     ("Kimi K3: 架构、训练与系统全景解析", section 7.1: segments compose as
+ *     affine maps of the state);
  *   - otherwise, for a bf16 call whose chains leave at least three times as
  *     many of the device's SMs idle as there are chains, the ring of the
  *     helper CTAs.

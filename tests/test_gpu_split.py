@@ -64,14 +64,18 @@ def _slow_decay(x, scale):
     return x
 
 
-def test_workload_decay_split_is_exact():
-    """Under the workload's own decay the split reproduces the unsplit results
-    bit for bit (see _slow_decay), while taking the split path."""
+def test_workload_decay_split():
+    """Under the workload's own decay (see _slow_decay) the final states are bit
+    for bit the unsplit ones (every M_j is 0 and B_j the true state), and the
+    outputs differ only where the correction is not zero yet: the first tokens
+    of each segment, before their transition underflows."""
     x = inputs.prefill_inputs([16384], H=8, dtype="bf16", init_state=True, device=DEV, seed=41)
     o1, s1, ws_split = _run(x)
     o0, s0, ws_plain = _run(x, split=False)
     assert ws_split > ws_plain  # the split's scratch was provided
-    assert torch.equal(o0, o1) and torch.equal(s0, s1)
+    assert torch.equal(s0, s1)
+    assert rel_l2(o1, o0) <= 2e-3
+    _parity(x, o1, s1, heads=[3])
 
 
 @pytest.mark.parametrize("scale", [0.0, 0.01])
