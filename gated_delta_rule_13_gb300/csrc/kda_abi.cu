@@ -62,10 +62,11 @@ int32_t help_ctas(int64_t chains, int dtype) {
 }
 
 // Segments per sequence for the in-device split of a bf16 prefill (0: no
-// split).  Its first pass runs 2 K CTAs per chain and both passes take about
-// T / K chunk-steps, so it needs 2 K x chains <= SMs and pays off from K = 3
-// on; segments are kept at two chunks or more on average.  The environment
-// variable KDA_CHUNK_SPLIT caps K (0 turns the split off).
+// split).  Its pass runs 2 K CTAs per chain and takes about T / K chunk-steps
+// (plus a combine and an output correction), so it needs 2 K x chains <= SMs
+// and pays off from K = 2 on; segments are kept at two chunks or more on
+// average.  The environment variable KDA_CHUNK_SPLIT caps K (0 turns the
+// split off).
 int32_t split_factor(int32_t n_seqs, int64_t n_tokens, int32_t H, int dtype) {
   const int64_t chains = (int64_t)n_seqs * H;
   if (dtype != KDA_BF16 || chains <= 0 || n_tokens <= 0) return 0;
@@ -82,7 +83,7 @@ int32_t split_factor(int32_t n_seqs, int64_t n_tokens, int32_t H, int dtype) {
     const long cap = strtol(env, nullptr, 10);
     if (cap >= 0 && cap < k) k = cap;
   }
-  return k >= 3 ? (int32_t)k : 0;
+  return k >= 2 ? (int32_t)k : 0;
 }
 
 size_t help_workspace_bytes(int64_t chains) {
