@@ -21,10 +21,12 @@
 #include <stdint.h>
 
 #include "kda_internal.h"
+#include "kda_sm100.cuh"
 
 namespace kda {
 namespace {
 
+using namespace sm100;
 constexpr int D = kHeadDim;
 constexpr int kThreads = 256;
 
@@ -150,9 +152,15 @@ kda_decode_step_kernel(float *__restrict__ state, const void *__restrict__ q,
 // cached inputs in order, n_b = n_accept[b] clamped to [0, T], keeping the
 // state in registers: one HBM read and one write of the state for all n_b
 // tokens (none at all when n_b = 0).  The inputs of up to kReplayGroup tokens
-// are fetched into shared memory in one cooperative pass, overlapping the
-// state load, so a group of tokens costs one memory latency and one barrier.
+// are fetched into shared memory in one cooperative pass.
+//
+// The CTAs are persistent (two per SM), each walking units with a stride of the
+// grid, and while one unit's tokens run from registers the next unit's state is
+// already being copied into shared memory by one bulk copy: the memory system
+// has the next 64 KB in flight throughout the compute, which a CTA per unit
+// (state load, then compute, then store) leaves idle.
 constexpr int kReplayGroup = 8;
+constexpr uint64_t kReplayWaitNs = 2000000000ull;  // bound on the state copy wait
 
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -160,91 +168,124 @@ kda_decode_replay_kernel(float *__restrict__ state, const void *__restrict__ q,
                          const void *__restrict__ k, const void *__restrict__ v,
                          const float *__restrict__ log_alpha, const float *__restrict__ beta,
                          const int32_t *__restrict__ n_accept, int32_t T, int32_t H,
-                         void *__restrict__ out) {
+                         int64_t units, void *__restrict__ out) {
+  extern __shared__ __align__(128) float stage[];  // the next unit's state, [D][D]
   __shared__ __align__(16) float s_alpha[kReplayGroup][D], s_k[kReplayGroup][D],
       s_q[kReplayGroup][D], s_v[kReplayGroup][D];
   __shared__ float s_beta[kReplayGroup];
-  const int64_t unit = blockIdx.x;  // b * H + h
-  const int64_t b = unit / H, h = unit % H;
-  int n = n_accept[b];
-  n = n < 0 ? 0 : (n > T ? T : n);
-  if (n == 0) return;  // nothing accepted: the state stays as it is
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int64_t s_next;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int col = 16 * warp + 4 * (lane & 3);
   const int row0 = lane >> 2;
-  float *S = state + unit * (int64_t)(D * D);
-
-  float4 s[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j)
-    s[j] = __ldcs(reinterpret_cast<const float4 *>(S + (row0 + 8 * j) * D + col));
-
-  for (int t0 = 0; t0 < n; t0 += kReplayGroup) {
-    const int cnt = n - t0 < kReplayGroup ? n - t0 : kReplayGroup;
-    if (t0 > 0) __syncthreads();  // the previous group's inputs are consumed
-    for (int e = tid; e < cnt * D; e += kThreads) {
-      const int t = e / D, c = e % D;
-      const int64_t iu = (b * T + t0 + t) * H + h;  // (sequence, token, head)
-      s_alpha[t][c] = expf(log_alpha[iu * D + c]);
-      s_k[t][c] = load_elem<BF16>(k, iu * D + c);
-      s_q[t][c] = load_elem<BF16>(q, iu * D + c);
-      s_v[t][c] = load_elem<BF16>(v, iu * D + c);
+  auto accepted = [&](int64_t u) {
+    const int n = n_accept[u / H];
+    return n < 0 ? 0 : (n > T ? T : n);
+  };
+  // thread 0: the next unit with accepted tokens after `u` (stride gridDim.x),
+  // its state copy issued into the stage
+  auto prefetch_from = [&](int64_t u) {
+    while (u < units && accepted(u) == 0) u += gridDim.x;
+    s_next = u;
+    if (u < units) {
+      mbar_arrive_expect_tx(&bar, D * D * sizeof(float));
+      bulk_load(smem_u32(stage), state + u * (int64_t)(D * D), D * D * sizeof(float), &bar);
     }
-    if (tid < cnt) s_beta[tid] = beta[(b * T + t0 + tid) * H + h];
-    __syncthreads();
-
-    for (int t = 0; t < cnt; ++t) {
-      const float *sa = s_alpha[t], *sk = s_k[t], *sq = s_q[t];
-      const float4 vv = *reinterpret_cast<const float4 *>(&s_v[t][col]);
-      const float bt = s_beta[t];
-      float pk0 = 0.f, pk1 = 0.f, pk2 = 0.f, pk3 = 0.f;
-      float pq0 = 0.f, pq1 = 0.f, pq2 = 0.f, pq3 = 0.f;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int r = row0 + 8 * j;
-        const float a = sa[r], kr = sk[r], qr = sq[r];
-        s[j].x *= a; s[j].y *= a; s[j].z *= a; s[j].w *= a;
-        pk0 = fmaf(kr, s[j].x, pk0); pk1 = fmaf(kr, s[j].y, pk1);
-        pk2 = fmaf(kr, s[j].z, pk2); pk3 = fmaf(kr, s[j].w, pk3);
-        pq0 = fmaf(qr, s[j].x, pq0); pq1 = fmaf(qr, s[j].y, pq1);
-        pq2 = fmaf(qr, s[j].z, pq2); pq3 = fmaf(qr, s[j].w, pq3);
-      }
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        pk0 += __shfl_xor_sync(0xffffffffu, pk0, off);
-        pk1 += __shfl_xor_sync(0xffffffffu, pk1, off);
-        pk2 += __shfl_xor_sync(0xffffffffu, pk2, off);
-        pk3 += __shfl_xor_sync(0xffffffffu, pk3, off);
-        pq0 += __shfl_xor_sync(0xffffffffu, pq0, off);
-        pq1 += __shfl_xor_sync(0xffffffffu, pq1, off);
-        pq2 += __shfl_xor_sync(0xffffffffu, pq2, off);
-        pq3 += __shfl_xor_sync(0xffffffffu, pq3, off);
-      }
-      float kq = 0.f;
-#pragma unroll
-      for (int j = 0; j < D / 32; ++j) kq = fmaf(sk[lane + 32 * j], sq[lane + 32 * j], kq);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
-
-      const float u0 = bt * (vv.x - pk0), u1 = bt * (vv.y - pk1);
-      const float u2 = bt * (vv.z - pk2), u3 = bt * (vv.w - pk3);
-      if (out != nullptr && row0 == 0) {
-        const int64_t iu = (b * T + t0 + t) * H + h;
-        store4<BF16>(out, iu * D + col,
-                     make_float4(fmaf(kq, u0, pq0), fmaf(kq, u1, pq1), fmaf(kq, u2, pq2),
-                                 fmaf(kq, u3, pq3)));
-      }
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float kr = sk[row0 + 8 * j];
-        s[j].x = fmaf(kr, u0, s[j].x); s[j].y = fmaf(kr, u1, s[j].y);
-        s[j].z = fmaf(kr, u2, s[j].z); s[j].w = fmaf(kr, u3, s[j].w);
-      }
-    }
+  };
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbarrier_init();
+    prefetch_from(blockIdx.x);
   }
+  __syncthreads();
+  int64_t u = s_next;
+  uint32_t phase = 0;
+  while (u < units) {
+    const bool landed = mbar_wait(&bar, phase, kReplayWaitNs);
+    if (__syncthreads_or(!landed)) {  // a copy that never lands: leave, every thread alike
+      if (tid == 0) mbar_wait(&bar, phase, kReplayWaitNs);  // (bounded) no copy outlives the CTA
+      return;
+    }
+    phase ^= 1u;
+    float4 s[16];
 #pragma unroll
-  for (int j = 0; j < 16; ++j)
-    __stcs(reinterpret_cast<float4 *>(S + (row0 + 8 * j) * D + col), s[j]);
+    for (int j = 0; j < 16; ++j)
+      s[j] = *reinterpret_cast<const float4 *>(stage + (row0 + 8 * j) * D + col);
+    __syncthreads();  // the stage is free for the next unit's state
+    if (tid == 0) prefetch_from(u + gridDim.x);
+
+    const int64_t b = u / H, h = u % H;
+    const int n = accepted(u);
+    float *S = state + u * (int64_t)(D * D);
+    for (int t0 = 0; t0 < n; t0 += kReplayGroup) {
+      const int cnt = n - t0 < kReplayGroup ? n - t0 : kReplayGroup;
+      if (t0 > 0) __syncthreads();  // the previous group's inputs are consumed
+      for (int e = tid; e < cnt * D; e += kThreads) {
+        const int t = e / D, c = e % D;
+        const int64_t iu = (b * T + t0 + t) * H + h;  // (sequence, token, head)
+        s_alpha[t][c] = expf(log_alpha[iu * D + c]);
+        s_k[t][c] = load_elem<BF16>(k, iu * D + c);
+        s_q[t][c] = load_elem<BF16>(q, iu * D + c);
+        s_v[t][c] = load_elem<BF16>(v, iu * D + c);
+      }
+      if (tid < cnt) s_beta[tid] = beta[(b * T + t0 + tid) * H + h];
+      __syncthreads();
+
+      for (int t = 0; t < cnt; ++t) {
+        const float *sa = s_alpha[t], *sk = s_k[t], *sq = s_q[t];
+        const float4 vv = *reinterpret_cast<const float4 *>(&s_v[t][col]);
+        const float bt = s_beta[t];
+        float pk0 = 0.f, pk1 = 0.f, pk2 = 0.f, pk3 = 0.f;
+        float pq0 = 0.f, pq1 = 0.f, pq2 = 0.f, pq3 = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int r = row0 + 8 * j;
+          const float a = sa[r], kr = sk[r], qr = sq[r];
+          s[j].x *= a; s[j].y *= a; s[j].z *= a; s[j].w *= a;
+          pk0 = fmaf(kr, s[j].x, pk0); pk1 = fmaf(kr, s[j].y, pk1);
+          pk2 = fmaf(kr, s[j].z, pk2); pk3 = fmaf(kr, s[j].w, pk3);
+          pq0 = fmaf(qr, s[j].x, pq0); pq1 = fmaf(qr, s[j].y, pq1);
+          pq2 = fmaf(qr, s[j].z, pq2); pq3 = fmaf(qr, s[j].w, pq3);
+        }
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          pk0 += __shfl_xor_sync(0xffffffffu, pk0, off);
+          pk1 += __shfl_xor_sync(0xffffffffu, pk1, off);
+          pk2 += __shfl_xor_sync(0xffffffffu, pk2, off);
+          pk3 += __shfl_xor_sync(0xffffffffu, pk3, off);
+          pq0 += __shfl_xor_sync(0xffffffffu, pq0, off);
+          pq1 += __shfl_xor_sync(0xffffffffu, pq1, off);
+          pq2 += __shfl_xor_sync(0xffffffffu, pq2, off);
+          pq3 += __shfl_xor_sync(0xffffffffu, pq3, off);
+        }
+        float kq = 0.f;
+#pragma unroll
+        for (int j = 0; j < D / 32; ++j) kq = fmaf(sk[lane + 32 * j], sq[lane + 32 * j], kq);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+
+        const float u0 = bt * (vv.x - pk0), u1 = bt * (vv.y - pk1);
+        const float u2 = bt * (vv.z - pk2), u3 = bt * (vv.w - pk3);
+        if (out != nullptr && row0 == 0) {
+          const int64_t iu = (b * T + t0 + t) * H + h;
+          store4<BF16>(out, iu * D + col,
+                       make_float4(fmaf(kq, u0, pq0), fmaf(kq, u1, pq1), fmaf(kq, u2, pq2),
+                                   fmaf(kq, u3, pq3)));
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float kr = sk[row0 + 8 * j];
+          s[j].x = fmaf(kr, u0, s[j].x); s[j].y = fmaf(kr, u1, s[j].y);
+          s[j].z = fmaf(kr, u2, s[j].z); s[j].w = fmaf(kr, u3, s[j].w);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      __stcs(reinterpret_cast<float4 *>(S + (row0 + 8 * j) * D + col), s[j]);
+    __syncthreads();  // s_next is set; the input buffers may be refilled
+    u = s_next;
+  }
 }
 
 }  // namespace
@@ -271,15 +312,17 @@ cudaError_t launch_decode_replay(float *state, const void *q, const void *k, con
                                  bool bf16, void *out, cudaStream_t stream) {
   const int64_t units = (int64_t)B * H;
   if (units == 0) return cudaSuccess;
-  if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
-  const dim3 grid((unsigned)units), block(kThreads);
-  if (bf16) {
-    kda_decode_replay_kernel<true><<<grid, block, 0, stream>>>(state, q, k, v, log_alpha, beta,
-                                                                n_accept, T, H, out);
-  } else {
-    kda_decode_replay_kernel<false><<<grid, block, 0, stream>>>(state, q, k, v, log_alpha, beta,
-                                                                 n_accept, T, H, out);
-  }
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int64_t ctas = units < 2 * (int64_t)sms ? units : 2 * (int64_t)sms;
+  const size_t stage = (size_t)D * D * sizeof(float);
+  auto kern = bf16 ? kda_decode_replay_kernel<true> : kda_decode_replay_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)stage);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)ctas, kThreads, stage, stream>>>(state, q, k, v, log_alpha, beta, n_accept, T,
+                                                    H, units, out);
   return cudaGetLastError();
 }
 
