@@ -108,6 +108,7 @@ struct Misc {
   float gamma[D];    // Gamma_C = e^{g_C} per key channel
   uint64_t bar_qk, bar_la, bar_v;                     // TMA arrivals
   uint64_t bar_gp, bar_m1, bar_u, bar_m2, bar_fin;    // MMA completions
+  uint64_t bar_gops;            // Gram operands of the chunk built (one arrival per warp)
   uint64_t bar_build, bar_om, bar_t1, bar_t, bar_ny, bar_ad;  // operands ready (one arrival per warp)
   uint64_t bar_plan;            // the issue thread has planned the next chunk
   uint64_t bar_pka, bar_pkb;    // package copies: [Gamma, Qt; Kt, Kdec] and [T', P]
@@ -330,6 +331,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     mbar_init(&m.bar_qk, 1); mbar_init(&m.bar_la, 1); mbar_init(&m.bar_v, 1);
     mbar_init(&m.bar_gp, 1); mbar_init(&m.bar_m1, 1); mbar_init(&m.bar_u, 1);
     mbar_init(&m.bar_m2, 1); mbar_init(&m.bar_fin, 1);
+    mbar_init(&m.bar_gops, kComputeWarps);
     mbar_init(&m.bar_build, kComputeWarps); mbar_init(&m.bar_om, kComputeWarps);
     mbar_init(&m.bar_t1, kComputeWarps / 2); mbar_init(&m.bar_t, kComputeWarps / 2);
     mbar_init(&m.bar_ny, kComputeWarps / 2);
@@ -535,7 +537,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         auto kd = [&](uint32_t off) { return sdesc_sw128(sa + off, 16, 1024); };
         auto mnd = [&](uint32_t off, uint32_t lbo) { return sdesc_sw128(sa + off, lbo, 1024); };
         const uint32_t to = tmb + TM_O + 64u * (uint32_t)(ci & 1);
-        if (!wait_bar(cx, &m.bar_build, par, 30, ci)) break;
+        if (!wait_bar(cx, &m.bar_gops, par, 30, ci)) break;
         if (*reinterpret_cast<volatile int *>(&m.abort)) break;  // no new copies once aborting
         PHASE_MARK_MMA(0);
         if (ci > 0 && !wait_bar(cx, &m.bar_m2, par ^ 1u, 36, ci - 1)) break;
@@ -575,6 +577,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         // [O^T | Y^T] = S^T [Qt; Kt]^T
         if (!wait_bar(cx, &m.bar_om, par, 31, ci)) break;
+        if (!wait_bar(cx, &m.bar_build, par, 40, ci)) break;  // [Qt; Kt] and Kdec of the chunk
         PHASE_MARK_MMA(1);
         if (helped_cur && !wait_bar(cx, &m.bar_pka, par ^ 1u, 38, ci)) break;
         if (has_next) {
@@ -782,6 +785,9 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         kraw[j] = ld_shared_b32(bK + (uint32_t)j * 128u + swzk[j & 7]);
         qraw[j] = ld_shared_b32(bQ + (uint32_t)j * 128u + swzk[j & 7]);
       }
+      // The Gram operands first, so that the Gram / P MMAs run under the rest
+      // of the build; the factors the rest needs stay packed in registers.
+      uint32_t g2s[16], kc2s[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const uint32_t o = (uint32_t)j * 128u + swzk[j & 7];
@@ -797,10 +803,17 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           if (a2 < ta) continue;
           st_shared_b32(bGB + 16u * blk(a2, 0) * 128u + o, hmul2_bf16(kc2, fb2[a2]));
         }
-        const uint32_t g2 = pack_bf16x2(e0 * fs0, e1 * fs1);
-        st_shared_b32(bST + o, hmul2_bf16(q2, g2));
-        st_shared_b32(bST + 8192u + o, hmul2_bf16(k2, g2));
-        st_shared_b32(bKD + o, hmul2_bf16(kc2, fd2));
+        g2s[j] = pack_bf16x2(e0 * fs0, e1 * fs1);
+        kc2s[j] = kc2;
+      }
+      fence_proxy_async_smem();
+      warp_arrive(&m.bar_gops, lane);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t o = (uint32_t)j * 128u + swzk[j & 7];
+        st_shared_b32(bST + o, hmul2_bf16(qraw[j], g2s[j]));
+        st_shared_b32(bST + 8192u + o, hmul2_bf16(kraw[j], g2s[j]));
+        st_shared_b32(bKD + o, hmul2_bf16(kc2s[j], fd2));
       }
       PHASE_MARK(15);
       PHASE_MARK_W7(2);
@@ -1172,6 +1185,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         if (helped) {
           chain_beta(ci + 1);
+          warp_arrive(&m.bar_gops, lane);
           warp_arrive(&m.bar_build, lane);
         } else if (!scan_build(ci + 1)) {
           failed = true;
