@@ -517,6 +517,9 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       bulk_wait_all();
       if (n_published) atomicAdd(&status->help_published, n_published);
     } else if (warp == kMmaWarp && lane == 0 && n_chunks > 0) {
+      // The issue thread polls its barriers (its reaction time is on the chain's
+      // critical path), except beside helper CTAs, where suspending waits are faster.
+      constexpr bool kPoll = kMode != kModeHelp;
       // A ready package of chunk ci sits in ring slot ci % kHelpSlots of this chain.
       unsigned char *my_ring =
           helping ? help.ring + (size_t)chain * kHelpSlots * kHelpSlotStride : nullptr;
@@ -538,10 +541,10 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         auto kd = [&](uint32_t off) { return sdesc_sw128(sa + off, 16, 1024); };
         auto mnd = [&](uint32_t off, uint32_t lbo) { return sdesc_sw128(sa + off, lbo, 1024); };
         const uint32_t to = tmb + TM_O + 64u * (uint32_t)(ci & 1);
-        if (!wait_bar(cx, &m.bar_gops, par, 30, ci, true)) break;
+        if (!wait_bar(cx, &m.bar_gops, par, 30, ci, kPoll)) break;
         if (*reinterpret_cast<volatile int *>(&m.abort)) break;  // no new copies once aborting
         PHASE_MARK_MMA(0);
-        if (ci > 0 && !wait_bar(cx, &m.bar_m2, par ^ 1u, 36, ci - 1, true)) break;
+        if (ci > 0 && !wait_bar(cx, &m.bar_m2, par ^ 1u, 36, ci - 1, kPoll)) break;
         tc_fence_after();
         if (helped_cur) {
           // T' and P of the package: the previous chunk's Delta and M2 MMAs have
@@ -577,10 +580,10 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           PHASE_STAMP(32 * kMmaWarp, 51);
         }
         // [O^T | Y^T] = S^T [Qt; Kt]^T
-        if (!wait_bar(cx, &m.bar_om, par, 31, ci, true)) break;
-        if (!wait_bar(cx, &m.bar_build, par, 40, ci, true)) break;  // [Qt; Kt] and Kdec of the chunk
+        if (!wait_bar(cx, &m.bar_om, par, 31, ci, kPoll)) break;
+        if (!wait_bar(cx, &m.bar_build, par, 40, ci, kPoll)) break;  // [Qt; Kt] and Kdec of the chunk
         PHASE_MARK_MMA(1);
-        if (helped_cur && !wait_bar(cx, &m.bar_pka, par ^ 1u, 38, ci, true)) break;
+        if (helped_cur && !wait_bar(cx, &m.bar_pka, par ^ 1u, 38, ci, kPoll)) break;
         if (has_next) {
           // Gamma of the next chunk (this chunk's state pass has read Gamma); the
           // phase's byte count covers the two copies issued after the (V - Y) pass.
@@ -607,7 +610,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         // columns 0-31 and K steps 2, 3 need only the diagonal and 16 -> 32 blocks
         // of T' and are issued as soon as those exist; the two remaining products
         // wait for the 32 -> 64 blocks.
-        if (!wait_bar(cx, &m.bar_ny, par, 33, ci, true)) break;
+        if (!wait_bar(cx, &m.bar_ny, par, 33, ci, kPoll)) break;
         PHASE_MARK_MMA(3);
         if (has_next) issue_v(ci + 1, h, tok(ci + 1));   // the (V - Y) pass has read this chunk's v tile
         if (helped_next) {
@@ -617,8 +620,8 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           bulk_load(sa + SM_KDEC + 16384u * (uint32_t)((ci + 1) & 1), slot_of(ci + 1) + PKG_KDEC,
                     16384, &m.bar_pka);
         }
-        if (!wait_bar(cx, &m.bar_t1, par, 37, ci, true)) break;
-        if (helped_cur && !wait_bar(cx, &m.bar_pkb, par, 39, ci, true)) break;
+        if (!wait_bar(cx, &m.bar_t1, par, 37, ci, kPoll)) break;
+        if (helped_cur && !wait_bar(cx, &m.bar_pkb, par, 39, ci, kPoll)) break;
         tc_fence_after();
         umma_ts(tmb + TM_D, tmb + TM_NY, kd(SM_TMAT), ID_N32, 0u);                       // r 0-31, s 0
         umma_ts(tmb + TM_D + 16u, tmb + TM_NY + 8u, kd(SM_TMAT + 16u * 128u + 32u), ID_N16,
@@ -627,7 +630,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 0u);                                                                   // r 32-63, s 2
         umma_ts(tmb + TM_D + 48u, tmb + TM_NY + 24u, kd(SM_TMAT + 48u * 128u + 96u), ID_N16,
                 1u);                                                                   // r 48-63, s 3
-        if (!wait_bar(cx, &m.bar_t, par, 32, ci, true)) break;
+        if (!wait_bar(cx, &m.bar_t, par, 32, ci, kPoll)) break;
         PHASE_MARK_MMA(2);
         tc_fence_after();
         umma_ts(tmb + TM_D + 32u, tmb + TM_NY, kd(SM_TMAT + 32u * 128u), ID_N32, 1u);        // r 32-63, s 0
@@ -635,7 +638,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 1u);                                                                   // r 32-63, s 1
         umma_commit(&m.bar_u);
         // S^T += Delta^T Kdec ; O^T += Delta^T P^T
-        if (!wait_bar(cx, &m.bar_ad, par, 35, ci, true)) break;
+        if (!wait_bar(cx, &m.bar_ad, par, 35, ci, kPoll)) break;
         PHASE_MARK_MMA(4);
         tc_fence_after();
         const uint32_t kdec = SM_KDEC + 16384u * (uint32_t)(ci & 1);
