@@ -155,11 +155,19 @@ kda_decode_step_kernel(float *__restrict__ state, const void *__restrict__ q,
 // are fetched into shared memory in one cooperative pass.
 //
 // The CTAs are persistent (two per SM), each walking units with a stride of the
-// grid, and while one unit's tokens run from registers the next unit's state is
-// already being copied into shared memory by one bulk copy: the memory system
-// has the next 64 KB in flight throughout the compute, which a CTA per unit
-// (state load, then compute, then store) leaves idle.
+// grid, and while one unit's tokens run from registers the next unit's state and
+// the cached inputs of its first kReplayGroup tokens are already being copied
+// into shared memory by bulk copies (its beta values ride in the issuing thread's
+// registers): the memory system has the next unit in flight throughout the
+// compute, and a unit starts without a round trip to HBM.
 constexpr int kReplayGroup = 8;
+// Staged inputs of one token: log_alpha (fp32), then k, q, v in the input type.
+template <bool BF16>
+constexpr int replay_raw_token_bytes() { return D * 4 + 3 * D * (BF16 ? 2 : 4); }
+template <bool BF16>
+constexpr size_t replay_smem_bytes() {
+  return (size_t)D * D * sizeof(float) + (size_t)kReplayGroup * replay_raw_token_bytes<BF16>();
+}
 constexpr uint64_t kReplayWaitNs = 2000000000ull;  // bound on the state copy wait
 
 template <bool BF16>
@@ -169,7 +177,10 @@ kda_decode_replay_kernel(float *__restrict__ state, const void *__restrict__ q,
                          const float *__restrict__ log_alpha, const float *__restrict__ beta,
                          const int32_t *__restrict__ n_accept, int32_t T, int32_t H,
                          int64_t units, void *__restrict__ out) {
-  extern __shared__ __align__(128) float stage[];  // the next unit's state, [D][D]
+  // the next unit's state [D][D], then the staged inputs of its first tokens
+  extern __shared__ __align__(128) float stage[];
+  constexpr int kEsz = BF16 ? 2 : 4, kRawTok = replay_raw_token_bytes<BF16>();
+  uint8_t *const raw = reinterpret_cast<uint8_t *>(stage + D * D);
   __shared__ __align__(16) float s_alpha[kReplayGroup][D], s_k[kReplayGroup][D],
       s_q[kReplayGroup][D], s_v[kReplayGroup][D];
   __shared__ float s_beta[kReplayGroup];
@@ -183,13 +194,31 @@ kda_decode_replay_kernel(float *__restrict__ state, const void *__restrict__ q,
     return n < 0 ? 0 : (n > T ? T : n);
   };
   // thread 0: the next unit with accepted tokens after `u` (stride gridDim.x),
-  // its state copy issued into the stage
+  // its state and first tokens' inputs copied into the stage, its betas loaded
+  // into nbeta
+  float nbeta[kReplayGroup];
   auto prefetch_from = [&](int64_t u) {
     while (u < units && accepted(u) == 0) u += gridDim.x;
     s_next = u;
     if (u < units) {
-      mbar_arrive_expect_tx(&bar, D * D * sizeof(float));
+      const int cnt = accepted(u) < kReplayGroup ? accepted(u) : kReplayGroup;
+      const int64_t b = u / H, h = u % H;
+      mbar_arrive_expect_tx(&bar, D * D * sizeof(float) + (uint32_t)(cnt * kRawTok));
       bulk_load(smem_u32(stage), state + u * (int64_t)(D * D), D * D * sizeof(float), &bar);
+#pragma unroll
+      for (int t = 0; t < kReplayGroup; ++t) {
+        if (t < cnt) {
+          const int64_t iu = (b * T + t) * H + h;  // (sequence, token, head)
+          const uint32_t dst = smem_u32(raw + t * kRawTok);
+          bulk_load(dst, log_alpha + iu * D, D * 4, &bar);
+          bulk_load(dst + D * 4, static_cast<const uint8_t *>(k) + iu * D * kEsz, D * kEsz, &bar);
+          bulk_load(dst + D * 4 + D * kEsz, static_cast<const uint8_t *>(q) + iu * D * kEsz,
+                    D * kEsz, &bar);
+          bulk_load(dst + D * 4 + 2 * D * kEsz, static_cast<const uint8_t *>(v) + iu * D * kEsz,
+                    D * kEsz, &bar);
+          nbeta[t] = beta[iu];
+        }
+      }
     }
   };
   if (tid == 0) {
@@ -211,16 +240,32 @@ kda_decode_replay_kernel(float *__restrict__ state, const void *__restrict__ q,
 #pragma unroll
     for (int j = 0; j < 16; ++j)
       s[j] = *reinterpret_cast<const float4 *>(stage + (row0 + 8 * j) * D + col);
-    __syncthreads();  // the stage is free for the next unit's state
-    if (tid == 0) prefetch_from(u + gridDim.x);
-
     const int64_t b = u / H, h = u % H;
     const int n = accepted(u);
+    {  // the first tokens' staged inputs, converted
+      const int cnt = n < kReplayGroup ? n : kReplayGroup;
+      for (int e = tid; e < cnt * D; e += kThreads) {
+        const int t = e / D, c = e % D;
+        const uint8_t *rt = raw + t * kRawTok;
+        s_alpha[t][c] = expf(reinterpret_cast<const float *>(rt)[c]);
+        s_k[t][c] = load_elem<BF16>(rt + D * 4, c);
+        s_q[t][c] = load_elem<BF16>(rt + D * 4 + D * kEsz, c);
+        s_v[t][c] = load_elem<BF16>(rt + D * 4 + 2 * D * kEsz, c);
+      }
+      if (tid == 0) {
+#pragma unroll
+        for (int t = 0; t < kReplayGroup; ++t)
+          if (t < cnt) s_beta[t] = nbeta[t];
+      }
+    }
+    __syncthreads();  // the stage is free for the next unit; the first inputs are in place
+    if (tid == 0) prefetch_from(u + gridDim.x);
+
     float *S = state + u * (int64_t)(D * D);
     for (int t0 = 0; t0 < n; t0 += kReplayGroup) {
       const int cnt = n - t0 < kReplayGroup ? n - t0 : kReplayGroup;
       if (t0 > 0) __syncthreads();  // the previous group's inputs are consumed
-      for (int e = tid; e < cnt * D; e += kThreads) {
+      for (int e = tid; t0 > 0 && e < cnt * D; e += kThreads) {
         const int t = e / D, c = e % D;
         const int64_t iu = (b * T + t0 + t) * H + h;  // (sequence, token, head)
         s_alpha[t][c] = expf(log_alpha[iu * D + c]);
@@ -228,8 +273,8 @@ kda_decode_replay_kernel(float *__restrict__ state, const void *__restrict__ q,
         s_q[t][c] = load_elem<BF16>(q, iu * D + c);
         s_v[t][c] = load_elem<BF16>(v, iu * D + c);
       }
-      if (tid < cnt) s_beta[tid] = beta[(b * T + t0 + tid) * H + h];
-      __syncthreads();
+      if (t0 > 0 && tid < cnt) s_beta[tid] = beta[(b * T + t0 + tid) * H + h];
+      if (t0 > 0) __syncthreads();
 
       for (int t = 0; t < cnt; ++t) {
         const float *sa = s_alpha[t], *sk = s_k[t], *sq = s_q[t];
@@ -317,7 +362,7 @@ cudaError_t launch_decode_replay(float *state, const void *q, const void *k, con
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int64_t ctas = units < 2 * (int64_t)sms ? units : 2 * (int64_t)sms;
-  const size_t stage = (size_t)D * D * sizeof(float);
+  const size_t stage = bf16 ? replay_smem_bytes<true>() : replay_smem_bytes<false>();
   auto kern = bf16 ? kda_decode_replay_kernel<true> : kda_decode_replay_kernel<false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)stage);
   if (e != cudaSuccess) return e;

@@ -51,6 +51,26 @@ def test_replay_matches_oracle(dtype):
         assert torch.isnan(out[b, nb:]).all()               # rejected rows never written
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_replay_more_tokens_than_one_group(dtype):
+    """T = 11 drafts: the first 8 accepted tokens come staged with the state, the
+    rest in a second group."""
+    B, T, H = 4, 11, 2
+    r = replay_inputs(B, T, H, dtype, seed=5)
+    n = np.array([11, 9, 8, 3], dtype=np.int32)
+    state = r["state"].clone()
+    out = torch.full((B, T, H, 128), float("nan"), dtype=r["q"].dtype, device=DEV)
+    kda.kda_decode_replay(state, r["q"], r["k"], r["v"], r["log_alpha"], r["beta"],
+                          torch.as_tensor(n, device=DEV), out=out)
+    torch.cuda.synchronize()
+    ref_out, ref_state = _oracle(r, n)
+    for b in range(B):
+        nb = int(n[b])
+        assert rel_l2(state[b], ref_state[b]) <= TOL[dtype]
+        assert rel_l2(out[b, :nb], ref_out[b, :nb]) <= TOL[dtype]
+        assert torch.isnan(out[b, nb:]).all()
+
+
 def test_replay_equals_consecutive_decode_steps():
     """Replaying every draft token equals that many kda_decode_step calls."""
     B, T, H = 3, 5, 4
