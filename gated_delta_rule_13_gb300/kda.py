@@ -244,12 +244,33 @@ def kda_state_combine(state_b, state_m, n_segments: int, init_state=None, *, sta
     return st, en
 
 
+def _piece_bounds(n_tokens: int, piece_tokens: int, min_tail: int = 1024) -> list:
+    """Token bounds of the pieces: ``piece_tokens`` each, except that the last
+    full piece is cut in halves down to ``min_tail`` tokens (multiples of the
+    64-token chunk), so that the prefill and output copy left after the last
+    input copy are short."""
+    bounds, p0 = [0], 0
+    while n_tokens - p0 > piece_tokens:
+        p0 += piece_tokens
+        bounds.append(p0)
+    rest = n_tokens - p0
+    while rest > max(min_tail, 64) and rest // 2 >= 64:
+        half = (rest // 2 + 63) // 64 * 64
+        p0 += half
+        bounds.append(p0)
+        rest -= half
+    if bounds[-1] != n_tokens:
+        bounds.append(n_tokens)
+    return bounds
+
+
 def kda_chunk_fwd_host(q, k, v, log_alpha, beta, init_state=None, *, out=None,
                        final_state=None, piece_tokens: int = 4096, device=None):
     """Prefill of ONE sequence whose inputs are in host memory (pinned for the
     copies to overlap): the tokens go through in pieces of ``piece_tokens`` (a
-    multiple of the 64-token chunk), each piece's host-to-device copy overlapping
-    the previous piece's prefill and the device-to-host copy of its outputs.
+    multiple of the 64-token chunk; the last one cut in halves down to 1024
+    tokens), each piece's host-to-device copy overlapping the previous piece's
+    prefill and the device-to-host copy of its outputs.
     Piece i starts from piece i-1's final state (fp32, exact), so the results
     are those of one kda_chunk_fwd call.  Returns host ``(out, final_state)``."""
     if piece_tokens <= 0 or piece_tokens % 64:
@@ -275,7 +296,7 @@ def kda_chunk_fwd_host(q, k, v, log_alpha, beta, init_state=None, *, out=None,
     ws = torch.empty(kda_chunk_fwd_workspace_size(1, piece_tokens, H, dk, dv, _dtype_code(q)),
                      dtype=torch.uint8, device=device)
     cu = {}
-    bounds = list(range(0, N, piece_tokens)) + [N]
+    bounds = _piece_bounds(N, piece_tokens)
     copied = []
     copy_in.wait_stream(compute)  # the device buffers are free
     for p0, p1 in zip(bounds[:-1], bounds[1:]):

@@ -267,3 +267,20 @@ def test_product_path_does_not_import_oracle():
                 text = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "kda_oracle" not in text, f
+
+
+def test_host_pipeline_piece_bounds():
+    """Pieces of kda_chunk_fwd_host: whole chunks except the sequence's end, the
+    last full piece cut in halves down to 1024 tokens, bounds increasing."""
+    from gated_delta_rule_13_gb300.kda import _piece_bounds
+    assert _piece_bounds(32768, 4096) == [0, 4096, 8192, 12288, 16384, 20480, 24576, 28672,
+                                          30720, 31744, 32768]
+    assert _piece_bounds(5000, 4096) == [0, 4096, 5000]
+    assert _piece_bounds(100, 4096) == [0, 100]
+    for n in (1, 63, 64, 65, 1000, 2048, 4097, 9999, 70000):
+        for piece in (64, 256, 4096):
+            b = _piece_bounds(n, piece)
+            assert b[0] == 0 and b[-1] == n
+            assert all(x % 64 == 0 for x in b[:-1])
+            assert all(b1 - b0 <= piece for b0, b1 in zip(b, b[1:]))
+            assert all(b0 < b1 for b0, b1 in zip(b, b[1:]))
