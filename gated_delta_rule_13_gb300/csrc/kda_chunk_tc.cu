@@ -42,9 +42,10 @@
 // s only touches output columns r >= 16 s.
 //
 // Pipeline.  O^T is double-buffered in TMEM and Kdec in shared memory, so the
-// next chunk's operand build overlaps this chunk's state MMAs, the triangular
-// solve (warps 0-3) overlaps the previous chunk's output stores and the (V - Y)
-// pass (warps 4-7), and the Gram MMAs of chunk c+1 overlap the state pass of c+1.
+// next chunk's operand build overlaps this chunk's state MMAs, and the triangular
+// solve (warps 0-3) overlaps the previous chunk's output stores, the O+Y MMAs and
+// the (V - Y) pass (warps 4-7).  The build writes the Gram operands first, so the
+// Gram MMAs of chunk c+1 run under the rest of its build.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
