@@ -40,11 +40,11 @@ size_t base_workspace_bytes(int32_t n_seqs) {
 }
 
 // Helper CTAs for a bf16 prefill of `chains` chains on the current device: the
-// SMs the chains leave idle, when they are at least three times as many as the
+// SMs the chains leave idle, when they are at least four times as many as the
 // chains.  With fewer, the helpers cover too few chunks to repay what the
-// protocol costs the chain CTAs (measured on a GB300: 8 chains 1.35x faster,
-// 32 chains 1.06x, 64 chains 0.91x).  The environment variable
-// KDA_CHUNK_HELPERS caps the count (0 turns helpers off).
+// protocol costs the chain CTAs (measured on a GB300 with 148 SMs: 8 chains
+// 1.22x faster, 24 chains 1.06x, 32 chains 0.97x, 96 chains 0.78x).  The
+// environment variable KDA_CHUNK_HELPERS caps the count (0 turns helpers off).
 int32_t help_ctas(int64_t chains, int dtype) {
   if (dtype != KDA_BF16 || chains <= 0) return 0;
   int dev = 0, sms = 0;
@@ -53,7 +53,7 @@ int32_t help_ctas(int64_t chains, int dtype) {
     cudaGetLastError();
     return 0;
   }
-  int64_t n = sms - chains < 3 * chains ? 0 : sms - chains;
+  int64_t n = sms - chains < 4 * chains ? 0 : sms - chains;
   if (const char *env = getenv("KDA_CHUNK_HELPERS")) {
     const long cap = strtol(env, nullptr, 10);
     if (cap >= 0 && cap < n) n = cap;

@@ -73,13 +73,13 @@ int kda_version(void);
  *     prefix sum records KDA_ERR_INVALID_ARG);
  *   - when cu_seqlens is a host pointer, a device copy of it;
  *   - for a bf16 call with few enough (sequence, head) chains that each
- *     sequence can be cut into K >= 3 segments with 2 K x chains <= SMs, the
+ *     sequence can be cut into K >= 2 segments with 2 K x chains <= SMs, the
  *     scratch of the in-device split (segment bounds, three fp32 states per
  *     segment and head, and one bf16 value per token, head and channel): the
  *     segments run side by side and their states are stitched together exactly
  *     ("Kimi K3: 架构、训练与系统全景解析", section 7.1: segments compose as
  *     affine maps of the state);
- *   - otherwise, for a bf16 call whose chains leave at least three times as
+ *   - otherwise, for a bf16 call whose chains leave at least four times as
  *     many of the device's SMs idle as there are chains, the ring of the
  *     helper CTAs.
  *     These run on the idle SMs and compute the state-independent half of
