@@ -62,12 +62,13 @@ int32_t help_ctas(int64_t chains, int dtype) {
 }
 
 // Segments per sequence for the in-device split of a bf16 prefill (0: no
-// split).  Its pass runs 2 K CTAs per chain and takes about T / K chunk-steps
-// (plus a combine and an output correction), so it needs 2 K x chains <= SMs
-// and pays off from K = 2 on; segments are kept at two chunks or more on
-// average.  The environment variable KDA_CHUNK_SPLIT caps K (0 turns the
-// split off).
-int32_t split_factor(int32_t n_seqs, int64_t n_tokens, int32_t H, int dtype) {
+// split).  Its pass runs 2 K CTAs per chain, or 2 K - 1 for a call without an
+// initial state (the first segment then needs no transition run), and takes
+// about T / K chunk-steps (plus a combine and an output correction), so it needs
+// (2 K or 2 K - 1) x chains <= SMs and pays off from K = 2 on; segments are kept
+// at two chunks or more on average.  The environment variable KDA_CHUNK_SPLIT
+// caps K (0 turns the split off).
+int32_t split_factor(int32_t n_seqs, int64_t n_tokens, int32_t H, int dtype, bool zero_init) {
   const int64_t chains = (int64_t)n_seqs * H;
   if (dtype != KDA_BF16 || chains <= 0 || n_tokens <= 0) return 0;
   int dev = 0, sms = 0;
@@ -76,7 +77,8 @@ int32_t split_factor(int32_t n_seqs, int64_t n_tokens, int32_t H, int dtype) {
     cudaGetLastError();
     return 0;
   }
-  int64_t k = sms / (2 * chains);
+  // 2 K C blocks in the first pass, or (2 K - 1) C without an initial state
+  int64_t k = zero_init ? (sms + chains) / (2 * chains) : sms / (2 * chains);
   const int64_t by_length = n_tokens / ((int64_t)n_seqs * 2 * kda::kChunk);
   if (by_length < k) k = by_length;
   if (const char *env = getenv("KDA_CHUNK_SPLIT")) {
@@ -100,12 +102,14 @@ size_t order_bytes(int32_t n_seqs, int dtype) {
 size_t workspace_bytes_for(int32_t n_seqs, int64_t n_tokens, int32_t H, int dtype) {
   const int64_t chains = (int64_t)n_seqs * H;
   size_t b = base_workspace_bytes(n_seqs) + order_bytes(n_seqs, dtype);
-  const int32_t n_split = split_factor(n_seqs, n_tokens, H, dtype);
-  if (n_split > 0)
-    b += kda::split_workspace_bytes(n_seqs, n_tokens, H, n_split);
-  else if (help_ctas(chains, dtype) > 0)
-    b += help_workspace_bytes(chains);
-  return b;
+  // the larger of the schedules a call may take: the split without an initial
+  // state (the most segments), else with one, else the helpers
+  const int32_t k_zero = split_factor(n_seqs, n_tokens, H, dtype, true);
+  const int32_t k_init = split_factor(n_seqs, n_tokens, H, dtype, false);
+  size_t extra = k_zero > 0 ? kda::split_workspace_bytes(n_seqs, n_tokens, H, k_zero) : 0;
+  if (k_init == 0 && help_ctas(chains, dtype) > 0 && help_workspace_bytes(chains) > extra)
+    extra = help_workspace_bytes(chains);
+  return b + extra;
 }
 
 // True when `p` is memory the device can read directly as a device array.
@@ -213,7 +217,7 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
     need += ob;
   }
   // The in-device split, when it applies and the workspace has its scratch.
-  const int32_t n_split = split_factor(n_seqs, n_tokens, H, dtype);
+  const int32_t n_split = split_factor(n_seqs, n_tokens, H, dtype, init_state == nullptr);
   if (n_split > 0 && workspace_bytes >= need + kda::split_workspace_bytes(n_seqs, n_tokens, H, n_split)) {
     const cudaError_t e = kda::launch_chunk_fwd_split(a, n_split, ws + need, st);
     if (e == cudaErrorNotSupported) return KDA_ERR_UNSUPPORTED;

@@ -262,8 +262,8 @@ __host__ __device__ constexpr int blk(int a, int b) { return a * (a + 1) / 2 + b
 
 // Kernel variants.  kModeHelp adds helper CTAs (and the chain CTAs' side of
 // their protocol); kModeTransitions is the first pass of the in-device split of
-// long sequences: block b < gridDim.x / 2 runs chain b from a zero state (its
-// final state is the segment's B), block b + gridDim.x / 2 runs the same chain
+// long sequences: block b < chains runs chain b from a zero state (its
+// final state is the segment's B), the block after the chains that carries b runs the same chain
 // as a transition (state I, v = 0: its final state is the segment's transition
 // matrix M), and neither writes outputs.  Each mode compiles its branches away
 // in the others, which keeps the plain path as fast as before (the runtime
@@ -283,16 +283,24 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const HelpRing help, float *__restrict__ final_state_m,
                         const int32_t *__restrict__ seq_order,
                         const __grid_constant__ CUtensorMap tm_om,
-                        __nv_bfloat16 *__restrict__ out_m, const int write_out) {
+                        __nv_bfloat16 *__restrict__ out_m, const int write_out,
+                        const int split_k) {
   // Indexing the __shared__ array directly (no integer round trip) keeps every
   // access a shared-memory instruction.  The 128-byte swizzle atoms need a
   // 1024-byte aligned base, checked below.
   extern __shared__ __align__(1024) uint8_t smem[];
   Misc &m = *reinterpret_cast<Misc *>(smem + SM_MISC);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // transition run of chain blockIdx.x - gridDim.x / 2 (first pass of a split)
-  const bool transition = kMode == kModeTransitions && blockIdx.x >= gridDim.x / 2;
-  const int slot = transition ? (int)(blockIdx.x - gridDim.x / 2) : (int)blockIdx.x;
+  // First pass of a split: blocks [0, n_seqs H) are the zero-start runs of the
+  // chains, the rest the transition runs, of every chain or, with split_k >= 2,
+  // of every chain but those of each sequence's first segment (sequences of
+  // split_k segments; a zero initial state needs no M_0).
+  const bool transition = kMode == kModeTransitions && (int64_t)blockIdx.x >= (int64_t)n_seqs * H;
+  int slot = (int)blockIdx.x;
+  if (transition) {
+    const int i = (int)(blockIdx.x - n_seqs * H);
+    slot = split_k >= 2 ? i + (i / ((split_k - 1) * H) + 1) * H : i;
+  }
   // Blocks past the chains are helpers (only when the call has a helper ring).
   const bool helping = kMode == kModeHelp && help.ring != nullptr;
   const bool helper = helping && slot >= help.n_chains;
@@ -1380,14 +1388,15 @@ cudaError_t launch_chunk_fwd_bf16_tc(const ChunkArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     seq_order = a.seq_order;
   }
-  const int64_t blocks = transitions ? 2 * chains : chains + n_help;
+  const int64_t m_runs = a.split_skip_k >= 2 ? chains / a.split_skip_k * (a.split_skip_k - 1) : chains;
+  const int64_t blocks = transitions ? chains + m_runs : chains + n_help;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   kernel<<<(unsigned)blocks, kThreads, SMEM_BYTES, stream>>>(
       mq, mk, mv, mla, mo, a.beta, a.init_state, a.cu_seqlens, a.n_seqs, a.n_tokens, a.H,
       static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.status, help, a.final_state_m,
       seq_order, transitions && a.out_m ? mom : mo,
       static_cast<__nv_bfloat16 *>(transitions && a.out_m ? a.out_m : a.out),
-      transitions ? (a.write_out ? 1 : 0) : 1);
+      transitions ? (a.write_out ? 1 : 0) : 1, transitions ? a.split_skip_k : 0);
   return cudaGetLastError();
 }
 

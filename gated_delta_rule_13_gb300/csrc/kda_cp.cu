@@ -89,13 +89,14 @@ kda_split_combine_kernel(const float *__restrict__ init, const float *__restrict
       for (int q = 0; q < 4; ++q) out[c4 + q] = sbuf[cur][row][c4 + q];
     }
     if (j == K || (j + 1 == K && !end)) break;
-    // S_{j+1}[row][cols] = B_j[row][cols] + sum_k M_j[row][k] S_j[k][cols]
+    // S_{j+1}[row][cols] = B_j[row][cols] + sum_k M_j[row][k] S_j[k][cols]; with
+    // no initial state S_0 = 0, and M_0 is not read (it may not have been made)
     const float *m = M + blk(seg) + (int64_t)row * D;
     const float4 *b = reinterpret_cast<const float4 *>(B + blk(seg) + (int64_t)row * D + col0);
     float4 acc[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[q] = b[c4 + q];
-    for (int k = 0; k < D; k += 4) {
+    for (int k = 0; (j > 0 || init) && k < D; k += 4) {
       const float4 mk = *reinterpret_cast<const float4 *>(m + k);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
@@ -232,6 +233,7 @@ cudaError_t launch_chunk_fwd_split(const ChunkArgs &a, int32_t K, unsigned char 
   p.help_ws = nullptr;
   p.n_help = 0;
   p.seq_order = nullptr;  // sized for the sequences, not the segments
+  p.split_skip_k = a.init_state == nullptr ? K : 0;  // S_0 = 0: M_0 is never needed
   e = launch_chunk_fwd_bf16_tc(p, stream);
   if (e != cudaSuccess) return e;
 

@@ -81,6 +81,10 @@ struct ChunkArgs {
   // no output is written at all (out is then only a valid tensor-map base).
   void *out_m = nullptr;
   bool write_out = true;
+  // kTransitions: with K >= 2, the chains are sequences of K segments each whose
+  // first segment starts from a zero state, so it gets no transition run (its
+  // M_0 and out_m rows are not written).  0: every chain gets one.
+  int32_t split_skip_k = 0;
 };
 
 cudaError_t launch_decode_step(float *state, const void *q, const void *k, const void *v,

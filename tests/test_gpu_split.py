@@ -112,3 +112,44 @@ def test_host_cu_seqlens_and_no_final_state():
     o1, s1, _ = _run(x, host_cu=True, final=False)
     assert s1 is None
     _parity(x, o1, None, heads=[1])
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("scale", [0.0, 0.01])
+def test_zero_init_split_takes_more_segments(scale):
+    """Without an initial state the first segment needs no transition run, so a
+    sequence over 16 heads is cut into K = (SMs + 16) // 32 segments (5 on a
+    GB300, one more than with an initial state): every M_j of a later segment
+    and the combine from S_0 = 0 against the oracle."""
+    x = _slow_decay(inputs.prefill_inputs([16384], H=16, dtype="bf16", device=DEV, seed=44),
+                    scale)
+    o1, s1, ws_split = _run(x)
+    o0, s0, ws_plain = _run(x, split=False)
+    assert ws_split > ws_plain
+    _parity(x, o1, s1, heads=[0, 9, 15])
+    assert rel_l2(o1, o0) <= 1e-2
+    assert rel_l2(s1, s0) <= 1e-2
+
+
+def test_zero_init_split_beyond_the_init_bound():
+    """40 chains: 2 K - 1 = 3 blocks per chain fit the SMs, 2 K = 4 do not, so
+    the call without an initial state is split in two and the one with an
+    initial state is not (bitwise the plain path)."""
+    sms = _sms()
+    if not ((sms + 40) // 80 >= 2 and sms // 80 < 2):
+        pytest.skip(f"{sms} SMs: not the case this test is about")
+    x = _slow_decay(inputs.prefill_inputs([4096], H=40, dtype="bf16", device=DEV, seed=45), 0.01)
+    o1, s1, ws_split = _run(x)
+    o0, s0, ws_plain = _run(x, split=False)
+    assert ws_split > ws_plain
+    assert not torch.equal(o1, o0)  # the split ran (its rounding differs)
+    _parity(x, o1, s1)
+    y = _slow_decay(inputs.prefill_inputs([4096], H=40, dtype="bf16", init_state=True,
+                                          device=DEV, seed=45), 0.01)
+    o2, s2, _ = _run(y)
+    o3, s3, _ = _run(y, split=False)
+    assert torch.equal(o2, o3) and torch.equal(s2, s3)
+    _parity(y, o2, s2, heads=[0, 39])
