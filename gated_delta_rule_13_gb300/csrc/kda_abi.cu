@@ -42,7 +42,7 @@ size_t base_workspace_bytes(int32_t n_seqs) {
 // Helper CTAs for a bf16 prefill of `chains` chains on the current device: the
 // SMs the chains leave idle, when they are at least four times as many as the
 // chains.  With fewer, the helpers cover too few chunks to repay what the
-// protocol costs the chain CTAs (measured on a GB300 with 148 SMs: 8 chains
+// protocol costs the chain CTAs (measured on a GB300 with 152 SMs: 8 chains
 // 1.22x faster, 24 chains 1.06x, 32 chains 0.97x, 96 chains 0.78x).  The
 // environment variable KDA_CHUNK_HELPERS caps the count (0 turns helpers off).
 int32_t help_ctas(int64_t chains, int dtype) {
