@@ -57,7 +57,8 @@ __global__ void kda_split_bounds_kernel(const int32_t *__restrict__ cu, int32_t 
 // One CTA per (sequence, head, 32-column block of the state): the columns of
 // S evolve independently under S <- M S + B.  start[s K + j] receives S_j
 // (j < K) and end[s] the composed S_K, each when non-null.
-constexpr int kCols = 32;
+constexpr int kCols = 16;          // columns of S per CTA (columns evolve independently)
+constexpr int kColQ = kCols / 8;   // float4 per thread: 2 threads per row
 __global__ void __launch_bounds__(256, 1)
 kda_split_combine_kernel(const float *__restrict__ init, const float *__restrict__ B,
                const float *__restrict__ M, int32_t n_seqs, int32_t K, int32_t H,
@@ -66,7 +67,7 @@ kda_split_combine_kernel(const float *__restrict__ init, const float *__restrict
   const int sh = blockIdx.x, s = sh / H, h = sh % H;
   const int col0 = kCols * blockIdx.y;
   const int t = threadIdx.x;
-  const int row = t >> 1, c4 = (t & 1) * 4;  // row of S, first of this thread's 4 float4 columns
+  const int row = t >> 1, c4 = (t & 1) * kColQ;  // row of S, first of this thread's float4 columns
   auto blk = [=](int64_t seg) {  // offset of the [seg][h] 128 x 128 block
     return ((seg * H + h) * (int64_t)D) * D;
   };
@@ -86,23 +87,23 @@ kda_split_combine_kernel(const float *__restrict__ init, const float *__restrict
     if (dst) {
       float4 *out = reinterpret_cast<float4 *>(dst + (int64_t)row * D + col0);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) out[c4 + q] = sbuf[cur][row][c4 + q];
+      for (int q = 0; q < kColQ; ++q) out[c4 + q] = sbuf[cur][row][c4 + q];
     }
     if (j == K || (j + 1 == K && !end)) break;
     // S_{j+1}[row][cols] = B_j[row][cols] + sum_k M_j[row][k] S_j[k][cols]; with
     // no initial state S_0 = 0, and M_0 is not read (it may not have been made)
     const float *m = M + blk(seg) + (int64_t)row * D;
     const float4 *b = reinterpret_cast<const float4 *>(B + blk(seg) + (int64_t)row * D + col0);
-    float4 acc[4];
+    float4 acc[kColQ];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) acc[q] = b[c4 + q];
+    for (int q = 0; q < kColQ; ++q) acc[q] = b[c4 + q];
     for (int k = 0; (j > 0 || init) && k < D; k += 4) {
       const float4 mk = *reinterpret_cast<const float4 *>(m + k);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const float mv = kk == 0 ? mk.x : kk == 1 ? mk.y : kk == 2 ? mk.z : mk.w;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < kColQ; ++q) {
           const float4 sv = sbuf[cur][k + kk][c4 + q];
           acc[q].x = fmaf(mv, sv.x, acc[q].x);
           acc[q].y = fmaf(mv, sv.y, acc[q].y);
@@ -112,7 +113,7 @@ kda_split_combine_kernel(const float *__restrict__ init, const float *__restrict
       }
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) sbuf[cur ^ 1][row][c4 + q] = acc[q];
+    for (int q = 0; q < kColQ; ++q) sbuf[cur ^ 1][row][c4 + q] = acc[q];
     __syncthreads();
   }
 }
@@ -126,21 +127,23 @@ kda_split_combine_kernel(const float *__restrict__ init, const float *__restrict
 // accumulation; `skip_first` leaves segment 0 of every sequence alone (its
 // start state is zero).
 constexpr int kCorrTile = 64;
+constexpr int kCorrTilesPerCta = 8;  // tiles of one segment and head per CTA (one S_j load)
 constexpr int kSbPitch = D + 8;   // u32 per row of the bf16 pairs of S_j: bank-conflict free
 constexpr int kQsPitch = D + 8;   // bf16 per row of the q_eff tile
 __global__ void __launch_bounds__(256, 2)
 kda_split_correct_kernel(__nv_bfloat16 *__restrict__ out, const __nv_bfloat16 *__restrict__ qe,
                          const float *__restrict__ start, const int32_t *__restrict__ seg_cu,
-                         int64_t n_tokens, int32_t K, int32_t H, int32_t tiles,
+                         int64_t n_tokens, int32_t K, int32_t H, int32_t ctas_per_seg,
                          int skip_first) {
   extern __shared__ __align__(16) uint32_t corr_smem[];
   uint32_t *sb = corr_smem;                                              // [64 k-pairs][kSbPitch]
   __nv_bfloat16 *qs = reinterpret_cast<__nv_bfloat16 *>(corr_smem + (D / 2) * kSbPitch);  // [64][kQsPitch]
-  const int seg = blockIdx.x / tiles, h = blockIdx.y;
+  const int seg = blockIdx.x / ctas_per_seg, h = blockIdx.y;
   if (skip_first && seg % K == 0) return;
   const int64_t s0 = seg_cu[seg], s1 = seg_cu[seg + 1];
-  const int64_t tb = s0 + (int64_t)kCorrTile * (blockIdx.x % tiles);
-  if (s0 < 0 || s1 > n_tokens || tb >= s1) return;
+  // this CTA's tiles: kCorrTilesPerCta consecutive ones from tb0
+  const int64_t tb0 = s0 + (int64_t)kCorrTile * kCorrTilesPerCta * (blockIdx.x % ctas_per_seg);
+  if (s0 < 0 || s1 > n_tokens || tb0 >= s1) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
   // S_j as bf16 pairs along k: sb[kp][n] = (S[2 kp][n], S[2 kp + 1][n])
@@ -151,7 +154,10 @@ kda_split_correct_kernel(__nv_bfloat16 *__restrict__ out, const __nv_bfloat16 *_
     sb[kp * kSbPitch + n] = *reinterpret_cast<const uint32_t *>(&v);
   }
   const int mt = warp & 3, nh = warp >> 2;  // 16 tokens x 64 columns per warp
-  {
+  for (int ti = 0; ti < kCorrTilesPerCta; ++ti) {
+    const int64_t tb = tb0 + (int64_t)kCorrTile * ti;
+    if (tb >= s1) break;  // uniform
+    if (ti > 0) __syncthreads();  // the previous tile's products have read qs
     const int rows = (int)(s1 - tb < kCorrTile ? s1 - tb : kCorrTile);
     for (int i = tid; i < kCorrTile * (D / 8); i += 256) {
       const int r = i / (D / 8), c8 = i % (D / 8);
@@ -250,10 +256,11 @@ cudaError_t launch_chunk_fwd_split(const ChunkArgs &a, int32_t K, unsigned char 
   // no segment is longer than ceil(ceil(N / 64) / K) chunks of 64 tokens
   const int64_t tiles = ((a.n_tokens + kChunk - 1) / kChunk + K - 1) / K;
   if (tiles == 0) return cudaSuccess;
-  if (nseg * tiles > 0x7fffffffLL || a.H > 65535) return cudaErrorInvalidValue;
-  kda_split_correct_kernel<<<dim3((unsigned)(nseg * tiles), (unsigned)a.H), 256, kCorrSmem,
+  const int64_t cps = (tiles + kCorrTilesPerCta - 1) / kCorrTilesPerCta;
+  if (nseg * cps > 0x7fffffffLL || a.H > 65535) return cudaErrorInvalidValue;
+  kda_split_correct_kernel<<<dim3((unsigned)(nseg * cps), (unsigned)a.H), 256, kCorrSmem,
                              stream>>>(static_cast<__nv_bfloat16 *>(a.out), qe, S, seg_cu,
-                                       a.n_tokens, K, a.H, (int32_t)tiles,
+                                       a.n_tokens, K, a.H, (int32_t)cps,
                                        a.init_state == nullptr ? 1 : 0);
   return cudaGetLastError();
 }
