@@ -605,14 +605,18 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           }
         }
         tc_fence_after();
+        // Y first: only it gates the (V - Y) pass; O follows in the same pipe
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t a = tmb + TM_AS + 8u * ks;
           const uint32_t off = SM_STACK + (ks >> 2) * 16384u + (ks & 3) * 32u;
-          umma_ts(to, a, kd(off), ID_N64, ks > 0 ? 1u : 0u);
-          umma_ts(tmb + TM_Y, a, kd(off + 8192u), ID_N64, ks > 0 ? 1u : 0u);
+          umma_ts(tmb + TM_Y, tmb + TM_AS + 8u * ks, kd(off + 8192u), ID_N64, ks > 0 ? 1u : 0u);
         }
         umma_commit(&m.bar_m1);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t off = SM_STACK + (ks >> 2) * 16384u + (ks & 3) * 32u;
+          umma_ts(to, tmb + TM_AS + 8u * ks, kd(off), ID_N64, ks > 0 ? 1u : 0u);
+        }
         PHASE_MARK_MMA(6);
         // Delta^T = (V - Y)^T T'^T, K step s covering tokens 16 s .. 16 s + 15 and
         // writing only output columns r >= 16 s (T' is lower triangular).  Output
