@@ -73,7 +73,9 @@ int kda_version(void);
  *     prefix sum records KDA_ERR_INVALID_ARG);
  *   - when cu_seqlens is a host pointer, a device copy of it;
  *   - for a bf16 call with few enough (sequence, head) chains that each
- *     sequence can be cut into K >= 2 segments with 2 K x chains <= SMs, the
+ *     sequence can be cut into K >= 2 segments with 2 K x chains <= SMs (or
+ *     (2 K - 1) x chains <= SMs for a call without an initial state, whose
+ *     first segments need no transition run; the size covers the larger K), the
  *     scratch of the in-device split (segment bounds, three fp32 states per
  *     segment and head, and one bf16 value per token, head and channel): the
  *     segments run side by side and their states are stitched together exactly
