@@ -16,8 +16,9 @@
 //   correct o_t = o0_t + S_j^T q_eff_t   (S_t = M_t S_j + B_t, so
 //           o_t = S_t^T q_t = o0_t + S_j^T M_t^T q_t)
 //
-// Pass 1 runs 2 K x chains CTAs in one wave, so the wall time is about T / K
-// chunk-steps instead of T, plus the combine and the correction.
+// Pass 1 runs 2 K x chains CTAs in one wave (2 K - 1 per chain for a call without
+// an initial state: the first segment needs no transition run), so the wall time
+// is about T / K chunk-steps instead of T, plus the combine and the correction.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -54,7 +55,7 @@ __global__ void kda_split_bounds_kernel(const int32_t *__restrict__ cu, int32_t 
   seg_cu[i] = (int32_t)(a + off);
 }
 
-// One CTA per (sequence, head, 32-column block of the state): the columns of
+// One CTA per (sequence, head, 16-column block of the state): the columns of
 // S evolve independently under S <- M S + B.  start[s K + j] receives S_j
 // (j < K) and end[s] the composed S_K, each when non-null.
 constexpr int kCols = 16;          // columns of S per CTA (columns evolve independently)
@@ -121,8 +122,9 @@ kda_split_combine_kernel(const float *__restrict__ init, const float *__restrict
 // out[t, h] += S_jᵀ q_eff[t, h] for the tokens t of segment j: the correction
 // that turns the zero-start outputs o⁰_t into the true ones,
 // o_t = o⁰_t + (M_t S_j)ᵀ q_t with q_eff = M_tᵀ q_t.  One CTA per (segment,
-// 64-token tile, head): block x = j * tiles + tile (tiles: a bound on any
-// segment's tile count; CTAs past their segment's end return).  Warp MMAs with
+// kCorrTilesPerCta consecutive 64-token tiles, head), which converts S_j once:
+// block x = j * ctas_per_seg + c (ctas_per_seg: a bound on any segment's tile
+// count over kCorrTilesPerCta; CTAs and tiles past their segment's end stop).  Warp MMAs with
 // bf16 operands (S_j rounded like the state operands of the prefill), fp32
 // accumulation; `skip_first` leaves segment 0 of every sequence alone (its
 // start state is zero).
