@@ -23,6 +23,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -94,11 +95,11 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu_index = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        fd, self.path = tempfile.mkstemp(prefix=f"kda_clocks_{gpu_index}_", suffix=".csv")
+        os.close(fd)
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}",
@@ -135,6 +136,10 @@ class ClockSampler:
             for name, val in zip(names, f[5:9]):
                 if val.lower() == "active":
                     reasons.add(name)
+        try:
+            os.unlink(self.path)
+        except OSError:
+            pass
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
@@ -320,50 +325,135 @@ def few_chains_bench(dev, peaks, steps: int = 20, warmup: int = 3, T: int = 6553
     fin = torch.empty(1, H, 128, 128, device=dev)
     res = {"workload": f"one sequence of {T} tokens x {H} heads, bf16"}
     stream = torch.cuda.current_stream()
-    saved = {k: os.environ.get(k) for k in ("KDA_CHUNK_SPLIT", "KDA_CHUNK_HELPERS")}
-    variants = (("plain", {"KDA_CHUNK_SPLIT": "0", "KDA_CHUNK_HELPERS": "0"}),
-                ("helpers", {"KDA_CHUNK_SPLIT": "0", "KDA_CHUNK_HELPERS": None}),
-                ("split", {"KDA_CHUNK_SPLIT": None, "KDA_CHUNK_HELPERS": None}))
-    try:
-        for name, env in variants:
-            for k, v in env.items():
-                if v is None:
-                    os.environ.pop(k, None)
-                else:
-                    os.environ[k] = v
-            ws = torch.empty(kda.kda_chunk_fwd_workspace_size(1, T, H, dtype=kda.KDA_BF16),
-                             dtype=torch.uint8, device=dev)
+    ws = torch.empty(kda.kda_chunk_fwd_workspace_size(1, T, H, dtype=kda.KDA_BF16),
+                     dtype=torch.uint8, device=dev)
+    # (max_split, max_helpers) of kda_chunk_fwd_sched; None: the library's choice
+    variants = (("plain", (0, 0)), ("helpers", (0, None)), ("split", (None, None)))
+    for name, (max_split, max_helpers) in variants:
 
-            def run():
-                kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], None,
-                                  x["cu_seqlens"], out=out, final_state=fin, workspace=ws)
+        def run():
+            kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], None,
+                              x["cu_seqlens"], out=out, final_state=fin, workspace=ws,
+                              max_split=max_split, max_helpers=max_helpers)
 
-            for _ in range(warmup):
-                run()
-            torch.cuda.synchronize()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for _ in range(steps):
-                run()
-            b.record(stream)
-            torch.cuda.synchronize()
-            ms = a.elapsed_time(b) / steps
-            pub, used = kda.kda_read_chunk_stats(ws)
-            gbs = prefill_bytes(x, H) / (ms / 1000.0) / 1e9
-            res[name] = {"tokens_per_s": T / (ms / 1000.0), "ms_per_launch": ms,
-                         "hbm_frac": gbs / peaks["hbm_gbs"]}
-            if name == "helpers":
-                res[name].update({"chunks_from_helpers": used, "packages_published": pub,
-                                  "chunks": H * ((T + 63) // 64)})
-    finally:
-        for k, v in saved.items():
-            if v is None:
-                os.environ.pop(k, None)
-            else:
-                os.environ[k] = v
+        for _ in range(warmup):
+            run()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            run()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / steps
+        pub, used = kda.kda_read_chunk_stats(ws)
+        gbs = prefill_bytes(x, H) / (ms / 1000.0) / 1e9
+        res[name] = {"tokens_per_s": T / (ms / 1000.0), "ms_per_launch": ms,
+                     "hbm_frac": gbs / peaks["hbm_gbs"]}
+        if name == "helpers":
+            res[name].update({"chunks_from_helpers": used, "packages_published": pub,
+                              "chunks": H * ((T + 63) // 64)})
     for name in ("helpers", "split"):
         res[name]["speedup_vs_plain"] = res["plain"]["ms_per_launch"] / res[name]["ms_per_launch"]
-    del x, out, fin
+    del x, out, fin, ws
+    return res
+
+
+def prefill_config_bench(dev, peaks, workload: str, steps: int, warmup: int = 3):
+    """One prefill workload timed on its own (CUDA events over `steps` launches
+    after `warmup`), with its roofline: the bytes of SURVEY's per-token-head
+    count (bf16 q, k, v, out, fp32 log_alpha and beta) plus the states read
+    and written, against the measured HBM copy peak."""
+    import torch
+    from gated_delta_rule_13_gb300 import inputs, kda
+    w = inputs.WORKLOADS[workload]
+    x = inputs.workload_inputs(workload, device=dev)
+    n_tok, H = int(x["q"].shape[0]), w.H
+    n_seqs = len(x["lengths"])
+    out = torch.empty(n_tok, H, 128, dtype=torch.bfloat16, device=dev)
+    fin = torch.empty(n_seqs, H, 128, 128, dtype=torch.float32, device=dev)
+    ws = torch.zeros(kda.kda_chunk_fwd_workspace_size(n_seqs, n_tok, H), dtype=torch.uint8,
+                     device=dev)
+
+    def run():
+        kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["init_state"],
+                          x["cu_seqlens"], out=out, final_state=fin, workspace=ws)
+
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        run()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ok = kda.kda_read_device_status(ws) == kda.KDA_OK
+    ms = a.elapsed_time(b) / steps
+    nbytes = prefill_bytes(x, H)
+    gbs = nbytes / (ms / 1000.0) / 1e9
+    flop = n_tok * H * PREFILL_FLOP_PER_TOKEN_HEAD
+    res = {"workload": f"{workload}: {w.note}", "tokens": n_tok, "heads": H,
+           "tokens_per_s": n_tok / (ms / 1000.0), "ms_per_launch": ms, "launches": steps,
+           "device_status_ok": ok,
+           "roofline": {"bound": "hbm", "kernel": "kda_chunk_fwd_tc_kernel", "achieved": gbs,
+                        "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                        "traffic": recorded_traffic("kda_chunk_fwd_tc_kernel", "kda_chunk_tc.cu",
+                                                    workload),
+                        "bytes_per_launch": nbytes,
+                        "tensor_frac": flop / (ms / 1000.0) / 1e12 / peaks["bf16_tflops"]}}
+    del x, out, fin, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def decode_sequence_bench(dev, peaks, steps: int = 100, warmup_steps: int = 3, seed: int = 0):
+    """The decode workload as specified: 512 sequences x 96 heads, `steps`
+    consecutive steps, each with fresh inputs, the fp32 state advanced in place
+    by every step.  CUDA events around every step; algorithmic bytes per step:
+    each state read and written once plus the token's q, k, v, log_alpha, beta
+    and output."""
+    import torch
+    from gated_delta_rule_13_gb300 import inputs, kda
+    dw = inputs.WORKLOADS["decode_b512_h96"]
+    d = inputs.decode_inputs(B=dw.B, H=dw.H, steps=steps, dtype=dw.dtype, device=dev, seed=seed)
+    state = d["state"]
+    out = torch.empty(dw.B, dw.H, 128, dtype=torch.bfloat16, device=dev)
+
+    def step(s):
+        kda.kda_decode_step(state, d["q"][s], d["k"][s], d["v"][s], d["log_alpha"][s],
+                            d["beta"][s], out=out)
+
+    for s in range(warmup_steps):          # warm-up on a copy of the state
+        st0 = state.clone()
+        step(s)
+        state.copy_(st0)
+        del st0
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for s in range(steps):
+        step(s)
+        ev[s + 1].record(stream)
+    torch.cuda.synchronize()
+    per = [ev[s].elapsed_time(ev[s + 1]) for s in range(steps)]
+    ms = sum(per) / steps
+    nbytes = dw.B * dw.H * DECODE_BYTES_PER_UNIT
+    gbs = nbytes / (ms / 1000.0) / 1e9
+    res = {"value": gbs, "unit": "GB/s", "ms_per_step": ms,
+           "ms_per_step_median": statistics.median(per), "ms_per_step_max": max(per),
+           "steps_in_sequence": steps, "tokens_per_s": dw.B / (ms / 1000.0),
+           "workload": f"decode_b512_h96: {dw.note}; fresh inputs each step, "
+                       f"{steps * d['q'][0].numel() * 2 * 3 / 1e9:.1f} GB of q, k, v in HBM",
+           "roofline": {"bound": "hbm", "kernel": "kda_decode_step_kernel", "achieved": gbs,
+                        "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                        "traffic": recorded_traffic("kda_decode_step_kernel", "kda_decode.cu",
+                                                    "decode_b512_h96"),
+                        "bytes_per_launch": nbytes}}
+    del d, state, out
+    torch.cuda.empty_cache()
     return res
 
 
@@ -399,7 +489,7 @@ def run_gpu(args):
     ws = torch.zeros(kda.kda_chunk_fwd_workspace_size(len(x["lengths"]), n_tok, H),
                      dtype=torch.uint8, device=dev)
     dw = inputs.WORKLOADS["decode_b512_h96"]
-    n_dec_steps = 4
+    n_dec_steps = args.warmup + args.steps     # fresh decode inputs for every step
     d = inputs.decode_inputs(B=dw.B, H=dw.H, steps=n_dec_steps, dtype=dw.dtype, device=dev,
                              seed=rank)
     state = d["state"]
@@ -490,11 +580,22 @@ def run_gpu(args):
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
         del host, dev_bufs
 
+    pbytes = prefill_bytes(x, H)
+    del x, out, fin, ws, d, state, dout
+    torch.cuda.empty_cache()
+    decode_seq = decode_sequence_bench(dev, peaks, steps=args.decode_steps, seed=rank)
     replay = replay_bench(dev, peaks, steps=args.sub_steps)
     few_chains = few_chains_bench(dev, peaks, steps=args.sub_steps)
     layer_ops = layer_ops_bench(dev, peaks, steps=args.sub_steps, T=args.layer_tokens)
+    configs = {}
+    for wl, n in (("b4_h16_t4096", args.sub_steps), ("varlen_h96_1m", args.varlen_steps)):
+        if n > 0:
+            configs[wl] = prefill_config_bench(dev, peaks, wl, steps=n)
     if world > 1:
         replay["ms_per_launch"], = max_over_ranks([replay["ms_per_launch"]], world, dev)
+        decode_seq["ms_per_step"], = max_over_ranks([decode_seq["ms_per_step"]], world, dev)
+        for c in configs.values():
+            c["ms_per_launch"], = max_over_ranks([c["ms_per_launch"]], world, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -505,7 +606,6 @@ def run_gpu(args):
 
     if rank != 0:
         return 0
-    pbytes = prefill_bytes(x, H)
     pflop = n_tok * H * PREFILL_FLOP_PER_TOKEN_HEAD
     achieved_gbs = pbytes / (pre_avg / 1000.0) / 1e9
     dbytes = dw.B * dw.H * DECODE_BYTES_PER_UNIT
@@ -530,14 +630,11 @@ def run_gpu(args):
                      "ms_per_launch": pre_avg,
                      "tensor_tflops": pflop / (pre_avg / 1000.0) / 1e12,
                      "tensor_frac": pflop / (pre_avg / 1000.0) / 1e12 / peaks["bf16_tflops"]},
-        "decode": {"value": dec_gbs, "unit": "GB/s", "ms_per_step": dec_avg,
-                   "tokens_per_s": dw.B / (dec_avg / 1000.0),
-                   "roofline": {"bound": "hbm", "kernel": "kda_decode_step_kernel",
-                                "achieved": dec_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                "frac": dec_gbs / peaks["hbm_gbs"],
-                                "traffic": recorded_traffic("kda_decode_step_kernel",
-                                                            "kda_decode.cu", "decode_b512_h96"),
-                                "bytes_per_launch": dbytes}},
+        "decode": dict(decode_seq, in_step={
+            "ms_per_step": dec_avg, "value": dec_gbs, "unit": "GB/s",
+            "frac": dec_gbs / peaks["hbm_gbs"],
+            "note": "the decode step inside each timed step, after the prefill"}),
+        "prefill_configs": configs,
         "replay": replay,
         "prefill_few_chains": few_chains,
         "layer_ops": layer_ops,
@@ -571,6 +668,10 @@ def main():
                     help="timed launches of the replay and per-token-step sub-benchmarks")
     ap.add_argument("--layer-tokens", type=int, default=32768,
                     help="tokens of the per-token-step sub-benchmark (96 heads)")
+    ap.add_argument("--decode-steps", type=int, default=100,
+                    help="consecutive in-place steps of the decode sub-benchmark")
+    ap.add_argument("--varlen-steps", type=int, default=5,
+                    help="timed launches of the million-token varlen prefill (0: skip it)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

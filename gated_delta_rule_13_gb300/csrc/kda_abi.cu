@@ -2,7 +2,6 @@
 // and dispatch to the kernels.  See include/kda.h for the contract.
 #include <cuda_runtime.h>
 #include <stdint.h>
-#include <stdlib.h>
 #include <string.h>
 
 #include <vector>
@@ -43,9 +42,9 @@ size_t base_workspace_bytes(int32_t n_seqs) {
 // SMs the chains leave idle, when they are at least four times as many as the
 // chains.  With fewer, the helpers cover too few chunks to repay what the
 // protocol costs the chain CTAs (measured on a GB300 with 152 SMs: 8 chains
-// 1.22x faster, 24 chains 1.06x, 32 chains 0.97x, 96 chains 0.78x).  The
-// environment variable KDA_CHUNK_HELPERS caps the count (0 turns helpers off).
-int32_t help_ctas(int64_t chains, int dtype) {
+// 1.22x faster, 24 chains 1.06x, 32 chains 0.97x, 96 chains 0.78x).  A
+// non-negative `cap` (the caller's max_helpers) caps the count; 0 turns helpers off.
+int32_t help_ctas(int64_t chains, int dtype, int32_t cap = -1) {
   if (dtype != KDA_BF16 || chains <= 0) return 0;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -54,10 +53,7 @@ int32_t help_ctas(int64_t chains, int dtype) {
     return 0;
   }
   int64_t n = sms - chains < 4 * chains ? 0 : sms - chains;
-  if (const char *env = getenv("KDA_CHUNK_HELPERS")) {
-    const long cap = strtol(env, nullptr, 10);
-    if (cap >= 0 && cap < n) n = cap;
-  }
+  if (cap >= 0 && cap < n) n = cap;
   return n > 0 ? (int32_t)n : 0;
 }
 
@@ -66,9 +62,10 @@ int32_t help_ctas(int64_t chains, int dtype) {
 // initial state (the first segment then needs no transition run), and takes
 // about T / K chunk-steps (plus a combine and an output correction), so it needs
 // (2 K or 2 K - 1) x chains <= SMs and pays off from K = 2 on; segments are kept
-// at two chunks or more on average.  The environment variable KDA_CHUNK_SPLIT
-// caps K (0 turns the split off).
-int32_t split_factor(int32_t n_seqs, int64_t n_tokens, int32_t H, int dtype, bool zero_init) {
+// at two chunks or more on average.  A non-negative `cap` (the caller's
+// max_split) caps K; 0 turns the split off.
+int32_t split_factor(int32_t n_seqs, int64_t n_tokens, int32_t H, int dtype, bool zero_init,
+                     int32_t cap = -1) {
   const int64_t chains = (int64_t)n_seqs * H;
   if (dtype != KDA_BF16 || chains <= 0 || n_tokens <= 0) return 0;
   int dev = 0, sms = 0;
@@ -81,10 +78,7 @@ int32_t split_factor(int32_t n_seqs, int64_t n_tokens, int32_t H, int dtype, boo
   int64_t k = zero_init ? (sms + chains) / (2 * chains) : sms / (2 * chains);
   const int64_t by_length = n_tokens / ((int64_t)n_seqs * 2 * kda::kChunk);
   if (by_length < k) k = by_length;
-  if (const char *env = getenv("KDA_CHUNK_SPLIT")) {
-    const long cap = strtol(env, nullptr, 10);
-    if (cap >= 0 && cap < k) k = cap;
-  }
+  if (cap >= 0 && cap < k) k = cap;
   return k >= 2 ? (int32_t)k : 0;
 }
 
@@ -97,17 +91,15 @@ size_t order_bytes(int32_t n_seqs, int dtype) {
   return (dtype == KDA_BF16 && n_seqs > 1) ? round_up(sizeof(int32_t) * (size_t)n_seqs, 1024) : 0;
 }
 
-// Full workspace: the base part, the sequence order, then the scratch of the
-// in-device split, or (when helpers would run instead) the helper header and ring.
+// Full workspace: the base part, the sequence order, then the larger of the
+// scratch of the in-device split (without an initial state: the most segments)
+// and the helper header and ring, so that any schedule a caller picks fits.
 size_t workspace_bytes_for(int32_t n_seqs, int64_t n_tokens, int32_t H, int dtype) {
   const int64_t chains = (int64_t)n_seqs * H;
   size_t b = base_workspace_bytes(n_seqs) + order_bytes(n_seqs, dtype);
-  // the larger of the schedules a call may take: the split without an initial
-  // state (the most segments), else with one, else the helpers
   const int32_t k_zero = split_factor(n_seqs, n_tokens, H, dtype, true);
-  const int32_t k_init = split_factor(n_seqs, n_tokens, H, dtype, false);
   size_t extra = k_zero > 0 ? kda::split_workspace_bytes(n_seqs, n_tokens, H, k_zero) : 0;
-  if (k_init == 0 && help_ctas(chains, dtype) > 0 && help_workspace_bytes(chains) > extra)
+  if (help_ctas(chains, dtype) > 0 && help_workspace_bytes(chains) > extra)
     extra = help_workspace_bytes(chains);
   return b + extra;
 }
@@ -158,6 +150,17 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
                   int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk, int32_t dv,
                   int dtype, void *out, float *final_state, void *workspace,
                   size_t workspace_bytes, void *stream) {
+  return kda_chunk_fwd_sched(q, k, v, log_alpha, beta, init_state, cu_seqlens, n_seqs, n_tokens,
+                             H, dk, dv, dtype, out, final_state, -1, -1, workspace,
+                             workspace_bytes, stream);
+}
+
+int kda_chunk_fwd_sched(const void *q, const void *k, const void *v, const float *log_alpha,
+                        const float *beta, const float *init_state, const int32_t *cu_seqlens,
+                        int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk, int32_t dv,
+                        int dtype, void *out, float *final_state, int32_t max_split,
+                        int32_t max_helpers, void *workspace, size_t workspace_bytes,
+                        void *stream) {
   // ---- host-side validation: nothing is launched unless all of it passes
   if (n_seqs < 0 || n_tokens < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
   const int d = check_dims(dk, dv, dtype);
@@ -209,6 +212,7 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
   a.H = H; a.out = out; a.final_state = final_state; a.status = status;
   a.help_ws = nullptr;
   a.n_help = 0;
+  a.test_control = reinterpret_cast<kda::TestControl *>(ws + kda::kTestControlOffset);
   const int64_t chains = (int64_t)n_seqs * H;
   // Longest sequences first, when the workspace has room for their order.
   const size_t ob = order_bytes(n_seqs, dtype);
@@ -217,7 +221,8 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
     need += ob;
   }
   // The in-device split, when it applies and the workspace has its scratch.
-  const int32_t n_split = split_factor(n_seqs, n_tokens, H, dtype, init_state == nullptr);
+  const int32_t n_split =
+      split_factor(n_seqs, n_tokens, H, dtype, init_state == nullptr, max_split);
   if (n_split > 0 && workspace_bytes >= need + kda::split_workspace_bytes(n_seqs, n_tokens, H, n_split)) {
     const cudaError_t e = kda::launch_chunk_fwd_split(a, n_split, ws + need, st);
     if (e == cudaErrorNotSupported) return KDA_ERR_UNSUPPORTED;
@@ -225,7 +230,7 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
   }
   // Helpers run when the workspace has room for their ring (a workspace sized by
   // kda_chunk_fwd_workspace_size on this device does); their header starts zeroed.
-  const int32_t n_help = help_ctas(chains, dtype);
+  const int32_t n_help = help_ctas(chains, dtype, max_helpers);
   if (n_help > 0 && n_tokens > 0 && workspace_bytes >= need + help_workspace_bytes(chains)) {
     a.help_ws = ws + need;
     a.n_help = n_help;
@@ -254,6 +259,50 @@ int kda_read_device_status(void *workspace, void *stream, int clear, int32_t *de
     return KDA_ERR_CUDA;
   }
   *device_status = host.code;
+  return KDA_OK;
+}
+
+int kda_read_device_status_detail(void *workspace, void *stream, int clear,
+                                  int32_t *detail4) {
+  if (!workspace || !detail4) return KDA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  kda::DeviceStatus host;
+  if (cudaStreamSynchronize(st) != cudaSuccess ||
+      cudaMemcpy(&host, workspace, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_CUDA;
+  }
+  if (clear && cudaMemset(workspace, 0, sizeof(host)) != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_CUDA;
+  }
+  detail4[0] = host.code;
+  detail4[1] = host.detail;
+  detail4[2] = host.chain;
+  detail4[3] = host.chunk;
+  return KDA_OK;
+}
+
+int kda_test_arm_timeout(void *workspace, int32_t chain, int32_t chunk, uint32_t wait_us,
+                         void *stream) {
+  if (!workspace || !aligned16(workspace)) return KDA_ERR_INVALID_ARG;
+  kda::TestControl c;
+  memset(&c, 0, sizeof(c));
+  if (chain >= 0) {
+    if (chunk < 0 || wait_us < 1 || wait_us > 2000000) return KDA_ERR_INVALID_ARG;
+    c.magic0 = kda::kTestMagic0;
+    c.magic1 = kda::kTestMagic1;
+    c.chain = chain;
+    c.chunk = chunk;
+    c.wait_us = wait_us;
+  }
+  unsigned char *dst = static_cast<unsigned char *>(workspace) + kda::kTestControlOffset;
+  if (cudaMemcpyAsync(dst, &c, sizeof(c), cudaMemcpyHostToDevice,
+                      static_cast<cudaStream_t>(stream)) != cudaSuccess ||
+      cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_CUDA;
+  }
   return KDA_OK;
 }
 

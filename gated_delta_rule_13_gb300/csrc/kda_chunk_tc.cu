@@ -116,6 +116,8 @@ struct Misc {
   uint64_t bar_wb;              // helper: the package has been read out of shared memory
   uint32_t tmem_base;
   int abort;
+  int test_chunk;               // chunk whose Gram-operand arrival a test withholds (-1: none)
+  uint64_t wait_ns;             // bound on any single wait of this CTA
   int32_t plan[2];              // chain CTA: 1 if that chunk's package comes from a helper
   HelpClaim claim[2];           // helper CTA: the chunk being built / the next one
   // Per copy barrier (TMA_*): phase index + 1 of the last phase that carried a
@@ -237,13 +239,14 @@ struct Ctx {
   int chain;
 };
 
-// Bounded mbarrier wait; on timeout records KDA_ERR_TIMEOUT and raises the abort
-// flag.  Compute warps test the flag only through compute_sync_abort, so they
-// all leave the chunk loop at the same point; the MMA thread leaves its loop at
-// the failed wait.
+// Bounded mbarrier wait (kWaitNs, or a test's shorter bound); on timeout records
+// KDA_ERR_TIMEOUT and raises the abort flag.  Compute warps test the flag only
+// through compute_sync_abort, so they all leave the chunk loop at the same point;
+// the MMA thread leaves its loop at the failed wait.
 __device__ bool wait_bar(const Ctx &x, uint64_t *bar, uint32_t parity, int where, int chunk,
                          bool poll = false) {
-  if (poll ? mbar_wait_poll(bar, parity, kWaitNs) : mbar_wait(bar, parity, kWaitNs)) return true;
+  const uint64_t limit = *reinterpret_cast<const volatile uint64_t *>(&x.m->wait_ns);
+  if (poll ? mbar_wait_poll(bar, parity, limit) : mbar_wait(bar, parity, limit)) return true;
   record_status(x.status, KDA_ERR_TIMEOUT, where, x.chain, chunk);
   atomicExch(&x.m->abort, 1);
   return false;
@@ -284,7 +287,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const int32_t *__restrict__ seq_order,
                         const __grid_constant__ CUtensorMap tm_om,
                         __nv_bfloat16 *__restrict__ out_m, const int write_out,
-                        const int split_k) {
+                        const int split_k, TestControl *test_control) {
   // Indexing the __shared__ array directly (no integer round trip) keeps every
   // access a shared-memory instruction.  The 128-byte swizzle atoms need a
   // 1024-byte aligned base, checked below.
@@ -351,6 +354,17 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     fence_mbarrier_init();
     m.abort = 0;
     for (int i = 0; i < 5; ++i) m.last_copy[i] = 0;
+    m.test_chunk = -1;
+    m.wait_ns = kWaitNs;
+    if (kMode == kModePlain && test_control != nullptr && !helper) {
+      const volatile TestControl *c = test_control;
+      if (c->magic0 == kTestMagic0 && c->magic1 == kTestMagic1 && c->chain == chain) {
+        m.test_chunk = c->chunk;
+        m.wait_ns = 1000ull * c->wait_us;
+        test_control->magic0 = 0;   // one shot
+        test_control->magic1 = 0;
+      }
+    }
   }
   if (warp == 0) {
     tmem_alloc(&m.tmem_base, TM_COLS);
@@ -363,6 +377,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   }
   cta_sync();
   const uint32_t tm = m.tmem_base;
+  const int test_chunk = kMode == kModePlain ? m.test_chunk : -1;
 
   if (warp >= kComputeWarps) {
     // ===================== TMA + MMA issue (one thread) =====================
@@ -824,7 +839,9 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         kc2s[j] = kc2;
       }
       fence_proxy_async_smem();
-      warp_arrive(&m.bar_gops, lane);
+      // (a test may withhold warp 0's arrival, so that the issue thread's wait
+      // on these operands gives up)
+      if (kMode != kModePlain || !(warp == 0 && ci == test_chunk)) warp_arrive(&m.bar_gops, lane);
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const uint32_t o = (uint32_t)j * 128u + swzk[j & 7];
@@ -1400,7 +1417,8 @@ cudaError_t launch_chunk_fwd_bf16_tc(const ChunkArgs &a, cudaStream_t stream) {
       static_cast<__nv_bfloat16 *>(a.out), a.final_state, a.status, help, a.final_state_m,
       seq_order, transitions && a.out_m ? mom : mo,
       static_cast<__nv_bfloat16 *>(transitions && a.out_m ? a.out_m : a.out),
-      transitions ? (a.write_out ? 1 : 0) : 1, transitions ? a.split_skip_k : 0);
+      transitions ? (a.write_out ? 1 : 0) : 1, transitions ? a.split_skip_k : 0,
+      (!transitions && n_help == 0) ? a.test_control : nullptr);
   return cudaGetLastError();
 }
 

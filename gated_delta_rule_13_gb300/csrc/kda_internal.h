@@ -23,6 +23,25 @@ struct DeviceStatus {
   int32_t help_consumed;   // of those, the ones a chain CTA used
 };
 
+// Test control of the bf16 prefill, at kTestControlOffset inside the status
+// block (not cleared by a call).  When both magic words are set, the chain CTA
+// `chain` of the next plain launch waits at most `wait_us` microseconds on any
+// barrier, one of its compute warps withholds its arrival on the "Gram operands
+// built" barrier of chunk `chunk`, and the CTA clears the magic words (one
+// shot).  The wait that can then never complete gives up and records
+// KDA_ERR_TIMEOUT, which is how the tests exercise the timeout path without
+// faulting or hanging anything.
+constexpr size_t kTestControlOffset = 128;
+constexpr uint64_t kTestMagic0 = 0x4b44412d74657374ull, kTestMagic1 = 0x74696d656f75742eull;
+struct TestControl {
+  uint64_t magic0, magic1;
+  int32_t chain, chunk;
+  uint32_t wait_us;
+  int32_t pad;
+};
+static_assert(sizeof(DeviceStatus) <= kTestControlOffset, "status block layout");
+static_assert(kTestControlOffset + sizeof(TestControl) <= kStatusBytes, "status block layout");
+
 // Helper CTAs of the tensor-core prefill.  When a call has fewer chains than the
 // GPU has SMs, the idle SMs run "helpers" that compute the state-independent
 // half of chunks ahead of the chain CTAs: the operand build, the Gram matrix,
@@ -85,6 +104,8 @@ struct ChunkArgs {
   // first segment starts from a zero state, so it gets no transition run (its
   // M_0 and out_m rows are not written).  0: every chain gets one.
   int32_t split_skip_k = 0;
+  // Test control in the status block (kPlain launches of the bf16 kernel), or nullptr.
+  TestControl *test_control = nullptr;
 };
 
 cudaError_t launch_decode_step(float *state, const void *q, const void *k, const void *v,

@@ -22,6 +22,14 @@
 //     that first call before any stream capture begins.
 //   * At most kda::kNoAllocMaxSeqs sequences per call; larger calls return
 //     KDA_ERR_WORKSPACE without launching anything.
+//   * The array has no room for the scratch of the in-device split, the helper
+//     ring or the longest-first sequence order, so this entry point always
+//     runs the plain schedule (one CTA per sequence and head, in index order).
+//     Its results equal kda_chunk_fwd's bitwise where kda_chunk_fwd takes the
+//     plain or helper schedule, and within the same tolerance where it splits.
+//   * Kernel-recorded errors (a malformed device cu_seqlens, a bounded wait
+//     that gave up) land in the array's status block; kda_noalloc_read_status
+//     reads them without allocating.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -62,6 +70,14 @@ cudaError_t scratch_address(void **ptr) {
 
 }  // namespace
 }  // namespace kda
+
+extern "C" int kda_noalloc_read_status(void *stream, int clear, int32_t *device_status) {
+  if (!device_status) return KDA_ERR_INVALID_ARG;
+  void *scratch = nullptr;
+  if (kda::scratch_address(&scratch) != cudaSuccess) return KDA_ERR_CUDA;
+  // The status block sits at the start of the scratch, as in a workspace.
+  return kda_read_device_status(scratch, stream, clear, device_status);
+}
 
 extern "C" int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
                                      const float *log_alpha, const float *beta,

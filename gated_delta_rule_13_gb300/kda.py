@@ -28,9 +28,11 @@ HEAD_DIM = 128
 
 # Symbols declared in include/kda.h.
 EXPORTED = ("kda_status_string", "kda_version", "kda_chunk_fwd_workspace_size",
-            "kda_chunk_fwd", "kda_read_device_status", "kda_decode_step",
-            "kda_chunk_fwd_noalloc", "kda_decode_replay", "kda_prep_fwd", "kda_post_fwd",
-            "kda_read_chunk_stats", "kda_chunk_fwd_transitions", "kda_state_combine")
+            "kda_chunk_fwd", "kda_chunk_fwd_sched", "kda_read_device_status",
+            "kda_read_device_status_detail", "kda_test_arm_timeout", "kda_decode_step",
+            "kda_chunk_fwd_noalloc", "kda_noalloc_read_status", "kda_decode_replay",
+            "kda_prep_fwd", "kda_post_fwd", "kda_read_chunk_stats", "kda_chunk_fwd_transitions",
+            "kda_state_combine")
 
 _lib = None
 
@@ -64,8 +66,17 @@ def library() -> ctypes.CDLL:
         lib.kda_chunk_fwd.restype = ctypes.c_int
         lib.kda_chunk_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32,
                                       ctypes.c_int, vp, vp, vp, sz, vp]
+        lib.kda_chunk_fwd_sched.restype = ctypes.c_int
+        lib.kda_chunk_fwd_sched.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32,
+                                            ctypes.c_int, vp, vp, i32, i32, vp, sz, vp]
         lib.kda_read_device_status.restype = ctypes.c_int
         lib.kda_read_device_status.argtypes = [vp, vp, ctypes.c_int, ctypes.POINTER(i32)]
+        lib.kda_read_device_status_detail.restype = ctypes.c_int
+        lib.kda_read_device_status_detail.argtypes = [vp, vp, ctypes.c_int, ctypes.POINTER(i32)]
+        lib.kda_test_arm_timeout.restype = ctypes.c_int
+        lib.kda_test_arm_timeout.argtypes = [vp, i32, i32, ctypes.c_uint32, vp]
+        lib.kda_noalloc_read_status.restype = ctypes.c_int
+        lib.kda_noalloc_read_status.argtypes = [vp, ctypes.c_int, ctypes.POINTER(i32)]
         lib.kda_read_chunk_stats.restype = ctypes.c_int
         lib.kda_read_chunk_stats.argtypes = [vp, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]
         lib.kda_chunk_fwd_transitions.restype = ctypes.c_int
@@ -143,11 +154,14 @@ def kda_chunk_fwd_workspace_size(n_seqs: int, n_tokens: int, H: int, dk: int = H
 
 
 def kda_chunk_fwd(q, k, v, log_alpha, beta, init_state=None, cu_seqlens=None, *, out=None,
-                  final_state=None, workspace=None, output_final_state=True, stream=None):
+                  final_state=None, workspace=None, output_final_state=True, max_split=None,
+                  max_helpers=None, stream=None):
     """Chunked KDA prefill.  q, k ``[N, H, 128]`` and v ``[N, H, 128]`` (bf16 or
     fp32, same dtype); log_alpha ``[N, H, 128]`` fp32; beta ``[N, H]`` fp32;
     init_state ``[n_seqs, H, 128, 128]`` fp32 or None; cu_seqlens int32
     ``[n_seqs + 1]`` (CUDA or CPU tensor) or None for one sequence.
+    ``max_split`` / ``max_helpers`` cap the schedule (``kda_chunk_fwd_sched``;
+    None: the library's choice, 0: off).
     Returns ``(out, final_state)`` (final_state None if not requested)."""
     _need_cuda("q", q)
     N, H, dk = q.shape
@@ -179,12 +193,16 @@ def kda_chunk_fwd(q, k, v, log_alpha, beta, init_state=None, cu_seqlens=None, *,
         # the library clears what it reads (status block, helper header) itself
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     _need_cuda("workspace", workspace)
-    rc = library().kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
-                                 _ptr(init_state), _ptr(cu_seqlens), n_seqs, N, H, dk, dv,
-                                 code, _ptr(out), _ptr(final_state), _ptr(workspace),
-                                 workspace.numel() * workspace.element_size(),
-                                 _stream_handle(stream))
-    _check(rc, "kda_chunk_fwd")
+    ws_args = (_ptr(workspace), workspace.numel() * workspace.element_size(),
+               _stream_handle(stream))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(init_state),
+            _ptr(cu_seqlens), n_seqs, N, H, dk, dv, code, _ptr(out), _ptr(final_state))
+    if max_split is None and max_helpers is None:
+        _check(library().kda_chunk_fwd(*args, *ws_args), "kda_chunk_fwd")
+    else:
+        caps = (-1 if max_split is None else int(max_split),
+                -1 if max_helpers is None else int(max_helpers))
+        _check(library().kda_chunk_fwd_sched(*args, *caps, *ws_args), "kda_chunk_fwd_sched")
     return out, final_state
 
 
@@ -265,14 +283,16 @@ def _piece_bounds(n_tokens: int, piece_tokens: int, min_tail: int = 1024) -> lis
 
 
 def kda_chunk_fwd_host(q, k, v, log_alpha, beta, init_state=None, *, out=None,
-                       final_state=None, piece_tokens: int = 4096, device=None):
+                       final_state=None, piece_tokens: int = 4096, device=None,
+                       max_split=None, max_helpers=None):
     """Prefill of ONE sequence whose inputs are in host memory (pinned for the
     copies to overlap): the tokens go through in pieces of ``piece_tokens`` (a
     multiple of the 64-token chunk; the last one cut in halves down to 1024
     tokens), each piece's host-to-device copy overlapping the previous piece's
     prefill and the device-to-host copy of its outputs.
     Piece i starts from piece i-1's final state (fp32, exact), so the results
-    are those of one kda_chunk_fwd call.  Returns host ``(out, final_state)``."""
+    are those of one kda_chunk_fwd call (with the same schedule caps, which
+    every piece gets).  Returns host ``(out, final_state)``."""
     if piece_tokens <= 0 or piece_tokens % 64:
         raise ValueError("piece_tokens must be a positive multiple of 64")
     device = torch.device(device or "cuda")
@@ -316,7 +336,8 @@ def kda_chunk_fwd_host(q, k, v, log_alpha, beta, init_state=None, *, out=None,
         kda_chunk_fwd(dev["q"][p0:p1], dev["k"][p0:p1], dev["v"][p0:p1],
                       dev["log_alpha"][p0:p1], dev["beta"][p0:p1],
                       s0 if i == 0 else states[(i - 1) & 1], cu[n_tok], out=d_out[p0:p1],
-                      final_state=states[i & 1], workspace=ws)
+                      final_state=states[i & 1], workspace=ws, max_split=max_split,
+                      max_helpers=max_helpers)
         ev = torch.cuda.Event()
         ev.record(compute)
         done.append(ev)
@@ -343,7 +364,8 @@ def kda_chunk_fwd_noalloc(q, k, v, log_alpha, beta, init_state=None, cu_seqlens=
     _need_cuda("log_alpha", log_alpha, torch.float32, (N, H, dk))
     _need_cuda("beta", beta, torch.float32, (N, H))
     if cu_seqlens is None:
-        cu_seqlens = torch.tensor([0, N], dtype=torch.int32, device=q.device)
+        # host memory: the library copies it into its own array (no device allocation)
+        cu_seqlens = torch.tensor([0, N], dtype=torch.int32)
     n_seqs = cu_seqlens.shape[0] - 1
     if init_state is not None:
         _need_cuda("init_state", init_state, torch.float32, (n_seqs, H, dk, dv))
@@ -379,6 +401,36 @@ def kda_read_device_status(workspace, stream=None, clear: bool = True) -> int:
                                             1 if clear else 0, ctypes.byref(st)),
            "kda_read_device_status")
     return st.value
+
+
+def kda_read_device_status_detail(workspace, stream=None, clear: bool = True):
+    """As ``kda_read_device_status``, returning ``(code, detail, chain, chunk)``."""
+    _need_cuda("workspace", workspace)
+    d = (ctypes.c_int32 * 4)()
+    _check(library().kda_read_device_status_detail(_ptr(workspace), _stream_handle(stream),
+                                                   1 if clear else 0, d),
+           "kda_read_device_status_detail")
+    return tuple(int(x) for x in d)
+
+
+def kda_noalloc_read_status(stream=None, clear: bool = True) -> int:
+    """Device status recorded by the last ``kda_chunk_fwd_noalloc`` calls on the
+    current device (the library's fixed array; allocates nothing)."""
+    st = ctypes.c_int32(0)
+    _check(library().kda_noalloc_read_status(_stream_handle(stream), 1 if clear else 0,
+                                             ctypes.byref(st)),
+           "kda_noalloc_read_status")
+    return st.value
+
+
+def kda_test_arm_timeout(workspace, chain: int, chunk: int, wait_us: int = 1000, stream=None):
+    """Test control of the bounded waits (see include/kda.h): the next bf16
+    plain-schedule ``kda_chunk_fwd`` on ``workspace`` times out in chain
+    ``chain`` at chunk ``chunk``; ``chain < 0`` disarms."""
+    _need_cuda("workspace", workspace)
+    _check(library().kda_test_arm_timeout(_ptr(workspace), int(chain), int(chunk), int(wait_us),
+                                          _stream_handle(stream)),
+           "kda_test_arm_timeout")
 
 
 def kda_decode_step(state, q, k, v, log_alpha, beta, *, out=None, stream=None):

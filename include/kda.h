@@ -21,7 +21,9 @@
  *   - All tensor pointers are caller-owned DEVICE memory unless stated
  *     otherwise and C-contiguous.  Alignment: see each entry point (beta is
  *     always only element-aligned).  The library never allocates or frees
- *     device memory and keeps no global state.
+ *     device memory, reads no environment variables and keeps no global state
+ *     (the one exception, kda_chunk_fwd_noalloc's fixed device array, is
+ *     described there).
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL = legacy default stream).  Inputs must stay alive and unmodified
  *     until the stream has passed the call.
@@ -87,11 +89,13 @@ int kda_version(void);
  *     These run on the idle SMs and compute the state-independent half of
  *     later chunks (operand build, Gram matrix, triangular solve); about
  *     455 KiB per chain.
+ * The size covers every schedule kda_chunk_fwd_sched may be asked for.
  * kda_chunk_fwd runs without the split or the helpers when the workspace it
  * gets has room for neither.  Helpers leave the results bitwise unchanged; the
- * split changes the rounding (its results meet the same tolerances).  The
- * environment variables KDA_CHUNK_SPLIT and KDA_CHUNK_HELPERS cap the segment
- * and helper counts (0 turns either off).
+ * split changes the rounding (its results meet the same tolerances).  Because
+ * the schedule follows the device's SM count, kda_chunk_fwd's results can
+ * differ in rounding between GPUs with different SM counts; a caller that
+ * needs the same bits everywhere passes max_split = 0 to kda_chunk_fwd_sched.
  * Errors: KDA_ERR_INVALID_ARG for a NULL `bytes` or negative sizes,
  * KDA_ERR_UNSUPPORTED for dk/dv/dtype outside the supported set.
  */
@@ -146,11 +150,31 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
                   size_t workspace_bytes, void *stream);
 
 /*
+ * kda_chunk_fwd with the schedule capped by the caller.  Arguments, results
+ * and errors are those of kda_chunk_fwd, plus:
+ *   max_split    upper bound on the segments per sequence of the in-device
+ *                split (-1: the library's choice, as in kda_chunk_fwd;
+ *                0 or 1: never split);
+ *   max_helpers  upper bound on the helper CTAs (-1: the library's choice;
+ *                0: no helpers).
+ * kda_chunk_fwd(...) is kda_chunk_fwd_sched(..., -1, -1, ...).  The caps only
+ * lower what the library would pick for the device (they never force a
+ * schedule that does not fit), so every call stays within the workspace size
+ * kda_chunk_fwd_workspace_size reports.
+ */
+int kda_chunk_fwd_sched(const void *q, const void *k, const void *v, const float *log_alpha,
+                        const float *beta, const float *init_state, const int32_t *cu_seqlens,
+                        int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk, int32_t dv,
+                        int dtype, void *out, float *final_state, int32_t max_split,
+                        int32_t max_helpers, void *workspace, size_t workspace_bytes,
+                        void *stream);
+
+/*
  * kda_chunk_fwd without a workspace argument, for callers that cannot provide
  * or allocate device memory for the library: for instance a serving engine
  * whose framework allocator owns all device memory and forbids cudaMalloc or
  * extra buffers outside its pool.  (Library-level entry point: the pages have
- * no counterpart; it computes exactly what kda_chunk_fwd computes.)
+ * no counterpart.)
  *
  * Arguments and errors are those of kda_chunk_fwd minus the workspace.  The
  * scratch kda_chunk_fwd keeps in its workspace (device status block, device
@@ -166,13 +190,28 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, once per device); make that first call before
  *     any stream capture begins.
- *   - The device status recorded by the kernels stays in the library's array;
- *     it is not readable through this entry point.
+ *   - The array has no room for the in-device split, the helper ring or the
+ *     longest-first order, so the call always takes the plain schedule (one
+ *     CTA per sequence and head).  Results equal kda_chunk_fwd's bitwise where
+ *     kda_chunk_fwd takes the plain or helper schedule, and meet the same
+ *     tolerance where it splits; few-chain shapes run slower than there.
+ *   - Kernel-recorded errors (a malformed device cu_seqlens, a bounded wait
+ *     that gave up) go to the array's status block: the call itself returns
+ *     KDA_OK; read them with kda_noalloc_read_status.
  */
 int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *log_alpha,
                           const float *beta, const float *init_state, const int32_t *cu_seqlens,
                           int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk, int32_t dv,
                           int dtype, void *out, float *final_state, void *stream);
+
+/*
+ * The device status of the last kda_chunk_fwd_noalloc calls on the current
+ * device, read from the library's fixed array exactly as
+ * kda_read_device_status reads a workspace (synchronises `stream` first;
+ * `clear` non-zero resets it).  Allocates nothing.  No counterpart on the pages.
+ * Errors: KDA_ERR_INVALID_ARG (NULL device_status), KDA_ERR_CUDA.
+ */
+int kda_noalloc_read_status(void *stream, int clear, int32_t *device_status);
 
 /*
  * Reads (and, if `clear` is non-zero, resets) the device status word of a
@@ -182,6 +221,31 @@ int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const flo
  * Errors: KDA_ERR_INVALID_ARG (NULL workspace or device_status), KDA_ERR_CUDA.
  */
 int kda_read_device_status(void *workspace, void *stream, int clear, int32_t *device_status);
+
+/*
+ * As kda_read_device_status, with where the status was recorded:
+ * detail4[0] = code, detail4[1] = a kernel-specific tag of the failing step,
+ * detail4[2] = the chain (sequence * H + head), detail4[3] = the chunk index.
+ */
+int kda_read_device_status_detail(void *workspace, void *stream, int clear, int32_t *detail4);
+
+/*
+ * TEST CONTROL of the bounded waits (fault-handling tests only; the pages have
+ * no counterpart).  Arms `workspace` so that, in the next bf16 kda_chunk_fwd
+ * call that takes the plain schedule with it, the CTA of chain `chain`
+ * (sequence * H + head) bounds each of its waits by `wait_us` microseconds and
+ * one of its warps withholds its arrival on the barrier that releases chunk
+ * `chunk`'s Gram products.  The wait that then never completes gives up:
+ * the kernel records KDA_ERR_TIMEOUT with that chain and chunk in the device
+ * status, drains its copies and MMAs, frees its tensor memory and returns,
+ * leaving that chain's outputs from the chunk before on, and its final
+ * state, unwritten.  Nothing traps or waits without bound.  The control is
+ * consumed by the CTA that acts on it; chain < 0 disarms it.  Synchronises
+ * `stream`.  Errors: KDA_ERR_INVALID_ARG (NULL or misaligned workspace,
+ * chunk < 0 or wait_us outside [1, 2000000] when arming), KDA_ERR_CUDA.
+ */
+int kda_test_arm_timeout(void *workspace, int32_t chain, int32_t chunk, uint32_t wait_us,
+                         void *stream);
 
 /*
  * The affine state map of every packed sequence, for context parallelism

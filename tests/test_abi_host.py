@@ -32,10 +32,12 @@ def declared_functions():
 
 def test_header_declares_expected_entry_points():
     names = declared_functions()
-    for n in ("kda_chunk_fwd", "kda_decode_step", "kda_decode_replay", "kda_prep_fwd",
-              "kda_post_fwd", "kda_chunk_fwd_workspace_size",
-              "kda_status_string", "kda_read_device_status", "kda_read_chunk_stats",
-              "kda_chunk_fwd_transitions", "kda_state_combine", "kda_version"):
+    for n in ("kda_chunk_fwd", "kda_chunk_fwd_sched", "kda_decode_step", "kda_decode_replay",
+              "kda_prep_fwd", "kda_post_fwd", "kda_chunk_fwd_workspace_size",
+              "kda_status_string", "kda_read_device_status", "kda_read_device_status_detail",
+              "kda_read_chunk_stats", "kda_chunk_fwd_transitions", "kda_state_combine",
+              "kda_version", "kda_test_arm_timeout", "kda_chunk_fwd_noalloc",
+              "kda_noalloc_read_status"):
         assert n in names
 
 
@@ -82,6 +84,47 @@ def _fwd(lib, **over):
 ])
 def test_chunk_fwd_rejects_before_launch(lib, over, code):
     assert _fwd(lib, **over) == code
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), 1), (dict(H=0), 1), (dict(dk=64), 2), (dict(dtype=7), 2),
+    (dict(la=A + 0x3002), 1), (dict(ws=None), 3), (dict(ws_bytes=16), 3),
+])
+@pytest.mark.parametrize("caps", [(-1, -1), (0, 0), (4, 7)])
+def test_chunk_fwd_sched_rejects_before_launch(lib, over, code, caps):
+    """The schedule caps change nothing about argument checking."""
+    args = dict(q=A, k=A + 0x1000, v=A + 0x2000, la=A + 0x3000, beta=A + 0x4000, s0=None,
+                cu=A + 0x5000, n_seqs=2, n_tokens=100, H=4, dk=128, dv=128, dtype=1,
+                out=A + 0x6000, fin=None, ws=A + 0x7000, ws_bytes=1 << 20, stream=None)
+    args.update(over)
+    vp = ctypes.c_void_p
+    rc = lib.kda_chunk_fwd_sched(
+        vp(args["q"]), vp(args["k"]), vp(args["v"]), vp(args["la"]), vp(args["beta"]),
+        vp(args["s0"]), vp(args["cu"]), args["n_seqs"], args["n_tokens"], args["H"], args["dk"],
+        args["dv"], args["dtype"], vp(args["out"]), vp(args["fin"]), caps[0], caps[1],
+        vp(args["ws"]), args["ws_bytes"], vp(args["stream"]))
+    assert rc == code
+
+
+def test_no_environment_reads():
+    """The schedule is an argument: the library source reads no environment."""
+    csrc = os.path.join(ROOT, "gated_delta_rule_13_gb300", "csrc")
+    for f in os.listdir(csrc):
+        text = open(os.path.join(csrc, f), encoding="utf-8").read()
+        assert "getenv" not in text, f
+
+
+def test_test_control_and_status_readers_reject_bad_arguments(lib):
+    vp = ctypes.c_void_p
+    assert lib.kda_test_arm_timeout(None, 0, 0, 1000, None) == 1
+    assert lib.kda_test_arm_timeout(vp(A + 8), 0, 0, 1000, None) == 1       # misaligned
+    assert lib.kda_test_arm_timeout(vp(A), 0, -1, 1000, None) == 1          # chunk < 0
+    assert lib.kda_test_arm_timeout(vp(A), 0, 0, 0, None) == 1              # no wait
+    assert lib.kda_test_arm_timeout(vp(A), 0, 0, 2000001, None) == 1        # beyond 2 s
+    d = (ctypes.c_int32 * 4)()
+    assert lib.kda_read_device_status_detail(None, None, 0, d) == 1
+    assert lib.kda_read_device_status_detail(vp(A), None, 0, None) == 1
+    assert lib.kda_noalloc_read_status(None, 0, None) == 1
 
 
 def test_workspace_size(lib):

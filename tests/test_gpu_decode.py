@@ -1,4 +1,5 @@
-"""GPU parity of kda_decode_step against the fp64 oracle."""
+"""GPU parity of kda_decode_step against the fp64 oracle (whole tensor, every
+(sequence, head) unit and every row)."""
 from __future__ import annotations
 
 import numpy as np
@@ -7,7 +8,7 @@ import torch
 
 import oracle
 from gated_delta_rule_13_gb300 import inputs, kda
-from parity_util import TOL, rel_l2
+from parity_util import TOL, assert_parity
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -31,6 +32,13 @@ def _oracle_steps(d, steps, units=None):
     return outs, state
 
 
+def _cmp(got, ref, tol, name):
+    """Units on axis 0 (each its own sequence), a unit head axis."""
+    got = got.reshape(ref.shape)
+    return assert_parity(got, ref, tol, cu=None if got.ndim == 4 else np.arange(ref.shape[0] + 1),
+                         name=name)
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_decode_steps_match_oracle(dtype):
     d = inputs.decode_inputs(B=3, H=5, steps=4, dtype=dtype, device=DEV)
@@ -42,8 +50,8 @@ def test_decode_steps_match_oracle(dtype):
     torch.cuda.synchronize()
     ref_outs, ref_state = _oracle_steps(d, 4)
     for s in range(4):
-        assert rel_l2(outs[s].reshape(15, 1, 128), ref_outs[s]) <= TOL[dtype]
-    assert rel_l2(state.reshape(15, 1, 128, 128), ref_state) <= TOL[dtype]
+        _cmp(outs[s], ref_outs[s], TOL[dtype], f"out, step {s}")
+    _cmp(state, ref_state, TOL[dtype], "state")
 
 
 def test_decode_full_size_sampled_units():
@@ -60,8 +68,8 @@ def test_decode_full_size_sampled_units():
     ref_outs, ref_state = _oracle_steps(d, 1, units=units)
     got_out = out.reshape(512 * 96, 1, 128)[torch.as_tensor(units, device=DEV)]
     got_state = state.reshape(512 * 96, 1, 128, 128)[torch.as_tensor(units, device=DEV)]
-    assert rel_l2(got_out, ref_outs[0]) <= TOL["bf16"]
-    assert rel_l2(got_state, ref_state) <= TOL["bf16"]
+    _cmp(got_out, ref_outs[0], TOL["bf16"], "out")
+    _cmp(got_state, ref_state, TOL["bf16"], "state")
     # and every unit was written: the new state differs from the old one everywhere
     # a token with beta > 0 arrived (beta = sigmoid(N(0,1)) is never 0).
     changed = (state != state0).reshape(512 * 96, -1).any(dim=1)
@@ -84,8 +92,8 @@ def test_decode_edge_values(case):
                               d["beta"][0])
     torch.cuda.synchronize()
     ref_outs, ref_state = _oracle_steps(d, 1)
-    assert rel_l2(out.reshape(12, 1, 128), ref_outs[0]) <= TOL["f32"]
-    assert rel_l2(state.reshape(12, 1, 128, 128), ref_state) <= TOL["f32"]
+    _cmp(out, ref_outs[0], TOL["f32"], "out")
+    _cmp(state, ref_state, TOL["f32"], "state")
 
 
 def test_decode_deterministic():
@@ -95,3 +103,30 @@ def test_decode_deterministic():
     ob = kda.kda_decode_step(b, d["q"][0], d["k"][0], d["v"][0], d["log_alpha"][0], d["beta"][0])
     torch.cuda.synchronize()
     assert torch.equal(a, b) and torch.equal(oa, ob)
+
+
+def test_decode_100_steps_in_place_sampled_units():
+    """The decode workload as specified: 512 sequences x 96 heads, 100
+    consecutive steps with fresh inputs each, the fp32 state advanced in place
+    by every step.  48 sampled (sequence, head) units are replayed by the oracle
+    over all 100 steps: every step's output and the final state must match."""
+    steps = 100
+    d = inputs.decode_inputs(B=512, H=96, steps=steps, dtype="bf16", device=DEV, seed=5)
+    state = d["state"].clone()
+    out = torch.empty(steps, 512, 96, 128, dtype=torch.bfloat16, device=DEV)
+    for s in range(steps):
+        kda.kda_decode_step(state, d["q"][s], d["k"][s], d["v"][s], d["log_alpha"][s],
+                            d["beta"][s], out=out[s])
+    torch.cuda.synchronize()
+    g = np.random.default_rng(5)
+    units = np.sort(g.choice(512 * 96, size=48, replace=False))
+    usel = torch.as_tensor(units, device=DEV)
+    ref_outs, ref_state = _oracle_steps(d, steps, units=units)
+    got = out.reshape(steps, 512 * 96, 1, 128).index_select(1, usel)
+    # all steps at once: rows = (step, unit), each unit's 100 rows one sequence
+    got_all = got.permute(1, 0, 2, 3).reshape(48 * steps, 1, 128)
+    ref_all = np.stack(ref_outs, axis=1).reshape(48 * steps, 1, 128)
+    assert_parity(got_all, ref_all, TOL["bf16"], cu=np.arange(49) * steps, name="out, 100 steps")
+    _cmp(state.reshape(512 * 96, 1, 128, 128)[usel], ref_state, TOL["bf16"], "state after 100 steps")
+    del d, out, state
+    torch.cuda.empty_cache()

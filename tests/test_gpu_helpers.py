@@ -5,63 +5,34 @@ be bitwise those of a run without helpers (same arithmetic, same order), and
 still match the oracle."""
 from __future__ import annotations
 
-import os
-
 import pytest
 import torch
 
 from gated_delta_rule_13_gb300 import inputs, kda
-from parity_util import TOL, oracle_prefill, rel_l2
+from parity_util import TOL, check_prefill
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
-@pytest.fixture(autouse=True)
-def _no_split():
-    """These calls are small enough for the in-device split, which takes
-    precedence over helpers: turn it off here."""
-    old = os.environ.get("KDA_CHUNK_SPLIT")
-    os.environ["KDA_CHUNK_SPLIT"] = "0"
-    yield
-    if old is None:
-        os.environ.pop("KDA_CHUNK_SPLIT", None)
-    else:
-        os.environ["KDA_CHUNK_SPLIT"] = old
-
-
 def _run(x, helpers):
-    """kda_chunk_fwd with helpers on (library default) or off; returns the
-    outputs and the helper counters of the call."""
-    old = os.environ.get("KDA_CHUNK_HELPERS")
-    try:
-        if helpers:
-            os.environ.pop("KDA_CHUNK_HELPERS", None)
-        else:
-            os.environ["KDA_CHUNK_HELPERS"] = "0"
-        n_seqs = x["cu_seqlens"].shape[0] - 1
-        N, H = x["q"].shape[0], x["q"].shape[1]
-        ws = torch.empty(kda.kda_chunk_fwd_workspace_size(n_seqs, N, H, dtype=kda.KDA_BF16),
-                         dtype=torch.uint8, device=DEV)
-        out, fin = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
-                                     x["init_state"], x["cu_seqlens"], workspace=ws)
-        stats = kda.kda_read_chunk_stats(ws)
-        assert kda.kda_read_device_status(ws) == kda.KDA_OK
-        return out.clone(), fin.clone(), stats
-    finally:
-        if old is None:
-            os.environ.pop("KDA_CHUNK_HELPERS", None)
-        else:
-            os.environ["KDA_CHUNK_HELPERS"] = old
+    """kda_chunk_fwd with the split off (these calls are small enough for it,
+    and it takes precedence over helpers) and helpers on (the library's count)
+    or off; returns the outputs and the helper counters of the call."""
+    n_seqs = x["cu_seqlens"].shape[0] - 1
+    N, H = x["q"].shape[0], x["q"].shape[1]
+    ws = torch.empty(kda.kda_chunk_fwd_workspace_size(n_seqs, N, H, dtype=kda.KDA_BF16),
+                     dtype=torch.uint8, device=DEV)
+    out, fin = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
+                                 x["init_state"], x["cu_seqlens"], workspace=ws, max_split=0,
+                                 max_helpers=None if helpers else 0)
+    stats = kda.kda_read_chunk_stats(ws)
+    assert kda.kda_read_device_status(ws) == kda.KDA_OK
+    return out.clone(), fin.clone(), stats
 
 
 def _sampled_parity(x, out, fin, heads):
-    o_ref, s_ref, idx = oracle_prefill(x, heads=heads)
-    hsel = torch.as_tensor(heads, device=DEV)
-    got_o = out.index_select(0, torch.as_tensor(idx, device=DEV)).index_select(1, hsel)
-    got_s = fin.index_select(1, hsel)
-    assert rel_l2(got_o, o_ref) <= TOL["bf16"]
-    assert rel_l2(got_s, s_ref) <= TOL["bf16"]
+    check_prefill(x, out, fin, TOL["bf16"], heads=heads)
 
 
 def test_long_chains_use_packages_bitwise():
@@ -98,7 +69,7 @@ def test_repeated_calls_same_workspace():
     outs = []
     for _ in range(3):
         out, fin = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], None,
-                                     x["cu_seqlens"], workspace=ws)
+                                     x["cu_seqlens"], workspace=ws, max_split=0)
         pub, con = kda.kda_read_chunk_stats(ws)
         assert 0 <= con <= pub
         outs.append((out.clone(), fin.clone()))

@@ -3,8 +3,6 @@ overlapping the prefill, each piece starting from the previous piece's final
 state.  It must give exactly the results of one kda_chunk_fwd call."""
 from __future__ import annotations
 
-import os
-
 import pytest
 import torch
 
@@ -14,29 +12,20 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
-@pytest.fixture
-def no_split():
-    """Bitwise comparisons need one schedule for the pieces and the whole: few
-    heads would otherwise take the in-device split for long calls only."""
-    old = os.environ.get("KDA_CHUNK_SPLIT")
-    os.environ["KDA_CHUNK_SPLIT"] = "0"
-    yield
-    if old is None:
-        os.environ.pop("KDA_CHUNK_SPLIT", None)
-    else:
-        os.environ["KDA_CHUNK_SPLIT"] = old
-
-
 @pytest.mark.parametrize("N,piece,init", [(1000, 256, True), (4096, 4096, False),
                                           (5000, 1024, True), (64, 64, False)])
-def test_pieces_equal_one_call(no_split, N, piece, init):
+def test_pieces_equal_one_call(N, piece, init):
+    """Bitwise: the pieces and the whole call run the plain schedule (few heads
+    would otherwise take the in-device split for long calls only)."""
     x = inputs.prefill_inputs([N], H=3, dtype="bf16", init_state=init, device=DEV, seed=71)
     o_ref, s_ref = kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
-                                     x["init_state"], x["cu_seqlens"])
+                                     x["init_state"], x["cu_seqlens"], max_split=0,
+                                     max_helpers=0)
     host = {n: x[n].cpu().pin_memory() for n in ("q", "k", "v", "log_alpha", "beta")}
     h_init = x["init_state"].cpu() if init else None
     out, fin = kda.kda_chunk_fwd_host(host["q"], host["k"], host["v"], host["log_alpha"],
-                                      host["beta"], h_init, piece_tokens=piece, device=DEV)
+                                      host["beta"], h_init, piece_tokens=piece, device=DEV,
+                                      max_split=0, max_helpers=0)
     torch.cuda.synchronize()
     assert torch.equal(out, o_ref.cpu()) and torch.equal(fin, s_ref.cpu())
 
@@ -44,7 +33,7 @@ def test_pieces_equal_one_call(no_split, N, piece, init):
 def test_default_schedules_match_oracle():
     """With the split allowed (long pieces over few heads take it), against the oracle."""
     import oracle
-    from parity_util import TOL, rel_l2
+    from parity_util import TOL, assert_parity
     x = inputs.prefill_inputs([9000], H=2, dtype="bf16", init_state=True, device=DEV, seed=73)
     host = {n: x[n].cpu().pin_memory() for n in ("q", "k", "v", "log_alpha", "beta")}
     out, fin = kda.kda_chunk_fwd_host(host["q"], host["k"], host["v"], host["log_alpha"],
@@ -53,7 +42,8 @@ def test_default_schedules_match_oracle():
     torch.cuda.synchronize()
     o_ref, s_ref = oracle.chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
                                     x["init_state"], x["cu_seqlens"])
-    assert rel_l2(out, o_ref) <= TOL["bf16"] and rel_l2(fin, s_ref) <= TOL["bf16"]
+    assert_parity(out, o_ref, TOL["bf16"], name="out")
+    assert_parity(fin, s_ref, TOL["bf16"], name="final state")
 
 
 def test_empty_sequence_and_bad_piece():

@@ -13,7 +13,7 @@ import oracle
 from gated_delta_rule_13_gb300 import inputs, kda
 from gated_delta_rule_13_gb300.kcp import KernelOps, stack_pairs, start_state
 from kcp_util import OracleOps, rank_segments
-from parity_util import TOL, rel_l2
+from parity_util import TOL, assert_parity
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -32,8 +32,8 @@ def test_transitions_match_oracle_pairs(decay):
                                          x["cu_seqlens"])
     torch.cuda.synchronize()
     rb, rm = OracleOps.pairs(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["cu_seqlens"])
-    assert rel_l2(b, rb) <= TOL["bf16"]
-    assert rel_l2(m, rm) <= TOL["bf16"]
+    assert_parity(b, rb, TOL["bf16"], name="B")
+    assert_parity(m, rm, TOL["bf16"], name="M")
     # an empty sequence maps every state to itself
     assert torch.equal(b[1], torch.zeros_like(b[1]))
     assert torch.equal(m[1], torch.eye(128, device=DEV).expand(3, 128, 128))
@@ -49,8 +49,8 @@ def test_state_combine_matches_numpy():
         starts, end = kda.kda_state_combine(b, m, K, s0)
         torch.cuda.synchronize()
         rs, re = OracleOps.combine(b, m, K, s0)
-        assert rel_l2(starts, rs) <= 1e-5
-        assert rel_l2(end, re) <= 1e-5
+        assert_parity(starts, rs, 1e-5, name="start states")
+        assert_parity(end, re, 1e-5, name="end states")
 
 
 @pytest.mark.parametrize("decay", [0.0, 0.02, 1.0])
@@ -74,5 +74,5 @@ def test_three_rank_kcp_matches_oracle(decay):
     torch.cuda.synchronize()
     o_ref, s_ref = oracle.chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
                                     x["init_state"], x["cu_seqlens"])
-    assert rel_l2(out, o_ref) <= TOL["bf16"]
-    assert rel_l2(end, s_ref) <= TOL["bf16"]
+    assert_parity(out, o_ref, TOL["bf16"], cu=x["cu_seqlens"].cpu().numpy(), name="out")
+    assert_parity(end, s_ref, TOL["bf16"], name="final state")

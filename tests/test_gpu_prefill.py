@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from gated_delta_rule_13_gb300 import inputs, kda
-from parity_util import TOL, oracle_prefill, rel_l2
+from parity_util import TOL, assert_parity, check_prefill
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -23,18 +23,9 @@ def run(x, **kw):
 
 
 def check(x, dtype, heads=None, seqs=None):
+    """Whole-tensor, per-(sequence, head) and per-row parity with the oracle."""
     out, fin = run(x)
-    o_ref, s_ref, idx = oracle_prefill(x, heads=heads, seqs=seqs)
-    H = x["q"].shape[1]
-    hsel = torch.as_tensor(heads if heads is not None else list(range(H)), device=DEV)
-    got_o = out.index_select(0, torch.as_tensor(idx, device=DEV)).index_select(1, hsel)
-    n_seqs = x["cu_seqlens"].shape[0] - 1
-    ssel = torch.as_tensor(seqs if seqs is not None else list(range(n_seqs)), device=DEV)
-    got_s = fin.index_select(0, ssel).index_select(1, hsel)
-    eo, es = rel_l2(got_o, o_ref), rel_l2(got_s, s_ref)
-    assert eo <= TOL[dtype], f"out rel L2 {eo:.3e}"
-    assert es <= TOL[dtype], f"final state rel L2 {es:.3e}"
-    return eo, es
+    return check_prefill(x, out, fin, TOL[dtype], heads=heads, seqs=seqs)
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -109,8 +100,8 @@ def test_split_with_state_handoff(dtype):
         b["init_state"] = s1
         o2, s2 = run(b)
         tol = TOL[dtype]
-        assert rel_l2(torch.cat([o1, o2]), out) <= tol
-        assert rel_l2(s2, fin) <= tol
+        assert_parity(torch.cat([o1, o2]), out, tol, name=f"out, cut at {cut}")
+        assert_parity(s2, fin, tol, name=f"final state, cut at {cut}")
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -126,8 +117,8 @@ def test_decode_steps_equal_prefill(dtype):
                                         x["beta"][t:t + 1]))
     torch.cuda.synchronize()
     tol = TOL[dtype]
-    assert rel_l2(torch.cat(outs), out) <= tol
-    assert rel_l2(state, fin) <= tol
+    assert_parity(torch.cat(outs), out, tol, name="out")
+    assert_parity(state, fin, tol, name="state")
 
 
 @pytest.mark.parametrize("dtype", DTYPES)

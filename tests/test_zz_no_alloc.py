@@ -1,6 +1,7 @@
 """kda_chunk_fwd_noalloc: the prefill entry point for callers that cannot give
 the library device memory (their framework allocator owns all of it), checked
-through the C ABI against kda_chunk_fwd on two consecutive calls.
+through the C ABI against the fp64 oracle and against kda_chunk_fwd on two
+consecutive calls, and its status reader on a malformed device cu_seqlens.
 
 Collected last on purpose: the entry point's device scratch is shared by every
 call, so this file must also pass after all other tests ran in the process.
@@ -13,7 +14,7 @@ import pytest
 import torch
 
 from gated_delta_rule_13_gb300 import inputs, kda
-from parity_util import TOL, rel_l2
+from parity_util import TOL, assert_parity, check_prefill
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -33,8 +34,16 @@ def _noalloc_c_call(x, out, fin, cu):
                                      vp(torch.cuda.current_stream().cuda_stream))
 
 
+def _status_c_call():
+    st = ctypes.c_int32(-1)
+    rc = kda.library().kda_noalloc_read_status(
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream), 1, ctypes.byref(st))
+    assert rc == kda.KDA_OK
+    return st.value
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_noalloc_matches_workspace_entry_point_twice(dtype):
+def test_noalloc_matches_oracle_and_workspace_entry_point_twice(dtype):
     for call, (lengths, seed, host_cu) in enumerate([([300, 0, 129, 64], 11, False),
                                                      ([77, 1024, 5], 12, True)]):
         x = inputs.prefill_inputs(lengths, H=3, dtype=dtype, init_state=True, device=DEV,
@@ -47,9 +56,26 @@ def test_noalloc_matches_workspace_entry_point_twice(dtype):
         rc = _noalloc_c_call(x, out, fin, cu)
         torch.cuda.synchronize()
         assert rc == kda.KDA_OK, f"call {call}: {kda.status_string(rc)}"
-        assert rel_l2(out, ref_out) <= TOL[dtype], f"call {call}"
-        assert rel_l2(fin, ref_fin) <= TOL[dtype], f"call {call}"
+        assert _status_c_call() == kda.KDA_OK
         assert torch.isfinite(out).all() and torch.isfinite(fin).all()
+        check_prefill(x, out, fin, TOL[dtype])
+        cu_np = x["cu_seqlens"].cpu().numpy()
+        assert_parity(out, ref_out, TOL[dtype], cu=cu_np, name=f"out vs kda_chunk_fwd, call {call}")
+        assert_parity(fin, ref_fin, TOL[dtype], name=f"final state vs kda_chunk_fwd, call {call}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_noalloc_status_reports_malformed_device_cu_seqlens(dtype):
+    """The call returns KDA_OK (the kernel validates a device cu_seqlens); the
+    status reader returns what the kernel recorded, then the cleared status."""
+    x = inputs.prefill_inputs([100, 50], H=2, dtype=dtype, device=DEV, seed=13)
+    bad = torch.tensor([0, 120, 110], dtype=torch.int32, device=DEV)
+    out = torch.empty_like(x["v"])
+    assert _noalloc_c_call(x, out, None, bad) == kda.KDA_OK
+    assert _status_c_call() == kda.KDA_ERR_INVALID_ARG
+    assert _status_c_call() == kda.KDA_OK
+    assert _noalloc_c_call(x, out, None, x["cu_seqlens"]) == kda.KDA_OK
+    assert _status_c_call() == kda.KDA_OK
 
 
 def test_noalloc_rejects_too_many_sequences():
