@@ -264,6 +264,60 @@ def replay_bench(dev, peaks, steps: int = 20, warmup: int = 3, T: int = 4):
                          "bytes_per_launch": nbytes}}
 
 
+def layer_replay_bench(dev, peaks, steps: int = 20, warmup: int = 3, T: int = 4):
+    """kda_layer_replay (the layer between its projections, fused, over the
+    accepted drafts) on 512 sequences x 96 heads x T cached drafts, accepted
+    counts seeded uniform in [0, T].  Algorithmic bytes per unit with an
+    accepted token: the state and the bf16 convolution window read and written
+    once, plus per accepted token the raw q, k, v and gate logits (bf16), the
+    decay logits (fp32), the beta logit and the bf16 output."""
+    import torch
+    from gated_delta_rule_13_gb300 import inputs, kda
+    B, H = 512, 96
+    x = inputs.layer_inputs([T] * B, H=H, dtype="bf16", device=dev, seed=19)
+    r = {n: x[n].reshape(B, T, H, *x[n].shape[2:]) for n in
+         ("q_raw", "k_raw", "v_raw", "a_logit", "b_logit", "g")}
+    gen = torch.Generator(device=dev).manual_seed(19)
+    state = 0.02 * torch.randn(B, H, 128, 128, generator=gen, device=dev)
+    win = torch.randn(B, 3, 3, H, 128, generator=gen, device=dev).to(torch.bfloat16)
+    g = torch.Generator(device="cpu").manual_seed(19)
+    n = torch.randint(0, T + 1, (B,), generator=g, dtype=torch.int32)
+    n_dev = n.to(dev)
+    out = torch.empty(B, T, H, 128, dtype=torch.bfloat16, device=dev)
+
+    def run():
+        kda.kda_layer_replay(state, win, r["q_raw"], r["k_raw"], r["v_raw"], r["a_logit"],
+                             r["b_logit"], r["g"], x["conv_w"], x["gamma"], n_dev, out=out)
+
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        run()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    accepted = int(n.sum())
+    active = int((n > 0).sum())
+    per_tok = 3 * 256 + 512 + 4 + 256 + 256
+    nbytes = H * (active * (2 * STATE_BYTES + 2 * 9 * 256) + accepted * per_tok)
+    gbs = nbytes / (ms / 1000.0) / 1e9
+    del x, r, state, win, out
+    return {"value": gbs, "unit": "GB/s", "ms_per_launch": ms,
+            "workload": f"512 sequences x 96 heads, {T} cached drafts (raw projections, bf16), "
+                        f"accepted counts seeded uniform in [0, {T}] (mean {accepted / B:.2f})",
+            "accepted_tokens_per_s": accepted / (ms / 1000.0),
+            "roofline": {"bound": "hbm", "kernel": "kda_layer_replay_kernel", "achieved": gbs,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"],
+                         "traffic": recorded_traffic("kda_layer_replay_kernel",
+                                                     "kda_layer_ops.cu", f"b{B}_h{H}_t{T}"),
+                         "bytes_per_launch": nbytes}}
+
+
 def layer_ops_bench(dev, peaks, steps: int = 20, warmup: int = 3, T: int = 32768):
     """kda_prep_fwd and kda_post_fwd on the K3 layout (one sequence of T = 32768
     tokens, 96 heads, bf16).  Algorithmic bytes per token-head: prep reads
@@ -587,12 +641,15 @@ def run_gpu(args):
     replay = replay_bench(dev, peaks, steps=args.sub_steps)
     few_chains = few_chains_bench(dev, peaks, steps=args.sub_steps)
     layer_ops = layer_ops_bench(dev, peaks, steps=args.sub_steps, T=args.layer_tokens)
+    layer_replay = layer_replay_bench(dev, peaks, steps=args.sub_steps)
     configs = {}
     for wl, n in (("b4_h16_t4096", args.sub_steps), ("varlen_h96_1m", args.varlen_steps)):
         if n > 0:
             configs[wl] = prefill_config_bench(dev, peaks, wl, steps=n)
     if world > 1:
         replay["ms_per_launch"], = max_over_ranks([replay["ms_per_launch"]], world, dev)
+        layer_replay["ms_per_launch"], = max_over_ranks([layer_replay["ms_per_launch"]], world,
+                                                        dev)
         decode_seq["ms_per_step"], = max_over_ranks([decode_seq["ms_per_step"]], world, dev)
         for c in configs.values():
             c["ms_per_launch"], = max_over_ranks([c["ms_per_launch"]], world, dev)
@@ -638,6 +695,7 @@ def run_gpu(args):
         "replay": replay,
         "prefill_few_chains": few_chains,
         "layer_ops": layer_ops,
+        "layer_replay": layer_replay,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": 2 * args.steps,

@@ -501,6 +501,95 @@ int kda_prep_fwd(const void *q_raw, const void *k_raw, const void *v_raw, const 
   return KDA_OK;
 }
 
+int kda_prep_fwd_state(const void *q_raw, const void *k_raw, const void *v_raw,
+                       const float *conv_w, const float *a_logit, const float *b_logit,
+                       const int32_t *cu_seqlens, int32_t n_seqs, int64_t n_tokens, int32_t H,
+                       int32_t dk, int32_t dv, int dtype, const void *conv_state_in,
+                       void *conv_state_out, void *q, void *k, void *v, float *log_alpha,
+                       float *beta, void *stream) {
+  if (n_seqs < 1 || n_tokens < 0 || n_tokens > 0x7fffffffLL || H <= 0) return KDA_ERR_INVALID_ARG;
+  const int d = check_dims(dk, dv, dtype);
+  if (d != KDA_OK) return d;
+  if (!q_raw || !k_raw || !v_raw || !conv_w || !a_logit || !b_logit || !cu_seqlens || !q || !k ||
+      !v || !log_alpha || !beta)
+    return KDA_ERR_INVALID_ARG;
+  const size_t esz = dtype == KDA_BF16 ? 2 : 4;
+  const void *vec[] = {q_raw, k_raw, v_raw, q, k, v, conv_state_in, conv_state_out};
+  for (const void *p : vec)
+    if (p && !aligned(p, 4 * esz)) return KDA_ERR_INVALID_ARG;
+  if (!aligned16(conv_w) || !aligned16(a_logit) || !aligned16(log_alpha) || !aligned(b_logit, 4) ||
+      !aligned(beta, 4) || !aligned(cu_seqlens, 4))
+    return KDA_ERR_INVALID_ARG;
+  const size_t n = (size_t)n_tokens * H * dk;
+  const void *outs[] = {q, k, v};
+  const void *ins[] = {q_raw, k_raw, v_raw};
+  for (const void *o : outs)
+    for (const void *i : ins)
+      if (n > 0 && ranges_overlap(o, n * esz, i, n * esz)) return KDA_ERR_INVALID_ARG;
+  if (n > 0 && (ranges_overlap(log_alpha, n * 4, a_logit, n * 4) ||
+                ranges_overlap(beta, (size_t)n_tokens * H * 4, b_logit, (size_t)n_tokens * H * 4)))
+    return KDA_ERR_INVALID_ARG;
+  // the window: 3 tensors x 3 rows x [H, 128] per sequence; in and out may be
+  // the same array (updated in place) but may not overlap otherwise, nor touch
+  // any input or output tensor
+  const size_t wb = (size_t)n_seqs * 9 * H * dk * esz;
+  if (conv_state_in && conv_state_out && conv_state_in != conv_state_out &&
+      ranges_overlap(conv_state_in, wb, conv_state_out, wb))
+    return KDA_ERR_INVALID_ARG;
+  const void *wins[] = {conv_state_in, conv_state_out};
+  const void *tens[] = {q_raw, k_raw, v_raw, q, k, v};
+  for (const void *w : wins) {
+    if (!w) continue;
+    for (const void *t : tens)
+      if (n > 0 && ranges_overlap(w, wb, t, n * esz)) return KDA_ERR_INVALID_ARG;
+  }
+  const cudaError_t e = kda::launch_prep_window(q_raw, k_raw, v_raw, conv_w, a_logit, b_logit,
+                                                cu_seqlens, n_seqs, n_tokens, H, dtype == KDA_BF16,
+                                                conv_state_in, conv_state_out, q, k, v, log_alpha,
+                                                beta, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_CUDA;
+  }
+  return KDA_OK;
+}
+
+int kda_layer_replay(float *state, void *conv_state, const void *q_raw, const void *k_raw,
+                     const void *v_raw, const float *a_logit, const float *b_logit, const void *g,
+                     const float *conv_w, const float *gamma, const int32_t *n_accept, int32_t B,
+                     int32_t T, int32_t H, int32_t dk, int32_t dv, int dtype, void *out,
+                     void *stream) {
+  if (B < 0 || T <= 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+  const int d = check_dims(dk, dv, dtype);
+  if (d != KDA_OK) return d;
+  if (!state || !conv_state || !q_raw || !k_raw || !v_raw || !a_logit || !b_logit || !g ||
+      !conv_w || !gamma || !n_accept)
+    return KDA_ERR_INVALID_ARG;
+  const size_t esz = dtype == KDA_BF16 ? 2 : 4;
+  if (!aligned16(state) || !aligned(conv_state, esz) || !aligned(q_raw, esz) ||
+      !aligned(k_raw, esz) || !aligned(v_raw, esz) || !aligned(g, esz) || !aligned(a_logit, 4) ||
+      !aligned(b_logit, 4) || !aligned16(conv_w) || !aligned16(gamma) || !aligned(n_accept, 4) ||
+      (out && !aligned(out, 4 * esz)))
+    return KDA_ERR_INVALID_ARG;
+  const size_t units = (size_t)B * H;
+  const size_t sb = units * dk * dv * sizeof(float), wb = (size_t)B * 9 * H * dk * esz;
+  if (units > 0 && ranges_overlap(state, sb, conv_state, wb)) return KDA_ERR_INVALID_ARG;
+  if (out && units > 0) {
+    const size_t ob = units * (size_t)T * dv * esz;
+    if (ranges_overlap(out, ob, state, sb) || ranges_overlap(out, ob, conv_state, wb))
+      return KDA_ERR_INVALID_ARG;
+  }
+  const cudaError_t e = kda::launch_layer_replay(state, conv_state, q_raw, k_raw, v_raw, a_logit,
+                                                 b_logit, g, conv_w, gamma, n_accept, B, T, H,
+                                                 dtype == KDA_BF16, out,
+                                                 static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_CUDA;
+  }
+  return KDA_OK;
+}
+
 int kda_post_fwd(const void *o, const void *g, const float *gamma, int64_t n_tokens, int32_t H,
                  int32_t dv, int dtype, void *out, void *stream) {
   if (n_tokens < 0 || H <= 0) return KDA_ERR_INVALID_ARG;

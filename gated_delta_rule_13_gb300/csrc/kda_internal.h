@@ -123,6 +123,22 @@ cudaError_t launch_prep(const void *q_raw, const void *k_raw, const void *v_raw,
                         bool bf16, void *q, void *k, void *v, float *log_alpha, float *beta,
                         cudaStream_t stream);
 
+// kda_prep_fwd with a carried convolution window (win_in may be NULL: zeros;
+// win_out may be NULL: not written; both [n_seqs, 3, 3, H, 128] dtype, and may
+// be the same array).
+cudaError_t launch_prep_window(const void *q_raw, const void *k_raw, const void *v_raw,
+                               const float *conv_w, const float *a_logit, const float *b_logit,
+                               const int32_t *cu_seqlens, int32_t n_seqs, int64_t n_tokens,
+                               int32_t H, bool bf16, const void *win_in, void *win_out, void *q,
+                               void *k, void *v, float *log_alpha, float *beta,
+                               cudaStream_t stream);
+
+cudaError_t launch_layer_replay(float *state, void *win, const void *q_raw, const void *k_raw,
+                                const void *v_raw, const float *a_logit, const float *b_logit,
+                                const void *g, const float *conv_w, const float *gamma,
+                                const int32_t *n_accept, int32_t B, int32_t T, int32_t H,
+                                bool bf16, void *out, cudaStream_t stream);
+
 cudaError_t launch_post(const void *o, const void *g, const float *gamma, int64_t n_tokens,
                         int32_t H, bool bf16, void *out, cudaStream_t stream);
 

@@ -110,6 +110,14 @@ template <bool BF16> __device__ __forceinline__ float4 to_f4(raw4_t<BF16> r) {
   }
 }
 
+__device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_float(float x) { return x; }
+template <typename T> __device__ __forceinline__ T from_float(float x);
+template <> __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+template <> __device__ __forceinline__ float from_float<float>(float x) { return x; }
+
 // Index of the sequence holding token t: the last s < n_seqs with cu[s] <= t.
 __device__ __forceinline__ int sequence_of(const int32_t *cu, int32_t n_seqs, int64_t t) {
   int lo = 0, hi = n_seqs;  // invariant: answer in [lo, hi)
@@ -144,14 +152,15 @@ __device__ __forceinline__ float4 conv_swish(float4 x0, float4 x1, float4 x2, fl
 // row is read once, plus a three-row halo per run.
 constexpr int kRunTokens = 32;
 
-template <bool BF16>
+template <bool BF16, bool kWindow>
 __global__ void __launch_bounds__(32 * kWarps, 4)
 kda_prep_kernel(const void *__restrict__ q_raw, const void *__restrict__ k_raw,
                 const void *__restrict__ v_raw, const float *__restrict__ conv_w,
                 const float *__restrict__ a_logit, const float *__restrict__ b_logit,
                 const int32_t *__restrict__ cu_seqlens, int32_t n_seqs, int64_t n_tokens,
                 int32_t H, void *__restrict__ q, void *__restrict__ k, void *__restrict__ v,
-                float *__restrict__ log_alpha, float *__restrict__ beta) {
+                float *__restrict__ log_alpha, float *__restrict__ beta,
+                const void *__restrict__ win_in) {
   constexpr int kGroup = BF16 ? 4 : 2;  // rows in flight per warp
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y * kWarps + warp;
@@ -229,11 +238,32 @@ kda_prep_kernel(const void *__restrict__ q_raw, const void *__restrict__ k_raw,
         ts = nxt;
         nxt = s + 1 < n_seqs ? cu_seqlens[s + 1] : INT32_MAX;
       }
-      const int32_t start = ts < t ? ts : t;
       const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 x0 = t - 3 >= start ? to_f4<BF16>(w0) : zero;
-      const float4 x1 = t - 2 >= start ? to_f4<BF16>(w1) : zero;
-      const float4 x2 = t - 1 >= start ? to_f4<BF16>(w2) : zero;
+      float4 x0, x1, x2;
+      if constexpr (!kWindow) {  // zeros before the sequence start
+        const int32_t start = ts < t ? ts : t;
+        x0 = t - 3 >= start ? to_f4<BF16>(w0) : zero;
+        x1 = t - 2 >= start ? to_f4<BF16>(w1) : zero;
+        x2 = t - 1 >= start ? to_f4<BF16>(w2) : zero;
+      } else {
+        x0 = to_f4<BF16>(w0);
+        x1 = to_f4<BF16>(w1);
+        x2 = to_f4<BF16>(w2);
+        if (t - 3 < ts) {
+          // taps before the sequence start read the carried window (rows oldest
+          // first: tap j of token ts + u is window row u + j), or zeros
+          const int u = t - ts;
+          auto tap = [&](int j, float4 x) -> float4 {
+            if (t - 3 + j >= ts) return x;
+            if (win_in == nullptr) return zero;
+            return to_f4<BF16>(ld_raw<BF16>(win_in, (((int64_t)s * 3 + z) * 3 + (u + j)) * rs +
+                                                        (int64_t)h * D + c0));
+          };
+          x0 = tap(0, x0);
+          x1 = tap(1, x1);
+          x2 = tap(2, x2);
+        }
+      }
       float4 o = conv_swish(x0, x1, x2, to_f4<BF16>(cur[i]), w);
       if (normalise)
         o = scale4(o, rsqrtf(warp_sum(o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w) + kL2Eps));
@@ -278,6 +308,231 @@ kda_post_kernel(const void *__restrict__ o, const void *__restrict__ g,
   }
 }
 
+// The carried window after a prep call: per sequence s and tensor z (q, k, v),
+// the three raw rows before the token after the call, oldest first: the
+// sequence's last three rows, or for a shorter one the newest rows of the
+// window it started from (zeros without one) followed by all of its rows.
+// Every lane reads its three rows before it writes any, so the window may be
+// updated in place; a malformed device cu_seqlens gives zeros, never an
+// out-of-range access.
+template <bool BF16>
+__global__ void __launch_bounds__(32 * kWarps)
+kda_conv_window_kernel(const void *__restrict__ q_raw, const void *__restrict__ k_raw,
+                       const void *__restrict__ v_raw, const int32_t *__restrict__ cu_seqlens,
+                       int32_t n_seqs, int64_t n_tokens, int32_t H, const void *win_in,
+                       void *win_out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int s = blockIdx.x, z = blockIdx.y, h = blockIdx.z * kWarps + warp;
+  if (h >= H) return;
+  const int c0 = 4 * lane;
+  const int64_t rs = (int64_t)H * D;
+  const void *x = z == 0 ? q_raw : (z == 1 ? k_raw : v_raw);
+  const int64_t a = cu_seqlens[s], e = cu_seqlens[s + 1];
+  const bool ok = a >= 0 && e >= a && e <= n_tokens;
+  const int64_t len = ok ? e - a : 0;
+  raw4_t<BF16> row[3];
+#pragma unroll
+  for (int r = 0; r < 3; ++r) {
+    const int64_t t = e - 3 + r;  // token of window row r
+    if (!ok) row[r] = raw_zero<BF16>();
+    else if (t >= a) row[r] = ld_raw<BF16>(x, t * rs + (int64_t)h * D + c0);
+    else if (win_in != nullptr)
+      row[r] = ld_raw<BF16>(win_in, (((int64_t)s * 3 + z) * 3 + (r + len)) * rs + (int64_t)h * D + c0);
+    else row[r] = raw_zero<BF16>();
+  }
+#pragma unroll
+  for (int r = 0; r < 3; ++r) {
+    const int64_t i = (((int64_t)s * 3 + z) * 3 + r) * rs + (int64_t)h * D + c0;
+    if constexpr (BF16) *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(win_out) + i) = row[r];
+    else *reinterpret_cast<float4 *>(static_cast<float *>(win_out) + i) = row[r];
+  }
+}
+
+// The whole layer between its projections, replayed over the accepted draft
+// tokens of a speculative step ("Kimi K3: 架构、训练与系统全景解析", KDA state
+// replay under speculative decoding: short convolution, norms, gating, the KDA
+// recurrence and the output norm in one kernel over the accepted prefix, the
+// state and the convolution window written back once).  Unit (b, h), tokens
+// t < n_b = n_accept[b] clamped to [0, T], one CTA of 8 warps:
+//   threads 0-127 (channel c): q and k of channel c (window, convolution,
+//     Swish), then L2Norm over the 128 channels;
+//   threads 128-255 (channel c - 128): v (window, convolution, Swish), the
+//     decay alpha = e^{-5 sigmoid(a)}, the output gate sigmoid(g), and beta;
+//   then every warp applies the token to its value columns of the state held in
+//   registers (the decode step's layout), and the output row goes through the
+//   head-wise RMSNorm times gamma times the gate before it is stored.
+// Nothing is read or written for a unit with no accepted token.
+constexpr int kReplayTokGroup = 2;  // tokens whose raw inputs are loaded together
+
+template <bool BF16>
+__global__ void __launch_bounds__(256, 2)
+kda_layer_replay_kernel(float *__restrict__ state, void *__restrict__ win,
+                        const void *__restrict__ q_raw, const void *__restrict__ k_raw,
+                        const void *__restrict__ v_raw, const float *__restrict__ a_logit,
+                        const float *__restrict__ b_logit, const void *__restrict__ g,
+                        const float *__restrict__ conv_w, const float *__restrict__ gamma,
+                        const int32_t *__restrict__ n_accept, int32_t T, int32_t H,
+                        void *__restrict__ out) {
+  using elem_t = typename std::conditional<BF16, __nv_bfloat16, float>::type;
+  __shared__ __align__(16) float s_q[D], s_k[D], s_v[D], s_alpha[D], s_gate[D];
+  __shared__ float s_red[3][kWarps];
+  __shared__ float s_beta;
+  __shared__ __align__(16) float s_w[3][D][kConv];  // the head's taps of q, k, v
+  const int64_t unit = blockIdx.x;
+  const int64_t b = unit / H;
+  const int h = (int)(unit % H);
+  const int na = n_accept[b];
+  const int n = na < 0 ? 0 : (na > T ? T : na);
+  if (n == 0) return;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int col = 16 * warp + 4 * (lane & 3);
+  const int row0 = lane >> 2;
+  const int role = tid >> 7, c = tid & (D - 1);
+  float *S = state + unit * (int64_t)(D * D);
+  float4 st[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    st[j] = __ldcs(reinterpret_cast<const float4 *>(S + (row0 + 8 * j) * D + col));
+
+  // channel c's taps and carried window rows (role 0: q and k, role 1: v)
+  const int64_t rs = (int64_t)H * D;  // elements per [H, D] row
+  const int za = role == 0 ? 0 : 2;
+  for (int e = tid; e < 3 * D; e += 256) {
+    const int z = e / D, ch = e % D;
+    *reinterpret_cast<float4 *>(s_w[z][ch]) =
+        *reinterpret_cast<const float4 *>(conv_w + (((int64_t)z * H + h) * D + ch) * kConv);
+  }
+  float xa[3], xb[3];
+  const elem_t *wv = static_cast<const elem_t *>(win);
+#pragma unroll
+  for (int r = 0; r < 3; ++r) {
+    xa[r] = to_float(wv[((b * 3 + za) * 3 + r) * rs + (int64_t)h * D + c]);
+    xb[r] = role == 0 ? to_float(wv[((b * 3 + 1) * 3 + r) * rs + (int64_t)h * D + c]) : 0.f;
+  }
+  const float4 gm = *reinterpret_cast<const float4 *>(gamma + col);
+
+  for (int t0 = 0; t0 < n; t0 += kReplayTokGroup) {
+    // raw inputs of up to kReplayTokGroup tokens, loaded together
+    float ra[kReplayTokGroup], rb[kReplayTokGroup], rg[kReplayTokGroup], rl[kReplayTokGroup];
+#pragma unroll
+    for (int i = 0; i < kReplayTokGroup; ++i) {
+      const int t = t0 + i;
+      ra[i] = rb[i] = rg[i] = rl[i] = 0.f;
+      if (t < n) {
+        const int64_t row = ((b * T + t) * H + h) * D + c;
+        if (role == 0) {
+          ra[i] = to_float(static_cast<const elem_t *>(q_raw)[row]);
+          rb[i] = to_float(static_cast<const elem_t *>(k_raw)[row]);
+        } else {
+          ra[i] = to_float(static_cast<const elem_t *>(v_raw)[row]);
+          rl[i] = a_logit[row];
+          rg[i] = to_float(static_cast<const elem_t *>(g)[row]);
+        }
+      }
+    }
+    for (int i = 0; i < kReplayTokGroup && t0 + i < n; ++i) {
+      const int t = t0 + i;
+      const int64_t tok = (b * T + t) * H + h;
+      // ---- convolution + Swish of this token, window shifted
+      if (t == 0) __syncthreads();  // the taps are in shared memory
+      const float4 wa = *reinterpret_cast<const float4 *>(s_w[za][c]);
+      float ya = wa.x * xa[0] + wa.y * xa[1] + wa.z * xa[2] + wa.w * ra[i];
+      ya *= sigmoidf(ya);
+      float yb = 0.f;
+      xa[0] = xa[1]; xa[1] = xa[2]; xa[2] = ra[i];
+      if (role == 0) {
+        const float4 wb = *reinterpret_cast<const float4 *>(s_w[1][c]);
+        yb = wb.x * xb[0] + wb.y * xb[1] + wb.z * xb[2] + wb.w * rb[i];
+        yb *= sigmoidf(yb);
+        xb[0] = xb[1]; xb[1] = xb[2]; xb[2] = rb[i];
+        // L2Norm sums of q and k over the 128 channels (warps 0-3)
+        const float sq = warp_sum(ya * ya), sk = warp_sum(yb * yb);
+        if (lane == 0) { s_red[0][warp] = sq; s_red[1][warp] = sk; }
+      } else {
+        s_v[c] = ya;
+        s_alpha[c] = __expf(kDecayBound * sigmoidf(rl[i]));
+        s_gate[c] = sigmoidf(rg[i]);
+        if (c == 0) s_beta = sigmoidf(b_logit[tok]);
+      }
+      __syncthreads();
+      if (role == 0) {
+        const float nq = rsqrtf(s_red[0][0] + s_red[0][1] + s_red[0][2] + s_red[0][3] + kL2Eps);
+        const float nk = rsqrtf(s_red[1][0] + s_red[1][1] + s_red[1][2] + s_red[1][3] + kL2Eps);
+        s_q[c] = ya * nq;
+        s_k[c] = yb * nk;
+      }
+      __syncthreads();
+      // ---- the recurrence step on this warp's value columns (the gate is read
+      // here too: the next token's inputs overwrite it once every warp is past
+      // the output barrier below)
+      const float4 vv = *reinterpret_cast<const float4 *>(&s_v[col]);
+      const float4 gt = *reinterpret_cast<const float4 *>(&s_gate[col]);
+      const float bt = s_beta;
+      float pk0 = 0.f, pk1 = 0.f, pk2 = 0.f, pk3 = 0.f;
+      float pq0 = 0.f, pq1 = 0.f, pq2 = 0.f, pq3 = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int r = row0 + 8 * j;
+        const float al = s_alpha[r], kr = s_k[r], qr = s_q[r];
+        st[j].x *= al; st[j].y *= al; st[j].z *= al; st[j].w *= al;
+        pk0 = fmaf(kr, st[j].x, pk0); pk1 = fmaf(kr, st[j].y, pk1);
+        pk2 = fmaf(kr, st[j].z, pk2); pk3 = fmaf(kr, st[j].w, pk3);
+        pq0 = fmaf(qr, st[j].x, pq0); pq1 = fmaf(qr, st[j].y, pq1);
+        pq2 = fmaf(qr, st[j].z, pq2); pq3 = fmaf(qr, st[j].w, pq3);
+      }
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        pk0 += __shfl_xor_sync(0xffffffffu, pk0, off);
+        pk1 += __shfl_xor_sync(0xffffffffu, pk1, off);
+        pk2 += __shfl_xor_sync(0xffffffffu, pk2, off);
+        pk3 += __shfl_xor_sync(0xffffffffu, pk3, off);
+        pq0 += __shfl_xor_sync(0xffffffffu, pq0, off);
+        pq1 += __shfl_xor_sync(0xffffffffu, pq1, off);
+        pq2 += __shfl_xor_sync(0xffffffffu, pq2, off);
+        pq3 += __shfl_xor_sync(0xffffffffu, pq3, off);
+      }
+      float kq = 0.f;
+#pragma unroll
+      for (int j = 0; j < D / 32; ++j) kq = fmaf(s_k[lane + 32 * j], s_q[lane + 32 * j], kq);
+      kq = warp_sum(kq);
+      const float u0 = bt * (vv.x - pk0), u1 = bt * (vv.y - pk1);
+      const float u2 = bt * (vv.z - pk2), u3 = bt * (vv.w - pk3);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float kr = s_k[row0 + 8 * j];
+        st[j].x = fmaf(kr, u0, st[j].x); st[j].y = fmaf(kr, u1, st[j].y);
+        st[j].z = fmaf(kr, u2, st[j].z); st[j].w = fmaf(kr, u3, st[j].w);
+      }
+      // ---- head-wise RMSNorm of the output row times gamma times the gate
+      const float o0 = fmaf(kq, u0, pq0), o1 = fmaf(kq, u1, pq1);
+      const float o2 = fmaf(kq, u2, pq2), o3 = fmaf(kq, u3, pq3);
+      float ss = o0 * o0 + o1 * o1 + o2 * o2 + o3 * o3;  // lanes 0-3 hold distinct columns
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+      if (lane == 0) s_red[2][warp] = ss;
+      __syncthreads();
+      if (out != nullptr && row0 == 0) {
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) tot += s_red[2][w];
+        const float nr = rsqrtf(tot * (1.0f / D) + kRmsEps);
+        st4<BF16>(out, tok * D + col,
+                  make_float4(o0 * nr * gm.x * gt.x, o1 * nr * gm.y * gt.y,
+                              o2 * nr * gm.z * gt.z, o3 * nr * gm.w * gt.w));
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    __stcs(reinterpret_cast<float4 *>(S + (row0 + 8 * j) * D + col), st[j]);
+  elem_t *wo = static_cast<elem_t *>(win);
+#pragma unroll
+  for (int r = 0; r < 3; ++r) {
+    wo[((b * 3 + za) * 3 + r) * rs + (int64_t)h * D + c] = from_float<elem_t>(xa[r]);
+    if (role == 0) wo[((b * 3 + 1) * 3 + r) * rs + (int64_t)h * D + c] = from_float<elem_t>(xb[r]);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_prep(const void *q_raw, const void *k_raw, const void *v_raw,
@@ -290,13 +545,65 @@ cudaError_t launch_prep(const void *q_raw, const void *k_raw, const void *v_raw,
   if (blocks > 0x7fffffffLL || H > 65535) return cudaErrorInvalidValue;
   const dim3 grid((unsigned)blocks, (unsigned)((H + kWarps - 1) / kWarps), 4), block(32 * kWarps);
   if (bf16)
-    kda_prep_kernel<true><<<grid, block, 0, stream>>>(q_raw, k_raw, v_raw, conv_w, a_logit,
+    kda_prep_kernel<true, false><<<grid, block, 0, stream>>>(q_raw, k_raw, v_raw, conv_w, a_logit,
                                                       b_logit, cu_seqlens, n_seqs, n_tokens, H,
-                                                      q, k, v, log_alpha, beta);
+                                                      q, k, v, log_alpha, beta, nullptr);
   else
-    kda_prep_kernel<false><<<grid, block, 0, stream>>>(q_raw, k_raw, v_raw, conv_w, a_logit,
+    kda_prep_kernel<false, false><<<grid, block, 0, stream>>>(q_raw, k_raw, v_raw, conv_w, a_logit,
                                                        b_logit, cu_seqlens, n_seqs, n_tokens, H,
-                                                       q, k, v, log_alpha, beta);
+                                                       q, k, v, log_alpha, beta, nullptr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prep_window(const void *q_raw, const void *k_raw, const void *v_raw,
+                               const float *conv_w, const float *a_logit, const float *b_logit,
+                               const int32_t *cu_seqlens, int32_t n_seqs, int64_t n_tokens,
+                               int32_t H, bool bf16, const void *win_in, void *win_out, void *q,
+                               void *k, void *v, float *log_alpha, float *beta,
+                               cudaStream_t stream) {
+  if (H == 0 || n_seqs == 0) return cudaSuccess;
+  if (n_tokens > 0) {
+    const int64_t blocks = (n_tokens + kRunTokens - 1) / kRunTokens;
+    if (blocks > 0x7fffffffLL || H > 65535) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)blocks, (unsigned)((H + kWarps - 1) / kWarps), 4);
+    if (bf16)
+      kda_prep_kernel<true, true><<<grid, 32 * kWarps, 0, stream>>>(
+          q_raw, k_raw, v_raw, conv_w, a_logit, b_logit, cu_seqlens, n_seqs, n_tokens, H, q, k, v,
+          log_alpha, beta, win_in);
+    else
+      kda_prep_kernel<false, true><<<grid, 32 * kWarps, 0, stream>>>(
+          q_raw, k_raw, v_raw, conv_w, a_logit, b_logit, cu_seqlens, n_seqs, n_tokens, H, q, k, v,
+          log_alpha, beta, win_in);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (win_out == nullptr) return cudaSuccess;
+  // after the prep kernel on the same stream: an in-place window is read first
+  if (n_seqs > 0x7fffffff || H > 65535 * kWarps) return cudaErrorInvalidValue;
+  const dim3 wgrid((unsigned)n_seqs, 3, (unsigned)((H + kWarps - 1) / kWarps));
+  if (bf16)
+    kda_conv_window_kernel<true><<<wgrid, 32 * kWarps, 0, stream>>>(
+        q_raw, k_raw, v_raw, cu_seqlens, n_seqs, n_tokens, H, win_in, win_out);
+  else
+    kda_conv_window_kernel<false><<<wgrid, 32 * kWarps, 0, stream>>>(
+        q_raw, k_raw, v_raw, cu_seqlens, n_seqs, n_tokens, H, win_in, win_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_layer_replay(float *state, void *win, const void *q_raw, const void *k_raw,
+                                const void *v_raw, const float *a_logit, const float *b_logit,
+                                const void *g, const float *conv_w, const float *gamma,
+                                const int32_t *n_accept, int32_t B, int32_t T, int32_t H,
+                                bool bf16, void *out, cudaStream_t stream) {
+  const int64_t units = (int64_t)B * H;
+  if (units == 0) return cudaSuccess;
+  if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (bf16)
+    kda_layer_replay_kernel<true><<<(unsigned)units, 256, 0, stream>>>(
+        state, win, q_raw, k_raw, v_raw, a_logit, b_logit, g, conv_w, gamma, n_accept, T, H, out);
+  else
+    kda_layer_replay_kernel<false><<<(unsigned)units, 256, 0, stream>>>(
+        state, win, q_raw, k_raw, v_raw, a_logit, b_logit, g, conv_w, gamma, n_accept, T, H, out);
   return cudaGetLastError();
 }
 

@@ -31,8 +31,8 @@ EXPORTED = ("kda_status_string", "kda_version", "kda_chunk_fwd_workspace_size",
             "kda_chunk_fwd", "kda_chunk_fwd_sched", "kda_read_device_status",
             "kda_read_device_status_detail", "kda_test_arm_timeout", "kda_decode_step",
             "kda_chunk_fwd_noalloc", "kda_noalloc_read_status", "kda_decode_replay",
-            "kda_prep_fwd", "kda_post_fwd", "kda_read_chunk_stats", "kda_chunk_fwd_transitions",
-            "kda_state_combine")
+            "kda_prep_fwd", "kda_prep_fwd_state", "kda_layer_replay", "kda_post_fwd",
+            "kda_read_chunk_stats", "kda_chunk_fwd_transitions", "kda_state_combine")
 
 _lib = None
 
@@ -93,6 +93,12 @@ def library() -> ctypes.CDLL:
         lib.kda_prep_fwd.restype = ctypes.c_int
         lib.kda_prep_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32,
                                      ctypes.c_int, vp, vp, vp, vp, vp, vp]
+        lib.kda_prep_fwd_state.restype = ctypes.c_int
+        lib.kda_prep_fwd_state.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32,
+                                           ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.kda_layer_replay.restype = ctypes.c_int
+        lib.kda_layer_replay.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
+                                         i32, i32, ctypes.c_int, vp, vp]
         lib.kda_post_fwd.restype = ctypes.c_int
         lib.kda_post_fwd.argtypes = [vp, vp, vp, i64, i32, i32, ctypes.c_int, vp, vp]
         lib.kda_decode_step.restype = ctypes.c_int
@@ -511,6 +517,75 @@ def kda_prep_fwd(q_raw, k_raw, v_raw, conv_w, a_logit, b_logit, cu_seqlens, *, s
                                 _ptr(log_alpha), _ptr(beta), _stream_handle(stream))
     _check(rc, "kda_prep_fwd")
     return q, k, v, log_alpha, beta
+
+
+def kda_prep_fwd_state(q_raw, k_raw, v_raw, conv_w, a_logit, b_logit, cu_seqlens,
+                       conv_state_in=None, conv_state_out=None, *, stream=None):
+    """``kda_prep_fwd`` continuing each packed sequence from a carried
+    convolution window: ``conv_state_in`` / ``conv_state_out``
+    ``[n_seqs, 3, 3, H, 128]`` in the dtype of the raw inputs ((q, k, v) x the
+    three raw rows before the sequence's next token, oldest first), either None
+    (zeros / not written), possibly the same tensor (updated in place).
+    Returns ``(q, k, v, log_alpha, beta)``."""
+    _need_cuda("q_raw", q_raw)
+    N, H, dk = q_raw.shape
+    dt = q_raw.dtype
+    _need_cuda("k_raw", k_raw, dt, (N, H, dk))
+    _need_cuda("v_raw", v_raw, dt, (N, H, dk))
+    _need_cuda("conv_w", conv_w, torch.float32, (3, H, dk, 4))
+    _need_cuda("a_logit", a_logit, torch.float32, (N, H, dk))
+    _need_cuda("b_logit", b_logit, torch.float32, (N, H))
+    _need_cuda("cu_seqlens", cu_seqlens, torch.int32)
+    n_seqs = cu_seqlens.shape[0] - 1
+    for name, w in (("conv_state_in", conv_state_in), ("conv_state_out", conv_state_out)):
+        if w is not None:
+            _need_cuda(name, w, dt, (n_seqs, 3, 3, H, dk))
+    q, k, v = (torch.empty_like(q_raw) for _ in range(3))
+    log_alpha = torch.empty_like(a_logit)
+    beta = torch.empty_like(b_logit)
+    rc = library().kda_prep_fwd_state(_ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(conv_w),
+                                      _ptr(a_logit), _ptr(b_logit), _ptr(cu_seqlens), n_seqs, N,
+                                      H, dk, dk, _dtype_code(q_raw), _ptr(conv_state_in),
+                                      _ptr(conv_state_out), _ptr(q), _ptr(k), _ptr(v),
+                                      _ptr(log_alpha), _ptr(beta), _stream_handle(stream))
+    _check(rc, "kda_prep_fwd_state")
+    return q, k, v, log_alpha, beta
+
+
+def kda_layer_replay(state, conv_state, q_raw, k_raw, v_raw, a_logit, b_logit, g, conv_w, gamma,
+                     n_accept, *, out=None, output=True, stream=None):
+    """The layer between its projections replayed over the accepted draft
+    tokens, in one kernel: state ``[B, H, 128, 128]`` fp32 and conv_state
+    ``[B, 3, 3, H, 128]`` (the raw inputs' dtype) are updated in place; q_raw,
+    k_raw, v_raw, g ``[B, T, H, 128]``; a_logit ``[B, T, H, 128]`` and b_logit
+    ``[B, T, H]`` fp32; conv_w ``[3, H, 128, 4]`` and gamma ``[128]`` fp32;
+    n_accept int32 CUDA ``[B]``.  Returns the gated, normalised layer output
+    ``[B, T, H, 128]`` (rows t >= n_accept[b] untouched) or None."""
+    _need_cuda("state", state, torch.float32)
+    B, H, dk, dv = state.shape
+    _need_cuda("q_raw", q_raw)
+    if q_raw.dim() != 4 or q_raw.shape[0] != B or q_raw.shape[2] != H or q_raw.shape[3] != dk:
+        raise ValueError("q_raw must be [B, T, H, 128]")
+    T = q_raw.shape[1]
+    dt = q_raw.dtype
+    for name, t in (("k_raw", k_raw), ("v_raw", v_raw), ("g", g)):
+        _need_cuda(name, t, dt, (B, T, H, dk))
+    _need_cuda("a_logit", a_logit, torch.float32, (B, T, H, dk))
+    _need_cuda("b_logit", b_logit, torch.float32, (B, T, H))
+    _need_cuda("conv_state", conv_state, dt, (B, 3, 3, H, dk))
+    _need_cuda("conv_w", conv_w, torch.float32, (3, H, dk, 4))
+    _need_cuda("gamma", gamma, torch.float32, (dk,))
+    _need_cuda("n_accept", n_accept, torch.int32, (B,))
+    if out is None and output:
+        out = torch.empty(B, T, H, dv, dtype=dt, device=q_raw.device)
+    if out is not None:
+        _need_cuda("out", out, dt, (B, T, H, dv))
+    rc = library().kda_layer_replay(_ptr(state), _ptr(conv_state), _ptr(q_raw), _ptr(k_raw),
+                                    _ptr(v_raw), _ptr(a_logit), _ptr(b_logit), _ptr(g),
+                                    _ptr(conv_w), _ptr(gamma), _ptr(n_accept), B, T, H, dk, dv,
+                                    _dtype_code(q_raw), _ptr(out), _stream_handle(stream))
+    _check(rc, "kda_layer_replay")
+    return out
 
 
 def kda_post_fwd(o, g, gamma, *, out=None, stream=None):

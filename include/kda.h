@@ -382,6 +382,67 @@ int kda_prep_fwd(const void *q_raw, const void *k_raw, const void *v_raw, const 
                  void *q, void *k, void *v, float *log_alpha, float *beta, void *stream);
 
 /*
+ * kda_prep_fwd continuing every packed sequence across calls: the short
+ * convolution reads the three raw rows before each sequence's first token in
+ * this call from a carried window instead of zeros, so a prefill may be split
+ * into several calls, and decode steps (every sequence of length 1) continue
+ * the same window ("Kimi K3: 架构、训练与系统全景解析", section 4.2.3: the short
+ * convolution of kernel size 4 before the recurrence; section 7.4: decode
+ * carries a fixed-size per-sequence state).  Arguments as kda_prep_fwd, plus:
+ *   conv_state_in  [n_seqs, 3, 3, H, 128] dtype or NULL (zeros): per sequence,
+ *                  for q, k and v, the three raw (unconvolved) rows before
+ *                  its first token here, oldest first;
+ *   conv_state_out [n_seqs, 3, 3, H, 128] dtype or NULL (not written): the
+ *                  same three rows before the token after this call: the
+ *                  sequence's last three raw rows, or, for a sequence shorter
+ *                  than three tokens, the newest rows of conv_state_in
+ *                  followed by all of its rows.
+ * conv_state_out may be conv_state_in itself (updated in place, after every
+ * read of it); otherwise neither may overlap the other or any tensor argument.
+ * The results equal kda_prep_fwd over the concatenated tokens of all calls.
+ * Alignment: the windows 4 elements.  Errors: as kda_prep_fwd.
+ */
+int kda_prep_fwd_state(const void *q_raw, const void *k_raw, const void *v_raw,
+                       const float *conv_w, const float *a_logit, const float *b_logit,
+                       const int32_t *cu_seqlens, int32_t n_seqs, int64_t n_tokens, int32_t H,
+                       int32_t dk, int32_t dv, int dtype, const void *conv_state_in,
+                       void *conv_state_out, void *q, void *k, void *v, float *log_alpha,
+                       float *beta, void *stream);
+
+/*
+ * The whole KDA layer between its projections, replayed over the accepted
+ * draft tokens of a speculative decode step in one kernel ("Kimi K3: 架构、训练
+ * 与系统全景解析", KDA state replay under speculative decoding: the short
+ * convolution, norms, gating, the KDA recurrence and the output norm are fused
+ * and replayed on chip over the accepted prefix; the recurrent state and the
+ * convolution window are written back once).  For every sequence b and head h,
+ * with n_b = n_accept[b] clamped to [0, T], tokens t = 0 .. n_b - 1 in order:
+ *   q, k, v, log_alpha, beta = kda_prep_fwd_state of the cached raw rows from
+ *       the sequence's window (so q, k are L2-normalised Swish(conv(.)) and v
+ *       is Swish(conv(.)), in fp32 inside the kernel);
+ *   the decode step of kda_decode_step on the state;
+ *   out = the kda_post_fwd of that step's output o with gate logits g.
+ *   state      [B, H, 128, 128] fp32, IN PLACE (untouched if n_b = 0)
+ *   conv_state [B, 3, 3, H, 128] dtype, IN PLACE: (q, k, v) x three raw rows,
+ *              oldest first, before the next token (untouched if n_b = 0)
+ *   q_raw, k_raw, v_raw, g  [B, T, H, 128] dtype  cached projections / gate logits
+ *   a_logit    [B, T, H, 128] fp32;  b_logit [B, T, H] fp32
+ *   conv_w     [3, H, 128, 4] fp32;  gamma [128] fp32
+ *   n_accept   [B] int32, DEVICE memory
+ *   out        [B, T, H, 128] dtype or NULL; rows t >= n_b are not written
+ * The library's layout, not the pages' (they give none).
+ * Alignment: state, conv_w, gamma 16 bytes; out 4 elements; the rest one element.
+ * Errors (before any launch): KDA_ERR_INVALID_ARG (NULL pointer other than
+ * out, B < 0, T <= 0, H <= 0, misalignment, out overlapping state or the
+ * window, the window overlapping the state), KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA.
+ */
+int kda_layer_replay(float *state, void *conv_state, const void *q_raw, const void *k_raw,
+                     const void *v_raw, const float *a_logit, const float *b_logit, const void *g,
+                     const float *conv_w, const float *gamma, const int32_t *n_accept, int32_t B,
+                     int32_t T, int32_t H, int32_t dk, int32_t dv, int dtype, void *out,
+                     void *stream);
+
+/*
  * The step after the recurrence ("Kimi K3: 架构、训练与系统全景解析", section
  * 4.2.6): head-wise RMSNorm of the recurrent output, then the sigmoid output
  * gate whose logits g come from the input-dependent full-rank projection

@@ -327,3 +327,56 @@ def test_host_pipeline_piece_bounds():
             assert all(x % 64 == 0 for x in b[:-1])
             assert all(b1 - b0 <= piece for b0, b1 in zip(b, b[1:]))
             assert all(b0 < b1 for b0, b1 in zip(b, b[1:]))
+
+
+def _prep_state(lib, **over):
+    n = 0x100000
+    args = dict(qr=A, kr=A + n, vr=A + 2 * n, w=A + 3 * n, a=A + 4 * n, b=A + 5 * n,
+                cu=A + 6 * n, n_seqs=1, N=64, H=2, dk=128, dv=128, dtype=1, wi=A + 12 * n,
+                wo=A + 13 * n, q=A + 7 * n, k=A + 8 * n, v=A + 9 * n, la=A + 10 * n,
+                beta=A + 11 * n, stream=None)
+    args.update(over)
+    vp = ctypes.c_void_p
+    return lib.kda_prep_fwd_state(*(vp(args[x]) for x in ("qr", "kr", "vr", "w", "a", "b", "cu")),
+                                  args["n_seqs"], args["N"], args["H"], args["dk"], args["dv"],
+                                  args["dtype"], vp(args["wi"]), vp(args["wo"]),
+                                  *(vp(args[x]) for x in ("q", "k", "v", "la", "beta", "stream")))
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(qr=None), 1), (dict(cu=None), 1), (dict(n_seqs=0), 1), (dict(H=0), 1),
+    (dict(dk=64), 2), (dict(dtype=3), 2), (dict(wi=A + 0xC00004), 1), (dict(wo=A + 0xD00002), 1),
+    (dict(wo=A + 0xC00100), 1),                 # windows overlap without being the same array
+    (dict(wo=A + 0x700000), 1),                 # window over the q output
+    (dict(wi=A), 1),                            # window over q_raw
+])
+def test_prep_state_rejects_before_launch(lib, over, code):
+    assert _prep_state(lib, **over) == code
+
+
+def _layer_replay(lib, **over):
+    n = 0x1000000
+    args = dict(state=A, win=A + n, qr=A + 2 * n, kr=A + 3 * n, vr=A + 4 * n, a=A + 5 * n,
+                b=A + 6 * n, g=A + 7 * n, w=A + 8 * n, gamma=A + 9 * n, na=A + 10 * n, B=4, T=3,
+                H=2, dk=128, dv=128, dtype=1, out=A + 11 * n, stream=None)
+    args.update(over)
+    vp = ctypes.c_void_p
+    return lib.kda_layer_replay(*(vp(args[x]) for x in ("state", "win", "qr", "kr", "vr", "a", "b",
+                                                         "g", "w", "gamma", "na")),
+                                args["B"], args["T"], args["H"], args["dk"], args["dv"],
+                                args["dtype"], vp(args["out"]), vp(args["stream"]))
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(state=None), 1), (dict(win=None), 1), (dict(g=None), 1), (dict(na=None), 1),
+    (dict(B=-1), 1), (dict(T=0), 1), (dict(H=0), 1), (dict(dk=64), 2), (dict(dtype=5), 2),
+    (dict(state=A + 8), 1), (dict(w=A + 0x8000004), 1), (dict(out=A + 0xB000002), 1),
+    (dict(win=A + 0x100), 1),                   # window inside the state
+    (dict(out=A + 0x1000000), 1),               # output over the window
+])
+def test_layer_replay_rejects_before_launch(lib, over, code):
+    assert _layer_replay(lib, **over) == code
+
+
+def test_layer_replay_empty_batch_launches_nothing(lib):
+    assert _layer_replay(lib, B=0) == 0

@@ -99,3 +99,107 @@ def test_post_closed_forms():
     big = L.post(o, np.full_like(g, 60.0), gamma)
     rms = np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + L.RMS_EPS)
     np.testing.assert_allclose(big, o / rms * gamma, rtol=1e-14)
+
+
+# ---- the convolution window carried across calls, and the fused layer replay
+
+def test_conv_window_of_zeros_equals_the_plain_convolution():
+    r = _rng(11)
+    lengths = [0, 1, 2, 3, 9]
+    H, d = 2, 5
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    w = r.standard_normal((H, d, 4))
+    x = r.standard_normal((cu[-1], H, d))
+    y, win = L.short_conv_state(x, w, cu, np.zeros((len(lengths), 3, H, d)))
+    np.testing.assert_array_equal(y, L.short_conv(x, w, cu))
+    # the window after the call: the last three raw rows, zeros before the start
+    for s, n in enumerate(lengths):
+        for i in range(3):
+            t = n - 3 + i
+            want = x[cu[s] + t] if t >= 0 else np.zeros((H, d))
+            np.testing.assert_array_equal(win[s, i], want)
+
+
+def test_conv_window_closed_form_on_zero_input():
+    """Zero input after a carried window s0, s1, s2 (oldest first): the taps read
+    the window, y[0] = w0 s0 + w1 s1 + w2 s2, y[1] = w0 s1 + w1 s2, y[2] = w0 s2,
+    then nothing; the window shifts in the zero rows."""
+    r = _rng(12)
+    H, d, T = 1, 3, 5
+    w = r.standard_normal((H, d, 4))
+    s = r.standard_normal((1, 3, H, d))
+    y, win = L.short_conv_state(np.zeros((T, H, d)), w, [0, T], s)
+    w0, w1, w2 = w[..., 0], w[..., 1], w[..., 2]
+    np.testing.assert_allclose(y[0], w0 * s[0, 0] + w1 * s[0, 1] + w2 * s[0, 2], rtol=1e-15)
+    np.testing.assert_allclose(y[1], w0 * s[0, 1] + w1 * s[0, 2], rtol=1e-15)
+    np.testing.assert_allclose(y[2], w0 * s[0, 2], rtol=1e-15)
+    assert not y[3:].any() and not win.any()
+    # a one-token call keeps the newest two rows of the window, then the token
+    x1 = r.standard_normal((1, H, d))
+    _, win1 = L.short_conv_state(x1, w, [0, 1], s)
+    np.testing.assert_array_equal(win1[0], np.stack([s[0, 1], s[0, 2], x1[0]]))
+
+
+def test_prep_split_at_any_token_with_the_carried_window_equals_one_call():
+    """prep of x[0:t] then prep of x[t:T] from the window the first call returned
+    equals prep of x[0:T], for cuts inside, before and at the kernel width, and
+    a two-call chain of one-token pieces."""
+    r = _rng(13)
+    T, H, d = 11, 2, 8
+    x = {n: r.standard_normal((T, H, d)) for n in ("q", "k", "v", "a")}
+    b = r.standard_normal((T, H))
+    cw = r.standard_normal((3, H, d, 4))
+    full = L.prep(x["q"], x["k"], x["v"], cw, x["a"], b, [0, T])
+    zero = np.zeros((1, 3, 3, H, d))
+    for cut in (0, 1, 2, 3, 4, 7, T):
+        first = L.prep_state(x["q"][:cut], x["k"][:cut], x["v"][:cut], cw, x["a"][:cut], b[:cut],
+                             [0, cut], zero)
+        second = L.prep_state(x["q"][cut:], x["k"][cut:], x["v"][cut:], cw, x["a"][cut:],
+                              b[cut:], [0, T - cut], first[5])
+        for i in range(5):
+            np.testing.assert_allclose(np.concatenate([first[i], second[i]]), full[i],
+                                       rtol=1e-14, atol=1e-15)
+    # token by token, as decode calls it
+    win = zero
+    for t in range(T):
+        step = L.prep_state(x["q"][t:t + 1], x["k"][t:t + 1], x["v"][t:t + 1], cw,
+                            x["a"][t:t + 1], b[t:t + 1], [0, 1], win)
+        win = step[5]
+        for i in range(5):
+            np.testing.assert_allclose(step[i][0], full[i][t], rtol=1e-14, atol=1e-15)
+
+
+def test_layer_replay_equals_prep_recurrence_post_chain():
+    """The fused replay against the unfused chain run independently: prep with
+    the window, the C oracle's chunk loop (a different code path from its
+    decode step) from the state, then post; rejected tokens leave nothing,
+    nothing accepted leaves state and window untouched, counts above T clamp."""
+    import oracle
+    r = _rng(14)
+    B, T, H, d = 4, 5, 2, 128
+    raw = {n: r.standard_normal((B, T, H, d)) for n in ("q", "k", "v", "a", "g")}
+    bl = r.standard_normal((B, T, H))
+    cw = 0.5 * r.standard_normal((3, H, d, 4))
+    gamma = 1 + 0.1 * r.standard_normal(d)
+    state0 = 0.02 * r.standard_normal((B, H, d, d))
+    win0 = r.standard_normal((B, 3, 3, H, d))
+    n = np.array([3, 0, 9, 1])
+    state, win = state0.copy(), win0.copy()
+    out = L.layer_replay(state, win, raw["q"], raw["k"], raw["v"], raw["a"], bl, raw["g"], cw,
+                         gamma, n, oracle.decode_step)
+    for b in range(B):
+        nb = min(int(n[b]), T)
+        if nb == 0:
+            np.testing.assert_array_equal(state[b], state0[b])
+            np.testing.assert_array_equal(win[b], win0[b])
+            assert not out[b].any()
+            continue
+        q, k, v, la, be, w_ref = L.prep_state(raw["q"][b, :nb], raw["k"][b, :nb],
+                                              raw["v"][b, :nb], cw, raw["a"][b, :nb],
+                                              bl[b, :nb], [0, nb], win0[b:b + 1])
+        o, fin = oracle.chunk_fwd(q, k, v, la, be, state0[b:b + 1], [0, nb])
+        np.testing.assert_allclose(out[b, :nb], L.post(o, raw["g"][b, :nb], gamma),
+                                   rtol=1e-10, atol=1e-12)
+        assert not out[b, nb:].any()
+        np.testing.assert_allclose(state[b], fin[0], rtol=1e-11, atol=1e-14)
+        np.testing.assert_array_equal(win[b], w_ref[0])
