@@ -5,7 +5,9 @@ TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 package.  The CUDA product path never imports it, and the two share no code.
 
 ``kda_oracle.c`` holds the token-by-token recurrence (update and read-out of
-the "Kimi K3" study notes, section 3-2 "2) Kimi Delta Attention"); ``affine.py``
+the "Kimi K3" study notes, section 3-2 "2) Kimi Delta Attention");
+``kda_oracle_bwd.c`` its gradient, the chain rule through the same token loop
+in reverse; ``affine.py``
 holds an independent brute-force form built from explicit transition matrices
 (the affine-pair view of "Kimi K3: 架构、训练与系统全景解析" section 7.1, KCP).
 """
@@ -22,11 +24,14 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kda_oracle.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libkda_oracle.so")
+_SRC_BWD = os.path.join(_HERE, "kda_oracle_bwd.c")
+_LIB_BWD_PATH = os.path.join(_BUILD_DIR, "libkda_oracle_bwd.so")
 # Same flags on x86_64 and aarch64: no FMA contraction, IEEE fp64 throughout.
 CFLAGS = ["-O2", "-fPIC", "-shared", "-pthread", "-ffp-contract=off", "-fno-fast-math"]
 
 _lock = threading.Lock()
 _lib = None
+_lib_bwd = None
 
 
 def compile_source(src: str, out_path: str) -> str:
@@ -38,13 +43,33 @@ def compile_source(src: str, out_path: str) -> str:
 
 
 def build(force: bool = False) -> str:
-    """Compile ``kda_oracle.c`` into ``oracle/_build/libkda_oracle.so``."""
+    """Compile ``kda_oracle.c`` into ``oracle/_build/libkda_oracle.so`` (and the
+    gradient, ``kda_oracle_bwd.c``, into ``libkda_oracle_bwd.so``)."""
     with _lock:
-        stale = (not os.path.exists(_LIB_PATH)) or (
-            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
-        if force or stale:
-            compile_source(_SRC, _LIB_PATH)
+        for src, lib in ((_SRC, _LIB_PATH), (_SRC_BWD, _LIB_BWD_PATH)):
+            stale = (not os.path.exists(lib)) or os.path.getmtime(lib) < os.path.getmtime(src)
+            if force or stale:
+                compile_source(src, lib)
     return _LIB_PATH
+
+
+def load_bwd_library(path: str) -> ctypes.CDLL:
+    lib = ctypes.CDLL(path)
+    dp = ctypes.POINTER(ctypes.c_double)
+    lib.kda_oracle_chunk_bwd.restype = ctypes.c_int
+    lib.kda_oracle_chunk_bwd.argtypes = [dp, dp, dp, dp, dp, dp, ctypes.POINTER(ctypes.c_int64),
+                                         ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                         ctypes.c_int64, dp, dp, dp, dp, dp, dp, dp, dp,
+                                         ctypes.c_int]
+    return lib
+
+
+def _default_bwd_lib() -> ctypes.CDLL:
+    global _lib_bwd
+    if _lib_bwd is None:
+        build()
+        _lib_bwd = load_bwd_library(_LIB_BWD_PATH)
+    return _lib_bwd
 
 
 def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
@@ -119,6 +144,36 @@ def chunk_fwd(q, k, v, log_alpha, beta, init_state=None, cu_seqlens=None,
     if rc != 0:
         raise RuntimeError(f"kda_oracle_chunk_fwd failed with code {rc}")
     return out, fin
+
+
+def chunk_bwd(q, k, v, log_alpha, beta, init_state, cu_seqlens, d_out, d_final=None,
+              n_threads: int | None = None, lib: ctypes.CDLL | None = None):
+    """Gradient of ``chunk_fwd`` for a loss with gradients ``d_out`` ``[N, H, dv]``
+    (every output) and ``d_final`` ``[n_seqs, H, dk, dv]`` or None (the final
+    states).  Returns ``(dq, dk, dv, d_log_alpha, d_beta, d_init_state)`` as fp64
+    numpy arrays in the layouts of q, k, v, log_alpha, beta and init_state."""
+    lib = lib or _default_bwd_lib()
+    q, k, v, la, b, do = (_f64(t) for t in (q, k, v, log_alpha, beta, d_out))
+    s0, df = _f64(init_state), _f64(d_final)
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    if cu_seqlens is None:
+        cu = np.array([0, N], dtype=np.int64)
+    else:
+        if hasattr(cu_seqlens, "detach"):
+            cu_seqlens = cu_seqlens.detach().to("cpu").numpy()
+        cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
+    n_seqs = cu.shape[0] - 1
+    dq, dkk = np.zeros((N, H, dk)), np.zeros((N, H, dk))
+    dvv, dla, db = np.zeros((N, H, dv)), np.zeros((N, H, dk)), np.zeros((N, H))
+    ds0 = np.zeros((n_seqs, H, dk, dv))
+    rc = lib.kda_oracle_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(b), _ptr(s0),
+                                  _ptr(cu, ctypes.c_int64), n_seqs, H, dk, dv, _ptr(do), _ptr(df),
+                                  _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dla), _ptr(db), _ptr(ds0),
+                                  int(n_threads or default_threads()))
+    if rc != 0:
+        raise RuntimeError(f"kda_oracle_chunk_bwd failed with code {rc}")
+    return dq, dkk, dvv, dla, db, ds0
 
 
 def decode_step(state, q, k, v, log_alpha, beta, lib: ctypes.CDLL | None = None):
