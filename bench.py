@@ -511,6 +511,69 @@ def decode_sequence_bench(dev, peaks, steps: int = 100, warmup_steps: int = 3, s
     return res
 
 
+# Backward pass: flops per token-head of the minimal chain rule with the states
+# at hand (X, p and S_t of the forward step, 3 d^2 multiply-adds; dS += q do^T,
+# dq, dd, dk (two terms), dX, dlog_alpha and dS_{t-1}, 8 d^2), 2 flops each.
+BWD_FLOP_PER_TOKEN_HEAD = 2 * 11 * 128 * 128
+# Bytes per token-head (bf16): q, k, v, d_out in, dq, dk, dv out (7 x 256), fp32
+# log_alpha in and its gradient out (2 x 512), beta and its gradient (8).
+BWD_BYTES_PER_TOKEN_HEAD = 7 * 256 + 2 * 512 + 8
+
+
+def fp32_alu_peak_tflops(dev):
+    """FP32 FMA peak from the unit counts: SMs x 128 FP32 lanes x 2 flops x the
+    maximum SM clock (2,070 MHz on a GB300)."""
+    import torch
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    return sms * 128 * 2 * 2.07e9 / 1e12
+
+
+def backward_bench(dev, peaks, workload: str = "b4_h16_t4096", steps: int = 5, warmup: int = 2):
+    """kda_chunk_bwd on a prefill workload (every gradient, random output and
+    final-state gradients): the checkpoint, backward and conversion kernels,
+    CUDA events around each launch."""
+    import torch
+    from gated_delta_rule_13_gb300 import inputs, kda
+    w = inputs.WORKLOADS[workload]
+    x = inputs.workload_inputs(workload, device=dev)
+    n_tok, H = int(x["q"].shape[0]), w.H
+    n_seqs = len(x["lengths"])
+    g = torch.Generator(device=dev).manual_seed(7)
+    do = torch.randn(n_tok, H, 128, generator=g, device=dev).to(x["q"].dtype)
+    df = torch.randn(n_seqs, H, 128, 128, generator=g, device=dev)
+    ws = torch.empty(kda.kda_chunk_bwd_workspace_size(n_seqs, n_tok, H), dtype=torch.uint8,
+                     device=dev)
+
+    def run():
+        kda.kda_chunk_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["init_state"],
+                          x["cu_seqlens"], do, df, workspace=ws)
+
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        run()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    th = n_tok * H
+    tflops = th * BWD_FLOP_PER_TOKEN_HEAD / (ms / 1000.0) / 1e12
+    peak = fp32_alu_peak_tflops(dev)
+    nbytes = th * BWD_BYTES_PER_TOKEN_HEAD + n_seqs * H * 3 * STATE_BYTES
+    del x, do, df, ws
+    torch.cuda.empty_cache()
+    return {"workload": f"{workload}: {w.note}", "ms_per_launch": ms,
+            "tokens_per_s": n_tok / (ms / 1000.0),
+            "hbm_gbs": nbytes / (ms / 1000.0) / 1e9,
+            "roofline": {"bound": "alu", "kernel": "kda_bwd_kernel", "achieved": tflops,
+                         "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                         "peak_source": "derived: SMs x 128 fp32 lanes x 2 x 2,070 MHz",
+                         "traffic": None, "flop_per_launch": th * BWD_FLOP_PER_TOKEN_HEAD}}
+
+
 def prefill_bytes(x, H):
     n_tok = int(x["q"].shape[0])
     n_seqs = int(x["cu_seqlens"].shape[0] - 1)
@@ -642,6 +705,7 @@ def run_gpu(args):
     few_chains = few_chains_bench(dev, peaks, steps=args.sub_steps)
     layer_ops = layer_ops_bench(dev, peaks, steps=args.sub_steps, T=args.layer_tokens)
     layer_replay = layer_replay_bench(dev, peaks, steps=args.sub_steps)
+    backward = backward_bench(dev, peaks) if args.backward else None
     configs = {}
     for wl, n in (("b4_h16_t4096", args.sub_steps), ("varlen_h96_1m", args.varlen_steps)):
         if n > 0:
@@ -696,6 +760,7 @@ def run_gpu(args):
         "prefill_few_chains": few_chains,
         "layer_ops": layer_ops,
         "layer_replay": layer_replay,
+        "backward": backward,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": 2 * args.steps,
@@ -728,6 +793,8 @@ def main():
                     help="tokens of the per-token-step sub-benchmark (96 heads)")
     ap.add_argument("--decode-steps", type=int, default=100,
                     help="consecutive in-place steps of the decode sub-benchmark")
+    ap.add_argument("--no-backward", dest="backward", action="store_false",
+                    help="skip the backward-pass sub-benchmark")
     ap.add_argument("--varlen-steps", type=int, default=5,
                     help="timed launches of the million-token varlen prefill (0: skip it)")
     args = ap.parse_args()

@@ -118,9 +118,121 @@ bool is_device_pointer(const void *p, bool *ok) {
   return attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged;
 }
 
+// Backward-pass workspace: status block, device copy of a host cu_seqlens, the
+// state checkpoints, and the fp32 accumulators of dq and dk.
+struct BwdLayout {
+  size_t cu, ckpt, dq, dk, total;
+};
+BwdLayout bwd_layout(int32_t n_seqs, int64_t n_tokens, int32_t H) {
+  BwdLayout l;
+  l.cu = kStatusBytes;
+  l.ckpt = l.cu + round_up(sizeof(int32_t) * ((size_t)n_seqs + 1), 256);
+  l.dq = l.ckpt + round_up(kda::bwd_ckpt_slots(n_seqs, n_tokens) * H * kHeadDim * kHeadDim * 4, 256);
+  l.dk = l.dq + round_up((size_t)n_tokens * H * kHeadDim * 4, 256);
+  l.total = l.dk + round_up((size_t)n_tokens * H * kHeadDim * 4, 256);
+  return l;
+}
+
 }  // namespace
 
 extern "C" {
+
+int kda_chunk_bwd_workspace_size(int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk,
+                                 int32_t dv, int dtype, size_t *bytes) {
+  if (!bytes || n_seqs < 0 || n_tokens < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+  const int d = check_dims(dk, dv, dtype);
+  if (d != KDA_OK) return d;
+  *bytes = bwd_layout(n_seqs, n_tokens, H).total;
+  return KDA_OK;
+}
+
+int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                  const float *beta, const float *init_state, const int32_t *cu_seqlens,
+                  int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk, int32_t dv, int dtype,
+                  const void *d_out, const float *d_final_state, void *dq, void *dk_, void *dv_,
+                  float *d_log_alpha, float *d_beta, float *d_init_state, void *workspace,
+                  size_t workspace_bytes, void *stream) {
+  if (n_seqs < 0 || n_tokens < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+  const int d = check_dims(dk, dv, dtype);
+  if (d != KDA_OK) return d;
+  if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
+  if (n_tokens > 0 && (!q || !k || !v || !log_alpha || !beta || !d_out || !dq || !dk_ || !dv_ ||
+                       !d_log_alpha || !d_beta))
+    return KDA_ERR_INVALID_ARG;
+  if ((int64_t)n_seqs * H * 4 > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+  const size_t esz = dtype == KDA_BF16 ? 2 : 4;
+  const void *elem[] = {q, k, v, d_out, dq, dk_, dv_};
+  for (const void *p : elem)
+    if (p && !aligned(p, esz)) return KDA_ERR_INVALID_ARG;
+  const void *f32[] = {log_alpha, beta, init_state, d_final_state, d_log_alpha, d_beta,
+                       d_init_state};
+  for (const void *p : f32)
+    if (p && !aligned(p, 4)) return KDA_ERR_INVALID_ARG;
+  // no output may overlap an input or another output
+  const size_t nt = (size_t)n_tokens * H;
+  const size_t sb = (size_t)n_seqs * H * dk * dv * 4;
+  const void *outs[] = {dq, dk_, dv_, d_log_alpha, d_beta, d_init_state};
+  const size_t out_b[] = {nt * dk * esz, nt * dk * esz, nt * dv * esz, nt * dk * 4, nt * 4, sb};
+  const void *ins[] = {q, k, v, log_alpha, beta, init_state, d_out, d_final_state};
+  const size_t in_b[] = {nt * dk * esz, nt * dk * esz, nt * dv * esz, nt * dk * 4, nt * 4, sb,
+                         nt * dv * esz, sb};
+  for (int i = 0; i < 6; ++i) {
+    if (!outs[i] || out_b[i] == 0) continue;
+    for (int j = 0; j < 8; ++j)
+      if (ins[j] && in_b[j] > 0 && ranges_overlap(outs[i], out_b[i], ins[j], in_b[j]))
+        return KDA_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 6; ++j)
+      if (outs[j] && out_b[j] > 0 && ranges_overlap(outs[i], out_b[i], outs[j], out_b[j]))
+        return KDA_ERR_INVALID_ARG;
+  }
+  const BwdLayout lay = bwd_layout(n_seqs, n_tokens, H);
+  if (!workspace || workspace_bytes < lay.total || !aligned16(workspace)) return KDA_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  bool attr_ok = false;
+  const bool cu_on_device = is_device_pointer(cu_seqlens, &attr_ok);
+  if (!attr_ok) return KDA_ERR_CUDA;
+  const int32_t *cu_dev = cu_seqlens;
+  if (!cu_on_device) {
+    if (cu_seqlens[0] != 0 || cu_seqlens[n_seqs] != n_tokens) return KDA_ERR_INVALID_ARG;
+    for (int32_t s = 0; s < n_seqs; ++s)
+      if (cu_seqlens[s + 1] < cu_seqlens[s]) return KDA_ERR_INVALID_ARG;
+    int32_t *dst = reinterpret_cast<int32_t *>(ws + lay.cu);
+    if (cudaMemcpyAsync(dst, cu_seqlens, sizeof(int32_t) * ((size_t)n_seqs + 1),
+                        cudaMemcpyHostToDevice, st) != cudaSuccess) {
+      cudaGetLastError();
+      return KDA_ERR_CUDA;
+    }
+    cu_dev = dst;
+  }
+  kda::DeviceStatus *status = reinterpret_cast<kda::DeviceStatus *>(ws);
+  const bool ok = cudaMemsetAsync(status, 0, sizeof(kda::DeviceStatus), st) == cudaSuccess &&
+                  (nt == 0 || (cudaMemsetAsync(ws + lay.dq, 0, lay.total - lay.dq, st) == cudaSuccess &&
+                               cudaMemsetAsync(d_log_alpha, 0, nt * dk * 4, st) == cudaSuccess &&
+                               cudaMemsetAsync(d_beta, 0, nt * 4, st) == cudaSuccess));
+  if (!ok) {
+    cudaGetLastError();
+    return KDA_ERR_CUDA;
+  }
+  if (n_seqs == 0) return KDA_OK;
+  kda::BwdArgs a;
+  a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.init_state = init_state;
+  a.cu_seqlens = cu_dev; a.n_seqs = n_seqs; a.n_tokens = n_tokens; a.H = H;
+  a.bf16 = dtype == KDA_BF16;
+  a.d_out = d_out; a.d_final = d_final_state;
+  a.dq = dq; a.dk = dk_; a.dv = dv_; a.d_log_alpha = d_log_alpha; a.d_beta = d_beta;
+  a.d_init = d_init_state;
+  a.ckpt = reinterpret_cast<float *>(ws + lay.ckpt);
+  a.dq_acc = reinterpret_cast<float *>(ws + lay.dq);
+  a.dk_acc = reinterpret_cast<float *>(ws + lay.dk);
+  a.status = status;
+  const cudaError_t e = kda::launch_chunk_bwd(a, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_CUDA;
+  }
+  return KDA_OK;
+}
 
 const char *kda_status_string(int status) {
   switch (status) {

@@ -139,6 +139,28 @@ cudaError_t launch_layer_replay(float *state, void *win, const void *q_raw, cons
                                 const int32_t *n_accept, int32_t B, int32_t T, int32_t H,
                                 bool bf16, void *out, cudaStream_t stream);
 
+// Backward pass (kda_chunk_bwd).  Workspace pieces are device pointers.
+struct BwdArgs {
+  const void *q, *k, *v;
+  const float *log_alpha, *beta, *init_state;
+  const int32_t *cu_seqlens;  // device
+  int32_t n_seqs;
+  int64_t n_tokens;
+  int32_t H;
+  bool bf16;
+  const void *d_out;
+  const float *d_final;       // or nullptr
+  void *dq, *dk, *dv;
+  float *d_log_alpha, *d_beta, *d_init;  // d_init may be nullptr
+  // workspace
+  float *ckpt;                // [bwd_ckpt_slots][H][128][128]
+  float *dq_acc, *dk_acc;     // [n_tokens][H][128], zeroed
+  DeviceStatus *status;
+};
+// Checkpoint slots the backward pass needs (states stored every 16 tokens).
+size_t bwd_ckpt_slots(int32_t n_seqs, int64_t n_tokens);
+cudaError_t launch_chunk_bwd(const BwdArgs &a, cudaStream_t stream);
+
 cudaError_t launch_post(const void *o, const void *g, const float *gamma, int64_t n_tokens,
                         int32_t H, bool bf16, void *out, cudaStream_t stream);
 

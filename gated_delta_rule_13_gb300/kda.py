@@ -32,7 +32,8 @@ EXPORTED = ("kda_status_string", "kda_version", "kda_chunk_fwd_workspace_size",
             "kda_read_device_status_detail", "kda_test_arm_timeout", "kda_decode_step",
             "kda_chunk_fwd_noalloc", "kda_noalloc_read_status", "kda_decode_replay",
             "kda_prep_fwd", "kda_prep_fwd_state", "kda_layer_replay", "kda_post_fwd",
-            "kda_read_chunk_stats", "kda_chunk_fwd_transitions", "kda_state_combine")
+            "kda_read_chunk_stats", "kda_chunk_fwd_transitions", "kda_state_combine",
+            "kda_chunk_bwd", "kda_chunk_bwd_workspace_size")
 
 _lib = None
 
@@ -99,6 +100,12 @@ def library() -> ctypes.CDLL:
         lib.kda_layer_replay.restype = ctypes.c_int
         lib.kda_layer_replay.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
                                          i32, i32, ctypes.c_int, vp, vp]
+        lib.kda_chunk_bwd.restype = ctypes.c_int
+        lib.kda_chunk_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32,
+                                      ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        lib.kda_chunk_bwd_workspace_size.restype = ctypes.c_int
+        lib.kda_chunk_bwd_workspace_size.argtypes = [i32, i64, i32, i32, i32, ctypes.c_int,
+                                                     ctypes.POINTER(sz)]
         lib.kda_post_fwd.restype = ctypes.c_int
         lib.kda_post_fwd.argtypes = [vp, vp, vp, i64, i32, i32, ctypes.c_int, vp, vp]
         lib.kda_decode_step.restype = ctypes.c_int
@@ -210,6 +217,59 @@ def kda_chunk_fwd(q, k, v, log_alpha, beta, init_state=None, cu_seqlens=None, *,
                 -1 if max_helpers is None else int(max_helpers))
         _check(library().kda_chunk_fwd_sched(*args, *caps, *ws_args), "kda_chunk_fwd_sched")
     return out, final_state
+
+
+def kda_chunk_bwd_workspace_size(n_seqs: int, n_tokens: int, H: int, dk: int = HEAD_DIM,
+                                 dv: int = HEAD_DIM, dtype: int = KDA_BF16) -> int:
+    out = ctypes.c_size_t(0)
+    _check(library().kda_chunk_bwd_workspace_size(n_seqs, n_tokens, H, dk, dv, dtype,
+                                                  ctypes.byref(out)),
+           "kda_chunk_bwd_workspace_size")
+    return out.value
+
+
+def kda_chunk_bwd(q, k, v, log_alpha, beta, init_state, cu_seqlens, d_out, d_final_state=None,
+                  *, workspace=None, want_d_init=True, stream=None):
+    """Gradients of ``kda_chunk_fwd`` for output gradients ``d_out`` ``[N, H, 128]``
+    (dtype of q) and final-state gradients ``d_final_state`` (or None).  Returns
+    ``(dq, dk, dv, d_log_alpha, d_beta, d_init_state)`` in the layouts of the
+    inputs (d_init_state None unless requested)."""
+    _need_cuda("q", q)
+    N, H, dk = q.shape
+    dt = q.dtype
+    _need_cuda("k", k, dt, (N, H, dk))
+    _need_cuda("v", v, dt)
+    dv = v.shape[2]
+    _need_cuda("log_alpha", log_alpha, torch.float32, (N, H, dk))
+    _need_cuda("beta", beta, torch.float32, (N, H))
+    _need_cuda("d_out", d_out, dt, (N, H, dv))
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, N], dtype=torch.int32, device=q.device)
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_contiguous():
+        raise TypeError("cu_seqlens must be a contiguous 1-D int32 tensor")
+    n_seqs = cu_seqlens.shape[0] - 1
+    if init_state is not None:
+        _need_cuda("init_state", init_state, torch.float32, (n_seqs, H, dk, dv))
+    if d_final_state is not None:
+        _need_cuda("d_final_state", d_final_state, torch.float32, (n_seqs, H, dk, dv))
+    dq, dkk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dla = torch.empty_like(log_alpha)
+    db = torch.empty_like(beta)
+    ds0 = (torch.empty(n_seqs, H, dk, dv, dtype=torch.float32, device=q.device)
+           if want_d_init else None)
+    code = _dtype_code(q)
+    if workspace is None:
+        workspace = torch.empty(kda_chunk_bwd_workspace_size(n_seqs, N, H, dk, dv, code),
+                                dtype=torch.uint8, device=q.device)
+    _need_cuda("workspace", workspace)
+    rc = library().kda_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                 _ptr(init_state), _ptr(cu_seqlens), n_seqs, N, H, dk, dv, code,
+                                 _ptr(d_out), _ptr(d_final_state), _ptr(dq), _ptr(dkk), _ptr(dvv),
+                                 _ptr(dla), _ptr(db), _ptr(ds0), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(),
+                                 _stream_handle(stream))
+    _check(rc, "kda_chunk_bwd")
+    return dq, dkk, dvv, dla, db, ds0
 
 
 def kda_chunk_fwd_transitions(q, k, v, log_alpha, beta, cu_seqlens=None, *, workspace=None,

@@ -150,6 +150,49 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
                   size_t workspace_bytes, void *stream);
 
 /*
+ * The gradient of kda_chunk_fwd (the backward pass for training: "Kimi K3:
+ * 架构、训练与系统全景解析", section 7.1, the chunked KDA kernel serves training
+ * as well as prefill; the pages print no gradient, so this is the chain rule
+ * through the update and read-out above, in reverse token order).  For a loss
+ * whose gradients with respect to every output o_t (d_out) and every final
+ * state (d_final_state) are given, it returns the gradients with respect to
+ * every input:
+ *   d_out        [N, H, dv]  dtype           gradient of the outputs
+ *   d_final_state [S, H, dk, dv] fp32 or NULL (zero)
+ *   dq, dk       [N, H, dk]  dtype;  dv [N, H, dv] dtype
+ *   d_log_alpha  [N, H, dk]  fp32;   d_beta [N, H] fp32
+ *   d_init_state [S, H, dk, dv] fp32 or NULL (not written); the gradient with
+ *                respect to init_state (also when init_state is NULL: the
+ *                gradient at the zero state)
+ * The other arguments are those of kda_chunk_fwd (same inputs, same
+ * cu_seqlens rules: host arrays are validated here, device arrays in the
+ * kernel, which records KDA_ERR_INVALID_ARG and writes nothing).  The states
+ * are recomputed: a forward sweep stores the state before every 16th token in
+ * the workspace, and the reverse sweep recomputes the states in between.  fp32
+ * arithmetic on CUDA cores; dq, dk, d_log_alpha and d_beta are sums over the
+ * value channels, added in fp32 in an order that may vary between calls (last
+ * bits only).
+ * Alignment: element alignment for every tensor.  No output may overlap an
+ * input or another output.
+ * Errors: as kda_chunk_fwd, with the workspace of kda_chunk_bwd_workspace_size.
+ */
+int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                  const float *beta, const float *init_state, const int32_t *cu_seqlens,
+                  int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk, int32_t dv, int dtype,
+                  const void *d_out, const float *d_final_state, void *dq, void *dk_, void *dv_,
+                  float *d_log_alpha, float *d_beta, float *d_init_state, void *workspace,
+                  size_t workspace_bytes, void *stream);
+
+/*
+ * Bytes of device workspace kda_chunk_bwd needs: the status block, a device
+ * copy of a host cu_seqlens, the stored states (64 KiB per head for every 16
+ * tokens and per sequence) and fp32 accumulators of dq and dk.
+ * Errors: as kda_chunk_fwd_workspace_size.
+ */
+int kda_chunk_bwd_workspace_size(int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk,
+                                 int32_t dv, int dtype, size_t *bytes);
+
+/*
  * kda_chunk_fwd with the schedule capped by the caller.  Arguments, results
  * and errors are those of kda_chunk_fwd, plus:
  *   max_split    upper bound on the segments per sequence of the in-device

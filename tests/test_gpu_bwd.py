@@ -1,0 +1,116 @@
+"""GPU parity of the backward pass (kda_chunk_bwd) against the fp64 gradient
+oracle (oracle/kda_oracle_bwd.c, itself pinned by finite differences of the
+forward oracle): every gradient, whole tensor, every (sequence, head) slice and
+every row."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_delta_rule_13_gb300 import inputs, kda
+from parity_util import TOL, assert_parity
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _grads_in(x, seed, d_final=True):
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    N, H, _ = x["q"].shape
+    do = torch.randn(N, H, 128, generator=g, device=DEV).to(x["q"].dtype)
+    n_seqs = x["cu_seqlens"].shape[0] - 1
+    df = torch.randn(n_seqs, H, 128, 128, generator=g, device=DEV) if d_final else None
+    return do, df
+
+
+def _check(x, do, df, dtype, heads=None):
+    got = kda.kda_chunk_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["init_state"],
+                            x["cu_seqlens"], do, df)
+    torch.cuda.synchronize()
+    hs = list(range(x["q"].shape[1])) if heads is None else heads
+    hsel = torch.as_tensor(hs, device=DEV)
+
+    def sub(t):
+        return t.detach().index_select(1, hsel).cpu() if t is not None else None
+
+    ref = oracle.chunk_bwd(sub(x["q"]), sub(x["k"]), sub(x["v"]), sub(x["log_alpha"]),
+                           sub(x["beta"]), sub(x["init_state"]), x["cu_seqlens"].cpu(), sub(do),
+                           sub(df))
+    cu = x["cu_seqlens"].cpu().numpy()
+    tol = TOL[dtype]
+    for name, gt, rf in zip(("dq", "dk", "dv", "d_log_alpha"), got[:4], ref[:4]):
+        assert_parity(sub(gt), rf, tol, cu=cu, name=name)
+    assert_parity(sub(got[4])[..., None], ref[4][..., None], tol, cu=cu, name="d_beta")
+    assert_parity(sub(got[5]), ref[5], tol, name="d_init_state")
+    return got
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("init,final", [(True, True), (False, True), (True, False)])
+def test_bwd_matches_oracle_ragged(dtype, init, final):
+    lengths = [0, 1, 15, 16, 17, 33, 64, 100]
+    x = inputs.prefill_inputs(lengths, H=2, dtype=dtype, init_state=init, device=DEV, seed=91)
+    do, df = _grads_in(x, 92, d_final=final)
+    _check(x, do, df, dtype)
+
+
+@pytest.mark.parametrize("case", ["la0", "la_floor", "beta1"])
+def test_bwd_edge_values(case):
+    x = inputs.prefill_inputs([70, 45], H=2, dtype="f32", init_state=True, device=DEV, seed=93)
+    if case == "la0":
+        x["log_alpha"].zero_()
+    elif case == "la_floor":
+        x["log_alpha"].fill_(-5.0)
+    else:
+        x["beta"].fill_(1.0)
+    do, df = _grads_in(x, 94)
+    _check(x, do, df, "f32")
+
+
+def test_bwd_host_cu_seqlens_and_deterministic_dv():
+    """A host cu_seqlens gives the results of a device one; dv and the initial-
+    state gradient (one column block each, no atomics) are bitwise repeatable."""
+    x = inputs.prefill_inputs([40, 90], H=3, dtype="bf16", init_state=True, device=DEV, seed=95)
+    do, df = _grads_in(x, 96)
+    a = kda.kda_chunk_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["init_state"],
+                          x["cu_seqlens"], do, df)
+    b = kda.kda_chunk_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["init_state"],
+                          x["cu_seqlens"].cpu(), do, df)
+    torch.cuda.synchronize()
+    assert torch.equal(a[2], b[2]) and torch.equal(a[5], b[5])
+    for i in (0, 1, 3, 4):
+        assert_parity(a[i] if i != 4 else a[i][..., None], b[i] if i != 4 else b[i][..., None],
+                      1e-5, cu=x["cu_seqlens"].cpu().numpy(), name=f"gradient {i}")
+
+
+def test_bwd_two_calls_chain_through_the_state():
+    """Backward of two calls with the state handed over equals the backward of
+    one call: the second call's initial-state gradient is the first call's
+    final-state gradient."""
+    T, cut = 300, 129
+    x = inputs.prefill_inputs([T], H=2, dtype="f32", init_state=True, device=DEV, seed=97)
+    do, df = _grads_in(x, 98)
+    whole = kda.kda_chunk_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
+                              x["init_state"], x["cu_seqlens"], do, df)
+    first = {n: x[n][:cut].contiguous() for n in ("q", "k", "v", "log_alpha", "beta")}
+    second = {n: x[n][cut:].contiguous() for n in ("q", "k", "v", "log_alpha", "beta")}
+    _, mid = kda.kda_chunk_fwd(first["q"], first["k"], first["v"], first["log_alpha"],
+                               first["beta"], x["init_state"])
+    g2 = kda.kda_chunk_bwd(second["q"], second["k"], second["v"], second["log_alpha"],
+                           second["beta"], mid, None, do[cut:].contiguous(), df)
+    g1 = kda.kda_chunk_bwd(first["q"], first["k"], first["v"], first["log_alpha"],
+                           first["beta"], x["init_state"], None, do[:cut].contiguous(), g2[5])
+    torch.cuda.synchronize()
+    for i, name in enumerate(("dq", "dk", "dv", "d_log_alpha")):
+        assert_parity(torch.cat([g1[i], g2[i]]), whole[i], 1e-4, name=name)
+    assert_parity(g1[5], whole[5], 1e-4, name="d_init_state")
+
+
+def test_bwd_b4_h16_t4096_sampled_heads():
+    """The B=4, H=16, T=4096 prefill workload (random initial states): heads 0
+    and 15 of every sequence against the oracle."""
+    x = inputs.workload_inputs("b4_h16_t4096", device=DEV)
+    do, df = _grads_in(x, 99)
+    _check(x, do, df, "bf16", heads=[0, 15])
