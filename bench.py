@@ -481,7 +481,7 @@ def decode_sequence_bench(dev, peaks, steps: int = 100, warmup_steps: int = 3, s
 
     for s in range(warmup_steps):          # warm-up on a copy of the state
         st0 = state.clone()
-        step(s)
+        step(s % steps)
         state.copy_(st0)
         del st0
     torch.cuda.synchronize()
@@ -571,7 +571,8 @@ def backward_bench(dev, peaks, workload: str = "b4_h16_t4096", steps: int = 5, w
             "roofline": {"bound": "alu", "kernel": "kda_bwd_kernel", "achieved": tflops,
                          "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
                          "peak_source": "derived: SMs x 128 fp32 lanes x 2 x 2,070 MHz",
-                         "traffic": None, "flop_per_launch": th * BWD_FLOP_PER_TOKEN_HEAD}}
+                         "traffic": recorded_traffic("kda_bwd_kernel", "kda_bwd.cu", workload),
+                         "flop_per_launch": th * BWD_FLOP_PER_TOKEN_HEAD}}
 
 
 def prefill_bytes(x, H):
