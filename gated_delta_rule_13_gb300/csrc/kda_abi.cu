@@ -558,9 +558,9 @@ int kda_decode_replay(float *state, const void *q, const void *k, const void *v,
   if (d != KDA_OK) return d;
   if (!state || !q || !k || !v || !log_alpha || !beta || !n_accept) return KDA_ERR_INVALID_ARG;
   const size_t esz = dtype == KDA_BF16 ? 2 : 4;
-  if (!aligned16(state) || !aligned(v, 4 * esz) || (out && !aligned(out, 4 * esz)) ||
-      !aligned(q, esz) || !aligned(k, esz) || !aligned(log_alpha, 4) || !aligned(beta, 4) ||
-      !aligned(n_accept, 4))
+  // q, k, v and log_alpha rows are fetched by bulk copies: 16-byte aligned bases
+  if (!aligned16(state) || !aligned16(v) || (out && !aligned(out, 4 * esz)) || !aligned16(q) ||
+      !aligned16(k) || !aligned16(log_alpha) || !aligned(beta, 4) || !aligned(n_accept, 4))
     return KDA_ERR_INVALID_ARG;
   const size_t units = (size_t)B * H;
   if (out && units > 0 &&
@@ -678,9 +678,10 @@ int kda_layer_replay(float *state, void *conv_state, const void *q_raw, const vo
       !conv_w || !gamma || !n_accept)
     return KDA_ERR_INVALID_ARG;
   const size_t esz = dtype == KDA_BF16 ? 2 : 4;
-  if (!aligned16(state) || !aligned(conv_state, esz) || !aligned(q_raw, esz) ||
-      !aligned(k_raw, esz) || !aligned(v_raw, esz) || !aligned(g, esz) || !aligned(a_logit, 4) ||
-      !aligned(b_logit, 4) || !aligned16(conv_w) || !aligned16(gamma) || !aligned(n_accept, 4) ||
+  // the window, taps and raw input rows are fetched by bulk copies: 16-byte aligned bases
+  if (!aligned16(state) || !aligned16(conv_state) || !aligned16(q_raw) || !aligned16(k_raw) ||
+      !aligned16(v_raw) || !aligned16(g) || !aligned16(a_logit) || !aligned(b_logit, 4) ||
+      !aligned16(conv_w) || !aligned16(gamma) || !aligned(n_accept, 4) ||
       (out && !aligned(out, 4 * esz)))
     return KDA_ERR_INVALID_ARG;
   const size_t units = (size_t)B * H;

@@ -21,9 +21,12 @@
 #include <type_traits>
 
 #include "kda_internal.h"
+#include "kda_sm100.cuh"
 
 namespace kda {
 namespace {
+
+using namespace sm100;
 
 constexpr int D = kHeadDim;
 constexpr int kWarps = 8;
@@ -353,7 +356,7 @@ kda_conv_window_kernel(const void *__restrict__ q_raw, const void *__restrict__ 
 // replay under speculative decoding: short convolution, norms, gating, the KDA
 // recurrence and the output norm in one kernel over the accepted prefix, the
 // state and the convolution window written back once).  Unit (b, h), tokens
-// t < n_b = n_accept[b] clamped to [0, T], one CTA of 8 warps:
+// t < n_b = n_accept[b] clamped to [0, T], 8 warps:
 //   threads 0-127 (channel c): q and k of channel c (window, convolution,
 //     Swish), then L2Norm over the 128 channels;
 //   threads 128-255 (channel c - 128): v (window, convolution, Swish), the
@@ -362,7 +365,36 @@ kda_conv_window_kernel(const void *__restrict__ q_raw, const void *__restrict__ 
 //   registers (the decode step's layout), and the output row goes through the
 //   head-wise RMSNorm times gamma times the gate before it is stored.
 // Nothing is read or written for a unit with no accepted token.
-constexpr int kReplayTokGroup = 2;  // tokens whose raw inputs are loaded together
+//
+// The CTAs are persistent (two per SM) and walk the units with a stride of the
+// grid.  While one unit's tokens run, bulk copies already bring the next unit's
+// state, its convolution taps and window, and the raw inputs of its first
+// kLrStageTok tokens into a shared-memory stage (its beta logits ride in the
+// issuing thread's registers), so a unit starts without a round trip to HBM.
+constexpr int kLrStageTok = 4;                       // tokens whose inputs ride in the prefetch
+constexpr uint32_t kLrTapBytes = 3 * D * kConv * 4;  // the unit's q, k, v taps
+template <bool BF16>
+constexpr uint32_t lr_esz() { return BF16 ? 2 : 4; }
+// Staged token: q, k, v, g rows in the input type, then the fp32 decay logits.
+template <bool BF16>
+constexpr uint32_t lr_tok_bytes() { return 4 * D * lr_esz<BF16>() + 4 * D; }
+template <bool BF16>
+constexpr uint32_t lr_win_bytes() { return 9 * D * lr_esz<BF16>(); }
+// Stage: state [D][D] fp32, taps [3][D][4] fp32, window [3][3][D], tokens.
+constexpr uint32_t kLrOffTaps = D * D * 4, kLrOffWin = kLrOffTaps + kLrTapBytes;
+template <bool BF16>
+constexpr uint32_t lr_off_tok() { return kLrOffWin + lr_win_bytes<BF16>(); }
+template <bool BF16>
+constexpr size_t lr_stage_bytes() { return lr_off_tok<BF16>() + kLrStageTok * lr_tok_bytes<BF16>(); }
+static_assert(kLrOffWin % 16 == 0 && lr_off_tok<true>() % 16 == 0 && lr_off_tok<false>() % 16 == 0,
+              "bulk-copy destinations are 16-byte aligned");
+constexpr uint64_t kLrWaitNs = 2000000000ull;  // bound on the stage's copy wait
+
+template <bool BF16>
+__device__ __forceinline__ float lr_elem(const uint8_t *row, int c) {
+  if constexpr (BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(row)[c]);
+  else return reinterpret_cast<const float *>(row)[c];
+}
 
 template <bool BF16>
 __global__ void __launch_bounds__(256, 2)
@@ -372,87 +404,159 @@ kda_layer_replay_kernel(float *__restrict__ state, void *__restrict__ win,
                         const float *__restrict__ b_logit, const void *__restrict__ g,
                         const float *__restrict__ conv_w, const float *__restrict__ gamma,
                         const int32_t *__restrict__ n_accept, int32_t T, int32_t H,
-                        void *__restrict__ out) {
+                        int64_t units, void *__restrict__ out) {
   using elem_t = typename std::conditional<BF16, __nv_bfloat16, float>::type;
+  constexpr uint32_t kEsz = lr_esz<BF16>(), kTok = lr_tok_bytes<BF16>();
+  extern __shared__ __align__(128) uint8_t stage[];
   __shared__ __align__(16) float s_q[D], s_k[D], s_v[D], s_alpha[D], s_gate[D];
   __shared__ float s_red[3][kWarps];
   __shared__ float s_beta;
-  __shared__ __align__(16) float s_w[3][D][kConv];  // the head's taps of q, k, v
-  const int64_t unit = blockIdx.x;
-  const int64_t b = unit / H;
-  const int h = (int)(unit % H);
-  const int na = n_accept[b];
-  const int n = na < 0 ? 0 : (na > T ? T : na);
-  if (n == 0) return;
+  __shared__ __align__(16) float s_w[3][D][kConv];           // the unit's taps of q, k, v
+  __shared__ __align__(16) uint8_t s_tok[kLrStageTok * kTok];  // its first tokens' raw inputs
+  __shared__ float s_blog[kLrStageTok];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int64_t s_next;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int col = 16 * warp + 4 * (lane & 3);
   const int row0 = lane >> 2;
   const int role = tid >> 7, c = tid & (D - 1);
-  float *S = state + unit * (int64_t)(D * D);
-  float4 st[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j)
-    st[j] = __ldcs(reinterpret_cast<const float4 *>(S + (row0 + 8 * j) * D + col));
-
-  // channel c's taps and carried window rows (role 0: q and k, role 1: v)
-  const int64_t rs = (int64_t)H * D;  // elements per [H, D] row
   const int za = role == 0 ? 0 : 2;
-  for (int e = tid; e < 3 * D; e += 256) {
-    const int z = e / D, ch = e % D;
-    *reinterpret_cast<float4 *>(s_w[z][ch]) =
-        *reinterpret_cast<const float4 *>(conv_w + (((int64_t)z * H + h) * D + ch) * kConv);
-  }
-  float xa[3], xb[3];
-  const elem_t *wv = static_cast<const elem_t *>(win);
+  const int64_t rs = (int64_t)H * D;  // elements per [H, D] row
+  auto accepted = [&](int64_t u) {
+    const int n = n_accept[u / H];
+    return n < 0 ? 0 : (n > T ? T : n);
+  };
+  // thread 0: the next unit with accepted tokens from `u` on (stride gridDim.x),
+  // its stage copies issued and its first beta logits loaded into nblog
+  float nblog[kLrStageTok];
+  auto prefetch_from = [&](int64_t u) {
+    while (u < units && accepted(u) == 0) u += gridDim.x;
+    s_next = u;
+    if (u >= units) return;
+    const int cnt = accepted(u) < kLrStageTok ? accepted(u) : kLrStageTok;
+    const int64_t b = u / H;
+    const int h = (int)(u % H);
+    const uint32_t s0 = smem_u32(stage);
+    mbar_arrive_expect_tx(&bar, kLrOffWin + lr_win_bytes<BF16>() + (uint32_t)cnt * kTok);
+    bulk_load(s0, state + u * (int64_t)(D * D), D * D * 4, &bar);
 #pragma unroll
-  for (int r = 0; r < 3; ++r) {
-    xa[r] = to_float(wv[((b * 3 + za) * 3 + r) * rs + (int64_t)h * D + c]);
-    xb[r] = role == 0 ? to_float(wv[((b * 3 + 1) * 3 + r) * rs + (int64_t)h * D + c]) : 0.f;
-  }
-  const float4 gm = *reinterpret_cast<const float4 *>(gamma + col);
-
-  for (int t0 = 0; t0 < n; t0 += kReplayTokGroup) {
-    // raw inputs of up to kReplayTokGroup tokens, loaded together
-    float ra[kReplayTokGroup], rb[kReplayTokGroup], rg[kReplayTokGroup], rl[kReplayTokGroup];
+    for (int z = 0; z < 3; ++z)
+      bulk_load(s0 + kLrOffTaps + z * (D * kConv * 4), conv_w + ((int64_t)z * H + h) * D * kConv,
+                D * kConv * 4, &bar);
 #pragma unroll
-    for (int i = 0; i < kReplayTokGroup; ++i) {
-      const int t = t0 + i;
-      ra[i] = rb[i] = rg[i] = rl[i] = 0.f;
-      if (t < n) {
-        const int64_t row = ((b * T + t) * H + h) * D + c;
-        if (role == 0) {
-          ra[i] = to_float(static_cast<const elem_t *>(q_raw)[row]);
-          rb[i] = to_float(static_cast<const elem_t *>(k_raw)[row]);
-        } else {
-          ra[i] = to_float(static_cast<const elem_t *>(v_raw)[row]);
-          rl[i] = a_logit[row];
-          rg[i] = to_float(static_cast<const elem_t *>(g)[row]);
-        }
+    for (int zr = 0; zr < 9; ++zr)
+      bulk_load(s0 + kLrOffWin + zr * (D * kEsz),
+                static_cast<const elem_t *>(win) + ((b * 3 + zr / 3) * 3 + zr % 3) * rs + (int64_t)h * D,
+                D * kEsz, &bar);
+#pragma unroll
+    for (int t = 0; t < kLrStageTok; ++t) {
+      if (t < cnt) {
+        const int64_t row = ((b * T + t) * H + h) * D;
+        const uint32_t dst = s0 + lr_off_tok<BF16>() + t * kTok;
+        bulk_load(dst, static_cast<const elem_t *>(q_raw) + row, D * kEsz, &bar);
+        bulk_load(dst + D * kEsz, static_cast<const elem_t *>(k_raw) + row, D * kEsz, &bar);
+        bulk_load(dst + 2 * D * kEsz, static_cast<const elem_t *>(v_raw) + row, D * kEsz, &bar);
+        bulk_load(dst + 3 * D * kEsz, static_cast<const elem_t *>(g) + row, D * kEsz, &bar);
+        bulk_load(dst + 4 * D * kEsz, a_logit + row, D * 4, &bar);
+        nblog[t] = b_logit[(b * T + t) * H + h];
       }
     }
-    for (int i = 0; i < kReplayTokGroup && t0 + i < n; ++i) {
-      const int t = t0 + i;
+  };
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbarrier_init();
+    prefetch_from(blockIdx.x);
+  }
+  __syncthreads();
+  const float4 gm = *reinterpret_cast<const float4 *>(gamma + col);
+  int64_t u = s_next;
+  uint32_t phase = 0;
+  while (u < units) {
+    const bool landed = mbar_wait(&bar, phase, kLrWaitNs);
+    if (__syncthreads_or(!landed)) {  // a copy that never lands: leave, every thread alike
+      if (tid == 0) mbar_wait(&bar, phase, kLrWaitNs);  // (bounded) no copy outlives the CTA
+      return;
+    }
+    phase ^= 1u;
+    const int64_t b = u / H;
+    const int h = (int)(u % H);
+    const int n = accepted(u);
+    // ---- the stage into registers and the unit's own shared arrays
+    float4 st[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      st[j] = *reinterpret_cast<const float4 *>(stage + 4 * ((row0 + 8 * j) * D + col));
+    for (int e = tid; e < 3 * D; e += 256)
+      *reinterpret_cast<float4 *>(&s_w[0][0][0] + 4 * e) =
+          *reinterpret_cast<const float4 *>(stage + kLrOffTaps + 16 * e);
+    float xa[3], xb[3];  // channel c's carried window rows (role 0: q and k, role 1: v)
+    {
+      const uint8_t *sw = stage + kLrOffWin;
+#pragma unroll
+      for (int r = 0; r < 3; ++r) {
+        xa[r] = lr_elem<BF16>(sw + (3 * za + r) * (D * kEsz), c);
+        xb[r] = role == 0 ? lr_elem<BF16>(sw + (3 + r) * (D * kEsz), c) : 0.f;
+      }
+    }
+    {
+      const int cnt = n < kLrStageTok ? n : kLrStageTok;
+      const uint4 *src = reinterpret_cast<const uint4 *>(stage + lr_off_tok<BF16>());
+      for (int e = tid; e < cnt * (int)(kTok / 16); e += 256)
+        reinterpret_cast<uint4 *>(s_tok)[e] = src[e];
+      if (tid == 0) {
+#pragma unroll
+        for (int t = 0; t < kLrStageTok; ++t)
+          if (t < cnt) s_blog[t] = nblog[t];
+      }
+    }
+    __syncthreads();  // the stage is free for the next unit; the taps and inputs are in place
+    if (tid == 0) prefetch_from(u + gridDim.x);
+
+    float *S = state + u * (int64_t)(D * D);
+    for (int t = 0; t < n; ++t) {
       const int64_t tok = (b * T + t) * H + h;
+      // ---- raw inputs of channel c: staged for the first tokens, else from HBM
+      float ra, rb = 0.f, rg = 0.f, rl = 0.f;
+      if (t < kLrStageTok) {
+        const uint8_t *tb = s_tok + t * kTok;
+        if (role == 0) {
+          ra = lr_elem<BF16>(tb, c);
+          rb = lr_elem<BF16>(tb + D * kEsz, c);
+        } else {
+          ra = lr_elem<BF16>(tb + 2 * D * kEsz, c);
+          rg = lr_elem<BF16>(tb + 3 * D * kEsz, c);
+          rl = reinterpret_cast<const float *>(tb + 4 * D * kEsz)[c];
+        }
+      } else {
+        const int64_t row = tok * D + c;
+        if (role == 0) {
+          ra = to_float(static_cast<const elem_t *>(q_raw)[row]);
+          rb = to_float(static_cast<const elem_t *>(k_raw)[row]);
+        } else {
+          ra = to_float(static_cast<const elem_t *>(v_raw)[row]);
+          rl = a_logit[row];
+          rg = to_float(static_cast<const elem_t *>(g)[row]);
+        }
+      }
       // ---- convolution + Swish of this token, window shifted
-      if (t == 0) __syncthreads();  // the taps are in shared memory
       const float4 wa = *reinterpret_cast<const float4 *>(s_w[za][c]);
-      float ya = wa.x * xa[0] + wa.y * xa[1] + wa.z * xa[2] + wa.w * ra[i];
+      float ya = wa.x * xa[0] + wa.y * xa[1] + wa.z * xa[2] + wa.w * ra;
       ya *= sigmoidf(ya);
       float yb = 0.f;
-      xa[0] = xa[1]; xa[1] = xa[2]; xa[2] = ra[i];
+      xa[0] = xa[1]; xa[1] = xa[2]; xa[2] = ra;
       if (role == 0) {
         const float4 wb = *reinterpret_cast<const float4 *>(s_w[1][c]);
-        yb = wb.x * xb[0] + wb.y * xb[1] + wb.z * xb[2] + wb.w * rb[i];
+        yb = wb.x * xb[0] + wb.y * xb[1] + wb.z * xb[2] + wb.w * rb;
         yb *= sigmoidf(yb);
-        xb[0] = xb[1]; xb[1] = xb[2]; xb[2] = rb[i];
+        xb[0] = xb[1]; xb[1] = xb[2]; xb[2] = rb;
         // L2Norm sums of q and k over the 128 channels (warps 0-3)
         const float sq = warp_sum(ya * ya), sk = warp_sum(yb * yb);
         if (lane == 0) { s_red[0][warp] = sq; s_red[1][warp] = sk; }
       } else {
         s_v[c] = ya;
-        s_alpha[c] = __expf(kDecayBound * sigmoidf(rl[i]));
-        s_gate[c] = sigmoidf(rg[i]);
-        if (c == 0) s_beta = sigmoidf(b_logit[tok]);
+        s_alpha[c] = __expf(kDecayBound * sigmoidf(rl));
+        s_gate[c] = sigmoidf(rg);
+        if (c == 0) s_beta = sigmoidf(t < kLrStageTok ? s_blog[t] : b_logit[tok]);
       }
       __syncthreads();
       if (role == 0) {
@@ -521,15 +625,17 @@ kda_layer_replay_kernel(float *__restrict__ state, void *__restrict__ win,
                               o2 * nr * gm.z * gt.z, o3 * nr * gm.w * gt.w));
       }
     }
-  }
 #pragma unroll
-  for (int j = 0; j < 16; ++j)
-    __stcs(reinterpret_cast<float4 *>(S + (row0 + 8 * j) * D + col), st[j]);
-  elem_t *wo = static_cast<elem_t *>(win);
+    for (int j = 0; j < 16; ++j)
+      __stcs(reinterpret_cast<float4 *>(S + (row0 + 8 * j) * D + col), st[j]);
+    elem_t *wo = static_cast<elem_t *>(win);
 #pragma unroll
-  for (int r = 0; r < 3; ++r) {
-    wo[((b * 3 + za) * 3 + r) * rs + (int64_t)h * D + c] = from_float<elem_t>(xa[r]);
-    if (role == 0) wo[((b * 3 + 1) * 3 + r) * rs + (int64_t)h * D + c] = from_float<elem_t>(xb[r]);
+    for (int r = 0; r < 3; ++r) {
+      wo[((b * 3 + za) * 3 + r) * rs + (int64_t)h * D + c] = from_float<elem_t>(xa[r]);
+      if (role == 0) wo[((b * 3 + 1) * 3 + r) * rs + (int64_t)h * D + c] = from_float<elem_t>(xb[r]);
+    }
+    __syncthreads();  // s_next is set; the unit's shared arrays may be refilled
+    u = s_next;
   }
 }
 
@@ -597,13 +703,17 @@ cudaError_t launch_layer_replay(float *state, void *win, const void *q_raw, cons
                                 bool bf16, void *out, cudaStream_t stream) {
   const int64_t units = (int64_t)B * H;
   if (units == 0) return cudaSuccess;
-  if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (bf16)
-    kda_layer_replay_kernel<true><<<(unsigned)units, 256, 0, stream>>>(
-        state, win, q_raw, k_raw, v_raw, a_logit, b_logit, g, conv_w, gamma, n_accept, T, H, out);
-  else
-    kda_layer_replay_kernel<false><<<(unsigned)units, 256, 0, stream>>>(
-        state, win, q_raw, k_raw, v_raw, a_logit, b_logit, g, conv_w, gamma, n_accept, T, H, out);
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int64_t ctas = units < 2 * (int64_t)sms ? units : 2 * (int64_t)sms;
+  const size_t stage = bf16 ? lr_stage_bytes<true>() : lr_stage_bytes<false>();
+  auto kern = bf16 ? kda_layer_replay_kernel<true> : kda_layer_replay_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)stage);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)ctas, 256, stage, stream>>>(state, win, q_raw, k_raw, v_raw, a_logit, b_logit,
+                                               g, conv_w, gamma, n_accept, T, H, units, out);
   return cudaGetLastError();
 }
 

@@ -380,8 +380,8 @@ int kda_decode_step(float *state, const void *q, const void *k, const void *v,
  *   n_accept   [B]            int32, DEVICE memory: accepted tokens per sequence
  *   out        [B, T, H, dv]  dtype  o_t of every replayed token, or NULL; rows
  *                                    t >= n_b are not written
- * Alignment: state 16 bytes; v and out 4 elements; q, k 1 element;
- * log_alpha, beta and n_accept 4 bytes.
+ * Alignment: state, q, k, v and log_alpha 16 bytes (their rows are fetched by
+ * bulk copies); out 4 elements; beta and n_accept 4 bytes.
  * Errors (before any launch): KDA_ERR_INVALID_ARG (NULL pointer other than
  * out, B < 0, T <= 0, H <= 0, misalignment, `out` overlapping `state`),
  * KDA_ERR_UNSUPPORTED (dk or dv != 128, unknown dtype), KDA_ERR_CUDA.
@@ -474,7 +474,9 @@ int kda_prep_fwd_state(const void *q_raw, const void *k_raw, const void *v_raw,
  *   n_accept   [B] int32, DEVICE memory
  *   out        [B, T, H, 128] dtype or NULL; rows t >= n_b are not written
  * The library's layout, not the pages' (they give none).
- * Alignment: state, conv_w, gamma 16 bytes; out 4 elements; the rest one element.
+ * Alignment: state, conv_state, q_raw, k_raw, v_raw, g, a_logit, conv_w and
+ * gamma 16 bytes (rows are fetched by bulk copies); out 4 elements; b_logit
+ * and n_accept 4 bytes.
  * Errors (before any launch): KDA_ERR_INVALID_ARG (NULL pointer other than
  * out, B < 0, T <= 0, H <= 0, misalignment, out overlapping state or the
  * window, the window overlapping the state), KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA.

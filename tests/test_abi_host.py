@@ -179,6 +179,8 @@ def _replay(lib, **over):
     (dict(state=None), 1), (dict(q=None), 1), (dict(n=None), 1), (dict(beta=None), 1),
     (dict(B=-1), 1), (dict(T=0), 1), (dict(H=0), 1), (dict(dk=32), 2), (dict(dtype=3), 2),
     (dict(k=A + 0x2001), 1), (dict(v=A + 0x3004), 1), (dict(n=A + 0x6002), 1),
+    # element-aligned but not 16-byte aligned: rows are fetched by bulk copies
+    (dict(q=A + 0x1002), 1), (dict(k=A + 0x2008), 1), (dict(la=A + 0x4004), 1),
     (dict(out=A + 0x800), 1),                               # out inside the state
 ])
 def test_replay_rejects_before_launch(lib, over, code):
@@ -371,6 +373,9 @@ def _layer_replay(lib, **over):
     (dict(state=None), 1), (dict(win=None), 1), (dict(g=None), 1), (dict(na=None), 1),
     (dict(B=-1), 1), (dict(T=0), 1), (dict(H=0), 1), (dict(dk=64), 2), (dict(dtype=5), 2),
     (dict(state=A + 8), 1), (dict(w=A + 0x8000004), 1), (dict(out=A + 0xB000002), 1),
+    # element-aligned but not 16-byte aligned: rows are fetched by bulk copies
+    (dict(win=A + 0x1000002), 1), (dict(qr=A + 0x2000002), 1), (dict(g=A + 0x7000008), 1),
+    (dict(a=A + 0x5000004), 1),
     (dict(win=A + 0x100), 1),                   # window inside the state
     (dict(out=A + 0x1000000), 1),               # output over the window
 ])
