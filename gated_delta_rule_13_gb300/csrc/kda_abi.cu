@@ -123,38 +123,57 @@ bool is_device_pointer(const void *p, bool *ok) {
 struct BwdLayout {
   size_t cu, ckpt, dq, dk, total;
 };
-BwdLayout bwd_layout(int32_t n_seqs, int64_t n_tokens, int32_t H) {
+BwdLayout bwd_layout(int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t every) {
   BwdLayout l;
   l.cu = kStatusBytes;
   l.ckpt = l.cu + round_up(sizeof(int32_t) * ((size_t)n_seqs + 1), 256);
-  l.dq = l.ckpt + round_up(kda::bwd_ckpt_slots(n_seqs, n_tokens) * H * kHeadDim * kHeadDim * 4, 256);
+  l.dq = l.ckpt +
+         round_up(kda::bwd_ckpt_slots(n_seqs, n_tokens, every) * H * kHeadDim * kHeadDim * 4, 256);
   l.dk = l.dq + round_up((size_t)n_tokens * H * kHeadDim * 4, 256);
   l.total = l.dk + round_up((size_t)n_tokens * H * kHeadDim * 4, 256);
   return l;
+}
+
+// The backward pass's checkpoint interval: the caller's (a power of two in
+// [4, kda::kMaxCkptEvery]) or, for 0, the library's choice; -1 if invalid.
+int32_t resolve_ckpt_every(int32_t want, int32_t n_seqs, int64_t n_tokens, int32_t H) {
+  if (want == 0) return kda::bwd_ckpt_every(n_seqs, n_tokens, H);
+  if (want < 4 || want > kda::kMaxCkptEvery || (want & (want - 1)) != 0) return -1;
+  return want;
 }
 
 }  // namespace
 
 extern "C" {
 
-int kda_chunk_bwd_workspace_size(int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk,
-                                 int32_t dv, int dtype, size_t *bytes) {
+int kda_chunk_bwd_workspace_size_sched(int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk,
+                                       int32_t dv, int dtype, int32_t ckpt_every, size_t *bytes) {
   if (!bytes || n_seqs < 0 || n_tokens < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
   const int d = check_dims(dk, dv, dtype);
   if (d != KDA_OK) return d;
-  *bytes = bwd_layout(n_seqs, n_tokens, H).total;
+  const int32_t every = resolve_ckpt_every(ckpt_every, n_seqs, n_tokens, H);
+  if (every < 0) return KDA_ERR_INVALID_ARG;
+  *bytes = bwd_layout(n_seqs, n_tokens, H, every).total;
   return KDA_OK;
 }
 
-int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *log_alpha,
-                  const float *beta, const float *init_state, const int32_t *cu_seqlens,
-                  int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk, int32_t dv, int dtype,
-                  const void *d_out, const float *d_final_state, void *dq, void *dk_, void *dv_,
-                  float *d_log_alpha, float *d_beta, float *d_init_state, void *workspace,
-                  size_t workspace_bytes, void *stream) {
+int kda_chunk_bwd_workspace_size(int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk,
+                                 int32_t dv, int dtype, size_t *bytes) {
+  return kda_chunk_bwd_workspace_size_sched(n_seqs, n_tokens, H, dk, dv, dtype, 0, bytes);
+}
+
+int kda_chunk_bwd_sched(const void *q, const void *k, const void *v, const float *log_alpha,
+                        const float *beta, const float *init_state, const int32_t *cu_seqlens,
+                        int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk, int32_t dv,
+                        int dtype, const void *d_out, const float *d_final_state, void *dq,
+                        void *dk_, void *dv_, float *d_log_alpha, float *d_beta,
+                        float *d_init_state, int32_t ckpt_every, void *workspace,
+                        size_t workspace_bytes, void *stream) {
   if (n_seqs < 0 || n_tokens < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
   const int d = check_dims(dk, dv, dtype);
   if (d != KDA_OK) return d;
+  const int32_t every = resolve_ckpt_every(ckpt_every, n_seqs, n_tokens, H);
+  if (every < 0) return KDA_ERR_INVALID_ARG;
   if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
   if (n_tokens > 0 && (!q || !k || !v || !log_alpha || !beta || !d_out || !dq || !dk_ || !dv_ ||
                        !d_log_alpha || !d_beta))
@@ -185,7 +204,7 @@ int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *log_
       if (outs[j] && out_b[j] > 0 && ranges_overlap(outs[i], out_b[i], outs[j], out_b[j]))
         return KDA_ERR_INVALID_ARG;
   }
-  const BwdLayout lay = bwd_layout(n_seqs, n_tokens, H);
+  const BwdLayout lay = bwd_layout(n_seqs, n_tokens, H, every);
   if (!workspace || workspace_bytes < lay.total || !aligned16(workspace)) return KDA_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   unsigned char *ws = static_cast<unsigned char *>(workspace);
@@ -222,6 +241,7 @@ int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *log_
   a.d_out = d_out; a.d_final = d_final_state;
   a.dq = dq; a.dk = dk_; a.dv = dv_; a.d_log_alpha = d_log_alpha; a.d_beta = d_beta;
   a.d_init = d_init_state;
+  a.ckpt_every = every;
   a.ckpt = reinterpret_cast<float *>(ws + lay.ckpt);
   a.dq_acc = reinterpret_cast<float *>(ws + lay.dq);
   a.dk_acc = reinterpret_cast<float *>(ws + lay.dk);
@@ -232,6 +252,17 @@ int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *log_
     return KDA_ERR_CUDA;
   }
   return KDA_OK;
+}
+
+int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                  const float *beta, const float *init_state, const int32_t *cu_seqlens,
+                  int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk, int32_t dv, int dtype,
+                  const void *d_out, const float *d_final_state, void *dq, void *dk_, void *dv_,
+                  float *d_log_alpha, float *d_beta, float *d_init_state, void *workspace,
+                  size_t workspace_bytes, void *stream) {
+  return kda_chunk_bwd_sched(q, k, v, log_alpha, beta, init_state, cu_seqlens, n_seqs, n_tokens,
+                             H, dk, dv, dtype, d_out, d_final_state, dq, dk_, dv_, d_log_alpha,
+                             d_beta, d_init_state, 0, workspace, workspace_bytes, stream);
 }
 
 const char *kda_status_string(int status) {

@@ -19,10 +19,14 @@
 // warp (a transposing butterfly) and added across the four blocks with fp32
 // atomics (so their last bits depend on the order of those four additions).
 //
-// States.  A forward pass stores the state before every kCkpt-th token; the
+// States.  A forward pass stores the state before every `every`-th token (a
+// power of two >= kGroup, chosen by the caller of launch_chunk_bwd); the
 // backward pass recomputes, for each group of kGroup tokens, the decayed states
 // X of those tokens from the nearest checkpoint into shared memory, then runs
-// them in reverse.  CUDA cores, fp32 arithmetic, fp32 state and gradients.
+// them in reverse.  With every == kGroup nothing is recomputed twice; a wider
+// interval trades (every / kGroup - 1) / 2 extra forward steps per token for
+// less checkpoint memory.  CUDA cores, fp32 arithmetic, fp32 state and
+// gradients.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -37,13 +41,14 @@ constexpr int kCols = 32;         // value columns per CTA
 constexpr int kBlocks = D / kCols;
 constexpr int kThreads = 256;
 constexpr int kRows = 16;         // key rows per thread
-constexpr int kCkpt = 16;         // tokens between stored states
 constexpr int kGroup = 4;         // tokens whose X a CTA keeps at a time
 
-// Checkpoint slot of sequence s: floor(cu[s] / kCkpt) + s.  Consecutive
+// Checkpoint slot of sequence s: floor(cu[s] / every) + s.  Consecutive
 // sequences never share slots, since floor(b / c) - floor(a / c) + 1 >=
 // ceil((b - a) / c).
-__device__ __forceinline__ int64_t ckpt_base(int64_t cu_s, int64_t s) { return cu_s / kCkpt + s; }
+__device__ __forceinline__ int64_t ckpt_base(int64_t cu_s, int64_t s, int every) {
+  return cu_s / every + s;
+}
 
 template <bool BF16>
 __device__ __forceinline__ float ld(const void *p, int64_t i) {
@@ -163,8 +168,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 kda_bwd_ckpt_kernel(const void *__restrict__ k, const void *__restrict__ v,
                     const float *__restrict__ la, const float *__restrict__ beta,
                     const float *__restrict__ init_state, const int32_t *__restrict__ cu,
-                    int32_t n_seqs, int64_t n_tokens, int32_t H, float *__restrict__ ckpt,
-                    DeviceStatus *status) {
+                    int32_t n_seqs, int64_t n_tokens, int32_t H, int every,
+                    float *__restrict__ ckpt, DeviceStatus *status) {
   __shared__ Stage st;
   __shared__ float red[kThreads / 32][kCols];
   const Chain c = chain_of(cu, n_seqs, n_tokens, H);
@@ -178,7 +183,7 @@ kda_bwd_ckpt_kernel(const void *__restrict__ k, const void *__restrict__ v,
   float s[kRows], x[kRows];
 #pragma unroll
   for (int j = 0; j < kRows; ++j) s[j] = init_state ? init_state[sbase + (r0 + j) * D + col] : 0.f;
-  const int64_t base = ckpt_base(c.t0, c.seq);
+  const int64_t base = ckpt_base(c.t0, c.seq, every);
   for (int64_t tb = c.t0; tb < c.t1; tb += kGroup) {
     const int n = (int)(c.t1 - tb < kGroup ? c.t1 - tb : kGroup);
     __syncthreads();  // the previous group's stage is consumed
@@ -186,8 +191,8 @@ kda_bwd_ckpt_kernel(const void *__restrict__ k, const void *__restrict__ v,
     __syncthreads();
     for (int i = 0; i < n; ++i) {
       const int64_t t = tb + i;
-      if ((t - c.t0) % kCkpt == 0) {
-        float *dst = ckpt + ((base + (t - c.t0) / kCkpt) * H + c.h) * D * D;
+      if ((t - c.t0) % every == 0) {
+        float *dst = ckpt + ((base + (t - c.t0) / every) * H + c.h) * D * D;
 #pragma unroll
         for (int j = 0; j < kRows; ++j) dst[(r0 + j) * D + col] = s[j];
       }
@@ -203,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 kda_bwd_kernel(const void *__restrict__ q, const void *__restrict__ k, const void *__restrict__ v,
                const float *__restrict__ la, const float *__restrict__ beta,
                const int32_t *__restrict__ cu, int32_t n_seqs, int64_t n_tokens, int32_t H,
-               const float *__restrict__ ckpt, const void *__restrict__ dout,
+               int every, const float *__restrict__ ckpt, const void *__restrict__ dout,
                const float *__restrict__ d_final, float *__restrict__ dq_acc,
                float *__restrict__ dk_acc, void *__restrict__ dv_out, float *__restrict__ dla,
                float *__restrict__ dbeta, float *__restrict__ d_init) {
@@ -219,12 +224,12 @@ kda_bwd_kernel(const void *__restrict__ q, const void *__restrict__ k, const voi
   float ds[kRows];
 #pragma unroll
   for (int j = 0; j < kRows; ++j) ds[j] = d_final ? d_final[sbase + (r0 + j) * D + col] : 0.f;
-  const int64_t base = ckpt_base(c.t0, c.seq);
+  const int64_t base = ckpt_base(c.t0, c.seq, every);
   const int64_t len = c.t1 - c.t0;
-  const int64_t n_ck = (len + kCkpt - 1) / kCkpt;
+  const int64_t n_ck = (len + every - 1) / every;
   for (int64_t blk = n_ck - 1; blk >= 0; --blk) {
-    const int64_t a = c.t0 + blk * kCkpt;
-    const int64_t e = a + kCkpt < c.t1 ? a + kCkpt : c.t1;
+    const int64_t a = c.t0 + blk * every;
+    const int64_t e = a + every < c.t1 ? a + every : c.t1;
     const int n_groups = (int)((e - a + kGroup - 1) / kGroup);
     for (int g = n_groups - 1; g >= 0; --g) {
       // state before token a, then forward to the group's first token
@@ -338,14 +343,26 @@ __global__ void kda_bwd_finish_kernel(const float *__restrict__ dq_acc,
 
 }  // namespace
 
-size_t bwd_ckpt_slots(int32_t n_seqs, int64_t n_tokens) {
-  return (size_t)(n_tokens / kCkpt) + (size_t)n_seqs + 1;
+size_t bwd_ckpt_slots(int32_t n_seqs, int64_t n_tokens, int32_t every) {
+  return (size_t)(n_tokens / every) + (size_t)n_seqs + 1;
+}
+
+int32_t bwd_ckpt_every(int32_t n_seqs, int64_t n_tokens, int32_t H) {
+  int32_t every = kGroup;
+  while (every < kMaxCkptEvery &&
+         bwd_ckpt_slots(n_seqs, n_tokens, every) * (size_t)H * D * D * sizeof(float) >
+             kCkptBudgetBytes)
+    every *= 2;
+  return every;
 }
 
 cudaError_t launch_chunk_bwd(const BwdArgs &a, cudaStream_t stream) {
   const int64_t chains = (int64_t)a.n_seqs * a.H;
   if (chains == 0) return cudaSuccess;
   if (chains * kBlocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (a.ckpt_every < kGroup || a.ckpt_every > kMaxCkptEvery ||
+      (a.ckpt_every & (a.ckpt_every - 1)) != 0)
+    return cudaErrorInvalidValue;
   const unsigned grid = (unsigned)(chains * kBlocks);
   const size_t xs_bytes = (size_t)kGroup * D * kCols * sizeof(float);
   auto bwd = a.bf16 ? kda_bwd_kernel<true> : kda_bwd_kernel<false>;
@@ -355,15 +372,17 @@ cudaError_t launch_chunk_bwd(const BwdArgs &a, cudaStream_t stream) {
   if (a.bf16)
     kda_bwd_ckpt_kernel<true><<<grid, kThreads, 0, stream>>>(a.k, a.v, a.log_alpha, a.beta,
                                                             a.init_state, a.cu_seqlens, a.n_seqs,
-                                                            a.n_tokens, a.H, a.ckpt, a.status);
+                                                            a.n_tokens, a.H, a.ckpt_every, a.ckpt,
+                                                            a.status);
   else
     kda_bwd_ckpt_kernel<false><<<grid, kThreads, 0, stream>>>(a.k, a.v, a.log_alpha, a.beta,
                                                              a.init_state, a.cu_seqlens, a.n_seqs,
-                                                             a.n_tokens, a.H, a.ckpt, a.status);
+                                                             a.n_tokens, a.H, a.ckpt_every, a.ckpt,
+                                                             a.status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   bwd<<<grid, kThreads, xs_bytes, stream>>>(a.q, a.k, a.v, a.log_alpha, a.beta, a.cu_seqlens,
-                                            a.n_seqs, a.n_tokens, a.H, a.ckpt, a.d_out,
+                                            a.n_seqs, a.n_tokens, a.H, a.ckpt_every, a.ckpt, a.d_out,
                                             a.d_final, a.dq_acc, a.dk_acc, a.dv, a.d_log_alpha,
                                             a.d_beta, a.d_init);
   e = cudaGetLastError();

@@ -152,13 +152,21 @@ struct BwdArgs {
   const float *d_final;       // or nullptr
   void *dq, *dk, *dv;
   float *d_log_alpha, *d_beta, *d_init;  // d_init may be nullptr
+  int32_t ckpt_every;         // tokens between stored states: a power of two in [4, 1024]
   // workspace
   float *ckpt;                // [bwd_ckpt_slots][H][128][128]
   float *dq_acc, *dk_acc;     // [n_tokens][H][128], zeroed
   DeviceStatus *status;
 };
-// Checkpoint slots the backward pass needs (states stored every 16 tokens).
-size_t bwd_ckpt_slots(int32_t n_seqs, int64_t n_tokens);
+// Checkpoint interval bounds of the backward pass, and the budget its default
+// interval keeps the stored states within.
+constexpr int32_t kMaxCkptEvery = 1024;
+constexpr size_t kCkptBudgetBytes = (size_t)16 << 30;
+// Checkpoint slots the backward pass needs with states stored every `every` tokens.
+size_t bwd_ckpt_slots(int32_t n_seqs, int64_t n_tokens, int32_t every);
+// The default interval: the smallest power of two >= 4 whose checkpoints fit
+// kCkptBudgetBytes (kMaxCkptEvery if none does).
+int32_t bwd_ckpt_every(int32_t n_seqs, int64_t n_tokens, int32_t H);
 cudaError_t launch_chunk_bwd(const BwdArgs &a, cudaStream_t stream);
 
 cudaError_t launch_post(const void *o, const void *g, const float *gamma, int64_t n_tokens,

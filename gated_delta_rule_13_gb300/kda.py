@@ -33,7 +33,8 @@ EXPORTED = ("kda_status_string", "kda_version", "kda_chunk_fwd_workspace_size",
             "kda_chunk_fwd_noalloc", "kda_noalloc_read_status", "kda_decode_replay",
             "kda_prep_fwd", "kda_prep_fwd_state", "kda_layer_replay", "kda_post_fwd",
             "kda_read_chunk_stats", "kda_chunk_fwd_transitions", "kda_state_combine",
-            "kda_chunk_bwd", "kda_chunk_bwd_workspace_size")
+            "kda_chunk_bwd", "kda_chunk_bwd_workspace_size", "kda_chunk_bwd_sched",
+            "kda_chunk_bwd_workspace_size_sched")
 
 _lib = None
 
@@ -106,6 +107,13 @@ def library() -> ctypes.CDLL:
         lib.kda_chunk_bwd_workspace_size.restype = ctypes.c_int
         lib.kda_chunk_bwd_workspace_size.argtypes = [i32, i64, i32, i32, i32, ctypes.c_int,
                                                      ctypes.POINTER(sz)]
+        lib.kda_chunk_bwd_sched.restype = ctypes.c_int
+        lib.kda_chunk_bwd_sched.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32,
+                                            ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp, i32,
+                                            vp, sz, vp]
+        lib.kda_chunk_bwd_workspace_size_sched.restype = ctypes.c_int
+        lib.kda_chunk_bwd_workspace_size_sched.argtypes = [i32, i64, i32, i32, i32, ctypes.c_int,
+                                                           i32, ctypes.POINTER(sz)]
         lib.kda_post_fwd.restype = ctypes.c_int
         lib.kda_post_fwd.argtypes = [vp, vp, vp, i64, i32, i32, ctypes.c_int, vp, vp]
         lib.kda_decode_step.restype = ctypes.c_int
@@ -220,20 +228,25 @@ def kda_chunk_fwd(q, k, v, log_alpha, beta, init_state=None, cu_seqlens=None, *,
 
 
 def kda_chunk_bwd_workspace_size(n_seqs: int, n_tokens: int, H: int, dk: int = HEAD_DIM,
-                                 dv: int = HEAD_DIM, dtype: int = KDA_BF16) -> int:
+                                 dv: int = HEAD_DIM, dtype: int = KDA_BF16,
+                                 ckpt_every: int = 0) -> int:
+    """Workspace bytes of the backward pass (``ckpt_every`` 0: the library's
+    checkpoint interval)."""
     out = ctypes.c_size_t(0)
-    _check(library().kda_chunk_bwd_workspace_size(n_seqs, n_tokens, H, dk, dv, dtype,
-                                                  ctypes.byref(out)),
-           "kda_chunk_bwd_workspace_size")
+    _check(library().kda_chunk_bwd_workspace_size_sched(n_seqs, n_tokens, H, dk, dv, dtype,
+                                                        int(ckpt_every), ctypes.byref(out)),
+           "kda_chunk_bwd_workspace_size_sched")
     return out.value
 
 
 def kda_chunk_bwd(q, k, v, log_alpha, beta, init_state, cu_seqlens, d_out, d_final_state=None,
-                  *, workspace=None, want_d_init=True, stream=None):
+                  *, workspace=None, want_d_init=True, ckpt_every=None, stream=None):
     """Gradients of ``kda_chunk_fwd`` for output gradients ``d_out`` ``[N, H, 128]``
     (dtype of q) and final-state gradients ``d_final_state`` (or None).  Returns
     ``(dq, dk, dv, d_log_alpha, d_beta, d_init_state)`` in the layouts of the
-    inputs (d_init_state None unless requested)."""
+    inputs (d_init_state None unless requested).  ``ckpt_every`` (a power of two
+    in [4, 1024]) picks the interval of stored states through
+    ``kda_chunk_bwd_sched``; None leaves it to the library."""
     _need_cuda("q", q)
     N, H, dk = q.shape
     dt = q.dtype
@@ -258,17 +271,20 @@ def kda_chunk_bwd(q, k, v, log_alpha, beta, init_state, cu_seqlens, d_out, d_fin
     ds0 = (torch.empty(n_seqs, H, dk, dv, dtype=torch.float32, device=q.device)
            if want_d_init else None)
     code = _dtype_code(q)
+    every = 0 if ckpt_every is None else int(ckpt_every)
     if workspace is None:
-        workspace = torch.empty(kda_chunk_bwd_workspace_size(n_seqs, N, H, dk, dv, code),
+        workspace = torch.empty(kda_chunk_bwd_workspace_size(n_seqs, N, H, dk, dv, code, every),
                                 dtype=torch.uint8, device=q.device)
     _need_cuda("workspace", workspace)
-    rc = library().kda_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
-                                 _ptr(init_state), _ptr(cu_seqlens), n_seqs, N, H, dk, dv, code,
-                                 _ptr(d_out), _ptr(d_final_state), _ptr(dq), _ptr(dkk), _ptr(dvv),
-                                 _ptr(dla), _ptr(db), _ptr(ds0), _ptr(workspace),
-                                 workspace.numel() * workspace.element_size(),
-                                 _stream_handle(stream))
-    _check(rc, "kda_chunk_bwd")
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(init_state),
+            _ptr(cu_seqlens), n_seqs, N, H, dk, dv, code, _ptr(d_out), _ptr(d_final_state),
+            _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dla), _ptr(db), _ptr(ds0))
+    ws_args = (_ptr(workspace), workspace.numel() * workspace.element_size(),
+               _stream_handle(stream))
+    if ckpt_every is None:
+        _check(library().kda_chunk_bwd(*args, *ws_args), "kda_chunk_bwd")
+    else:
+        _check(library().kda_chunk_bwd_sched(*args, every, *ws_args), "kda_chunk_bwd_sched")
     return dq, dkk, dvv, dla, db, ds0
 
 

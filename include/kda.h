@@ -167,8 +167,11 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
  * The other arguments are those of kda_chunk_fwd (same inputs, same
  * cu_seqlens rules: host arrays are validated here, device arrays in the
  * kernel, which records KDA_ERR_INVALID_ARG and writes nothing).  The states
- * are recomputed: a forward sweep stores the state before every 16th token in
- * the workspace, and the reverse sweep recomputes the states in between.  fp32
+ * are recomputed: a forward sweep stores the state before every E-th token in
+ * the workspace, and the reverse sweep recomputes the states in between, in
+ * groups of four tokens.  E is the smallest power of two >= 4 whose stored
+ * states (64 KiB per head for every E tokens and per sequence) fit in 16 GiB,
+ * or 1024; kda_chunk_bwd_sched takes it from the caller instead.  fp32
  * arithmetic on CUDA cores; dq, dk, d_log_alpha and d_beta are sums over the
  * value channels, added in fp32 in an order that may vary between calls (last
  * bits only).
@@ -185,12 +188,36 @@ int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *log_
 
 /*
  * Bytes of device workspace kda_chunk_bwd needs: the status block, a device
- * copy of a host cu_seqlens, the stored states (64 KiB per head for every 16
- * tokens and per sequence) and fp32 accumulators of dq and dk.
+ * copy of a host cu_seqlens, the stored states (64 KiB per head for every E
+ * tokens and per sequence, E as in kda_chunk_bwd) and fp32 accumulators of dq
+ * and dk.
  * Errors: as kda_chunk_fwd_workspace_size.
  */
 int kda_chunk_bwd_workspace_size(int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk,
                                  int32_t dv, int dtype, size_t *bytes);
+
+/*
+ * kda_chunk_bwd with the checkpoint interval E chosen by the caller:
+ * ckpt_every = 0 is the library's choice (as kda_chunk_bwd), otherwise a power
+ * of two in [4, 1024].  E = 4 recomputes nothing twice and stores the most
+ * states; each doubling halves the stored states and adds about (E / 4 - 1) / 2
+ * recomputed forward steps per token.  Every E gives the same results: the
+ * states replayed from a stored one are the forward sweep's own, bit for bit.
+ * Arguments, results and errors otherwise those of kda_chunk_bwd; another
+ * ckpt_every is KDA_ERR_INVALID_ARG.  The workspace must hold
+ * kda_chunk_bwd_workspace_size_sched bytes for the same ckpt_every.
+ */
+int kda_chunk_bwd_sched(const void *q, const void *k, const void *v, const float *log_alpha,
+                        const float *beta, const float *init_state, const int32_t *cu_seqlens,
+                        int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk, int32_t dv,
+                        int dtype, const void *d_out, const float *d_final_state, void *dq,
+                        void *dk_, void *dv_, float *d_log_alpha, float *d_beta,
+                        float *d_init_state, int32_t ckpt_every, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+/* Workspace bytes of kda_chunk_bwd_sched for ckpt_every (0: the library's choice). */
+int kda_chunk_bwd_workspace_size_sched(int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk,
+                                       int32_t dv, int dtype, int32_t ckpt_every, size_t *bytes);
 
 /*
  * kda_chunk_fwd with the schedule capped by the caller.  Arguments, results

@@ -385,3 +385,48 @@ def test_layer_replay_rejects_before_launch(lib, over, code):
 
 def test_layer_replay_empty_batch_launches_nothing(lib):
     assert _layer_replay(lib, B=0) == 0
+
+
+def _bwd(lib, **over):
+    n = 0x1000000
+    args = dict(q=A, k=A + n, v=A + 2 * n, la=A + 3 * n, beta=A + 4 * n, init=None, cu=A + 5 * n,
+                n_seqs=1, N=64, H=2, dk=128, dv=128, dtype=1, do=A + 6 * n, df=None, dq=A + 7 * n,
+                dkk=A + 8 * n, dvv=A + 9 * n, dla=A + 10 * n, db=A + 11 * n, dinit=None, every=0,
+                ws=None, ws_bytes=0, stream=None)
+    args.update(over)
+    vp = ctypes.c_void_p
+    return lib.kda_chunk_bwd_sched(
+        *(vp(args[x]) for x in ("q", "k", "v", "la", "beta", "init", "cu")), args["n_seqs"],
+        args["N"], args["H"], args["dk"], args["dv"], args["dtype"],
+        *(vp(args[x]) for x in ("do", "df", "dq", "dkk", "dvv", "dla", "db", "dinit")),
+        args["every"], vp(args["ws"]), args["ws_bytes"], vp(args["stream"]))
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(), 3),                                      # everything valid but the workspace
+    (dict(every=16), 3), (dict(every=1024), 3),
+    (dict(every=3), 1), (dict(every=2), 1), (dict(every=6), 1), (dict(every=2048), 1),
+    (dict(every=-1), 1),
+    (dict(q=None), 1), (dict(cu=None), 1), (dict(dk=64), 2), (dict(dtype=4), 2),
+    (dict(q=A + 1), 1), (dict(la=A + 0x3000002), 1),
+    (dict(dq=A), 1),                                  # dq over q
+    (dict(db=A + 0xA000000), 1),                      # d_beta over d_log_alpha
+])
+def test_bwd_rejects_before_launch(lib, over, code):
+    assert _bwd(lib, **over) == code
+
+
+def test_bwd_workspace_size_follows_the_checkpoint_interval(lib):
+    from gated_delta_rule_13_gb300 import kda
+    small = kda.kda_chunk_bwd_workspace_size(4, 16384, 16)
+    assert small == kda.kda_chunk_bwd_workspace_size(4, 16384, 16, ckpt_every=4)
+    s16 = kda.kda_chunk_bwd_workspace_size(4, 16384, 16, ckpt_every=16)
+    state = 128 * 128 * 4
+    assert small - s16 == (16384 // 4 - 16384 // 16) * 16 * state
+    # a long problem gets a wider default interval, its states within 16 GiB
+    big = kda.kda_chunk_bwd_workspace_size(8, 1 << 20, 96)
+    acc = 2 * (1 << 20) * 96 * 128 * 4
+    assert big - acc <= (16 << 30) + (1 << 20)
+    for bad in (3, 6, 2048, -4):
+        with pytest.raises(RuntimeError):
+            kda.kda_chunk_bwd_workspace_size(1, 64, 1, ckpt_every=bad)

@@ -114,3 +114,26 @@ def test_bwd_b4_h16_t4096_sampled_heads():
     x = inputs.workload_inputs("b4_h16_t4096", device=DEV)
     do, df = _grads_in(x, 99)
     _check(x, do, df, "bf16", heads=[0, 15])
+
+
+def test_bwd_checkpoint_interval_changes_nothing():
+    """Every checkpoint interval gives the default's gradients: the states
+    replayed from a stored one are the forward sweep's own, so dv and the
+    initial-state gradient (no atomics) are bitwise equal and the atomically
+    summed ones equal to their last bits.  Sequences shorter and longer than
+    the intervals, one of them empty, cover the recomputation of whole and
+    partial groups."""
+    lengths = [0, 3, 16, 47, 130, 300]
+    x = inputs.prefill_inputs(lengths, H=2, dtype="f32", init_state=True, device=DEV, seed=101)
+    do, df = _grads_in(x, 102)
+    base = kda.kda_chunk_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["init_state"],
+                             x["cu_seqlens"], do, df)
+    cu = x["cu_seqlens"].cpu().numpy()
+    for every in (4, 8, 16, 64, 1024):
+        g = kda.kda_chunk_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["init_state"],
+                              x["cu_seqlens"], do, df, ckpt_every=every)
+        torch.cuda.synchronize()
+        assert torch.equal(g[2], base[2]) and torch.equal(g[5], base[5]), every
+        for i in (0, 1, 3):
+            assert_parity(g[i], base[i], 1e-5, cu=cu, name=f"gradient {i}, every {every}")
+        assert_parity(g[4][..., None], base[4][..., None], 1e-5, cu=cu, name=f"d_beta, every {every}")
