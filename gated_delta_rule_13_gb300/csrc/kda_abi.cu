@@ -180,11 +180,14 @@ int kda_chunk_bwd_sched(const void *q, const void *k, const void *v, const float
     return KDA_ERR_INVALID_ARG;
   if ((int64_t)n_seqs * H * 4 > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
   const size_t esz = dtype == KDA_BF16 ? 2 : 4;
-  const void *elem[] = {q, k, v, d_out, dq, dk_, dv_};
+  // q, k, v, log_alpha and d_out rows are fetched by 16-byte asynchronous copies
+  const void *rows[] = {q, k, v, log_alpha, d_out};
+  for (const void *p : rows)
+    if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  const void *elem[] = {dq, dk_, dv_};
   for (const void *p : elem)
     if (p && !aligned(p, esz)) return KDA_ERR_INVALID_ARG;
-  const void *f32[] = {log_alpha, beta, init_state, d_final_state, d_log_alpha, d_beta,
-                       d_init_state};
+  const void *f32[] = {beta, init_state, d_final_state, d_log_alpha, d_beta, d_init_state};
   for (const void *p : f32)
     if (p && !aligned(p, 4)) return KDA_ERR_INVALID_ARG;
   // no output may overlap an input or another output

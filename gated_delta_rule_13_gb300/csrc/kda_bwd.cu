@@ -82,6 +82,97 @@ __device__ void stage_tokens(Stage &st, int64_t tb, int n, int h, int H, int cb,
   if (threadIdx.x < n) st.beta[threadIdx.x] = beta[(tb + threadIdx.x) * H + h];
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only), and its group fences.
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+// Raw inputs of up to kGroup tokens as they sit in HBM, copied asynchronously
+// one group ahead: per token the q, k and log_alpha rows, then the CTA's
+// 32-column blocks of v and d_out (q, d_out unused by the forward sweep).
+template <bool BF16>
+struct RawLayout {
+  static constexpr int kEsz = BF16 ? 2 : 4;
+  static constexpr int kQ = 0, kK = D * kEsz, kLa = 2 * D * kEsz, kV = kLa + 4 * D,
+                       kDo = kV + kCols * kEsz, kTok = kDo + kCols * kEsz;
+  // 16-byte pieces per token: q, k, log_alpha rows, v and d_out blocks
+  static constexpr int kRowPieces = D * kEsz / 16, kLaPieces = D * 4 / 16,
+                       kBlkPieces = kCols * kEsz / 16;
+  static constexpr int kPieces = 2 * kRowPieces + kLaPieces + 2 * kBlkPieces;
+};
+static_assert(RawLayout<true>::kTok % 16 == 0 && RawLayout<false>::kTok % 16 == 0,
+              "raw token rows keep 16-byte alignment");
+constexpr int kRawBytes = kGroup * RawLayout<false>::kTok;  // the larger (fp32) layout
+
+// Issues (every thread) the copies of tokens tb .. tb + n - 1 of head h, value
+// block cb into raw; with_q also their q and d_out.  One commit group.
+template <bool BF16>
+__device__ void prefetch_tokens(uint8_t *raw, int64_t tb, int n, int h, int H, int cb,
+                                bool with_q, const void *q, const void *k, const void *v,
+                                const float *la, const void *dout) {
+  using L = RawLayout<BF16>;
+  for (int e = threadIdx.x; e < n * L::kPieces; e += kThreads) {
+    const int i = e / L::kPieces;
+    int r = e % L::kPieces;
+    const int64_t row = (tb + i) * H + h;  // token row of the [N, H, 128] tensors
+    uint8_t *dst = raw + i * L::kTok;
+    const uint8_t *src = nullptr;
+    if (r < L::kRowPieces) {
+      if (with_q) src = static_cast<const uint8_t *>(q) + row * D * L::kEsz + 16 * r;
+      dst += L::kQ + 16 * r;
+    } else if ((r -= L::kRowPieces) < L::kRowPieces) {
+      src = static_cast<const uint8_t *>(k) + row * D * L::kEsz + 16 * r;
+      dst += L::kK + 16 * r;
+    } else if ((r -= L::kRowPieces) < L::kLaPieces) {
+      src = reinterpret_cast<const uint8_t *>(la + row * D) + 16 * r;
+      dst += L::kLa + 16 * r;
+    } else if ((r -= L::kLaPieces) < L::kBlkPieces) {
+      src = static_cast<const uint8_t *>(v) + (row * D + cb * kCols) * L::kEsz + 16 * r;
+      dst += L::kV + 16 * r;
+    } else {
+      r -= L::kBlkPieces;
+      if (with_q) src = static_cast<const uint8_t *>(dout) + (row * D + cb * kCols) * L::kEsz + 16 * r;
+      dst += L::kDo + 16 * r;
+    }
+    if (src) cp_async16(dst, src);
+  }
+  cp_async_commit();
+}
+
+template <bool BF16>
+__device__ __forceinline__ float raw_elem(const uint8_t *p, int c) {
+  if constexpr (BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[c]);
+  else return reinterpret_cast<const float *>(p)[c];
+}
+
+// The landed raw inputs of n tokens into st (alpha = e^{log_alpha}); the betas
+// come from the threads that loaded them (thread i: token i).
+template <bool BF16>
+__device__ void convert_tokens(Stage &st, const uint8_t *raw, int n, bool with_q, float my_beta) {
+  using L = RawLayout<BF16>;
+  for (int e = threadIdx.x; e < n * D; e += kThreads) {
+    const int i = e / D, c = e % D;
+    const uint8_t *t = raw + i * L::kTok;
+    st.q[i][c] = with_q ? raw_elem<BF16>(t + L::kQ, c) : 0.f;
+    st.k[i][c] = raw_elem<BF16>(t + L::kK, c);
+    st.alpha[i][c] = expf(reinterpret_cast<const float *>(t + L::kLa)[c]);
+  }
+  for (int e = threadIdx.x; e < n * kCols; e += kThreads) {
+    const int i = e / kCols, c = e % kCols;
+    const uint8_t *t = raw + i * L::kTok;
+    st.v[i][c] = raw_elem<BF16>(t + L::kV, c);
+    st.dout[i][c] = with_q ? raw_elem<BF16>(t + L::kDo, c) : 0.f;
+  }
+  if (threadIdx.x < n) st.beta[threadIdx.x] = my_beta;
+}
+
 // One forward token on this thread's 16 state values (rows r0 + j, column
 // lane); the decayed state X and the per-column p, d are returned.  Uses red.
 __device__ __forceinline__ void fwd_token(float (&s)[kRows], float (&x)[kRows], float &p, float &d,
@@ -162,7 +253,7 @@ __device__ __forceinline__ Chain chain_of(const int32_t *cu, int32_t n_seqs, int
   return c;
 }
 
-// Forward pass: the state before every kCkpt-th token, per block of columns.
+// Forward pass: the state before every `every`-th token, per block of columns.
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 2)
 kda_bwd_ckpt_kernel(const void *__restrict__ k, const void *__restrict__ v,
@@ -172,6 +263,7 @@ kda_bwd_ckpt_kernel(const void *__restrict__ k, const void *__restrict__ v,
                     float *__restrict__ ckpt, DeviceStatus *status) {
   __shared__ Stage st;
   __shared__ float red[kThreads / 32][kCols];
+  __shared__ __align__(16) uint8_t raw[kRawBytes];
   const Chain c = chain_of(cu, n_seqs, n_tokens, H);
   if (!c.ok) {
     if (threadIdx.x == 0) atomicCAS(&status->code, 0, 1 /* KDA_ERR_INVALID_ARG */);
@@ -184,11 +276,22 @@ kda_bwd_ckpt_kernel(const void *__restrict__ k, const void *__restrict__ v,
 #pragma unroll
   for (int j = 0; j < kRows; ++j) s[j] = init_state ? init_state[sbase + (r0 + j) * D + col] : 0.f;
   const int64_t base = ckpt_base(c.t0, c.seq, every);
+  // the inputs of each group are copied while the group before it runs
+  auto group_len = [&](int64_t tb) { return (int)(c.t1 - tb < kGroup ? c.t1 - tb : kGroup); };
+  float nbeta = 0.f;
+  auto prefetch = [&](int64_t tb) {
+    const int n = group_len(tb);
+    prefetch_tokens<BF16>(raw, tb, n, c.h, H, c.cb, false, nullptr, k, v, la, nullptr);
+    if (threadIdx.x < n) nbeta = beta[(tb + threadIdx.x) * H + c.h];
+  };
+  if (c.t0 < c.t1) prefetch(c.t0);
   for (int64_t tb = c.t0; tb < c.t1; tb += kGroup) {
-    const int n = (int)(c.t1 - tb < kGroup ? c.t1 - tb : kGroup);
-    __syncthreads();  // the previous group's stage is consumed
-    stage_tokens<BF16>(st, tb, n, c.h, H, c.cb, nullptr, k, v, la, beta, nullptr);
-    __syncthreads();
+    const int n = group_len(tb);
+    cp_async_wait_all();
+    __syncthreads();  // the group's copies landed; the previous group's stage is consumed
+    convert_tokens<BF16>(st, raw, n, false, nbeta);
+    __syncthreads();  // st ready, raw free
+    if (tb + kGroup < c.t1) prefetch(tb + kGroup);
     for (int i = 0; i < n; ++i) {
       const int64_t t = tb + i;
       if ((t - c.t0) % every == 0) {
@@ -213,9 +316,11 @@ kda_bwd_kernel(const void *__restrict__ q, const void *__restrict__ k, const voi
                float *__restrict__ dk_acc, void *__restrict__ dv_out, float *__restrict__ dla,
                float *__restrict__ dbeta, float *__restrict__ d_init) {
   extern __shared__ __align__(16) float xs[];  // [kGroup][D][kCols] decayed states
-  __shared__ Stage st;
+  __shared__ Stage st, st_rec;  // the group's inputs; a recomputed earlier group's
   __shared__ float red[kThreads / 32][kCols];
   __shared__ float s_p[kGroup][kCols], s_d[kGroup][kCols];
+  __shared__ __align__(16) float ckbuf[D][kCols];  // the block's stored state, this CTA's columns
+  __shared__ __align__(16) uint8_t raw[kRawBytes];
   const Chain c = chain_of(cu, n_seqs, n_tokens, H);
   if (!c.ok) return;  // recorded by the forward pass
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, r0 = kRows * warp;
@@ -227,31 +332,58 @@ kda_bwd_kernel(const void *__restrict__ q, const void *__restrict__ k, const voi
   const int64_t base = ckpt_base(c.t0, c.seq, every);
   const int64_t len = c.t1 - c.t0;
   const int64_t n_ck = (len + every - 1) / every;
+  // Work items (block blk of `every` tokens, group g of kGroup tokens in it), in
+  // reverse.  Each item's stored state and own inputs are copied while the item
+  // before it runs; the inputs of the groups it recomputes are loaded in place.
+  auto block_end = [&](int64_t blk) {
+    const int64_t e = c.t0 + (blk + 1) * every;
+    return e < c.t1 ? e : c.t1;
+  };
+  auto groups_of = [&](int64_t blk) {
+    return (int)((block_end(blk) - (c.t0 + blk * every) + kGroup - 1) / kGroup);
+  };
+  float nbeta = 0.f;
+  auto prefetch = [&](int64_t blk, int g) {
+    const float *src = ckpt + ((base + blk) * H + c.h) * D * D + c.cb * kCols;
+    for (int e = threadIdx.x; e < D * (kCols / 4); e += kThreads) {
+      const int row = e / (kCols / 4), q4 = e % (kCols / 4);
+      cp_async16(&ckbuf[row][4 * q4], src + row * D + 4 * q4);
+    }
+    const int64_t gb = c.t0 + blk * every + (int64_t)g * kGroup;
+    const int64_t e = block_end(blk);
+    const int n = (int)(e - gb < kGroup ? e - gb : kGroup);
+    prefetch_tokens<BF16>(raw, gb, n, c.h, H, c.cb, true, q, k, v, la, dout);
+    if (threadIdx.x < n) nbeta = beta[(gb + threadIdx.x) * H + c.h];
+  };
+  if (n_ck > 0) prefetch(n_ck - 1, groups_of(n_ck - 1) - 1);
   for (int64_t blk = n_ck - 1; blk >= 0; --blk) {
     const int64_t a = c.t0 + blk * every;
-    const int64_t e = a + every < c.t1 ? a + every : c.t1;
-    const int n_groups = (int)((e - a + kGroup - 1) / kGroup);
+    const int64_t e = block_end(blk);
+    const int n_groups = groups_of(blk);
     for (int g = n_groups - 1; g >= 0; --g) {
-      // state before token a, then forward to the group's first token
+      const int64_t gb = a + (int64_t)g * kGroup;
+      const int n = (int)(e - gb < kGroup ? e - gb : kGroup);
+      // the item's copies have landed: the state before token a, the group's inputs
+      cp_async_wait_all();
+      __syncthreads();
       float s[kRows], x[kRows];
-      const float *src = ckpt + ((base + blk) * H + c.h) * D * D;
 #pragma unroll
-      for (int j = 0; j < kRows; ++j) s[j] = src[(r0 + j) * D + col];
-      for (int64_t tb = a; tb < a + (int64_t)g * kGroup; tb += kGroup) {
+      for (int j = 0; j < kRows; ++j) s[j] = ckbuf[r0 + j][lane];
+      convert_tokens<BF16>(st, raw, n, true, nbeta);
+      __syncthreads();  // ckbuf and raw are free; st is ready
+      if (g > 0) prefetch(blk, g - 1);
+      else if (blk > 0) prefetch(blk - 1, groups_of(blk - 1) - 1);
+      // forward to the group's first token
+      for (int64_t tb = a; tb < gb; tb += kGroup) {
         __syncthreads();
-        stage_tokens<BF16>(st, tb, kGroup, c.h, H, c.cb, nullptr, k, v, la, beta, nullptr);
+        stage_tokens<BF16>(st_rec, tb, kGroup, c.h, H, c.cb, nullptr, k, v, la, beta, nullptr);
         __syncthreads();
         for (int i = 0; i < kGroup; ++i) {
           float p, d;
-          fwd_token(s, x, p, d, st, i, r0, lane, warp, red);
+          fwd_token(s, x, p, d, st_rec, i, r0, lane, warp, red);
         }
       }
       // the group's tokens: X, p and d kept
-      const int64_t gb = a + (int64_t)g * kGroup;
-      const int n = (int)(e - gb < kGroup ? e - gb : kGroup);
-      __syncthreads();
-      stage_tokens<BF16>(st, gb, n, c.h, H, c.cb, q, k, v, la, beta, dout);
-      __syncthreads();
       for (int i = 0; i < n; ++i) {
         float p, d;
         fwd_token(s, x, p, d, st, i, r0, lane, warp, red);

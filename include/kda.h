@@ -175,8 +175,9 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
  * arithmetic on CUDA cores; dq, dk, d_log_alpha and d_beta are sums over the
  * value channels, added in fp32 in an order that may vary between calls (last
  * bits only).
- * Alignment: element alignment for every tensor.  No output may overlap an
- * input or another output.
+ * Alignment: q, k, v, log_alpha and d_out 16 bytes (their rows are fetched by
+ * 16-byte asynchronous copies); element alignment for every other tensor.  No
+ * output may overlap an input or another output.
  * Errors: as kda_chunk_fwd, with the workspace of kda_chunk_bwd_workspace_size.
  */
 int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *log_alpha,

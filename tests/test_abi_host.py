@@ -409,6 +409,9 @@ def _bwd(lib, **over):
     (dict(every=-1), 1),
     (dict(q=None), 1), (dict(cu=None), 1), (dict(dk=64), 2), (dict(dtype=4), 2),
     (dict(q=A + 1), 1), (dict(la=A + 0x3000002), 1),
+    # element-aligned but not 16-byte aligned: rows are fetched by 16-byte copies
+    (dict(q=A + 2), 1), (dict(v=A + 0x2000008), 1), (dict(do=A + 0x6000004), 1),
+    (dict(dq=A + 0x7000002), 3),                      # outputs need element alignment only
     (dict(dq=A), 1),                                  # dq over q
     (dict(db=A + 0xA000000), 1),                      # d_beta over d_log_alpha
 ])
