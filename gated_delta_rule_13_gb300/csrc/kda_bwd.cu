@@ -173,26 +173,31 @@ __device__ void convert_tokens(Stage &st, const uint8_t *raw, int n, bool with_q
   if (threadIdx.x < n) st.beta[threadIdx.x] = my_beta;
 }
 
+// The per-warp column partial sums, in two buffers used in turn (rp counts the
+// uses): a buffer is rewritten only two uses later, after a barrier every
+// thread passes once it has read it, so one barrier per use suffices.
+using Red = float[2][kThreads / 32][kCols];
+
 // One forward token on this thread's 16 state values (rows r0 + j, column
-// lane); the decayed state X and the per-column p, d are returned.  Uses red.
+// lane); the decayed state X and the per-column p, d are returned.
 __device__ __forceinline__ void fwd_token(float (&s)[kRows], float (&x)[kRows], float &p, float &d,
                                           const Stage &st, int i, int r0, int lane, int warp,
-                                          float (*red)[kCols]) {
+                                          Red &red, uint32_t &rp) {
   float part = 0.f;
 #pragma unroll
   for (int j = 0; j < kRows; ++j) {
     x[j] = st.alpha[i][r0 + j] * s[j];
     part = fmaf(x[j], st.k[i][r0 + j], part);
   }
-  red[warp][lane] = part;
+  float (&rb)[kThreads / 32][kCols] = red[rp++ & 1u];
+  rb[warp][lane] = part;
   __syncthreads();
   p = 0.f;
 #pragma unroll
-  for (int w = 0; w < kThreads / 32; ++w) p += red[w][lane];
+  for (int w = 0; w < kThreads / 32; ++w) p += rb[w][lane];
   d = st.beta[i] * (st.v[i][lane] - p);
 #pragma unroll
   for (int j = 0; j < kRows; ++j) s[j] = fmaf(st.k[i][r0 + j], d, x[j]);
-  __syncthreads();  // red is free again
 }
 
 // Sum of v[j] over the 32 lanes, for each of the 16 rows j: after four
@@ -262,7 +267,8 @@ kda_bwd_ckpt_kernel(const void *__restrict__ k, const void *__restrict__ v,
                     int32_t n_seqs, int64_t n_tokens, int32_t H, int every,
                     float *__restrict__ ckpt, DeviceStatus *status) {
   __shared__ Stage st;
-  __shared__ float red[kThreads / 32][kCols];
+  __shared__ Red red;
+  uint32_t rp = 0;
   __shared__ __align__(16) uint8_t raw[kRawBytes];
   const Chain c = chain_of(cu, n_seqs, n_tokens, H);
   if (!c.ok) {
@@ -300,7 +306,7 @@ kda_bwd_ckpt_kernel(const void *__restrict__ k, const void *__restrict__ v,
         for (int j = 0; j < kRows; ++j) dst[(r0 + j) * D + col] = s[j];
       }
       float p, d;
-      fwd_token(s, x, p, d, st, i, r0, lane, warp, red);
+      fwd_token(s, x, p, d, st, i, r0, lane, warp, red, rp);
     }
   }
 }
@@ -317,7 +323,8 @@ kda_bwd_kernel(const void *__restrict__ q, const void *__restrict__ k, const voi
                float *__restrict__ dbeta, float *__restrict__ d_init) {
   extern __shared__ __align__(16) float xs[];  // [kGroup][D][kCols] decayed states
   __shared__ Stage st, st_rec;  // the group's inputs; a recomputed earlier group's
-  __shared__ float red[kThreads / 32][kCols];
+  __shared__ Red red;
+  uint32_t rp = 0;
   __shared__ float s_p[kGroup][kCols], s_d[kGroup][kCols];
   __shared__ __align__(16) float ckbuf[D][kCols];  // the block's stored state, this CTA's columns
   __shared__ __align__(16) uint8_t raw[kRawBytes];
@@ -380,13 +387,13 @@ kda_bwd_kernel(const void *__restrict__ q, const void *__restrict__ k, const voi
         __syncthreads();
         for (int i = 0; i < kGroup; ++i) {
           float p, d;
-          fwd_token(s, x, p, d, st_rec, i, r0, lane, warp, red);
+          fwd_token(s, x, p, d, st_rec, i, r0, lane, warp, red, rp);
         }
       }
       // the group's tokens: X, p and d kept
       for (int i = 0; i < n; ++i) {
         float p, d;
-        fwd_token(s, x, p, d, st, i, r0, lane, warp, red);
+        fwd_token(s, x, p, d, st, i, r0, lane, warp, red, rp);
 #pragma unroll
         for (int j = 0; j < kRows; ++j) xs[(i * D + r0 + j) * kCols + lane] = x[j];
         if (warp == 0) {
@@ -413,11 +420,12 @@ kda_bwd_kernel(const void *__restrict__ q, const void *__restrict__ k, const voi
           part = fmaf(ds[j], kr, part);                  // dd = dS^T k (column sums)
           cl[j] = xv;                                    // X, kept for the next pass
         }
-        red[warp][lane] = part;
+        float (&rb)[kThreads / 32][kCols] = red[rp++ & 1u];
+        rb[warp][lane] = part;
         __syncthreads();
         float dd = 0.f;
 #pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) dd += red[w][lane];
+        for (int w = 0; w < kThreads / 32; ++w) dd += rb[w][lane];
         const float dp = -b * dd;
         if (warp == 0) {
           const float dvv = b * dd;
@@ -446,7 +454,6 @@ kda_bwd_kernel(const void *__restrict__ q, const void *__restrict__ k, const voi
           atomicAdd(dk_acc + trow + r, sk);
           atomicAdd(dla + trow + r, sl);
         }
-        __syncthreads();  // red is free again
       }
     }
   }
