@@ -153,7 +153,7 @@ __device__ __forceinline__ float4 conv_swish(float4 x0, float4 x1, float4 x2, fl
 // warp slides a window of the three previous raw rows through registers and
 // loads the next kGroup rows while it works on the current ones, so each input
 // row is read once, plus a three-row halo per run.
-constexpr int kRunTokens = 32;
+constexpr int kRunTokens = 128;
 
 template <bool BF16, bool kWindow>
 __global__ void __launch_bounds__(32 * kWarps, 4)
@@ -174,8 +174,7 @@ kda_prep_kernel(const void *__restrict__ q_raw, const void *__restrict__ k_raw,
   auto row_of = [&](int64_t t) { return (t * H + h) * D + c0; };
 
   if (blockIdx.z == 3) {  // gates: log_alpha = -5 sigmoid(a), beta = sigmoid(b)
-    const int64_t tb = t0 + lane;
-    if (tb < t_end) beta[tb * H + h] = sigmoidf(b_logit[tb * H + h]);
+    for (int64_t tb = t0 + lane; tb < t_end; tb += 32) beta[tb * H + h] = sigmoidf(b_logit[tb * H + h]);
     const int64_t rs = (int64_t)H * D;
     const float *ain = a_logit + row_of(t0);
     float *aout = log_alpha + row_of(t0);

@@ -25,6 +25,9 @@ PREP_CASES = [
     ([0, 1, 3, 4, 37, 130], 3),
     # many tiny and empty sequences inside one run of tokens; H not a multiple of 8
     ([1, 0, 0, 2, 1, 5, 0, 3, 33, 1, 2, 0, 70], 9),
+    # sequence starts just before, at and after the boundaries of 128-token runs,
+    # and one sequence across several runs
+    ([127, 1, 129, 0, 2, 300], 3),
 ]
 
 
