@@ -114,6 +114,7 @@ struct Misc {
   uint64_t bar_plan;            // the issue thread has planned the next chunk
   uint64_t bar_pka, bar_pkb;    // package copies: [Gamma, Qt; Kt, Kdec] and [T', P]
   uint64_t bar_wb;              // helper: the package has been read out of shared memory
+  uint64_t bar_stg;             // chain with helpers: the staged output rows have been read
   uint32_t tmem_base;
   int abort;
   int test_chunk;               // chunk whose Gram-operand arrival a test withholds (-1: none)
@@ -350,7 +351,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     mbar_init(&m.bar_ny, kComputeWarps / 2);
     mbar_init(&m.bar_ad, kComputeWarps);
     mbar_init(&m.bar_plan, 1); mbar_init(&m.bar_pka, 1); mbar_init(&m.bar_pkb, 1);
-    mbar_init(&m.bar_wb, 1);
+    mbar_init(&m.bar_wb, 1); mbar_init(&m.bar_stg, 1);
     fence_mbarrier_init();
     m.abort = 0;
     for (int i = 0; i < 5; ++i) m.last_copy[i] = 0;
@@ -641,13 +642,6 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (!wait_bar(cx, &m.bar_ny, par, 33, ci, kPoll)) break;
         PHASE_MARK_MMA(3);
         if (has_next) issue_v(ci + 1, h, tok(ci + 1));   // the (V - Y) pass has read this chunk's v tile
-        if (helped_next) {
-          // [Qt; Kt] and Kdec of the next chunk: this chunk's O+Y MMAs have read
-          // the stack and the staged output stores have left the Kdec buffer.
-          bulk_load(sa + SM_STACK, slot_of(ci + 1) + PKG_STACK, 32768, &m.bar_pka);
-          bulk_load(sa + SM_KDEC + 16384u * (uint32_t)((ci + 1) & 1), slot_of(ci + 1) + PKG_KDEC,
-                    16384, &m.bar_pka);
-        }
         if (!wait_bar(cx, &m.bar_t1, par, 37, ci, kPoll)) break;
         if (helped_cur && !wait_bar(cx, &m.bar_pkb, par, 39, ci, kPoll)) break;
         tc_fence_after();
@@ -665,6 +659,16 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         umma_ts(tmb + TM_D + 32u, tmb + TM_NY + 8u, kd(SM_TMAT + 32u * 128u + 32u), ID_N32,
                 1u);                                                                   // r 32-63, s 1
         umma_commit(&m.bar_u);
+        if (helped_next) {
+          // [Qt; Kt] of the next chunk once every MMA up to this chunk's Delta has
+          // completed (its O MMAs read the stack), and its Kdec once the staged
+          // output stores have read the Kdec buffer they share.
+          if (!wait_bar(cx, &m.bar_u, par, 46, ci, kPoll)) break;
+          bulk_load(sa + SM_STACK, slot_of(ci + 1) + PKG_STACK, 32768, &m.bar_pka);
+          if (!wait_bar(cx, &m.bar_stg, par, 47, ci, kPoll)) break;
+          bulk_load(sa + SM_KDEC + 16384u * (uint32_t)((ci + 1) & 1), slot_of(ci + 1) + PKG_KDEC,
+                    16384, &m.bar_pka);
+        }
         // S^T += Delta^T Kdec ; O^T += Delta^T P^T
         if (!wait_bar(cx, &m.bar_ad, par, 35, ci, kPoll)) break;
         PHASE_MARK_MMA(4);
@@ -1180,10 +1184,13 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         tc_fence_before();
         // The staged output stores must have read the Kdec buffer before anything
-        // reuses it: a package copy (issued once bar_ny completes) or the next build.
-        if (helping && tid == 128) bulk_wait_read_all();
+        // reuses it: the next build (after barriers thread 128 joins only past
+        // this wait) or, with helpers, a package copy (issued on bar_stg).
         warp_arrive(&m.bar_ny, lane);
-        if (!helping && tid == 128) bulk_wait_read_all();
+        if (tid == 128) {
+          bulk_wait_read_all();
+          if (helping) mbar_arrive(&m.bar_stg);
+        }
         PHASE_MARK_W4(3);
         PHASE_MARK_W7(1);
       }
