@@ -415,9 +415,9 @@ def few_chains_bench(dev, peaks, steps: int = 20, warmup: int = 3, T: int = 6553
 
 def prefill_config_bench(dev, peaks, workload: str, steps: int, warmup: int = 3):
     """One prefill workload timed on its own (CUDA events over `steps` launches
-    after `warmup`), with its roofline: the bytes of SURVEY's per-token-head
-    count (bf16 q, k, v, out, fp32 log_alpha and beta) plus the states read
-    and written, against the measured HBM copy peak."""
+    after `warmup`), with its roofline: the algorithmic bytes per token-head
+    (bf16 q, k, v, out, fp32 log_alpha and beta) plus the states read and
+    written, against the measured HBM copy peak."""
     import torch
     from gated_delta_rule_13_gb300 import inputs, kda
     w = inputs.WORKLOADS[workload]
