@@ -424,10 +424,12 @@ def prefill_config_bench(dev, peaks, workload: str, steps: int, warmup: int = 3)
     x = inputs.workload_inputs(workload, device=dev)
     n_tok, H = int(x["q"].shape[0]), w.H
     n_seqs = len(x["lengths"])
-    out = torch.empty(n_tok, H, 128, dtype=torch.bfloat16, device=dev)
+    bf16 = x["q"].dtype == torch.bfloat16
+    out = torch.empty(n_tok, H, 128, dtype=x["q"].dtype, device=dev)
     fin = torch.empty(n_seqs, H, 128, 128, dtype=torch.float32, device=dev)
-    ws = torch.zeros(kda.kda_chunk_fwd_workspace_size(n_seqs, n_tok, H), dtype=torch.uint8,
-                     device=dev)
+    ws = torch.zeros(kda.kda_chunk_fwd_workspace_size(
+        n_seqs, n_tok, H, dtype=kda.KDA_BF16 if bf16 else kda.KDA_F32), dtype=torch.uint8,
+        device=dev)
 
     def run():
         kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["init_state"],
@@ -451,10 +453,12 @@ def prefill_config_bench(dev, peaks, workload: str, steps: int, warmup: int = 3)
     res = {"workload": f"{workload}: {w.note}", "tokens": n_tok, "heads": H,
            "tokens_per_s": n_tok / (ms / 1000.0), "ms_per_launch": ms, "launches": steps,
            "device_status_ok": ok,
-           "roofline": {"bound": "hbm", "kernel": "kda_chunk_fwd_tc_kernel", "achieved": gbs,
+           "roofline": {"bound": "hbm",
+                        "kernel": "kda_chunk_fwd_tc_kernel" if bf16 else "kda_chunk_fwd_f32_kernel",
+                        "achieved": gbs,
                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
                         "traffic": recorded_traffic("kda_chunk_fwd_tc_kernel", "kda_chunk_tc.cu",
-                                                    workload),
+                                                    workload) if bf16 else None,
                         "bytes_per_launch": nbytes,
                         "tensor_frac": flop / (ms / 1000.0) / 1e12 / peaks["bf16_tflops"]}}
     del x, out, fin, ws
@@ -576,10 +580,15 @@ def backward_bench(dev, peaks, workload: str = "b4_h16_t4096", steps: int = 5, w
 
 
 def prefill_bytes(x, H):
+    """Algorithmic bytes of one prefill launch: per token-head q, k, v and the
+    output in the input type, fp32 log_alpha and beta (1,540 B for bf16, 2,564 B
+    for fp32), plus the states read and written."""
+    import torch
     n_tok = int(x["q"].shape[0])
     n_seqs = int(x["cu_seqlens"].shape[0] - 1)
     states = n_seqs * H * (2 if x["init_state"] is not None else 1)
-    return n_tok * H * PREFILL_BYTES_PER_TOKEN_HEAD + states * STATE_BYTES
+    per_th = PREFILL_BYTES_PER_TOKEN_HEAD if x["q"].dtype == torch.bfloat16 else 4 * 128 * 4 + 512 + 4
+    return n_tok * H * per_th + states * STATE_BYTES
 
 
 def run_gpu(args):
@@ -708,7 +717,8 @@ def run_gpu(args):
     layer_replay = layer_replay_bench(dev, peaks, steps=args.sub_steps)
     backward = backward_bench(dev, peaks) if args.backward else None
     configs = {}
-    for wl, n in (("b4_h16_t4096", args.sub_steps), ("varlen_h96_1m", args.varlen_steps)):
+    for wl, n in (("tiny_f32", args.sub_steps), ("b4_h16_t4096", args.sub_steps),
+                  ("varlen_h96_1m", args.varlen_steps)):
         if n > 0:
             configs[wl] = prefill_config_bench(dev, peaks, wl, steps=n)
     if world > 1:

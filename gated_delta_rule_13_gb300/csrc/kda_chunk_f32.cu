@@ -1,9 +1,8 @@
 // fp32 chunkwise KDA prefill on CUDA cores (fp32 inputs, fp32 arithmetic).
 //
-// This is the plain chunk algebra with no tile factorisation of the decay: every
-// decay ratio exp(g_r - g_i) is evaluated directly, so it serves fp32 callers
-// that need ~1e-4 agreement with the exact recurrence.  One CTA carries one
-// (sequence, head) chain through chunks of C = 32 tokens.
+// One CTA carries one (sequence, head) chain through chunks of C = 32 tokens,
+// fp32 throughout, so it serves fp32 callers that need ~1e-4 agreement with the
+// exact recurrence.
 //
 // Chunk algebra (plainest reading of "Kimi K3: 架构、训练与系统全景解析",
 // section 4.2.4: state passed across chunks, lower-triangular matrix products
@@ -20,6 +19,15 @@
 // Rows past the end of a sequence get beta = 0 and log_alpha = 0, which makes
 // their Delta rows zero and leaves g constant, so a partial chunk needs no
 // other special case.
+//
+// Decay ratios.  e^{g_r - g_i} is split at the chunk's middle row m:
+// E_r = e^{g_r - g_m} and Ei_i = e^{g_m - g_i}, each one accurate expf, and
+// e^{g_r - g_i} = E_r Ei_i.  With log_alpha >= -5 (the K3 bound; "Kimi K3:
+// 架构、训练与系统全景解析", section 4.2.5) each factor lies within e^{+-80}, far
+// inside fp32, and for i <= r their product is the ratio itself (<= 1); the
+// arguments are clamped at 80 so that inputs outside the bound stay finite.
+// The products are register-tiled: every thread owns a small output tile and
+// streams the shared contraction dimension.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -31,23 +39,31 @@ namespace {
 
 constexpr int D = kHeadDim;
 constexpr int C = kChunkF32;
-constexpr int P = D + 1;  // padded pitch: column walks over rows are conflict-free
 constexpr int kThreads = 256;
+constexpr int PR = D + 4;   // pitch of row-streamed [C][D] arrays (16-byte aligned rows)
+constexpr int PC = D + 1;   // pitch of column-walked [C][D] arrays (conflict-free columns)
+constexpr int PT = C + 4;   // pitch of the C x C matrices (16-byte aligned rows)
+constexpr float kMaxArg = 80.f;
+static_assert(C == 32 && kThreads == 256, "the tilings below assume C = 32 and 256 threads");
 
 struct F32Smem {
-  float S[D][D];   // state [key c][value n]
-  float q[C][P];   // q, then q o e^{g}
-  float k[C][P];   // k, then k o e^{g}
-  float v[C][P];
-  float g[C][P];   // log_alpha, then cumulative log-decay, then O
-  float w[C][P];   // W
-  float u[C][P];   // U, then Delta
-  float kd[C][P];  // k o e^{g_C - g}
-  float A[C][C + 1];
-  float Pm[C][C + 1];
-  float T[C][C + 1];  // T Diag(beta)
+  float S[D][D];     // state [key c][value n]
+  float qe[C][PR];   // q, then q o E
+  float ke[C][PR];   // k o E
+  float kei[C][PC];  // k, then k o Ei
+  float kd[C][PR];   // Kdec = K o e^{g_C - g}
+  float v[C][PR];    // v
+  float g[C][PR];    // log_alpha, then the cumulative log-decay
+  float w[C][PR];    // W = T' (K o e^g)
+  float u[C][PR];    // U = T' V, then Delta
+  float At[C][PT];   // A^T (beta-scaled, strictly lower A)
+  float Pm[C][PT];   // P (lower incl. diagonal)
+  float Tp[C][PT];   // T' = T Diag(beta)
   float beta[C];
-  float gC[D];
+  float egm[D];      // e^{g_m}
+  float egc[D];      // e^{g_C}
+  float egcm[D];     // e^{g_C - g_m}
+  float gm[D];       // g_m
 };
 
 __device__ void record_error(DeviceStatus *st, int code, int detail, int chain, int chunk) {
@@ -58,6 +74,9 @@ __device__ void record_error(DeviceStatus *st, int code, int detail, int chain, 
   }
 }
 
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ void st4(float *p, float4 x) { *reinterpret_cast<float4 *>(p) = x; }
+
 __global__ void __launch_bounds__(kThreads, 1)
 kda_chunk_fwd_f32_kernel(const float *__restrict__ q, const float *__restrict__ k,
                          const float *__restrict__ v, const float *__restrict__ log_alpha,
@@ -67,7 +86,7 @@ kda_chunk_fwd_f32_kernel(const float *__restrict__ q, const float *__restrict__ 
                          float *__restrict__ final_state, DeviceStatus *status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   F32Smem &sm = *reinterpret_cast<F32Smem *>(smem_raw);
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int chain = blockIdx.x;
   const int seq = chain / H, h = chain % H;
 
@@ -92,104 +111,184 @@ kda_chunk_fwd_f32_kernel(const float *__restrict__ q, const float *__restrict__ 
       const int r = e / D, c = e % D;
       const bool ok = r < nv;
       const int64_t off = ((t0 + c0 + r) * H + h) * D + c;
-      sm.q[r][c] = ok ? q[off] : 0.f;
-      sm.k[r][c] = ok ? k[off] : 0.f;
+      sm.qe[r][c] = ok ? q[off] : 0.f;
+      sm.kei[r][c] = ok ? k[off] : 0.f;
       sm.v[r][c] = ok ? v[off] : 0.f;
       sm.g[r][c] = ok ? log_alpha[off] : 0.f;
     }
     if (tid < C) sm.beta[tid] = tid < nv ? beta[(t0 + c0 + tid) * H + h] : 0.f;
     __syncthreads();
-    // ---- within-chunk cumulative log-decay per key channel
+    // ---- within-chunk cumulative log-decay per key channel, its middle and end
     if (tid < D) {
-      float acc = 0.f;
+      float acc = 0.f, mid = 0.f;
       for (int r = 0; r < C; ++r) {
         acc += sm.g[r][tid];
         sm.g[r][tid] = acc;
+        if (r == C / 2 - 1) mid = acc;
       }
-      sm.gC[tid] = acc;
+      sm.gm[tid] = mid;
+      sm.egm[tid] = expf(mid);
+      sm.egc[tid] = expf(acc);
+      sm.egcm[tid] = expf(acc - mid);
     }
     __syncthreads();
-    // ---- A (strictly lower, beta-scaled) and P (lower incl. diagonal)
-    for (int e = tid; e < C * C; e += kThreads) {
-      const int r = e / C, i = e % C;
-      float a = 0.f, p = 0.f;
-      if (i <= r) {
+    // ---- the split decay factors: K o E, Q o E, K o Ei
+    for (int e = tid; e < C * D; e += kThreads) {
+      const int r = e / D, c = e % D;
+      const float x = sm.g[r][c] - sm.gm[c];
+      const float E = expf(fminf(x, kMaxArg)), Ei = expf(fminf(-x, kMaxArg));
+      const float kr = sm.kei[r][c];
+      sm.ke[r][c] = kr * E;
+      sm.qe[r][c] *= E;
+      sm.kei[r][c] = kr * Ei;
+      sm.kd[r][c] = kr * Ei * sm.egcm[c];
+    }
+    __syncthreads();
+    // ---- A (strictly lower, beta-scaled; stored transposed) and P (lower incl.):
+    // thread tile rows r0, r0 + 1 x columns i0, i0 + 1
+    {
+      const int r0 = 2 * (tid >> 4), i0 = 2 * (tid & 15);
+      float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+      float p00 = 0.f, p01 = 0.f, p10 = 0.f, p11 = 0.f;
+      if (i0 <= r0 + 1) {
+#pragma unroll 8
         for (int c = 0; c < D; ++c) {
-          const float ki = sm.k[i][c] * expf(sm.g[r][c] - sm.g[i][c]);
-          a = fmaf(sm.k[r][c], ki, a);
-          p = fmaf(sm.q[r][c], ki, p);
+          const float k0 = sm.ke[r0][c], k1 = sm.ke[r0 + 1][c];
+          const float q0 = sm.qe[r0][c], q1 = sm.qe[r0 + 1][c];
+          const float x0 = sm.kei[i0][c], x1 = sm.kei[i0 + 1][c];
+          a00 = fmaf(k0, x0, a00); a01 = fmaf(k0, x1, a01);
+          a10 = fmaf(k1, x0, a10); a11 = fmaf(k1, x1, a11);
+          p00 = fmaf(q0, x0, p00); p01 = fmaf(q0, x1, p01);
+          p10 = fmaf(q1, x0, p10); p11 = fmaf(q1, x1, p11);
         }
       }
-      sm.A[r][i] = i < r ? sm.beta[r] * a : 0.f;
-      sm.Pm[r][i] = p;
+      const float b0 = sm.beta[r0], b1 = sm.beta[r0 + 1];
+      sm.At[i0][r0] = i0 < r0 ? b0 * a00 : 0.f;
+      sm.At[i0 + 1][r0] = i0 + 1 < r0 ? b0 * a01 : 0.f;
+      sm.At[i0][r0 + 1] = i0 < r0 + 1 ? b1 * a10 : 0.f;
+      sm.At[i0 + 1][r0 + 1] = i0 + 1 < r0 + 1 ? b1 * a11 : 0.f;
+      sm.Pm[r0][i0] = i0 <= r0 ? p00 : 0.f;
+      sm.Pm[r0][i0 + 1] = i0 + 1 <= r0 ? p01 : 0.f;
+      sm.Pm[r0 + 1][i0] = i0 <= r0 + 1 ? p10 : 0.f;
+      sm.Pm[r0 + 1][i0 + 1] = i0 + 1 <= r0 + 1 ? p11 : 0.f;
     }
     __syncthreads();
-    // ---- T = (I + A)^{-1} by forward substitution; lane j owns column j.
-    if (tid < 32) {
-      const int j = tid;
-      float tcol[C];
+    // ---- T = (I + A)^{-1} by column-oriented forward substitution (warp 0,
+    // lane j owns column j: once t[m] is final it is eliminated from every later
+    // row), then T' = T Diag(beta)
+    if (warp == 0) {
+      const int j = lane;
+      float t[C];
 #pragma unroll
-      for (int r = 0; r < C; ++r) {
-        float acc = 0.f;
+      for (int r = 0; r < C; ++r) t[r] = (r == j) ? 1.f : 0.f;
 #pragma unroll
-        for (int m = 0; m < r; ++m) acc = fmaf(sm.A[r][m], tcol[m], acc);
-        tcol[r] = (j == r) ? 1.f : (j < r ? -acc : 0.f);
+      for (int m = 0; m < C - 1; ++m) {
+        const float tm = t[m];
+#pragma unroll
+        for (int r4 = 0; r4 < C / 4; ++r4) {
+          if (4 * r4 + 3 <= m) continue;
+          const float4 a = ld4(&sm.At[m][4 * r4]);
+          const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+          for (int z = 0; z < 4; ++z)
+            if (4 * r4 + z > m) t[4 * r4 + z] = fmaf(-av[z], tm, t[4 * r4 + z]);
+        }
       }
       const float bj = sm.beta[j];
 #pragma unroll
-      for (int r = 0; r < C; ++r) sm.T[r][j] = tcol[r] * bj;
-    }
-    // ---- decay-weighted operands (P already used the raw q, k)
-    for (int e = tid; e < C * D; e += kThreads) {
-      const int r = e / D, c = e % D;
-      const float g = sm.g[r][c];
-      const float kr = sm.k[r][c];
-      sm.kd[r][c] = kr * expf(sm.gC[c] - g);
-      sm.k[r][c] = kr * expf(g);
-      sm.q[r][c] *= expf(g);
+      for (int r = 0; r < C; ++r) sm.Tp[r][j] = t[r] * bj;
     }
     __syncthreads();
-    // ---- W = T' (K o e^g), U = T' V
-    for (int e = tid; e < C * D; e += kThreads) {
-      const int r = e / D, c = e % D;
-      float w = 0.f, u = 0.f;
-      for (int i = 0; i <= r; ++i) {
-        const float t = sm.T[r][i];
-        w = fmaf(t, sm.k[i][c], w);
-        u = fmaf(t, sm.v[i][c], u);
+    // ---- W = T' (K o e^g), U = T' V: thread tile rows r0..r0+3 x key columns k0..k0+3
+    {
+      const int r0 = 4 * warp, k0 = 4 * lane;
+      const float4 em = ld4(&sm.egm[k0]);
+      float4 w[4], u[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) w[a] = u[a] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = 0; i <= r0 + 3; ++i) {
+        float4 kt = ld4(&sm.ke[i][k0]);
+        kt.x *= em.x; kt.y *= em.y; kt.z *= em.z; kt.w *= em.w;
+        const float4 vv = ld4(&sm.v[i][k0]);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const float tp = sm.Tp[r0 + a][i];
+          w[a].x = fmaf(tp, kt.x, w[a].x); w[a].y = fmaf(tp, kt.y, w[a].y);
+          w[a].z = fmaf(tp, kt.z, w[a].z); w[a].w = fmaf(tp, kt.w, w[a].w);
+          u[a].x = fmaf(tp, vv.x, u[a].x); u[a].y = fmaf(tp, vv.y, u[a].y);
+          u[a].z = fmaf(tp, vv.z, u[a].z); u[a].w = fmaf(tp, vv.w, u[a].w);
+        }
       }
-      sm.w[r][c] = w;
-      sm.u[r][c] = u;
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        st4(&sm.w[r0 + a][k0], w[a]);
+        st4(&sm.u[r0 + a][k0], u[a]);
+      }
     }
     __syncthreads();
-    // ---- Delta = U - W S and O_inter = (Q o e^g) S
-    for (int e = tid; e < C * D; e += kThreads) {
-      const int r = e / D, n = e % D;
-      float ws = 0.f, qs = 0.f;
+    // ---- Delta = U - W S and O_inter = (Q o e^g) S: thread tile rows
+    // r0..r0+3 x value columns n0..n0+3; then O = O_inter + P Delta
+    {
+      const int r0 = 4 * warp, n0 = 4 * lane;
+      float4 dl[4], oi[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) dl[a] = oi[a] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
       for (int c = 0; c < D; ++c) {
-        const float s = sm.S[c][n];
-        ws = fmaf(sm.w[r][c], s, ws);
-        qs = fmaf(sm.q[r][c], s, qs);
+        const float4 s4 = ld4(&sm.S[c][n0]);
+        const float em = sm.egm[c];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const float wv = sm.w[r0 + a][c], qv = sm.qe[r0 + a][c] * em;
+          dl[a].x = fmaf(wv, s4.x, dl[a].x); dl[a].y = fmaf(wv, s4.y, dl[a].y);
+          dl[a].z = fmaf(wv, s4.z, dl[a].z); dl[a].w = fmaf(wv, s4.w, dl[a].w);
+          oi[a].x = fmaf(qv, s4.x, oi[a].x); oi[a].y = fmaf(qv, s4.y, oi[a].y);
+          oi[a].z = fmaf(qv, s4.z, oi[a].z); oi[a].w = fmaf(qv, s4.w, oi[a].w);
+        }
       }
-      sm.u[r][n] -= ws;
-      sm.g[r][n] = qs;
-    }
-    __syncthreads();
-    // ---- O = O_inter + P Delta (valid rows only)
-    for (int e = tid; e < C * D; e += kThreads) {
-      const int r = e / D, n = e % D;
-      if (r < nv) {
-        float o = sm.g[r][n];
-        for (int i = 0; i <= r; ++i) o = fmaf(sm.Pm[r][i], sm.u[i][n], o);
-        out[((t0 + c0 + r) * H + h) * D + n] = o;
+      __syncthreads();  // every thread has read W and U's rows it needs
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        float4 uu = ld4(&sm.u[r0 + a][n0]);
+        uu.x -= dl[a].x; uu.y -= dl[a].y; uu.z -= dl[a].z; uu.w -= dl[a].w;
+        st4(&sm.u[r0 + a][n0], uu);
       }
+      __syncthreads();  // Delta complete
+      for (int i = 0; i <= r0 + 3; ++i) {
+        const float4 d4 = ld4(&sm.u[i][n0]);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const float pv = sm.Pm[r0 + a][i];
+          oi[a].x = fmaf(pv, d4.x, oi[a].x); oi[a].y = fmaf(pv, d4.y, oi[a].y);
+          oi[a].z = fmaf(pv, d4.z, oi[a].z); oi[a].w = fmaf(pv, d4.w, oi[a].w);
+        }
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+        if (r0 + a < nv) st4(out + ((t0 + c0 + r0 + a) * H + h) * D + n0, oi[a]);
     }
-    // ---- S <- Diag(e^{g_C}) S + Kdec^T Delta
-    for (int e = tid; e < D * D; e += kThreads) {
-      const int c = e / D, n = e % D;
-      float s = sm.S[c][n] * expf(sm.gC[c]);
-      for (int i = 0; i < C; ++i) s = fmaf(sm.kd[i][c], sm.u[i][n], s);
-      sm.S[c][n] = s;
+    // ---- S <- Diag(e^{g_C}) S + Kdec^T Delta: thread tile key rows
+    // k0..k0+15 x value columns n0..n0+3
+    {
+      const int k0 = 16 * warp, n0 = 4 * lane;
+      float4 acc[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float4 s4 = ld4(&sm.S[k0 + j][n0]);
+        const float gc = sm.egc[k0 + j];
+        acc[j] = make_float4(s4.x * gc, s4.y * gc, s4.z * gc, s4.w * gc);
+      }
+      for (int i = 0; i < C; ++i) {
+        const float4 d4 = ld4(&sm.u[i][n0]);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float kd = sm.kd[i][k0 + j];
+          acc[j].x = fmaf(kd, d4.x, acc[j].x); acc[j].y = fmaf(kd, d4.y, acc[j].y);
+          acc[j].z = fmaf(kd, d4.z, acc[j].z); acc[j].w = fmaf(kd, d4.w, acc[j].w);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) st4(&sm.S[k0 + j][n0], acc[j]);
     }
     __syncthreads();
   }
