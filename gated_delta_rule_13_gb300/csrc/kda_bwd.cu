@@ -12,12 +12,16 @@
 //   dlog_alpha = rowsum(dX o X);  dS_{t-1} = Diag(alpha) dX.
 //
 // Work split.  The columns of S (value channels) evolve independently, so a
-// chain is cut into four blocks of 32 value columns, one CTA each (8 warps:
-// lane = value column, warp w = key rows 16w .. 16w + 15, 16 state values per
-// thread).  dv and the initial-state gradient belong to one block; dq, dk,
-// dlog_alpha and dbeta are sums over all value columns, reduced inside the
-// warp (a transposing butterfly) and added across the four blocks with fp32
-// atomics (so their last bits depend on the order of those four additions).
+// chain is cut into four blocks of 32 value columns, one CTA each (8 warps).
+// Lane l of warp w holds value columns 2 (l mod 16) and 2 (l mod 16) + 1 of key
+// rows 16 w + 8 floor(l / 16) .. + 7: 16 state values per thread.  Column sums
+// over the 128 key rows are in-thread over 8 rows, one shuffle between the
+// half-warps and a shared-memory sum over the warps; row sums over the 32
+// columns are in-thread over a column pair and a transposing butterfly over the
+// 16 lanes of a half-warp.  dv and the initial-state gradient belong to one
+// block; dq, dk, dlog_alpha and dbeta are sums over all value columns, added
+// across the four blocks with fp32 atomics (so their last bits depend on the
+// order of those four additions).
 //
 // States.  A forward pass stores the state before every `every`-th token (a
 // power of two >= kGroup, chosen by the caller of launch_chunk_bwd); the
@@ -40,7 +44,7 @@ constexpr int D = kHeadDim;       // 128
 constexpr int kCols = 32;         // value columns per CTA
 constexpr int kBlocks = D / kCols;
 constexpr int kThreads = 256;
-constexpr int kRows = 16;         // key rows per thread
+constexpr int kRows = 8;          // key rows per thread (two value columns each)
 constexpr int kGroup = 4;         // tokens whose X a CTA keeps at a time
 
 // Checkpoint slot of sequence s: floor(cu[s] / every) + s.  Consecutive
@@ -178,65 +182,71 @@ __device__ void convert_tokens(Stage &st, const uint8_t *raw, int n, bool with_q
 // thread passes once it has read it, so one barrier per use suffices.
 using Red = float[2][kThreads / 32][kCols];
 
-// One forward token on this thread's 16 state values (rows r0 + j, column
-// lane); the decayed state X and the per-column p, d are returned.
-__device__ __forceinline__ void fwd_token(float (&s)[kRows], float (&x)[kRows], float &p, float &d,
-                                          const Stage &st, int i, int r0, int lane, int warp,
-                                          Red &red, uint32_t &rp) {
-  float part = 0.f;
+// One forward token on this thread's 16 state values (rows r0 + j, value
+// columns ca, ca + 1 of the block); the decayed state X and the per-column p, d
+// of those two columns are returned.
+__device__ __forceinline__ void fwd_token(float (&s)[kRows][2], float (&x)[kRows][2], float2 &p,
+                                          float2 &d, const Stage &st, int i, int r0, int ca,
+                                          int lane, int warp, Red &red, uint32_t &rp) {
+  float pa = 0.f, pb = 0.f;
 #pragma unroll
   for (int j = 0; j < kRows; ++j) {
-    x[j] = st.alpha[i][r0 + j] * s[j];
-    part = fmaf(x[j], st.k[i][r0 + j], part);
+    const float al = st.alpha[i][r0 + j], kr = st.k[i][r0 + j];
+    x[j][0] = al * s[j][0];
+    x[j][1] = al * s[j][1];
+    pa = fmaf(x[j][0], kr, pa);
+    pb = fmaf(x[j][1], kr, pb);
   }
+  pa += __shfl_xor_sync(0xffffffffu, pa, 16);  // the other 8 rows of this warp's 16
+  pb += __shfl_xor_sync(0xffffffffu, pb, 16);
   float (&rb)[kThreads / 32][kCols] = red[rp++ & 1u];
-  rb[warp][lane] = part;
+  if (lane < 16) *reinterpret_cast<float2 *>(&rb[warp][ca]) = make_float2(pa, pb);
   __syncthreads();
-  p = 0.f;
+  p = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int w = 0; w < kThreads / 32; ++w) p += rb[w][lane];
-  d = st.beta[i] * (st.v[i][lane] - p);
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const float2 v2 = *reinterpret_cast<const float2 *>(&rb[w][ca]);
+    p.x += v2.x;
+    p.y += v2.y;
+  }
+  d = make_float2(st.beta[i] * (st.v[i][ca] - p.x), st.beta[i] * (st.v[i][ca + 1] - p.y));
 #pragma unroll
-  for (int j = 0; j < kRows; ++j) s[j] = fmaf(st.k[i][r0 + j], d, x[j]);
+  for (int j = 0; j < kRows; ++j) {
+    const float kr = st.k[i][r0 + j];
+    s[j][0] = fmaf(kr, d.x, x[j][0]);
+    s[j][1] = fmaf(kr, d.y, x[j][1]);
+  }
 }
 
-// Sum of v[j] over the 32 lanes, for each of the 16 rows j: after four
-// halving exchanges lane L holds one row, row_of(L), summed over 16 lanes,
-// and the last exchange completes it (lanes 2m and 2m + 1 hold the same row).
-__device__ __forceinline__ float row_sum(float (&v)[kRows], int lane) {
-  float a[8];
-  {
-    const bool hi = lane & 16;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float mine = hi ? v[8 + j] : v[j], give = hi ? v[j] : v[8 + j];
-      a[j] = mine + __shfl_xor_sync(0xffffffffu, give, 16);
-    }
-  }
-  float b[4];
+// Sum of v[j] over the 16 lanes of a half-warp, for each of the 8 rows j:
+// after three halving exchanges lane L holds one row, row_of(L), summed over 8
+// lanes, and the last exchange completes it (lanes 2m and 2m + 1 hold the same
+// row).  The exchanges stay inside each half-warp.
+__device__ __forceinline__ float row_sum(const float (&v)[kRows], int lane) {
+  float a[4];
   {
     const bool hi = lane & 8;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float mine = hi ? a[4 + j] : a[j], give = hi ? a[j] : a[4 + j];
-      b[j] = mine + __shfl_xor_sync(0xffffffffu, give, 8);
+      const float mine = hi ? v[4 + j] : v[j], give = hi ? v[j] : v[4 + j];
+      a[j] = mine + __shfl_xor_sync(0xffffffffu, give, 8);
     }
   }
-  float c[2];
+  float b[2];
   {
     const bool hi = lane & 4;
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const float mine = hi ? b[2 + j] : b[j], give = hi ? b[j] : b[2 + j];
-      c[j] = mine + __shfl_xor_sync(0xffffffffu, give, 4);
+      const float mine = hi ? a[2 + j] : a[j], give = hi ? a[j] : a[2 + j];
+      b[j] = mine + __shfl_xor_sync(0xffffffffu, give, 4);
     }
   }
   const bool hi = lane & 2;
-  float e = (hi ? c[1] : c[0]) + __shfl_xor_sync(0xffffffffu, hi ? c[0] : c[1], 2);
+  const float e = (hi ? b[1] : b[0]) + __shfl_xor_sync(0xffffffffu, hi ? b[0] : b[1], 2);
   return e + __shfl_xor_sync(0xffffffffu, e, 1);
 }
 __device__ __forceinline__ int row_of(int lane) {
-  return 8 * ((lane >> 4) & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) + ((lane >> 1) & 1);
+  return 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) + ((lane >> 1) & 1);
 }
 
 struct Chain {
@@ -275,12 +285,15 @@ kda_bwd_ckpt_kernel(const void *__restrict__ k, const void *__restrict__ v,
     if (threadIdx.x == 0) atomicCAS(&status->code, 0, 1 /* KDA_ERR_INVALID_ARG */);
     return;
   }
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, r0 = kRows * warp;
-  const int col = c.cb * kCols + lane;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ca = 2 * (lane & 15), r0 = 16 * warp + kRows * (lane >> 4);
+  const int col = c.cb * kCols + ca;
   const int64_t sbase = ((int64_t)c.seq * H + c.h) * D * D;
-  float s[kRows], x[kRows];
+  float s[kRows][2], x[kRows][2];
 #pragma unroll
-  for (int j = 0; j < kRows; ++j) s[j] = init_state ? init_state[sbase + (r0 + j) * D + col] : 0.f;
+  for (int j = 0; j < kRows; ++j)
+#pragma unroll
+    for (int z = 0; z < 2; ++z) s[j][z] = init_state ? init_state[sbase + (r0 + j) * D + col + z] : 0.f;
   const int64_t base = ckpt_base(c.t0, c.seq, every);
   // the inputs of each group are copied while the group before it runs
   auto group_len = [&](int64_t tb) { return (int)(c.t1 - tb < kGroup ? c.t1 - tb : kGroup); };
@@ -303,10 +316,11 @@ kda_bwd_ckpt_kernel(const void *__restrict__ k, const void *__restrict__ v,
       if ((t - c.t0) % every == 0) {
         float *dst = ckpt + ((base + (t - c.t0) / every) * H + c.h) * D * D;
 #pragma unroll
-        for (int j = 0; j < kRows; ++j) dst[(r0 + j) * D + col] = s[j];
+        for (int j = 0; j < kRows; ++j)
+          *reinterpret_cast<float2 *>(dst + (r0 + j) * D + col) = make_float2(s[j][0], s[j][1]);
       }
-      float p, d;
-      fwd_token(s, x, p, d, st, i, r0, lane, warp, red, rp);
+      float2 p, d;
+      fwd_token(s, x, p, d, st, i, r0, ca, lane, warp, red, rp);
     }
   }
 }
@@ -330,12 +344,15 @@ kda_bwd_kernel(const void *__restrict__ q, const void *__restrict__ k, const voi
   __shared__ __align__(16) uint8_t raw[kRawBytes];
   const Chain c = chain_of(cu, n_seqs, n_tokens, H);
   if (!c.ok) return;  // recorded by the forward pass
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, r0 = kRows * warp;
-  const int col = c.cb * kCols + lane;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ca = 2 * (lane & 15), r0 = 16 * warp + kRows * (lane >> 4);
+  const int col = c.cb * kCols + ca;
   const int64_t sbase = ((int64_t)c.seq * H + c.h) * D * D;
-  float ds[kRows];
+  float ds[kRows][2];
 #pragma unroll
-  for (int j = 0; j < kRows; ++j) ds[j] = d_final ? d_final[sbase + (r0 + j) * D + col] : 0.f;
+  for (int j = 0; j < kRows; ++j)
+#pragma unroll
+    for (int z = 0; z < 2; ++z) ds[j][z] = d_final ? d_final[sbase + (r0 + j) * D + col + z] : 0.f;
   const int64_t base = ckpt_base(c.t0, c.seq, every);
   const int64_t len = c.t1 - c.t0;
   const int64_t n_ck = (len + every - 1) / every;
@@ -373,9 +390,13 @@ kda_bwd_kernel(const void *__restrict__ q, const void *__restrict__ k, const voi
       // the item's copies have landed: the state before token a, the group's inputs
       cp_async_wait_all();
       __syncthreads();
-      float s[kRows], x[kRows];
+      float s[kRows][2], x[kRows][2];
 #pragma unroll
-      for (int j = 0; j < kRows; ++j) s[j] = ckbuf[r0 + j][lane];
+      for (int j = 0; j < kRows; ++j) {
+        const float2 v2 = *reinterpret_cast<const float2 *>(&ckbuf[r0 + j][ca]);
+        s[j][0] = v2.x;
+        s[j][1] = v2.y;
+      }
       convert_tokens<BF16>(st, raw, n, true, nbeta);
       __syncthreads();  // ckbuf and raw are free; st is ready
       if (g > 0) prefetch(blk, g - 1);
@@ -386,19 +407,20 @@ kda_bwd_kernel(const void *__restrict__ q, const void *__restrict__ k, const voi
         stage_tokens<BF16>(st_rec, tb, kGroup, c.h, H, c.cb, nullptr, k, v, la, beta, nullptr);
         __syncthreads();
         for (int i = 0; i < kGroup; ++i) {
-          float p, d;
-          fwd_token(s, x, p, d, st_rec, i, r0, lane, warp, red, rp);
+          float2 p, d;
+          fwd_token(s, x, p, d, st_rec, i, r0, ca, lane, warp, red, rp);
         }
       }
       // the group's tokens: X, p and d kept
       for (int i = 0; i < n; ++i) {
-        float p, d;
-        fwd_token(s, x, p, d, st, i, r0, lane, warp, red, rp);
+        float2 p, d;
+        fwd_token(s, x, p, d, st, i, r0, ca, lane, warp, red, rp);
 #pragma unroll
-        for (int j = 0; j < kRows; ++j) xs[(i * D + r0 + j) * kCols + lane] = x[j];
-        if (warp == 0) {
-          s_p[i][lane] = p;
-          s_d[i][lane] = d;
+        for (int j = 0; j < kRows; ++j)
+          *reinterpret_cast<float2 *>(&xs[(i * D + r0 + j) * kCols + ca]) = make_float2(x[j][0], x[j][1]);
+        if (warp == 0 && lane < 16) {
+          *reinterpret_cast<float2 *>(&s_p[i][ca]) = p;
+          *reinterpret_cast<float2 *>(&s_d[i][ca]) = d;
         }
       }
       __syncthreads();
@@ -406,46 +428,65 @@ kda_bwd_kernel(const void *__restrict__ q, const void *__restrict__ k, const voi
       for (int i = n - 1; i >= 0; --i) {
         const int64_t t = gb + i;
         const int64_t trow = (t * H + c.h) * D;
-        const float p = s_p[i][lane], d = s_d[i][lane], b = st.beta[i];
-        const float dov = st.dout[i][lane];
-        float cq[kRows], ck[kRows], cl[kRows];
-        float part = 0.f;
+        const float2 p = *reinterpret_cast<const float2 *>(&s_p[i][ca]);
+        const float2 d = *reinterpret_cast<const float2 *>(&s_d[i][ca]);
+        const float b = st.beta[i];
+        const float2 dov = make_float2(st.dout[i][ca], st.dout[i][ca + 1]);
+        float cq[kRows], ck[kRows], cl[kRows], xa[kRows], xb[kRows];
+        float pa = 0.f, pb = 0.f;
 #pragma unroll
         for (int j = 0; j < kRows; ++j) {
           const int r = r0 + j;
-          const float xv = xs[(i * D + r) * kCols + lane];
-          const float kr = st.k[i][r];
-          cq[j] = fmaf(kr, d, xv) * dov;                // S_t do (row sums: dq)
-          ds[j] = fmaf(st.q[i][r], dov, ds[j]);          // dS += q do^T
-          part = fmaf(ds[j], kr, part);                  // dd = dS^T k (column sums)
-          cl[j] = xv;                                    // X, kept for the next pass
+          const float2 xv = *reinterpret_cast<const float2 *>(&xs[(i * D + r) * kCols + ca]);
+          const float kr = st.k[i][r], qr = st.q[i][r];
+          // S_t do (row sums: dq), over this thread's two columns
+          cq[j] = fmaf(fmaf(kr, d.x, xv.x), dov.x, fmaf(kr, d.y, xv.y) * dov.y);
+          ds[j][0] = fmaf(qr, dov.x, ds[j][0]);          // dS += q do^T
+          ds[j][1] = fmaf(qr, dov.y, ds[j][1]);
+          pa = fmaf(ds[j][0], kr, pa);                   // dd = dS^T k (column sums)
+          pb = fmaf(ds[j][1], kr, pb);
+          xa[j] = xv.x;                                  // X, kept for the next pass
+          xb[j] = xv.y;
         }
+        pa += __shfl_xor_sync(0xffffffffu, pa, 16);
+        pb += __shfl_xor_sync(0xffffffffu, pb, 16);
         float (&rb)[kThreads / 32][kCols] = red[rp++ & 1u];
-        rb[warp][lane] = part;
+        if (lane < 16) *reinterpret_cast<float2 *>(&rb[warp][ca]) = make_float2(pa, pb);
         __syncthreads();
-        float dd = 0.f;
+        float2 dd = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) dd += rb[w][lane];
-        const float dp = -b * dd;
+        for (int w = 0; w < kThreads / 32; ++w) {
+          const float2 v2 = *reinterpret_cast<const float2 *>(&rb[w][ca]);
+          dd.x += v2.x;
+          dd.y += v2.y;
+        }
+        const float2 dp = make_float2(-b * dd.x, -b * dd.y);
         if (warp == 0) {
-          const float dvv = b * dd;
-          if constexpr (BF16)
-            static_cast<__nv_bfloat16 *>(dv_out)[trow + col] = __float2bfloat16_rn(dvv);
-          else
-            static_cast<float *>(dv_out)[trow + col] = dvv;
-          float db = dd * (st.v[i][lane] - p);
+          if (lane < 16) {
+            if constexpr (BF16) {  // (dv is only element-aligned: two scalar stores)
+              static_cast<__nv_bfloat16 *>(dv_out)[trow + col] = __float2bfloat16_rn(b * dd.x);
+              static_cast<__nv_bfloat16 *>(dv_out)[trow + col + 1] = __float2bfloat16_rn(b * dd.y);
+            } else {
+              static_cast<float *>(dv_out)[trow + col] = b * dd.x;
+              static_cast<float *>(dv_out)[trow + col + 1] = b * dd.y;
+            }
+          }
+          // (both half-warps hold the same column pairs: sum within one half)
+          float db = dd.x * (st.v[i][ca] - p.x) + dd.y * (st.v[i][ca + 1] - p.y);
 #pragma unroll
-          for (int off = 16; off > 0; off >>= 1) db += __shfl_xor_sync(0xffffffffu, db, off);
+          for (int off = 8; off > 0; off >>= 1) db += __shfl_xor_sync(0xffffffffu, db, off);
           if (lane == 0) atomicAdd(dbeta + t * H + c.h, db);
         }
 #pragma unroll
         for (int j = 0; j < kRows; ++j) {
           const int r = r0 + j;
-          const float xv = cl[j];
-          const float dx = fmaf(st.k[i][r], dp, ds[j]);  // dX = dS + k dp^T
-          ck[j] = fmaf(ds[j], d, xv * dp);               // dk: dS d + X dp
-          cl[j] = dx * xv;                               // dlog_alpha: dX o X
-          ds[j] = st.alpha[i][r] * dx;                   // dS_{t-1} = Diag(alpha) dX
+          const float kr = st.k[i][r], al = st.alpha[i][r];
+          const float dx0 = fmaf(kr, dp.x, ds[j][0]);     // dX = dS + k dp^T
+          const float dx1 = fmaf(kr, dp.y, ds[j][1]);
+          ck[j] = fmaf(ds[j][0], d.x, fmaf(xa[j], dp.x, fmaf(ds[j][1], d.y, xb[j] * dp.y)));  // dk: dS d + X dp
+          cl[j] = fmaf(dx0, xa[j], dx1 * xb[j]);          // dlog_alpha: dX o X
+          ds[j][0] = al * dx0;                             // dS_{t-1} = Diag(alpha) dX
+          ds[j][1] = al * dx1;
         }
         const float sq = row_sum(cq, lane), sk = row_sum(ck, lane), sl = row_sum(cl, lane);
         if ((lane & 1) == 0) {
@@ -459,7 +500,9 @@ kda_bwd_kernel(const void *__restrict__ q, const void *__restrict__ k, const voi
   }
   if (d_init) {
 #pragma unroll
-    for (int j = 0; j < kRows; ++j) d_init[sbase + (r0 + j) * D + col] = ds[j];
+    for (int j = 0; j < kRows; ++j)
+#pragma unroll
+      for (int z = 0; z < 2; ++z) d_init[sbase + (r0 + j) * D + col + z] = ds[j][z];
   }
 }
 
