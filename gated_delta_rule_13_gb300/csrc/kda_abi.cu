@@ -118,28 +118,45 @@ bool is_device_pointer(const void *p, bool *ok) {
   return attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged;
 }
 
+// The backward pass's schedule: its checkpoint interval and which pass runs.
+// The caller's interval (a power of two in [4, kda::kMaxCkptEvery]) selects the
+// token-loop pass with that interval.  0 leaves the choice to the library: for
+// bf16 the chunked tensor-core pass (states every kda::kBwdChunk tokens) when
+// those states fit kda::kCkptBudgetBytes, else, and for fp32, the token-loop
+// pass with kda::bwd_ckpt_every's interval.  every < 0: invalid.
+struct BwdPlan {
+  int32_t every;
+  bool chunked;
+};
+BwdPlan bwd_plan(int32_t want, int32_t n_seqs, int64_t n_tokens, int32_t H, int dtype) {
+  if (want != 0) {
+    if (want < 4 || want > kda::kMaxCkptEvery || (want & (want - 1)) != 0) return {-1, false};
+    return {want, false};
+  }
+  if (dtype == KDA_BF16 &&
+      kda::bwd_ckpt_slots(n_seqs, n_tokens, kda::kBwdChunk) * (size_t)H * kHeadDim * kHeadDim *
+              sizeof(float) <= kda::kCkptBudgetBytes)
+    return {kda::kBwdChunk, true};
+  return {kda::bwd_ckpt_every(n_seqs, n_tokens, H), false};
+}
+
 // Backward-pass workspace: status block, device copy of a host cu_seqlens, the
-// state checkpoints, and the fp32 accumulators of dq and dk.
+// state checkpoints, and (token-loop pass only) the fp32 accumulators of dq
+// and dk.
 struct BwdLayout {
   size_t cu, ckpt, dq, dk, total;
 };
-BwdLayout bwd_layout(int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t every) {
+BwdLayout bwd_layout(int32_t n_seqs, int64_t n_tokens, int32_t H, BwdPlan plan) {
   BwdLayout l;
   l.cu = kStatusBytes;
   l.ckpt = l.cu + round_up(sizeof(int32_t) * ((size_t)n_seqs + 1), 256);
-  l.dq = l.ckpt +
-         round_up(kda::bwd_ckpt_slots(n_seqs, n_tokens, every) * H * kHeadDim * kHeadDim * 4, 256);
-  l.dk = l.dq + round_up((size_t)n_tokens * H * kHeadDim * 4, 256);
-  l.total = l.dk + round_up((size_t)n_tokens * H * kHeadDim * 4, 256);
+  l.dq = l.ckpt + round_up(kda::bwd_ckpt_slots(n_seqs, n_tokens, plan.every) * H * kHeadDim *
+                               kHeadDim * 4,
+                           256);
+  const size_t acc = plan.chunked ? 0 : round_up((size_t)n_tokens * H * kHeadDim * 4, 256);
+  l.dk = l.dq + acc;
+  l.total = l.dk + acc;
   return l;
-}
-
-// The backward pass's checkpoint interval: the caller's (a power of two in
-// [4, kda::kMaxCkptEvery]) or, for 0, the library's choice; -1 if invalid.
-int32_t resolve_ckpt_every(int32_t want, int32_t n_seqs, int64_t n_tokens, int32_t H) {
-  if (want == 0) return kda::bwd_ckpt_every(n_seqs, n_tokens, H);
-  if (want < 4 || want > kda::kMaxCkptEvery || (want & (want - 1)) != 0) return -1;
-  return want;
 }
 
 }  // namespace
@@ -151,9 +168,9 @@ int kda_chunk_bwd_workspace_size_sched(int32_t n_seqs, int64_t n_tokens, int32_t
   if (!bytes || n_seqs < 0 || n_tokens < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
   const int d = check_dims(dk, dv, dtype);
   if (d != KDA_OK) return d;
-  const int32_t every = resolve_ckpt_every(ckpt_every, n_seqs, n_tokens, H);
-  if (every < 0) return KDA_ERR_INVALID_ARG;
-  *bytes = bwd_layout(n_seqs, n_tokens, H, every).total;
+  const BwdPlan plan = bwd_plan(ckpt_every, n_seqs, n_tokens, H, dtype);
+  if (plan.every < 0) return KDA_ERR_INVALID_ARG;
+  *bytes = bwd_layout(n_seqs, n_tokens, H, plan).total;
   return KDA_OK;
 }
 
@@ -172,8 +189,8 @@ int kda_chunk_bwd_sched(const void *q, const void *k, const void *v, const float
   if (n_seqs < 0 || n_tokens < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
   const int d = check_dims(dk, dv, dtype);
   if (d != KDA_OK) return d;
-  const int32_t every = resolve_ckpt_every(ckpt_every, n_seqs, n_tokens, H);
-  if (every < 0) return KDA_ERR_INVALID_ARG;
+  const BwdPlan plan = bwd_plan(ckpt_every, n_seqs, n_tokens, H, dtype);
+  if (plan.every < 0) return KDA_ERR_INVALID_ARG;
   if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
   if (n_tokens > 0 && (!q || !k || !v || !log_alpha || !beta || !d_out || !dq || !dk_ || !dv_ ||
                        !d_log_alpha || !d_beta))
@@ -207,7 +224,7 @@ int kda_chunk_bwd_sched(const void *q, const void *k, const void *v, const float
       if (outs[j] && out_b[j] > 0 && ranges_overlap(outs[i], out_b[i], outs[j], out_b[j]))
         return KDA_ERR_INVALID_ARG;
   }
-  const BwdLayout lay = bwd_layout(n_seqs, n_tokens, H, every);
+  const BwdLayout lay = bwd_layout(n_seqs, n_tokens, H, plan);
   if (!workspace || workspace_bytes < lay.total || !aligned16(workspace)) return KDA_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   unsigned char *ws = static_cast<unsigned char *>(workspace);
@@ -228,10 +245,13 @@ int kda_chunk_bwd_sched(const void *q, const void *k, const void *v, const float
     cu_dev = dst;
   }
   kda::DeviceStatus *status = reinterpret_cast<kda::DeviceStatus *>(ws);
+  // the token-loop pass adds into its accumulators and into d_log_alpha and
+  // d_beta; the chunked pass writes every element once
   const bool ok = cudaMemsetAsync(status, 0, sizeof(kda::DeviceStatus), st) == cudaSuccess &&
-                  (nt == 0 || (cudaMemsetAsync(ws + lay.dq, 0, lay.total - lay.dq, st) == cudaSuccess &&
-                               cudaMemsetAsync(d_log_alpha, 0, nt * dk * 4, st) == cudaSuccess &&
-                               cudaMemsetAsync(d_beta, 0, nt * 4, st) == cudaSuccess));
+                  (nt == 0 || plan.chunked ||
+                   (cudaMemsetAsync(ws + lay.dq, 0, lay.total - lay.dq, st) == cudaSuccess &&
+                    cudaMemsetAsync(d_log_alpha, 0, nt * dk * 4, st) == cudaSuccess &&
+                    cudaMemsetAsync(d_beta, 0, nt * 4, st) == cudaSuccess));
   if (!ok) {
     cudaGetLastError();
     return KDA_ERR_CUDA;
@@ -244,7 +264,8 @@ int kda_chunk_bwd_sched(const void *q, const void *k, const void *v, const float
   a.d_out = d_out; a.d_final = d_final_state;
   a.dq = dq; a.dk = dk_; a.dv = dv_; a.d_log_alpha = d_log_alpha; a.d_beta = d_beta;
   a.d_init = d_init_state;
-  a.ckpt_every = every;
+  a.ckpt_every = plan.every;
+  a.chunked = plan.chunked;
   a.ckpt = reinterpret_cast<float *>(ws + lay.ckpt);
   a.dq_acc = reinterpret_cast<float *>(ws + lay.dq);
   a.dk_acc = reinterpret_cast<float *>(ws + lay.dk);

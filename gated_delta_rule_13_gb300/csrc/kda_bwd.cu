@@ -47,11 +47,8 @@ constexpr int kThreads = 256;
 constexpr int kRows = 8;          // key rows per thread (two value columns each)
 constexpr int kGroup = 4;         // tokens whose X a CTA keeps at a time
 
-// Checkpoint slot of sequence s: floor(cu[s] / every) + s.  Consecutive
-// sequences never share slots, since floor(b / c) - floor(a / c) + 1 >=
-// ceil((b - a) / c).
 __device__ __forceinline__ int64_t ckpt_base(int64_t cu_s, int64_t s, int every) {
-  return cu_s / every + s;
+  return bwd_ckpt_slot_base(cu_s, s, every);
 }
 
 template <bool BF16>
@@ -545,6 +542,10 @@ cudaError_t launch_chunk_bwd(const BwdArgs &a, cudaStream_t stream) {
   if (a.ckpt_every < kGroup || a.ckpt_every > kMaxCkptEvery ||
       (a.ckpt_every & (a.ckpt_every - 1)) != 0)
     return cudaErrorInvalidValue;
+  if (a.chunked) {
+    if (!a.bf16 || a.ckpt_every != kBwdChunk) return cudaErrorInvalidValue;
+    return launch_bwd_chunk(a, stream);  // its own checkpoint pass, then the chunks
+  }
   const unsigned grid = (unsigned)(chains * kBlocks);
   const size_t xs_bytes = (size_t)kGroup * D * kCols * sizeof(float);
   auto bwd = a.bf16 ? kda_bwd_kernel<true> : kda_bwd_kernel<false>;

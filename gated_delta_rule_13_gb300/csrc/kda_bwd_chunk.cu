@@ -1,0 +1,901 @@
+// Chunked backward pass of the KDA recurrence for bf16 inputs: 16-token chunks,
+// every product on the tensor cores (warp-level bf16 MMAs, fp32 accumulation).
+//
+// The pages give no gradient ("Kimi K3: 架构、训练与系统全景解析", section 7.1:
+// the chunked KDA kernel serves training as well as prefill).  This is the
+// chain rule through the chunk form of the update and read-out ("Kimi K3" study
+// notes, section 3-2 "2) Kimi Delta Attention"; 全景解析 sections 4.2.4-4.2.5 for
+// the chunk form).  Per chunk of n <= 16 tokens (rows r, i), padded to 16 with
+// k = q = v = dO = 0, log_alpha = 0, beta = 0, with g_r the cumulative
+// log_alpha through row r, the middle row m = 7 as the decay reference and
+// l = 15 the last row (padding leaves g_l = g_{n-1}):
+//   Kt = K e^{g - g_m}, Qt = Q e^{g - g_m}, Kh = K e^{g_m - g}, Kd = K e^{g_l - g}
+//   Ks = K e^{g}, Qs = Q e^{g}            (each factor within e^{+-40} or <= 1)
+//   G = Kt Kh^T, A = tril(Diag(beta) G, -1), P = tril(Qt Kh^T), T = (I + A)^{-1}
+//   R = V - Ks S, U = Diag(beta) R, delta = T U
+//   S' = Diag(e^{g_l}) S + Kd^T delta,   O = Qs S + P delta
+// and in reverse, from dS' (the gradient of S') and dO:
+//   d delta = P^T dO + Kd dS',  dU = T^T d delta,  dR = Diag(beta) dU = dv
+//   dA = tril(-dU delta^T, -1),  dP = tril(dO delta^T),  dG = Diag(beta) dA
+//   dbeta = rowsum(R o dU) + rowsum(dA o G)
+//   dKt = -e^{g_m} o (dR S^T) + dG Kh,   dQt = e^{g_m} o (dO S^T) + dP Kh
+//   dKh = dG^T Kt + dP^T Qt,   dKd = delta dS'^T
+//   X = Qs^T dO - Ks^T dR,   dS = Diag(e^{g_l}) dS' + X
+//   dq = dQt e^{g - g_m},  dk = dKt e^{g - g_m} + dKh e^{g_m - g} + dKd e^{g_l - g}
+//   dg = dKt o Kt + dQt o Qt - dKh o Kh - dKd o Kd,  then at row m
+//        - colsum(dKt o Kt + dQt o Qt) + colsum(dKh o Kh) + rowsum_v(S o X)
+//   and at row l  colsum(dKd o Kd) + e^{g_l} rowsum_v(S o dS'),
+//   dlog_alpha_j = sum_{r >= j} dg_r (within the chunk).
+// (Written out from the token form by hand and checked in fp64 against the
+// gradient oracle on ragged lengths.)
+//
+// Work split: one CTA of 8 warps per (sequence, head) chain, walking its
+// chunks from the last.  dS lives in registers as MMA accumulators (warp w:
+// key rows 16 w .. 16 w + 15, all 128 value columns); the chunk's operands are
+// bf16 tiles in shared memory, read by ldmatrix.  Products with 128 output
+// columns give warp w the columns 16 w .. 16 w + 15; the 16 x 16 products (G,
+// P, dA, dP) and T = (I + A)^{-1} (forward substitution) run on warps 0-1.
+// The state at every chunk start comes from the checkpoint pass (states every
+// 16 tokens).  Every gradient element is written once: no atomics, results
+// independent of scheduling.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda_internal.h"
+#include "kda_sm100.cuh"
+
+namespace kda {
+namespace {
+
+using namespace sm100;
+
+constexpr int D = kHeadDim;  // 128
+constexpr int CB = kBwdChunk;  // 16 tokens per chunk
+constexpr int kMid = 7;      // reference row of the decay factors
+constexpr int kLast = CB - 1;
+constexpr int kThreads = 256;
+constexpr int TP = D + 8;    // bf16 pitch of 128-wide tiles: 272 B, ldmatrix conflict free
+constexpr int SP = CB + 8;   // bf16 pitch of 16-wide tiles: 48 B
+constexpr int GP = CB + 1;   // fp32 pitch of the 16 x 16 matrices
+
+struct __align__(16) Smem {
+  __nv_bfloat16 S[D][TP];     // checkpointed state at the chunk start, bf16
+  __nv_bfloat16 dSn[D][TP];   // dS' (gradient of the chunk-end state), bf16
+  __nv_bfloat16 dSlo[D][TP];  // dS' - dSn, bf16: the pair carries dS' to ~2^-16
+  __nv_bfloat16 q[CB][TP], k[CB][TP], v[CB][TP], dout[CB][TP];  // raw inputs
+  __nv_bfloat16 kt[CB][TP], qt[CB][TP], kh[CB][TP], kd[CB][TP], ks[CB][TP], qs[CB][TP];
+  __nv_bfloat16 u[CB][TP], dl[CB][TP], ddl[CB][TP], du[CB][TP], ndr[CB][TP];
+  __nv_bfloat16 tm[CB][SP], pm[CB][SP], dgm[CB][SP], dpm[CB][SP];
+  float la[CB][D];            // log_alpha rows
+  float et[CB][D];            // e^{g_r - g_m}
+  float dgr[CB][D];           // dg_r
+  float G[CB][GP];
+  float em[D], gam[D], t1[D], t2[D];
+  float beta[CB];
+  float dbp[8][CB];           // row sums of R o dU per warp
+  float dba[CB];              // row sums of dA o G
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t a, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+
+// Fragment loads of the m16n8k16 operands from bf16 tiles (pitch in elements).
+// A (16 x 16 at m0, k0) from a tile stored [m][k] ...
+__device__ __forceinline__ void lda(const __nv_bfloat16 *tile, int pitch, int m0, int k0, int lane,
+                                    uint32_t (&a)[4]) {
+  ldsm_x4(smem_u32(tile + (m0 + (lane & 15)) * pitch + k0 + (lane >> 4) * 8), a);
+}
+// ... or stored [k][m].
+__device__ __forceinline__ void lda_t(const __nv_bfloat16 *tile, int pitch, int m0, int k0,
+                                      int lane, uint32_t (&a)[4]) {
+  ldsm_x4_t(smem_u32(tile + (k0 + (lane & 7) + ((lane >> 4) << 3)) * pitch + m0 +
+                     ((lane >> 3) & 1) * 8),
+            a);
+}
+// B for two n-tiles (16 x 16 at k0, n0): b[0], b[1] for columns n0 .. n0 + 7,
+// b[2], b[3] for n0 + 8 .. n0 + 15; from a tile stored [n][k] ...
+__device__ __forceinline__ void ldb(const __nv_bfloat16 *tile, int pitch, int n0, int k0, int lane,
+                                    uint32_t (&b)[4]) {
+  ldsm_x4(smem_u32(tile + (n0 + (lane & 7) + ((lane >> 4) << 3)) * pitch + k0 +
+                   ((lane >> 3) & 1) * 8),
+          b);
+}
+// ... or stored [k][n].
+__device__ __forceinline__ void ldb_t(const __nv_bfloat16 *tile, int pitch, int n0, int k0,
+                                      int lane, uint32_t (&b)[4]) {
+  ldsm_x4_t(smem_u32(tile + (k0 + (lane & 7) + ((lane >> 3) & 1) * 8) * pitch + n0 +
+                     (lane >> 4) * 8),
+            b);
+}
+__device__ __forceinline__ void mma2(float (&c)[2][4], const uint32_t (&a)[4],
+                                     const uint32_t (&b)[4]) {
+  mma_bf16_16x8x16(c[0], a[0], a[1], a[2], a[3], b[0], b[1]);
+  mma_bf16_16x8x16(c[1], a[0], a[1], a[2], a[3], b[2], b[3]);
+}
+__device__ __forceinline__ void zero(float (&c)[2][4]) {
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[j][i] = 0.f;
+}
+__device__ __forceinline__ void st_bf2(__nv_bfloat16 *p, float x, float y) {
+  *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(x, y);
+}
+// Two bf16 global stores: the gradient outputs are only element aligned.
+__device__ __forceinline__ void st_bf2_g(__nv_bfloat16 *p, float x, float y) {
+  p[0] = __float2bfloat16_rn(x);
+  p[1] = __float2bfloat16_rn(y);
+}
+__device__ __forceinline__ float2 ld_bf2(const __nv_bfloat16 *p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
+}
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+kda_bwd_chunk_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                     const __nv_bfloat16 *__restrict__ v, const float *__restrict__ la,
+                     const float *__restrict__ beta, const int32_t *__restrict__ cu,
+                     int32_t n_seqs, int64_t n_tokens, int32_t H,
+                     const float *__restrict__ ckpt, const __nv_bfloat16 *__restrict__ dout,
+                     const float *__restrict__ d_final, __nv_bfloat16 *__restrict__ dq,
+                     __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv,
+                     float *__restrict__ d_la, float *__restrict__ d_beta,
+                     float *__restrict__ d_init, DeviceStatus *status) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int seq = (int)(blockIdx.x / H), h = (int)(blockIdx.x % H);
+  const int64_t t0 = cu[seq], t1 = cu[seq + 1];
+  if (!(t0 >= 0 && t1 >= t0 && t1 <= n_tokens && (seq != 0 || (cu[0] == 0 && cu[n_seqs] == n_tokens)))) {
+    if (tid == 0) atomicCAS(&status->code, 0, 1 /* KDA_ERR_INVALID_ARG */);
+    return;
+  }
+  const int kr0 = 16 * warp;  // this warp's key rows of dS, and its output columns
+  const int64_t sbase = ((int64_t)seq * H + h) * D * D;
+
+  // dS (gradient of the state after the sequence), MMA accumulator layout:
+  // ds[j] covers value columns 8 j .. 8 j + 7 of key rows kr0 + g, kr0 + g + 8.
+  float ds[16][4];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int c = 8 * j + 2 * t;
+    ds[j][0] = ds[j][1] = ds[j][2] = ds[j][3] = 0.f;
+    if (d_final) {
+      const float *fa = d_final + sbase + (kr0 + g) * D + c, *fb = fa + 8 * D;
+      ds[j][0] = fa[0];
+      ds[j][1] = fa[1];
+      ds[j][2] = fb[0];
+      ds[j][3] = fb[1];
+    }
+  }
+
+  const int64_t n_ch = (t1 - t0 + CB - 1) / CB;
+  const int64_t slot0 = bwd_ckpt_slot_base(t0, seq, CB);
+  for (int64_t ch = n_ch - 1; ch >= 0; --ch) {
+    const int64_t tb = t0 + CB * ch;
+    const int n = (int)(t1 - tb < CB ? t1 - tb : CB);
+    __syncthreads();  // the previous chunk is done with every tile
+    // ---- inputs of the chunk (rows past n are zero)
+    for (int e = tid; e < CB * 16; e += kThreads) {
+      const int r = e >> 4, s8 = 8 * (e & 15);
+      if (r < n) {
+        const int64_t row = ((tb + r) * H + h) * D + s8;
+        cp_async16(&sm.q[r][s8], q + row);
+        cp_async16(&sm.k[r][s8], k + row);
+        cp_async16(&sm.v[r][s8], v + row);
+        cp_async16(&sm.dout[r][s8], dout + row);
+      } else {
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(&sm.q[r][s8]) = z;
+        *reinterpret_cast<uint4 *>(&sm.k[r][s8]) = z;
+        *reinterpret_cast<uint4 *>(&sm.v[r][s8]) = z;
+        *reinterpret_cast<uint4 *>(&sm.dout[r][s8]) = z;
+      }
+    }
+    for (int e = tid; e < CB * 32; e += kThreads) {
+      const int r = e >> 5, s4 = 4 * (e & 31);
+      if (r < n) cp_async16(&sm.la[r][s4], la + ((tb + r) * H + h) * D + s4);
+      else *reinterpret_cast<float4 *>(&sm.la[r][s4]) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (tid < CB) sm.beta[tid] = tid < n ? beta[(tb + tid) * H + h] : 0.f;
+    // the state at the chunk start (bf16 operand) and rowsum_v(S o dS'); dS' as bf16
+    const float *Sg = ckpt + ((slot0 + ch) * H + h) * (int64_t)(D * D);
+    float p1a = 0.f, p1b = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int c = 8 * j + 2 * t;
+      const float2 a = *reinterpret_cast<const float2 *>(Sg + (kr0 + g) * D + c);
+      const float2 b = *reinterpret_cast<const float2 *>(Sg + (kr0 + g + 8) * D + c);
+      st_bf2(&sm.S[kr0 + g][c], a.x, a.y);
+      st_bf2(&sm.S[kr0 + g + 8][c], b.x, b.y);
+      p1a = fmaf(a.x, ds[j][0], fmaf(a.y, ds[j][1], p1a));
+      p1b = fmaf(b.x, ds[j][2], fmaf(b.y, ds[j][3], p1b));
+      const __nv_bfloat162 ha = __floats2bfloat162_rn(ds[j][0], ds[j][1]);
+      const __nv_bfloat162 hb = __floats2bfloat162_rn(ds[j][2], ds[j][3]);
+      *reinterpret_cast<__nv_bfloat162 *>(&sm.dSn[kr0 + g][c]) = ha;
+      *reinterpret_cast<__nv_bfloat162 *>(&sm.dSn[kr0 + g + 8][c]) = hb;
+      const float2 fa = __bfloat1622float2(ha), fb = __bfloat1622float2(hb);
+      st_bf2(&sm.dSlo[kr0 + g][c], ds[j][0] - fa.x, ds[j][1] - fa.y);
+      st_bf2(&sm.dSlo[kr0 + g + 8][c], ds[j][2] - fb.x, ds[j][3] - fb.y);
+    }
+    p1a += __shfl_xor_sync(0xffffffffu, p1a, 1);
+    p1a += __shfl_xor_sync(0xffffffffu, p1a, 2);
+    p1b += __shfl_xor_sync(0xffffffffu, p1b, 1);
+    p1b += __shfl_xor_sync(0xffffffffu, p1b, 2);
+    if (t == 0) {
+      sm.t1[kr0 + g] = p1a;
+      sm.t1[kr0 + g + 8] = p1b;
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    // ---- decay factors and the factor-scaled operands (thread: one key column;
+    // threads 0-127 the k-derived tiles, 128-255 the q-derived ones)
+    {
+      const int c = tid & (D - 1);
+      float gr[CB];
+      float acc = 0.f;
+#pragma unroll
+      for (int r = 0; r < CB; ++r) {
+        acc += sm.la[r][c];
+        gr[r] = acc;
+      }
+      const float gm = gr[kMid], gl = gr[kLast];
+      if (tid < D) {
+        sm.em[c] = expf(gm);
+        sm.gam[c] = expf(gl);
+#pragma unroll
+        for (int r = 0; r < CB; ++r) {
+          const float kf = __bfloat162float(sm.k[r][c]);
+          const float e1 = expf(gr[r] - gm);
+          sm.et[r][c] = e1;
+          sm.kt[r][c] = __float2bfloat16_rn(kf * e1);
+          sm.kh[r][c] = __float2bfloat16_rn(kf * expf(gm - gr[r]));
+          sm.kd[r][c] = __float2bfloat16_rn(kf * expf(gl - gr[r]));
+          sm.ks[r][c] = __float2bfloat16_rn(kf * expf(gr[r]));
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < CB; ++r) {
+          const float qf = __bfloat162float(sm.q[r][c]);
+          sm.qt[r][c] = __float2bfloat16_rn(qf * expf(gr[r] - gm));
+          sm.qs[r][c] = __float2bfloat16_rn(qf * expf(gr[r]));
+        }
+      }
+    }
+    __syncthreads();
+
+    // ---- G = Kt Kh^T (warp 0); R = V - Ks S, U = Diag(beta) R (all warps)
+    if (warp == 0) {
+      float a2[2][4], b2[2][4];
+      zero(a2);
+      zero(b2);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; kk += 2) {
+        uint32_t a[4], b[4];
+        lda(&sm.kt[0][0], TP, 0, 16 * kk, lane, a);
+        ldb(&sm.kh[0][0], TP, 0, 16 * kk, lane, b);
+        mma2(a2, a, b);
+        lda(&sm.kt[0][0], TP, 0, 16 * kk + 16, lane, a);
+        ldb(&sm.kh[0][0], TP, 0, 16 * kk + 16, lane, b);
+        mma2(b2, a, b);
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int c = 8 * j + 2 * t;
+        sm.G[g][c] = a2[j][0] + b2[j][0];
+        sm.G[g][c + 1] = a2[j][1] + b2[j][1];
+        sm.G[g + 8][c] = a2[j][2] + b2[j][2];
+        sm.G[g + 8][c + 1] = a2[j][3] + b2[j][3];
+      }
+    } else if (warp == 1) {  // P = tril(Qt Kh^T), bf16
+      float a2[2][4], b2[2][4];
+      zero(a2);
+      zero(b2);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; kk += 2) {
+        uint32_t a[4], b[4];
+        lda(&sm.qt[0][0], TP, 0, 16 * kk, lane, a);
+        ldb(&sm.kh[0][0], TP, 0, 16 * kk, lane, b);
+        mma2(a2, a, b);
+        lda(&sm.qt[0][0], TP, 0, 16 * kk + 16, lane, a);
+        ldb(&sm.kh[0][0], TP, 0, 16 * kk + 16, lane, b);
+        mma2(b2, a, b);
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int c = 8 * j + 2 * t;
+        st_bf2(&sm.pm[g][c], c <= g ? a2[j][0] + b2[j][0] : 0.f,
+               c + 1 <= g ? a2[j][1] + b2[j][1] : 0.f);
+        st_bf2(&sm.pm[g + 8][c], c <= g + 8 ? a2[j][2] + b2[j][2] : 0.f,
+               c + 1 <= g + 8 ? a2[j][3] + b2[j][3] : 0.f);
+      }
+    }
+    const int n0 = 16 * warp;  // this warp's 16 output columns
+    float rr[2][4];
+    {
+      zero(rr);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        uint32_t a[4], b[4];
+        lda(&sm.ks[0][0], TP, 0, 16 * kk, lane, a);
+        ldb_t(&sm.S[0][0], TP, n0, 16 * kk, lane, b);
+        mma2(rr, a, b);
+      }
+      const float bg = sm.beta[g], bg8 = sm.beta[g + 8];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int c = n0 + 8 * j + 2 * t;
+        const float2 va = ld_bf2(&sm.v[g][c]), vb = ld_bf2(&sm.v[g + 8][c]);
+        rr[j][0] = va.x - rr[j][0];
+        rr[j][1] = va.y - rr[j][1];
+        rr[j][2] = vb.x - rr[j][2];
+        rr[j][3] = vb.y - rr[j][3];
+        st_bf2(&sm.u[g][c], bg * rr[j][0], bg * rr[j][1]);
+        st_bf2(&sm.u[g + 8][c], bg8 * rr[j][2], bg8 * rr[j][3]);
+      }
+    }
+    __syncthreads();
+
+    // ---- T = (I + A)^{-1}, A = tril(Diag(beta) G, -1): lane j < 16 of warp 0
+    // owns column j (forward substitution over the rows)
+    if (warp == 0 && lane < CB) {
+      const int j = lane;
+      float tc[CB];
+#pragma unroll
+      for (int r = 0; r < CB; ++r) {
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < r; ++i) s = fmaf(sm.G[r][i], tc[i], s);
+        tc[r] = (r == j ? 1.f : 0.f) - sm.beta[r] * s;
+      }
+#pragma unroll
+      for (int r = 0; r < CB; ++r) sm.tm[r][j] = __float2bfloat16_rn(tc[r]);
+    }
+    __syncthreads();
+
+    // ---- delta = T U; d delta = P^T dO + Kd dS'
+    float dd[2][4];
+    {
+      float dlt[2][4];
+      zero(dlt);
+      uint32_t a[4], b[4];
+      lda(&sm.tm[0][0], SP, 0, 0, lane, a);
+      ldb_t(&sm.u[0][0], TP, n0, 0, lane, b);
+      mma2(dlt, a, b);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int c = n0 + 8 * j + 2 * t;
+        st_bf2(&sm.dl[g][c], dlt[j][0], dlt[j][1]);
+        st_bf2(&sm.dl[g + 8][c], dlt[j][2], dlt[j][3]);
+      }
+      zero(dd);
+      lda_t(&sm.pm[0][0], SP, 0, 0, lane, a);
+      ldb_t(&sm.dout[0][0], TP, n0, 0, lane, b);
+      mma2(dd, a, b);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {  // dS' as its bf16 pair: d beta is a
+        lda(&sm.kd[0][0], TP, 0, 16 * kk, lane, a);  // dot product with cancellation
+        ldb_t(&sm.dSn[0][0], TP, n0, 16 * kk, lane, b);
+        mma2(dd, a, b);
+        ldb_t(&sm.dSlo[0][0], TP, n0, 16 * kk, lane, b);
+        mma2(dd, a, b);
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int c = n0 + 8 * j + 2 * t;
+        st_bf2(&sm.ddl[g][c], dd[j][0], dd[j][1]);
+        st_bf2(&sm.ddl[g + 8][c], dd[j][2], dd[j][3]);
+      }
+    }
+    __syncthreads();
+
+    // ---- dU = T^T d delta, dR = Diag(beta) dU (= dv); rowsum(R o dU)
+    {
+      float du[2][4];
+      zero(du);
+      uint32_t a[4], b[4];
+      lda_t(&sm.tm[0][0], SP, 0, 0, lane, a);
+      ldb_t(&sm.ddl[0][0], TP, n0, 0, lane, b);
+      mma2(du, a, b);
+      const float bg = sm.beta[g], bg8 = sm.beta[g + 8];
+      float pa = 0.f, pb = 0.f;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int c = n0 + 8 * j + 2 * t;
+        pa = fmaf(rr[j][0], du[j][0], fmaf(rr[j][1], du[j][1], pa));
+        pb = fmaf(rr[j][2], du[j][2], fmaf(rr[j][3], du[j][3], pb));
+        st_bf2(&sm.du[g][c], du[j][0], du[j][1]);
+        st_bf2(&sm.du[g + 8][c], du[j][2], du[j][3]);
+        st_bf2(&sm.ndr[g][c], -bg * du[j][0], -bg * du[j][1]);
+        st_bf2(&sm.ndr[g + 8][c], -bg8 * du[j][2], -bg8 * du[j][3]);
+        if (g < n) st_bf2_g(dv + ((tb + g) * H + h) * D + c, bg * du[j][0], bg * du[j][1]);
+        if (g + 8 < n) st_bf2_g(dv + ((tb + g + 8) * H + h) * D + c, bg8 * du[j][2], bg8 * du[j][3]);
+      }
+      pa += __shfl_xor_sync(0xffffffffu, pa, 1);
+      pa += __shfl_xor_sync(0xffffffffu, pa, 2);
+      pb += __shfl_xor_sync(0xffffffffu, pb, 1);
+      pb += __shfl_xor_sync(0xffffffffu, pb, 2);
+      if (t == 0) {
+        sm.dbp[warp][g] = pa;
+        sm.dbp[warp][g + 8] = pb;
+      }
+    }
+    __syncthreads();
+
+    // ---- dA, dP (warps 0, 1); dS = Diag(e^{g_l}) dS' + Qs^T dO - Ks^T dR (all)
+    if (warp < 2) {
+      const __nv_bfloat16 *lhs = warp == 0 ? &sm.du[0][0] : &sm.dout[0][0];
+      float a2[2][4], b2[2][4];
+      zero(a2);
+      zero(b2);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; kk += 2) {
+        uint32_t a[4], b[4];
+        lda(lhs, TP, 0, 16 * kk, lane, a);
+        ldb(&sm.dl[0][0], TP, 0, 16 * kk, lane, b);
+        mma2(a2, a, b);
+        lda(lhs, TP, 0, 16 * kk + 16, lane, a);
+        ldb(&sm.dl[0][0], TP, 0, 16 * kk + 16, lane, b);
+        mma2(b2, a, b);
+      }
+      if (warp == 0) {  // dA = tril(-dU delta^T, -1); dG = Diag(beta) dA; rowsum(dA o G)
+        const float bg = sm.beta[g], bg8 = sm.beta[g + 8];
+        float pa = 0.f, pb = 0.f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int c = 8 * j + 2 * t;
+          const float x0 = c < g ? -(a2[j][0] + b2[j][0]) : 0.f;
+          const float x1 = c + 1 < g ? -(a2[j][1] + b2[j][1]) : 0.f;
+          const float x2 = c < g + 8 ? -(a2[j][2] + b2[j][2]) : 0.f;
+          const float x3 = c + 1 < g + 8 ? -(a2[j][3] + b2[j][3]) : 0.f;
+          pa = fmaf(x0, sm.G[g][c], fmaf(x1, sm.G[g][c + 1], pa));
+          pb = fmaf(x2, sm.G[g + 8][c], fmaf(x3, sm.G[g + 8][c + 1], pb));
+          st_bf2(&sm.dgm[g][c], bg * x0, bg * x1);
+          st_bf2(&sm.dgm[g + 8][c], bg8 * x2, bg8 * x3);
+        }
+        pa += __shfl_xor_sync(0xffffffffu, pa, 1);
+        pa += __shfl_xor_sync(0xffffffffu, pa, 2);
+        pb += __shfl_xor_sync(0xffffffffu, pb, 1);
+        pb += __shfl_xor_sync(0xffffffffu, pb, 2);
+        if (t == 0) {
+          sm.dba[g] = pa;
+          sm.dba[g + 8] = pb;
+        }
+      } else {  // dP = tril(dO delta^T)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int c = 8 * j + 2 * t;
+          st_bf2(&sm.dpm[g][c], c <= g ? a2[j][0] + b2[j][0] : 0.f,
+                 c + 1 <= g ? a2[j][1] + b2[j][1] : 0.f);
+          st_bf2(&sm.dpm[g + 8][c], c <= g + 8 ? a2[j][2] + b2[j][2] : 0.f,
+                 c + 1 <= g + 8 ? a2[j][3] + b2[j][3] : 0.f);
+        }
+      }
+    }
+    {
+      const float ga = sm.gam[kr0 + g], gb = sm.gam[kr0 + g + 8];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        ds[j][0] *= ga; ds[j][1] *= ga; ds[j][2] *= gb; ds[j][3] *= gb;
+      }
+      uint32_t aq[4], ak[4];
+      lda_t(&sm.qs[0][0], TP, kr0, 0, lane, aq);
+      lda_t(&sm.ks[0][0], TP, kr0, 0, lane, ak);
+#pragma unroll
+      for (int jp = 0; jp < 8; ++jp) {
+        uint32_t b[4];
+        ldb_t(&sm.dout[0][0], TP, 16 * jp, 0, lane, b);
+        mma_bf16_16x8x16(ds[2 * jp], aq[0], aq[1], aq[2], aq[3], b[0], b[1]);
+        mma_bf16_16x8x16(ds[2 * jp + 1], aq[0], aq[1], aq[2], aq[3], b[2], b[3]);
+        ldb_t(&sm.ndr[0][0], TP, 16 * jp, 0, lane, b);
+        mma_bf16_16x8x16(ds[2 * jp], ak[0], ak[1], ak[2], ak[3], b[0], b[1]);
+        mma_bf16_16x8x16(ds[2 * jp + 1], ak[0], ak[1], ak[2], ak[3], b[2], b[3]);
+      }
+      // rowsum_v(S o dS) with the fp32 state
+      float p2a = 0.f, p2b = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int c = 8 * j + 2 * t;
+        const float2 a = *reinterpret_cast<const float2 *>(Sg + (kr0 + g) * D + c);
+        const float2 b = *reinterpret_cast<const float2 *>(Sg + (kr0 + g + 8) * D + c);
+        p2a = fmaf(a.x, ds[j][0], fmaf(a.y, ds[j][1], p2a));
+        p2b = fmaf(b.x, ds[j][2], fmaf(b.y, ds[j][3], p2b));
+      }
+      p2a += __shfl_xor_sync(0xffffffffu, p2a, 1);
+      p2a += __shfl_xor_sync(0xffffffffu, p2a, 2);
+      p2b += __shfl_xor_sync(0xffffffffu, p2b, 1);
+      p2b += __shfl_xor_sync(0xffffffffu, p2b, 2);
+      if (t == 0) {
+        sm.t2[kr0 + g] = p2a;
+        sm.t2[kr0 + g + 8] = p2b;
+      }
+    }
+    // ---- dKd = delta dS'^T, (-dR) S^T, dO S^T (columns n0 .. n0 + 15 = keys)
+    float akd[2][4], akt[2][4], aqt[2][4];
+    zero(akd);
+    zero(akt);
+    zero(aqt);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      uint32_t a[4], b[4];
+      lda(&sm.dl[0][0], TP, 0, 16 * kk, lane, a);
+      ldb(&sm.dSn[0][0], TP, n0, 16 * kk, lane, b);
+      mma2(akd, a, b);
+      ldb(&sm.S[0][0], TP, n0, 16 * kk, lane, b);
+      lda(&sm.ndr[0][0], TP, 0, 16 * kk, lane, a);
+      mma2(akt, a, b);
+      lda(&sm.dout[0][0], TP, 0, 16 * kk, lane, a);
+      mma2(aqt, a, b);
+    }
+    __syncthreads();  // dG, dP, rowsum(dA o G), t2 are in place
+
+    // ---- dKt = e^{g_m} o ((-dR) S^T) + dG Kh, dQt = e^{g_m} o (dO S^T) + dP Kh,
+    // dKh = dG^T Kt + dP^T Qt; then dq, dk and dg for this warp's key columns
+    {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int c = n0 + 8 * j + 2 * t;
+        const float e0 = sm.em[c], e1 = sm.em[c + 1];
+        akt[j][0] *= e0; akt[j][1] *= e1; akt[j][2] *= e0; akt[j][3] *= e1;
+        aqt[j][0] *= e0; aqt[j][1] *= e1; aqt[j][2] *= e0; aqt[j][3] *= e1;
+      }
+      float akh[2][4];
+      zero(akh);
+      uint32_t a[4], b[4];
+      ldb_t(&sm.kh[0][0], TP, n0, 0, lane, b);
+      lda(&sm.dgm[0][0], SP, 0, 0, lane, a);
+      mma2(akt, a, b);
+      lda(&sm.dpm[0][0], SP, 0, 0, lane, a);
+      mma2(aqt, a, b);
+      ldb_t(&sm.kt[0][0], TP, n0, 0, lane, b);
+      lda_t(&sm.dgm[0][0], SP, 0, 0, lane, a);
+      mma2(akh, a, b);
+      ldb_t(&sm.qt[0][0], TP, n0, 0, lane, b);
+      lda_t(&sm.dpm[0][0], SP, 0, 0, lane, a);
+      mma2(akh, a, b);
+
+      float sphi[2][2], spsi[2][2], schi[2][2];  // column sums [j][e]
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int c = n0 + 8 * j + 2 * t;
+        const float etl0 = sm.et[kLast][c], etl1 = sm.et[kLast][c + 1];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) sphi[j][e] = spsi[j][e] = schi[j][e] = 0.f;
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {  // rows g, g + 8
+          const int r = g + 8 * hr;
+          // dg pairs each gradient with the bf16 operand value its product used,
+          // so the terms of a product that cancel in exact arithmetic (the Gram
+          // and P pairs within the chunk) cancel here too
+          const float2 vkt = ld_bf2(&sm.kt[r][c]), vqt = ld_bf2(&sm.qt[r][c]);
+          const float2 vkh = ld_bf2(&sm.kh[r][c]), vkd = ld_bf2(&sm.kd[r][c]);
+          float dqv[2], dkv[2], dgv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float et = sm.et[r][c + e];
+            const float eh = __fdividef(1.0f, et);  // et in [e^-40, e^40]
+            const float ed = (e ? etl1 : etl0) * eh;
+            const float gkt = akt[j][2 * hr + e], gqt = aqt[j][2 * hr + e];
+            const float gkh = akh[j][2 * hr + e], gkd = akd[j][2 * hr + e];
+            dqv[e] = gqt * et;
+            dkv[e] = gkt * et + gkh * eh + gkd * ed;
+            const float phi = gkt * (e ? vkt.y : vkt.x) + gqt * (e ? vqt.y : vqt.x);
+            const float psi = gkh * (e ? vkh.y : vkh.x);
+            const float chi = gkd * (e ? vkd.y : vkd.x);
+            sphi[j][e] += phi;
+            spsi[j][e] += psi;
+            schi[j][e] += chi;
+            dgv[e] = phi - psi - chi;
+          }
+          if (r < n) {
+            st_bf2_g(dq + ((tb + r) * H + h) * D + c, dqv[0], dqv[1]);
+            st_bf2_g(dk + ((tb + r) * H + h) * D + c, dkv[0], dkv[1]);
+          }
+          sm.dgr[r][c] = dgv[0];
+          sm.dgr[r][c + 1] = dgv[1];
+        }
+      }
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            sphi[j][e] += __shfl_xor_sync(0xffffffffu, sphi[j][e], off);
+            spsi[j][e] += __shfl_xor_sync(0xffffffffu, spsi[j][e], off);
+            schi[j][e] += __shfl_xor_sync(0xffffffffu, schi[j][e], off);
+          }
+      if (g == kMid) {  // this lane also wrote rows kMid and kLast = kMid + 8
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int c = n0 + 8 * j + 2 * t + e;
+            const float gt1 = sm.gam[c] * sm.t1[c];
+            sm.dgr[kMid][c] += -sphi[j][e] + spsi[j][e] + (sm.t2[c] - gt1);
+            sm.dgr[kLast][c] += schi[j][e] + gt1;
+          }
+      }
+    }
+    __syncthreads();
+
+    // ---- dlog_alpha: reverse cumulative sum over the chunk; dbeta
+    if (tid < D) {
+      float acc = 0.f;
+#pragma unroll
+      for (int r = CB - 1; r >= 0; --r) {
+        acc += sm.dgr[r][tid];
+        if (r < n) d_la[((tb + r) * H + h) * D + tid] = acc;
+      }
+    } else if (tid < D + CB) {
+      const int r = tid - D;
+      if (r < n) {
+        float s = sm.dba[r];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) s += sm.dbp[w][r];
+        d_beta[(tb + r) * H + h] = s;
+      }
+    }
+  }
+  if (d_init) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int c = 8 * j + 2 * t;
+      float *pa = d_init + sbase + (kr0 + g) * D + c, *pb = pa + 8 * D;
+      pa[0] = ds[j][0];
+      pa[1] = ds[j][1];
+      pb[0] = ds[j][2];
+      pb[1] = ds[j][3];
+    }
+  }
+}
+
+// Forward pass for the chunked backward: the state at every chunk start
+// (checkpoint slot bwd_ckpt_slot_base(cu[s], s, 16) + chunk), by the chunk form
+// above with the same bf16 operands: R = V - Ks S, delta = T Diag(beta) R,
+// S' = Diag(e^{g_l}) S + Kd^T delta.  The state stays in registers as MMA
+// accumulators (warp w: key rows 16 w .. 16 w + 15).
+struct __align__(16) CkSmem {
+  __nv_bfloat16 S[D][TP];
+  __nv_bfloat16 k[CB][TP], v[CB][TP], kt[CB][TP], kh[CB][TP], ks[CB][TP], kd[CB][TP];
+  __nv_bfloat16 u[CB][TP], dl[CB][TP];
+  __nv_bfloat16 tm[CB][SP];
+  float la[CB][D];
+  float G[CB][GP];
+  float gam[D];
+  float beta[CB];
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+kda_bwd_chunk_ckpt_kernel(const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
+                          const float *__restrict__ la, const float *__restrict__ beta,
+                          const float *__restrict__ init_state, const int32_t *__restrict__ cu,
+                          int32_t n_seqs, int64_t n_tokens, int32_t H, float *__restrict__ ckpt,
+                          DeviceStatus *status) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  CkSmem &sm = *reinterpret_cast<CkSmem *>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int seq = (int)(blockIdx.x / H), h = (int)(blockIdx.x % H);
+  const int64_t t0 = cu[seq], t1 = cu[seq + 1];
+  if (!(t0 >= 0 && t1 >= t0 && t1 <= n_tokens && (seq != 0 || (cu[0] == 0 && cu[n_seqs] == n_tokens)))) {
+    if (tid == 0) atomicCAS(&status->code, 0, 1 /* KDA_ERR_INVALID_ARG */);
+    return;
+  }
+  const int kr0 = 16 * warp, n0 = 16 * warp;
+  float st[16][4];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int c = 8 * j + 2 * t;
+    st[j][0] = st[j][1] = st[j][2] = st[j][3] = 0.f;
+    if (init_state) {
+      const float *pa = init_state + ((int64_t)seq * H + h) * D * D + (kr0 + g) * D + c;
+      st[j][0] = pa[0];
+      st[j][1] = pa[1];
+      st[j][2] = pa[8 * D];
+      st[j][3] = pa[8 * D + 1];
+    }
+  }
+  const int64_t n_ch = (t1 - t0 + CB - 1) / CB;
+  const int64_t slot0 = bwd_ckpt_slot_base(t0, seq, CB);
+  for (int64_t ch = 0; ch < n_ch; ++ch) {
+    const int64_t tb = t0 + CB * ch;
+    const int n = (int)(t1 - tb < CB ? t1 - tb : CB);
+    __syncthreads();  // the previous chunk is done with every tile
+    float *Sg = ckpt + ((slot0 + ch) * H + h) * (int64_t)(D * D);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int c = 8 * j + 2 * t;
+      *reinterpret_cast<float2 *>(Sg + (kr0 + g) * D + c) = make_float2(st[j][0], st[j][1]);
+      *reinterpret_cast<float2 *>(Sg + (kr0 + g + 8) * D + c) = make_float2(st[j][2], st[j][3]);
+      st_bf2(&sm.S[kr0 + g][c], st[j][0], st[j][1]);
+      st_bf2(&sm.S[kr0 + g + 8][c], st[j][2], st[j][3]);
+    }
+    for (int e = tid; e < CB * 16; e += kThreads) {
+      const int r = e >> 4, s8 = 8 * (e & 15);
+      if (r < n) {
+        const int64_t row = ((tb + r) * H + h) * D + s8;
+        cp_async16(&sm.k[r][s8], k + row);
+        cp_async16(&sm.v[r][s8], v + row);
+      } else {
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(&sm.k[r][s8]) = z;
+        *reinterpret_cast<uint4 *>(&sm.v[r][s8]) = z;
+      }
+    }
+    for (int e = tid; e < CB * 32; e += kThreads) {
+      const int r = e >> 5, s4 = 4 * (e & 31);
+      if (r < n) cp_async16(&sm.la[r][s4], la + ((tb + r) * H + h) * D + s4);
+      else *reinterpret_cast<float4 *>(&sm.la[r][s4]) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (tid < CB) sm.beta[tid] = tid < n ? beta[(tb + tid) * H + h] : 0.f;
+    cp_async_wait_all();
+    __syncthreads();
+    {  // factor-scaled k tiles: threads 0-127 Kt, Kh; 128-255 Ks, Kd
+      const int c = tid & (D - 1);
+      float gr[CB];
+      float acc = 0.f;
+#pragma unroll
+      for (int r = 0; r < CB; ++r) {
+        acc += sm.la[r][c];
+        gr[r] = acc;
+      }
+      const float gm = gr[kMid], gl = gr[kLast];
+      if (tid < D) {
+#pragma unroll
+        for (int r = 0; r < CB; ++r) {
+          const float kf = __bfloat162float(sm.k[r][c]);
+          sm.kt[r][c] = __float2bfloat16_rn(kf * expf(gr[r] - gm));
+          sm.kh[r][c] = __float2bfloat16_rn(kf * expf(gm - gr[r]));
+        }
+      } else {
+        sm.gam[c] = expf(gl);
+#pragma unroll
+        for (int r = 0; r < CB; ++r) {
+          const float kf = __bfloat162float(sm.k[r][c]);
+          sm.ks[r][c] = __float2bfloat16_rn(kf * expf(gr[r]));
+          sm.kd[r][c] = __float2bfloat16_rn(kf * expf(gl - gr[r]));
+        }
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {  // G = Kt Kh^T
+      float a2[2][4], b2[2][4];
+      zero(a2);
+      zero(b2);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; kk += 2) {
+        uint32_t a[4], b[4];
+        lda(&sm.kt[0][0], TP, 0, 16 * kk, lane, a);
+        ldb(&sm.kh[0][0], TP, 0, 16 * kk, lane, b);
+        mma2(a2, a, b);
+        lda(&sm.kt[0][0], TP, 0, 16 * kk + 16, lane, a);
+        ldb(&sm.kh[0][0], TP, 0, 16 * kk + 16, lane, b);
+        mma2(b2, a, b);
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int c = 8 * j + 2 * t;
+        sm.G[g][c] = a2[j][0] + b2[j][0];
+        sm.G[g][c + 1] = a2[j][1] + b2[j][1];
+        sm.G[g + 8][c] = a2[j][2] + b2[j][2];
+        sm.G[g + 8][c + 1] = a2[j][3] + b2[j][3];
+      }
+    }
+    {  // U = Diag(beta) (V - Ks S), this warp's value columns
+      float rr[2][4];
+      zero(rr);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        uint32_t a[4], b[4];
+        lda(&sm.ks[0][0], TP, 0, 16 * kk, lane, a);
+        ldb_t(&sm.S[0][0], TP, n0, 16 * kk, lane, b);
+        mma2(rr, a, b);
+      }
+      const float bg = sm.beta[g], bg8 = sm.beta[g + 8];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int c = n0 + 8 * j + 2 * t;
+        const float2 va = ld_bf2(&sm.v[g][c]), vb = ld_bf2(&sm.v[g + 8][c]);
+        st_bf2(&sm.u[g][c], bg * (va.x - rr[j][0]), bg * (va.y - rr[j][1]));
+        st_bf2(&sm.u[g + 8][c], bg8 * (vb.x - rr[j][2]), bg8 * (vb.y - rr[j][3]));
+      }
+    }
+    __syncthreads();
+    if (warp == 0 && lane < CB) {  // T = (I + A)^{-1}, column `lane`
+      const int j = lane;
+      float tc[CB];
+#pragma unroll
+      for (int r = 0; r < CB; ++r) {
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < r; ++i) s = fmaf(sm.G[r][i], tc[i], s);
+        tc[r] = (r == j ? 1.f : 0.f) - sm.beta[r] * s;
+      }
+#pragma unroll
+      for (int r = 0; r < CB; ++r) sm.tm[r][j] = __float2bfloat16_rn(tc[r]);
+    }
+    __syncthreads();
+    {  // delta = T U
+      float dlt[2][4];
+      zero(dlt);
+      uint32_t a[4], b[4];
+      lda(&sm.tm[0][0], SP, 0, 0, lane, a);
+      ldb_t(&sm.u[0][0], TP, n0, 0, lane, b);
+      mma2(dlt, a, b);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int c = n0 + 8 * j + 2 * t;
+        st_bf2(&sm.dl[g][c], dlt[j][0], dlt[j][1]);
+        st_bf2(&sm.dl[g + 8][c], dlt[j][2], dlt[j][3]);
+      }
+    }
+    __syncthreads();
+    {  // S' = Diag(e^{g_l}) S + Kd^T delta
+      const float ga = sm.gam[kr0 + g], gb = sm.gam[kr0 + g + 8];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        st[j][0] *= ga; st[j][1] *= ga; st[j][2] *= gb; st[j][3] *= gb;
+      }
+      uint32_t a[4];
+      lda_t(&sm.kd[0][0], TP, kr0, 0, lane, a);
+#pragma unroll
+      for (int jp = 0; jp < 8; ++jp) {
+        uint32_t b[4];
+        ldb_t(&sm.dl[0][0], TP, 16 * jp, 0, lane, b);
+        mma_bf16_16x8x16(st[2 * jp], a[0], a[1], a[2], a[3], b[0], b[1]);
+        mma_bf16_16x8x16(st[2 * jp + 1], a[0], a[1], a[2], a[3], b[2], b[3]);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+size_t bwd_chunk_smem_bytes() { return sizeof(Smem); }
+
+cudaError_t launch_bwd_chunk(const BwdArgs &a, cudaStream_t stream) {
+  const int64_t chains = (int64_t)a.n_seqs * a.H;
+  if (chains == 0) return cudaSuccess;
+  if (chains > 0x7fffffffLL || !a.bf16 || a.ckpt_every != CB) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(kda_bwd_chunk_ckpt_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)sizeof(CkSmem));
+  if (e != cudaSuccess) return e;
+  kda_bwd_chunk_ckpt_kernel<<<(unsigned)chains, kThreads, sizeof(CkSmem), stream>>>(
+      static_cast<const __nv_bfloat16 *>(a.k), static_cast<const __nv_bfloat16 *>(a.v),
+      a.log_alpha, a.beta, a.init_state, a.cu_seqlens, a.n_seqs, a.n_tokens, a.H, a.ckpt,
+      a.status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t smem = sizeof(Smem);
+  e = cudaFuncSetAttribute(kda_bwd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
+  if (e != cudaSuccess) return e;
+  kda_bwd_chunk_kernel<<<(unsigned)chains, kThreads, smem, stream>>>(
+      static_cast<const __nv_bfloat16 *>(a.q), static_cast<const __nv_bfloat16 *>(a.k),
+      static_cast<const __nv_bfloat16 *>(a.v), a.log_alpha, a.beta, a.cu_seqlens, a.n_seqs,
+      a.n_tokens, a.H, a.ckpt, static_cast<const __nv_bfloat16 *>(a.d_out), a.d_final,
+      static_cast<__nv_bfloat16 *>(a.dq), static_cast<__nv_bfloat16 *>(a.dk),
+      static_cast<__nv_bfloat16 *>(a.dv), a.d_log_alpha, a.d_beta, a.d_init, a.status);
+  return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -153,11 +153,21 @@ struct BwdArgs {
   void *dq, *dk, *dv;
   float *d_log_alpha, *d_beta, *d_init;  // d_init may be nullptr
   int32_t ckpt_every;         // tokens between stored states: a power of two in [4, 1024]
+  bool chunked;               // bf16 only: the chunked tensor-core pass (ckpt_every == kBwdChunk)
   // workspace
   float *ckpt;                // [bwd_ckpt_slots][H][128][128]
   float *dq_acc, *dk_acc;     // [n_tokens][H][128], zeroed
   DeviceStatus *status;
 };
+// Tokens per chunk of the chunked (tensor-core) backward pass, which takes its
+// states every kBwdChunk tokens.
+constexpr int32_t kBwdChunk = 16;
+// Checkpoint slot of the first state of sequence s (states every `every`
+// tokens from its start): floor(cu[s] / every) + s.  Consecutive sequences never
+// share slots, since floor(b / c) - floor(a / c) + 1 >= ceil((b - a) / c).
+__host__ __device__ inline int64_t bwd_ckpt_slot_base(int64_t cu_s, int64_t s, int32_t every) {
+  return cu_s / every + s;
+}
 // Checkpoint interval bounds of the backward pass, and the budget its default
 // interval keeps the stored states within.
 constexpr int32_t kMaxCkptEvery = 1024;
@@ -168,6 +178,9 @@ size_t bwd_ckpt_slots(int32_t n_seqs, int64_t n_tokens, int32_t every);
 // kCkptBudgetBytes (kMaxCkptEvery if none does).
 int32_t bwd_ckpt_every(int32_t n_seqs, int64_t n_tokens, int32_t H);
 cudaError_t launch_chunk_bwd(const BwdArgs &a, cudaStream_t stream);
+// The chunked pass proper (after the checkpoints), and its shared memory.
+cudaError_t launch_bwd_chunk(const BwdArgs &a, cudaStream_t stream);
+size_t bwd_chunk_smem_bytes();
 
 cudaError_t launch_post(const void *o, const void *g, const float *gamma, int64_t n_tokens,
                         int32_t H, bool bf16, void *out, cudaStream_t stream);

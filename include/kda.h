@@ -166,15 +166,23 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
  *                gradient at the zero state)
  * The other arguments are those of kda_chunk_fwd (same inputs, same
  * cu_seqlens rules: host arrays are validated here, device arrays in the
- * kernel, which records KDA_ERR_INVALID_ARG and writes nothing).  The states
- * are recomputed: a forward sweep stores the state before every E-th token in
- * the workspace, and the reverse sweep recomputes the states in between, in
- * groups of four tokens.  E is the smallest power of two >= 4 whose stored
- * states (64 KiB per head for every E tokens and per sequence) fit in 16 GiB,
- * or 1024; kda_chunk_bwd_sched takes it from the caller instead.  fp32
- * arithmetic on CUDA cores; dq, dk, d_log_alpha and d_beta are sums over the
- * value channels, added in fp32 in an order that may vary between calls (last
- * bits only).
+ * kernel, which records KDA_ERR_INVALID_ARG and writes nothing).  A forward
+ * sweep stores states in the workspace and a reverse sweep recomputes what it
+ * needs from them.  Two passes:
+ *  - bf16 (when the states fit in 16 GiB): the chunked pass.  States every 16
+ *    tokens (64 KiB per head for every 16 tokens and per sequence); the reverse
+ *    sweep takes 16-token chunks in the chunk form of the recurrence, every
+ *    product on the tensor cores with bf16 operands and fp32 accumulation (the
+ *    gradient of the state as an operand in a pair of bf16 terms), fp32 state
+ *    gradient.  Every result element is written once: results do not vary
+ *    between calls.
+ *  - otherwise, and for fp32: the token-loop pass.  States every E tokens, E
+ *    the smallest power of two >= 4 whose stored states fit in 16 GiB, or 1024
+ *    (kda_chunk_bwd_sched takes E from the caller, and with it this pass, for
+ *    bf16 too); the reverse sweep recomputes the states in between in groups
+ *    of four tokens.  fp32 arithmetic on CUDA cores; dq, dk, d_log_alpha and
+ *    d_beta are sums over the value channels, added in fp32 in an order that
+ *    may vary between calls (last bits only).
  * Alignment: q, k, v, log_alpha and d_out 16 bytes (their rows are fetched by
  * 16-byte asynchronous copies); element alignment for every other tensor.  No
  * output may overlap an input or another output.
@@ -189,9 +197,9 @@ int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *log_
 
 /*
  * Bytes of device workspace kda_chunk_bwd needs: the status block, a device
- * copy of a host cu_seqlens, the stored states (64 KiB per head for every E
- * tokens and per sequence, E as in kda_chunk_bwd) and fp32 accumulators of dq
- * and dk.
+ * copy of a host cu_seqlens, the stored states (64 KiB per head for every 16
+ * or E tokens and per sequence, as in kda_chunk_bwd) and, for the token-loop
+ * pass, fp32 accumulators of dq and dk.
  * Errors: as kda_chunk_fwd_workspace_size.
  */
 int kda_chunk_bwd_workspace_size(int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk,
@@ -200,10 +208,13 @@ int kda_chunk_bwd_workspace_size(int32_t n_seqs, int64_t n_tokens, int32_t H, in
 /*
  * kda_chunk_bwd with the checkpoint interval E chosen by the caller:
  * ckpt_every = 0 is the library's choice (as kda_chunk_bwd), otherwise a power
- * of two in [4, 1024].  E = 4 recomputes nothing twice and stores the most
+ * of two in [4, 1024], which selects the token-loop pass with that interval
+ * for either dtype.  E = 4 recomputes nothing twice and stores the most
  * states; each doubling halves the stored states and adds about (E / 4 - 1) / 2
  * recomputed forward steps per token.  Every E gives the same results: the
- * states replayed from a stored one are the forward sweep's own, bit for bit.
+ * states replayed from a stored one are the forward sweep's own, bit for bit
+ * (the token-loop pass; the chunked pass rounds differently, within the same
+ * tolerance).
  * Arguments, results and errors otherwise those of kda_chunk_bwd; another
  * ckpt_every is KDA_ERR_INVALID_ARG.  The workspace must hold
  * kda_chunk_bwd_workspace_size_sched bytes for the same ckpt_every.

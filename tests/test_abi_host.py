@@ -421,15 +421,24 @@ def test_bwd_rejects_before_launch(lib, over, code):
 
 def test_bwd_workspace_size_follows_the_checkpoint_interval(lib):
     from gated_delta_rule_13_gb300 import kda
-    small = kda.kda_chunk_bwd_workspace_size(4, 16384, 16)
-    assert small == kda.kda_chunk_bwd_workspace_size(4, 16384, 16, ckpt_every=4)
-    s16 = kda.kda_chunk_bwd_workspace_size(4, 16384, 16, ckpt_every=16)
+    f32 = kda.KDA_F32
+    small = kda.kda_chunk_bwd_workspace_size(4, 16384, 16, dtype=f32)
+    assert small == kda.kda_chunk_bwd_workspace_size(4, 16384, 16, dtype=f32, ckpt_every=4)
+    s16 = kda.kda_chunk_bwd_workspace_size(4, 16384, 16, dtype=f32, ckpt_every=16)
     state = 128 * 128 * 4
     assert small - s16 == (16384 // 4 - 16384 // 16) * 16 * state
+    # bf16 by default: the chunked pass, states every 16 tokens and no fp32
+    # accumulators of dq and dk; an explicit interval selects the token loop
+    acc = 2 * 16384 * 16 * 128 * 4
+    chunked = kda.kda_chunk_bwd_workspace_size(4, 16384, 16)
+    assert chunked == kda.kda_chunk_bwd_workspace_size(4, 16384, 16, ckpt_every=16) - acc
+    assert kda.kda_chunk_bwd_workspace_size(4, 16384, 16, ckpt_every=4) == small
     # a long problem gets a wider default interval, its states within 16 GiB
-    big = kda.kda_chunk_bwd_workspace_size(8, 1 << 20, 96)
-    acc = 2 * (1 << 20) * 96 * 128 * 4
-    assert big - acc <= (16 << 30) + (1 << 20)
+    # (for bf16 too: states every 16 tokens would not fit)
+    for dt in (kda.KDA_BF16, f32):
+        big = kda.kda_chunk_bwd_workspace_size(8, 1 << 20, 96, dtype=dt)
+        acc = 2 * (1 << 20) * 96 * 128 * 4
+        assert big - acc <= (16 << 30) + (1 << 20)
     for bad in (3, 6, 2048, -4):
         with pytest.raises(RuntimeError):
             kda.kda_chunk_bwd_workspace_size(1, 64, 1, ckpt_every=bad)

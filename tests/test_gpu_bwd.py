@@ -25,9 +25,9 @@ def _grads_in(x, seed, d_final=True):
     return do, df
 
 
-def _check(x, do, df, dtype, heads=None):
+def _check(x, do, df, dtype, heads=None, every=None):
     got = kda.kda_chunk_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["init_state"],
-                            x["cu_seqlens"], do, df)
+                            x["cu_seqlens"], do, df, ckpt_every=every)
     torch.cuda.synchronize()
     hs = list(range(x["q"].shape[1])) if heads is None else heads
     hsel = torch.as_tensor(hs, device=DEV)
@@ -56,9 +56,13 @@ def test_bwd_matches_oracle_ragged(dtype, init, final):
     _check(x, do, df, dtype)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("case", ["la0", "la_floor", "beta1"])
-def test_bwd_edge_values(case):
-    x = inputs.prefill_inputs([70, 45], H=2, dtype="f32", init_state=True, device=DEV, seed=93)
+def test_bwd_edge_values(case, dtype):
+    """No decay, the decay floor (log alpha = -5 on every channel: a 16-token
+    chunk spans e^-80, the chunked pass's factors e^+-40 around its middle row)
+    and beta = 1."""
+    x = inputs.prefill_inputs([70, 45], H=2, dtype=dtype, init_state=True, device=DEV, seed=93)
     if case == "la0":
         x["log_alpha"].zero_()
     elif case == "la_floor":
@@ -66,21 +70,36 @@ def test_bwd_edge_values(case):
     else:
         x["beta"].fill_(1.0)
     do, df = _grads_in(x, 94)
-    _check(x, do, df, "f32")
+    _check(x, do, df, dtype)
 
 
-def test_bwd_host_cu_seqlens_and_deterministic_dv():
-    """A host cu_seqlens gives the results of a device one; dv and the initial-
-    state gradient (one column block each, no atomics) are bitwise repeatable."""
+def test_bwd_bf16_token_loop_pass():
+    """An explicit checkpoint interval selects the token-loop pass for bf16
+    too: the same oracle parity on ragged lengths."""
+    lengths = [0, 1, 15, 16, 17, 33, 64, 100]
+    x = inputs.prefill_inputs(lengths, H=2, dtype="bf16", init_state=True, device=DEV, seed=97)
+    do, df = _grads_in(x, 98)
+    _check(x, do, df, "bf16", every=8)
+
+
+@pytest.mark.parametrize("every", [None, 4])
+def test_bwd_host_cu_seqlens_and_deterministic_dv(every):
+    """A host cu_seqlens gives the results of a device one.  The chunked pass
+    (bf16 default) writes every gradient element once: all of them bitwise
+    repeatable.  The token-loop pass: dv and the initial-state gradient (one
+    column block each, no atomics) bitwise, the atomically summed ones to their
+    last bits."""
     x = inputs.prefill_inputs([40, 90], H=3, dtype="bf16", init_state=True, device=DEV, seed=95)
     do, df = _grads_in(x, 96)
     a = kda.kda_chunk_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["init_state"],
-                          x["cu_seqlens"], do, df)
+                          x["cu_seqlens"], do, df, ckpt_every=every)
     b = kda.kda_chunk_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["init_state"],
-                          x["cu_seqlens"].cpu(), do, df)
+                          x["cu_seqlens"].cpu(), do, df, ckpt_every=every)
     torch.cuda.synchronize()
     assert torch.equal(a[2], b[2]) and torch.equal(a[5], b[5])
     for i in (0, 1, 3, 4):
+        if every is None:
+            assert torch.equal(a[i], b[i]), i
         assert_parity(a[i] if i != 4 else a[i][..., None], b[i] if i != 4 else b[i][..., None],
                       1e-5, cu=x["cu_seqlens"].cpu().numpy(), name=f"gradient {i}")
 
