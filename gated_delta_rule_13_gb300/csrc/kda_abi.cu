@@ -135,14 +135,14 @@ BwdPlan bwd_plan(int32_t want, int32_t n_seqs, int64_t n_tokens, int32_t H, int 
   }
   if (dtype == KDA_BF16 &&
       kda::bwd_ckpt_slots(n_seqs, n_tokens, kda::kBwdChunk) * (size_t)H * kHeadDim * kHeadDim *
-              sizeof(float) <= kda::kCkptBudgetBytes)
+              kda::kBwdChunkStateBytes <= kda::kCkptBudgetBytes)
     return {kda::kBwdChunk, true};
   return {kda::bwd_ckpt_every(n_seqs, n_tokens, H), false};
 }
 
 // Backward-pass workspace: status block, device copy of a host cu_seqlens, the
-// state checkpoints, and (token-loop pass only) the fp32 accumulators of dq
-// and dk.
+// state checkpoints (fp32, or bf16 for the chunked pass), and (token-loop pass
+// only) the fp32 accumulators of dq and dk.
 struct BwdLayout {
   size_t cu, ckpt, dq, dk, total;
 };
@@ -150,8 +150,9 @@ BwdLayout bwd_layout(int32_t n_seqs, int64_t n_tokens, int32_t H, BwdPlan plan) 
   BwdLayout l;
   l.cu = kStatusBytes;
   l.ckpt = l.cu + round_up(sizeof(int32_t) * ((size_t)n_seqs + 1), 256);
+  const size_t state_elem = plan.chunked ? kda::kBwdChunkStateBytes : sizeof(float);
   l.dq = l.ckpt + round_up(kda::bwd_ckpt_slots(n_seqs, n_tokens, plan.every) * H * kHeadDim *
-                               kHeadDim * 4,
+                               kHeadDim * state_elem,
                            256);
   const size_t acc = plan.chunked ? 0 : round_up((size_t)n_tokens * H * kHeadDim * 4, 256);
   l.dk = l.dq + acc;

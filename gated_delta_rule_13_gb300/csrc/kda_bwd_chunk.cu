@@ -60,7 +60,7 @@ constexpr int SP = CB + 8;   // bf16 pitch of 16-wide tiles: 48 B
 constexpr int GP = CB + 1;   // fp32 pitch of the 16 x 16 matrices
 
 struct __align__(16) Smem {
-  __nv_bfloat16 S[D][TP];     // checkpointed state at the chunk start, bf16
+  __nv_bfloat16 S[D][TP];     // the state at the chunk start (bf16 checkpoint)
   __nv_bfloat16 dSn[D][TP];   // dS' (gradient of the chunk-end state), bf16
   __nv_bfloat16 dSlo[D][TP];  // dS' - dSn, bf16: the pair carries dS' to ~2^-16
   __nv_bfloat16 q[CB][TP], k[CB][TP], v[CB][TP], dout[CB][TP];  // raw inputs
@@ -146,12 +146,55 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
 }
 
+// Rows tb .. tb + n - 1 of head h of a [N, H, 128] bf16 tensor into a [16][TP]
+// tile by 16-byte asynchronous copies; rows n .. 15 zero.
+__device__ __forceinline__ void stage_rows(__nv_bfloat16 (*tile)[TP], const __nv_bfloat16 *src,
+                                           int64_t tb, int n, int h, int H, int tid) {
+  for (int e = tid; e < CB * 16; e += kThreads) {
+    const int r = e >> 4, s8 = 8 * (e & 15);
+    if (r < n) cp_async16(&tile[r][s8], src + ((tb + r) * H + h) * D + s8);
+    else *reinterpret_cast<uint4 *>(&tile[r][s8]) = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+// ... of an fp32 tensor (log_alpha) into [16][128] fp32.
+__device__ __forceinline__ void stage_rows_f32(float (*tile)[D], const float *src, int64_t tb,
+                                               int n, int h, int H, int tid) {
+  for (int e = tid; e < CB * 32; e += kThreads) {
+    const int r = e >> 5, s4 = 4 * (e & 31);
+    if (r < n) cp_async16(&tile[r][s4], src + ((tb + r) * H + h) * D + s4);
+    else *reinterpret_cast<float4 *>(&tile[r][s4]) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// Decay factors of one key column c of a chunk from its log_alpha rows:
+// g_r = cumulative sum, et_r = e^{g_r - g_m} (the one exponential per row),
+// e^{g_m - g_r} = 1 / et_r, e^{g_l - g_r} = et_l / et_r, e^{g_r} = e^{g_m} et_r
+// (each a product of factors within e^{+-40}).
+struct ColFactors {
+  float et[CB];
+  float em, etl;  // e^{g_m}, e^{g_l - g_m}
+};
+__device__ __forceinline__ void col_factors(const float (*la)[D], int c, ColFactors &f) {
+  float gr[CB];
+  float acc = 0.f;
+#pragma unroll
+  for (int r = 0; r < CB; ++r) {
+    acc += la[r][c];
+    gr[r] = acc;
+  }
+  const float gm = gr[kMid];
+#pragma unroll
+  for (int r = 0; r < CB; ++r) f.et[r] = expf(gr[r] - gm);
+  f.em = expf(gm);
+  f.etl = f.et[kLast];
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 kda_bwd_chunk_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                      const __nv_bfloat16 *__restrict__ v, const float *__restrict__ la,
                      const float *__restrict__ beta, const int32_t *__restrict__ cu,
                      int32_t n_seqs, int64_t n_tokens, int32_t H,
-                     const float *__restrict__ ckpt, const __nv_bfloat16 *__restrict__ dout,
+                     const __nv_bfloat16 *__restrict__ ckpt, const __nv_bfloat16 *__restrict__ dout,
                      const float *__restrict__ d_final, __nv_bfloat16 *__restrict__ dq,
                      __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv,
                      float *__restrict__ d_la, float *__restrict__ d_beta,
@@ -187,43 +230,42 @@ kda_bwd_chunk_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
 
   const int64_t n_ch = (t1 - t0 + CB - 1) / CB;
   const int64_t slot0 = bwd_ckpt_slot_base(t0, seq, CB);
+  // Inputs of chunk c arrive by asynchronous copies issued during chunk c + 1,
+  // each tile as soon as chunk c + 1 has used it for the last time.
+  auto chunk_len = [&](int64_t c) { return (int)(t1 - (t0 + CB * c) < CB ? t1 - (t0 + CB * c) : CB); };
+  auto issue_qkl = [&](int64_t c) {
+    const int64_t tb = t0 + CB * c;
+    const int n = chunk_len(c);
+    stage_rows(sm.q, q, tb, n, h, H, tid);
+    stage_rows(sm.k, k, tb, n, h, H, tid);
+    stage_rows_f32(sm.la, la, tb, n, h, H, tid);
+  };
+  auto issue_v = [&](int64_t c) { stage_rows(sm.v, v, t0 + CB * c, chunk_len(c), h, H, tid); };
+  auto issue_rest = [&](int64_t c) {  // dO, beta and the state
+    const int64_t tb = t0 + CB * c;
+    const int n = chunk_len(c);
+    stage_rows(sm.dout, dout, tb, n, h, H, tid);
+    if (tid < CB) sm.beta[tid] = tid < n ? beta[(tb + tid) * H + h] : 0.f;
+    const __nv_bfloat16 *Sg = ckpt + ((slot0 + c) * H + h) * (int64_t)(D * D);
+    for (int e = tid; e < D * 16; e += kThreads)
+      cp_async16(&sm.S[e >> 4][8 * (e & 15)], Sg + 8 * e);
+  };
+  if (n_ch > 0) {
+    issue_qkl(n_ch - 1);
+    issue_v(n_ch - 1);
+    issue_rest(n_ch - 1);
+  }
   for (int64_t ch = n_ch - 1; ch >= 0; --ch) {
     const int64_t tb = t0 + CB * ch;
-    const int n = (int)(t1 - tb < CB ? t1 - tb : CB);
-    __syncthreads();  // the previous chunk is done with every tile
-    // ---- inputs of the chunk (rows past n are zero)
-    for (int e = tid; e < CB * 16; e += kThreads) {
-      const int r = e >> 4, s8 = 8 * (e & 15);
-      if (r < n) {
-        const int64_t row = ((tb + r) * H + h) * D + s8;
-        cp_async16(&sm.q[r][s8], q + row);
-        cp_async16(&sm.k[r][s8], k + row);
-        cp_async16(&sm.v[r][s8], v + row);
-        cp_async16(&sm.dout[r][s8], dout + row);
-      } else {
-        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4 *>(&sm.q[r][s8]) = z;
-        *reinterpret_cast<uint4 *>(&sm.k[r][s8]) = z;
-        *reinterpret_cast<uint4 *>(&sm.v[r][s8]) = z;
-        *reinterpret_cast<uint4 *>(&sm.dout[r][s8]) = z;
-      }
-    }
-    for (int e = tid; e < CB * 32; e += kThreads) {
-      const int r = e >> 5, s4 = 4 * (e & 31);
-      if (r < n) cp_async16(&sm.la[r][s4], la + ((tb + r) * H + h) * D + s4);
-      else *reinterpret_cast<float4 *>(&sm.la[r][s4]) = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    if (tid < CB) sm.beta[tid] = tid < n ? beta[(tb + tid) * H + h] : 0.f;
-    // the state at the chunk start (bf16 operand) and rowsum_v(S o dS'); dS' as bf16
-    const float *Sg = ckpt + ((slot0 + ch) * H + h) * (int64_t)(D * D);
+    const int n = chunk_len(ch);
+    cp_async_wait_all();
+    __syncthreads();  // the chunk's inputs are in place; the previous chunk is done
+    // rowsum_v(S o dS') with the bf16 state; dS' as a pair of bf16 tiles
     float p1a = 0.f, p1b = 0.f;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int c = 8 * j + 2 * t;
-      const float2 a = *reinterpret_cast<const float2 *>(Sg + (kr0 + g) * D + c);
-      const float2 b = *reinterpret_cast<const float2 *>(Sg + (kr0 + g + 8) * D + c);
-      st_bf2(&sm.S[kr0 + g][c], a.x, a.y);
-      st_bf2(&sm.S[kr0 + g + 8][c], b.x, b.y);
+      const float2 a = ld_bf2(&sm.S[kr0 + g][c]), b = ld_bf2(&sm.S[kr0 + g + 8][c]);
       p1a = fmaf(a.x, ds[j][0], fmaf(a.y, ds[j][1], p1a));
       p1b = fmaf(b.x, ds[j][2], fmaf(b.y, ds[j][3], p1b));
       const __nv_bfloat162 ha = __floats2bfloat162_rn(ds[j][0], ds[j][1]);
@@ -242,44 +284,37 @@ kda_bwd_chunk_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
       sm.t1[kr0 + g] = p1a;
       sm.t1[kr0 + g + 8] = p1b;
     }
-    cp_async_wait_all();
-    __syncthreads();
 
     // ---- decay factors and the factor-scaled operands (thread: one key column;
     // threads 0-127 the k-derived tiles, 128-255 the q-derived ones)
     {
       const int c = tid & (D - 1);
-      float gr[CB];
-      float acc = 0.f;
-#pragma unroll
-      for (int r = 0; r < CB; ++r) {
-        acc += sm.la[r][c];
-        gr[r] = acc;
-      }
-      const float gm = gr[kMid], gl = gr[kLast];
+      ColFactors f;
+      col_factors(sm.la, c, f);
       if (tid < D) {
-        sm.em[c] = expf(gm);
-        sm.gam[c] = expf(gl);
+        sm.em[c] = f.em;
+        sm.gam[c] = f.em * f.etl;
 #pragma unroll
         for (int r = 0; r < CB; ++r) {
           const float kf = __bfloat162float(sm.k[r][c]);
-          const float e1 = expf(gr[r] - gm);
-          sm.et[r][c] = e1;
-          sm.kt[r][c] = __float2bfloat16_rn(kf * e1);
-          sm.kh[r][c] = __float2bfloat16_rn(kf * expf(gm - gr[r]));
-          sm.kd[r][c] = __float2bfloat16_rn(kf * expf(gl - gr[r]));
-          sm.ks[r][c] = __float2bfloat16_rn(kf * expf(gr[r]));
+          const float eh = __fdividef(1.0f, f.et[r]);
+          sm.et[r][c] = f.et[r];
+          sm.kt[r][c] = __float2bfloat16_rn(kf * f.et[r]);
+          sm.kh[r][c] = __float2bfloat16_rn(kf * eh);
+          sm.kd[r][c] = __float2bfloat16_rn(kf * (f.etl * eh));
+          sm.ks[r][c] = __float2bfloat16_rn(kf * (f.em * f.et[r]));
         }
       } else {
 #pragma unroll
         for (int r = 0; r < CB; ++r) {
           const float qf = __bfloat162float(sm.q[r][c]);
-          sm.qt[r][c] = __float2bfloat16_rn(qf * expf(gr[r] - gm));
-          sm.qs[r][c] = __float2bfloat16_rn(qf * expf(gr[r]));
+          sm.qt[r][c] = __float2bfloat16_rn(qf * f.et[r]);
+          sm.qs[r][c] = __float2bfloat16_rn(qf * (f.em * f.et[r]));
         }
       }
     }
     __syncthreads();
+    if (ch > 0) issue_qkl(ch - 1);  // q, k and log_alpha are used up
 
     // ---- G = Kt Kh^T (warp 0); R = V - Ks S, U = Diag(beta) R (all warps)
     if (warp == 0) {
@@ -352,6 +387,7 @@ kda_bwd_chunk_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
       }
     }
     __syncthreads();
+    if (ch > 0) issue_v(ch - 1);  // v is used up
 
     // ---- T = (I + A)^{-1}, A = tril(Diag(beta) G, -1): lane j < 16 of warp 0
     // owns column j (forward substitution over the rows)
@@ -508,13 +544,12 @@ kda_bwd_chunk_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
         mma_bf16_16x8x16(ds[2 * jp], ak[0], ak[1], ak[2], ak[3], b[0], b[1]);
         mma_bf16_16x8x16(ds[2 * jp + 1], ak[0], ak[1], ak[2], ak[3], b[2], b[3]);
       }
-      // rowsum_v(S o dS) with the fp32 state
+      // rowsum_v(S o dS)
       float p2a = 0.f, p2b = 0.f;
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int c = 8 * j + 2 * t;
-        const float2 a = *reinterpret_cast<const float2 *>(Sg + (kr0 + g) * D + c);
-        const float2 b = *reinterpret_cast<const float2 *>(Sg + (kr0 + g + 8) * D + c);
+        const float2 a = ld_bf2(&sm.S[kr0 + g][c]), b = ld_bf2(&sm.S[kr0 + g + 8][c]);
         p2a = fmaf(a.x, ds[j][0], fmaf(a.y, ds[j][1], p2a));
         p2b = fmaf(b.x, ds[j][2], fmaf(b.y, ds[j][3], p2b));
       }
@@ -545,6 +580,7 @@ kda_bwd_chunk_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
       mma2(aqt, a, b);
     }
     __syncthreads();  // dG, dP, rowsum(dA o G), t2 are in place
+    if (ch > 0) issue_rest(ch - 1);  // dO, beta and the state are used up
 
     // ---- dKt = e^{g_m} o ((-dR) S^T) + dG Kh, dQt = e^{g_m} o (dO S^T) + dP Kh,
     // dKh = dG^T Kt + dP^T Qt; then dq, dk and dg for this warp's key columns
@@ -667,8 +703,9 @@ kda_bwd_chunk_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
   }
 }
 
-// Forward pass for the chunked backward: the state at every chunk start
-// (checkpoint slot bwd_ckpt_slot_base(cu[s], s, 16) + chunk), by the chunk form
+// Forward pass for the chunked backward: the state at every chunk start, as
+// bf16 (checkpoint slot bwd_ckpt_slot_base(cu[s], s, 16) + chunk, 32 KiB per
+// head; the backward pass uses the state only as a bf16 operand), by the chunk form
 // above with the same bf16 operands: R = V - Ks S, delta = T Diag(beta) R,
 // S' = Diag(e^{g_l}) S + Kd^T delta.  The state stays in registers as MMA
 // accumulators (warp w: key rows 16 w .. 16 w + 15).
@@ -687,8 +724,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 kda_bwd_chunk_ckpt_kernel(const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
                           const float *__restrict__ la, const float *__restrict__ beta,
                           const float *__restrict__ init_state, const int32_t *__restrict__ cu,
-                          int32_t n_seqs, int64_t n_tokens, int32_t H, float *__restrict__ ckpt,
-                          DeviceStatus *status) {
+                          int32_t n_seqs, int64_t n_tokens, int32_t H,
+                          __nv_bfloat16 *__restrict__ ckpt, DeviceStatus *status) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   CkSmem &sm = *reinterpret_cast<CkSmem *>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -715,67 +752,59 @@ kda_bwd_chunk_ckpt_kernel(const __nv_bfloat16 *__restrict__ k, const __nv_bfloat
   }
   const int64_t n_ch = (t1 - t0 + CB - 1) / CB;
   const int64_t slot0 = bwd_ckpt_slot_base(t0, seq, CB);
+  // inputs of chunk c + 1 are copied during chunk c, each tile after its last use
+  auto chunk_len = [&](int64_t c) { return (int)(t1 - (t0 + CB * c) < CB ? t1 - (t0 + CB * c) : CB); };
+  auto issue_kl = [&](int64_t c) {
+    stage_rows(sm.k, k, t0 + CB * c, chunk_len(c), h, H, tid);
+    stage_rows_f32(sm.la, la, t0 + CB * c, chunk_len(c), h, H, tid);
+  };
+  auto issue_v = [&](int64_t c) { stage_rows(sm.v, v, t0 + CB * c, chunk_len(c), h, H, tid); };
+  auto load_beta = [&](int64_t c) {
+    const int n = chunk_len(c);
+    if (tid < CB) sm.beta[tid] = tid < n ? beta[(t0 + CB * c + tid) * H + h] : 0.f;
+  };
+  if (n_ch > 0) {
+    issue_kl(0);
+    issue_v(0);
+    load_beta(0);
+  }
   for (int64_t ch = 0; ch < n_ch; ++ch) {
-    const int64_t tb = t0 + CB * ch;
-    const int n = (int)(t1 - tb < CB ? t1 - tb : CB);
-    __syncthreads();  // the previous chunk is done with every tile
-    float *Sg = ckpt + ((slot0 + ch) * H + h) * (int64_t)(D * D);
+    cp_async_wait_all();
+    __syncthreads();  // the chunk's inputs are in place; the previous chunk is done
+    __nv_bfloat16 *Sg = ckpt + ((slot0 + ch) * H + h) * (int64_t)(D * D);
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int c = 8 * j + 2 * t;
-      *reinterpret_cast<float2 *>(Sg + (kr0 + g) * D + c) = make_float2(st[j][0], st[j][1]);
-      *reinterpret_cast<float2 *>(Sg + (kr0 + g + 8) * D + c) = make_float2(st[j][2], st[j][3]);
-      st_bf2(&sm.S[kr0 + g][c], st[j][0], st[j][1]);
-      st_bf2(&sm.S[kr0 + g + 8][c], st[j][2], st[j][3]);
+      const __nv_bfloat162 ha = __floats2bfloat162_rn(st[j][0], st[j][1]);
+      const __nv_bfloat162 hb = __floats2bfloat162_rn(st[j][2], st[j][3]);
+      *reinterpret_cast<__nv_bfloat162 *>(Sg + (kr0 + g) * D + c) = ha;
+      *reinterpret_cast<__nv_bfloat162 *>(Sg + (kr0 + g + 8) * D + c) = hb;
+      *reinterpret_cast<__nv_bfloat162 *>(&sm.S[kr0 + g][c]) = ha;
+      *reinterpret_cast<__nv_bfloat162 *>(&sm.S[kr0 + g + 8][c]) = hb;
     }
-    for (int e = tid; e < CB * 16; e += kThreads) {
-      const int r = e >> 4, s8 = 8 * (e & 15);
-      if (r < n) {
-        const int64_t row = ((tb + r) * H + h) * D + s8;
-        cp_async16(&sm.k[r][s8], k + row);
-        cp_async16(&sm.v[r][s8], v + row);
-      } else {
-        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4 *>(&sm.k[r][s8]) = z;
-        *reinterpret_cast<uint4 *>(&sm.v[r][s8]) = z;
-      }
-    }
-    for (int e = tid; e < CB * 32; e += kThreads) {
-      const int r = e >> 5, s4 = 4 * (e & 31);
-      if (r < n) cp_async16(&sm.la[r][s4], la + ((tb + r) * H + h) * D + s4);
-      else *reinterpret_cast<float4 *>(&sm.la[r][s4]) = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    if (tid < CB) sm.beta[tid] = tid < n ? beta[(tb + tid) * H + h] : 0.f;
-    cp_async_wait_all();
-    __syncthreads();
-    {  // factor-scaled k tiles: threads 0-127 Kt, Kh; 128-255 Ks, Kd
+    {  // factor-scaled k tiles (as in the backward pass): threads 0-127 Kt, Kh; 128-255 Ks, Kd
       const int c = tid & (D - 1);
-      float gr[CB];
-      float acc = 0.f;
-#pragma unroll
-      for (int r = 0; r < CB; ++r) {
-        acc += sm.la[r][c];
-        gr[r] = acc;
-      }
-      const float gm = gr[kMid], gl = gr[kLast];
+      ColFactors f;
+      col_factors(sm.la, c, f);
       if (tid < D) {
 #pragma unroll
         for (int r = 0; r < CB; ++r) {
           const float kf = __bfloat162float(sm.k[r][c]);
-          sm.kt[r][c] = __float2bfloat16_rn(kf * expf(gr[r] - gm));
-          sm.kh[r][c] = __float2bfloat16_rn(kf * expf(gm - gr[r]));
+          sm.kt[r][c] = __float2bfloat16_rn(kf * f.et[r]);
+          sm.kh[r][c] = __float2bfloat16_rn(kf * __fdividef(1.0f, f.et[r]));
         }
       } else {
-        sm.gam[c] = expf(gl);
+        sm.gam[c] = f.em * f.etl;
 #pragma unroll
         for (int r = 0; r < CB; ++r) {
           const float kf = __bfloat162float(sm.k[r][c]);
-          sm.ks[r][c] = __float2bfloat16_rn(kf * expf(gr[r]));
-          sm.kd[r][c] = __float2bfloat16_rn(kf * expf(gl - gr[r]));
+          sm.ks[r][c] = __float2bfloat16_rn(kf * (f.em * f.et[r]));
+          sm.kd[r][c] = __float2bfloat16_rn(kf * (f.etl * __fdividef(1.0f, f.et[r])));
         }
       }
     }
     __syncthreads();
+    if (ch + 1 < n_ch) issue_kl(ch + 1);  // k and log_alpha are used up
     if (warp == 0) {  // G = Kt Kh^T
       float a2[2][4], b2[2][4];
       zero(a2);
@@ -819,6 +848,7 @@ kda_bwd_chunk_ckpt_kernel(const __nv_bfloat16 *__restrict__ k, const __nv_bfloat
       }
     }
     __syncthreads();
+    if (ch + 1 < n_ch) issue_v(ch + 1);  // v is used up
     if (warp == 0 && lane < CB) {  // T = (I + A)^{-1}, column `lane`
       const int j = lane;
       float tc[CB];
@@ -833,6 +863,7 @@ kda_bwd_chunk_ckpt_kernel(const __nv_bfloat16 *__restrict__ k, const __nv_bfloat
       for (int r = 0; r < CB; ++r) sm.tm[r][j] = __float2bfloat16_rn(tc[r]);
     }
     __syncthreads();
+    if (ch + 1 < n_ch) load_beta(ch + 1);  // beta is used up
     {  // delta = T U
       float dlt[2][4];
       zero(dlt);
@@ -881,8 +912,8 @@ cudaError_t launch_bwd_chunk(const BwdArgs &a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   kda_bwd_chunk_ckpt_kernel<<<(unsigned)chains, kThreads, sizeof(CkSmem), stream>>>(
       static_cast<const __nv_bfloat16 *>(a.k), static_cast<const __nv_bfloat16 *>(a.v),
-      a.log_alpha, a.beta, a.init_state, a.cu_seqlens, a.n_seqs, a.n_tokens, a.H, a.ckpt,
-      a.status);
+      a.log_alpha, a.beta, a.init_state, a.cu_seqlens, a.n_seqs, a.n_tokens, a.H,
+      reinterpret_cast<__nv_bfloat16 *>(a.ckpt), a.status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(Smem);
@@ -892,7 +923,8 @@ cudaError_t launch_bwd_chunk(const BwdArgs &a, cudaStream_t stream) {
   kda_bwd_chunk_kernel<<<(unsigned)chains, kThreads, smem, stream>>>(
       static_cast<const __nv_bfloat16 *>(a.q), static_cast<const __nv_bfloat16 *>(a.k),
       static_cast<const __nv_bfloat16 *>(a.v), a.log_alpha, a.beta, a.cu_seqlens, a.n_seqs,
-      a.n_tokens, a.H, a.ckpt, static_cast<const __nv_bfloat16 *>(a.d_out), a.d_final,
+      a.n_tokens, a.H, reinterpret_cast<const __nv_bfloat16 *>(a.ckpt),
+      static_cast<const __nv_bfloat16 *>(a.d_out), a.d_final,
       static_cast<__nv_bfloat16 *>(a.dq), static_cast<__nv_bfloat16 *>(a.dk),
       static_cast<__nv_bfloat16 *>(a.dv), a.d_log_alpha, a.d_beta, a.d_init, a.status);
   return cudaGetLastError();

@@ -155,13 +155,14 @@ struct BwdArgs {
   int32_t ckpt_every;         // tokens between stored states: a power of two in [4, 1024]
   bool chunked;               // bf16 only: the chunked tensor-core pass (ckpt_every == kBwdChunk)
   // workspace
-  float *ckpt;                // [bwd_ckpt_slots][H][128][128]
+  float *ckpt;                // [bwd_ckpt_slots][H][128][128] fp32 (chunked pass: bf16)
   float *dq_acc, *dk_acc;     // [n_tokens][H][128], zeroed
   DeviceStatus *status;
 };
 // Tokens per chunk of the chunked (tensor-core) backward pass, which takes its
-// states every kBwdChunk tokens.
+// states every kBwdChunk tokens, stored as bf16 (bytes per element).
 constexpr int32_t kBwdChunk = 16;
+constexpr size_t kBwdChunkStateBytes = 2;
 // Checkpoint slot of the first state of sequence s (states every `every`
 // tokens from its start): floor(cu[s] / every) + s.  Consecutive sequences never
 // share slots, since floor(b / c) - floor(a / c) + 1 >= ceil((b - a) / c).

@@ -170,7 +170,8 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
  * sweep stores states in the workspace and a reverse sweep recomputes what it
  * needs from them.  Two passes:
  *  - bf16 (when the states fit in 16 GiB): the chunked pass.  States every 16
- *    tokens (64 KiB per head for every 16 tokens and per sequence); the reverse
+ *    tokens, as bf16 (32 KiB per head for every 16 tokens and per sequence),
+ *    from a chunked forward sweep with the same bf16 operands; the reverse
  *    sweep takes 16-token chunks in the chunk form of the recurrence, every
  *    product on the tensor cores with bf16 operands and fp32 accumulation (the
  *    gradient of the state as an operand in a pair of bf16 terms), fp32 state
@@ -197,9 +198,9 @@ int kda_chunk_bwd(const void *q, const void *k, const void *v, const float *log_
 
 /*
  * Bytes of device workspace kda_chunk_bwd needs: the status block, a device
- * copy of a host cu_seqlens, the stored states (64 KiB per head for every 16
- * or E tokens and per sequence, as in kda_chunk_bwd) and, for the token-loop
- * pass, fp32 accumulators of dq and dk.
+ * copy of a host cu_seqlens, the stored states (32 KiB per head for every 16
+ * tokens, or 64 KiB for every E, and per sequence, as in kda_chunk_bwd) and,
+ * for the token-loop pass, fp32 accumulators of dq and dk.
  * Errors: as kda_chunk_fwd_workspace_size.
  */
 int kda_chunk_bwd_workspace_size(int32_t n_seqs, int64_t n_tokens, int32_t H, int32_t dk,

@@ -427,11 +427,12 @@ def test_bwd_workspace_size_follows_the_checkpoint_interval(lib):
     s16 = kda.kda_chunk_bwd_workspace_size(4, 16384, 16, dtype=f32, ckpt_every=16)
     state = 128 * 128 * 4
     assert small - s16 == (16384 // 4 - 16384 // 16) * 16 * state
-    # bf16 by default: the chunked pass, states every 16 tokens and no fp32
+    # bf16 by default: the chunked pass, bf16 states every 16 tokens and no fp32
     # accumulators of dq and dk; an explicit interval selects the token loop
     acc = 2 * 16384 * 16 * 128 * 4
+    half_states = (16384 // 16 + 4 + 1) * 16 * 128 * 128 * 2
     chunked = kda.kda_chunk_bwd_workspace_size(4, 16384, 16)
-    assert chunked == kda.kda_chunk_bwd_workspace_size(4, 16384, 16, ckpt_every=16) - acc
+    assert chunked == kda.kda_chunk_bwd_workspace_size(4, 16384, 16, ckpt_every=16) - acc - half_states
     assert kda.kda_chunk_bwd_workspace_size(4, 16384, 16, ckpt_every=4) == small
     # a long problem gets a wider default interval, its states within 16 GiB
     # (for bf16 too: states every 16 tokens would not fit)
