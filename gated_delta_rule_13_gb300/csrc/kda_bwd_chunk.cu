@@ -167,25 +167,27 @@ __device__ __forceinline__ void stage_rows_f32(float (*tile)[D], const float *sr
 }
 
 // Decay factors of one key column c of a chunk from its log_alpha rows:
-// g_r = cumulative sum, et_r = e^{g_r - g_m} (the one exponential per row),
-// e^{g_m - g_r} = 1 / et_r, e^{g_l - g_r} = et_l / et_r, e^{g_r} = e^{g_m} et_r
-// (each a product of factors within e^{+-40}).
+// g_r = cumulative sum (kept in log2 units), et_r = e^{g_r - g_m} (the one
+// exponential per row, ex2 on the special-function unit, relative error below
+// 2^-22), e^{g_m - g_r} = 1 / et_r, e^{g_l - g_r} = et_l / et_r,
+// e^{g_r} = e^{g_m} et_r (each a product of factors within e^{+-40}).
 struct ColFactors {
   float et[CB];
   float em, etl;  // e^{g_m}, e^{g_l - g_m}
 };
 __device__ __forceinline__ void col_factors(const float (*la)[D], int c, ColFactors &f) {
+  constexpr float kLog2e = 1.4426950408889634f;
   float gr[CB];
   float acc = 0.f;
 #pragma unroll
   for (int r = 0; r < CB; ++r) {
-    acc += la[r][c];
+    acc = fmaf(la[r][c], kLog2e, acc);
     gr[r] = acc;
   }
   const float gm = gr[kMid];
 #pragma unroll
-  for (int r = 0; r < CB; ++r) f.et[r] = expf(gr[r] - gm);
-  f.em = expf(gm);
+  for (int r = 0; r < CB; ++r) f.et[r] = ex2(gr[r] - gm);
+  f.em = ex2(gm);
   f.etl = f.et[kLast];
 }
 
@@ -389,8 +391,9 @@ kda_bwd_chunk_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
     __syncthreads();
     if (ch > 0) issue_v(ch - 1);  // v is used up
 
-    // ---- T = (I + A)^{-1}, A = tril(Diag(beta) G, -1): lane j < 16 of warp 0
-    // owns column j (forward substitution over the rows)
+    // ---- T = (I + A)^{-1}, A = tril(Diag(beta) G, -1), on lanes 0-15 of warp 0
+    // (lane j: column j, forward substitution over the rows), alongside
+    // d delta = P^T dO + Kd dS' on every warp (its value columns; no T needed)
     if (warp == 0 && lane < CB) {
       const int j = lane;
       float tc[CB];
@@ -404,24 +407,10 @@ kda_bwd_chunk_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
 #pragma unroll
       for (int r = 0; r < CB; ++r) sm.tm[r][j] = __float2bfloat16_rn(tc[r]);
     }
-    __syncthreads();
-
-    // ---- delta = T U; d delta = P^T dO + Kd dS'
-    float dd[2][4];
     {
-      float dlt[2][4];
-      zero(dlt);
-      uint32_t a[4], b[4];
-      lda(&sm.tm[0][0], SP, 0, 0, lane, a);
-      ldb_t(&sm.u[0][0], TP, n0, 0, lane, b);
-      mma2(dlt, a, b);
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int c = n0 + 8 * j + 2 * t;
-        st_bf2(&sm.dl[g][c], dlt[j][0], dlt[j][1]);
-        st_bf2(&sm.dl[g + 8][c], dlt[j][2], dlt[j][3]);
-      }
+      float dd[2][4];
       zero(dd);
+      uint32_t a[4], b[4];
       lda_t(&sm.pm[0][0], SP, 0, 0, lane, a);
       ldb_t(&sm.dout[0][0], TP, n0, 0, lane, b);
       mma2(dd, a, b);
@@ -440,13 +429,24 @@ kda_bwd_chunk_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
         st_bf2(&sm.ddl[g + 8][c], dd[j][2], dd[j][3]);
       }
     }
-    __syncthreads();
+    __syncthreads();  // T is in place (each warp reads back only its own d delta)
 
-    // ---- dU = T^T d delta, dR = Diag(beta) dU (= dv); rowsum(R o dU)
+    // ---- delta = T U; dU = T^T d delta, dR = Diag(beta) dU (= dv); rowsum(R o dU)
     {
+      uint32_t a[4], b[4];
+      float dlt[2][4];
+      zero(dlt);
+      lda(&sm.tm[0][0], SP, 0, 0, lane, a);
+      ldb_t(&sm.u[0][0], TP, n0, 0, lane, b);
+      mma2(dlt, a, b);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int c = n0 + 8 * j + 2 * t;
+        st_bf2(&sm.dl[g][c], dlt[j][0], dlt[j][1]);
+        st_bf2(&sm.dl[g + 8][c], dlt[j][2], dlt[j][3]);
+      }
       float du[2][4];
       zero(du);
-      uint32_t a[4], b[4];
       lda_t(&sm.tm[0][0], SP, 0, 0, lane, a);
       ldb_t(&sm.ddl[0][0], TP, n0, 0, lane, b);
       mma2(du, a, b);
