@@ -534,8 +534,10 @@ def fp32_alu_peak_tflops(dev):
 
 def backward_bench(dev, peaks, workload: str = "b4_h16_t4096", steps: int = 5, warmup: int = 2):
     """kda_chunk_bwd on a prefill workload (every gradient, random output and
-    final-state gradients): the checkpoint, backward and conversion kernels,
-    CUDA events around each launch."""
+    final-state gradients): for bf16 the chunked pass (its checkpoint kernel and
+    the reverse chunk kernel, warp-level bf16 MMAs), CUDA events around each
+    call.  Roofline: the token form's flops against the measured bf16 tensor
+    peak (the pass is bound by its serial chunk steps, not by either roof)."""
     import torch
     from gated_delta_rule_13_gb300 import inputs, kda
     w = inputs.WORKLOADS[workload]
@@ -565,17 +567,20 @@ def backward_bench(dev, peaks, workload: str = "b4_h16_t4096", steps: int = 5, w
     ms = a.elapsed_time(b) / steps
     th = n_tok * H
     tflops = th * BWD_FLOP_PER_TOKEN_HEAD / (ms / 1000.0) / 1e12
-    peak = fp32_alu_peak_tflops(dev)
+    peak = peaks["bf16_tflops"]
     nbytes = th * BWD_BYTES_PER_TOKEN_HEAD + n_seqs * H * 3 * STATE_BYTES
     del x, do, df, ws
     torch.cuda.empty_cache()
     return {"workload": f"{workload}: {w.note}", "ms_per_launch": ms,
             "tokens_per_s": n_tok / (ms / 1000.0),
             "hbm_gbs": nbytes / (ms / 1000.0) / 1e9,
-            "roofline": {"bound": "alu", "kernel": "kda_bwd_kernel", "achieved": tflops,
+            "chunk_steps_per_chain": -(-n_tok // n_seqs // 16),
+            "roofline": {"bound": "tensor", "kernel": "kda_bwd_chunk_kernel", "achieved": tflops,
                          "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
-                         "peak_source": "derived: SMs x 128 fp32 lanes x 2 x 2,070 MHz",
-                         "traffic": recorded_traffic("kda_bwd_kernel", "kda_bwd.cu", workload),
+                         "peak_source": "measured bf16 burst (MEASURED_PEAKS.json)",
+                         "alu_frac": tflops / fp32_alu_peak_tflops(dev),
+                         "traffic": recorded_traffic("kda_bwd_chunk_kernel", "kda_bwd_chunk.cu",
+                                                     workload),
                          "flop_per_launch": th * BWD_FLOP_PER_TOKEN_HEAD}}
 
 
