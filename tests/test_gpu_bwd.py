@@ -127,6 +127,17 @@ def test_bwd_two_calls_chain_through_the_state():
     assert_parity(g1[5], whole[5], 1e-4, name="d_init_state")
 
 
+def test_bwd_one_cta_per_chain():
+    """With more chains than half the SMs the chunked pass takes one CTA per
+    chain (with fewer, a two-CTA cluster splits each chain's value columns):
+    80 chains of ragged lengths, 6 heads against the oracle."""
+    lengths = [0, 1, 37, 16, 130]
+    x = inputs.prefill_inputs(lengths, H=20, dtype="bf16", init_state=True, device=DEV, seed=103)
+    do, df = _grads_in(x, 104)
+    assert len(lengths) * 20 * 2 > torch.cuda.get_device_properties(0).multi_processor_count
+    _check(x, do, df, "bf16", heads=[0, 3, 7, 11, 16, 19])
+
+
 def test_bwd_b4_h16_t4096_sampled_heads():
     """The B=4, H=16, T=4096 prefill workload (random initial states): heads 0
     and 15 of every sequence against the oracle."""
