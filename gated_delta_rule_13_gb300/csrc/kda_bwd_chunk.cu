@@ -801,10 +801,13 @@ kda_bwd_chunk_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *_
     constexpr int NK = kPair ? 64 : D;  // keys this CTA finishes
     if (tid < NK) {
       const int c = (kPair ? 64 * rank : 0) + tid;
+      float dgc[CB];  // every row first: the stores then run back to back
+#pragma unroll
+      for (int r = 0; r < CB; ++r) dgc[r] = sm.dgr[r][c];
       float acc = 0.f;
 #pragma unroll
       for (int r = CB - 1; r >= 0; --r) {
-        acc += sm.dgr[r][c];
+        acc += dgc[r];
         if (r < n) d_la[((tb + r) * H + h) * D + c] = acc;
       }
     } else if (tid < NK + CB && rank == 0) {
