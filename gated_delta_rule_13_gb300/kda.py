@@ -475,8 +475,8 @@ def kda_read_chunk_stats(workspace, stream=None):
 
 
 def kda_read_device_status(workspace, stream=None, clear: bool = True) -> int:
-    """Synchronise the stream and return the device status a kda_chunk_fwd
-    workspace recorded (KDA_OK or a kda_status code)."""
+    """Synchronise the stream and return the device status a kda_chunk_fwd or
+    kda_chunk_bwd workspace recorded (KDA_OK or a kda_status code)."""
     _need_cuda("workspace", workspace)
     st = ctypes.c_int32(0)
     _check(library().kda_read_device_status(_ptr(workspace), _stream_handle(stream),

@@ -166,7 +166,8 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
  *                gradient at the zero state)
  * The other arguments are those of kda_chunk_fwd (same inputs, same
  * cu_seqlens rules: host arrays are validated here, device arrays in the
- * kernel, which records KDA_ERR_INVALID_ARG and writes nothing).  A forward
+ * kernels, which record KDA_ERR_INVALID_ARG in the workspace's status word; the
+ * gradients are then undefined).  A forward
  * sweep stores states in the workspace and a reverse sweep recomputes what it
  * needs from them.  Two passes:
  *  - bf16 (when the states fit in 16 GiB): the chunked pass.  States every 16
@@ -298,7 +299,7 @@ int kda_noalloc_read_status(void *stream, int clear, int32_t *device_status);
 
 /*
  * Reads (and, if `clear` is non-zero, resets) the device status word of a
- * kda_chunk_fwd workspace.  Synchronises `stream` first, so it reports the
+ * kda_chunk_fwd or kda_chunk_bwd workspace (both start with it).  Synchronises `stream` first, so it reports the
  * status of every call issued on that stream before it.  *device_status gets
  * KDA_OK or the kda_status code a kernel recorded.
  * Errors: KDA_ERR_INVALID_ARG (NULL workspace or device_status), KDA_ERR_CUDA.

@@ -138,6 +138,26 @@ def test_bwd_one_cta_per_chain():
     _check(x, do, df, "bf16", heads=[0, 3, 7, 11, 16, 19])
 
 
+@pytest.mark.parametrize("every,H", [(None, 2), (None, 80), (4, 2)])
+def test_bwd_invalid_device_cu_seqlens_reports_status(every, H):
+    """A malformed device cu_seqlens: every kernel of the pass (a two-CTA
+    cluster per chain, one CTA per chain, the token loop) records
+    KDA_ERR_INVALID_ARG in the workspace (both CTAs of a cluster leave before
+    their first cluster barrier); the same workspace then serves a valid call,
+    which reports OK."""
+    x = inputs.prefill_inputs([100, 50], H=H, dtype="bf16", init_state=True, device=DEV, seed=8)
+    do, df = _grads_in(x, 9)
+    ws = torch.zeros(kda.kda_chunk_bwd_workspace_size(2, 150, H, ckpt_every=every or 0),
+                     dtype=torch.uint8, device=DEV)
+    bad = torch.tensor([0, 120, 110], dtype=torch.int32, device=DEV)
+    kda.kda_chunk_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["init_state"], bad, do,
+                      df, workspace=ws, ckpt_every=every)
+    assert kda.kda_read_device_status(ws) == kda.KDA_ERR_INVALID_ARG
+    kda.kda_chunk_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["init_state"],
+                      x["cu_seqlens"], do, df, workspace=ws, ckpt_every=every)
+    assert kda.kda_read_device_status(ws) == kda.KDA_OK
+
+
 def test_bwd_b4_h16_t4096_sampled_heads():
     """The B=4, H=16, T=4096 prefill workload (random initial states): heads 0
     and 15 of every sequence against the oracle."""
