@@ -51,7 +51,6 @@
 #include "kda_internal.h"
 #include "kda_sm100.cuh"
 
-
 namespace kda {
 namespace {
 
