@@ -51,6 +51,7 @@
 #include "kda_internal.h"
 #include "kda_sm100.cuh"
 
+
 namespace kda {
 namespace {
 
