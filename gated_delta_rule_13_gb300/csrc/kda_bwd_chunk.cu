@@ -1042,6 +1042,42 @@ kda_bwd_chunk_ckpt_kernel(const __nv_bfloat16 *__restrict__ k, const __nv_bfloat
   }
 }
 
+// Launch configuration of the reverse kernel for NV value columns per CTA
+// (a cluster of D / NV CTAs per chain).
+template <int NV>
+struct ReverseLaunch {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  ReverseLaunch(int64_t chains, cudaStream_t stream) {
+    cfg.gridDim = dim3((unsigned)(chains * (D / NV)));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = sizeof(Smem<NV>);
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = D / NV;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = NV < D ? 1 : 0;
+  }
+};
+
+template <int NV>
+cudaError_t launch_reverse(const BwdArgs &a, int64_t chains, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(kda_bwd_chunk_kernel<NV>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)sizeof(Smem<NV>));
+  if (e != cudaSuccess) return e;
+  ReverseLaunch<NV> l(chains, stream);
+  return cudaLaunchKernelEx(
+      &l.cfg, kda_bwd_chunk_kernel<NV>, static_cast<const __nv_bfloat16 *>(a.q),
+      static_cast<const __nv_bfloat16 *>(a.k), static_cast<const __nv_bfloat16 *>(a.v),
+      a.log_alpha, a.beta, a.cu_seqlens, a.n_seqs, a.n_tokens, a.H,
+      reinterpret_cast<const __nv_bfloat16 *>(a.ckpt), static_cast<const __nv_bfloat16 *>(a.d_out),
+      a.d_final, static_cast<__nv_bfloat16 *>(a.dq), static_cast<__nv_bfloat16 *>(a.dk),
+      static_cast<__nv_bfloat16 *>(a.dv), a.d_log_alpha, a.d_beta, a.d_init, a.status);
+}
+
 template <int NV>
 cudaError_t launch_pass(const BwdArgs &a, int64_t chains, cudaStream_t stream) {
   constexpr int VS = D / NV;
@@ -1055,46 +1091,39 @@ cudaError_t launch_pass(const BwdArgs &a, int64_t chains, cudaStream_t stream) {
       reinterpret_cast<__nv_bfloat16 *>(a.ckpt), a.status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const size_t smem = sizeof(Smem<NV>);
-  e = cudaFuncSetAttribute(kda_bwd_chunk_kernel<NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(chains * VS));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = VS;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = VS > 1 ? 1 : 0;
-  return cudaLaunchKernelEx(
-      &cfg, kda_bwd_chunk_kernel<NV>, static_cast<const __nv_bfloat16 *>(a.q),
-      static_cast<const __nv_bfloat16 *>(a.k), static_cast<const __nv_bfloat16 *>(a.v),
-      a.log_alpha, a.beta, a.cu_seqlens, a.n_seqs, a.n_tokens, a.H,
-      reinterpret_cast<const __nv_bfloat16 *>(a.ckpt), static_cast<const __nv_bfloat16 *>(a.d_out),
-      a.d_final, static_cast<__nv_bfloat16 *>(a.dq), static_cast<__nv_bfloat16 *>(a.dk),
-      static_cast<__nv_bfloat16 *>(a.dv), a.d_log_alpha, a.d_beta, a.d_init, a.status);
+  e = launch_reverse<NV>(a, chains, stream);
+  if (e != cudaSuccess && VS > 1) {
+    // a cluster launch the device refuses (the stored states are the same for
+    // both reverse kernels): one CTA per chain instead
+    cudaGetLastError();
+    e = launch_reverse<D>(a, chains, stream);
+  }
+  return e;
 }
 
 }  // namespace
 
 size_t bwd_chunk_smem_bytes() { return sizeof(Smem<D>); }
 
-// Two CTAs per chain (64 value columns each, a cluster) when every pair fits in
-// one wave on the device's SMs; else one CTA per chain.
+// Two CTAs per chain (64 value columns each, a cluster) when every pair can be
+// resident at once (the runtime's count of active two-CTA clusters of the
+// reverse kernel); else one CTA per chain.
 cudaError_t launch_bwd_chunk(const BwdArgs &a, cudaStream_t stream) {
   const int64_t chains = (int64_t)a.n_seqs * a.H;
   if (chains == 0) return cudaSuccess;
   if (chains > 0x3fffffffLL || !a.bf16 || a.ckpt_every != CB) return cudaErrorInvalidValue;
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t e = cudaFuncSetAttribute(kda_bwd_chunk_kernel<D / 2>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)sizeof(Smem<D / 2>));
   if (e != cudaSuccess) return e;
-  if (2 * chains <= sms) return launch_pass<D / 2>(a, chains, stream);
+  ReverseLaunch<D / 2> l(chains, stream);
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, kda_bwd_chunk_kernel<D / 2>, &l.cfg) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    clusters = 0;
+  }
+  if (chains <= clusters) return launch_pass<D / 2>(a, chains, stream);
   return launch_pass<D>(a, chains, stream);
 }
 
