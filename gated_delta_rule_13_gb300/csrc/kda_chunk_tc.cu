@@ -84,7 +84,7 @@ constexpr uint32_t SM_Q = 0;                    // q chunk (TMA), 64 rows
 constexpr uint32_t SM_K = SM_Q + 16384;         // k chunk (TMA), 64 rows
 constexpr uint32_t SM_V = SM_K + 16384;         // v chunk (TMA), [64 r][128 n] bf16, unswizzled
 constexpr uint32_t SM_LA = SM_V + 16384;        // log_alpha fp32 [64][128]; then tile totals
-constexpr uint32_t SM_GA = SM_LA + 32768;       // Gram rows, 128 rows; then A^T fp32
+constexpr uint32_t SM_GA = SM_LA + 32768;       // Gram rows, 128 rows; then A fp32
 constexpr uint32_t SM_GB = SM_GA + 32768;       // Gram columns, 160 rows; then T, X, T'
 constexpr uint32_t SM_STACK = SM_GB + 40960;    // [Qt; Kt], 128 rows
 constexpr uint32_t SM_KDEC = SM_STACK + 32768;  // 2 x (K o e^{g_C - g}), 64 rows (MN-major)
@@ -92,7 +92,8 @@ constexpr uint32_t SM_PMAT = SM_KDEC + 32768;   // P, K-major [64 r][64 i]
 constexpr uint32_t SM_MISC = SM_PMAT + 8192;
 
 constexpr uint32_t GB_ROWS = 160;
-constexpr int FP = 72;  // pitch (floats) of the fp32 64 x 64 matrices of the solve
+constexpr int FP = 72;  // pitch (floats) of the fp32 64 x 64 T of the solve
+constexpr int FA = 68;  // pitch (floats) of A: rows 16 B aligned, 4-word bank steps
 constexpr int XP = 24;  // pitch (floats) of the 16 x 16 intermediate blocks
 constexpr uint32_t OFF_TINV = 0;                     // inside SM_GB, after the Gram MMAs
 constexpr uint32_t OFF_XBUF = 64 * FP * 4;           // 4 blocks of 16 x XP fp32
@@ -131,7 +132,7 @@ constexpr uint32_t SMEM_BYTES = SM_MISC + sizeof(Misc);
 constexpr uint32_t SM_BETA = SM_MISC + offsetof(Misc, beta);
 constexpr uint32_t SM_GAMMA = SM_MISC + offsetof(Misc, gamma);
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(64 * FP * 4 <= 32768, "A^T fits SM_GA");
+static_assert(64 * FA * 4 <= 32768, "A fits SM_GA");
 static_assert(OFF_TMAT % 1024 == 0 && OFF_TMAT + 8192 <= 40960, "T, X and T' fit SM_GB");
 
 // TMEM columns (fp32 cells).
@@ -878,7 +879,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       return build_tiles(ci, (uint32_t)(ci & 1), chunk_rows(ci), SM_KDEC + 16384u * (uint32_t)(ci & 1));
     };
 
-    // Gram / P accumulators -> A^T (fp32, for the solve) and P (bf16, K-major
+    // Gram / P accumulators -> A (fp32 row-major, for the solve) and P (bf16, K-major
     // [r][i]), with the chunk's beta at sbeta.  Quadrant q4 holds row tile a = q4:
     // lanes 0-15 key rows, 16-31 query rows.
     auto ap_epilogue = [&](uint32_t sbeta, int ci) {
@@ -888,14 +889,18 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         const int a = q4, j = lane & 15, r = 16 * a + j;
         const bool isq = lane >= 16;
         const float br = ld_shared_f32(sbeta + 4u * r);
-        const uint32_t sat = sb + SM_GA;  // A^T, fp32 [i][r], pitch FP
+        const uint32_t sat = sb + SM_GA;  // A = Diag(beta) G, fp32 [r][i], pitch FA
         const int b0 = 2 * hf, nb = a + 1 - b0 < 2 ? a + 1 - b0 : 2;  // warp-uniform
         uint32_t v[32];
         auto block = [&](int b, int off) {
           if (!isq) {   // entries i >= r of A are never read by the solve
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj)
-              st_shared_f32(sat + 4u * ((16 * b + jj) * FP + r), br * __uint_as_float(v[off + jj]));
+            for (int q4v = 0; q4v < 4; ++q4v)
+              st_shared_v4(sat + 4u * (r * FA + 16 * b + 4 * q4v),
+                           __float_as_uint(br * __uint_as_float(v[off + 4 * q4v])),
+                           __float_as_uint(br * __uint_as_float(v[off + 4 * q4v + 1])),
+                           __float_as_uint(br * __uint_as_float(v[off + 4 * q4v + 2])),
+                           __float_as_uint(br * __uint_as_float(v[off + 4 * q4v + 3])));
           } else {
 #pragma unroll
             for (int g8 = 0; g8 < 2; ++g8) {
@@ -931,39 +936,39 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
     };
 
-    // T = (I + A)^{-1} and T' = T Diag(beta) from A^T (warps 0-3), beta at sbeta;
+    // T = (I + A)^{-1} and T' = T Diag(beta) from A (warps 0-3), beta at sbeta;
     // arrives on bar_t1 once the diagonal and 16 -> 32 blocks of T' exist and on
     // bar_t when all of T' does.
     auto solve_T = [&](uint32_t sbeta, int ci) {
       // ---- T = (I + A)^{-1} and T' = T Diag(beta) (warps 0-3)
-      const uint32_t sat = sb + SM_GA;                // A^T, fp32 [i][r], pitch FP
+      const uint32_t sat = sb + SM_GA;                // A, fp32 [r][i], pitch FA
       const uint32_t stv = sb + SM_GB + OFF_TINV;     // T, fp32 [r][i], pitch FP
       const uint32_t sxb = sb + SM_GB + OFF_XBUF;     // 4 blocks of 16 x XP fp32
       if (warp < 2) {
-        // Diagonal 16 x 16 blocks by column-oriented forward substitution: lane
-        // owns column j of block a; after step m, t[m] is final and is eliminated
-        // from every later row.  Columns stream through a ring, three steps ahead.
+        // Diagonal 16 x 16 blocks by forward substitution over the rows: lane
+        // owns column j of block a; t[r] = [r = j] - sum_{i<r} A[r][i] t[i],
+        // accumulated in i order so only the last product waits for t[r - 1].
+        // Rows of A stream through a ring, three rows ahead.
         const int a = 2 * warp + (lane >> 4), j = lane & 15, b0 = 16 * a;
         float t[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) t[r] = (r == j) ? 1.f : 0.f;
-        float cbuf[4][16];
+        float rbuf[4][16];
 #pragma unroll
         for (int p = 0; p < 3; ++p) {
-          lds8(*reinterpret_cast<float(*)[8]>(cbuf[p]), sat + 4u * ((b0 + p) * FP + b0));
-          lds8(*reinterpret_cast<float(*)[8]>(cbuf[p] + 8), sat + 4u * ((b0 + p) * FP + b0 + 8));
+          lds8(*reinterpret_cast<float(*)[8]>(rbuf[p]), sat + 4u * ((b0 + p) * FA + b0));
+          lds8(*reinterpret_cast<float(*)[8]>(rbuf[p] + 8), sat + 4u * ((b0 + p) * FA + b0 + 8));
         }
 #pragma unroll
-        for (int mc = 0; mc < 15; ++mc) {
-          if (mc + 3 < 15) {
-            float *nb = cbuf[(mc + 3) & 3];
-            lds8(*reinterpret_cast<float(*)[8]>(nb), sat + 4u * ((b0 + mc + 3) * FP + b0));
-            lds8(*reinterpret_cast<float(*)[8]>(nb + 8), sat + 4u * ((b0 + mc + 3) * FP + b0 + 8));
+        for (int r = 0; r < 16; ++r) {
+          if (r + 3 < 16) {
+            float *nb = rbuf[(r + 3) & 3];
+            lds8(*reinterpret_cast<float(*)[8]>(nb), sat + 4u * ((b0 + r + 3) * FA + b0));
+            lds8(*reinterpret_cast<float(*)[8]>(nb + 8), sat + 4u * ((b0 + r + 3) * FA + b0 + 8));
           }
-          const float tmv = t[mc];
-          const float *col = cbuf[mc & 3];
+          const float *row = rbuf[r & 3];
+          float sacc = 0.f;
 #pragma unroll
-          for (int r = mc + 1; r < 16; ++r) t[r] = fmaf(-col[r], tmv, t[r]);
+          for (int i = 0; i < r; ++i) sacc = fmaf(row[i], t[i], sacc);
+          t[r] = (r == j ? 1.f : 0.f) - sacc;
         }
         // T (fp32, for the block recursion) and T' = T Diag(beta) (bf16 MMA operand;
         // the block's upper triangle is zero because t[r] = 0 for r < j).
@@ -981,15 +986,15 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       // Off-diagonal blocks, block-recursive: 16 -> 32 (blocks (1,0), (3,2)), then
       // 32 -> 64 (blocks (2,0), (2,1), (3,0), (3,1)), TF32 warp MMAs.
       const int g = lane >> 2, t4 = lane & 3;
-      // acc (+)= A_{ab} T_{mb} with A from A^T (column-major, pitch FP) ...
+      // acc (+)= A_{ab} T_{mb} with A row-major (pitch FA) ...
       auto mul_AT = [&](float (&acc)[2][4], int ab, int mb, int tcol) {
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
           const int kc = 16 * mb + 8 * kk;
-          const uint32_t a0 = to_tf32(ld_shared_f32(sat + 4u * ((kc + t4) * FP + 16 * ab + g)));
-          const uint32_t a1 = to_tf32(ld_shared_f32(sat + 4u * ((kc + t4) * FP + 16 * ab + g + 8)));
-          const uint32_t a2 = to_tf32(ld_shared_f32(sat + 4u * ((kc + t4 + 4) * FP + 16 * ab + g)));
-          const uint32_t a3 = to_tf32(ld_shared_f32(sat + 4u * ((kc + t4 + 4) * FP + 16 * ab + g + 8)));
+          const uint32_t a0 = to_tf32(ld_shared_f32(sat + 4u * ((16 * ab + g) * FA + kc + t4)));
+          const uint32_t a1 = to_tf32(ld_shared_f32(sat + 4u * ((16 * ab + g + 8) * FA + kc + t4)));
+          const uint32_t a2 = to_tf32(ld_shared_f32(sat + 4u * ((16 * ab + g) * FA + kc + t4 + 4)));
+          const uint32_t a3 = to_tf32(ld_shared_f32(sat + 4u * ((16 * ab + g + 8) * FA + kc + t4 + 4)));
           const uint32_t b0p = stv + 4u * ((kc + t4) * FP + tcol + g);
           const uint32_t b1p = stv + 4u * ((kc + t4 + 4) * FP + tcol + g);
           mma_tf32_16x8x8(acc[0], a0, a1, a2, a3, to_tf32(ld_shared_f32(b0p)),
@@ -1137,7 +1142,7 @@ kda_chunk_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (!helped) fence_proxy_async_smem();
       tc_fence_before();
       warp_arrive(&m.bar_om, lane);  // S^T operand ready, Gram columns free: O+M1 may start
-      // A^T visible to the solve warps
+      // A visible to the solve warps
       if (compute_sync_abort(&m.abort)) { failed = true; break; }
       PHASE_MARK(4);
 
