@@ -157,9 +157,13 @@ kda_decode_step_kernel(float *__restrict__ state, const void *__restrict__ q,
 // The CTAs are persistent (two per SM), each walking units with a stride of the
 // grid, and while one unit's tokens run from registers the next unit's state and
 // the cached inputs of its first kReplayGroup tokens are already being copied
-// into shared memory by bulk copies (its beta values ride in the issuing thread's
-// registers): the memory system has the next unit in flight throughout the
-// compute, and a unit starts without a round trip to HBM.
+// into shared memory by bulk copies (its beta values by 4-byte asynchronous
+// copies): the memory system has the next unit in flight throughout the
+// compute, and a unit starts without a round trip to HBM.  The issuing thread
+// waits on no load either: the accepted count of the unit after next is copied
+// the same way one unit ahead of its use (a synchronous load of the count
+// stalled that thread's warp, and with it the whole CTA at its next barrier, by
+// a memory round trip per unit).
 constexpr int kReplayGroup = 8;
 // Staged inputs of one token: log_alpha (fp32), then k, q, v in the input type.
 template <bool BF16>
@@ -184,6 +188,9 @@ kda_decode_replay_kernel(float *__restrict__ state, const void *__restrict__ q,
   __shared__ __align__(16) float s_alpha[kReplayGroup][D], s_k[kReplayGroup][D],
       s_q[kReplayGroup][D], s_v[kReplayGroup][D];
   __shared__ float s_beta[kReplayGroup];
+  __shared__ float s_nbeta[2][kReplayGroup];  // staged betas of the first tokens, by unit parity
+  __shared__ int64_t s_cand;                  // the next unit to look at (thread 0)
+  __shared__ int32_t s_cand_n;                // its accepted count, unclamped
   __shared__ __align__(8) uint64_t bar;
   __shared__ int64_t s_next;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -193,15 +200,21 @@ kda_decode_replay_kernel(float *__restrict__ state, const void *__restrict__ q,
     const int n = n_accept[u / H];
     return n < 0 ? 0 : (n > T ? T : n);
   };
-  // thread 0: the next unit with accepted tokens after `u` (stride gridDim.x),
-  // its state and first tokens' inputs copied into the stage, its betas loaded
-  // into nbeta
-  float nbeta[kReplayGroup];
-  auto prefetch_from = [&](int64_t u) {
-    while (u < units && accepted(u) == 0) u += gridDim.x;
+  // thread 0: the next unit with accepted tokens from s_cand on (stride
+  // gridDim.x), its state and first tokens' inputs copied into the stage, its
+  // betas into s_nbeta[slot]; then the count of the candidate after it
+  auto prefetch_next = [&](int slot) {
+    int64_t u = s_cand;
+    int n_u = u < units ? (s_cand_n < 0 ? 0 : (s_cand_n > T ? T : s_cand_n)) : 0;
+    while (u < units && n_u == 0) {
+      u += gridDim.x;
+      n_u = u < units ? accepted(u) : 0;
+    }
     s_next = u;
+    s_cand = u + gridDim.x;
+    if (u + gridDim.x < units) cp_async4(&s_cand_n, n_accept + (u + gridDim.x) / H);
     if (u < units) {
-      const int cnt = accepted(u) < kReplayGroup ? accepted(u) : kReplayGroup;
+      const int cnt = n_u < kReplayGroup ? n_u : kReplayGroup;
       const int64_t b = u / H, h = u % H;
       mbar_arrive_expect_tx(&bar, D * D * sizeof(float) + (uint32_t)(cnt * kRawTok));
       bulk_load(smem_u32(stage), state + u * (int64_t)(D * D), D * D * sizeof(float), &bar);
@@ -216,25 +229,30 @@ kda_decode_replay_kernel(float *__restrict__ state, const void *__restrict__ q,
                     D * kEsz, &bar);
           bulk_load(dst + D * 4 + 2 * D * kEsz, static_cast<const uint8_t *>(v) + iu * D * kEsz,
                     D * kEsz, &bar);
-          nbeta[t] = beta[iu];
+          cp_async4(&s_nbeta[slot][t], beta + iu);
         }
       }
     }
+    cp_async_commit();
   };
   if (tid == 0) {
     mbar_init(&bar, 1);
     fence_mbarrier_init();
-    prefetch_from(blockIdx.x);
+    s_cand = blockIdx.x;
+    s_cand_n = (int64_t)blockIdx.x < units ? n_accept[blockIdx.x / H] : 0;
+    prefetch_next(0);
   }
   __syncthreads();
   int64_t u = s_next;
   uint32_t phase = 0;
   while (u < units) {
     const bool landed = mbar_wait(&bar, phase, kReplayWaitNs);
+    if (tid == 0) cp_async_wait_all();  // the betas and the next candidate's count
     if (__syncthreads_or(!landed)) {  // a copy that never lands: leave, every thread alike
       if (tid == 0) mbar_wait(&bar, phase, kReplayWaitNs);  // (bounded) no copy outlives the CTA
       return;
     }
+    const int slot = (int)phase;  // this unit's parity
     phase ^= 1u;
     float4 s[16];
 #pragma unroll
@@ -252,14 +270,10 @@ kda_decode_replay_kernel(float *__restrict__ state, const void *__restrict__ q,
         s_q[t][c] = load_elem<BF16>(rt + D * 4 + D * kEsz, c);
         s_v[t][c] = load_elem<BF16>(rt + D * 4 + 2 * D * kEsz, c);
       }
-      if (tid == 0) {
-#pragma unroll
-        for (int t = 0; t < kReplayGroup; ++t)
-          if (t < cnt) s_beta[t] = nbeta[t];
-      }
+      if (tid < cnt) s_beta[tid] = s_nbeta[slot][tid];
     }
     __syncthreads();  // the stage is free for the next unit; the first inputs are in place
-    if (tid == 0) prefetch_from(u + gridDim.x);
+    if (tid == 0) prefetch_next(slot ^ 1);
 
     float *S = state + u * (int64_t)(D * D);
     for (int t0 = 0; t0 < n; t0 += kReplayGroup) {

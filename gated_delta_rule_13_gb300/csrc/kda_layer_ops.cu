@@ -355,22 +355,27 @@ kda_conv_window_kernel(const void *__restrict__ q_raw, const void *__restrict__ 
 // replay under speculative decoding: short convolution, norms, gating, the KDA
 // recurrence and the output norm in one kernel over the accepted prefix, the
 // state and the convolution window written back once).  Unit (b, h), tokens
-// t < n_b = n_accept[b] clamped to [0, T], 8 warps:
-//   threads 0-127 (channel c): q and k of channel c (window, convolution,
-//     Swish), then L2Norm over the 128 channels;
+// t < n_b = n_accept[b] clamped to [0, T], 8 warps, the tokens in groups of up
+// to kLrGroup (three block barriers per group):
+//   threads 0-127 (channel c): q and k of channel c for every token of the
+//     group (window, convolution, Swish), then L2Norm over the 128 channels;
 //   threads 128-255 (channel c - 128): v (window, convolution, Swish), the
 //     decay alpha = e^{-5 sigmoid(a)}, the output gate sigmoid(g), and beta;
-//   then every warp applies the token to its value columns of the state held in
-//   registers (the decode step's layout), and the output row goes through the
-//   head-wise RMSNorm times gamma times the gate before it is stored.
+//   then every warp applies the group's tokens in order to its value columns of
+//   the state held in registers (the decode step's layout), and the group's
+//   output rows go through the head-wise RMSNorm times gamma times the gate
+//   before they are stored.
 // Nothing is read or written for a unit with no accepted token.
 //
 // The CTAs are persistent (two per SM) and walk the units with a stride of the
 // grid.  While one unit's tokens run, bulk copies already bring the next unit's
 // state, its convolution taps and window, and the raw inputs of its first
-// kLrStageTok tokens into a shared-memory stage (its beta logits ride in the
-// issuing thread's registers), so a unit starts without a round trip to HBM.
+// kLrStageTok tokens into a shared-memory stage (its beta logits by 4-byte
+// asynchronous copies), so a unit starts without a round trip to HBM.  The
+// issuing thread waits on no load either: the accepted count of the unit after
+// next is copied the same way, one unit ahead of its use.
 constexpr int kLrStageTok = 4;                       // tokens whose inputs ride in the prefetch
+constexpr int kLrGroup = 4;                          // tokens prepared together
 constexpr uint32_t kLrTapBytes = 3 * D * kConv * 4;  // the unit's q, k, v taps
 template <bool BF16>
 constexpr uint32_t lr_esz() { return BF16 ? 2 : 4; }
@@ -388,6 +393,7 @@ constexpr size_t lr_stage_bytes() { return lr_off_tok<BF16>() + kLrStageTok * lr
 static_assert(kLrOffWin % 16 == 0 && lr_off_tok<true>() % 16 == 0 && lr_off_tok<false>() % 16 == 0,
               "bulk-copy destinations are 16-byte aligned");
 constexpr uint64_t kLrWaitNs = 2000000000ull;  // bound on the stage's copy wait
+
 
 template <bool BF16>
 __device__ __forceinline__ float lr_elem(const uint8_t *row, int c) {
@@ -407,12 +413,17 @@ kda_layer_replay_kernel(float *__restrict__ state, void *__restrict__ win,
   using elem_t = typename std::conditional<BF16, __nv_bfloat16, float>::type;
   constexpr uint32_t kEsz = lr_esz<BF16>(), kTok = lr_tok_bytes<BF16>();
   extern __shared__ __align__(128) uint8_t stage[];
-  __shared__ __align__(16) float s_q[D], s_k[D], s_v[D], s_alpha[D], s_gate[D];
-  __shared__ float s_red[3][kWarps];
-  __shared__ float s_beta;
+  // the group's prepared tokens and raw output rows
+  __shared__ __align__(16) float s_q[kLrGroup][D], s_k[kLrGroup][D], s_v[kLrGroup][D];
+  __shared__ __align__(16) float s_alpha[kLrGroup][D], s_gate[kLrGroup][D], s_o[kLrGroup][D];
+  __shared__ __align__(16) float s_gamma[D];
+  __shared__ float s_red[kLrGroup][3][kWarps];
+  __shared__ float s_beta[kLrGroup];
   __shared__ __align__(16) float s_w[3][D][kConv];           // the unit's taps of q, k, v
   __shared__ __align__(16) uint8_t s_tok[kLrStageTok * kTok];  // its first tokens' raw inputs
-  __shared__ float s_blog[kLrStageTok];
+  __shared__ float s_blog[2][kLrStageTok];  // beta logits of the first tokens, by unit parity
+  __shared__ int64_t s_cand;                 // the next unit to look at (thread 0)
+  __shared__ int32_t s_cand_n;               // its accepted count, unclamped
   __shared__ __align__(8) uint64_t bar;
   __shared__ int64_t s_next;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -425,14 +436,23 @@ kda_layer_replay_kernel(float *__restrict__ state, void *__restrict__ win,
     const int n = n_accept[u / H];
     return n < 0 ? 0 : (n > T ? T : n);
   };
-  // thread 0: the next unit with accepted tokens from `u` on (stride gridDim.x),
-  // its stage copies issued and its first beta logits loaded into nblog
-  float nblog[kLrStageTok];
-  auto prefetch_from = [&](int64_t u) {
-    while (u < units && accepted(u) == 0) u += gridDim.x;
+  // thread 0: the next unit with accepted tokens from s_cand on (stride
+  // gridDim.x), its stage copies issued and its first beta logits copied into
+  // s_blog[slot].  The accepted count of the candidate after it is copied
+  // asynchronously too, a unit ahead of its use, so that issuing the stage
+  // waits on no load unless a unit without accepted tokens is skipped.
+  auto prefetch_next = [&](int slot) {
+    int64_t u = s_cand;
+    int n_u = u < units ? (s_cand_n < 0 ? 0 : (s_cand_n > T ? T : s_cand_n)) : 0;
+    while (u < units && n_u == 0) {
+      u += gridDim.x;
+      n_u = u < units ? accepted(u) : 0;
+    }
     s_next = u;
-    if (u >= units) return;
-    const int cnt = accepted(u) < kLrStageTok ? accepted(u) : kLrStageTok;
+    s_cand = u + gridDim.x;
+    if (u + gridDim.x < units) cp_async4(&s_cand_n, n_accept + (u + gridDim.x) / H);
+    if (u < units) {
+    const int cnt = n_u < kLrStageTok ? n_u : kLrStageTok;
     const int64_t b = u / H;
     const int h = (int)(u % H);
     const uint32_t s0 = smem_u32(stage);
@@ -457,25 +477,31 @@ kda_layer_replay_kernel(float *__restrict__ state, void *__restrict__ win,
         bulk_load(dst + 2 * D * kEsz, static_cast<const elem_t *>(v_raw) + row, D * kEsz, &bar);
         bulk_load(dst + 3 * D * kEsz, static_cast<const elem_t *>(g) + row, D * kEsz, &bar);
         bulk_load(dst + 4 * D * kEsz, a_logit + row, D * 4, &bar);
-        nblog[t] = b_logit[(b * T + t) * H + h];
+        cp_async4(&s_blog[slot][t], b_logit + (b * T + t) * H + h);
       }
     }
+    }
+    cp_async_commit();
   };
   if (tid == 0) {
     mbar_init(&bar, 1);
     fence_mbarrier_init();
-    prefetch_from(blockIdx.x);
+    s_cand = blockIdx.x;
+    s_cand_n = (int64_t)blockIdx.x < units ? n_accept[blockIdx.x / H] : 0;
+    prefetch_next(0);
   }
+  if (tid < D) s_gamma[tid] = gamma[tid];
   __syncthreads();
-  const float4 gm = *reinterpret_cast<const float4 *>(gamma + col);
   int64_t u = s_next;
   uint32_t phase = 0;
   while (u < units) {
     const bool landed = mbar_wait(&bar, phase, kLrWaitNs);
+    if (tid == 0) cp_async_wait_all();  // the beta logits and the next candidate's count
     if (__syncthreads_or(!landed)) {  // a copy that never lands: leave, every thread alike
       if (tid == 0) mbar_wait(&bar, phase, kLrWaitNs);  // (bounded) no copy outlives the CTA
       return;
     }
+    const int slot = (int)phase;  // this unit's parity
     phase ^= 1u;
     const int64_t b = u / H;
     const int h = (int)(u % H);
@@ -502,126 +528,144 @@ kda_layer_replay_kernel(float *__restrict__ state, void *__restrict__ win,
       const uint4 *src = reinterpret_cast<const uint4 *>(stage + lr_off_tok<BF16>());
       for (int e = tid; e < cnt * (int)(kTok / 16); e += 256)
         reinterpret_cast<uint4 *>(s_tok)[e] = src[e];
-      if (tid == 0) {
-#pragma unroll
-        for (int t = 0; t < kLrStageTok; ++t)
-          if (t < cnt) s_blog[t] = nblog[t];
-      }
     }
     __syncthreads();  // the stage is free for the next unit; the taps and inputs are in place
-    if (tid == 0) prefetch_from(u + gridDim.x);
+    if (tid == 0) prefetch_next(slot ^ 1);
 
     float *S = state + u * (int64_t)(D * D);
-    for (int t = 0; t < n; ++t) {
-      const int64_t tok = (b * T + t) * H + h;
-      // ---- raw inputs of channel c: staged for the first tokens, else from HBM
-      float ra, rb = 0.f, rg = 0.f, rl = 0.f;
-      if (t < kLrStageTok) {
-        const uint8_t *tb = s_tok + t * kTok;
-        if (role == 0) {
-          ra = lr_elem<BF16>(tb, c);
-          rb = lr_elem<BF16>(tb + D * kEsz, c);
-        } else {
-          ra = lr_elem<BF16>(tb + 2 * D * kEsz, c);
-          rg = lr_elem<BF16>(tb + 3 * D * kEsz, c);
-          rl = reinterpret_cast<const float *>(tb + 4 * D * kEsz)[c];
+    for (int t0 = 0; t0 < n; t0 += kLrGroup) {
+      const int gn = n - t0 < kLrGroup ? n - t0 : kLrGroup;
+      if (t0 > 0) __syncthreads();  // the last group's output rows are out of the arrays
+      // ---- convolution + Swish of the group's tokens, the window shifted token
+      // by token; raw inputs staged for the first tokens, else from HBM
+#pragma unroll
+      for (int gi = 0; gi < kLrGroup; ++gi) {
+        if (gi < gn) {
+          const int t = t0 + gi;
+          const int64_t tok = (b * T + t) * H + h;
+          float ra, rb = 0.f, rg = 0.f, rl = 0.f;
+          if (t < kLrStageTok) {
+            const uint8_t *tb = s_tok + t * kTok;
+            if (role == 0) {
+              ra = lr_elem<BF16>(tb, c);
+              rb = lr_elem<BF16>(tb + D * kEsz, c);
+            } else {
+              ra = lr_elem<BF16>(tb + 2 * D * kEsz, c);
+              rg = lr_elem<BF16>(tb + 3 * D * kEsz, c);
+              rl = reinterpret_cast<const float *>(tb + 4 * D * kEsz)[c];
+            }
+          } else {
+            const int64_t row = tok * D + c;
+            if (role == 0) {
+              ra = to_float(static_cast<const elem_t *>(q_raw)[row]);
+              rb = to_float(static_cast<const elem_t *>(k_raw)[row]);
+            } else {
+              ra = to_float(static_cast<const elem_t *>(v_raw)[row]);
+              rl = a_logit[row];
+              rg = to_float(static_cast<const elem_t *>(g)[row]);
+            }
+          }
+          const float4 wa = *reinterpret_cast<const float4 *>(s_w[za][c]);
+          float y = wa.x * xa[0] + wa.y * xa[1] + wa.z * xa[2] + wa.w * ra;
+          y *= sigmoidf(y);
+          xa[0] = xa[1]; xa[1] = xa[2]; xa[2] = ra;
+          if (role == 0) {
+            const float4 wb = *reinterpret_cast<const float4 *>(s_w[1][c]);
+            float y2 = wb.x * xb[0] + wb.y * xb[1] + wb.z * xb[2] + wb.w * rb;
+            y2 *= sigmoidf(y2);
+            xb[0] = xb[1]; xb[1] = xb[2]; xb[2] = rb;
+            // q and k before the L2Norm, and their sums of squares (warps 0-3)
+            s_q[gi][c] = y;
+            s_k[gi][c] = y2;
+            const float sq = warp_sum(y * y), sk = warp_sum(y2 * y2);
+            if (lane == 0) { s_red[gi][0][warp] = sq; s_red[gi][1][warp] = sk; }
+          } else {
+            s_v[gi][c] = y;
+            s_alpha[gi][c] = __expf(kDecayBound * sigmoidf(rl));
+            s_gate[gi][c] = sigmoidf(rg);
+            if (c == 0) s_beta[gi] = sigmoidf(t < kLrStageTok ? s_blog[slot][t] : b_logit[tok]);
+          }
         }
-      } else {
-        const int64_t row = tok * D + c;
-        if (role == 0) {
-          ra = to_float(static_cast<const elem_t *>(q_raw)[row]);
-          rb = to_float(static_cast<const elem_t *>(k_raw)[row]);
-        } else {
-          ra = to_float(static_cast<const elem_t *>(v_raw)[row]);
-          rl = a_logit[row];
-          rg = to_float(static_cast<const elem_t *>(g)[row]);
+      }
+      __syncthreads();
+      if (role == 0) {
+#pragma unroll
+        for (int gi = 0; gi < kLrGroup; ++gi) {
+          if (gi < gn) {
+            const float nq = rsqrtf(s_red[gi][0][0] + s_red[gi][0][1] + s_red[gi][0][2] +
+                                    s_red[gi][0][3] + kL2Eps);
+            const float nk = rsqrtf(s_red[gi][1][0] + s_red[gi][1][1] + s_red[gi][1][2] +
+                                    s_red[gi][1][3] + kL2Eps);
+            s_q[gi][c] *= nq;
+            s_k[gi][c] *= nk;
+          }
         }
       }
-      // ---- convolution + Swish of this token, window shifted
-      const float4 wa = *reinterpret_cast<const float4 *>(s_w[za][c]);
-      float ya = wa.x * xa[0] + wa.y * xa[1] + wa.z * xa[2] + wa.w * ra;
-      ya *= sigmoidf(ya);
-      float yb = 0.f;
-      xa[0] = xa[1]; xa[1] = xa[2]; xa[2] = ra;
-      if (role == 0) {
-        const float4 wb = *reinterpret_cast<const float4 *>(s_w[1][c]);
-        yb = wb.x * xb[0] + wb.y * xb[1] + wb.z * xb[2] + wb.w * rb;
-        yb *= sigmoidf(yb);
-        xb[0] = xb[1]; xb[1] = xb[2]; xb[2] = rb;
-        // L2Norm sums of q and k over the 128 channels (warps 0-3)
-        const float sq = warp_sum(ya * ya), sk = warp_sum(yb * yb);
-        if (lane == 0) { s_red[0][warp] = sq; s_red[1][warp] = sk; }
-      } else {
-        s_v[c] = ya;
-        s_alpha[c] = __expf(kDecayBound * sigmoidf(rl));
-        s_gate[c] = sigmoidf(rg);
-        if (c == 0) s_beta = sigmoidf(t < kLrStageTok ? s_blog[t] : b_logit[tok]);
+      __syncthreads();
+      // ---- the recurrence over the group's tokens, on this warp's value columns
+      for (int gi = 0; gi < gn; ++gi) {
+        const float4 vv = *reinterpret_cast<const float4 *>(&s_v[gi][col]);
+        const float bt = s_beta[gi];
+        const float *qg = s_q[gi], *kg = s_k[gi], *ag = s_alpha[gi];
+        float pk0 = 0.f, pk1 = 0.f, pk2 = 0.f, pk3 = 0.f;
+        float pq0 = 0.f, pq1 = 0.f, pq2 = 0.f, pq3 = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int r = row0 + 8 * j;
+          const float al = ag[r], kr = kg[r], qr = qg[r];
+          st[j].x *= al; st[j].y *= al; st[j].z *= al; st[j].w *= al;
+          pk0 = fmaf(kr, st[j].x, pk0); pk1 = fmaf(kr, st[j].y, pk1);
+          pk2 = fmaf(kr, st[j].z, pk2); pk3 = fmaf(kr, st[j].w, pk3);
+          pq0 = fmaf(qr, st[j].x, pq0); pq1 = fmaf(qr, st[j].y, pq1);
+          pq2 = fmaf(qr, st[j].z, pq2); pq3 = fmaf(qr, st[j].w, pq3);
+        }
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          pk0 += __shfl_xor_sync(0xffffffffu, pk0, off);
+          pk1 += __shfl_xor_sync(0xffffffffu, pk1, off);
+          pk2 += __shfl_xor_sync(0xffffffffu, pk2, off);
+          pk3 += __shfl_xor_sync(0xffffffffu, pk3, off);
+          pq0 += __shfl_xor_sync(0xffffffffu, pq0, off);
+          pq1 += __shfl_xor_sync(0xffffffffu, pq1, off);
+          pq2 += __shfl_xor_sync(0xffffffffu, pq2, off);
+          pq3 += __shfl_xor_sync(0xffffffffu, pq3, off);
+        }
+        float kq = 0.f;
+#pragma unroll
+        for (int j = 0; j < D / 32; ++j) kq = fmaf(kg[lane + 32 * j], qg[lane + 32 * j], kq);
+        kq = warp_sum(kq);
+        const float u0 = bt * (vv.x - pk0), u1 = bt * (vv.y - pk1);
+        const float u2 = bt * (vv.z - pk2), u3 = bt * (vv.w - pk3);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float kr = kg[row0 + 8 * j];
+          st[j].x = fmaf(kr, u0, st[j].x); st[j].y = fmaf(kr, u1, st[j].y);
+          st[j].z = fmaf(kr, u2, st[j].z); st[j].w = fmaf(kr, u3, st[j].w);
+        }
+        // the raw output row and its sum of squares, for the norm below
+        const float o0 = fmaf(kq, u0, pq0), o1 = fmaf(kq, u1, pq1);
+        const float o2 = fmaf(kq, u2, pq2), o3 = fmaf(kq, u3, pq3);
+        float ss = o0 * o0 + o1 * o1 + o2 * o2 + o3 * o3;  // lanes 0-3 hold distinct columns
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+        if (row0 == 0) *reinterpret_cast<float4 *>(&s_o[gi][col]) = make_float4(o0, o1, o2, o3);
+        if (lane == 0) s_red[gi][2][warp] = ss;
       }
       __syncthreads();
-      if (role == 0) {
-        const float nq = rsqrtf(s_red[0][0] + s_red[0][1] + s_red[0][2] + s_red[0][3] + kL2Eps);
-        const float nk = rsqrtf(s_red[1][0] + s_red[1][1] + s_red[1][2] + s_red[1][3] + kL2Eps);
-        s_q[c] = ya * nq;
-        s_k[c] = yb * nk;
-      }
-      __syncthreads();
-      // ---- the recurrence step on this warp's value columns (the gate is read
-      // here too: the next token's inputs overwrite it once every warp is past
-      // the output barrier below)
-      const float4 vv = *reinterpret_cast<const float4 *>(&s_v[col]);
-      const float4 gt = *reinterpret_cast<const float4 *>(&s_gate[col]);
-      const float bt = s_beta;
-      float pk0 = 0.f, pk1 = 0.f, pk2 = 0.f, pk3 = 0.f;
-      float pq0 = 0.f, pq1 = 0.f, pq2 = 0.f, pq3 = 0.f;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int r = row0 + 8 * j;
-        const float al = s_alpha[r], kr = s_k[r], qr = s_q[r];
-        st[j].x *= al; st[j].y *= al; st[j].z *= al; st[j].w *= al;
-        pk0 = fmaf(kr, st[j].x, pk0); pk1 = fmaf(kr, st[j].y, pk1);
-        pk2 = fmaf(kr, st[j].z, pk2); pk3 = fmaf(kr, st[j].w, pk3);
-        pq0 = fmaf(qr, st[j].x, pq0); pq1 = fmaf(qr, st[j].y, pq1);
-        pq2 = fmaf(qr, st[j].z, pq2); pq3 = fmaf(qr, st[j].w, pq3);
-      }
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        pk0 += __shfl_xor_sync(0xffffffffu, pk0, off);
-        pk1 += __shfl_xor_sync(0xffffffffu, pk1, off);
-        pk2 += __shfl_xor_sync(0xffffffffu, pk2, off);
-        pk3 += __shfl_xor_sync(0xffffffffu, pk3, off);
-        pq0 += __shfl_xor_sync(0xffffffffu, pq0, off);
-        pq1 += __shfl_xor_sync(0xffffffffu, pq1, off);
-        pq2 += __shfl_xor_sync(0xffffffffu, pq2, off);
-        pq3 += __shfl_xor_sync(0xffffffffu, pq3, off);
-      }
-      float kq = 0.f;
-#pragma unroll
-      for (int j = 0; j < D / 32; ++j) kq = fmaf(s_k[lane + 32 * j], s_q[lane + 32 * j], kq);
-      kq = warp_sum(kq);
-      const float u0 = bt * (vv.x - pk0), u1 = bt * (vv.y - pk1);
-      const float u2 = bt * (vv.z - pk2), u3 = bt * (vv.w - pk3);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float kr = s_k[row0 + 8 * j];
-        st[j].x = fmaf(kr, u0, st[j].x); st[j].y = fmaf(kr, u1, st[j].y);
-        st[j].z = fmaf(kr, u2, st[j].z); st[j].w = fmaf(kr, u3, st[j].w);
-      }
-      // ---- head-wise RMSNorm of the output row times gamma times the gate
-      const float o0 = fmaf(kq, u0, pq0), o1 = fmaf(kq, u1, pq1);
-      const float o2 = fmaf(kq, u2, pq2), o3 = fmaf(kq, u3, pq3);
-      float ss = o0 * o0 + o1 * o1 + o2 * o2 + o3 * o3;  // lanes 0-3 hold distinct columns
-      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-      if (lane == 0) s_red[2][warp] = ss;
-      __syncthreads();
-      if (out != nullptr && row0 == 0) {
+      // ---- head-wise RMSNorm of the group's output rows times gamma times the
+      // gate (32 threads per row, four columns each)
+      if (out != nullptr && tid < 32 * gn) {
+        const int gi = tid >> 5, c4 = 4 * lane;
         float tot = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) tot += s_red[2][w];
+        for (int w = 0; w < kWarps; ++w) tot += s_red[gi][2][w];
         const float nr = rsqrtf(tot * (1.0f / D) + kRmsEps);
-        st4<BF16>(out, tok * D + col,
-                  make_float4(o0 * nr * gm.x * gt.x, o1 * nr * gm.y * gt.y,
-                              o2 * nr * gm.z * gt.z, o3 * nr * gm.w * gt.w));
+        const float4 o = *reinterpret_cast<const float4 *>(&s_o[gi][c4]);
+        const float4 gt = *reinterpret_cast<const float4 *>(&s_gate[gi][c4]);
+        const float4 gm = *reinterpret_cast<const float4 *>(&s_gamma[c4]);
+        st4<BF16>(out, ((b * T + t0 + gi) * H + h) * D + c4,
+                  make_float4(o.x * nr * gm.x * gt.x, o.y * nr * gm.y * gt.y,
+                              o.z * nr * gm.z * gt.z, o.w * nr * gm.w * gt.w));
       }
     }
 #pragma unroll

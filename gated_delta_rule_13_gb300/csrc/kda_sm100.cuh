@@ -121,6 +121,22 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// A 4-byte asynchronous copy, global -> shared, in this thread's cp.async
+// group: no register holds the value, so nothing waits for the load before
+// cp_async_wait_all.  Both addresses 4-byte aligned.
+__device__ __forceinline__ void cp_async4(void *smem_dst, const void *gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// This thread's committed cp.async copies have landed (visible to the thread;
+// to the rest of the block after a barrier).
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
 // Plain (untiled) bulk copies; addresses 16-byte aligned, sizes multiples of 16.
 // Global -> shared, completing `bytes` of the barrier's transaction count.
 __device__ __forceinline__ void bulk_load(uint32_t smem_dst, const void *gsrc, uint32_t bytes,
