@@ -156,6 +156,28 @@ def test_layer_replay_matches_oracle(dtype, T):
     _check_replay(r, n, out, state, win, T, TOL[dtype])
 
 
+def test_layer_replay_each_cta_walks_units_across_skipped_runs():
+    """More units than the persistent grid (two CTAs per SM), so every CTA walks
+    several units, with a run of sequences that accept nothing longer than two
+    grid strides and the last units empty.  Every unit against the oracle;
+    skipped units keep their state and window."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    H, T = 1, 3
+    B = 8 * sms + 37
+    g = np.random.default_rng(43)
+    n = g.integers(1, T + 1, size=B).astype(np.int32)
+    n[50:50 + 6 * sms] = 0
+    n[-5:] = 0
+    r = replay_layer_inputs(B, T, H, "f32", seed=43)
+    state, win = r["state"].clone(), r["window"].clone()
+    out = torch.full((B, T, H, 128), float("nan"), device=DEV, dtype=r["q_raw"].dtype)
+    kda.kda_layer_replay(state, win, r["q_raw"], r["k_raw"], r["v_raw"], r["a_logit"],
+                         r["b_logit"], r["g"], r["conv_w"], r["gamma"],
+                         torch.as_tensor(n, device=DEV), out=out)
+    torch.cuda.synchronize()
+    _check_replay(r, n, out, state, win, T, TOL["f32"])
+
+
 def test_layer_replay_equals_the_unfused_gpu_chain():
     """prep with the window, the decode replay, then post (three kernels, with
     bf16 rounding between them) against the fused kernel: each is within the

@@ -84,6 +84,32 @@ def test_replay_more_tokens_than_one_group(dtype):
         assert torch.isnan(out[b, int(n[b]):]).all()
 
 
+def test_replay_each_cta_walks_units_across_skipped_runs():
+    """More units than the persistent grid (two CTAs per SM), so every CTA walks
+    several units, with a run of sequences that accept nothing longer than two
+    grid strides and the last units empty: each CTA's next count is copied a
+    unit ahead, and units without accepted tokens are crossed one by one.
+    Every unit against the oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    H, T = 1, 3
+    B = 8 * sms + 37                                        # about four units per CTA
+    g = np.random.default_rng(41)
+    n = g.integers(1, T + 1, size=B).astype(np.int32)
+    n[50:50 + 6 * sms] = 0
+    n[-5:] = 0
+    r = replay_inputs(B, T, H, "f32", seed=41)
+    state = r["state"].clone()
+    out = torch.full((B, T, H, 128), float("nan"), dtype=r["q"].dtype, device=DEV)
+    kda.kda_decode_replay(state, r["q"], r["k"], r["v"], r["log_alpha"], r["beta"],
+                          torch.as_tensor(n, device=DEV), out=out)
+    torch.cuda.synchronize()
+    ref_out, ref_state = _oracle(r, n)
+    _check(out, state, ref_out, ref_state, n, T, TOL["f32"])
+    skipped = torch.as_tensor(np.flatnonzero(n == 0), device=DEV)
+    assert torch.equal(state[skipped], r["state"][skipped])
+    assert torch.isnan(out[skipped]).all()
+
+
 def test_replay_equals_consecutive_decode_steps():
     """Replaying every draft token equals that many kda_decode_step calls."""
     B, T, H = 3, 5, 4
