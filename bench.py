@@ -216,14 +216,14 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------------------- GPU arm
-def replay_bench(dev, peaks, steps: int = 20, warmup: int = 3, T: int = 4):
-    """kda_decode_replay on 512 sequences x 96 heads x T cached draft tokens with
+def replay_bench(dev, peaks, steps: int = 20, warmup: int = 3, T: int = 4, B: int = 512):
+    """kda_decode_replay on B (default 512) sequences x 96 heads x T cached draft tokens with
     seeded accepted counts in [0, T] (the step after a speculative verification).
     Algorithmic bytes: one state read and write per unit with an accepted token,
     plus the accepted tokens' inputs and outputs."""
     import torch
     from gated_delta_rule_13_gb300 import inputs, kda
-    B, H = 512, 96
+    H = 96
     d = inputs.decode_inputs(B=B, H=H, steps=T, dtype="bf16", device=dev, seed=17)
     r = {x: d[x].transpose(0, 1).contiguous() for x in ("q", "k", "v", "log_alpha", "beta")}
     state = d["state"]
@@ -253,7 +253,7 @@ def replay_bench(dev, peaks, steps: int = 20, warmup: int = 3, T: int = 4):
     gbs = nbytes / (ms / 1000.0) / 1e9
     del d, r, state, out
     return {"value": gbs, "unit": "GB/s", "ms_per_launch": ms,
-            "workload": f"512 sequences x 96 heads, {T} cached draft tokens, accepted counts "
+            "workload": f"{B} sequences x 96 heads, {T} cached draft tokens, accepted counts "
                         f"seeded uniform in [0, {T}] (mean {accepted / B:.2f})",
             "accepted_tokens_per_s": accepted / (ms / 1000.0),
             "roofline": {"bound": "hbm", "kernel": "kda_decode_replay_kernel", "achieved": gbs,
@@ -264,16 +264,16 @@ def replay_bench(dev, peaks, steps: int = 20, warmup: int = 3, T: int = 4):
                          "bytes_per_launch": nbytes}}
 
 
-def layer_replay_bench(dev, peaks, steps: int = 20, warmup: int = 3, T: int = 4):
+def layer_replay_bench(dev, peaks, steps: int = 20, warmup: int = 3, T: int = 4, B: int = 512):
     """kda_layer_replay (the layer between its projections, fused, over the
-    accepted drafts) on 512 sequences x 96 heads x T cached drafts, accepted
+    accepted drafts) on B (default 512) sequences x 96 heads x T cached drafts, accepted
     counts seeded uniform in [0, T].  Algorithmic bytes per unit with an
     accepted token: the state and the bf16 convolution window read and written
     once, plus per accepted token the raw q, k, v and gate logits (bf16), the
     decay logits (fp32), the beta logit and the bf16 output."""
     import torch
     from gated_delta_rule_13_gb300 import inputs, kda
-    B, H = 512, 96
+    H = 96
     x = inputs.layer_inputs([T] * B, H=H, dtype="bf16", device=dev, seed=19)
     r = {n: x[n].reshape(B, T, H, *x[n].shape[2:]) for n in
          ("q_raw", "k_raw", "v_raw", "a_logit", "b_logit", "g")}
@@ -307,7 +307,7 @@ def layer_replay_bench(dev, peaks, steps: int = 20, warmup: int = 3, T: int = 4)
     gbs = nbytes / (ms / 1000.0) / 1e9
     del x, r, state, win, out
     return {"value": gbs, "unit": "GB/s", "ms_per_launch": ms,
-            "workload": f"512 sequences x 96 heads, {T} cached drafts (raw projections, bf16), "
+            "workload": f"{B} sequences x 96 heads, {T} cached drafts (raw projections, bf16), "
                         f"accepted counts seeded uniform in [0, {T}] (mean {accepted / B:.2f})",
             "accepted_tokens_per_s": accepted / (ms / 1000.0),
             "roofline": {"bound": "hbm", "kernel": "kda_layer_replay_kernel", "achieved": gbs,
@@ -716,10 +716,10 @@ def run_gpu(args):
     del x, out, fin, ws, d, state, dout
     torch.cuda.empty_cache()
     decode_seq = decode_sequence_bench(dev, peaks, steps=args.decode_steps, seed=rank)
-    replay = replay_bench(dev, peaks, steps=args.sub_steps)
+    replay = replay_bench(dev, peaks, steps=args.sub_steps, B=args.replay_batch)
     few_chains = few_chains_bench(dev, peaks, steps=args.sub_steps)
     layer_ops = layer_ops_bench(dev, peaks, steps=args.sub_steps, T=args.layer_tokens)
-    layer_replay = layer_replay_bench(dev, peaks, steps=args.sub_steps)
+    layer_replay = layer_replay_bench(dev, peaks, steps=args.sub_steps, B=args.replay_batch)
     backward = backward_bench(dev, peaks) if args.backward else None
     configs = {}
     for wl, n in (("tiny_f32", args.sub_steps), ("b4_h16_t4096", args.sub_steps),
@@ -807,6 +807,8 @@ def main():
                     help="timed launches of the replay and per-token-step sub-benchmarks")
     ap.add_argument("--layer-tokens", type=int, default=32768,
                     help="tokens of the per-token-step sub-benchmark (96 heads)")
+    ap.add_argument("--replay-batch", type=int, default=512,
+                    help="sequences of the two replay sub-benchmarks (96 heads, 4 drafts)")
     ap.add_argument("--decode-steps", type=int, default=100,
                     help="consecutive in-place steps of the decode sub-benchmark")
     ap.add_argument("--no-backward", dest="backward", action="store_false",
