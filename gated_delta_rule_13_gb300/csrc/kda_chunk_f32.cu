@@ -28,6 +28,12 @@
 // arguments are clamped at 80 so that inputs outside the bound stay finite.
 // The products are register-tiled: every thread owns a small output tile and
 // streams the shared contraction dimension.
+//
+// The value columns of S evolve independently (every key-side quantity above is
+// shared by all of them), so a chain may be split over P = 128 / NVS CTAs, each
+// carrying NVS value columns of S, U, Delta and O and repeating the key-side
+// work; they exchange nothing.  With few chains (a single long sequence) this
+// runs P CTAs side by side instead of one.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -46,16 +52,18 @@ constexpr int PT = C + 4;   // pitch of the C x C matrices (16-byte aligned rows
 constexpr float kMaxArg = 80.f;
 static_assert(C == 32 && kThreads == 256, "the tilings below assume C = 32 and 256 threads");
 
+template <int NVS>
 struct F32Smem {
-  float S[D][D];     // state [key c][value n]
+  static constexpr int PV = NVS + 4;  // pitch of the value-column arrays
+  float S[D][NVS];   // the CTA's value columns of the state [key c][value n]
   float qe[C][PR];   // q, then q o E
   float ke[C][PR];   // k o E
   float kei[C][PC];  // k, then k o Ei
   float kd[C][PR];   // Kdec = K o e^{g_C - g}
-  float v[C][PR];    // v
+  float v[C][PV];    // v (the CTA's columns)
   float g[C][PR];    // log_alpha, then the cumulative log-decay
   float w[C][PR];    // W = T' (K o e^g)
-  float u[C][PR];    // U = T' V, then Delta
+  float u[C][PV];    // U = T' V, then Delta (the CTA's columns)
   float At[C][PT];   // A^T (beta-scaled, strictly lower A)
   float Pm[C][PT];   // P (lower incl. diagonal)
   float Tp[C][PT];   // T' = T Diag(beta)
@@ -77,6 +85,7 @@ __device__ void record_error(DeviceStatus *st, int code, int detail, int chain, 
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
 __device__ __forceinline__ void st4(float *p, float4 x) { *reinterpret_cast<float4 *>(p) = x; }
 
+template <int NVS>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_chunk_fwd_f32_kernel(const float *__restrict__ q, const float *__restrict__ k,
                          const float *__restrict__ v, const float *__restrict__ log_alpha,
@@ -84,10 +93,15 @@ kda_chunk_fwd_f32_kernel(const float *__restrict__ q, const float *__restrict__ 
                          const int32_t *__restrict__ cu_seqlens, int32_t n_seqs,
                          int64_t n_tokens, int32_t H, float *__restrict__ out,
                          float *__restrict__ final_state, DeviceStatus *status) {
+  static_assert(NVS == 32 || NVS == 64 || NVS == 128, "value columns per CTA");
+  constexpr int P = D / NVS;        // CTAs per chain
+  constexpr int RT = NVS / 32;      // rows of a thread's C x NVS output tile (4 columns)
+  constexpr int KT = NVS / 8;       // key rows of a thread's D x NVS state tile (4 columns)
+  constexpr int NG = NVS / 4;       // 4-column groups of the CTA's value columns
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  F32Smem &sm = *reinterpret_cast<F32Smem *>(smem_raw);
+  F32Smem<NVS> &sm = *reinterpret_cast<F32Smem<NVS> *>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int chain = blockIdx.x;
+  const int chain = blockIdx.x / P, nb = NVS * (blockIdx.x % P);  // chain, first value column
   const int seq = chain / H, h = chain % H;
 
   const int64_t t0 = cu_seqlens[seq], t1 = cu_seqlens[seq + 1];
@@ -99,8 +113,8 @@ kda_chunk_fwd_f32_kernel(const float *__restrict__ q, const float *__restrict__ 
   }
 
   const int64_t sbase = ((int64_t)seq * H + h) * D * D;
-  for (int e = tid; e < D * D; e += kThreads)
-    (&sm.S[0][0])[e] = init_state ? init_state[sbase + e] : 0.f;
+  for (int e = tid; e < D * NVS; e += kThreads)
+    sm.S[e / NVS][e % NVS] = init_state ? init_state[sbase + (e / NVS) * D + nb + e % NVS] : 0.f;
 
   const int64_t len = t1 - t0;
   for (int64_t c0 = 0; c0 < len; c0 += C) {
@@ -113,8 +127,11 @@ kda_chunk_fwd_f32_kernel(const float *__restrict__ q, const float *__restrict__ 
       const int64_t off = ((t0 + c0 + r) * H + h) * D + c;
       sm.qe[r][c] = ok ? q[off] : 0.f;
       sm.kei[r][c] = ok ? k[off] : 0.f;
-      sm.v[r][c] = ok ? v[off] : 0.f;
       sm.g[r][c] = ok ? log_alpha[off] : 0.f;
+    }
+    for (int e = tid; e < C * NVS; e += kThreads) {
+      const int r = e / NVS, n = e % NVS;
+      sm.v[r][n] = r < nv ? v[((t0 + c0 + r) * H + h) * D + nb + n] : 0.f;
     }
     if (tid < C) sm.beta[tid] = tid < nv ? beta[(t0 + c0 + tid) * H + h] : 0.f;
     __syncthreads();
@@ -199,46 +216,56 @@ kda_chunk_fwd_f32_kernel(const float *__restrict__ q, const float *__restrict__ 
       for (int r = 0; r < C; ++r) sm.Tp[r][j] = t[r] * bj;
     }
     __syncthreads();
-    // ---- W = T' (K o e^g), U = T' V: thread tile rows r0..r0+3 x key columns k0..k0+3
+    // ---- W = T' (K o e^g): thread tile rows r0..r0+3 x key columns k0..k0+3;
+    // U = T' V: rows ru..ru+RT-1 x the CTA's value columns nu..nu+3
     {
       const int r0 = 4 * warp, k0 = 4 * lane;
       const float4 em = ld4(&sm.egm[k0]);
-      float4 w[4], u[4];
+      float4 w[4];
 #pragma unroll
-      for (int a = 0; a < 4; ++a) w[a] = u[a] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int a = 0; a < 4; ++a) w[a] = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int i = 0; i <= r0 + 3; ++i) {
         float4 kt = ld4(&sm.ke[i][k0]);
         kt.x *= em.x; kt.y *= em.y; kt.z *= em.z; kt.w *= em.w;
-        const float4 vv = ld4(&sm.v[i][k0]);
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
           const float tp = sm.Tp[r0 + a][i];
           w[a].x = fmaf(tp, kt.x, w[a].x); w[a].y = fmaf(tp, kt.y, w[a].y);
           w[a].z = fmaf(tp, kt.z, w[a].z); w[a].w = fmaf(tp, kt.w, w[a].w);
+        }
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a) st4(&sm.w[r0 + a][k0], w[a]);
+      const int ru = RT * (tid / NG), nu = 4 * (tid % NG);
+      float4 u[RT];
+#pragma unroll
+      for (int a = 0; a < RT; ++a) u[a] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = 0; i <= ru + RT - 1; ++i) {
+        const float4 vv = ld4(&sm.v[i][nu]);
+#pragma unroll
+        for (int a = 0; a < RT; ++a) {
+          const float tp = sm.Tp[ru + a][i];
           u[a].x = fmaf(tp, vv.x, u[a].x); u[a].y = fmaf(tp, vv.y, u[a].y);
           u[a].z = fmaf(tp, vv.z, u[a].z); u[a].w = fmaf(tp, vv.w, u[a].w);
         }
       }
 #pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        st4(&sm.w[r0 + a][k0], w[a]);
-        st4(&sm.u[r0 + a][k0], u[a]);
-      }
+      for (int a = 0; a < RT; ++a) st4(&sm.u[ru + a][nu], u[a]);
     }
     __syncthreads();
     // ---- Delta = U - W S and O_inter = (Q o e^g) S: thread tile rows
-    // r0..r0+3 x value columns n0..n0+3; then O = O_inter + P Delta
+    // r0..r0+RT-1 x the CTA's value columns n0..n0+3; then O = O_inter + P Delta
     {
-      const int r0 = 4 * warp, n0 = 4 * lane;
-      float4 dl[4], oi[4];
+      const int r0 = RT * (tid / NG), n0 = 4 * (tid % NG);
+      float4 dl[RT], oi[RT];
 #pragma unroll
-      for (int a = 0; a < 4; ++a) dl[a] = oi[a] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int a = 0; a < RT; ++a) dl[a] = oi[a] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
       for (int c = 0; c < D; ++c) {
         const float4 s4 = ld4(&sm.S[c][n0]);
         const float em = sm.egm[c];
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
+        for (int a = 0; a < RT; ++a) {
           const float wv = sm.w[r0 + a][c], qv = sm.qe[r0 + a][c] * em;
           dl[a].x = fmaf(wv, s4.x, dl[a].x); dl[a].y = fmaf(wv, s4.y, dl[a].y);
           dl[a].z = fmaf(wv, s4.z, dl[a].z); dl[a].w = fmaf(wv, s4.w, dl[a].w);
@@ -248,32 +275,32 @@ kda_chunk_fwd_f32_kernel(const float *__restrict__ q, const float *__restrict__ 
       }
       __syncthreads();  // every thread has read W and U's rows it needs
 #pragma unroll
-      for (int a = 0; a < 4; ++a) {
+      for (int a = 0; a < RT; ++a) {
         float4 uu = ld4(&sm.u[r0 + a][n0]);
         uu.x -= dl[a].x; uu.y -= dl[a].y; uu.z -= dl[a].z; uu.w -= dl[a].w;
         st4(&sm.u[r0 + a][n0], uu);
       }
       __syncthreads();  // Delta complete
-      for (int i = 0; i <= r0 + 3; ++i) {
+      for (int i = 0; i <= r0 + RT - 1; ++i) {
         const float4 d4 = ld4(&sm.u[i][n0]);
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
+        for (int a = 0; a < RT; ++a) {
           const float pv = sm.Pm[r0 + a][i];
           oi[a].x = fmaf(pv, d4.x, oi[a].x); oi[a].y = fmaf(pv, d4.y, oi[a].y);
           oi[a].z = fmaf(pv, d4.z, oi[a].z); oi[a].w = fmaf(pv, d4.w, oi[a].w);
         }
       }
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
-        if (r0 + a < nv) st4(out + ((t0 + c0 + r0 + a) * H + h) * D + n0, oi[a]);
+      for (int a = 0; a < RT; ++a)
+        if (r0 + a < nv) st4(out + ((t0 + c0 + r0 + a) * H + h) * D + nb + n0, oi[a]);
     }
     // ---- S <- Diag(e^{g_C}) S + Kdec^T Delta: thread tile key rows
-    // k0..k0+15 x value columns n0..n0+3
+    // k0..k0+KT-1 x the CTA's value columns n0..n0+3
     {
-      const int k0 = 16 * warp, n0 = 4 * lane;
-      float4 acc[16];
+      const int k0 = KT * (tid / NG), n0 = 4 * (tid % NG);
+      float4 acc[KT];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
+      for (int j = 0; j < KT; ++j) {
         const float4 s4 = ld4(&sm.S[k0 + j][n0]);
         const float gc = sm.egc[k0 + j];
         acc[j] = make_float4(s4.x * gc, s4.y * gc, s4.z * gc, s4.w * gc);
@@ -281,37 +308,54 @@ kda_chunk_fwd_f32_kernel(const float *__restrict__ q, const float *__restrict__ 
       for (int i = 0; i < C; ++i) {
         const float4 d4 = ld4(&sm.u[i][n0]);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < KT; ++j) {
           const float kd = sm.kd[i][k0 + j];
           acc[j].x = fmaf(kd, d4.x, acc[j].x); acc[j].y = fmaf(kd, d4.y, acc[j].y);
           acc[j].z = fmaf(kd, d4.z, acc[j].z); acc[j].w = fmaf(kd, d4.w, acc[j].w);
         }
       }
 #pragma unroll
-      for (int j = 0; j < 16; ++j) st4(&sm.S[k0 + j][n0], acc[j]);
+      for (int j = 0; j < KT; ++j) st4(&sm.S[k0 + j][n0], acc[j]);
     }
     __syncthreads();
   }
   if (final_state) {
-    for (int e = tid; e < D * D; e += kThreads) final_state[sbase + e] = (&sm.S[0][0])[e];
+    for (int e = tid; e < D * NVS; e += kThreads)
+      final_state[sbase + (e / NVS) * D + nb + e % NVS] = sm.S[e / NVS][e % NVS];
   }
 }
 
-}  // namespace
-
-cudaError_t launch_chunk_fwd_f32(const ChunkArgs &a, cudaStream_t stream) {
-  const int64_t chains = (int64_t)a.n_seqs * a.H;
-  if (chains == 0) return cudaSuccess;
-  if (chains > 0x7fffffffLL) return cudaErrorInvalidValue;
-  const size_t smem = sizeof(F32Smem);
-  cudaError_t e = cudaFuncSetAttribute(kda_chunk_fwd_f32_kernel,
+template <int NVS>
+cudaError_t launch_f32(const ChunkArgs &a, int64_t chains, cudaStream_t stream) {
+  const int64_t ctas = chains * (D / NVS);
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const size_t smem = sizeof(F32Smem<NVS>);
+  cudaError_t e = cudaFuncSetAttribute(kda_chunk_fwd_f32_kernel<NVS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kda_chunk_fwd_f32_kernel<<<(unsigned)chains, kThreads, smem, stream>>>(
+  kda_chunk_fwd_f32_kernel<NVS><<<(unsigned)ctas, kThreads, smem, stream>>>(
       static_cast<const float *>(a.q), static_cast<const float *>(a.k),
       static_cast<const float *>(a.v), a.log_alpha, a.beta, a.init_state, a.cu_seqlens,
       a.n_seqs, a.n_tokens, a.H, static_cast<float *>(a.out), a.final_state, a.status);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+// CTAs per chain: as many as fit the device's SMs beside the other chains (4,
+// 2 or 1; each CTA repeats the chain's key-side work).
+cudaError_t launch_chunk_fwd_f32(const ChunkArgs &a, cudaStream_t stream) {
+  const int64_t chains = (int64_t)a.n_seqs * a.H;
+  if (chains == 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    sms = 0;
+  }
+  if (4 * chains <= sms) return launch_f32<32>(a, chains, stream);
+  if (2 * chains <= sms) return launch_f32<64>(a, chains, stream);
+  return launch_f32<128>(a, chains, stream);
 }
 
 }  // namespace kda

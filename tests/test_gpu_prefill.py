@@ -43,6 +43,17 @@ def test_ragged_lengths(dtype, with_init):
     check(x, dtype)
 
 
+@pytest.mark.parametrize("H", [2, 20, 40])
+def test_f32_value_columns_split_over_ctas(H):
+    """The fp32 path runs a chain on 4, 2 or 1 CTAs (32, 64 or 128 value columns
+    each) by how many chains fit the SMs: 4, 40 and 80 chains here.  Every form
+    against the oracle, with ragged last chunks and random initial states."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert 4 * 4 <= sms and 2 * 40 <= sms < 4 * 40 and sms < 2 * 80
+    x = inputs.prefill_inputs([37, 70], H=H, dtype="f32", init_state=True, device=DEV, seed=7)
+    check(x, "f32", heads=None if H == 2 else [0, H // 2, H - 1])
+
+
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("case", ["la0", "la_floor", "beta0", "beta1"])
 def test_edge_values(dtype, case):
