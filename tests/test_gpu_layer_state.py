@@ -125,7 +125,7 @@ def _oracle_replay(r, n):
 
 def _check_replay(r, n, out, state, win, T, tol):
     ref_out, ref_state, ref_win = _oracle_replay(r, n)
-    nb = np.minimum(n, T)
+    nb = np.clip(n, 0, T)
     rows = [(b, t) for b in range(len(nb)) for t in range(int(nb[b]))]
     bi = torch.as_tensor([b for b, _ in rows], device=DEV)
     ti = torch.as_tensor([t for _, t in rows], device=DEV)
@@ -168,6 +168,8 @@ def test_layer_replay_each_cta_walks_units_across_skipped_runs():
     n = g.integers(1, T + 1, size=B).astype(np.int32)
     n[50:50 + 6 * sms] = 0
     n[-5:] = 0
+    n[[7, 7 + 2 * sms]] = -3                                # clamped to 0
+    n[[9, 9 + 2 * sms]] = T + 5                             # clamped to T
     r = replay_layer_inputs(B, T, H, "f32", seed=43)
     state, win = r["state"].clone(), r["window"].clone()
     out = torch.full((B, T, H, 128), float("nan"), device=DEV, dtype=r["q_raw"].dtype)

@@ -34,7 +34,7 @@ def _check(out, state, ref_out, ref_state, n, T, tol):
     """Accepted rows of every sequence (one row range per sequence, all heads)
     and the states of the sequences with an accepted token, against the oracle
     (whole tensor, every (sequence, head) slice, every row)."""
-    nb = np.minimum(n, T)
+    nb = np.clip(n, 0, T)
     rows = [(b, t) for b in range(len(nb)) for t in range(int(nb[b]))]
     if rows:
         bi = torch.as_tensor([b for b, _ in rows], device=DEV)
@@ -97,6 +97,8 @@ def test_replay_each_cta_walks_units_across_skipped_runs():
     n = g.integers(1, T + 1, size=B).astype(np.int32)
     n[50:50 + 6 * sms] = 0
     n[-5:] = 0
+    n[[7, 7 + 2 * sms]] = -3                                # clamped to 0
+    n[[9, 9 + 2 * sms]] = T + 5                             # clamped to T
     r = replay_inputs(B, T, H, "f32", seed=41)
     state = r["state"].clone()
     out = torch.full((B, T, H, 128), float("nan"), dtype=r["q"].dtype, device=DEV)
@@ -105,7 +107,7 @@ def test_replay_each_cta_walks_units_across_skipped_runs():
     torch.cuda.synchronize()
     ref_out, ref_state = _oracle(r, n)
     _check(out, state, ref_out, ref_state, n, T, TOL["f32"])
-    skipped = torch.as_tensor(np.flatnonzero(n == 0), device=DEV)
+    skipped = torch.as_tensor(np.flatnonzero(n <= 0), device=DEV)
     assert torch.equal(state[skipped], r["state"][skipped])
     assert torch.isnan(out[skipped]).all()
 
