@@ -74,6 +74,39 @@ struct F32Smem {
   float gm[D];       // g_m
 };
 
+// With a split chain (NVS < 128) the next chunk's raw inputs also fit: copied
+// by asynchronous 16-byte copies while the current chunk computes.
+template <int NVS>
+struct F32Ahead {
+  float q[C][D], k[C][D], la[C][D];
+  float v[C][NVS];
+  float beta[C];
+};
+template <int NVS> constexpr bool kF32Ahead = NVS < D;
+template <int NVS>
+constexpr size_t f32_smem_bytes() {
+  return sizeof(F32Smem<NVS>) + (kF32Ahead<NVS> ? sizeof(F32Ahead<NVS>) : 0);
+}
+
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(smem_dst)),
+               "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *smem_dst, const void *gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(smem_dst)),
+               "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
 __device__ void record_error(DeviceStatus *st, int code, int detail, int chain, int chunk) {
   if (atomicCAS(&st->code, 0, code) == 0) {
     st->detail = detail;
@@ -100,6 +133,7 @@ kda_chunk_fwd_f32_kernel(const float *__restrict__ q, const float *__restrict__ 
   constexpr int NG = NVS / 4;       // 4-column groups of the CTA's value columns
   extern __shared__ __align__(16) unsigned char smem_raw[];
   F32Smem<NVS> &sm = *reinterpret_cast<F32Smem<NVS> *>(smem_raw);
+  F32Ahead<NVS> &ah = *reinterpret_cast<F32Ahead<NVS> *>(smem_raw + sizeof(F32Smem<NVS>));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int chain = blockIdx.x / P, nb = NVS * (blockIdx.x % P);  // chain, first value column
   const int seq = chain / H, h = chain % H;
@@ -117,23 +151,65 @@ kda_chunk_fwd_f32_kernel(const float *__restrict__ q, const float *__restrict__ 
     sm.S[e / NVS][e % NVS] = init_state ? init_state[sbase + (e / NVS) * D + nb + e % NVS] : 0.f;
 
   const int64_t len = t1 - t0;
+  // the raw inputs of the valid rows of the chunk at c0, copied ahead
+  auto issue_ahead = [&](int64_t c0) {
+    const int64_t rem = len - c0;
+    const int nv = rem < C ? (int)rem : C;
+    for (int e = tid; e < C * (D / 4); e += kThreads) {
+      const int r = e / (D / 4), c = 4 * (e % (D / 4));
+      if (r < nv) {
+        const int64_t off = ((t0 + c0 + r) * H + h) * D + c;
+        cp_async16(&ah.q[r][c], q + off);
+        cp_async16(&ah.k[r][c], k + off);
+        cp_async16(&ah.la[r][c], log_alpha + off);
+      }
+    }
+    for (int e = tid; e < C * (NVS / 4); e += kThreads) {
+      const int r = e / (NVS / 4), n = 4 * (e % (NVS / 4));
+      if (r < nv) cp_async16(&ah.v[r][n], v + ((t0 + c0 + r) * H + h) * D + nb + n);
+    }
+    if (tid < nv) cp_async4(&ah.beta[tid], beta + (t0 + c0 + tid) * H + h);
+    cp_async_commit();
+  };
+  if constexpr (kF32Ahead<NVS>) {
+    if (len > 0) issue_ahead(0);
+  }
   for (int64_t c0 = 0; c0 < len; c0 += C) {
     const int64_t rem = len - c0;
     const int nv = rem < C ? (int)rem : C;
     // ---- load the chunk (rows >= nv: zero, beta = 0, log_alpha = 0)
-    for (int e = tid; e < C * D; e += kThreads) {
-      const int r = e / D, c = e % D;
-      const bool ok = r < nv;
-      const int64_t off = ((t0 + c0 + r) * H + h) * D + c;
-      sm.qe[r][c] = ok ? q[off] : 0.f;
-      sm.kei[r][c] = ok ? k[off] : 0.f;
-      sm.g[r][c] = ok ? log_alpha[off] : 0.f;
+    if constexpr (kF32Ahead<NVS>) {
+      cp_async_commit_wait_all();  // this thread's copies of the chunk
+      __syncthreads();             // everyone's
+      for (int e = tid; e < C * D; e += kThreads) {
+        const int r = e / D, c = e % D;
+        const bool ok = r < nv;
+        sm.qe[r][c] = ok ? ah.q[r][c] : 0.f;
+        sm.kei[r][c] = ok ? ah.k[r][c] : 0.f;
+        sm.g[r][c] = ok ? ah.la[r][c] : 0.f;
+      }
+      for (int e = tid; e < C * NVS; e += kThreads) {
+        const int r = e / NVS, n = e % NVS;
+        sm.v[r][n] = r < nv ? ah.v[r][n] : 0.f;
+      }
+      if (tid < C) sm.beta[tid] = tid < nv ? ah.beta[tid] : 0.f;
+      __syncthreads();             // the ahead buffers are free
+      if (c0 + C < len) issue_ahead(c0 + C);
+    } else {
+      for (int e = tid; e < C * D; e += kThreads) {
+        const int r = e / D, c = e % D;
+        const bool ok = r < nv;
+        const int64_t off = ((t0 + c0 + r) * H + h) * D + c;
+        sm.qe[r][c] = ok ? q[off] : 0.f;
+        sm.kei[r][c] = ok ? k[off] : 0.f;
+        sm.g[r][c] = ok ? log_alpha[off] : 0.f;
+      }
+      for (int e = tid; e < C * NVS; e += kThreads) {
+        const int r = e / NVS, n = e % NVS;
+        sm.v[r][n] = r < nv ? v[((t0 + c0 + r) * H + h) * D + nb + n] : 0.f;
+      }
+      if (tid < C) sm.beta[tid] = tid < nv ? beta[(t0 + c0 + tid) * H + h] : 0.f;
     }
-    for (int e = tid; e < C * NVS; e += kThreads) {
-      const int r = e / NVS, n = e % NVS;
-      sm.v[r][n] = r < nv ? v[((t0 + c0 + r) * H + h) * D + nb + n] : 0.f;
-    }
-    if (tid < C) sm.beta[tid] = tid < nv ? beta[(t0 + c0 + tid) * H + h] : 0.f;
     __syncthreads();
     // ---- within-chunk cumulative log-decay per key channel, its middle and end
     if (tid < D) {
@@ -329,7 +405,7 @@ template <int NVS>
 cudaError_t launch_f32(const ChunkArgs &a, int64_t chains, cudaStream_t stream) {
   const int64_t ctas = chains * (D / NVS);
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
-  const size_t smem = sizeof(F32Smem<NVS>);
+  const size_t smem = f32_smem_bytes<NVS>();
   cudaError_t e = cudaFuncSetAttribute(kda_chunk_fwd_f32_kernel<NVS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
